@@ -1,0 +1,210 @@
+"""Python entry to the float64 oracle (``ss_oracle.c``) and its small helpers.
+
+TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may use this module; the product path never
+does. Nothing here imports the CUDA library or its binding.
+
+* ``scan`` / ``scan_rows`` run the plain float64 loop of ``ss_oracle.c`` over
+  all rows or over a sample of rows, in parallel over rows (the C call releases
+  the GIL).
+* ``decode_chain`` runs that same loop over consecutive single-token inputs:
+  the decode update is one step of the scan, so a chain of steps equals the
+  scan over the tokens ("Mamba and selective state spaces", section "Decoding
+  with a constant-size cache").
+* ``zoh``, ``affine_combine`` and ``affine_scan`` are the zero-order-hold
+  discretisation and the affine-map composition of the pages ("Mamba,
+  annotated", sections "Discretization (equation 4)" and "The scan, in one
+  equation"); the tests pin them to the pages' printed numbers.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import subprocess
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "ss_oracle.c")
+_LIB = os.path.join(_HERE, "libss_oracle.so")
+_lib = None
+
+
+def build(force: bool = False, src: str = _SRC, out: str = _LIB) -> str:
+    """Compile ``src`` with gcc -O2 (no fast-math) into the shared library ``out``."""
+    if force or not os.path.exists(out) or os.path.getmtime(out) < os.path.getmtime(src):
+        tmp = out + ".tmp%d" % os.getpid()
+        subprocess.check_call(["gcc", "-O2", "-fPIC", "-shared", "-o", tmp, src, "-lm"])
+        os.replace(tmp, out)
+    return out
+
+
+def load(path: str | None = None):
+    """Load (building first if needed) the oracle library; returns the CDLL."""
+    global _lib
+    if path is None and _lib is not None:
+        return _lib
+    lib = ctypes.CDLL(path or build())
+    dp = ctypes.POINTER(ctypes.c_double)
+    lib.oracle_softplus.argtypes = [ctypes.c_double]
+    lib.oracle_softplus.restype = ctypes.c_double
+    lib.oracle_scan_rows.argtypes = [dp] * 8 + [ctypes.c_int, dp, dp, dp] + [ctypes.c_int64] * 6
+    lib.oracle_scan_rows.restype = ctypes.c_int
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def _f64(a):
+    if a is None:
+        return None
+    if hasattr(a, "detach"):  # torch tensor (CPU): exact widening to float64
+        a = a.detach().to("cpu").double().numpy()
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+
+
+def _ptr(a):
+    if a is None:
+        return None
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def default_threads() -> int:
+    return max(1, len(os.sched_getaffinity(0)))
+
+
+def softplus(v: float) -> float:
+    return load().oracle_softplus(float(v))
+
+
+def scan(x, dt, A, B, C, D=None, z=None, dt_bias=None, delta_softplus=True, h0=None,
+         threads: int | None = None, lib=None):
+    """Full selective scan in float64.
+
+    x, dt, z: (batch, d_inner, L); B, C: (batch, N, L); A: (d_inner, N);
+    D, dt_bias: (d_inner,); h0: (batch, d_inner, N) or None.
+    Returns (y (batch, d_inner, L), final_state (batch, d_inner, N)), float64.
+    """
+    lib = lib or load()
+    x, dt, A, B, C = map(_f64, (x, dt, A, B, C))
+    D, z, dt_bias, h0 = map(_f64, (D, z, dt_bias, h0))
+    batch, d_inner, L = x.shape
+    N = A.shape[1]
+    assert dt.shape == x.shape and B.shape == (batch, N, L) and C.shape == (batch, N, L)
+    assert A.shape == (d_inner, N)
+    y = np.empty((batch, d_inner, L), dtype=np.float64)
+    fs = np.empty((batch, d_inner, N), dtype=np.float64)
+    rows = batch * d_inner
+    nt = max(1, min(threads or default_threads(), rows)) if rows else 1
+    bounds = [(rows * i) // nt for i in range(nt + 1)]
+
+    def run(i):
+        return lib.oracle_scan_rows(_ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
+                                    _ptr(dt_bias), int(bool(delta_softplus)), _ptr(h0), _ptr(y),
+                                    _ptr(fs), batch, d_inner, L, N, bounds[i], bounds[i + 1])
+
+    if nt == 1:
+        codes = [run(0)]
+    else:
+        with ThreadPoolExecutor(nt) as ex:
+            codes = list(ex.map(run, range(nt)))
+    if any(c != 0 for c in codes):
+        raise RuntimeError("oracle_scan_rows failed: %r" % (codes,))
+    return y, fs
+
+
+def scan_rows(inp: dict, rows, delta_softplus=True, use_D=True, use_z=True, use_bias=True,
+              threads: int | None = None):
+    """Scan only the listed rows r = b * d_inner + d of a workload.
+
+    ``inp`` holds x, dt, z (batch, d_inner, L), B, C (batch, N, L), A, D,
+    dt_bias (CPU tensors or arrays). Each row is run as its own one-channel
+    problem. Returns (y (len(rows), L), final_state (len(rows), N)).
+    """
+    lib = load()
+    batch, d_inner, L = tuple(inp["x"].shape)
+    rows = [int(r) for r in rows]
+
+    def one(r):
+        b, d = divmod(r, d_inner)
+        sl = lambda t: _f64(t[b, d])[None, None, :]
+        y, fs = scan(sl(inp["x"]), sl(inp["dt"]), _f64(inp["A"][d])[None, :],
+                     _f64(inp["B"][b])[None], _f64(inp["C"][b])[None],
+                     D=_f64(inp["D"][d:d + 1]) if use_D and inp.get("D") is not None else None,
+                     z=sl(inp["z"]) if use_z and inp.get("z") is not None else None,
+                     dt_bias=(_f64(inp["dt_bias"][d:d + 1])
+                              if use_bias and inp.get("dt_bias") is not None else None),
+                     delta_softplus=delta_softplus, threads=1, lib=lib)
+        return y[0, 0], fs[0, 0]
+
+    nt = max(1, min(threads or default_threads(), len(rows))) if rows else 1
+    with ThreadPoolExecutor(nt) as ex:
+        res = list(ex.map(one, rows))
+    N = inp["A"].shape[1]
+    if not res:
+        return np.empty((0, L)), np.empty((0, N))
+    return np.stack([r[0] for r in res]), np.stack([r[1] for r in res])
+
+
+def decode_chain(tokens: dict, params: dict, rows, use_D=True, use_z=True, h0=None,
+                 threads: int | None = None):
+    """Outputs of consecutive single-token updates for the listed rows.
+
+    tokens: x, delta, z (steps, batch, d_inner), B, C (steps, batch, N);
+    params: A (d_inner, N), D (d_inner,). The step ``delta`` is final (no bias,
+    no softplus). h0: None (zero state) or (len(rows), N).
+    Returns (y (len(rows), steps), state after the last step (len(rows), N)).
+    """
+    lib = load()
+    steps, batch, d_inner = tuple(tokens["x"].shape)
+    rows = [int(r) for r in rows]
+
+    def one(i):
+        r = rows[i]
+        b, d = divmod(r, d_inner)
+        col = lambda t: _f64(t[:, b, d])[None, None, :]
+        Bb = _f64(tokens["B"][:, b, :]).T[None].copy()
+        Cb = _f64(tokens["C"][:, b, :]).T[None].copy()
+        y, fs = scan(col(tokens["x"]), col(tokens["delta"]), _f64(params["A"][d])[None, :], Bb, Cb,
+                     D=_f64(params["D"][d:d + 1]) if use_D else None,
+                     z=col(tokens["z"]) if use_z else None, dt_bias=None, delta_softplus=False,
+                     h0=None if h0 is None else _f64(h0[i])[None, None, :], threads=1, lib=lib)
+        return y[0, 0], fs[0, 0]
+
+    nt = max(1, min(threads or default_threads(), len(rows))) if rows else 1
+    with ThreadPoolExecutor(nt) as ex:
+        res = list(ex.map(one, range(len(rows))))
+    N = params["A"].shape[1]
+    if not res:
+        return np.empty((0, steps)), np.empty((0, N))
+    return np.stack([r[0] for r in res]), np.stack([r[1] for r in res])
+
+
+# ---------------------------------------------------------------- helpers
+
+def zoh(delta: float, A: float, B: float):
+    """Zero-order hold of the scalar system h' = A h + B x over a step delta:
+    (e^{delta A}, (e^{delta A} - 1) / A * B). Used only to pin the pages'
+    printed discretisation examples; the scan itself uses delta * B."""
+    a_bar = math.exp(delta * A)
+    return a_bar, (a_bar - 1.0) / A * B
+
+
+def affine_combine(first, then):
+    """Composition of two affine maps h -> a h + b: first (a1, b1), then
+    (a2, b2), gives (a1 a2, a2 b1 + b2)."""
+    a1, b1 = first
+    a2, b2 = then
+    return a1 * a2, a2 * b1 + b2
+
+
+def affine_scan(pairs, h0: float = 0.0):
+    """States of h_t = a_t h_{t-1} + b_t, one after another, from h0."""
+    out = []
+    h = h0
+    for a, b in pairs:
+        h = a * h + b
+        out.append(h)
+    return out

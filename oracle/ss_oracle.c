@@ -1,0 +1,108 @@
+/*
+ * ss_oracle.c -- plain float64 CPU reference of the Mamba selective scan (S6).
+ *
+ * TEST INFRASTRUCTURE ONLY. Nothing in the product path may call, link or
+ * load this file; only the tests, the smoke check and the CPU-baseline leg of
+ * the benchmark do. It shares no code with the CUDA library.
+ *
+ * What it computes, for every batch row b and channel d, one time step after
+ * another ("Mamba and selective state spaces", box "Selective state-space
+ * model (S6)" and section "The discretization the code actually uses"):
+ *
+ *   v       = dt[b,d,t] + dt_bias[d]                 (bias 0 when absent)
+ *   delta   = softplus(v) if the flag is set, else v
+ *   h[n]    = exp(delta * A[d,n]) * h[n] + delta * B[b,n,t] * x[b,d,t]
+ *   y       = sum_n C[b,n,t] * h[n] + D[d] * x[b,d,t]  (state read after the
+ *                                                        write of token t)
+ *   y      *= z * sigmoid(z)                         (gate, when z is given;
+ *                                                     "The Mamba block")
+ *
+ * starting from h = 0 (or from h0 when given: the decode step of "Decoding
+ * with a constant-size cache" continues from a cached state). The input weight
+ * is delta*B (exponential-Euler), not the zero-order-hold weight.
+ *
+ * Layouts (row-major, contiguous): x, dt, z, y: (batch, d_inner, L);
+ * B, C: (batch, N, L); A: (d_inner, N); D, dt_bias: (d_inner);
+ * h0, final_state: (batch, d_inner, N). A row is r = b * d_inner + d.
+ *
+ * Every quantity is double; there is no blocking, reordering or fusion beyond
+ * the loop order above.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+
+/* log(1 + e^v), in the form max(v, 0) + log1p(e^-|v|), finite for any finite v. */
+double oracle_softplus(double v)
+{
+    if (v > 0.0)
+        return v + log1p(exp(-v));
+    return log1p(exp(v));
+}
+
+static double sigmoid(double v)
+{
+    return 1.0 / (1.0 + exp(-v));
+}
+
+/*
+ * Runs rows [row_begin, row_end). Returns 0 on success, -1 on bad arguments,
+ * -2 when the state buffer cannot be allocated. D, z, dt_bias, h0 and
+ * final_state may be NULL.
+ */
+int oracle_scan_rows(const double *x, const double *dt, const double *A,
+                     const double *B, const double *C, const double *D,
+                     const double *z, const double *dt_bias, int delta_softplus,
+                     const double *h0, double *y, double *final_state,
+                     int64_t batch, int64_t d_inner, int64_t L, int64_t N,
+                     int64_t row_begin, int64_t row_end)
+{
+    if (!x || !dt || !A || !B || !C || !y)
+        return -1;
+    if (batch < 0 || d_inner < 0 || L < 0 || N <= 0)
+        return -1;
+    if (row_begin < 0 || row_end > batch * d_inner || row_begin > row_end)
+        return -1;
+
+    double *h = (double *)malloc((size_t)N * sizeof(double));
+    if (!h)
+        return -2;
+
+    for (int64_t r = row_begin; r < row_end; ++r) {
+        const int64_t b = r / d_inner;
+        const int64_t d = r % d_inner;
+        const double *xr = x + r * L;
+        const double *dtr = dt + r * L;
+        const double *zr = z ? z + r * L : NULL;
+        double *yr = y + r * L;
+
+        for (int64_t n = 0; n < N; ++n)
+            h[n] = h0 ? h0[r * N + n] : 0.0;
+
+        for (int64_t t = 0; t < L; ++t) {
+            double v = dtr[t] + (dt_bias ? dt_bias[d] : 0.0);
+            double delta = delta_softplus ? oracle_softplus(v) : v;
+
+            for (int64_t n = 0; n < N; ++n) {
+                double a_bar = exp(delta * A[d * N + n]);
+                double write = delta * B[(b * N + n) * L + t] * xr[t];
+                h[n] = a_bar * h[n] + write;
+            }
+
+            double out = 0.0;
+            for (int64_t n = 0; n < N; ++n)
+                out += C[(b * N + n) * L + t] * h[n];
+            out += (D ? D[d] : 0.0) * xr[t];
+
+            if (zr)
+                out *= zr[t] * sigmoid(zr[t]);
+            yr[t] = out;
+        }
+
+        if (final_state)
+            for (int64_t n = 0; n < N; ++n)
+                final_state[r * N + n] = h[n];
+    }
+    free(h);
+    return 0;
+}

@@ -1,0 +1,258 @@
+"""Pins of the float64 oracle to facts outside itself.
+
+Each ``check_*`` takes the loaded oracle library (so the same checks can be run
+against deliberately broken copies of the oracle, see test_oracle_mutants.py)
+and raises AssertionError when the oracle disagrees with:
+  * numbers printed on the pages (tests/golden/pages_fixed_points.json),
+  * closed forms derived from the pages' definitions and theorems, or
+  * brute-force evaluations of the pages' unrolled (mixing-matrix) form, which
+    use a different computation (exponential of summed steps, matrix product,
+    numpy convolution) from the oracle's loop.
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+
+import numpy as np
+from scipy.special import expit
+
+from oracle import oracle as O
+
+GOLDEN = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "pages_fixed_points.json")))
+
+
+def _round_eq(got, want, digits):
+    assert round(float(got), digits) == round(float(want), digits), (got, want, digits)
+
+
+def _scan1(lib, x, delta, A=-1.0, B=1.0, C=1.0, D=None, softplus=False, dt_bias=None, z=None, h0=None):
+    """One channel, one state: scalar helper around the oracle scan."""
+    L = len(x)
+    xs = np.asarray(x, dtype=np.float64).reshape(1, 1, L)
+    dts = np.asarray(delta, dtype=np.float64).reshape(1, 1, L)
+    Bs = np.broadcast_to(np.asarray(B, dtype=np.float64), (L,)).reshape(1, 1, L).copy()
+    Cs = np.broadcast_to(np.asarray(C, dtype=np.float64), (L,)).reshape(1, 1, L).copy()
+    y, fs = O.scan(xs, dts, np.array([[A]]), Bs, Cs,
+                   D=None if D is None else np.array([D]),
+                   z=None if z is None else np.asarray(z, dtype=np.float64).reshape(1, 1, L),
+                   dt_bias=None if dt_bias is None else np.array([dt_bias]),
+                   delta_softplus=softplus,
+                   h0=None if h0 is None else np.array(h0, dtype=np.float64).reshape(1, 1, 1),
+                   threads=1, lib=lib)
+    return y[0, 0], fs[0, 0, 0]
+
+
+# ------------------------------------------------------------ page numbers
+
+def check_recurrence_example(lib):
+    """A_bar = 0.5, B_bar = 1, C = 1, x = (1,0,0,2) gives states 1, .5, .25, 2.125.
+    With the scan's Euler rule: delta = ln 2 and A = -1 give exp(delta A) = 0.5;
+    B = 1/ln 2 gives delta*B = 1."""
+    g = GOLDEN["recurrence"]
+    y, fs = _scan1(lib, g["x"], [math.log(2.0)] * 4, A=-1.0, B=1.0 / math.log(2.0), C=g["C"])
+    np.testing.assert_allclose(y, g["y"], rtol=0, atol=1e-12)
+    assert abs(fs - g["y"][-1]) < 1e-12
+    # the same outputs by the convolution with the printed kernel
+    K = np.array(g["kernel"])
+    conv = np.convolve(np.array(g["x"]), K)[:4]
+    np.testing.assert_allclose(y, conv, atol=1e-12)
+    assert abs(conv[3] - g["y4_by_convolution"]) < 1e-12
+
+
+def check_softplus_values(lib):
+    for v, want, digits in GOLDEN["softplus"]["cases"]:
+        _round_eq(lib.oracle_softplus(v), want, digits)
+    # extreme inputs stay finite ("Selection is a gate, numerically")
+    assert lib.oracle_softplus(1000.0) == 1000.0
+    assert lib.oracle_softplus(-1000.0) == 0.0
+    for v, want, digits in GOLDEN["softplus_inverse"]["cases"]:
+        _round_eq(math.log(math.expm1(v)), want, digits)
+    u, want, digits = GOLDEN["softplus_inverse"]["roundtrip"]
+    _round_eq(lib.oracle_softplus(math.log(math.expm1(u))), want, digits)
+
+
+def check_gate_theorem(lib):
+    """Selection is a gate: with N = 1, A = -1, B = 1 and delta = softplus(z),
+    the decay is 1 - sigma(z). Under the scan's Euler rule the write is
+    softplus(z) (the theorem's closing remark). Checked through the scan with
+    the bias split off: dt = z - b, dt_bias = b."""
+    for c in GOLDEN["gate"]["cases"]:
+        z = c["z"]
+        _round_eq(lib.oracle_softplus(z), c["delta"], GOLDEN["gate"]["digits"])
+        _round_eq(math.exp(-lib.oracle_softplus(z)), c["A_bar"], GOLDEN["gate"]["digits"])
+        _round_eq(expit(z), c["gate"], GOLDEN["gate"]["digits"])
+    rng = np.random.default_rng(11)
+    zs = rng.normal(0, 3, size=40)
+    zs[5], zs[17] = 40.0, -40.0
+    xs = rng.normal(size=40)
+    b = 0.37
+    y, _ = _scan1(lib, xs, zs - b, A=-1.0, B=1.0, C=1.0, softplus=True, dt_bias=b)
+    h = 0.0
+    for t in range(40):
+        h = (1.0 - expit(zs[t])) * h + np.logaddexp(0.0, zs[t]) * xs[t]
+        assert abs(y[t] - h) <= 1e-12 * max(1.0, abs(h)), (t, y[t], h)
+
+
+def check_selective_copy_euler(lib):
+    """The hand example's inputs x = (3,9,9,7,9), delta = (5,0,0,5,0) under the
+    scan's Euler rule: h1 = 5*3 = 15, filler leaves it, h4 = e^-5 * 15 + 5*7."""
+    g = GOLDEN["selective_copy_zoh"]
+    y, fs = _scan1(lib, g["x"], g["delta"], A=g["A"], B=g["B"], C=g["C"])
+    h4 = math.exp(-5.0) * 15.0 + 35.0
+    np.testing.assert_allclose(y, [15.0, 15.0, 15.0, h4, h4], rtol=1e-14, atol=0)
+    _round_eq(h4, 35.1011, 4)
+
+
+# ------------------------------------------------------------ closed forms
+
+def check_impulse_response(lib):
+    """Impulse response of a 4-state channel ("State-space models & Mamba",
+    section 'Discretization: making SSMs computable'): A = (-1,-.5,-.25,-.1),
+    B = 1, C = (.5,.3,.15,.05), delta = .1, x = unit impulse, Euler input weight
+    delta*B. Closed form: y[t] = sum_n C_n exp(t delta a_n) delta."""
+    a = np.array([-1.0, -0.5, -0.25, -0.1])
+    Cn = np.array([0.5, 0.3, 0.15, 0.05])
+    T, dlt = 50, 0.1
+    x = np.zeros((1, 1, T)); x[0, 0, 0] = 1.0
+    dt = np.full((1, 1, T), dlt)
+    B = np.ones((1, 4, T))
+    C = np.repeat(Cn[None, :, None], T, axis=2)
+    y, _ = O.scan(x, dt, a[None, :], B, C, delta_softplus=False, threads=1, lib=lib)
+    t = np.arange(T)
+    want = (Cn[None, :] * np.exp(np.outer(t, a) * dlt) * dlt).sum(axis=1)
+    np.testing.assert_allclose(y[0, 0], want, rtol=1e-13, atol=0)
+    assert abs(y[0, 0, 0] - 0.1) < 1e-15
+
+
+def mixing_matrix_reference(x, dt, A, B, C, D, z, dt_bias, softplus):
+    """y from the unrolled form M^(c)_{ts} = sum_n C_{t,n} exp(lambda_{cn}
+    sum_{r=s+1}^{t} delta_r) delta_s B_{s,n} ("Mamba and selective state
+    spaces", theorem 'The mixing matrix of a selective SSM', second form), then
+    y = M x + D x, gated by z sigma(z). Also returns the final state
+    h_{L,n} = sum_s exp(lambda_n sum_{r=s+1}^{L} delta_r) delta_s B_{s,n} x_s."""
+    bt, dn, L = x.shape
+    N = A.shape[1]
+    v = dt + (0.0 if dt_bias is None else dt_bias[None, :, None])
+    delta = np.logaddexp(0.0, v) if softplus else v
+    y = np.zeros_like(x)
+    fs = np.zeros((bt, dn, N))
+    for b in range(bt):
+        for c in range(dn):
+            cum = np.concatenate([[0.0], np.cumsum(delta[b, c])])  # cum[k] = sum_{r<k}
+            M = np.zeros((L, L))
+            for t in range(L):
+                for s in range(t + 1):
+                    seg = cum[t + 1] - cum[s + 1]  # sum_{r=s+1}^{t} delta_r
+                    M[t, s] = np.sum(C[b, :, t] * np.exp(A[c, :] * seg) * delta[b, c, s] * B[b, :, s])
+            out = M @ x[b, c] + (0.0 if D is None else D[c]) * x[b, c]
+            if z is not None:
+                out = out * z[b, c] * expit(z[b, c])
+            y[b, c] = out
+            seg_end = cum[L] - cum[1:]  # sum_{r=s+1}^{L-1}
+            fs[b, c] = (np.exp(A[c, :, None] * seg_end[None, :]) * delta[b, c][None, :]
+                        * B[b] * x[b, c][None, :]).sum(axis=1)
+    return y, fs
+
+
+def random_problem(rng, bt=2, dn=3, L=12, N=4):
+    x = rng.normal(size=(bt, dn, L))
+    dt = rng.normal(0, 0.8, size=(bt, dn, L))
+    A = -np.exp(rng.normal(0, 0.7, size=(dn, N)))
+    B = rng.normal(size=(bt, N, L))
+    C = rng.normal(size=(bt, N, L))
+    D = rng.normal(size=dn)
+    z = rng.normal(size=(bt, dn, L))
+    dt_bias = rng.normal(0, 0.5, size=dn)
+    return x, dt, A, B, C, D, z, dt_bias
+
+
+def check_mixing_matrix(lib):
+    rng = np.random.default_rng(5)
+    for softplus in (True, False):
+        x, dt, A, B, C, D, z, dt_bias = random_problem(rng)
+        if not softplus:
+            dt = np.abs(dt)
+            dt_bias = np.abs(dt_bias)
+        y, fs = O.scan(x, dt, A, B, C, D=D, z=z, dt_bias=dt_bias, delta_softplus=softplus,
+                       threads=2, lib=lib)
+        yr, fr = mixing_matrix_reference(x, dt, A, B, C, D, z, dt_bias, softplus)
+        np.testing.assert_allclose(y, yr, rtol=1e-10, atol=1e-12)
+        np.testing.assert_allclose(fs, fr, rtol=1e-10, atol=1e-12)
+    # optional parts absent: no D, no gate, no bias
+    x, dt, A, B, C, D, z, dt_bias = random_problem(rng, bt=1, dn=2, L=9, N=3)
+    y, fs = O.scan(x, dt, A, B, C, delta_softplus=True, threads=1, lib=lib)
+    yr, fr = mixing_matrix_reference(x, dt, A, B, C, None, None, None, True)
+    np.testing.assert_allclose(y, yr, rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(fs, fr, rtol=1e-10, atol=1e-12)
+
+
+def check_lti_convolution(lib):
+    """Constant delta, B and C make the layer the convolution
+    y_t = sum_j K_j x_{t-j} + D x_t with K_j = sum_n C_n exp(delta A_n)^j delta B_n."""
+    rng = np.random.default_rng(7)
+    L, N = 40, 5
+    dlt = 0.3
+    An = -np.exp(rng.normal(0, 0.5, size=N))
+    Bn, Cn = rng.normal(size=N), rng.normal(size=N)
+    x = rng.normal(size=L)
+    Dd = 0.7
+    y, _ = O.scan(x[None, None, :], np.full((1, 1, L), dlt), An[None, :],
+                  np.repeat(Bn[None, :, None], L, axis=2), np.repeat(Cn[None, :, None], L, axis=2),
+                  D=np.array([Dd]), delta_softplus=False, threads=1, lib=lib)
+    j = np.arange(L)
+    K = (Cn[None, :] * np.exp(dlt * An)[None, :] ** j[:, None] * dlt * Bn[None, :]).sum(axis=1)
+    want = np.convolve(x, K)[:L] + Dd * x
+    np.testing.assert_allclose(y[0, 0], want, rtol=1e-11, atol=1e-12)
+
+
+def check_zero_and_huge_step(lib):
+    """delta = 0 leaves the state untouched (y = C h_prev + D x); a huge step
+    (delta = 50, A = -1) replaces the state by delta * B * x ("The
+    discretization the code actually uses", 'What a huge step means')."""
+    rng = np.random.default_rng(3)
+    L, N = 6, 4
+    h0 = rng.normal(size=(1, 1, N))
+    x = rng.normal(size=(1, 1, L))
+    B = rng.normal(size=(1, N, L)); C = rng.normal(size=(1, N, L))
+    A = -np.arange(1.0, N + 1)[None, :]
+    y, fs = O.scan(x, np.zeros((1, 1, L)), A, B, C, D=np.array([0.5]), delta_softplus=False,
+                   h0=h0, threads=1, lib=lib)
+    np.testing.assert_allclose(y[0, 0], (C[0] * h0[0, 0][:, None]).sum(0) + 0.5 * x[0, 0], atol=1e-14)
+    np.testing.assert_allclose(fs, h0, atol=0)
+    y, fs = O.scan(x, np.full((1, 1, L), 50.0), np.full((1, N), -1.0), B, C, delta_softplus=False,
+                   h0=h0, threads=1, lib=lib)
+    np.testing.assert_allclose(fs[0, 0], 50.0 * B[0, :, -1] * x[0, 0, -1], rtol=1e-12)
+    np.testing.assert_allclose(y[0, 0], (C[0] * 50.0 * B[0] * x[0, 0][None, :]).sum(0), rtol=1e-9)
+
+
+def check_causality_linearity_chain(lib):
+    rng = np.random.default_rng(9)
+    x, dt, A, B, C, D, z, dt_bias = random_problem(rng, bt=2, dn=3, L=30, N=4)
+    kw = dict(D=D, z=z, dt_bias=dt_bias, delta_softplus=True, threads=2, lib=lib)
+    y, fs = O.scan(x, dt, A, B, C, **kw)
+    # causality: a change of x at t0 leaves every earlier output as it was
+    x2 = x.copy(); x2[:, :, 17] += 3.0
+    y2, _ = O.scan(x2, dt, A, B, C, **kw)
+    np.testing.assert_array_equal(y2[:, :, :17], y[:, :, :17])
+    assert np.all(np.abs(y2[:, :, 17] - y[:, :, 17]) > 0)
+    # linearity in x with the steps, B, C and gate held fixed
+    x3 = rng.normal(size=x.shape)
+    ya, fa = O.scan(2.0 * x - 0.5 * x3, dt, A, B, C, **kw)
+    yb, fb = O.scan(x3, dt, A, B, C, **kw)
+    np.testing.assert_allclose(ya, 2.0 * y - 0.5 * yb, rtol=1e-9, atol=1e-11)
+    np.testing.assert_allclose(fa, 2.0 * fs - 0.5 * fb, rtol=1e-9, atol=1e-11)
+    # prefill then continue from the final state == one scan over everything
+    L1 = 11
+    ya, fa = O.scan(x[:, :, :L1], dt[:, :, :L1], A, B[:, :, :L1], C[:, :, :L1], D=D,
+                    z=z[:, :, :L1], dt_bias=dt_bias, delta_softplus=True, threads=2, lib=lib)
+    yb, fb = O.scan(x[:, :, L1:], dt[:, :, L1:], A, B[:, :, L1:], C[:, :, L1:], D=D,
+                    z=z[:, :, L1:], dt_bias=dt_bias, delta_softplus=True, h0=fa, threads=2, lib=lib)
+    np.testing.assert_allclose(np.concatenate([ya, yb], axis=2), y, rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(fb, fs, rtol=1e-12, atol=1e-14)
+
+
+ALL_CHECKS = [check_recurrence_example, check_softplus_values, check_gate_theorem,
+              check_selective_copy_euler, check_impulse_response, check_mixing_matrix,
+              check_lti_convolution, check_zero_and_huge_step, check_causality_linearity_chain]

@@ -1,0 +1,54 @@
+"""Plants plausible mistakes in copies of the oracle (on the CPU) and checks
+that the pins catch every one of them."""
+import os
+
+import pytest
+
+from oracle import oracle as O
+from tests import oracle_pins as P
+
+SRC = open(os.path.join(os.path.dirname(O.__file__), "ss_oracle.c")).read()
+
+WRITE = "double write = delta * B[(b * N + n) * L + t] * xr[t];"
+READ = "out += C[(b * N + n) * L + t] * h[n];"
+SKIP = "out += (D ? D[d] : 0.0) * xr[t];"
+GATE = "out *= zr[t] * sigmoid(zr[t]);"
+DELTA = "double delta = delta_softplus ? oracle_softplus(v) : v;"
+DECAY = "double a_bar = exp(delta * A[d * N + n]);"
+BIAS = "double v = dtr[t] + (dt_bias ? dt_bias[d] : 0.0);"
+
+MUTANTS = {
+    "drop_skip_term": [(SKIP, "")],
+    "read_before_write": [(READ, "out += C[(b * N + n) * L + t] * (h[n] - delta * B[(b * N + n) * L + t]"
+                                 " * xr[t]) / exp(delta * A[d * N + n]);")],
+    "softplus_twice": [(DELTA, "double delta = delta_softplus ? oracle_softplus(oracle_softplus(v)) : v;")],
+    "gate_before_skip": [(SKIP, ""), (GATE, GATE + " out += (D ? D[d] : 0.0) * xr[t];")],
+    "swap_B_and_C": [(WRITE, "double write = delta * C[(b * N + n) * L + t] * xr[t];"),
+                     (READ, "out += B[(b * N + n) * L + t] * h[n];")],
+    "A_transposed": [(DECAY, "double a_bar = exp(delta * A[n * d_inner + d]);")],
+    "bias_ignored": [(BIAS, "double v = dtr[t];")],
+    "zoh_write": [(WRITE, "double write = (a_bar - 1.0) / A[d * N + n] * B[(b * N + n) * L + t] * xr[t];")],
+    "decay_sign": [(DECAY, "double a_bar = exp(-delta * A[d * N + n]);")],
+    "gate_without_z": [(GATE, "out *= sigmoid(zr[t]);")],
+    "B_one_step_late": [(WRITE, "double write = delta * B[(b * N + n) * L + (t > 0 ? t - 1 : 0)] * xr[t];")],
+    "x_missing_in_write": [(WRITE, "double write = delta * B[(b * N + n) * L + t];")],
+    "final_state_stale": [("final_state[r * N + n] = h[n];", "final_state[r * N + n] = h[n] * (L > 1 ? 0.5 : 1.0);")],
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_planted_mistake(name, tmp_path):
+    src = SRC
+    for old, new in MUTANTS[name]:
+        assert old in src, (name, old)
+        src = src.replace(old, new, 1)
+    path = tmp_path / ("mutant_%s.c" % name)
+    path.write_text(src)
+    lib = O.load(O.build(force=True, src=str(path), out=str(tmp_path / ("lib%s.so" % name))))
+    failed = []
+    for check in P.ALL_CHECKS:
+        try:
+            check(lib)
+        except (AssertionError, FloatingPointError, OverflowError, ValueError):
+            failed.append(check.__name__)
+    assert failed, "no pin caught mutant %s" % name
