@@ -1,0 +1,489 @@
+#!/usr/bin/env python
+"""Benchmark of the selective scan (S6) and its decode state update on B300.
+
+One step = one selective-scan pass (softplus step, discretisation, recurrence,
+readout, gate, final state) over the Mamba-130M-layer workload: batch 8,
+d_inner 1536, L 2048, N 16, bf16 io with fp32 state. The metric is
+element-steps per second (batch * d_inner * L * N / s), with achieved HBM GB/s
+as a fraction of the measured copy bandwidth in the roofline object.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+For N > 1 launch with torch.distributed.run; every rank scans its own batch
+shard (independent sequences, no collective on the data path: weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from selective_state_space_138_b300 import inputs as I  # noqa: E402
+
+HEADLINE = I.MAMBA130M
+METRIC = "selective-scan element-steps/s (B*D*L*N)"
+UNIT = "element-steps/s"
+L2_FLUSH_BYTES = 256 << 20  # > the 126 MB L2
+FALLBACK_HBM_GBS = 6400.0
+SRC = os.path.join(ROOT, "selective_state_space_138_b300", "csrc", "ss_scan.cu")
+
+
+# ----------------------------------------------------------------- helpers
+
+def io_bytes(io: str) -> int:
+    return 2 if io == "bf16" else 4
+
+
+def scan_alg_bytes(spec: I.ScanSpec, final_state: bool = True) -> int:
+    """Bytes the fused scan must move: read x, dt, z and write y (batch, d_inner,
+    L); read B, C (batch, N, L); read A (d_inner, N), D and dt_bias; write the
+    final state (batch, d_inner, N) fp32."""
+    s = io_bytes(spec.io)
+    bdl = spec.batch * spec.d_inner * spec.L
+    b = 4 * bdl * s + spec.batch * spec.L * 2 * spec.N * s + spec.d_inner * spec.N * 4 + 2 * spec.d_inner * 4
+    if final_state:
+        b += spec.batch * spec.d_inner * spec.N * 4
+    return b
+
+
+def decode_alg_bytes(spec: I.DecodeSpec) -> int:
+    """Per step: read and write the fp32 state, read x, delta, z and write y,
+    read B, C, A and D."""
+    bd = spec.batch * spec.d_inner
+    return 2 * bd * spec.N * 4 + 4 * bd * 2 + 2 * spec.batch * spec.N * 2 + spec.d_inner * spec.N * 4 + spec.d_inner * 4
+
+
+def measured_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": FALLBACK_HBM_GBS, "source": "fallback"}
+
+
+def profiled_traffic(kernel_key: str):
+    """Bytes per launch (dram read + write) from the committed ncu summary of
+    ``kernel_key``, when the kernel source has not changed since the capture."""
+    src_hash = hashlib.sha256(open(SRC, "rb").read()).hexdigest()
+    path = os.path.join(ROOT, "profiles", kernel_key + ".md")
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    for line in open(path):
+        if ":" in line and line.strip().startswith(("traffic_bytes_per_launch", "source_sha256")):
+            k, v = line.strip().strip("`").split(":", 1)
+            vals[k.strip()] = v.strip().strip("`")
+    if vals.get("source_sha256") != src_hash:
+        return None
+    try:
+        return float(vals["traffic_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        os.unlink(self.path)
+        busy = [s for s, p in zip(sm, power)]
+        return {"sm_mhz": statistics.median(busy) if busy else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm),
+                "power_w_max": max(power) if power else None,
+                "reasons": sorted(reasons)}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def reduce_max(value: float, world: int) -> float:
+    if world == 1:
+        return value
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ----------------------------------------------------------------- GPU arm
+
+def shard_spec(spec: I.ScanSpec, rank: int) -> I.ScanSpec:
+    """Rank r scans its own batch shard: the same shape, a distinct seed."""
+    import dataclasses
+    return dataclasses.replace(spec, seed=spec.seed + 1000 * rank)
+
+
+def time_scan(spec: I.ScanSpec, steps: int, warmup: int, flush: bool = True, soak_s: float = 0.0):
+    """Per-launch device times (ms) of the scan kernel over ``steps`` launches,
+    each preceded by an L2 flush; events on the launching stream."""
+    from selective_state_space_138_b300 import binding
+    inp = I.make_scan_inputs(spec)
+    g = {k: v.cuda() for k, v in inp.items() if k != "reset_pos"}
+    y = torch.empty_like(g["x"])
+    fs = torch.empty(spec.batch, spec.d_inner, spec.N, device="cuda", dtype=torch.float32)
+    scratch = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+
+    def run():
+        binding.scan_fwd(g["x"], g["dt"], g["A"], g["B"], g["C"], D=g["D"], z=g["z"], dt_bias=g["dt_bias"],
+                         y=y, final_state=fs)
+
+    for _ in range(warmup):
+        run()
+    torch.cuda.synchronize()
+    if soak_s > 0:  # untimed: let clocks settle under this load
+        t_end = time.time() + soak_s
+        while time.time() < t_end:
+            for _ in range(20):
+                run()
+            torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    torch.cuda.synchronize()
+    for i in range(steps):
+        if flush:
+            scratch.zero_()
+        starts[i].record()
+        run()
+        ends[i].record()
+    torch.cuda.synchronize()
+    times = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    del g, y, fs, scratch
+    torch.cuda.empty_cache()
+    return times
+
+
+def time_scan_e2e(spec: I.ScanSpec, steps: int, warmup: int):
+    """Same metric through the C ABI with pinned host buffers: every step copies
+    its inputs host->device, scans, and copies y and the final state back."""
+    from selective_state_space_138_b300 import binding
+    inp = I.make_scan_inputs(spec)
+    keys = ("x", "dt", "z", "B", "C", "A", "D", "dt_bias")
+    host = {k: inp[k].pin_memory() for k in keys}
+    g = {k: torch.empty_like(host[k], device="cuda") for k in keys}
+    y = torch.empty_like(g["x"])
+    fs = torch.empty(spec.batch, spec.d_inner, spec.N, device="cuda", dtype=torch.float32)
+    y_h = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
+    fs_h = torch.empty(fs.shape, dtype=fs.dtype, pin_memory=True)
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = y.numel() * y.element_size() + fs.numel() * fs.element_size()
+
+    def step():
+        for k in keys:
+            g[k].copy_(host[k], non_blocking=True)
+        binding.scan_fwd(g["x"], g["dt"], g["A"], g["B"], g["C"], D=g["D"], z=g["z"], dt_bias=g["dt_bias"],
+                         y=y, final_state=fs)
+        y_h.copy_(y, non_blocking=True)
+        fs_h.copy_(fs, non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    s = torch.cuda.Event(enable_timing=True)
+    e = torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(steps):
+        step()
+    e.record()
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / steps
+    return ms, h2d, d2h
+
+
+def time_decode(spec: I.DecodeSpec, reps: int, warmup: int):
+    """1024 consecutive single-token updates captured in one CUDA graph; also
+    the same updates launched one by one with an L2 flush before each."""
+    from selective_state_space_138_b300 import binding
+    tok = I.make_decode_tokens(spec)
+    par = I.make_decode_params(spec)
+    gt = {k: v.cuda() for k, v in tok.items()}
+    del tok
+    A = par["A"].cuda()
+    D = par["D"].cuda()
+    state = torch.zeros(spec.batch, spec.d_inner, spec.N, device="cuda")
+    ys = torch.empty_like(gt["x"])
+    T = spec.steps
+
+    def chain():
+        for t in range(T):
+            binding.state_update(state, gt["x"][t], gt["delta"][t], A, gt["B"][t], gt["C"][t], D=D, z=gt["z"][t],
+                                 y=ys[t])
+
+    chain()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s, capture_error_mode="relaxed"):
+            chain()
+    torch.cuda.synchronize()
+    for _ in range(warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    ev[0].record()
+    for _ in range(reps):
+        graph.replay()
+    ev[1].record()
+    torch.cuda.synchronize()
+    graph_ms_per_token = ev[0].elapsed_time(ev[1]) / (reps * T)
+
+    scratch = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    n_flushed = min(T, 64)
+    st = [torch.cuda.Event(enable_timing=True) for _ in range(n_flushed)]
+    en = [torch.cuda.Event(enable_timing=True) for _ in range(n_flushed)]
+    for t in range(n_flushed):
+        scratch.zero_()
+        st[t].record()
+        binding.state_update(state, gt["x"][t], gt["delta"][t], A, gt["B"][t], gt["C"][t], D=D, z=gt["z"][t],
+                             y=ys[t])
+        en[t].record()
+    torch.cuda.synchronize()
+    flushed_ms = statistics.median([a.elapsed_time(b) for a, b in zip(st, en)])
+    del gt, ys, state, scratch, graph
+    torch.cuda.empty_cache()
+    return graph_ms_per_token, flushed_ms
+
+
+def roofline_obj(alg_bytes: float, ms: float, peaks: dict, traffic):
+    achieved = alg_bytes / (ms * 1e-3) / 1e9
+    return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
+            "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs)" if peaks["source"] == "measured"
+            else "fallback 6400 GB/s"}
+
+
+# ----------------------------------------------------------------- CPU (oracle)
+
+def oracle_rate(spec: I.ScanSpec, budget_s: float, inp=None):
+    """The float64 oracle timed on this host's cores on a bounded sample of the
+    workload's rows (whole rows, every time step). Returns (elem-steps/s,
+    cores, sample description, seconds)."""
+    from oracle import oracle as O
+    inp = inp if inp is not None else I.make_scan_inputs(spec)
+    cores = O.default_threads()
+    rows_total = spec.batch * spec.d_inner
+    probe_rows = list(range(0, rows_total, max(1, rows_total // (4 * cores))))[: 4 * cores]
+    t = time.time()
+    O.scan_rows(inp, probe_rows, threads=cores)
+    per_row = (time.time() - t) / len(probe_rows)
+    n_rows = int(min(rows_total, max(cores, budget_s / max(per_row, 1e-9))))
+    stride = max(1, rows_total // n_rows)
+    rows = list(range(0, rows_total, stride))[:n_rows]
+    t = time.time()
+    O.scan_rows(inp, rows, threads=cores)
+    sec = time.time() - t
+    elems = len(rows) * spec.L * spec.N
+    desc = "%d of %d (batch, channel) rows, every %d-th, all %d steps x %d states" % (
+        len(rows), rows_total, stride, spec.L, spec.N)
+    return elems / sec, cores, desc, sec
+
+
+def reference_arm(args, rank, world):
+    """The oracle as the reference arm: rank 0 only, host cores."""
+    if rank != 0:
+        return 0
+    spec = HEADLINE
+    inp = I.make_scan_inputs(spec)
+    for _ in range(args.warmup):
+        oracle_rate(spec, budget_s=1.0, inp=inp)
+    rates, secs = [], 0.0
+    desc, cores = "", 1
+    t0 = time.time()
+    for _ in range(args.steps):
+        r, cores, desc, s = oracle_rate(spec, budget_s=3.0, inp=inp)
+        rates.append(r)
+        secs += s
+    value = statistics.median(rates)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / max(1, args.steps),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": spec.name, "batch": spec.batch, "d_inner": spec.d_inner, "L": spec.L, "N": spec.N,
+                   "io": spec.io},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "wall_s": round(time.time() - t0, 2),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------- main
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--headline-only", action="store_true", help="skip the other workloads")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        return reference_arm(args, rank, world)
+
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    gpu_index = torch.cuda.current_device()
+
+    from selective_state_space_138_b300 import binding
+    binding.lib()  # fails loudly if the CUDA library is missing
+
+    peaks = measured_peaks()
+    spec = shard_spec(HEADLINE, rank)
+
+    sampler = ClockSampler(gpu_index) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    t_wall = time.time()
+    times = time_scan(spec, args.steps, args.warmup, flush=True, soak_s=1.0)
+    torch.cuda.synchronize()
+    barrier(world)
+    wall = time.time() - t_wall
+    clocks = sampler.stop() if sampler else None
+
+    total_ms = sum(times)
+    total_ms_max = reduce_max(total_ms, world)
+    ms_per_step = total_ms_max / args.steps
+    elems = spec.elem_steps
+    value = world * elems / (ms_per_step * 1e-3)
+    alg = scan_alg_bytes(spec)
+    traffic = profiled_traffic("scan_fwd_" + HEADLINE.name)
+
+    e2e_ms, h2d, d2h = time_scan_e2e(spec, max(3, args.steps // 5), 3)
+    e2e_ms = reduce_max(e2e_ms, world)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "io_dtype": "bf16", "data": "synthetic",
+        "config": {"workload": HEADLINE.name, "batch": spec.batch, "d_inner": spec.d_inner, "L": spec.L,
+                   "N": spec.N, "io": spec.io, "per_gpu": True, "l2": "flushed (256 MB write) before every step",
+                   "parallelism": "dp%d (independent batch shards)" % world},
+        "kernel_ms": {"median": statistics.median(times), "min": min(times), "max": max(times)},
+        "roofline": roofline_obj(alg, ms_per_step, peaks, traffic),
+        "alg_bytes_per_step": alg,
+        "gpu_launches": args.steps,
+        "e2e": {"value": world * elems / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "clocks": clocks,
+        "wall_s": round(wall, 3),
+    }
+
+    if rank == 0 and world == 1 and not args.headline_only:
+        extras = {}
+        for wspec in (I.MAMBA1P4B, I.LONGSEQ):
+            t = time_scan(wspec, 10, 3, flush=True)
+            ms = statistics.median(t)
+            extras[wspec.name] = {
+                "elem_steps_per_s": wspec.elem_steps / (ms * 1e-3), "kernel_ms_median": ms,
+                "roofline": roofline_obj(scan_alg_bytes(wspec), ms, peaks, profiled_traffic("scan_fwd_" + wspec.name))}
+        t = time_scan(I.TINY, 20, 3, flush=False)
+        extras[I.TINY.name] = {"elem_steps_per_s": I.TINY.elem_steps / (statistics.median(t) * 1e-3),
+                               "kernel_ms_median": statistics.median(t), "note": "launch-bound; parity case"}
+        gms, fms = time_decode(I.DECODE, reps=3, warmup=3)
+        dbytes = decode_alg_bytes(I.DECODE)
+        extras[I.DECODE.name] = {
+            "elem_steps_per_s": I.DECODE.elem_steps_per_step / (gms * 1e-3),
+            "ms_per_token_graph": gms, "ms_per_token_l2_flushed": fms,
+            "roofline_graph": roofline_obj(dbytes, gms, peaks, None),
+            "roofline_l2_flushed": roofline_obj(dbytes, fms, peaks, profiled_traffic("state_update_" + I.DECODE.name)),
+            "note": "graph: 1024 updates back to back, the 84 MB fp32 state can stay in the 126 MB L2; "
+                    "l2_flushed: each update after a 256 MB write"}
+        line["workloads"] = extras
+
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        r, cores, desc, sec = oracle_rate(spec, budget_s=12.0)
+        line["cpu_baseline"] = {"value": r, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc,
+                                "seconds": round(sec, 2)}
+
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,137 @@
+/*
+ * ss_scan.h -- C ABI of the B300 (sm_103a) selective-scan library (libssscan.so).
+ *
+ * The library computes the Mamba selective state-space layer (S6) forward
+ * pass and its single-token state update, as defined in "Mamba and selective
+ * state spaces" (box "Selective state-space model (S6)", section "The
+ * discretization the code actually uses"):
+ *
+ *   delta_t   = softplus(dt_t + dt_bias_d)             (or dt_t + dt_bias_d)
+ *   h_t[n]    = exp(delta_t * A[d,n]) * h_{t-1}[n] + delta_t * B_t[n] * x_t
+ *   y_t       = sum_n C_t[n] * h_t[n] + D[d] * x_t
+ *   out_t     = y_t * z_t * sigmoid(z_t)                (gate, "The Mamba block")
+ *
+ * with the exponential-Euler input weight delta*B (not zero-order hold), the
+ * state read after the write of token t, and h_0 = 0.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Every tensor pointer is DEVICE memory of the current CUDA device,
+ *   contiguous and row-major, owned by the caller. The library allocates
+ *   nothing and keeps no state between calls, apart from a thread-local
+ *   message for the last error (ss_last_error).
+ * - A is the negative real state eigenvalue lambda itself (not its log).
+ *   A, D, dt_bias and every state buffer are fp32 whatever the io dtype.
+ * - "bf16" arguments are raw bfloat16 bit patterns (ss_bf16).
+ * - Work is enqueued on `stream` (0 = legacy default stream) and the call
+ *   returns without synchronising: a fault during execution surfaces at the
+ *   caller's next synchronisation, like any CUDA launch.
+ * - Arguments are validated on the host before anything is enqueued; a
+ *   non-zero ss_status means nothing was launched. There is no CPU fallback.
+ * - Outputs must not overlap any input.
+ */
+#ifndef SS_SCAN_H
+#define SS_SCAN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *cudaStream_t;
+typedef uint16_t ss_bf16; /* raw bfloat16 bits */
+
+typedef enum ss_status {
+    SS_OK = 0,
+    SS_ERR_NULL = -1,        /* a required pointer is NULL */
+    SS_ERR_DIM = -2,         /* a size is <= 0 or the element count overflows */
+    SS_ERR_N = -3,           /* N outside [1, SS_MAX_N] */
+    SS_ERR_DEVICE_PTR = -4,  /* a pointer is not device memory of the current device */
+    SS_ERR_LAUNCH = -5,      /* the kernel launch itself failed */
+    SS_ERR_INTERNAL = -6     /* a CUDA runtime query failed */
+} ss_status;
+
+#define SS_MAX_N 64
+#define SS_ABI_VERSION 1
+
+/*
+ * ss_scan_fwd_bf16 / ss_scan_fwd_f32 -- selective scan over a whole sequence.
+ *
+ * Defines: "Mamba and selective state spaces", box "Selective state-space
+ * model (S6)" (the recurrence and readout), section "The discretization the
+ * code actually uses" (input weight delta*B), section "The Mamba block" (the
+ * silu(z) gate); the fused one-pass design of section "Why the scan must be
+ * fused" (only x, delta, z, B, C, A are read, only y and the final state are
+ * written; the (batch, L, d_inner, N) states are never stored).
+ *
+ *   x, delta, z : (batch, d_inner, L) io dtype. `delta` is the raw step dt.
+ *   A           : (d_inner, N) fp32, the eigenvalues lambda (normally < 0).
+ *   B, C        : (batch, N, L) io dtype, shared by all channels.
+ *   D           : (d_inner) fp32 skip weight, or NULL for none.
+ *   z           : or NULL for no gate.
+ *   dt_bias     : (d_inner) fp32, or NULL for a bias of 0.
+ *   delta_softplus : non-zero: step = softplus(delta + dt_bias);
+ *                    zero:     step = delta + dt_bias.
+ *                    The bias is added exactly once in either case.
+ *   y           : (batch, d_inner, L) io dtype output (gated when z != NULL).
+ *   final_state : (batch, d_inner, N) fp32 output h_L, or NULL to skip.
+ *   batch, d_inner, L >= 1; 1 <= N <= SS_MAX_N.
+ *
+ * Errors: SS_ERR_NULL (x, delta, A, B, C or y NULL), SS_ERR_DIM, SS_ERR_N,
+ * SS_ERR_DEVICE_PTR, SS_ERR_LAUNCH, SS_ERR_INTERNAL.
+ * Alignment: 16-byte aligned io pointers and L a multiple of 16 select the
+ * vectorised path; any other layout takes a scalar-load path (not an error).
+ */
+ss_status ss_scan_fwd_bf16(const ss_bf16 *x, const ss_bf16 *delta, const float *A,
+                           const ss_bf16 *B, const ss_bf16 *C, const float *D,
+                           const ss_bf16 *z, const float *dt_bias, int delta_softplus,
+                           ss_bf16 *y, float *final_state, int64_t batch,
+                           int64_t d_inner, int64_t L, int64_t N, cudaStream_t stream);
+
+ss_status ss_scan_fwd_f32(const float *x, const float *delta, const float *A,
+                          const float *B, const float *C, const float *D,
+                          const float *z, const float *dt_bias, int delta_softplus,
+                          float *y, float *final_state, int64_t batch,
+                          int64_t d_inner, int64_t L, int64_t N, cudaStream_t stream);
+
+/*
+ * ss_state_update_bf16 / ss_state_update_f32 -- one decode step on a cached
+ * state, "Mamba and selective state spaces", section "Decoding with a
+ * constant-size cache": the state update of the definition applied once,
+ * O(d_inner * N) work whatever the context length.
+ *
+ *   state  : (batch, d_inner, N) fp32, read and updated in place
+ *            (h <- exp(delta*A) * h + delta * B * x).
+ *   x, delta, z, y : (batch, d_inner) io dtype; `delta` is the final positive
+ *            step (no bias, no softplus is applied here).
+ *   A      : (d_inner, N) fp32.  D : (d_inner) fp32 or NULL.  z : or NULL.
+ *   B, C   : (batch, N) io dtype.
+ *   y      : output, sum_n C[n] * h[n] + D * x, gated by silu(z).
+ *
+ * Errors: as ss_scan_fwd_*; state, x, delta, A, B, C and y are required.
+ */
+ss_status ss_state_update_bf16(float *state, const ss_bf16 *x, const ss_bf16 *delta,
+                               const float *A, const ss_bf16 *B, const ss_bf16 *C,
+                               const float *D, const ss_bf16 *z, ss_bf16 *y,
+                               int64_t batch, int64_t d_inner, int64_t N,
+                               cudaStream_t stream);
+
+ss_status ss_state_update_f32(float *state, const float *x, const float *delta,
+                              const float *A, const float *B, const float *C,
+                              const float *D, const float *z, float *y,
+                              int64_t batch, int64_t d_inner, int64_t N,
+                              cudaStream_t stream);
+
+/* Message describing the last non-OK status returned on this host thread
+ * ("" if none). The string is owned by the library. */
+const char *ss_last_error(void);
+
+/* SS_ABI_VERSION of the loaded library. */
+int ss_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SS_SCAN_H */

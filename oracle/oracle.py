@@ -120,32 +120,31 @@ def scan_rows(inp: dict, rows, delta_softplus=True, use_D=True, use_z=True, use_
     """Scan only the listed rows r = b * d_inner + d of a workload.
 
     ``inp`` holds x, dt, z (batch, d_inner, L), B, C (batch, N, L), A, D,
-    dt_bias (CPU tensors or arrays). Each row is run as its own one-channel
-    problem. Returns (y (len(rows), L), final_state (len(rows), N)).
+    dt_bias (CPU tensors or arrays). Rows of the same batch row b are run as
+    one problem over the selected channels. Returns (y (len(rows), L),
+    final_state (len(rows), N)) in the order of ``rows``.
     """
-    lib = load()
     batch, d_inner, L = tuple(inp["x"].shape)
-    rows = [int(r) for r in rows]
-
-    def one(r):
-        b, d = divmod(r, d_inner)
-        sl = lambda t: _f64(t[b, d])[None, None, :]
-        y, fs = scan(sl(inp["x"]), sl(inp["dt"]), _f64(inp["A"][d])[None, :],
-                     _f64(inp["B"][b])[None], _f64(inp["C"][b])[None],
-                     D=_f64(inp["D"][d:d + 1]) if use_D and inp.get("D") is not None else None,
-                     z=sl(inp["z"]) if use_z and inp.get("z") is not None else None,
-                     dt_bias=(_f64(inp["dt_bias"][d:d + 1])
-                              if use_bias and inp.get("dt_bias") is not None else None),
-                     delta_softplus=delta_softplus, threads=1, lib=lib)
-        return y[0, 0], fs[0, 0]
-
-    nt = max(1, min(threads or default_threads(), len(rows))) if rows else 1
-    with ThreadPoolExecutor(nt) as ex:
-        res = list(ex.map(one, rows))
     N = inp["A"].shape[1]
-    if not res:
-        return np.empty((0, L)), np.empty((0, N))
-    return np.stack([r[0] for r in res]), np.stack([r[1] for r in res])
+    rows = [int(r) for r in rows]
+    y = np.empty((len(rows), L))
+    fs = np.empty((len(rows), N))
+    by_b = {}
+    for i, r in enumerate(rows):
+        by_b.setdefault(r // d_inner, []).append(i)
+    for b, idx in by_b.items():
+        ds = [rows[i] % d_inner for i in idx]
+        pick = lambda t: _f64(t[b][ds])[None]
+        yb, fb = scan(pick(inp["x"]), pick(inp["dt"]), _f64(inp["A"][ds]),
+                      _f64(inp["B"][b])[None], _f64(inp["C"][b])[None],
+                      D=_f64(inp["D"][ds]) if use_D and inp.get("D") is not None else None,
+                      z=pick(inp["z"]) if use_z and inp.get("z") is not None else None,
+                      dt_bias=(_f64(inp["dt_bias"][ds])
+                               if use_bias and inp.get("dt_bias") is not None else None),
+                      delta_softplus=delta_softplus, threads=threads)
+        y[idx] = yb[0]
+        fs[idx] = fb[0]
+    return y, fs
 
 
 def decode_chain(tokens: dict, params: dict, rows, use_D=True, use_z=True, h0=None,
@@ -157,29 +156,27 @@ def decode_chain(tokens: dict, params: dict, rows, use_D=True, use_z=True, h0=No
     no softplus). h0: None (zero state) or (len(rows), N).
     Returns (y (len(rows), steps), state after the last step (len(rows), N)).
     """
-    lib = load()
     steps, batch, d_inner = tuple(tokens["x"].shape)
+    N = params["A"].shape[1]
     rows = [int(r) for r in rows]
-
-    def one(i):
-        r = rows[i]
-        b, d = divmod(r, d_inner)
-        col = lambda t: _f64(t[:, b, d])[None, None, :]
+    y = np.empty((len(rows), steps))
+    fs = np.empty((len(rows), N))
+    by_b = {}
+    for i, r in enumerate(rows):
+        by_b.setdefault(r // d_inner, []).append(i)
+    for b, idx in by_b.items():
+        ds = [rows[i] % d_inner for i in idx]
+        col = lambda t: _f64(t[:, b][:, ds]).T[None].copy()  # (1, len(ds), steps)
         Bb = _f64(tokens["B"][:, b, :]).T[None].copy()
         Cb = _f64(tokens["C"][:, b, :]).T[None].copy()
-        y, fs = scan(col(tokens["x"]), col(tokens["delta"]), _f64(params["A"][d])[None, :], Bb, Cb,
-                     D=_f64(params["D"][d:d + 1]) if use_D else None,
-                     z=col(tokens["z"]) if use_z else None, dt_bias=None, delta_softplus=False,
-                     h0=None if h0 is None else _f64(h0[i])[None, None, :], threads=1, lib=lib)
-        return y[0, 0], fs[0, 0]
-
-    nt = max(1, min(threads or default_threads(), len(rows))) if rows else 1
-    with ThreadPoolExecutor(nt) as ex:
-        res = list(ex.map(one, range(len(rows))))
-    N = params["A"].shape[1]
-    if not res:
-        return np.empty((0, steps)), np.empty((0, N))
-    return np.stack([r[0] for r in res]), np.stack([r[1] for r in res])
+        yb, fb = scan(col(tokens["x"]), col(tokens["delta"]), _f64(params["A"][ds]), Bb, Cb,
+                      D=_f64(params["D"][ds]) if use_D else None,
+                      z=col(tokens["z"]) if use_z else None, dt_bias=None, delta_softplus=False,
+                      h0=None if h0 is None else _f64(np.asarray(h0)[idx])[None],
+                      threads=threads)
+        y[idx] = yb[0]
+        fs[idx] = fb[0]
+    return y, fs
 
 
 # ---------------------------------------------------------------- helpers

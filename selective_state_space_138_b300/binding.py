@@ -1,0 +1,157 @@
+"""ctypes binding of ``libssscan.so`` (C ABI in include/ss_scan.h).
+
+Argument marshalling only: shapes and dtypes are checked, outputs are
+allocated with torch when the caller passes none, and the raw device pointers
+plus the current CUDA stream are handed to the library. Every step of the
+computation runs in the library's CUDA kernels; there is no fallback. If the
+library is missing or a call fails, an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libssscan.so")
+
+# names declared in include/ss_scan.h
+EXPORTS = ("ss_scan_fwd_bf16", "ss_scan_fwd_f32", "ss_state_update_bf16", "ss_state_update_f32",
+           "ss_last_error", "ss_abi_version")
+
+STATUS = {0: "SS_OK", -1: "SS_ERR_NULL", -2: "SS_ERR_DIM", -3: "SS_ERR_N", -4: "SS_ERR_DEVICE_PTR",
+          -5: "SS_ERR_LAUNCH", -6: "SS_ERR_INTERNAL"}
+MAX_N = 64
+
+_lib = None
+
+
+class SSError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__("%s (%d): %s" % (STATUS.get(status, "?"), status, message))
+        self.status = status
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError("CUDA library %s is missing; build it with "
+                           "`python -m selective_state_space_138_b300.build`" % LIB_PATH)
+    L = ctypes.CDLL(LIB_PATH)
+    vp, i64, ci = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    scan_args = [vp] * 8 + [ci, vp, vp, i64, i64, i64, i64, vp]
+    upd_args = [vp] * 9 + [i64, i64, i64, vp]
+    for name in ("ss_scan_fwd_bf16", "ss_scan_fwd_f32"):
+        getattr(L, name).argtypes = scan_args
+        getattr(L, name).restype = ci
+    for name in ("ss_state_update_bf16", "ss_state_update_f32"):
+        getattr(L, name).argtypes = upd_args
+        getattr(L, name).restype = ci
+    L.ss_last_error.argtypes = []
+    L.ss_last_error.restype = ctypes.c_char_p
+    L.ss_abi_version.argtypes = []
+    L.ss_abi_version.restype = ci
+    _lib = L
+    return L
+
+
+def last_error() -> str:
+    return lib().ss_last_error().decode()
+
+
+def abi_version() -> int:
+    return lib().ss_abi_version()
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(status: int):
+    if status != 0:
+        raise SSError(status, last_error())
+
+
+def _need(t, name, dtype, shape):
+    if t is None:
+        return
+    if t.dtype != dtype:
+        raise TypeError("%s: dtype %s, expected %s" % (name, t.dtype, dtype))
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError("%s: shape %s, expected %s" % (name, tuple(t.shape), tuple(shape)))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+
+
+def _io_suffix(dtype):
+    if dtype == torch.bfloat16:
+        return "bf16"
+    if dtype == torch.float32:
+        return "f32"
+    raise TypeError("io dtype must be bfloat16 or float32, got %s" % dtype)
+
+
+def scan_fwd(x, delta, A, B, C, D=None, z=None, dt_bias=None, delta_softplus=True,
+             y=None, final_state=None, return_final_state=True, stream=None):
+    """Selective scan over (batch, d_inner, L) inputs; see ``ss_scan_fwd_*``.
+
+    x, delta, z: (batch, d_inner, L); B, C: (batch, N, L) in the io dtype
+    (bf16 or fp32); A: (d_inner, N), D, dt_bias: (d_inner,) fp32.
+    Returns (y, final_state); final_state is None unless requested.
+    """
+    io = x.dtype
+    sfx = _io_suffix(io)
+    batch, d_inner, L = x.shape
+    N = A.shape[1] if A.dim() == 2 else -1
+    _need(x, "x", io, (batch, d_inner, L))
+    _need(delta, "delta", io, (batch, d_inner, L))
+    _need(z, "z", io, (batch, d_inner, L))
+    _need(B, "B", io, (batch, N, L))
+    _need(C, "C", io, (batch, N, L))
+    _need(A, "A", torch.float32, (d_inner, N))
+    _need(D, "D", torch.float32, (d_inner,))
+    _need(dt_bias, "dt_bias", torch.float32, (d_inner,))
+    if y is None:
+        y = torch.empty_like(x)
+    _need(y, "y", io, (batch, d_inner, L))
+    if final_state is None and return_final_state:
+        final_state = torch.empty((batch, d_inner, N), dtype=torch.float32, device=x.device)
+    _need(final_state, "final_state", torch.float32, (batch, d_inner, N))
+    fn = getattr(lib(), "ss_scan_fwd_" + sfx)
+    _check(fn(_ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(dt_bias),
+              int(bool(delta_softplus)), _ptr(y), _ptr(final_state), batch, d_inner, L, N,
+              _stream(stream)))
+    return y, final_state
+
+
+def state_update(state, x, delta, A, B, C, D=None, z=None, y=None, stream=None):
+    """One decode step on ``state`` (batch, d_inner, N) fp32, updated in place;
+    see ``ss_state_update_*``. x, delta, z: (batch, d_inner); B, C: (batch, N).
+    Returns y (batch, d_inner)."""
+    io = x.dtype
+    sfx = _io_suffix(io)
+    batch, d_inner = x.shape
+    N = A.shape[1] if A.dim() == 2 else -1
+    _need(state, "state", torch.float32, (batch, d_inner, N))
+    _need(delta, "delta", io, (batch, d_inner))
+    _need(z, "z", io, (batch, d_inner))
+    _need(B, "B", io, (batch, N))
+    _need(C, "C", io, (batch, N))
+    _need(A, "A", torch.float32, (d_inner, N))
+    _need(D, "D", torch.float32, (d_inner,))
+    if y is None:
+        y = torch.empty_like(x)
+    _need(y, "y", io, (batch, d_inner))
+    fn = getattr(lib(), "ss_state_update_" + sfx)
+    _check(fn(_ptr(state), _ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(y),
+              batch, d_inner, N, _stream(stream)))
+    return y

@@ -1,0 +1,96 @@
+"""The C-ABI library loads, exports every symbol its header declares, and
+rejects bad arguments on the host before touching a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+from selective_state_space_138_b300 import binding, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ss_scan.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ss_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_and_binding_agree():
+    assert declared_functions() == sorted(binding.EXPORTS)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    out = os.popen("nm -D --defined-only %s" % binding.LIB_PATH).read()
+    for name in declared_functions():
+        assert re.search(r"\bT %s$" % name, out, flags=re.M), name
+
+
+def test_abi_version_and_empty_error(lib):
+    assert binding.abi_version() == 1
+    assert isinstance(binding.last_error(), str)
+
+
+def test_library_has_no_torch_dependency(lib):
+    out = os.popen("ldd %s" % binding.LIB_PATH).read()
+    assert "torch" not in out and "c10" not in out
+
+
+def test_library_built_for_sm103a():
+    assert build.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+NULL = None
+
+
+def _scan(lib, sfx, x=1, dt=1, A=1, B=1, C=1, y=1, batch=1, d=1, L=1, N=16):
+    p = lambda v: ctypes.c_void_p(v) if v else None
+    fn = getattr(lib, "ss_scan_fwd_" + sfx)
+    return fn(p(x), p(dt), p(A), p(B), p(C), None, None, None, 1, p(y), None, batch, d, L, N, None)
+
+
+@pytest.mark.parametrize("sfx", ["bf16", "f32"])
+def test_scan_host_validation(lib, sfx):
+    assert _scan(lib, sfx, batch=0) == -2
+    assert _scan(lib, sfx, L=-3) == -2
+    assert "positive" in binding.last_error()
+    assert _scan(lib, sfx, N=0) == -3
+    assert _scan(lib, sfx, N=65) == -3
+    assert "N=65" in binding.last_error()
+    assert _scan(lib, sfx, x=0) == -1
+    assert "x" in binding.last_error()
+    assert _scan(lib, sfx, y=0) == -1
+    assert _scan(lib, sfx, batch=1 << 30, d=1 << 30, L=1 << 20) == -2
+
+
+@pytest.mark.parametrize("sfx", ["bf16", "f32"])
+def test_update_host_validation(lib, sfx):
+    fn = getattr(lib, "ss_state_update_" + sfx)
+    one = ctypes.c_void_p(1)
+    assert fn(one, one, one, one, one, one, None, None, one, 0, 4, 16, None) == -2
+    assert fn(one, one, one, one, one, one, None, None, one, 2, 4, 100, None) == -3
+    assert fn(None, one, one, one, one, one, None, None, one, 2, 4, 16, None) == -1
+    assert "state" in binding.last_error()
+
+
+def test_binding_checks_shapes_before_calling():
+    x = torch.zeros(2, 3, 8)
+    with pytest.raises(ValueError):
+        binding.scan_fwd(x, torch.zeros(2, 3, 9), torch.zeros(3, 4), torch.zeros(2, 4, 8), torch.zeros(2, 4, 8))
+    with pytest.raises(TypeError):
+        binding.scan_fwd(x.half(), x.half(), torch.zeros(3, 4), torch.zeros(2, 4, 8).half(),
+                         torch.zeros(2, 4, 8).half())
+    with pytest.raises(TypeError):
+        binding.scan_fwd(x, x, torch.zeros(3, 4, dtype=torch.float64), torch.zeros(2, 4, 8),
+                         torch.zeros(2, 4, 8))
