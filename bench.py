@@ -66,12 +66,15 @@ def decode_alg_bytes(spec: I.DecodeSpec) -> int:
 
 def measured_peaks() -> dict:
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count \
+        if torch.cuda.is_available() else 148
     try:
         with open(path) as f:
             d = json.load(f)
-        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured", "sms": sms,
+                "sm_max_mhz": float(d.get("sm_max_mhz", 2032.0))}
     except Exception:
-        return {"hbm_gbs": FALLBACK_HBM_GBS, "source": "fallback"}
+        return {"hbm_gbs": FALLBACK_HBM_GBS, "source": "fallback", "sms": sms, "sm_max_mhz": 2032.0}
 
 
 def profiled_traffic(kernel_key: str):
@@ -313,12 +316,23 @@ def time_decode(spec: I.DecodeSpec, reps: int, warmup: int):
     return graph_ms_per_token, flushed_ms
 
 
-def roofline_obj(alg_bytes: float, ms: float, peaks: dict, traffic):
+def roofline_obj(alg_bytes: float, ms: float, peaks: dict, traffic, elem_steps: float | None = None):
+    """HBM roofline of one launch: algorithmic bytes / launch time against the
+    measured copy bandwidth. For a scan, also the fraction of the ALU ceiling:
+    one exponential (MUFU ex2, 32 per clock per SM) and four FMA-pipe
+    operations (128 lanes per clock per SM) per element-step, i.e. 32
+    element-steps per clock per SM at the maximum SM clock."""
     achieved = alg_bytes / (ms * 1e-3) / 1e9
-    return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-            "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
-            "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs)" if peaks["source"] == "measured"
-            else "fallback 6400 GB/s"}
+    out = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+           "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
+           "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs)" if peaks["source"] == "measured"
+           else "fallback 6400 GB/s"}
+    if elem_steps is not None:
+        ceiling = peaks["sms"] * 32 * peaks["sm_max_mhz"] * 1e6
+        rate = elem_steps / (ms * 1e-3)
+        out["alu_ceiling"] = {"elem_steps_per_s": ceiling, "achieved": rate, "frac": round(rate / ceiling, 4),
+                              "derivation": "%d SMs x 32 element-steps/clk x %.0f MHz" % (peaks["sms"], peaks["sm_max_mhz"])}
+    return out
 
 
 # ----------------------------------------------------------------- CPU (oracle)
@@ -377,6 +391,38 @@ def reference_arm(args, rank, world):
     return 0
 
 
+def ncu_case(args):
+    """Launches of one kernel only (for ncu): ``warmup + steps`` launches of the
+    headline scan on the same inputs, or of the decode update on the first
+    ``warmup + steps`` tokens of the decode workload; no L2 flush, no other
+    kernels of this library."""
+    from selective_state_space_138_b300 import binding
+    torch.cuda.set_device(0)
+    if args.ncu_case == "decode":
+        spec = I.DECODE
+        T = args.warmup + args.steps
+        tok = {k: v.cuda() for k, v in I.make_decode_tokens(spec, steps=T).items()}
+        par = I.make_decode_params(spec)
+        A, Dp = par["A"].cuda(), par["D"].cuda()
+        state = torch.zeros(spec.batch, spec.d_inner, spec.N, device="cuda")
+        y = torch.empty_like(tok["x"])
+        for t in range(T):
+            binding.state_update(state, tok["x"][t], tok["delta"][t], A, tok["B"][t], tok["C"][t], D=Dp,
+                                 z=tok["z"][t], y=y[t])
+        torch.cuda.synchronize()
+        return 0
+    spec = HEADLINE
+    inp = I.make_scan_inputs(spec)
+    g = {k: v.cuda() for k, v in inp.items() if k != "reset_pos"}
+    y = torch.empty_like(g["x"])
+    fs = torch.empty(spec.batch, spec.d_inner, spec.N, device="cuda", dtype=torch.float32)
+    for _ in range(args.warmup + args.steps):
+        binding.scan_fwd(g["x"], g["dt"], g["A"], g["B"], g["C"], D=g["D"], z=g["z"], dt_bias=g["dt_bias"],
+                         y=y, final_state=fs)
+    torch.cuda.synchronize()
+    return 0
+
+
 # ----------------------------------------------------------------- main
 
 def main(argv=None):
@@ -387,11 +433,17 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--headline-only", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-soak", action="store_true", help="skip the 1 s untimed soak before timing")
+    ap.add_argument("--ncu-case", choices=["scan", "decode"], default=None,
+                    help="profiling case: warmup + steps launches of the headline scan (or of the decode "
+                         "update, on the first warmup + steps tokens of the decode workload), nothing else")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
 
     rank, world, local = dist_env()
+    if args.ncu_case:
+        return ncu_case(args)
     if args.impl == "reference":
         return reference_arm(args, rank, world)
 
@@ -415,7 +467,7 @@ def main(argv=None):
     barrier(world)
     torch.cuda.synchronize()
     t_wall = time.time()
-    times = time_scan(spec, args.steps, args.warmup, flush=True, soak_s=1.0)
+    times = time_scan(spec, args.steps, args.warmup, flush=True, soak_s=0.0 if args.no_soak else 1.0)
     torch.cuda.synchronize()
     barrier(world)
     wall = time.time() - t_wall
@@ -440,7 +492,7 @@ def main(argv=None):
                    "N": spec.N, "io": spec.io, "per_gpu": True, "l2": "flushed (256 MB write) before every step",
                    "parallelism": "dp%d (independent batch shards)" % world},
         "kernel_ms": {"median": statistics.median(times), "min": min(times), "max": max(times)},
-        "roofline": roofline_obj(alg, ms_per_step, peaks, traffic),
+        "roofline": roofline_obj(alg, ms_per_step, peaks, traffic, elem_steps=elems),
         "alg_bytes_per_step": alg,
         "gpu_launches": args.steps,
         "e2e": {"value": world * elems / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
@@ -456,7 +508,8 @@ def main(argv=None):
             ms = statistics.median(t)
             extras[wspec.name] = {
                 "elem_steps_per_s": wspec.elem_steps / (ms * 1e-3), "kernel_ms_median": ms,
-                "roofline": roofline_obj(scan_alg_bytes(wspec), ms, peaks, profiled_traffic("scan_fwd_" + wspec.name))}
+                "roofline": roofline_obj(scan_alg_bytes(wspec), ms, peaks, profiled_traffic("scan_fwd_" + wspec.name),
+                                         elem_steps=wspec.elem_steps)}
         t = time_scan(I.TINY, 20, 3, flush=False)
         extras[I.TINY.name] = {"elem_steps_per_s": I.TINY.elem_steps / (statistics.median(t) * 1e-3),
                                "kernel_ms_median": statistics.median(t), "note": "launch-bound; parity case"}

@@ -42,7 +42,6 @@
 namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;  // log2(e)
-constexpr float kLn2 = 0.6931471805599453f;    // ln(2)
 
 // ------------------------------------------------------------------ device math
 
@@ -53,13 +52,6 @@ __device__ __forceinline__ float ex2_approx(float x)
     return y;
 }
 
-__device__ __forceinline__ float lg2_approx(float x)
-{
-    float y;
-    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
 __device__ __forceinline__ float rcp_approx(float x)
 {
     float y;
@@ -67,20 +59,24 @@ __device__ __forceinline__ float rcp_approx(float x)
     return y;
 }
 
-// softplus(v) = log(1 + e^v) = max(v, 0) + log1p(e), e = e^{-|v|} in (0, 1].
-// log1p(e) is taken from its alternating Taylor series when e <= 1/16
-// (five terms; the first omitted term e^6/6 is below 2^-24 relative), and
-// otherwise as ln2 * log2(u) - r with u = fl(1 + e) and r = (u - 1) - e, the
-// exact rounding error of 1 + e (Sterbenz), which removes the cancellation of
-// log2(1 + e) to first order. Finite for every finite v.
+// softplus(v) = log(1 + e^v) = max(v, 0) + log1p(w), w = e^{-|v|} in (0, 1],
+// finite for every finite v. log1p(w) = w * Q(w) with Q of degree 8, fitted
+// to log1p(w)/w on [0, 1] by Lawson-reweighted least squares on Chebyshev
+// nodes (csrc/fit_log1p.py); relative error 2.3e-7 in float32 Horner
+// evaluation, i.e. at float32 rounding level.
 __device__ __forceinline__ float softplus_f(float v)
 {
-    const float e = ex2_approx(-fabsf(v) * kLog2e);
-    const float series = e * fmaf(e, fmaf(e, fmaf(e, fmaf(e, 0.2f, -0.25f), 1.0f / 3.0f), -0.5f), 1.0f);
-    const float u = 1.0f + e;
-    const float r = (u - 1.0f) - e;
-    const float viaLog = fmaf(lg2_approx(u), kLn2, -r);
-    return fmaxf(v, 0.0f) + (e <= 0.0625f ? series : viaLog);
+    const float w = ex2_approx(-fabsf(v) * kLog2e);
+    float q = 5.232624244e-03f;
+    q = fmaf(q, w, -2.950495668e-02f);
+    q = fmaf(q, w, 7.822549343e-02f);
+    q = fmaf(q, w, -1.366320699e-01f);
+    q = fmaf(q, w, 1.910598874e-01f);
+    q = fmaf(q, w, -2.484297752e-01f);
+    q = fmaf(q, w, 3.331909478e-01f);
+    q = fmaf(q, w, -4.999949336e-01f);
+    q = fmaf(q, w, 9.999999404e-01f);
+    return fmaf(w, q, fmaxf(v, 0.0f));
 }
 
 // z * sigmoid(z) = z / (1 + e^{-z}); e^{-z} = inf for very negative z gives 0.
@@ -345,6 +341,559 @@ scan_fwd_kernel(const ScanParams p)
     }
 }
 
+// ------------------------------------------------------------------ 16-byte pieces
+
+// kPerVec consecutive elements of `row` starting at step t, as raw 16 bytes;
+// steps at or past L read as 0.
+template <typename T>
+__device__ __forceinline__ uint4 load_piece(const T *row, int64_t t, int64_t L, bool vec)
+{
+    constexpr int V = Io<T>::kPerVec;
+    if (vec && t + V <= L)
+        return __ldg(reinterpret_cast<const uint4 *>(row + t));
+    float v[V];
+#pragma unroll
+    for (int i = 0; i < V; ++i)
+        v[i] = (t + i < L) ? Io<T>::load1(row + t + i) : 0.0f;
+    uint4 o;
+    if constexpr (V == 4) {
+        o.x = __float_as_uint(v[0]); o.y = __float_as_uint(v[1]);
+        o.z = __float_as_uint(v[2]); o.w = __float_as_uint(v[3]);
+    } else {
+        o.x = pack_bf16x2(v[0], v[1]); o.y = pack_bf16x2(v[2], v[3]);
+        o.z = pack_bf16x2(v[4], v[5]); o.w = pack_bf16x2(v[6], v[7]);
+    }
+    return o;
+}
+
+template <typename T>
+__device__ __forceinline__ void unpack_piece(const uint4 &w, float *out)
+{
+    if constexpr (Io<T>::kPerVec == 4) {
+        out[0] = __uint_as_float(w.x); out[1] = __uint_as_float(w.y);
+        out[2] = __uint_as_float(w.z); out[3] = __uint_as_float(w.w);
+    } else {
+        out[0] = bf16lo(w.x); out[1] = bf16hi(w.x);
+        out[2] = bf16lo(w.y); out[3] = bf16hi(w.y);
+        out[4] = bf16lo(w.z); out[5] = bf16hi(w.z);
+        out[6] = bf16lo(w.w); out[7] = bf16hi(w.w);
+    }
+}
+
+// ------------------------------------------------------------------ packed pairs
+//
+// A pair of fp32 values lives in one 64-bit register (low word first), the
+// operand form of the sm_100+ f32x2 instructions.
+
+typedef unsigned long long u64;
+
+__device__ __forceinline__ u64 pk(float a, float b)
+{
+    u64 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+
+__device__ __forceinline__ void upk(u64 v, float &a, float &b)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+
+__device__ __forceinline__ u64 mul2(u64 a, u64 b)
+{
+    u64 d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+__device__ __forceinline__ u64 add2(u64 a, u64 b)
+{
+    u64 d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+__device__ __forceinline__ u64 fma2(u64 a, u64 b, u64 c)
+{
+    u64 d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+// 2^v elementwise
+__device__ __forceinline__ u64 ex2_2(u64 v)
+{
+    u64 d;
+    asm("{ .reg .f32 a, b;\n\t"
+        "mov.b64 {a, b}, %1;\n\t"
+        "ex2.approx.ftz.f32 a, a;\n\t"
+        "ex2.approx.ftz.f32 b, b;\n\t"
+        "mov.b64 %0, {a, b}; }"
+        : "=l"(d) : "l"(v));
+    return d;
+}
+
+// 1/v elementwise
+__device__ __forceinline__ u64 rcp_2(u64 v)
+{
+    u64 d;
+    asm("{ .reg .f32 a, b;\n\t"
+        "mov.b64 {a, b}, %1;\n\t"
+        "rcp.approx.ftz.f32 a, a;\n\t"
+        "rcp.approx.ftz.f32 b, b;\n\t"
+        "mov.b64 %0, {a, b}; }"
+        : "=l"(d) : "l"(v));
+    return d;
+}
+
+__device__ __forceinline__ u64 splat(float a) { return pk(a, a); }
+
+__device__ __forceinline__ float hsum(u64 v)
+{
+    float a, b;
+    upk(v, a, b);
+    return a + b;
+}
+
+// softplus of a pair: max(v, 0) + w Q(w), w = e^{-|v|} (see softplus_f)
+__device__ __forceinline__ u64 softplus2(u64 v)
+{
+    float v0, v1;
+    upk(v, v0, v1);
+    const u64 w = ex2_2(pk(-fabsf(v0) * kLog2e, -fabsf(v1) * kLog2e));
+    u64 q = splat(5.232624244e-03f);
+    q = fma2(q, w, splat(-2.950495668e-02f));
+    q = fma2(q, w, splat(7.822549343e-02f));
+    q = fma2(q, w, splat(-1.366320699e-01f));
+    q = fma2(q, w, splat(1.910598874e-01f));
+    q = fma2(q, w, splat(-2.484297752e-01f));
+    q = fma2(q, w, splat(3.331909478e-01f));
+    q = fma2(q, w, splat(-4.999949336e-01f));
+    q = fma2(q, w, splat(9.999999404e-01f));
+    return fma2(w, q, pk(fmaxf(v0, 0.0f), fmaxf(v1, 0.0f)));
+}
+
+// z sigmoid(z) of a pair
+__device__ __forceinline__ u64 silu2(u64 z)
+{
+    const u64 e = ex2_2(mul2(z, splat(-kLog2e)));
+    return mul2(z, rcp_2(add2(e, splat(1.0f))));
+}
+
+// ------------------------------------------------------------------ n-split scan kernel
+//
+// A CTA owns batch row b and CH = 32 channels, with S warps (S = ceil(N/4),
+// N padded to 4S with A = B = C = 0, which leaves the padded states at zero):
+// warp q holds states 4q..4q+3 of all 32 channels, lane c holding channel c.
+// Every lane walks the whole sequence one step after another, so each
+// element-step costs one exponential and four fp32 multiply(-add)s, done in
+// pairs with the packed f32x2 instructions; time is not split, so no combine
+// work is added.
+//
+// Shared-memory traffic sets the pace on this part (a 16-byte load by 32
+// lanes takes four shared-memory cycles), so the layout keeps it low: B_t and
+// C_t of a warp's states are the same for all its lanes (a warp-uniform load
+// costs half of a scattered one), the per-step pair (delta, delta*x) is 8
+// bytes, and the raw tiles are read with conflict-free 16-byte loads.
+//
+// The sequence is cut into chunks of LC = 32 steps. Per chunk k:
+//   scan      lane c of warp q advances its 4 states over the chunk (decays of
+//             the next AHEAD steps formed ahead of the state update) and
+//             keeps its partial readouts sum over its states of C_t[n] h_t[n]
+//             in registers, storing them when the chunk is done;
+//   -- barrier --
+//   epilogue  thread (c, r) adds the S partials of its RL = LC / S steps,
+//             adds D x, applies the silu(z) gate and stores y;
+//   prep      the same thread forms delta = softplus(dt + bias) (or dt + bias)
+//             and delta*x for its steps of chunk k+1, and B, C of chunk k+1
+//             are converted to fp32 [t][n];
+//   -- barrier --
+// The raw x, dt, z, B, C tiles of every chunk are copied into a ring of
+// STAGES chunks with cp.async (16-byte pieces, zero fill past the ends) three
+// chunks ahead of their use, so DRAM latency hides behind three iterations.
+// The per-step work (softplus, gate, conversions) is done once per (channel,
+// step), two steps at a time with f32x2 arithmetic.
+
+#ifndef SS_NSPLIT_AHEAD
+#define SS_NSPLIT_AHEAD 4  // steps whose decays are formed ahead of the state update
+#endif
+#define SS_NSPLIT_STAGES 4  // raw chunks resident in shared memory: k .. k+3
+
+template <typename T, int S>
+struct NSplitShape {
+    static constexpr int CH = 32;                 // channels per CTA
+    static constexpr int NT = CH * S;             // threads per CTA
+    static constexpr int NS = 4 * S;              // padded states
+    static constexpr int LC = 32;                 // steps per chunk
+    static constexpr int RL = LC / S;             // steps per epilogue/prep thread
+    static constexpr int STAGES = SS_NSPLIT_STAGES;
+    static constexpr int EPP = 16 / (int)sizeof(T);        // elements per 16-byte piece
+    static constexpr int PR = LC / EPP;                    // pieces per raw row
+    static constexpr int ROWB = LC * (int)sizeof(T) + 16;  // raw x/dt/z row stride, padded
+    static constexpr int RAW_X = CH * ROWB;                // one raw x, dt or z tile
+    static constexpr int RAW_BC = NS * LC * (int)sizeof(T);  // one raw B or C tile
+    static constexpr int STAGE_BYTES = 3 * RAW_X + 2 * RAW_BC;
+    static constexpr int NPIECE = (3 * CH + 2 * NS) * PR;
+    static constexpr int PPT = (NPIECE + NT - 1) / NT;    // raw pieces per thread
+    static constexpr int YROW = LC + 4;           // floats per partial row (conflict-free)
+    static constexpr int YQ = CH * YROW;          // floats per state group
+    static constexpr int PD_BYTES = LC * CH * 8;
+    static constexpr int BC_BYTES = LC * NS * 4;
+    static constexpr int Y_BYTES = S * YQ * 4;
+    static constexpr size_t BYTES = (size_t)STAGES * STAGE_BYTES + PD_BYTES + 2 * BC_BYTES + Y_BYTES;
+    static_assert(RL % 2 == 0, "steps are processed in pairs");
+};
+
+__device__ __forceinline__ void cp_async16(uint32_t smem_dst, const void *gsrc, int src_bytes)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(smem_dst), "l"(gsrc), "r"(src_bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+
+template <int PENDING>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(PENDING) : "memory"); }
+
+// element pair i, i+1 of a raw shared-memory row (i even)
+template <typename T>
+__device__ __forceinline__ u64 raw_pair(const unsigned char *row, int i)
+{
+    if constexpr (sizeof(T) == 4) {
+        return *reinterpret_cast<const u64 *>(row + 4 * i);
+    } else {
+        const uint32_t x = *reinterpret_cast<const uint32_t *>(row + 2 * i);
+        return pk(bf16lo(x), bf16hi(x));
+    }
+}
+
+template <typename T, int RL>
+__device__ __forceinline__ void write_run(T *row, int64_t t, int64_t L, bool vec, const float *v)
+{
+    if constexpr ((RL * sizeof(T)) % 16 == 0) {
+        if (vec && t + RL <= L) {
+#pragma unroll
+            for (int e = 0; e < RL; e += Io<T>::kPerVec)
+                Io<T>::storevec(row + t + e, v + e);
+            return;
+        }
+    } else if constexpr (RL * sizeof(T) == 8 && sizeof(T) == 2) {
+        if (vec && t + RL <= L) {
+            *reinterpret_cast<uint2 *>(row + t) = make_uint2(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]));
+            return;
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < RL; ++i)
+        if (t + i < L)
+            Io<T>::store1(row + t + i, v[i]);
+}
+
+// RL raw elements of a shared-memory row starting at element offset off, as
+// 32-bit words, with the widest aligned loads
+template <typename T, int RL>
+__device__ __forceinline__ void read_run_raw(const unsigned char *row, int off, uint32_t *w)
+{
+    constexpr int BYTES = RL * (int)sizeof(T);
+    const unsigned char *s = row + off * (int)sizeof(T);
+    if constexpr (BYTES % 16 == 0) {
+#pragma unroll
+        for (int v = 0; v < BYTES / 16; ++v) {
+            const uint4 x = *reinterpret_cast<const uint4 *>(s + 16 * v);
+            w[4 * v] = x.x; w[4 * v + 1] = x.y; w[4 * v + 2] = x.z; w[4 * v + 3] = x.w;
+        }
+    } else if constexpr (BYTES % 8 == 0) {
+#pragma unroll
+        for (int v = 0; v < BYTES / 8; ++v) {
+            const uint2 x = *reinterpret_cast<const uint2 *>(s + 8 * v);
+            w[2 * v] = x.x; w[2 * v + 1] = x.y;
+        }
+    } else {
+#pragma unroll
+        for (int v = 0; v < BYTES / 4; ++v)
+            w[v] = *reinterpret_cast<const uint32_t *>(s + 4 * v);
+    }
+}
+
+// element pair i, i+1 (i even) of a run read by read_run_raw
+template <typename T>
+__device__ __forceinline__ u64 word_pair(const uint32_t *w, int i)
+{
+    if constexpr (sizeof(T) == 4)
+        return pk(__uint_as_float(w[i]), __uint_as_float(w[i + 1]));
+    else
+        return pk(bf16lo(w[i / 2]), bf16hi(w[i / 2]));
+}
+
+template <typename T, int S>
+__global__ void __launch_bounds__(NSplitShape<T, S>::NT, NSplitShape<T, S>::NT <= 128 ? 3 : 1)
+scan_nsplit_kernel(const ScanParams p)
+{
+    using SH = NSplitShape<T, S>;
+    constexpr int NT = SH::NT, CH = SH::CH, NS = SH::NS, LC = SH::LC, RL = SH::RL, PR = SH::PR;
+    constexpr int STAGES = SH::STAGES, EPP = SH::EPP, PPT = SH::PPT;
+    constexpr int D = SS_NSPLIT_AHEAD;
+    constexpr int RW = RL * (int)sizeof(T) / 4;   // 32-bit words per prep/epilogue run
+    static_assert(LC % 4 == 0 && D >= 1 && D <= LC, "chunk shape");
+
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    unsigned char *raw = smem_raw;                                          // [STAGES][x, dt, z, B, C]
+    u64 *Pd = reinterpret_cast<u64 *>(smem_raw + STAGES * SH::STAGE_BYTES);  // [LC][CH] (delta, delta x)
+    float *Bf = reinterpret_cast<float *>(Pd + LC * CH);                    // [LC][NS]
+    float *Cf = Bf + LC * NS;                                               // [LC][NS]
+    float *Yp = Cf + LC * NS;                                               // [S][CH][YROW]
+    const uint32_t raw_s = static_cast<uint32_t>(__cvta_generic_to_shared(raw));
+
+    const int tid = threadIdx.x;
+    const int64_t b = blockIdx.y;
+    const int64_t d0 = static_cast<int64_t>(blockIdx.x) * CH;
+    const int64_t L = p.L, N = p.N, Dn = p.d_inner;
+    const bool vec = p.vec != 0;
+
+    // scan role: channel cs = lane, state group q = warp
+    const int cs = tid % CH;
+    const int q = tid / CH;
+    const bool act_s = d0 + cs < Dn;
+    const int64_t ds = act_s ? d0 + cs : 0;
+    // epilogue/prep role: channel ce, run re (steps re*RL .. re*RL+RL-1 of a chunk)
+    const int ce = tid % CH;
+    const int re = tid / CH;
+    const bool act_e = d0 + ce < Dn;
+    const int64_t de = act_e ? d0 + ce : 0;
+    T *yr = static_cast<T *>(p.y) + (b * Dn + de) * L;
+
+    const u64 bias2 = splat((p.dt_bias && act_e) ? __ldg(p.dt_bias + de) : 0.0f);
+    const u64 D2 = splat((p.D && act_e) ? __ldg(p.D + de) : 0.0f);
+    const bool gate = p.z != nullptr;
+
+    float A2[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const int n = 4 * q + e;
+        A2[e] = (n < N) ? __ldg(p.A + ds * N + n) * kLog2e : 0.0f;
+    }
+    const u64 A01 = pk(A2[0], A2[1]);
+    const u64 A23 = pk(A2[2], A2[3]);
+    u64 h01 = 0, h23 = 0;   // +0.0f in both halves
+
+    // the raw pieces this thread copies: source row pointer, element offset
+    // within the chunk, shared-memory offset within a stage; rows past d_inner
+    // or N (and a missing z) copy nothing
+    const T *src[PPT];
+    uint32_t soff[PPT];
+    int poff[PPT];
+#pragma unroll
+    for (int u = 0; u < PPT; ++u) {
+        const int pi = tid + u * NT;
+        int r, pc;
+        const T *base;
+        uint32_t off;
+        bool ok = pi < SH::NPIECE;
+        if (pi < 3 * CH * PR) {
+            const int tensor = pi / (CH * PR);
+            r = (pi % (CH * PR)) / PR;
+            pc = pi % PR;
+            const T *g = static_cast<const T *>(tensor == 0 ? p.x : (tensor == 1 ? p.dt : p.z));
+            ok = ok && d0 + r < Dn && g != nullptr;
+            base = ok ? g + (b * Dn + d0 + r) * L : static_cast<const T *>(p.x);
+            off = tensor * SH::RAW_X + r * SH::ROWB;
+        } else {
+            const int v = pi - 3 * CH * PR;
+            const int m = v / (NS * PR);
+            r = (v % (NS * PR)) / PR;
+            pc = v % PR;
+            ok = ok && r < N;
+            base = static_cast<const T *>(m == 0 ? p.B : p.C) + (b * N + (ok ? r : 0)) * L;
+            off = 3 * SH::RAW_X + m * SH::RAW_BC + r * LC * (int)sizeof(T);
+        }
+        src[u] = base;
+        soff[u] = off + pc * 16;
+        poff[u] = ok ? pc * EPP : (1 << 30);   // a piece that does not exist is always past the end
+    }
+
+    // copy the raw pieces of chunk j into stage j % STAGES (steps past L and
+    // rows that do not exist are zero)
+    auto stage_in = [&](int64_t j) {
+        const uint32_t st = raw_s + static_cast<uint32_t>((j % STAGES) * SH::STAGE_BYTES);
+        const int64_t t1 = j * LC;
+        const int rem = static_cast<int>(L - t1 < (1 << 29) ? L - t1 : (1 << 29));   // steps left from t1
+#pragma unroll
+        for (int u = 0; u < PPT; ++u) {
+            if (tid + u * NT >= SH::NPIECE)
+                break;
+            const int left = rem - poff[u];
+            const int nb = left >= EPP ? 16 : (left > 0 ? left * (int)sizeof(T) : 0);
+            const T *g = src[u] + (nb > 0 ? t1 + poff[u] : 0);
+            if (vec) {
+                cp_async16(st + soff[u], g, nb);
+            } else {
+                unsigned char *dst = raw + (j % STAGES) * SH::STAGE_BYTES + soff[u];
+                const int ne = nb / (int)sizeof(T);
+#pragma unroll
+                for (int e = 0; e < EPP; ++e) {
+                    if constexpr (sizeof(T) == 4)
+                        reinterpret_cast<float *>(dst)[e] = e < ne ? g[e] : 0.0f;
+                    else
+                        reinterpret_cast<unsigned short *>(dst)[e] =
+                            e < ne ? reinterpret_cast<const unsigned short *>(g)[e] : (unsigned short)0;
+                }
+            }
+        }
+        cp_async_commit();
+    };
+
+    // raw B, C of chunk j -> fp32 [t][n]: each item is (tensor, step t,
+    // states 4g..4g+3), written as one 16-byte word
+    auto convert_bc = [&](int64_t j) {
+        const unsigned char *st = raw + (j % STAGES) * SH::STAGE_BYTES + 3 * SH::RAW_X;
+        for (int w = tid; w < 2 * LC * S; w += NT) {
+            const int m = w / (LC * S);
+            const int t = (w % (LC * S)) / S;
+            const int g = w % S;
+            const T *srcm = reinterpret_cast<const T *>(st + m * SH::RAW_BC);
+            float v[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                if constexpr (sizeof(T) == 4)
+                    v[e] = srcm[(4 * g + e) * LC + t];
+                else
+                    v[e] = __uint_as_float(static_cast<uint32_t>(
+                                               reinterpret_cast<const unsigned short *>(srcm)[(4 * g + e) * LC + t])
+                                           << 16);
+            }
+            *reinterpret_cast<float4 *>((m == 0 ? Bf : Cf) + t * NS + 4 * g) = make_float4(v[0], v[1], v[2], v[3]);
+        }
+    };
+
+    // delta and delta*x of this thread's steps of chunk j
+    auto prep = [&](int64_t j) {
+        const unsigned char *st = raw + (j % STAGES) * SH::STAGE_BYTES;
+        uint32_t xw[RW], dw[RW];
+        read_run_raw<T, RL>(st + ce * SH::ROWB, re * RL, xw);
+        read_run_raw<T, RL>(st + SH::RAW_X + ce * SH::ROWB, re * RL, dw);
+        const int64_t left64 = L - (j * LC + re * RL);
+        const int lim = act_e ? static_cast<int>(left64 < RL ? left64 : RL) : 0;
+#pragma unroll
+        for (int i = 0; i < RL; i += 2) {
+            const u64 xx = word_pair<T>(xw, i);
+            const u64 u = add2(word_pair<T>(dw, i), bias2);
+            const u64 s2 = p.softplus ? softplus2(u) : u;
+            float s0, s1;
+            upk(s2, s0, s1);
+            s0 = i < lim ? s0 : 0.0f;
+            s1 = i + 1 < lim ? s1 : 0.0f;
+            float sx0, sx1;
+            upk(mul2(pk(s0, s1), xx), sx0, sx1);
+            Pd[(re * RL + i) * CH + ce] = pk(s0, sx0);
+            Pd[(re * RL + i + 1) * CH + ce] = pk(s1, sx1);
+        }
+    };
+
+    const int64_t nchunks = (L + LC - 1) / LC;
+#pragma unroll
+    for (int s = 0; s < STAGES - 1; ++s)
+        if (s < nchunks)
+            stage_in(s);
+        else
+            cp_async_commit();
+    cp_async_wait<STAGES - 2>();
+    __syncthreads();
+    prep(0);
+    convert_bc(0);
+    __syncthreads();
+
+    float *yq_s = Yp + q * SH::YQ + cs * SH::YROW;   // this lane's partial readouts
+    const float *Bq_s = Bf + 4 * q;                   // this warp's states of B_t, C_t
+    const float *Cq_s = Cf + 4 * q;
+    for (int64_t k = 0; k < nchunks; ++k) {
+        const int64_t t0 = k * LC;
+        if (k + STAGES - 1 < nchunks)
+            stage_in(k + STAGES - 1);
+        else
+            cp_async_commit();
+
+        // ---- scan: 4 states of channel cs over the chunk; the decays and
+        // writes of step t + D are formed while the state takes step t
+        {
+            u64 ra01[D], ra23[D], rb01[D], rb23[D];
+            float yv[LC];
+            auto form = [&](int t, int slot) {
+                float dl, dx;
+                upk(Pd[t * CH + cs], dl, dx);
+                const ulonglong2 Bq = *reinterpret_cast<const ulonglong2 *>(Bq_s + t * NS);
+                const u64 dd = splat(dl);
+                const u64 xx = splat(dx);
+                ra01[slot] = ex2_2(mul2(dd, A01));
+                ra23[slot] = ex2_2(mul2(dd, A23));
+                rb01[slot] = mul2(xx, Bq.x);
+                rb23[slot] = mul2(xx, Bq.y);
+            };
+#pragma unroll
+            for (int i = 0; i < D; ++i)
+                form(i, i);
+#pragma unroll
+            for (int t = 0; t < LC; ++t) {
+                const int slot = t % D;
+                const u64 a01 = ra01[slot], a23 = ra23[slot], b01 = rb01[slot], b23 = rb23[slot];
+                if (t + D < LC)
+                    form(t + D, slot);
+                const ulonglong2 Cq = *reinterpret_cast<const ulonglong2 *>(Cq_s + t * NS);
+                h01 = fma2(a01, h01, b01);
+                h23 = fma2(a23, h23, b23);
+                yv[t] = hsum(fma2(Cq.y, h23, mul2(Cq.x, h01)));
+            }
+#pragma unroll
+            for (int t = 0; t < LC; t += 4)
+                *reinterpret_cast<float4 *>(yq_s + t) = make_float4(yv[t], yv[t + 1], yv[t + 2], yv[t + 3]);
+        }
+        cp_async_wait<STAGES - 2>();   // chunk k+1 has landed (this thread's copies)
+        __syncthreads();
+
+        // ---- epilogue of chunk k: sum partials, skip term, gate, store
+        {
+            const unsigned char *st = raw + (k % STAGES) * SH::STAGE_BYTES;
+            uint32_t xw[RW], zw[RW];
+            read_run_raw<T, RL>(st + ce * SH::ROWB, re * RL, xw);
+            if (gate)
+                read_run_raw<T, RL>(st + 2 * SH::RAW_X + ce * SH::ROWB, re * RL, zw);
+            float out[RL];
+#pragma unroll
+            for (int i = 0; i < RL; i += 2) {
+                const float *yp = Yp + ce * SH::YROW + re * RL + i;
+                u64 acc = *reinterpret_cast<const u64 *>(yp);
+#pragma unroll
+                for (int qq = 1; qq < S; ++qq)
+                    acc = add2(acc, *reinterpret_cast<const u64 *>(yp + qq * SH::YQ));
+                acc = fma2(D2, word_pair<T>(xw, i), acc);
+                if (gate)
+                    acc = mul2(acc, silu2(word_pair<T>(zw, i)));
+                upk(acc, out[i], out[i + 1]);
+            }
+            if (act_e)
+                write_run<T, RL>(yr, t0 + re * RL, L, vec, out);
+        }
+
+        // ---- prep of chunk k+1
+        if (k + 1 < nchunks) {
+            prep(k + 1);
+            convert_bc(k + 1);
+        }
+        __syncthreads();
+    }
+    cp_async_wait<0>();
+
+    if (p.final_state && act_s) {
+        float *fs = p.final_state + (b * Dn + ds) * N;
+        float hv[4];
+        upk(h01, hv[0], hv[1]);
+        upk(h23, hv[2], hv[3]);
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            if (4 * q + e < N)
+                fs[4 * q + e] = hv[e];
+    }
+}
+
 // ------------------------------------------------------------------ decode kernel
 
 struct UpdateParams {
@@ -566,6 +1115,58 @@ ss_status dispatch_scan_lanes(const ScanParams &p, int lanes, cudaStream_t s)
     }
 }
 
+template <typename T, int S>
+ss_status launch_nsplit(const ScanParams &p, cudaStream_t stream)
+{
+    using SH = NSplitShape<T, S>;
+    const size_t smem = SH::BYTES;
+    if (smem > 48u * 1024u) {
+        cudaError_t e = cudaFuncSetAttribute(scan_nsplit_kernel<T, S>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem));
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return fail(SS_ERR_LAUNCH, "cudaFuncSetAttribute failed: %s", cudaGetErrorString(e));
+        }
+    }
+    const int64_t gx = (p.d_inner + SH::CH - 1) / SH::CH;
+    if (gx > 0x7fffffff || p.batch > 65535)
+        return fail(SS_ERR_DIM, "grid too large: %lld channel blocks x %lld batch rows",
+                    (long long)gx, (long long)p.batch);
+    dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(p.batch));
+    scan_nsplit_kernel<T, S><<<grid, SH::NT, smem, stream>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return fail(SS_ERR_LAUNCH, "scan kernel launch failed: %s", cudaGetErrorString(e));
+    return SS_OK;
+}
+
+template <typename T>
+ss_status dispatch_nsplit(const ScanParams &p, cudaStream_t s)
+{
+    if (p.N <= 4) return launch_nsplit<T, 1>(p, s);
+    if (p.N <= 8) return launch_nsplit<T, 2>(p, s);
+    if (p.N <= 16) return launch_nsplit<T, 4>(p, s);
+    return launch_nsplit<T, 8>(p, s);
+}
+
+// n-split (N <= 32) when channels x state groups fill every SM with at least
+// two warps per scheduler; otherwise time lanes.
+bool use_nsplit(int64_t channels, int64_t N, int sms)
+{
+    if (N > 32)
+        return false;
+    const char *env = getenv("SS_SCAN_KERNEL");
+    if (env && strcmp(env, "nsplit") == 0)
+        return true;
+    if (env && strcmp(env, "lanes") == 0)
+        return false;
+    int64_t s = 1;
+    while (4 * s < N)
+        s *= 2;
+    return channels * s >= static_cast<int64_t>(sms) * 256;
+}
+
 template <typename T>
 ss_status scan_fwd(const void *x, const void *dt, const float *A, const void *B, const void *C,
                    const float *D, const void *z, const float *dt_bias, int softplus, void *y,
@@ -597,6 +1198,8 @@ ss_status scan_fwd(const void *x, const void *dt, const float *A, const void *B,
     p.softplus = softplus ? 1 : 0;
     p.vec = (L % 16 == 0) && aligned16(x) && aligned16(dt) && aligned16(y) && (!z || aligned16(z));
 
+    if (use_nsplit(batch * d_inner, N, sm_count(dev)))
+        return dispatch_nsplit<T>(p, stream);
     const int lanes = pick_lanes(batch * d_inner, L, sm_count(dev));
     if (N <= 4)
         return dispatch_scan_lanes<T, 4>(p, lanes, stream);

@@ -19,11 +19,16 @@ from tests.gpu_util import TOL, assert_close, dev, gpu_scan, oracle_scan
 
 pytestmark = pytest.mark.gpu
 
-LANES = ["1", "4", "16"]
+# kernel variants: the n-split kernel, and the time-lane kernel with 1, 4, 16 lanes
+LANES = ["nsplit", "1", "4", "16"]
 
 
 @pytest.fixture
 def lanes(request, monkeypatch):
+    if request.param == "nsplit":
+        monkeypatch.setenv("SS_SCAN_KERNEL", "nsplit")
+        return 0
+    monkeypatch.setenv("SS_SCAN_KERNEL", "lanes")
     monkeypatch.setenv("SS_SCAN_LANES", request.param)
     return int(request.param)
 
@@ -62,7 +67,7 @@ OPTIONAL = [dict(use_D=False), dict(use_z=False), dict(use_bias=False), dict(sof
             dict(use_D=False, use_z=False, use_bias=False, softplus=False), dict(final_state=False)]
 
 
-@pytest.mark.parametrize("lanes", ["1", "16"], indirect=True)
+@pytest.mark.parametrize("lanes", ["nsplit", "1", "16"], indirect=True)
 @pytest.mark.parametrize("opt", OPTIONAL, ids=lambda o: "_".join("%s=%s" % kv for kv in o.items()))
 @pytest.mark.parametrize("io", ["bf16", "f32"])
 def test_optional_pointers_and_flag(opt, io, lanes):
@@ -83,7 +88,8 @@ def test_optional_pointers_and_flag(opt, io, lanes):
 
 
 @pytest.mark.parametrize("io", ["bf16", "f32"])
-def test_unaligned_pointers_take_the_scalar_path(io):
+@pytest.mark.parametrize("lanes", ["nsplit", "16"], indirect=True)
+def test_unaligned_pointers_take_the_scalar_path(io, lanes):
     inp = I.make_scan_inputs(I.ScanSpec(batch=2, d_inner=10, L=48, N=16, io=io, seed=8))
     g = dev(inp)
     shifted = {}
@@ -100,7 +106,8 @@ def test_unaligned_pointers_take_the_scalar_path(io):
     assert_close(fs.cpu().numpy(), fr, inp["x"].dtype, "final_state")
 
 
-def test_extreme_steps_stay_finite():
+@pytest.mark.parametrize("lanes", ["nsplit", "1"], indirect=True)
+def test_extreme_steps_stay_finite(lanes):
     """Very large and very negative raw steps (softplus saturating both ways)."""
     inp = I.make_scan_inputs(I.ScanSpec(batch=1, d_inner=16, L=64, N=16, io="f32", seed=9))
     inp["dt"][0, :4, ::7] = 60.0
@@ -235,3 +242,47 @@ def test_full_size_decode_on_sampled_rows():
     got = ys.view(spec.steps, -1)[:, rows].float().cpu().numpy().T
     assert_close(got, yr, torch.bfloat16, "decode y (every step)")
     assert_close(st.view(-1, spec.N)[rows].cpu().numpy(), fr, torch.bfloat16, "decode state")
+
+
+# ----------------------------------------------------------------- device math probes
+
+@pytest.mark.parametrize("lanes", ["nsplit", "1"], indirect=True)
+def test_step_softplus_through_the_abi(lanes):
+    """With L = 1, A = 0, B = C = x = 1 and no skip or gate, y = softplus(dt + bias)."""
+    v = np.concatenate([np.linspace(-30, 30, 4001), [-1000.0, -88.0, -20.0, 0.0, 20.0, 88.0, 1000.0]])
+    d = v.size
+    bias = np.float32(0.37)
+    dt = torch.tensor(v - bias, dtype=torch.float32).view(1, d, 1)
+    ones = torch.ones(1, 1, 1, device="cuda")
+    y, _ = binding.scan_fwd(torch.ones(1, d, 1, device="cuda"), dt.cuda(), torch.zeros(d, 1, device="cuda"),
+                            ones, ones, dt_bias=torch.full((d,), float(bias), device="cuda"),
+                            return_final_state=False)
+    got = y.view(-1).cpu().double().numpy()
+    arg = dt.view(-1).double().numpy() + np.float64(bias)
+    ref = np.array([O.softplus(a) for a in arg])
+    # float32 rounding of the exponent argument v*log2(e) costs up to about
+    # |v| * 6e-8 relative; results below the float32 normal range flush to zero
+    err = np.abs(got - ref)
+    tol = (2e-6 + 1e-7 * np.abs(arg)) * ref
+    ok = (err <= tol) | ((ref < 1.18e-38) & (err <= 1.18e-38))
+    assert np.all(np.isfinite(got))
+    assert ok.all(), (arg[~ok][:5], got[~ok][:5], ref[~ok][:5])
+
+
+@pytest.mark.parametrize("lanes", ["nsplit", "1"], indirect=True)
+def test_gate_silu_through_the_abi(lanes):
+    """With L = 1, B = C = 0, D = 1, x = 1, y = silu(z) = z sigmoid(z)."""
+    zv = np.concatenate([np.linspace(-40, 40, 4001), [-200.0, -88.0, 88.0, 200.0]])
+    d = zv.size
+    z = torch.tensor(zv, dtype=torch.float32).view(1, d, 1)
+    zeros = torch.zeros(1, 1, 1, device="cuda")
+    y, _ = binding.scan_fwd(torch.ones(1, d, 1, device="cuda"), torch.zeros(1, d, 1, device="cuda"),
+                            torch.zeros(d, 1, device="cuda"), zeros, zeros, D=torch.ones(d, device="cuda"),
+                            z=z.cuda(), delta_softplus=False, return_final_state=False)
+    got = y.view(-1).cpu().double().numpy()
+    zz = z.view(-1).double().numpy()
+    ref = zz / (1.0 + np.exp(-zz))
+    err = np.abs(got - ref)
+    tol = (2e-6 + 1e-7 * np.abs(zz)) * np.abs(ref) + 1e-30
+    assert np.all(np.isfinite(got))
+    assert np.all(err <= tol), (zz[err > tol][:5], got[err > tol][:5], ref[err > tol][:5])
