@@ -28,6 +28,7 @@
 
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <cooperative_groups.h>
 
 #include <stdarg.h>
 #include <stdint.h>
@@ -38,6 +39,8 @@
 #include <atomic>
 
 #include "ss_scan.h"
+
+namespace cg = cooperative_groups;
 
 namespace {
 
@@ -179,7 +182,9 @@ struct ScanParams {
     float *final_state;
     int64_t batch, d_inner, L, N;
     int softplus;
-    int vec;  // 16-byte vector loads/stores allowed
+    int vec;          // 16-byte vector loads/stores allowed
+    int nseg;         // segments per channel group (a thread-block cluster when > 1)
+    int64_t seg_len;  // steps per segment, a multiple of the chunk length
 };
 
 constexpr int kBlock = 128;
@@ -540,7 +545,8 @@ struct NSplitShape {
     static constexpr int PD_BYTES = LC * CH * 8;
     static constexpr int BC_BYTES = LC * NS * 4;
     static constexpr int Y_BYTES = S * YQ * 4;
-    static constexpr size_t BYTES = (size_t)STAGES * STAGE_BYTES + PD_BYTES + 2 * BC_BYTES + Y_BYTES;
+    static constexpr int X_BYTES = S * CH * 16 + S * CH * 4;   // segment end states and step sums
+    static constexpr size_t BYTES = (size_t)STAGES * STAGE_BYTES + PD_BYTES + 2 * BC_BYTES + Y_BYTES + X_BYTES;
     static_assert(RL % 2 == 0, "steps are processed in pairs");
 };
 
@@ -625,6 +631,8 @@ __device__ __forceinline__ u64 word_pair(const uint32_t *w, int i)
         return pk(bf16lo(w[i / 2]), bf16hi(w[i / 2]));
 }
 
+template <bool V> struct Flag { static constexpr bool value = V; };
+
 template <typename T, int S>
 __global__ void __launch_bounds__(NSplitShape<T, S>::NT, NSplitShape<T, S>::NT <= 128 ? 3 : 1)
 scan_nsplit_kernel(const ScanParams p)
@@ -642,12 +650,18 @@ scan_nsplit_kernel(const ScanParams p)
     float *Bf = reinterpret_cast<float *>(Pd + LC * CH);                    // [LC][NS]
     float *Cf = Bf + LC * NS;                                               // [LC][NS]
     float *Yp = Cf + LC * NS;                                               // [S][CH][YROW]
+    float4 *Hx = reinterpret_cast<float4 *>(Yp + S * SH::YQ);               // [S][CH] segment end states
+    float *Sx = reinterpret_cast<float *>(Hx + S * CH);                     // [S][CH] step sums
     const uint32_t raw_s = static_cast<uint32_t>(__cvta_generic_to_shared(raw));
 
     const int tid = threadIdx.x;
+    const int nseg = p.nseg;
+    const int seg = static_cast<int>(blockIdx.x % nseg);
     const int64_t b = blockIdx.y;
-    const int64_t d0 = static_cast<int64_t>(blockIdx.x) * CH;
+    const int64_t d0 = static_cast<int64_t>(blockIdx.x / nseg) * CH;
     const int64_t L = p.L, N = p.N, Dn = p.d_inner;
+    const int64_t t_lo = seg * p.seg_len;
+    const int64_t t_hi = (t_lo + p.seg_len < L) ? t_lo + p.seg_len : L;
     const bool vec = p.vec != 0;
 
     // scan role: channel cs = lane, state group q = warp
@@ -677,11 +691,13 @@ scan_nsplit_kernel(const ScanParams p)
     u64 h01 = 0, h23 = 0;   // +0.0f in both halves
 
     // the raw pieces this thread copies: source row pointer, element offset
-    // within the chunk, shared-memory offset within a stage; rows past d_inner
-    // or N (and a missing z) copy nothing
+    // within the chunk, shared-memory offset within a stage, whether the piece
+    // is needed by the readout only (z, C); rows past d_inner or N (and a
+    // missing z) copy nothing
     const T *src[PPT];
     uint32_t soff[PPT];
     int poff[PPT];
+    bool ro_only[PPT];
 #pragma unroll
     for (int u = 0; u < PPT; ++u) {
         const int pi = tid + u * NT;
@@ -697,6 +713,7 @@ scan_nsplit_kernel(const ScanParams p)
             ok = ok && d0 + r < Dn && g != nullptr;
             base = ok ? g + (b * Dn + d0 + r) * L : static_cast<const T *>(p.x);
             off = tensor * SH::RAW_X + r * SH::ROWB;
+            ro_only[u] = tensor == 2;
         } else {
             const int v = pi - 3 * CH * PR;
             const int m = v / (NS * PR);
@@ -705,22 +722,25 @@ scan_nsplit_kernel(const ScanParams p)
             ok = ok && r < N;
             base = static_cast<const T *>(m == 0 ? p.B : p.C) + (b * N + (ok ? r : 0)) * L;
             off = 3 * SH::RAW_X + m * SH::RAW_BC + r * LC * (int)sizeof(T);
+            ro_only[u] = m == 1;
         }
         src[u] = base;
         soff[u] = off + pc * 16;
         poff[u] = ok ? pc * EPP : (1 << 30);   // a piece that does not exist is always past the end
     }
 
-    // copy the raw pieces of chunk j into stage j % STAGES (steps past L and
-    // rows that do not exist are zero)
-    auto stage_in = [&](int64_t j) {
+    // copy the raw pieces of chunk j of the segment into stage j % STAGES
+    // (steps at or past the segment end and rows that do not exist are zero)
+    auto stage_in = [&](int64_t j, bool readout) {
         const uint32_t st = raw_s + static_cast<uint32_t>((j % STAGES) * SH::STAGE_BYTES);
-        const int64_t t1 = j * LC;
-        const int rem = static_cast<int>(L - t1 < (1 << 29) ? L - t1 : (1 << 29));   // steps left from t1
+        const int64_t t1 = t_lo + j * LC;
+        const int rem = static_cast<int>(t_hi - t1 < (1 << 29) ? t_hi - t1 : (1 << 29));   // steps left
 #pragma unroll
         for (int u = 0; u < PPT; ++u) {
             if (tid + u * NT >= SH::NPIECE)
                 break;
+            if (!readout && ro_only[u])
+                continue;
             const int left = rem - poff[u];
             const int nb = left >= EPP ? 16 : (left > 0 ? left * (int)sizeof(T) : 0);
             const T *g = src[u] + (nb > 0 ? t1 + poff[u] : 0);
@@ -742,11 +762,12 @@ scan_nsplit_kernel(const ScanParams p)
         cp_async_commit();
     };
 
-    // raw B, C of chunk j -> fp32 [t][n]: each item is (tensor, step t,
+    // raw B (and C) of chunk j -> fp32 [t][n]: each item is (tensor, step t,
     // states 4g..4g+3), written as one 16-byte word
-    auto convert_bc = [&](int64_t j) {
+    auto convert_bc = [&](int64_t j, bool readout) {
         const unsigned char *st = raw + (j % STAGES) * SH::STAGE_BYTES + 3 * SH::RAW_X;
-        for (int w = tid; w < 2 * LC * S; w += NT) {
+        const int items = (readout ? 2 : 1) * LC * S;
+        for (int w = tid; w < items; w += NT) {
             const int m = w / (LC * S);
             const int t = (w % (LC * S)) / S;
             const int g = w % S;
@@ -765,13 +786,22 @@ scan_nsplit_kernel(const ScanParams p)
         }
     };
 
+    // this thread's sum of the steps it prepares (compensated), for the segment carry
+    float ssum = 0.0f, scomp = 0.0f;
+    auto kahan = [&](float v) {
+        const float yv = v - scomp;
+        const float tv = ssum + yv;
+        scomp = (tv - ssum) - yv;
+        ssum = tv;
+    };
+
     // delta and delta*x of this thread's steps of chunk j
-    auto prep = [&](int64_t j) {
+    auto prep = [&](int64_t j, bool sum_steps) {
         const unsigned char *st = raw + (j % STAGES) * SH::STAGE_BYTES;
         uint32_t xw[RW], dw[RW];
         read_run_raw<T, RL>(st + ce * SH::ROWB, re * RL, xw);
         read_run_raw<T, RL>(st + SH::RAW_X + ce * SH::ROWB, re * RL, dw);
-        const int64_t left64 = L - (j * LC + re * RL);
+        const int64_t left64 = t_hi - (t_lo + j * LC + re * RL);
         const int lim = act_e ? static_cast<int>(left64 < RL ? left64 : RL) : 0;
 #pragma unroll
         for (int i = 0; i < RL; i += 2) {
@@ -782,6 +812,10 @@ scan_nsplit_kernel(const ScanParams p)
             upk(s2, s0, s1);
             s0 = i < lim ? s0 : 0.0f;
             s1 = i + 1 < lim ? s1 : 0.0f;
+            if (sum_steps) {
+                kahan(s0);
+                kahan(s1);
+            }
             float sx0, sx1;
             upk(mul2(pk(s0, s1), xx), sx0, sx1);
             Pd[(re * RL + i) * CH + ce] = pk(s0, sx0);
@@ -789,100 +823,145 @@ scan_nsplit_kernel(const ScanParams p)
         }
     };
 
-    const int64_t nchunks = (L + LC - 1) / LC;
-#pragma unroll
-    for (int s = 0; s < STAGES - 1; ++s)
-        if (s < nchunks)
-            stage_in(s);
-        else
-            cp_async_commit();
-    cp_async_wait<STAGES - 2>();
-    __syncthreads();
-    prep(0);
-    convert_bc(0);
-    __syncthreads();
-
     float *yq_s = Yp + q * SH::YQ + cs * SH::YROW;   // this lane's partial readouts
     const float *Bq_s = Bf + 4 * q;                   // this warp's states of B_t, C_t
     const float *Cq_s = Cf + 4 * q;
-    for (int64_t k = 0; k < nchunks; ++k) {
-        const int64_t t0 = k * LC;
-        if (k + STAGES - 1 < nchunks)
-            stage_in(k + STAGES - 1);
-        else
-            cp_async_commit();
 
-        // ---- scan: 4 states of channel cs over the chunk; the decays and
-        // writes of step t + D are formed while the state takes step t
-        {
-            u64 ra01[D], ra23[D], rb01[D], rb23[D];
-            float yv[LC];
-            auto form = [&](int t, int slot) {
-                float dl, dx;
-                upk(Pd[t * CH + cs], dl, dx);
-                const ulonglong2 Bq = *reinterpret_cast<const ulonglong2 *>(Bq_s + t * NS);
-                const u64 dd = splat(dl);
-                const u64 xx = splat(dx);
-                ra01[slot] = ex2_2(mul2(dd, A01));
-                ra23[slot] = ex2_2(mul2(dd, A23));
-                rb01[slot] = mul2(xx, Bq.x);
-                rb23[slot] = mul2(xx, Bq.y);
-            };
+    // walk the segment [t_lo, t_hi): with the readout (y stored) or without
+    // it (state and step sum only)
+    auto run = [&](auto ro) {
+        constexpr bool RO = decltype(ro)::value;
+        const int64_t nchunks = (t_hi - t_lo + LC - 1) / LC;
 #pragma unroll
-            for (int i = 0; i < D; ++i)
-                form(i, i);
-#pragma unroll
-            for (int t = 0; t < LC; ++t) {
-                const int slot = t % D;
-                const u64 a01 = ra01[slot], a23 = ra23[slot], b01 = rb01[slot], b23 = rb23[slot];
-                if (t + D < LC)
-                    form(t + D, slot);
-                const ulonglong2 Cq = *reinterpret_cast<const ulonglong2 *>(Cq_s + t * NS);
-                h01 = fma2(a01, h01, b01);
-                h23 = fma2(a23, h23, b23);
-                yv[t] = hsum(fma2(Cq.y, h23, mul2(Cq.x, h01)));
-            }
-#pragma unroll
-            for (int t = 0; t < LC; t += 4)
-                *reinterpret_cast<float4 *>(yq_s + t) = make_float4(yv[t], yv[t + 1], yv[t + 2], yv[t + 3]);
-        }
-        cp_async_wait<STAGES - 2>();   // chunk k+1 has landed (this thread's copies)
+        for (int s = 0; s < STAGES - 1; ++s)
+            if (s < nchunks)
+                stage_in(s, RO);
+            else
+                cp_async_commit();
+        cp_async_wait<STAGES - 2>();
+        __syncthreads();
+        prep(0, !RO);
+        convert_bc(0, RO);
         __syncthreads();
 
-        // ---- epilogue of chunk k: sum partials, skip term, gate, store
-        {
-            const unsigned char *st = raw + (k % STAGES) * SH::STAGE_BYTES;
-            uint32_t xw[RW], zw[RW];
-            read_run_raw<T, RL>(st + ce * SH::ROWB, re * RL, xw);
-            if (gate)
-                read_run_raw<T, RL>(st + 2 * SH::RAW_X + ce * SH::ROWB, re * RL, zw);
-            float out[RL];
+        for (int64_t k = 0; k < nchunks; ++k) {
+            const int64_t t0 = t_lo + k * LC;
+            if (k + STAGES - 1 < nchunks)
+                stage_in(k + STAGES - 1, RO);
+            else
+                cp_async_commit();
+
+            // ---- scan: 4 states of channel cs over the chunk; the decays and
+            // writes of step t + D are formed while the state takes step t
+            {
+                u64 ra01[D], ra23[D], rb01[D], rb23[D];
+                float yv[LC];
+                auto form = [&](int t, int slot) {
+                    float dl, dx;
+                    upk(Pd[t * CH + cs], dl, dx);
+                    const ulonglong2 Bq = *reinterpret_cast<const ulonglong2 *>(Bq_s + t * NS);
+                    const u64 dd = splat(dl);
+                    const u64 xx = splat(dx);
+                    ra01[slot] = ex2_2(mul2(dd, A01));
+                    ra23[slot] = ex2_2(mul2(dd, A23));
+                    rb01[slot] = mul2(xx, Bq.x);
+                    rb23[slot] = mul2(xx, Bq.y);
+                };
 #pragma unroll
-            for (int i = 0; i < RL; i += 2) {
-                const float *yp = Yp + ce * SH::YROW + re * RL + i;
-                u64 acc = *reinterpret_cast<const u64 *>(yp);
+                for (int i = 0; i < D; ++i)
+                    form(i, i);
 #pragma unroll
-                for (int qq = 1; qq < S; ++qq)
-                    acc = add2(acc, *reinterpret_cast<const u64 *>(yp + qq * SH::YQ));
-                acc = fma2(D2, word_pair<T>(xw, i), acc);
+                for (int t = 0; t < LC; ++t) {
+                    const int slot = t % D;
+                    const u64 a01 = ra01[slot], a23 = ra23[slot], b01 = rb01[slot], b23 = rb23[slot];
+                    if (t + D < LC)
+                        form(t + D, slot);
+                    h01 = fma2(a01, h01, b01);
+                    h23 = fma2(a23, h23, b23);
+                    if constexpr (RO) {
+                        const ulonglong2 Cq = *reinterpret_cast<const ulonglong2 *>(Cq_s + t * NS);
+                        yv[t] = hsum(fma2(Cq.y, h23, mul2(Cq.x, h01)));
+                    }
+                }
+                if constexpr (RO) {
+#pragma unroll
+                    for (int t = 0; t < LC; t += 4)
+                        *reinterpret_cast<float4 *>(yq_s + t) = make_float4(yv[t], yv[t + 1], yv[t + 2], yv[t + 3]);
+                }
+            }
+            cp_async_wait<STAGES - 2>();   // chunk k+1 has landed (this thread's copies)
+            __syncthreads();
+
+            // ---- epilogue of chunk k: sum partials, skip term, gate, store
+            if constexpr (RO) {
+                const unsigned char *st = raw + (k % STAGES) * SH::STAGE_BYTES;
+                uint32_t xw[RW], zw[RW];
+                read_run_raw<T, RL>(st + ce * SH::ROWB, re * RL, xw);
                 if (gate)
-                    acc = mul2(acc, silu2(word_pair<T>(zw, i)));
-                upk(acc, out[i], out[i + 1]);
+                    read_run_raw<T, RL>(st + 2 * SH::RAW_X + ce * SH::ROWB, re * RL, zw);
+                float out[RL];
+#pragma unroll
+                for (int i = 0; i < RL; i += 2) {
+                    const float *yp = Yp + ce * SH::YROW + re * RL + i;
+                    u64 acc = *reinterpret_cast<const u64 *>(yp);
+#pragma unroll
+                    for (int qq = 1; qq < S; ++qq)
+                        acc = add2(acc, *reinterpret_cast<const u64 *>(yp + qq * SH::YQ));
+                    acc = fma2(D2, word_pair<T>(xw, i), acc);
+                    if (gate)
+                        acc = mul2(acc, silu2(word_pair<T>(zw, i)));
+                    upk(acc, out[i], out[i + 1]);
+                }
+                if (act_e)
+                    write_run<T, RL>(yr, t0 + re * RL, t_hi, vec, out);
             }
-            if (act_e)
-                write_run<T, RL>(yr, t0 + re * RL, L, vec, out);
-        }
 
-        // ---- prep of chunk k+1
-        if (k + 1 < nchunks) {
-            prep(k + 1);
-            convert_bc(k + 1);
+            // ---- prep of chunk k+1
+            if (k + 1 < nchunks) {
+                prep(k + 1, !RO);
+                convert_bc(k + 1, RO);
+            }
+            __syncthreads();
         }
-        __syncthreads();
+        cp_async_wait<0>();
+    };
+
+    if (nseg > 1) {
+        // Segments of one channel group form a thread-block cluster. Each
+        // segment but the last walks its steps from a zero state (no readout)
+        // and publishes its end state and step sum; the state entering
+        // segment s is then the predecessors' maps folded in order,
+        // h <- exp(A * sum of steps) h + end state, read through distributed
+        // shared memory.
+        cg::cluster_group cluster = cg::this_cluster();
+        if (seg < nseg - 1)
+            run(Flag<false>{});
+        float hv[4];
+        upk(h01, hv[0], hv[1]);
+        upk(h23, hv[2], hv[3]);
+        Hx[q * CH + cs] = make_float4(hv[0], hv[1], hv[2], hv[3]);
+        Sx[re * CH + ce] = ssum;
+        cluster.sync();
+        u64 f01 = 0, f23 = 0;
+        for (int sp = 0; sp < seg; ++sp) {
+            const float4 *ph = cluster.map_shared_rank(Hx, sp);
+            const float *psum = cluster.map_shared_rank(Sx, sp);
+            float tot = 0.0f;
+#pragma unroll
+            for (int r = 0; r < S; ++r)
+                tot += psum[r * CH + cs];
+            const float4 he = ph[q * CH + cs];
+            const u64 tt = splat(tot);
+            f01 = fma2(ex2_2(mul2(tt, A01)), f01, pk(he.x, he.y));
+            f23 = fma2(ex2_2(mul2(tt, A23)), f23, pk(he.z, he.w));
+        }
+        cluster.sync();   // peers have finished reading this CTA's end state
+        h01 = f01;
+        h23 = f23;
     }
-    cp_async_wait<0>();
+    run(Flag<true>{});
 
-    if (p.final_state && act_s) {
+    if (p.final_state && act_s && seg == nseg - 1) {
         float *fs = p.final_state + (b * Dn + ds) * N;
         float hv[4];
         upk(h01, hv[0], hv[1]);
@@ -902,8 +981,71 @@ struct UpdateParams {
     const float *A, *D;
     void *y;
     int64_t batch, d_inner, N;
-    int vec;  // N % 4 == 0 and 16-byte aligned state/A, 8-byte aligned B/C
+    int vec;     // N % 4 == 0 and 16-byte aligned state and A
+    int vec_bc;  // B and C rows are whole 16-byte words (16-byte aligned, N * sizeof(T) % 16 == 0)
 };
+
+// One thread per (batch row, channel) holding all N = 4 NV states: the state
+// and A of the row move as 16-byte words, B and C of the batch row (shared by
+// all its channels, so served from L1 after the first warp) as 16-byte words
+// where their size allows, and the readout is summed inside the thread.
+template <typename T, int NV>
+__global__ void __launch_bounds__(kBlock)
+state_update_row_kernel(const UpdateParams p)
+{
+    constexpr int N = 4 * NV;
+    const int64_t row = static_cast<int64_t>(blockIdx.x) * kBlock + threadIdx.x;
+    if (row >= p.batch * p.d_inner)
+        return;
+    const int64_t b = row / p.d_inner;
+    const int64_t d = row % p.d_inner;
+    float4 *st = reinterpret_cast<float4 *>(p.state + row * N);
+    const float4 *Ad = reinterpret_cast<const float4 *>(p.A + d * N);
+    const T *Bb = static_cast<const T *>(p.B) + b * N;
+    const T *Cb = static_cast<const T *>(p.C) + b * N;
+
+    float4 h[NV], a[NV];
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+        h[v] = st[v];
+        a[v] = __ldg(Ad + v);
+    }
+    float bv[N], cv[N];
+    if (p.vec_bc) {
+#pragma unroll
+        for (int e = 0; e < N; e += Io<T>::kPerVec) {
+            Io<T>::loadvec(Bb + e, bv + e);
+            Io<T>::loadvec(Cb + e, cv + e);
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < N; ++e) {
+            bv[e] = Io<T>::load1(Bb + e);
+            cv[e] = Io<T>::load1(Cb + e);
+        }
+    }
+    const float xv = Io<T>::load1(static_cast<const T *>(p.x) + row);
+    const float dl = Io<T>::load1(static_cast<const T *>(p.delta) + row);
+    const float dx = dl * xv;
+    const float dl2 = dl * kLog2e;
+    float out = 0.0f;
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+        float *hv = reinterpret_cast<float *>(&h[v]);
+        const float *av = reinterpret_cast<const float *>(&a[v]);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int n = 4 * v + e;
+            hv[e] = fmaf(ex2_approx(dl2 * av[e]), hv[e], dx * bv[n]);
+            out = fmaf(cv[n], hv[e], out);
+        }
+        st[v] = h[v];
+    }
+    out = fmaf(p.D ? __ldg(p.D + d) : 0.0f, xv, out);
+    if (p.z)
+        out *= silu_f(Io<T>::load1(static_cast<const T *>(p.z) + row));
+    Io<T>::store1(static_cast<T *>(p.y) + row, out);
+}
 
 // One thread per (row, group of 4 states); the NQ threads of a row are
 // adjacent lanes of one warp and sum their partial readouts by shuffles.
@@ -1115,56 +1257,111 @@ ss_status dispatch_scan_lanes(const ScanParams &p, int lanes, cudaStream_t s)
     }
 }
 
+// Segments per channel group for the n-split kernel: when the channel groups
+// fill less than half of the CTA slots of the GPU, the sequence is cut into
+// up to 8 segments (one thread-block cluster per group) so that the grid
+// fills one wave, keeping at least 4 chunks per segment.
+int pick_segments(int64_t groups, int64_t L, int64_t lc, int64_t slots)
+{
+    const char *env = getenv("SS_SCAN_SEGMENTS");
+    if (env) {
+        const int v = atoi(env);
+        if (v >= 1 && v <= 8)
+            return v;
+    }
+    if (2 * groups > slots)
+        return 1;
+    int64_t n = slots / groups;
+    n = n < 8 ? n : 8;
+    const int64_t by_len = L / (4 * lc);
+    n = n < by_len ? n : by_len;
+    return n < 1 ? 1 : static_cast<int>(n);
+}
+
 template <typename T, int S>
-ss_status launch_nsplit(const ScanParams &p, cudaStream_t stream)
+ss_status launch_nsplit(const ScanParams &p0, cudaStream_t stream, int sms)
 {
     using SH = NSplitShape<T, S>;
+    auto kernel = scan_nsplit_kernel<T, S>;
     const size_t smem = SH::BYTES;
     if (smem > 48u * 1024u) {
-        cudaError_t e = cudaFuncSetAttribute(scan_nsplit_kernel<T, S>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(smem));
         if (e != cudaSuccess) {
             cudaGetLastError();
             return fail(SS_ERR_LAUNCH, "cudaFuncSetAttribute failed: %s", cudaGetErrorString(e));
         }
     }
-    const int64_t gx = (p.d_inner + SH::CH - 1) / SH::CH;
-    if (gx > 0x7fffffff || p.batch > 65535)
+    ScanParams p = p0;
+    const int64_t gpr = (p.d_inner + SH::CH - 1) / SH::CH;   // channel groups per batch row
+    int occ = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, SH::NT, smem) != cudaSuccess || occ < 1) {
+        cudaGetLastError();
+        occ = 1;
+    }
+    int nseg = pick_segments(gpr * p.batch, p.L, SH::LC, static_cast<int64_t>(sms) * occ);
+    int64_t seg_len = (p.L + nseg - 1) / nseg;
+    seg_len = (seg_len + SH::LC - 1) / SH::LC * SH::LC;
+    nseg = static_cast<int>((p.L + seg_len - 1) / seg_len);
+    if (gpr * nseg > 0x7fffffff || p.batch > 65535)
         return fail(SS_ERR_DIM, "grid too large: %lld channel blocks x %lld batch rows",
-                    (long long)gx, (long long)p.batch);
-    dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(p.batch));
-    scan_nsplit_kernel<T, S><<<grid, SH::NT, smem, stream>>>(p);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess)
+                    (long long)(gpr * nseg), (long long)p.batch);
+
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.gridDim = dim3(static_cast<unsigned>(gpr * nseg), static_cast<unsigned>(p.batch));
+    cfg.blockDim = dim3(SH::NT);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    if (nseg > 1) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = nseg;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int clusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg) != cudaSuccess || clusters < 1) {
+            cudaGetLastError();   // a cluster of this size cannot be placed: do not split
+            nseg = 1;
+            seg_len = p.L;
+            cfg.gridDim.x = static_cast<unsigned>(gpr);
+            cfg.attrs = nullptr;
+            cfg.numAttrs = 0;
+        }
+    }
+    p.nseg = nseg;
+    p.seg_len = seg_len;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, p);
+    if (e == cudaSuccess)
+        e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        cudaGetLastError();
         return fail(SS_ERR_LAUNCH, "scan kernel launch failed: %s", cudaGetErrorString(e));
+    }
     return SS_OK;
 }
 
 template <typename T>
-ss_status dispatch_nsplit(const ScanParams &p, cudaStream_t s)
+ss_status dispatch_nsplit(const ScanParams &p, cudaStream_t s, int sms)
 {
-    if (p.N <= 4) return launch_nsplit<T, 1>(p, s);
-    if (p.N <= 8) return launch_nsplit<T, 2>(p, s);
-    if (p.N <= 16) return launch_nsplit<T, 4>(p, s);
-    return launch_nsplit<T, 8>(p, s);
+    if (p.N <= 4) return launch_nsplit<T, 1>(p, s, sms);
+    if (p.N <= 8) return launch_nsplit<T, 2>(p, s, sms);
+    if (p.N <= 16) return launch_nsplit<T, 4>(p, s, sms);
+    return launch_nsplit<T, 8>(p, s, sms);
 }
 
-// n-split (N <= 32) when channels x state groups fill every SM with at least
-// two warps per scheduler; otherwise time lanes.
-bool use_nsplit(int64_t channels, int64_t N, int sms)
+// The n-split kernel serves N <= 32 (cutting long sequences into segments
+// when the channels alone do not fill the GPU); the time-lane kernel serves
+// N > 32. SS_SCAN_KERNEL=nsplit|lanes overrides the choice.
+bool use_nsplit(int64_t N)
 {
     if (N > 32)
         return false;
     const char *env = getenv("SS_SCAN_KERNEL");
-    if (env && strcmp(env, "nsplit") == 0)
-        return true;
     if (env && strcmp(env, "lanes") == 0)
         return false;
-    int64_t s = 1;
-    while (4 * s < N)
-        s *= 2;
-    return channels * s >= static_cast<int64_t>(sms) * 256;
+    return true;
 }
 
 template <typename T>
@@ -1198,8 +1395,10 @@ ss_status scan_fwd(const void *x, const void *dt, const float *A, const void *B,
     p.softplus = softplus ? 1 : 0;
     p.vec = (L % 16 == 0) && aligned16(x) && aligned16(dt) && aligned16(y) && (!z || aligned16(z));
 
-    if (use_nsplit(batch * d_inner, N, sm_count(dev)))
-        return dispatch_nsplit<T>(p, stream);
+    p.nseg = 1;
+    p.seg_len = L;
+    if (use_nsplit(N))
+        return dispatch_nsplit<T>(p, stream, sm_count(dev));
     const int lanes = pick_lanes(batch * d_inner, L, sm_count(dev));
     if (N <= 4)
         return dispatch_scan_lanes<T, 4>(p, lanes, stream);
@@ -1216,6 +1415,19 @@ ss_status launch_update(const UpdateParams &p, cudaStream_t stream)
     if (blocks > 0x7fffffff)
         return fail(SS_ERR_DIM, "grid too large");
     state_update_kernel<T, NQ><<<static_cast<unsigned>(blocks), kBlock, 0, stream>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return fail(SS_ERR_LAUNCH, "state update launch failed: %s", cudaGetErrorString(e));
+    return SS_OK;
+}
+
+template <typename T, int NV>
+ss_status launch_update_rows(const UpdateParams &p, cudaStream_t stream)
+{
+    const int64_t blocks = (p.batch * p.d_inner + kBlock - 1) / kBlock;
+    if (blocks > 0x7fffffff)
+        return fail(SS_ERR_DIM, "grid too large");
+    state_update_row_kernel<T, NV><<<static_cast<unsigned>(blocks), kBlock, 0, stream>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
         return fail(SS_ERR_LAUNCH, "state update launch failed: %s", cudaGetErrorString(e));
@@ -1247,6 +1459,15 @@ ss_status state_update(float *state, const void *x, const void *delta, const flo
     p.A = A; p.D = D; p.y = y;
     p.batch = batch; p.d_inner = d_inner; p.N = N;
     p.vec = (N % 4 == 0) && aligned16(state) && aligned16(A);
+    p.vec_bc = ((N * static_cast<int64_t>(sizeof(T))) % 16 == 0) && aligned16(B) && aligned16(C);
+    if (p.vec && N <= 16) {
+        switch (N / 4) {
+        case 1: return launch_update_rows<T, 1>(p, stream);
+        case 2: return launch_update_rows<T, 2>(p, stream);
+        case 3: return launch_update_rows<T, 3>(p, stream);
+        default: return launch_update_rows<T, 4>(p, stream);
+        }
+    }
     const int64_t nq = (N + 3) / 4;
     if (nq <= 1) return launch_update<T, 1>(p, stream);
     if (nq <= 2) return launch_update<T, 2>(p, stream);

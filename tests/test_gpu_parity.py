@@ -19,14 +19,21 @@ from tests.gpu_util import TOL, assert_close, dev, gpu_scan, oracle_scan
 
 pytestmark = pytest.mark.gpu
 
-# kernel variants: the n-split kernel, and the time-lane kernel with 1, 4, 16 lanes
-LANES = ["nsplit", "1", "4", "16"]
+# kernel variants: the n-split kernel (whole sequence, or cut into 3 or 8
+# segments joined through a thread-block cluster), and the time-lane kernel
+# with 1, 4, 16 lanes
+LANES = ["nsplit", "seg3", "seg8", "1", "4", "16"]
 
 
 @pytest.fixture
 def lanes(request, monkeypatch):
     if request.param == "nsplit":
         monkeypatch.setenv("SS_SCAN_KERNEL", "nsplit")
+        monkeypatch.setenv("SS_SCAN_SEGMENTS", "1")
+        return 0
+    if request.param.startswith("seg"):
+        monkeypatch.setenv("SS_SCAN_KERNEL", "nsplit")
+        monkeypatch.setenv("SS_SCAN_SEGMENTS", request.param[3:])
         return 0
     monkeypatch.setenv("SS_SCAN_KERNEL", "lanes")
     monkeypatch.setenv("SS_SCAN_LANES", request.param)
@@ -67,7 +74,7 @@ OPTIONAL = [dict(use_D=False), dict(use_z=False), dict(use_bias=False), dict(sof
             dict(use_D=False, use_z=False, use_bias=False, softplus=False), dict(final_state=False)]
 
 
-@pytest.mark.parametrize("lanes", ["nsplit", "1", "16"], indirect=True)
+@pytest.mark.parametrize("lanes", ["nsplit", "seg3", "1", "16"], indirect=True)
 @pytest.mark.parametrize("opt", OPTIONAL, ids=lambda o: "_".join("%s=%s" % kv for kv in o.items()))
 @pytest.mark.parametrize("io", ["bf16", "f32"])
 def test_optional_pointers_and_flag(opt, io, lanes):
@@ -88,7 +95,7 @@ def test_optional_pointers_and_flag(opt, io, lanes):
 
 
 @pytest.mark.parametrize("io", ["bf16", "f32"])
-@pytest.mark.parametrize("lanes", ["nsplit", "16"], indirect=True)
+@pytest.mark.parametrize("lanes", ["nsplit", "seg3", "16"], indirect=True)
 def test_unaligned_pointers_take_the_scalar_path(io, lanes):
     inp = I.make_scan_inputs(I.ScanSpec(batch=2, d_inner=10, L=48, N=16, io=io, seed=8))
     g = dev(inp)
@@ -106,7 +113,7 @@ def test_unaligned_pointers_take_the_scalar_path(io, lanes):
     assert_close(fs.cpu().numpy(), fr, inp["x"].dtype, "final_state")
 
 
-@pytest.mark.parametrize("lanes", ["nsplit", "1"], indirect=True)
+@pytest.mark.parametrize("lanes", ["nsplit", "seg8", "1"], indirect=True)
 def test_extreme_steps_stay_finite(lanes):
     """Very large and very negative raw steps (softplus saturating both ways)."""
     inp = I.make_scan_inputs(I.ScanSpec(batch=1, d_inner=16, L=64, N=16, io="f32", seed=9))
