@@ -316,6 +316,55 @@ def time_decode(spec: I.DecodeSpec, reps: int, warmup: int):
     return graph_ms_per_token, flushed_ms
 
 
+def time_conv(spec: I.ScanSpec, steps: int, warmup: int, k: int = 4):
+    """Causal conv1d + SiLU over the layer input, L2 flushed before each launch.
+    Returns (median ms, algorithmic bytes: x read, out written, weights, bias,
+    history written)."""
+    from selective_state_space_138_b300 import binding
+    x = I.normal(spec.seed, 11, (spec.batch, spec.d_inner, spec.L), 1.0, torch.bfloat16).cuda()
+    w = I.normal(spec.seed, 12, (spec.d_inner, k), 0.5, torch.float32).cuda()
+    bias = I.normal(spec.seed, 13, (spec.d_inner,), 0.2, torch.float32).cuda()
+    out = torch.empty_like(x)
+    st = torch.empty((spec.batch, k - 1, spec.d_inner), dtype=x.dtype, device="cuda")
+    scratch = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    for _ in range(warmup):
+        binding.causal_conv1d(x, w, bias, out=out, state_out=st)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for a, b in ev:
+        scratch.zero_()
+        a.record()
+        binding.causal_conv1d(x, w, bias, out=out, state_out=st)
+        b.record()
+    torch.cuda.synchronize()
+    ms = statistics.median([a.elapsed_time(b) for a, b in ev])
+    bdl = spec.batch * spec.d_inner * spec.L
+    return ms, 2 * bdl * 2 + spec.d_inner * (k + 1) * 4 + spec.batch * (k - 1) * spec.d_inner * 2
+
+
+def time_conv_step(spec: I.DecodeSpec, steps: int, k: int = 4):
+    """One decode step of the convolution on the decode workload's shape, L2
+    flushed before each launch. Returns (median ms, algorithmic bytes)."""
+    from selective_state_space_138_b300 import binding
+    x = I.normal(spec.seed, 11, (spec.batch, spec.d_inner), 1.0, torch.bfloat16).cuda()
+    w = I.normal(spec.seed, 12, (spec.d_inner, k), 0.5, torch.float32).cuda()
+    bias = I.normal(spec.seed, 13, (spec.d_inner,), 0.2, torch.float32).cuda()
+    st = I.normal(spec.seed, 14, (spec.batch, k - 1, spec.d_inner), 1.0, torch.bfloat16).cuda()
+    out = torch.empty_like(x)
+    scratch = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    for _ in range(3):
+        binding.conv_state_update(st, x, w, bias, out=out)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for a, b in ev:
+        scratch.zero_()
+        a.record()
+        binding.conv_state_update(st, x, w, bias, out=out)
+        b.record()
+    torch.cuda.synchronize()
+    ms = statistics.median([a.elapsed_time(b) for a, b in ev])
+    bd = spec.batch * spec.d_inner
+    return ms, bd * 2 * 2 + 2 * bd * (k - 1) * 2 + spec.d_inner * (k + 1) * 4
+
+
 def roofline_obj(alg_bytes: float, ms: float, peaks: dict, traffic, elem_steps: float | None = None):
     """HBM roofline of one launch: algorithmic bytes / launch time against the
     measured copy bandwidth. For a scan, also the fraction of the ALU ceiling:
@@ -513,6 +562,15 @@ def main(argv=None):
         t = time_scan(I.TINY, 20, 3, flush=False)
         extras[I.TINY.name] = {"elem_steps_per_s": I.TINY.elem_steps / (statistics.median(t) * 1e-3),
                                "kernel_ms_median": statistics.median(t), "note": "launch-bound; parity case"}
+        cms, cbytes = time_conv(HEADLINE, 10, 3)
+        extras["conv1d_silu_k4_" + HEADLINE.name] = {
+            "elems_per_s": HEADLINE.batch * HEADLINE.d_inner * HEADLINE.L / (cms * 1e-3), "kernel_ms_median": cms,
+            "roofline": roofline_obj(cbytes, cms, peaks, None),
+            "note": "causal depthwise conv (k = 4) + SiLU on the layer's (batch, d_inner, L) input, history out"}
+        sms_, sbytes = time_conv_step(I.DECODE, 20)
+        extras["conv_state_update_k4_" + I.DECODE.name] = {
+            "ms_per_token": sms_, "roofline": roofline_obj(sbytes, sms_, peaks, None),
+            "note": "one decode step of the convolution (cache of 3 inputs per channel), L2 flushed before each"}
         gms, fms = time_decode(I.DECODE, reps=3, warmup=3)
         dbytes = decode_alg_bytes(I.DECODE)
         extras[I.DECODE.name] = {

@@ -1,6 +1,10 @@
 /*
  * ss_scan.h -- C ABI of the B300 (sm_103a) selective-scan library (libssscan.so).
  *
+ * Besides the scan and its decode update, the library carries the causal
+ * depthwise convolution that feeds the scan in a Mamba block, with its
+ * decode cache.
+ *
  * The library computes the Mamba selective state-space layer (S6) forward
  * pass and its single-token state update, as defined in "Mamba and selective
  * state spaces" (box "Selective state-space model (S6)", section "The
@@ -122,6 +126,59 @@ ss_status ss_state_update_f32(float *state, const float *x, const float *delta,
                               const float *D, const float *z, float *y,
                               int64_t batch, int64_t d_inner, int64_t N,
                               cudaStream_t stream);
+
+#define SS_MAX_CONV_K 8
+
+/*
+ * ss_causal_conv1d_bf16 / ss_causal_conv1d_f32 -- the causal depthwise
+ * convolution that precedes the scan in a Mamba block ("Mamba and selective
+ * state spaces", box "The Mamba block"):
+ *
+ *   out[b,d,t] = act( sum_{i=0}^{k-1} w[d,i] * x[b,d,t-i] + bias[d] ),
+ *   act = SiLU(v) = v * sigmoid(v) when `silu` is non-zero, identity otherwise,
+ *
+ * where w[d,i] weighs the input i steps back and the inputs before t = 0 are
+ * zero ("x~_s = 0 for s <= 0"), or, when `state_in` is given, the k-1 inputs
+ * that preceded this call.
+ *
+ *   x, out         : (batch, d_inner, L) io dtype.
+ *   w              : (d_inner, k) fp32.   bias : (d_inner) fp32 or NULL.
+ *   state_in       : (batch, k-1, d_inner) io dtype, oldest first, or NULL.
+ *   state_out      : (batch, k-1, d_inner) io dtype or NULL: receives the last
+ *                    k-1 inputs, oldest first -- the decode cache that prefill
+ *                    hands to ss_conv_state_update ("Decoding with a
+ *                    constant-size cache"). It must not overlap state_in.
+ *   1 <= k <= SS_MAX_CONV_K.
+ * Errors: as ss_scan_fwd_* (SS_ERR_DIM also for k out of range).
+ */
+ss_status ss_causal_conv1d_bf16(const ss_bf16 *x, const float *w, const float *bias,
+                                const ss_bf16 *state_in, int silu, ss_bf16 *out,
+                                ss_bf16 *state_out, int64_t batch, int64_t d_inner,
+                                int64_t L, int64_t k, cudaStream_t stream);
+
+ss_status ss_causal_conv1d_f32(const float *x, const float *w, const float *bias,
+                               const float *state_in, int silu, float *out, float *state_out,
+                               int64_t batch, int64_t d_inner, int64_t L, int64_t k,
+                               cudaStream_t stream);
+
+/*
+ * ss_conv_state_update_bf16 / ss_conv_state_update_f32 -- one decode step of
+ * the convolution ("Decoding with a constant-size cache"): with the cached
+ * k-1 previous inputs and the new input x, out = act(sum_i w[d,i] x_{t-i} +
+ * bias[d]); then the cache drops its oldest entry and appends x (the cache
+ * holds the convolution's inputs, not its outputs).
+ *
+ *   conv_state : (batch, k-1, d_inner) io dtype, oldest first, updated in
+ *                place (may be NULL when k = 1).
+ *   x, out     : (batch, d_inner) io dtype.  w : (d_inner, k).  bias : or NULL.
+ */
+ss_status ss_conv_state_update_bf16(ss_bf16 *conv_state, const ss_bf16 *x, const float *w,
+                                    const float *bias, int silu, ss_bf16 *out, int64_t batch,
+                                    int64_t d_inner, int64_t k, cudaStream_t stream);
+
+ss_status ss_conv_state_update_f32(float *conv_state, const float *x, const float *w,
+                                   const float *bias, int silu, float *out, int64_t batch,
+                                   int64_t d_inner, int64_t k, cudaStream_t stream);
 
 /* Message describing the last non-OK status returned on this host thread
  * ("" if none). The string is owned by the library. */

@@ -7,6 +7,8 @@ does. Nothing here imports the CUDA library or its binding.
 * ``scan`` / ``scan_rows`` run the plain float64 loop of ``ss_oracle.c`` over
   all rows or over a sample of rows, in parallel over rows (the C call releases
   the GIL).
+* ``causal_conv1d`` is the block's causal depthwise convolution (+ SiLU)
+  with an optional carried history of k-1 inputs, in float64.
 * ``decode_chain`` runs that same loop over consecutive single-token inputs:
   the decode update is one step of the scan, so a chain of steps equals the
   scan over the tokens ("Mamba and selective state spaces", section "Decoding
@@ -52,6 +54,9 @@ def load(path: str | None = None):
     lib.oracle_softplus.restype = ctypes.c_double
     lib.oracle_scan_rows.argtypes = [dp] * 8 + [ctypes.c_int, dp, dp, dp] + [ctypes.c_int64] * 6
     lib.oracle_scan_rows.restype = ctypes.c_int
+    if hasattr(lib, "oracle_causal_conv1d_rows"):
+        lib.oracle_causal_conv1d_rows.argtypes = [dp, dp, dp, ctypes.c_int, dp, dp, dp] + [ctypes.c_int64] * 6
+        lib.oracle_causal_conv1d_rows.restype = ctypes.c_int
     if path is None:
         _lib = lib
     return lib
@@ -177,6 +182,36 @@ def decode_chain(tokens: dict, params: dict, rows, use_D=True, use_z=True, h0=No
         y[idx] = yb[0]
         fs[idx] = fb[0]
     return y, fs
+
+
+def causal_conv1d(xin, w, bias=None, silu=True, state=None, threads: int | None = None, lib=None):
+    """Causal depthwise convolution of the Mamba block in float64.
+
+    xin: (batch, d_inner, L); w: (d_inner, k); bias: (d_inner,) or None;
+    state: previous k-1 inputs (batch, k-1, d_inner), oldest first, or None
+    (zero history). Returns (out (batch, d_inner, L), last k-1 inputs
+    (batch, k-1, d_inner)).
+    """
+    lib = lib or load()
+    xin, w, bias, state = map(_f64, (xin, w, bias, state))
+    batch, d_inner, L = xin.shape
+    k = w.shape[1]
+    out = np.empty((batch, d_inner, L))
+    st = np.empty((batch, max(k - 1, 0), d_inner))
+    rows = batch * d_inner
+    nt = max(1, min(threads or default_threads(), rows)) if rows else 1
+    bounds = [(rows * i) // nt for i in range(nt + 1)]
+
+    def run(i):
+        return lib.oracle_causal_conv1d_rows(_ptr(xin), _ptr(w), _ptr(bias), int(bool(silu)), _ptr(state),
+                                             _ptr(out), _ptr(st) if k > 1 else None, batch, d_inner, L, k,
+                                             bounds[i], bounds[i + 1])
+
+    with ThreadPoolExecutor(nt) as ex:
+        codes = list(ex.map(run, range(nt)))
+    if any(c != 0 for c in codes):
+        raise RuntimeError("oracle_causal_conv1d_rows failed: %r" % (codes,))
+    return out, st
 
 
 # ---------------------------------------------------------------- helpers

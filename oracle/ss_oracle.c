@@ -106,3 +106,62 @@ int oracle_scan_rows(const double *x, const double *dt, const double *A,
     free(h);
     return 0;
 }
+
+/*
+ * Causal depthwise convolution of "The Mamba block" (box "The Mamba block"):
+ *
+ *   out[b,d,t] = act( sum_{i=0}^{k-1} w[d,i] * xin[b,d,t-i] + bias[d] )
+ *
+ * with act = SiLU (v * sigmoid(v)) when `silu` is set, identity otherwise. The
+ * inputs before t = 0 are the k-1 values in `state` (batch, k-1, d_inner),
+ * oldest first, or zero when `state` is NULL (the block's zero history). When
+ * `state_out` is given, the last k-1 inputs (oldest first, reaching into
+ * `state` for short sequences) are written there: the decode cache that
+ * prefill hands to the single-token steps ("Decoding with a constant-size
+ * cache"). Layouts: xin, out (batch, d_inner, L); w (d_inner, k); bias
+ * (d_inner). Runs rows r = b * d_inner + d in [row_begin, row_end).
+ */
+int oracle_causal_conv1d_rows(const double *xin, const double *w, const double *bias,
+                              int silu, const double *state, double *out, double *state_out,
+                              int64_t batch, int64_t d_inner, int64_t L, int64_t k,
+                              int64_t row_begin, int64_t row_end)
+{
+    if (!xin || !w || !out || k < 1 || L < 0 || batch < 0 || d_inner < 0)
+        return -1;
+    if (row_begin < 0 || row_end > batch * d_inner || row_begin > row_end)
+        return -1;
+    for (int64_t r = row_begin; r < row_end; ++r) {
+        const int64_t b = r / d_inner;
+        const int64_t d = r % d_inner;
+        const double *xr = xin + r * L;
+        for (int64_t t = 0; t < L; ++t) {
+            double acc = bias ? bias[d] : 0.0;
+            for (int64_t i = 0; i < k; ++i) {
+                const int64_t s = t - i;   /* input i steps back */
+                double v;
+                if (s >= 0)
+                    v = xr[s];
+                else if (state)
+                    v = state[(b * (k - 1) + (k - 1 + s)) * d_inner + d];
+                else
+                    v = 0.0;
+                acc += w[d * k + i] * v;
+            }
+            out[r * L + t] = silu ? acc * sigmoid(acc) : acc;
+        }
+        if (state_out) {
+            for (int64_t j = 0; j < k - 1; ++j) {
+                const int64_t s = L - (k - 1) + j;   /* input index held in slot j */
+                double v;
+                if (s >= 0)
+                    v = xr[s];
+                else if (state)
+                    v = state[(b * (k - 1) + (k - 1 + s)) * d_inner + d];
+                else
+                    v = 0.0;
+                state_out[(b * (k - 1) + j) * d_inner + d] = v;
+            }
+        }
+    }
+    return 0;
+}

@@ -18,11 +18,13 @@ LIB_PATH = os.path.join(_PKG, "libssscan.so")
 
 # names declared in include/ss_scan.h
 EXPORTS = ("ss_scan_fwd_bf16", "ss_scan_fwd_f32", "ss_state_update_bf16", "ss_state_update_f32",
-           "ss_last_error", "ss_abi_version")
+           "ss_causal_conv1d_bf16", "ss_causal_conv1d_f32", "ss_conv_state_update_bf16",
+           "ss_conv_state_update_f32", "ss_last_error", "ss_abi_version")
 
 STATUS = {0: "SS_OK", -1: "SS_ERR_NULL", -2: "SS_ERR_DIM", -3: "SS_ERR_N", -4: "SS_ERR_DEVICE_PTR",
           -5: "SS_ERR_LAUNCH", -6: "SS_ERR_INTERNAL"}
 MAX_N = 64
+MAX_CONV_K = 8
 
 _lib = None
 
@@ -50,6 +52,12 @@ def lib() -> ctypes.CDLL:
         getattr(L, name).restype = ci
     for name in ("ss_state_update_bf16", "ss_state_update_f32"):
         getattr(L, name).argtypes = upd_args
+        getattr(L, name).restype = ci
+    for name in ("ss_causal_conv1d_bf16", "ss_causal_conv1d_f32"):
+        getattr(L, name).argtypes = [vp, vp, vp, vp, ci, vp, vp, i64, i64, i64, i64, vp]
+        getattr(L, name).restype = ci
+    for name in ("ss_conv_state_update_bf16", "ss_conv_state_update_f32"):
+        getattr(L, name).argtypes = [vp, vp, vp, vp, ci, vp, i64, i64, i64, vp]
         getattr(L, name).restype = ci
     L.ss_last_error.argtypes = []
     L.ss_last_error.restype = ctypes.c_char_p
@@ -155,3 +163,49 @@ def state_update(state, x, delta, A, B, C, D=None, z=None, y=None, stream=None):
     _check(fn(_ptr(state), _ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(y),
               batch, d_inner, N, _stream(stream)))
     return y
+
+
+def causal_conv1d(x, w, bias=None, state_in=None, silu=True, out=None, state_out=None, return_state=False,
+                  stream=None):
+    """Causal depthwise convolution (+ SiLU) of the Mamba block; see
+    ``ss_causal_conv1d_*``. x: (batch, d_inner, L) bf16/fp32; w: (d_inner, k)
+    fp32; bias: (d_inner,) fp32; state_in / state_out: (batch, k-1, d_inner)
+    in the io dtype, oldest first. Returns (out, state_out)."""
+    io = x.dtype
+    sfx = _io_suffix(io)
+    batch, d_inner, L = x.shape
+    k = w.shape[1] if w.dim() == 2 else -1
+    _need(x, "x", io, (batch, d_inner, L))
+    _need(w, "w", torch.float32, (d_inner, k))
+    _need(bias, "bias", torch.float32, (d_inner,))
+    _need(state_in, "state_in", io, (batch, k - 1, d_inner))
+    if out is None:
+        out = torch.empty_like(x)
+    _need(out, "out", io, (batch, d_inner, L))
+    if state_out is None and return_state and k > 1:
+        state_out = torch.empty((batch, k - 1, d_inner), dtype=io, device=x.device)
+    _need(state_out, "state_out", io, (batch, k - 1, d_inner))
+    fn = getattr(lib(), "ss_causal_conv1d_" + sfx)
+    _check(fn(_ptr(x), _ptr(w), _ptr(bias), _ptr(state_in), int(bool(silu)), _ptr(out), _ptr(state_out),
+              batch, d_inner, L, k, _stream(stream)))
+    return out, state_out
+
+
+def conv_state_update(conv_state, x, w, bias=None, silu=True, out=None, stream=None):
+    """One decode step of the convolution; ``conv_state`` (batch, k-1, d_inner)
+    is updated in place; see ``ss_conv_state_update_*``. Returns out
+    (batch, d_inner)."""
+    io = x.dtype
+    sfx = _io_suffix(io)
+    batch, d_inner = x.shape
+    k = w.shape[1] if w.dim() == 2 else -1
+    _need(w, "w", torch.float32, (d_inner, k))
+    _need(bias, "bias", torch.float32, (d_inner,))
+    _need(conv_state, "conv_state", io, (batch, k - 1, d_inner))
+    if out is None:
+        out = torch.empty_like(x)
+    _need(out, "out", io, (batch, d_inner))
+    fn = getattr(lib(), "ss_conv_state_update_" + sfx)
+    _check(fn(_ptr(conv_state), _ptr(x), _ptr(w), _ptr(bias), int(bool(silu)), _ptr(out), batch, d_inner, k,
+              _stream(stream)))
+    return out

@@ -1127,6 +1127,138 @@ state_update_kernel(const UpdateParams p)
     }
 }
 
+// ------------------------------------------------------------------ causal depthwise conv1d
+//
+// out[b,d,t] = act(sum_{i<k} w[d,i] xin[b,d,t-i] + bias[d]), act = SiLU or
+// identity ("The Mamba block"); inputs before t = 0 come from the carried
+// history (batch, k-1, d_inner), oldest first, or are zero. One thread per
+// EPP-element (16-byte) piece of a row: it reads its piece and the HP pieces
+// before it (the halo of k-1 inputs), and writes its outputs as one 16-byte
+// word.
+
+struct ConvParams {
+    const void *x, *state_in;
+    const float *w, *bias;
+    void *out, *state_out;
+    int64_t batch, d_inner, L;
+    int silu;
+    int vec;  // 16-byte aligned rows of whole pieces
+};
+
+template <typename T, int K>
+__global__ void __launch_bounds__(kBlock)
+causal_conv1d_kernel(const ConvParams p)
+{
+    constexpr int EPP = 16 / (int)sizeof(T);
+    constexpr int HP = (K - 1 + EPP - 1) / EPP;   // halo pieces
+    const int64_t npieces = (p.L + EPP - 1) / EPP;
+    const int64_t gid = static_cast<int64_t>(blockIdx.x) * kBlock + threadIdx.x;
+    if (gid >= p.batch * p.d_inner * npieces)
+        return;
+    const int64_t row = gid / npieces;
+    const int64_t pc = gid % npieces;
+    const int64_t b = row / p.d_inner;
+    const int64_t d = row % p.d_inner;
+    const T *xr = static_cast<const T *>(p.x) + row * p.L;
+    const int64_t t0 = pc * EPP;
+
+    // inputs t0 - HP*EPP .. t0 + EPP - 1
+    float win[(HP + 1) * EPP];
+#pragma unroll
+    for (int v = 0; v <= HP; ++v) {
+        const int64_t ts = t0 - (HP - v) * EPP;
+        if (p.vec && ts >= 0 && ts + EPP <= p.L) {
+            Io<T>::loadvec(xr + ts, win + v * EPP);
+        } else {
+#pragma unroll
+            for (int e = 0; e < EPP; ++e) {
+                const int64_t t = ts + e;
+                float val = 0.0f;
+                if (t >= 0 && t < p.L)
+                    val = Io<T>::load1(xr + t);
+                else if (t < 0 && t >= -(K - 1) && p.state_in)
+                    val = Io<T>::load1(static_cast<const T *>(p.state_in) + (b * (K - 1) + (K - 1 + t)) * p.d_inner + d);
+                win[v * EPP + e] = val;
+            }
+        }
+    }
+    float wd[K];
+#pragma unroll
+    for (int i = 0; i < K; ++i)
+        wd[i] = __ldg(p.w + d * K + i);
+    const float bv = p.bias ? __ldg(p.bias + d) : 0.0f;
+    float o[EPP];
+#pragma unroll
+    for (int e = 0; e < EPP; ++e) {
+        float acc = bv;
+#pragma unroll
+        for (int i = 0; i < K; ++i)
+            acc = fmaf(wd[i], win[HP * EPP + e - i], acc);
+        o[e] = p.silu ? silu_f(acc) : acc;
+    }
+    T *orow = static_cast<T *>(p.out) + row * p.L;
+    if (p.vec && t0 + EPP <= p.L) {
+        Io<T>::storevec(orow + t0, o);
+    } else {
+#pragma unroll
+        for (int e = 0; e < EPP; ++e)
+            if (t0 + e < p.L)
+                Io<T>::store1(orow + t0 + e, o[e]);
+    }
+
+    // the piece holding the last input writes the history for the next call
+    if (K > 1 && p.state_out && t0 <= p.L - 1 && p.L - 1 < t0 + EPP) {
+        T *so = static_cast<T *>(p.state_out);
+#pragma unroll
+        for (int j = 0; j < K - 1; ++j) {
+            const int64_t t = p.L - (K - 1) + j;
+            float val = 0.0f;
+            if (t >= 0)
+                val = Io<T>::load1(xr + t);
+            else if (p.state_in)
+                val = Io<T>::load1(static_cast<const T *>(p.state_in) + (b * (K - 1) + (K - 1 + t)) * p.d_inner + d);
+            Io<T>::store1(so + (b * (K - 1) + j) * p.d_inner + d, val);
+        }
+    }
+}
+
+// One decode step of the convolution: the k-1 cached inputs (oldest first)
+// and the new input give the output; the cache then drops its oldest entry
+// and takes the new input ("Decoding with a constant-size cache").
+struct ConvStepParams {
+    void *state;
+    const void *x;
+    const float *w, *bias;
+    void *out;
+    int64_t batch, d_inner;
+    int silu;
+};
+
+template <typename T, int K>
+__global__ void __launch_bounds__(kBlock)
+conv_state_update_kernel(const ConvStepParams p)
+{
+    const int64_t row = static_cast<int64_t>(blockIdx.x) * kBlock + threadIdx.x;
+    if (row >= p.batch * p.d_inner)
+        return;
+    const int64_t b = row / p.d_inner;
+    const int64_t d = row % p.d_inner;
+    T *st = static_cast<T *>(p.state);
+    float hist[K];   // hist[i]: input i steps back, hist[0] = the new input
+    hist[0] = Io<T>::load1(static_cast<const T *>(p.x) + row);
+#pragma unroll
+    for (int i = 1; i < K; ++i)
+        hist[i] = Io<T>::load1(st + (b * (K - 1) + (K - 1 - i)) * p.d_inner + d);
+    float acc = p.bias ? __ldg(p.bias + d) : 0.0f;
+#pragma unroll
+    for (int i = 0; i < K; ++i)
+        acc = fmaf(__ldg(p.w + d * K + i), hist[i], acc);
+    Io<T>::store1(static_cast<T *>(p.out) + row, p.silu ? silu_f(acc) : acc);
+#pragma unroll
+    for (int j = 0; j < K - 1; ++j)   // slot j takes the input (K-2-j) steps back
+        Io<T>::store1(st + (b * (K - 1) + j) * p.d_inner + d, hist[K - 2 - j]);
+}
+
 // ------------------------------------------------------------------ host side
 
 thread_local char g_err[512] = "";
@@ -1476,6 +1608,102 @@ ss_status state_update(float *state, const void *x, const void *delta, const flo
     return launch_update<T, 16>(p, stream);
 }
 
+template <typename T, int K>
+ss_status launch_conv(const ConvParams &p, cudaStream_t stream)
+{
+    constexpr int EPP = 16 / (int)sizeof(T);
+    const int64_t threads = p.batch * p.d_inner * ((p.L + EPP - 1) / EPP);
+    const int64_t blocks = (threads + kBlock - 1) / kBlock;
+    if (blocks > 0x7fffffff)
+        return fail(SS_ERR_DIM, "grid too large");
+    causal_conv1d_kernel<T, K><<<static_cast<unsigned>(blocks), kBlock, 0, stream>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return fail(SS_ERR_LAUNCH, "conv launch failed: %s", cudaGetErrorString(e));
+    return SS_OK;
+}
+
+template <typename T>
+ss_status causal_conv1d(const void *x, const float *w, const float *bias, const void *state_in, int silu, void *out,
+                        void *state_out, int64_t batch, int64_t d_inner, int64_t L, int64_t k, cudaStream_t stream)
+{
+    g_err[0] = '\0';
+    if (batch <= 0 || d_inner <= 0 || L <= 0)
+        return fail(SS_ERR_DIM, "sizes must be positive: batch=%lld d_inner=%lld L=%lld",
+                    (long long)batch, (long long)d_inner, (long long)L);
+    if (k < 1 || k > SS_MAX_CONV_K)
+        return fail(SS_ERR_DIM, "k=%lld outside [1, %d]", (long long)k, SS_MAX_CONV_K);
+    if (batch > (int64_t(1) << 40) / d_inner || batch * d_inner > (int64_t(1) << 50) / L)
+        return fail(SS_ERR_DIM, "element count overflows");
+    const PtrCheck list[] = {{x, "x", true}, {w, "w", true}, {out, "out", true}, {bias, "bias", false},
+                             {state_in, "state_in", false}, {state_out, "state_out", false}};
+    int dev = 0;
+    ss_status st = check_ptrs(list, static_cast<int>(sizeof(list) / sizeof(list[0])), &dev);
+    if (st != SS_OK)
+        return st;
+    ConvParams p;
+    p.x = x; p.state_in = k > 1 ? state_in : nullptr; p.w = w; p.bias = bias;
+    p.out = out; p.state_out = k > 1 ? state_out : nullptr;
+    p.batch = batch; p.d_inner = d_inner; p.L = L; p.silu = silu ? 1 : 0;
+    p.vec = ((L * static_cast<int64_t>(sizeof(T))) % 16 == 0) && aligned16(x) && aligned16(out);
+    switch (k) {
+    case 1: return launch_conv<T, 1>(p, stream);
+    case 2: return launch_conv<T, 2>(p, stream);
+    case 3: return launch_conv<T, 3>(p, stream);
+    case 4: return launch_conv<T, 4>(p, stream);
+    case 5: return launch_conv<T, 5>(p, stream);
+    case 6: return launch_conv<T, 6>(p, stream);
+    case 7: return launch_conv<T, 7>(p, stream);
+    default: return launch_conv<T, 8>(p, stream);
+    }
+}
+
+template <typename T, int K>
+ss_status launch_conv_step(const ConvStepParams &p, cudaStream_t stream)
+{
+    const int64_t blocks = (p.batch * p.d_inner + kBlock - 1) / kBlock;
+    if (blocks > 0x7fffffff)
+        return fail(SS_ERR_DIM, "grid too large");
+    conv_state_update_kernel<T, K><<<static_cast<unsigned>(blocks), kBlock, 0, stream>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return fail(SS_ERR_LAUNCH, "conv step launch failed: %s", cudaGetErrorString(e));
+    return SS_OK;
+}
+
+template <typename T>
+ss_status conv_state_update(void *state, const void *x, const float *w, const float *bias, int silu, void *out,
+                            int64_t batch, int64_t d_inner, int64_t k, cudaStream_t stream)
+{
+    g_err[0] = '\0';
+    if (batch <= 0 || d_inner <= 0)
+        return fail(SS_ERR_DIM, "sizes must be positive: batch=%lld d_inner=%lld", (long long)batch,
+                    (long long)d_inner);
+    if (k < 1 || k > SS_MAX_CONV_K)
+        return fail(SS_ERR_DIM, "k=%lld outside [1, %d]", (long long)k, SS_MAX_CONV_K);
+    if (batch > (int64_t(1) << 40) / d_inner)
+        return fail(SS_ERR_DIM, "element count overflows");
+    const PtrCheck list[] = {{x, "x", true}, {w, "w", true}, {out, "out", true},
+                             {state, "conv_state", k > 1}, {bias, "bias", false}};
+    int dev = 0;
+    ss_status st = check_ptrs(list, static_cast<int>(sizeof(list) / sizeof(list[0])), &dev);
+    if (st != SS_OK)
+        return st;
+    ConvStepParams p;
+    p.state = state; p.x = x; p.w = w; p.bias = bias; p.out = out;
+    p.batch = batch; p.d_inner = d_inner; p.silu = silu ? 1 : 0;
+    switch (k) {
+    case 1: return launch_conv_step<T, 1>(p, stream);
+    case 2: return launch_conv_step<T, 2>(p, stream);
+    case 3: return launch_conv_step<T, 3>(p, stream);
+    case 4: return launch_conv_step<T, 4>(p, stream);
+    case 5: return launch_conv_step<T, 5>(p, stream);
+    case 6: return launch_conv_step<T, 6>(p, stream);
+    case 7: return launch_conv_step<T, 7>(p, stream);
+    default: return launch_conv_step<T, 8>(p, stream);
+    }
+}
+
 }  // namespace
 
 // ------------------------------------------------------------------ C ABI
@@ -1513,6 +1741,33 @@ ss_status ss_state_update_f32(float *state, const float *x, const float *delta, 
                               int64_t batch, int64_t d_inner, int64_t N, cudaStream_t stream)
 {
     return state_update<float>(state, x, delta, A, B, C, D, z, y, batch, d_inner, N, stream);
+}
+
+ss_status ss_causal_conv1d_bf16(const ss_bf16 *x, const float *w, const float *bias, const ss_bf16 *state_in,
+                                int silu, ss_bf16 *out, ss_bf16 *state_out, int64_t batch, int64_t d_inner,
+                                int64_t L, int64_t k, cudaStream_t stream)
+{
+    return causal_conv1d<__nv_bfloat16>(x, w, bias, state_in, silu, out, state_out, batch, d_inner, L, k, stream);
+}
+
+ss_status ss_causal_conv1d_f32(const float *x, const float *w, const float *bias, const float *state_in, int silu,
+                               float *out, float *state_out, int64_t batch, int64_t d_inner, int64_t L, int64_t k,
+                               cudaStream_t stream)
+{
+    return causal_conv1d<float>(x, w, bias, state_in, silu, out, state_out, batch, d_inner, L, k, stream);
+}
+
+ss_status ss_conv_state_update_bf16(ss_bf16 *conv_state, const ss_bf16 *x, const float *w, const float *bias,
+                                    int silu, ss_bf16 *out, int64_t batch, int64_t d_inner, int64_t k,
+                                    cudaStream_t stream)
+{
+    return conv_state_update<__nv_bfloat16>(conv_state, x, w, bias, silu, out, batch, d_inner, k, stream);
+}
+
+ss_status ss_conv_state_update_f32(float *conv_state, const float *x, const float *w, const float *bias, int silu,
+                                   float *out, int64_t batch, int64_t d_inner, int64_t k, cudaStream_t stream)
+{
+    return conv_state_update<float>(conv_state, x, w, bias, silu, out, batch, d_inner, k, stream);
 }
 
 const char *ss_last_error(void) { return g_err; }

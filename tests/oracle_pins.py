@@ -253,6 +253,64 @@ def check_causality_linearity_chain(lib):
     np.testing.assert_allclose(fb, fs, rtol=1e-12, atol=1e-14)
 
 
+# ------------------------------------------------------------ causal conv1d
+
+def check_conv_impulse_and_silu(lib):
+    """The block's convolution weighs the input i steps back by w_i ("The
+    Mamba block"): an impulse at t0 gives w_i at t0 + i; SiLU(v) = v sigma(v)."""
+    rng = np.random.default_rng(31)
+    for k in (1, 2, 4, 7):
+        L, t0 = 20, 5
+        w = rng.normal(size=(3, k))
+        bias = rng.normal(size=3)
+        x = np.zeros((2, 3, L)); x[:, :, t0] = 1.0
+        out, _ = O.causal_conv1d(x, w, None, silu=False, threads=1, lib=lib)
+        want = np.zeros((2, 3, L))
+        want[:, :, t0:t0 + k] = w[None, :, :min(k, L - t0)]
+        np.testing.assert_allclose(out, want, atol=1e-15)
+        out, _ = O.causal_conv1d(x, w, bias, silu=True, threads=1, lib=lib)
+        pre = want + bias[None, :, None]
+        np.testing.assert_allclose(out, pre * expit(pre), rtol=1e-13, atol=1e-15)
+    # printed-value-free closed form: SiLU(1) = 1/(1+e^-1), SiLU(0) = 0
+    x = np.ones((1, 1, 1))
+    out, _ = O.causal_conv1d(x, np.array([[1.0]]), None, silu=True, threads=1, lib=lib)
+    assert abs(out[0, 0, 0] - 1.0 / (1.0 + math.exp(-1.0))) < 1e-15
+
+
+def check_conv_constant_input_and_zero_history(lib):
+    """Constant input c with zero history: partial sums of the taps for the
+    first k-1 steps, then c * sum(w)."""
+    k, L, c = 4, 9, 1.5
+    w = np.array([[0.5, -0.25, 0.125, 2.0]])
+    out, _ = O.causal_conv1d(np.full((1, 1, L), c), w, np.array([0.1]), silu=False, threads=1, lib=lib)
+    want = [c * w[0, :min(t + 1, k)].sum() + 0.1 for t in range(L)]
+    np.testing.assert_allclose(out[0, 0], want, rtol=1e-14)
+
+
+def check_conv_history_chain(lib):
+    """The decode cache holds the last k-1 inputs, oldest first; a sequence cut
+    in two with the cache carried equals one pass, and token-by-token steps
+    equal it too ("Decoding with a constant-size cache")."""
+    rng = np.random.default_rng(32)
+    for k in (2, 4, 5):
+        x = rng.normal(size=(2, 3, 23))
+        w = rng.normal(size=(3, k))
+        bias = rng.normal(size=3)
+        full, st_full = O.causal_conv1d(x, w, bias, threads=1, lib=lib)
+        for cut in (0, 1, k - 2, 11):
+            a, st = O.causal_conv1d(x[:, :, :cut], w, bias, threads=1, lib=lib)
+            b2, st2 = O.causal_conv1d(x[:, :, cut:], w, bias, state=st, threads=1, lib=lib)
+            np.testing.assert_allclose(np.concatenate([a, b2], axis=2), full, rtol=1e-14, atol=1e-15)
+            np.testing.assert_allclose(st2, st_full, atol=0)
+        # the cache is the last k-1 inputs, oldest first
+        np.testing.assert_array_equal(st_full, np.transpose(x[:, :, -(k - 1):], (0, 2, 1)))
+        st = None
+        for t in range(x.shape[2]):
+            o1, st = O.causal_conv1d(x[:, :, t:t + 1], w, bias, state=st, threads=1, lib=lib)
+            np.testing.assert_allclose(o1[:, :, 0], full[:, :, t], rtol=1e-14, atol=1e-15)
+
+
 ALL_CHECKS = [check_recurrence_example, check_softplus_values, check_gate_theorem,
               check_selective_copy_euler, check_impulse_response, check_mixing_matrix,
-              check_lti_convolution, check_zero_and_huge_step, check_causality_linearity_chain]
+              check_lti_convolution, check_zero_and_huge_step, check_causality_linearity_chain,
+              check_conv_impulse_and_silu, check_conv_constant_input_and_zero_history, check_conv_history_chain]

@@ -94,3 +94,18 @@ def test_binding_checks_shapes_before_calling():
     with pytest.raises(TypeError):
         binding.scan_fwd(x, x, torch.zeros(3, 4, dtype=torch.float64), torch.zeros(2, 4, 8),
                          torch.zeros(2, 4, 8))
+
+
+@pytest.mark.parametrize("sfx", ["bf16", "f32"])
+def test_conv_host_validation(lib, sfx):
+    one = ctypes.c_void_p(1)
+    fn = getattr(lib, "ss_causal_conv1d_" + sfx)
+    assert fn(one, one, None, None, 1, one, None, 1, 4, 16, 9, None) == -2
+    assert "k=9" in binding.last_error()
+    assert fn(one, one, None, None, 1, one, None, 1, 4, 16, 0, None) == -2
+    assert fn(None, one, None, None, 1, one, None, 1, 4, 16, 4, None) == -1
+    assert fn(one, one, None, None, 1, one, None, 0, 4, 16, 4, None) == -2
+    step = getattr(lib, "ss_conv_state_update_" + sfx)
+    assert step(None, one, one, None, 1, one, 2, 4, 4, None) == -1
+    assert "conv_state" in binding.last_error()
+    assert step(one, one, one, None, 1, one, 2, 4, 12, None) == -2

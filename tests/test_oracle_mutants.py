@@ -33,6 +33,14 @@ MUTANTS = {
     "B_one_step_late": [(WRITE, "double write = delta * B[(b * N + n) * L + (t > 0 ? t - 1 : 0)] * xr[t];")],
     "x_missing_in_write": [(WRITE, "double write = delta * B[(b * N + n) * L + t];")],
     "final_state_stale": [("final_state[r * N + n] = h[n];", "final_state[r * N + n] = h[n] * (L > 1 ? 0.5 : 1.0);")],
+    "conv_taps_reversed": [("acc += w[d * k + i] * v;", "acc += w[d * k + (k - 1 - i)] * v;")],
+    "conv_lag_off_by_one": [("const int64_t s = t - i;   /* input i steps back */",
+                             "const int64_t s = t - i - 1;")],
+    "conv_silu_before_bias": [("double acc = bias ? bias[d] : 0.0;", "double acc = 0.0;"),
+                              ("out[r * L + t] = silu ? acc * sigmoid(acc) : acc;",
+                               "out[r * L + t] = (silu ? acc * sigmoid(acc) : acc) + (bias ? bias[d] : 0.0);")],
+    "conv_history_newest_first": [("v = state[(b * (k - 1) + (k - 1 + s)) * d_inner + d];\n                else\n                    v = 0.0;\n                acc",
+                                   "v = state[(b * (k - 1) + (-1 - s)) * d_inner + d];\n                else\n                    v = 0.0;\n                acc")],
 }
 
 
