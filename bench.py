@@ -460,6 +460,17 @@ def ncu_case(args):
                                  z=tok["z"][t], y=y[t])
         torch.cuda.synchronize()
         return 0
+    if args.ncu_case == "conv":
+        spec, k = HEADLINE, 4
+        x = I.normal(spec.seed, 11, (spec.batch, spec.d_inner, spec.L), 1.0, torch.bfloat16).cuda()
+        w = I.normal(spec.seed, 12, (spec.d_inner, k), 0.5, torch.float32).cuda()
+        bias = I.normal(spec.seed, 13, (spec.d_inner,), 0.2, torch.float32).cuda()
+        out = torch.empty_like(x)
+        st = torch.empty((spec.batch, k - 1, spec.d_inner), dtype=x.dtype, device="cuda")
+        for _ in range(args.warmup + args.steps):
+            binding.causal_conv1d(x, w, bias, out=out, state_out=st)
+        torch.cuda.synchronize()
+        return 0
     spec = HEADLINE
     inp = I.make_scan_inputs(spec)
     g = {k: v.cuda() for k, v in inp.items() if k != "reset_pos"}
@@ -483,7 +494,7 @@ def main(argv=None):
     ap.add_argument("--headline-only", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-soak", action="store_true", help="skip the 1 s untimed soak before timing")
-    ap.add_argument("--ncu-case", choices=["scan", "decode"], default=None,
+    ap.add_argument("--ncu-case", choices=["scan", "decode", "conv"], default=None,
                     help="profiling case: warmup + steps launches of the headline scan (or of the decode "
                          "update, on the first warmup + steps tokens of the decode workload), nothing else")
     args = ap.parse_args(argv)

@@ -37,6 +37,7 @@
 #ifndef SS_SCAN_H
 #define SS_SCAN_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -179,6 +180,62 @@ ss_status ss_conv_state_update_bf16(ss_bf16 *conv_state, const ss_bf16 *x, const
 ss_status ss_conv_state_update_f32(float *conv_state, const float *x, const float *w,
                                    const float *bias, int silu, float *out, int64_t batch,
                                    int64_t d_inner, int64_t k, cudaStream_t stream);
+
+/*
+ * ss_scan_bwd_bf16 / ss_scan_bwd_f32 -- gradient of ss_scan_fwd_* (training).
+ *
+ * Defines: the backward pass of section "Why the scan must be fused"
+ * ("Mamba and selective state spaces"): the states are not stored by the
+ * forward pass; this call reloads the forward inputs and recomputes them, and
+ * runs the adjoint of the recurrence (itself a linear recurrence) in reverse.
+ * With g(z) = z sigmoid(z), s = sigmoid(z), per channel d and state n:
+ *   gy_t   = dout_t g(z_t)                  (dout_t when z == NULL)
+ *   lam_t  = exp(delta_{t+1} A) lam_{t+1} + C_t gy_t,  lam_{L-1} = dfinal + C_{L-1} gy_{L-1}
+ *   dx_t   = D gy_t + delta_t sum_n lam_t B_t
+ *   ddelta = (sum_n lam_t (A a_t h_{t-1} + B_t x_t)) * (sigmoid(delta_t + dt_bias) with softplus)
+ *   dA    += sum_t lam_t delta_t a_t h_{t-1}     dB_t += lam_t delta_t x_t
+ *   dC_t  += gy_t h_t                            dD   += sum_t gy_t x_t
+ *   dz_t   = dout_t y_t s (1 + z (1 - s)),  y_t the output before the gate
+ *   ddt_bias = sum_t ddelta_t,  dh0 = exp(delta_0 A) lam_0
+ * (a_t = exp(delta_t A); delta_t here is the step after bias and softplus.)
+ *
+ *   Inputs x .. delta_softplus : exactly as given to ss_scan_fwd_*.
+ *   h0          : (batch, d_inner, N) fp32 initial state, or NULL for zero.
+ *   dout        : (batch, d_inner, L) io dtype, gradient of y.
+ *   dfinal_state: (batch, d_inner, N) fp32 gradient of final_state, or NULL.
+ *   dx, ddelta  : (batch, d_inner, L) io dtype outputs; ddelta is the
+ *                 gradient of the raw `delta` input (and of delta + dt_bias).
+ *   dz          : (batch, d_inner, L) io dtype, or NULL (ignored if z NULL).
+ *   dA          : (d_inner, N) fp32.   dB, dC : (batch, N, L) fp32.
+ *   dD, ddt_bias: (d_inner) fp32, or NULL to skip (dD ignored if D NULL).
+ *   dh0         : (batch, d_inner, N) fp32, or NULL to skip.
+ *   workspace   : device scratch of at least ss_scan_bwd_workspace_bytes(...)
+ *                 bytes, 16-byte aligned, owned by the caller; it holds the
+ *                 state at every 16th step between the forward and reverse
+ *                 walks and may be reused after the call's work completes.
+ *   1 <= N <= 32.
+ * dA, dB, dC, dD and ddt_bias are cleared on `stream` and accumulated with
+ * fp32 atomic adds, so their last bits may differ between runs.
+ * Errors: as ss_scan_fwd_* (SS_ERR_N for N > 32; SS_ERR_DIM also for a
+ * workspace that is too small or misaligned).
+ */
+size_t ss_scan_bwd_workspace_bytes(int64_t batch, int64_t d_inner, int64_t L, int64_t N);
+
+ss_status ss_scan_bwd_bf16(const ss_bf16 *x, const ss_bf16 *delta, const float *A, const ss_bf16 *B,
+                           const ss_bf16 *C, const float *D, const ss_bf16 *z, const float *dt_bias,
+                           int delta_softplus, const float *h0, const ss_bf16 *dout,
+                           const float *dfinal_state, ss_bf16 *dx, ss_bf16 *ddelta, float *dA, float *dB,
+                           float *dC, float *dD, ss_bf16 *dz, float *ddt_bias, float *dh0,
+                           void *workspace, size_t workspace_bytes, int64_t batch, int64_t d_inner,
+                           int64_t L, int64_t N, cudaStream_t stream);
+
+ss_status ss_scan_bwd_f32(const float *x, const float *delta, const float *A, const float *B,
+                          const float *C, const float *D, const float *z, const float *dt_bias,
+                          int delta_softplus, const float *h0, const float *dout,
+                          const float *dfinal_state, float *dx, float *ddelta, float *dA, float *dB,
+                          float *dC, float *dD, float *dz, float *ddt_bias, float *dh0, void *workspace,
+                          size_t workspace_bytes, int64_t batch, int64_t d_inner, int64_t L, int64_t N,
+                          cudaStream_t stream);
 
 /* Message describing the last non-OK status returned on this host thread
  * ("" if none). The string is owned by the library. */

@@ -7,6 +7,8 @@ does. Nothing here imports the CUDA library or its binding.
 * ``scan`` / ``scan_rows`` run the plain float64 loop of ``ss_oracle.c`` over
   all rows or over a sample of rows, in parallel over rows (the C call releases
   the GIL).
+* ``scan_bwd`` is the gradient of the scan by the chain rule (float64; the
+  states are kept, the reverse recurrence is run literally).
 * ``causal_conv1d`` is the block's causal depthwise convolution (+ SiLU)
   with an optional carried history of k-1 inputs, in float64.
 * ``decode_chain`` runs that same loop over consecutive single-token inputs:
@@ -54,6 +56,9 @@ def load(path: str | None = None):
     lib.oracle_softplus.restype = ctypes.c_double
     lib.oracle_scan_rows.argtypes = [dp] * 8 + [ctypes.c_int, dp, dp, dp] + [ctypes.c_int64] * 6
     lib.oracle_scan_rows.restype = ctypes.c_int
+    if hasattr(lib, "oracle_scan_bwd_rows"):
+        lib.oracle_scan_bwd_rows.argtypes = [dp] * 8 + [ctypes.c_int] + [dp] * 12 + [ctypes.c_int64] * 6
+        lib.oracle_scan_bwd_rows.restype = ctypes.c_int
     if hasattr(lib, "oracle_causal_conv1d_rows"):
         lib.oracle_causal_conv1d_rows.argtypes = [dp, dp, dp, ctypes.c_int, dp, dp, dp] + [ctypes.c_int64] * 6
         lib.oracle_causal_conv1d_rows.restype = ctypes.c_int
@@ -118,6 +123,54 @@ def scan(x, dt, A, B, C, D=None, z=None, dt_bias=None, delta_softplus=True, h0=N
     if any(c != 0 for c in codes):
         raise RuntimeError("oracle_scan_rows failed: %r" % (codes,))
     return y, fs
+
+
+def scan_bwd(x, dt, A, B, C, dout, D=None, z=None, dt_bias=None, delta_softplus=True, h0=None,
+             dfinal=None, threads: int | None = None, lib=None):
+    """Gradient of the selective scan in float64 (``oracle_scan_bwd_rows``).
+
+    Same inputs as ``scan`` plus dout (batch, d_inner, L), the gradient of the
+    (gated) output, and dfinal (batch, d_inner, N) or None, the gradient of the
+    final state. Returns a dict of float64 arrays: dx, ddt (of the raw step
+    input dt), dz (None without z), dA, dB, dC, dD (None without D), ddt_bias
+    (None without dt_bias) and dh0 (gradient of the initial state).
+    """
+    lib = lib or load()
+    x, dt, A, B, C, dout = map(_f64, (x, dt, A, B, C, dout))
+    D, z, dt_bias, h0, dfinal = map(_f64, (D, z, dt_bias, h0, dfinal))
+    batch, d_inner, L = x.shape
+    N = A.shape[1]
+    assert dt.shape == x.shape and dout.shape == x.shape
+    assert B.shape == (batch, N, L) and C.shape == (batch, N, L) and A.shape == (d_inner, N)
+    dx = np.empty_like(x)
+    ddt = np.empty_like(x)
+    dz = np.empty_like(x) if z is not None else None
+    dh0 = np.empty((batch, d_inner, N))
+    rows = batch * d_inner
+    nt = max(1, min(threads or default_threads(), rows)) if rows else 1
+    bounds = [(rows * i) // nt for i in range(nt + 1)]
+    acc = [dict(dA=np.zeros((d_inner, N)), dB=np.zeros((batch, N, L)), dC=np.zeros((batch, N, L)),
+                dD=np.zeros(d_inner), ddt_bias=np.zeros(d_inner)) for _ in range(nt)]
+
+    def run(i):
+        a = acc[i]
+        return lib.oracle_scan_bwd_rows(_ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
+                                        _ptr(dt_bias), int(bool(delta_softplus)), _ptr(h0), _ptr(dout),
+                                        _ptr(dfinal), _ptr(dx), _ptr(ddt), _ptr(dz), _ptr(a["dA"]),
+                                        _ptr(a["dB"]), _ptr(a["dC"]), _ptr(a["dD"]), _ptr(a["ddt_bias"]),
+                                        _ptr(dh0), batch, d_inner, L, N, bounds[i], bounds[i + 1])
+
+    if nt == 1:
+        codes = [run(0)]
+    else:
+        with ThreadPoolExecutor(nt) as ex:
+            codes = list(ex.map(run, range(nt)))
+    if any(c != 0 for c in codes):
+        raise RuntimeError("oracle_scan_bwd_rows failed: %r" % (codes,))
+    tot = {k: sum(a[k] for a in acc) for k in acc[0]}
+    return dict(dx=dx, ddt=ddt, dz=dz, dA=tot["dA"], dB=tot["dB"], dC=tot["dC"],
+                dD=tot["dD"] if D is not None else None,
+                ddt_bias=tot["ddt_bias"] if dt_bias is not None else None, dh0=dh0)
 
 
 def scan_rows(inp: dict, rows, delta_softplus=True, use_D=True, use_z=True, use_bias=True,

@@ -165,3 +165,126 @@ int oracle_causal_conv1d_rows(const double *xin, const double *w, const double *
     }
     return 0;
 }
+
+/*
+ * Gradient of the selective scan (oracle_scan_rows) by the chain rule, run as
+ * the pages describe the backward pass ("Mamba and selective state spaces",
+ * section "Why the scan must be fused": the states are recomputed from the
+ * inputs, and the backward of a linear recurrence is a linear recurrence run
+ * in reverse). The formulas are derived here; the pages do not print them.
+ *
+ * With g(z) = z sigmoid(z) and, per row (b, d) and state n,
+ *   a_t = exp(delta_t A_n),  h_t = a_t h_{t-1} + delta_t B_t x_t,
+ *   y_t = sum_n C_t h_t + D x_t,  out_t = y_t g(z_t),
+ * and the incoming gradients dout_t (of out) and dh_L (of the final state):
+ *   gy_t     = dout_t g(z_t)                       (dout_t without the gate)
+ *   dz_t     = dout_t y_t g'(z_t),  g'(z) = s (1 + z (1 - s)), s = sigmoid(z)
+ *   lam_{L-1} = dh_L + C_{L-1} gy_{L-1},  lam_t = a_{t+1} lam_{t+1} + C_t gy_t
+ *   dx_t     = D gy_t + sum_n lam_t delta_t B_t
+ *   ddelta_t = sum_n lam_t (A_n a_t h_{t-1} + B_t x_t)
+ *   dA_n    += sum_t lam_t delta_t a_t h_{t-1}
+ *   dB_t[n] += lam_t delta_t x_t          (summed over the channels d)
+ *   dC_t[n] += gy_t h_t                   (summed over the channels d)
+ *   dD      += sum_t gy_t x_t
+ *   ddt_t    = ddelta_t sigmoid(v_t) with softplus, ddelta_t without
+ *   ddt_bias += sum_t ddt_t
+ *   dh0[n]   = a_0 lam_0                  (gradient of the initial state)
+ *
+ * Per-row outputs dx, ddt, dz (batch, d_inner, L) and dh0 (batch, d_inner, N)
+ * are written; dA (d_inner, N), dB, dC (batch, N, L), dD and ddt_bias
+ * (d_inner) are ADDED to (the caller zeroes them). dz, dD, ddt_bias, dh0,
+ * dfinal and h0 may be NULL. All states of a row are kept (L x N doubles):
+ * this is the plain reference, not the recomputing kernel.
+ */
+int oracle_scan_bwd_rows(const double *x, const double *dt, const double *A,
+                         const double *B, const double *C, const double *D,
+                         const double *z, const double *dt_bias, int delta_softplus,
+                         const double *h0, const double *dout, const double *dfinal,
+                         double *dx, double *ddt, double *dz, double *dA, double *dB,
+                         double *dC, double *dD, double *ddt_bias, double *dh0,
+                         int64_t batch, int64_t d_inner, int64_t L, int64_t N,
+                         int64_t row_begin, int64_t row_end)
+{
+    if (!x || !dt || !A || !B || !C || !dout || !dx || !ddt || !dA || !dB || !dC)
+        return -1;
+    if (batch < 0 || d_inner < 0 || L < 1 || N <= 0)
+        return -1;
+    if (row_begin < 0 || row_end > batch * d_inner || row_begin > row_end)
+        return -1;
+
+    double *hs = (double *)malloc((size_t)(L + 1) * N * sizeof(double)); /* hs[t+1] = h_t, hs[0] = h_{-1} */
+    double *as = (double *)malloc((size_t)L * N * sizeof(double));
+    double *del = (double *)malloc((size_t)L * sizeof(double));
+    double *lam = (double *)malloc((size_t)N * sizeof(double));
+    if (!hs || !as || !del || !lam) {
+        free(hs); free(as); free(del); free(lam);
+        return -2;
+    }
+
+    for (int64_t r = row_begin; r < row_end; ++r) {
+        const int64_t b = r / d_inner;
+        const int64_t d = r % d_inner;
+        const double *xr = x + r * L;
+        const double *dtr = dt + r * L;
+        const double *zr = z ? z + r * L : NULL;
+        const double *gr = dout + r * L;
+        const double Dd = D ? D[d] : 0.0;
+
+        /* forward, keeping every state */
+        for (int64_t n = 0; n < N; ++n)
+            hs[n] = h0 ? h0[r * N + n] : 0.0;
+        for (int64_t t = 0; t < L; ++t) {
+            const double v = dtr[t] + (dt_bias ? dt_bias[d] : 0.0);
+            del[t] = delta_softplus ? oracle_softplus(v) : v;
+            for (int64_t n = 0; n < N; ++n) {
+                const double a = exp(del[t] * A[d * N + n]);
+                as[t * N + n] = a;
+                hs[(t + 1) * N + n] = a * hs[t * N + n] + del[t] * B[(b * N + n) * L + t] * xr[t];
+            }
+        }
+
+        /* reverse */
+        for (int64_t n = 0; n < N; ++n)
+            lam[n] = dfinal ? dfinal[r * N + n] : 0.0;
+        for (int64_t t = L - 1; t >= 0; --t) {
+            double y = Dd * xr[t];
+            for (int64_t n = 0; n < N; ++n)
+                y += C[(b * N + n) * L + t] * hs[(t + 1) * N + n];
+            double gy = gr[t];
+            if (zr) {
+                const double s = sigmoid(zr[t]);
+                gy = gr[t] * zr[t] * s;
+                if (dz)
+                    dz[r * L + t] = gr[t] * y * s * (1.0 + zr[t] * (1.0 - s));
+            }
+            double dxt = Dd * gy;
+            double ddel = 0.0;
+            for (int64_t n = 0; n < N; ++n) {
+                const double Bn = B[(b * N + n) * L + t];
+                const double Cn = C[(b * N + n) * L + t];
+                if (t < L - 1)
+                    lam[n] *= as[(t + 1) * N + n];
+                lam[n] += Cn * gy;
+                const double ah = as[t * N + n] * hs[t * N + n];  /* a_t h_{t-1} */
+                dxt += lam[n] * del[t] * Bn;
+                ddel += lam[n] * (A[d * N + n] * ah + Bn * xr[t]);
+                dA[d * N + n] += lam[n] * del[t] * ah;
+                dB[(b * N + n) * L + t] += lam[n] * del[t] * xr[t];
+                dC[(b * N + n) * L + t] += gy * hs[(t + 1) * N + n];
+            }
+            dx[r * L + t] = dxt;
+            const double v = dtr[t] + (dt_bias ? dt_bias[d] : 0.0);
+            const double dv = delta_softplus ? ddel * sigmoid(v) : ddel;
+            ddt[r * L + t] = dv;
+            if (ddt_bias)
+                ddt_bias[d] += dv;
+            if (dD)
+                dD[d] += gy * xr[t];
+        }
+        if (dh0)
+            for (int64_t n = 0; n < N; ++n)
+                dh0[r * N + n] = as[n] * lam[n];
+    }
+    free(hs); free(as); free(del); free(lam);
+    return 0;
+}

@@ -19,7 +19,8 @@ LIB_PATH = os.path.join(_PKG, "libssscan.so")
 # names declared in include/ss_scan.h
 EXPORTS = ("ss_scan_fwd_bf16", "ss_scan_fwd_f32", "ss_state_update_bf16", "ss_state_update_f32",
            "ss_causal_conv1d_bf16", "ss_causal_conv1d_f32", "ss_conv_state_update_bf16",
-           "ss_conv_state_update_f32", "ss_last_error", "ss_abi_version")
+           "ss_conv_state_update_f32", "ss_scan_bwd_bf16", "ss_scan_bwd_f32", "ss_scan_bwd_workspace_bytes",
+           "ss_last_error", "ss_abi_version")
 
 STATUS = {0: "SS_OK", -1: "SS_ERR_NULL", -2: "SS_ERR_DIM", -3: "SS_ERR_N", -4: "SS_ERR_DEVICE_PTR",
           -5: "SS_ERR_LAUNCH", -6: "SS_ERR_INTERNAL"}
@@ -59,6 +60,11 @@ def lib() -> ctypes.CDLL:
     for name in ("ss_conv_state_update_bf16", "ss_conv_state_update_f32"):
         getattr(L, name).argtypes = [vp, vp, vp, vp, ci, vp, i64, i64, i64, vp]
         getattr(L, name).restype = ci
+    for name in ("ss_scan_bwd_bf16", "ss_scan_bwd_f32"):
+        getattr(L, name).argtypes = [vp] * 8 + [ci] + [vp] * 13 + [ctypes.c_size_t] + [i64] * 4 + [vp]
+        getattr(L, name).restype = ci
+    L.ss_scan_bwd_workspace_bytes.argtypes = [i64] * 4
+    L.ss_scan_bwd_workspace_bytes.restype = ctypes.c_size_t
     L.ss_last_error.argtypes = []
     L.ss_last_error.restype = ctypes.c_char_p
     L.ss_abi_version.argtypes = []
@@ -209,3 +215,58 @@ def conv_state_update(conv_state, x, w, bias=None, silu=True, out=None, stream=N
     _check(fn(_ptr(conv_state), _ptr(x), _ptr(w), _ptr(bias), int(bool(silu)), _ptr(out), batch, d_inner, k,
               _stream(stream)))
     return out
+
+
+def scan_bwd_workspace_bytes(batch, d_inner, L, N) -> int:
+    """Bytes of device scratch ``scan_bwd`` needs (0 for unsupported sizes)."""
+    return int(lib().ss_scan_bwd_workspace_bytes(batch, d_inner, L, N))
+
+
+def scan_bwd(x, delta, A, B, C, dout, D=None, z=None, dt_bias=None, delta_softplus=True, h0=None,
+             dfinal_state=None, grads=None, workspace=None, stream=None):
+    """Gradient of ``scan_fwd`` (see ``ss_scan_bwd_*``): the forward inputs,
+    dout (batch, d_inner, L) in the io dtype and optionally dfinal_state
+    (batch, d_inner, N) fp32. ``grads`` may hold preallocated outputs under the
+    names below; missing ones are allocated. ``workspace`` is a uint8 device
+    tensor of at least ``scan_bwd_workspace_bytes`` bytes (allocated when None).
+
+    Returns a dict: dx, ddelta, dz (io dtype; dz None without z), dA, dB, dC,
+    dD, ddt_bias, dh0 (fp32; dD / ddt_bias None without D / dt_bias, dh0 None
+    without h0)."""
+    io = x.dtype
+    sfx = _io_suffix(io)
+    batch, d_inner, L = x.shape
+    N = A.shape[1] if A.dim() == 2 else -1
+    for t, n, dt_, shp in ((delta, "delta", io, x.shape), (z, "z", io, x.shape), (dout, "dout", io, x.shape),
+                           (B, "B", io, (batch, N, L)), (C, "C", io, (batch, N, L)),
+                           (A, "A", torch.float32, (d_inner, N)), (D, "D", torch.float32, (d_inner,)),
+                           (dt_bias, "dt_bias", torch.float32, (d_inner,)),
+                           (h0, "h0", torch.float32, (batch, d_inner, N)),
+                           (dfinal_state, "dfinal_state", torch.float32, (batch, d_inner, N))):
+        _need(t, n, dt_, shp)
+    g = dict(grads or {})
+    dev = x.device
+    shapes = {"dx": (io, x.shape), "ddelta": (io, x.shape), "dA": (torch.float32, (d_inner, N)),
+              "dB": (torch.float32, (batch, N, L)), "dC": (torch.float32, (batch, N, L))}
+    if z is not None:
+        shapes["dz"] = (io, x.shape)
+    if D is not None:
+        shapes["dD"] = (torch.float32, (d_inner,))
+    if dt_bias is not None:
+        shapes["ddt_bias"] = (torch.float32, (d_inner,))
+    if h0 is not None:
+        shapes["dh0"] = (torch.float32, (batch, d_inner, N))
+    for k, (dt_, shp) in shapes.items():
+        if g.get(k) is None:
+            g[k] = torch.empty(shp, dtype=dt_, device=dev)
+        _need(g[k], k, dt_, shp)
+    need = scan_bwd_workspace_bytes(batch, d_inner, L, N)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    fn = getattr(lib(), "ss_scan_bwd_" + sfx)
+    _check(fn(_ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(dt_bias),
+              int(bool(delta_softplus)), _ptr(h0), _ptr(dout), _ptr(dfinal_state), _ptr(g["dx"]),
+              _ptr(g["ddelta"]), _ptr(g["dA"]), _ptr(g["dB"]), _ptr(g["dC"]), _ptr(g.get("dD")),
+              _ptr(g.get("dz")), _ptr(g.get("ddt_bias")), _ptr(g.get("dh0")), _ptr(workspace),
+              workspace.numel() * workspace.element_size(), batch, d_inner, L, N, _stream(stream)))
+    return {k: g.get(k) for k in ("dx", "ddelta", "dz", "dA", "dB", "dC", "dD", "ddt_bias", "dh0")}

@@ -43,6 +43,8 @@ _BLOCK = 1 << 22
 
 # tensor tags in draw order
 TAG_X, TAG_Z, TAG_B, TAG_C, TAG_DT, TAG_U, TAG_EPS, TAG_RESET = 1, 2, 3, 4, 5, 6, 7, 8
+# incoming gradients and initial state of the backward workloads
+TAG_DOUT, TAG_DFINAL, TAG_H0 = 9, 10, 11
 
 _POOL_THREADS = max(1, min(16, len(os.sched_getaffinity(0))))
 
@@ -244,3 +246,13 @@ def make_decode_tokens(spec: DecodeSpec, steps: int | None = None) -> dict:
         with ThreadPoolExecutor(_POOL_THREADS) as ex:
             list(ex.map(one, range(nblk)))
     return dict(x=x, delta=delta, z=z, B=B, C=C)
+
+
+def make_bwd_inputs(spec: ScanSpec) -> dict:
+    """Incoming gradients for a scan workload, all N(0, 1): dout (batch,
+    d_inner, L) in the io dtype and dfinal (batch, d_inner, N) float32, plus an
+    initial state h0 (batch, d_inner, N) float32 for the initial-state cases."""
+    Bt, Dn, L, N, s = spec.batch, spec.d_inner, spec.L, spec.N, spec.seed
+    return dict(dout=normal(s, TAG_DOUT, (Bt, Dn, L), 1.0, spec.torch_dtype),
+                dfinal=normal(s, TAG_DFINAL, (Bt, Dn, N), 1.0, torch.float32),
+                h0=normal(s, TAG_H0, (Bt, Dn, N), 1.0, torch.float32))

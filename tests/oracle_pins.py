@@ -310,7 +310,95 @@ def check_conv_history_chain(lib):
             np.testing.assert_allclose(o1[:, :, 0], full[:, :, t], rtol=1e-14, atol=1e-15)
 
 
+def _bwd_problem(rng, bt=2, dn=3, L=9, N=4):
+    return dict(x=rng.normal(size=(bt, dn, L)), dt=rng.normal(size=(bt, dn, L)) * 0.5,
+                A=-rng.uniform(0.2, 2.0, size=(dn, N)), B=rng.normal(size=(bt, N, L)),
+                C=rng.normal(size=(bt, N, L)), D=rng.normal(size=dn), z=rng.normal(size=(bt, dn, L)),
+                dt_bias=rng.normal(size=dn) * 0.3, h0=rng.normal(size=(bt, dn, N)))
+
+
+def check_bwd_finite_differences(lib):
+    """The gradient equals the derivative of the forward scan: central
+    differences of <dout, out> + <dfinal, final_state> in every input, with
+    every option on, and with softplus, gate, skip and bias off."""
+    rng = np.random.default_rng(41)
+    eps = 1e-6
+    for full in (True, False):
+        p = _bwd_problem(rng)
+        if not full:
+            p.update(D=None, z=None, dt_bias=None)
+            p["dt"] = np.abs(p["dt"]) + 0.05   # a positive step without softplus
+        dout = rng.normal(size=p["x"].shape)
+        dfin = rng.normal(size=p["h0"].shape)
+
+        def loss(**over):
+            q = dict(p, **over)
+            y, fs = O.scan(q["x"], q["dt"], q["A"], q["B"], q["C"], D=q["D"], z=q["z"], dt_bias=q["dt_bias"],
+                           delta_softplus=full, h0=q["h0"], threads=1, lib=lib)
+            return float((y * dout).sum() + (fs * dfin).sum())
+
+        g = O.scan_bwd(p["x"], p["dt"], p["A"], p["B"], p["C"], dout, D=p["D"], z=p["z"], dt_bias=p["dt_bias"],
+                       delta_softplus=full, h0=p["h0"], dfinal=dfin, threads=1, lib=lib)
+        names = [("x", "dx"), ("dt", "ddt"), ("A", "dA"), ("B", "dB"), ("C", "dC"), ("h0", "dh0")]
+        if full:
+            names += [("D", "dD"), ("z", "dz"), ("dt_bias", "ddt_bias")]
+        for name, gk in names:
+            arr = p[name]
+            fd = np.zeros_like(arr)
+            for i in np.ndindex(arr.shape):
+                hi, lo = arr.copy(), arr.copy()
+                hi[i] += eps
+                lo[i] -= eps
+                fd[i] = (loss(**{name: hi}) - loss(**{name: lo})) / (2 * eps)
+            np.testing.assert_allclose(g[gk], fd, rtol=1e-6, atol=1e-6, err_msg=name)
+
+
+def check_bwd_impulse_closed_form(lib):
+    """One state, constant step, an impulse x = (1, 0, ...), B = C = 1, no
+    softplus, no gate: y_T = e^{A (delta_1 + ... + delta_T)} delta_0, so
+    d y_T / dA = T delta^2 e^{T delta A}, d y_T / d delta_0 = e^{T delta A},
+    d y_T / d delta_s = A delta e^{T delta A} (1 <= s <= T), dB_0 = dx_0 =
+    delta e^{T delta A}, dC_T = y_T, and nothing reaches steps after T."""
+    A, dl, L = -0.7, 0.3, 12
+    for T in (0, 1, 5, 11):
+        x = np.zeros((1, 1, L))
+        x[0, 0, 0] = 1.0
+        dt = np.full((1, 1, L), dl)
+        ones = np.ones((1, 1, L))
+        dout = np.zeros((1, 1, L))
+        dout[0, 0, T] = 1.0
+        g = O.scan_bwd(x, dt, np.array([[A]]), ones, ones, dout, delta_softplus=False, threads=1, lib=lib)
+        e = math.exp(T * dl * A)
+        want_ddt = np.zeros(L)
+        want_ddt[0] = e
+        want_ddt[1:T + 1] = A * dl * e
+        np.testing.assert_allclose(g["dA"][0, 0], T * dl * dl * e, rtol=1e-13, atol=1e-15)
+        np.testing.assert_allclose(g["ddt"][0, 0], want_ddt, rtol=1e-13, atol=1e-15)
+        np.testing.assert_allclose(g["dB"][0, 0, 0], dl * e, rtol=1e-13)
+        np.testing.assert_allclose(g["dx"][0, 0, 0], dl * e, rtol=1e-13)
+        np.testing.assert_allclose(g["dC"][0, 0, T], dl * e, rtol=1e-13)
+        assert not g["dC"][0, 0, T + 1:].any() and not g["dB"][0, 0, T + 1:].any()
+        np.testing.assert_allclose(g["dh0"][0, 0, 0], math.exp((T + 1) * dl * A), rtol=1e-13)
+
+
+def check_bwd_linear_in_cotangent(lib):
+    """The gradient is linear in the incoming gradients (dout, dfinal)."""
+    rng = np.random.default_rng(43)
+    p = _bwd_problem(rng, L=7)
+    d1, d2 = rng.normal(size=p["x"].shape), rng.normal(size=p["x"].shape)
+    f1, f2 = rng.normal(size=p["h0"].shape), rng.normal(size=p["h0"].shape)
+
+    def grad(do, df):
+        return O.scan_bwd(p["x"], p["dt"], p["A"], p["B"], p["C"], do, D=p["D"], z=p["z"], dt_bias=p["dt_bias"],
+                          h0=p["h0"], dfinal=df, threads=1, lib=lib)
+
+    g1, g2, g12 = grad(d1, f1), grad(d2, f2), grad(2.0 * d1 - 3.0 * d2, 2.0 * f1 - 3.0 * f2)
+    for k in ("dx", "ddt", "dz", "dA", "dB", "dC", "dD", "ddt_bias", "dh0"):
+        np.testing.assert_allclose(g12[k], 2.0 * g1[k] - 3.0 * g2[k], rtol=1e-10, atol=1e-12, err_msg=k)
+
+
 ALL_CHECKS = [check_recurrence_example, check_softplus_values, check_gate_theorem,
               check_selective_copy_euler, check_impulse_response, check_mixing_matrix,
               check_lti_convolution, check_zero_and_huge_step, check_causality_linearity_chain,
-              check_conv_impulse_and_silu, check_conv_constant_input_and_zero_history, check_conv_history_chain]
+              check_conv_impulse_and_silu, check_conv_constant_input_and_zero_history, check_conv_history_chain,
+              check_bwd_finite_differences, check_bwd_impulse_closed_form, check_bwd_linear_in_cotangent]

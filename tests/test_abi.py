@@ -109,3 +109,31 @@ def test_conv_host_validation(lib, sfx):
     assert step(None, one, one, None, 1, one, 2, 4, 4, None) == -1
     assert "conv_state" in binding.last_error()
     assert step(one, one, one, None, 1, one, 2, 4, 12, None) == -2
+
+
+@pytest.mark.parametrize("sfx", ["bf16", "f32"])
+def test_bwd_host_validation(lib, sfx):
+    one = ctypes.c_void_p(1)
+    fn = getattr(lib, "ss_scan_bwd_" + sfx)
+
+    def call(x=one, ws=one, ws_bytes=1 << 40, batch=2, d=4, L=16, N=16, dout=one):
+        return fn(x, one, one, one, one, None, None, None, 1, None, dout, None, one, one, one, one, one,
+                  None, None, None, None, ws, ws_bytes, batch, d, L, N, None)
+
+    assert call(batch=0) == -2
+    assert call(N=33) == -3
+    assert "N=33" in binding.last_error()
+    assert call(x=None) == -1
+    assert call(dout=None) == -1
+    assert "dout" in binding.last_error()
+    assert call(ws=None) == -1
+    assert "workspace" in binding.last_error()
+
+
+def test_bwd_workspace_size(lib):
+    ws = binding.scan_bwd_workspace_bytes
+    # one 16-byte state group (4 states) per channel and batch row at every 16th step
+    assert ws(8, 1536, 2048, 16) == 8 * 1536 * (2048 // 16) * 4 * 16
+    assert ws(1, 1, 17, 1) == 2 * 16
+    assert ws(2, 3, 16, 20) == 2 * 3 * 1 * 8 * 16
+    assert ws(1, 1, 1, 33) == 0 and ws(0, 1, 1, 1) == 0

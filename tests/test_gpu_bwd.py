@@ -1,0 +1,132 @@
+"""Backward pass of the scan (states recomputed on the GPU) against the
+float64 oracle's chain-rule gradient on the same inputs, every output element
+by element."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import oracle as O
+from selective_state_space_138_b300 import binding
+from selective_state_space_138_b300 import inputs as I
+
+pytestmark = pytest.mark.gpu
+
+# |gpu - ref| <= RTOL |ref| + ATOL_REL rms(ref), per element. io-dtype outputs
+# (dx, ddelta, dz) are rounded once to the io dtype; the fp32 sums (dA, dB,
+# dC, dD, ddt_bias, dh0) carry fp32 rounding of long sums whose terms cancel,
+# hence the scale term.
+GTOL = {torch.bfloat16: {"io": (2e-2, 2e-3), "f32": (2e-3, 2e-4)},
+        torch.float32: {"io": (1e-4, 1e-5), "f32": (1e-4, 1e-5)}}
+IO_KEYS = ("dx", "ddelta", "dz")
+
+
+def assert_grad_close(got, ref, io_dtype, key):
+    rtol, arel = GTOL[io_dtype]["io" if key in IO_KEYS else "f32"]
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape, (key, got.shape, ref.shape)
+    assert np.all(np.isfinite(got)), "%s: non-finite GPU output" % key
+    scale = float(np.sqrt(np.mean(ref * ref))) if ref.size else 0.0
+    err = np.abs(got - ref) / (rtol * np.abs(ref) + arel * scale + 1e-30)
+    worst = np.unravel_index(np.argmax(err), err.shape)
+    assert err.max() <= 1.0, "%s: normalised error %.3f at %s (gpu %r, oracle %r, rms %g)" % (
+        key, err.max(), worst, got[worst], ref[worst], scale)
+    return float(err.max())
+
+
+def run_case(spec, use_D=True, use_z=True, use_bias=True, softplus=True, use_h0=False, use_dfinal=True):
+    inp = I.make_scan_inputs(spec)
+    if not softplus and not use_bias:
+        # without softplus and bias the raw step is the step: keep it positive
+        # (a negative step makes the recurrence grow without bound)
+        inp["dt"] = (inp["dt"].float().abs() + 0.05).to(inp["dt"].dtype)
+    bw = I.make_bwd_inputs(spec)
+    g = {k: inp[k].cuda() for k in ("x", "dt", "z", "B", "C", "A", "D", "dt_bias")}
+    h0 = bw["h0"] if use_h0 else None
+    dfin = bw["dfinal"] if use_dfinal else None
+    got = binding.scan_bwd(g["x"], g["dt"], g["A"], g["B"], g["C"], bw["dout"].cuda(),
+                           D=g["D"] if use_D else None, z=g["z"] if use_z else None,
+                           dt_bias=g["dt_bias"] if use_bias else None, delta_softplus=softplus,
+                           h0=None if h0 is None else h0.cuda(),
+                           dfinal_state=None if dfin is None else dfin.cuda())
+    torch.cuda.synchronize()
+    ref = O.scan_bwd(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], bw["dout"],
+                     D=inp["D"] if use_D else None, z=inp["z"] if use_z else None,
+                     dt_bias=inp["dt_bias"] if use_bias else None, delta_softplus=softplus, h0=h0, dfinal=dfin)
+    errs = {}
+    for k, r in ref.items():
+        kg = "ddelta" if k == "ddt" else k   # the oracle names it after its dt argument
+        if r is None:
+            assert got.get(kg) is None or kg == "dh0", kg
+            continue
+        if kg == "dh0" and not use_h0:
+            continue
+        errs[kg] = assert_grad_close(got[kg].float().cpu().numpy(), r, spec.torch_dtype, kg)
+    return errs
+
+
+SHAPES = [  # batch, d_inner, L, N
+    (1, 1, 1, 1), (1, 3, 5, 4), (2, 5, 16, 16), (1, 32, 32, 16), (2, 33, 47, 16), (1, 40, 100, 5),
+    (2, 64, 256, 16), (1, 37, 129, 8), (3, 20, 70, 20), (1, 24, 64, 32), (2, 70, 33, 1), (1, 16, 300, 12)]
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "b%d_d%d_l%d_n%d" % s)
+def test_bwd_matches_oracle(shape, io):
+    b, d, L, N = shape
+    spec = I.ScanSpec(b, d, L, N, io=io, seed=1000 + L + N)
+    run_case(spec)
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("opts", [dict(use_D=False, use_z=False, use_bias=False, softplus=False),
+                                  dict(use_h0=True), dict(use_dfinal=False), dict(use_z=False),
+                                  dict(softplus=False), dict(use_h0=True, use_dfinal=False, use_D=False)],
+                         ids=["bare", "h0", "no_dfinal", "no_gate", "no_softplus", "h0_only"])
+def test_bwd_options(opts, io):
+    spec = I.ScanSpec(2, 45, 77, 16, io=io, seed=7)
+    if not opts.get("softplus", True):
+        # a positive raw step without softplus: dt ~ |N(0, 0.1)| + bias > 0 is not
+        # guaranteed, so shift the bias up
+        spec = I.ScanSpec(2, 45, 77, 16, io=io, seed=8, dt_bias_const=5.0)
+    run_case(spec, **opts)
+
+
+def test_bwd_long_and_reset_steps():
+    """A long row with sparse reset steps (step 5): the stored states at every
+    16th step and the reverse walk over many chunks."""
+    spec = I.ScanSpec(1, 64, 4096, 16, io="bf16", seed=3, dt_bias_const=1e-3, reset_frac=0.004)
+    run_case(spec)
+
+
+def test_bwd_headline_layer_full():
+    """The headline layer shape (batch 8, d_inner 1536, L 2048, N 16, bf16),
+    every gradient element against the oracle."""
+    run_case(I.MAMBA130M)
+
+
+def test_bwd_workspace_too_small_is_rejected():
+    spec = I.ScanSpec(1, 8, 64, 16, io="f32", seed=1)
+    inp = I.make_scan_inputs(spec)
+    g = {k: v.cuda() for k, v in inp.items() if k != "reset_pos"}
+    need = binding.scan_bwd_workspace_bytes(1, 8, 64, 16)
+    ws = torch.empty(need - 16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(binding.SSError) as ei:
+        binding.scan_bwd(g["x"], g["dt"], g["A"], g["B"], g["C"], torch.ones_like(g["x"]), workspace=ws)
+    assert ei.value.status == -2
+
+
+def test_bwd_repeat_is_stable():
+    """Two calls on the same inputs: the io-dtype outputs are identical (the
+    atomically accumulated fp32 sums may differ in their last bits)."""
+    spec = I.ScanSpec(2, 64, 200, 16, io="bf16", seed=11)
+    inp = I.make_scan_inputs(spec)
+    bw = I.make_bwd_inputs(spec)
+    g = {k: inp[k].cuda() for k in ("x", "dt", "z", "B", "C", "A", "D", "dt_bias")}
+    outs = [binding.scan_bwd(g["x"], g["dt"], g["A"], g["B"], g["C"], bw["dout"].cuda(), D=g["D"], z=g["z"],
+                             dt_bias=g["dt_bias"]) for _ in range(2)]
+    torch.cuda.synchronize()
+    for k in ("dx", "ddelta", "dz"):
+        assert torch.equal(outs[0][k], outs[1][k]), k
+    for k in ("dA", "dB", "dC", "dD", "ddt_bias"):
+        torch.testing.assert_close(outs[0][k], outs[1][k], rtol=1e-5, atol=1e-5)

@@ -23,7 +23,9 @@ def _conv_inputs(batch, d, L, k, io, seed):
 
 CASES = [(1, 1, 1, 4), (2, 3, 3, 4), (2, 5, 7, 4), (1, 16, 8, 4), (3, 33, 9, 4), (2, 64, 100, 4),
          (1, 40, 257, 1), (2, 40, 64, 2), (2, 40, 65, 3), (2, 24, 131, 5), (1, 24, 96, 6), (1, 24, 77, 7),
-         (2, 24, 200, 8), (8, 1536, 2048, 4)]
+         (2, 24, 200, 8), (8, 1536, 2048, 4),
+         # several shared-memory tiles per row, history longer than a piece, L shorter than the history
+         (2, 17, 2056, 6), (1, 12, 3072, 8), (2, 9, 4, 8), (3, 11, 1032, 4)]
 
 
 @pytest.mark.parametrize("io", ["bf16", "f32"])
@@ -54,12 +56,13 @@ def test_conv_unaligned_input_takes_the_scalar_path():
     assert_close(out.float().cpu().numpy(), ref, x.dtype, "conv out")
 
 
+@pytest.mark.parametrize("d", [40, 37])
 @pytest.mark.parametrize("k", [1, 2, 4, 8])
 @pytest.mark.parametrize("io", ["bf16", "f32"])
-def test_conv_decode_steps_equal_one_pass(k, io):
+def test_conv_decode_steps_equal_one_pass(k, io, d):
     """Prefill a prompt, hand its last k-1 inputs to the decode cache, then
     step token by token: every step's output equals the one-pass convolution."""
-    batch, d, L, L1 = 3, 40, 37, 20
+    batch, L, L1 = 3, 37, 20
     x, w, bias, _ = _conv_inputs(batch, d, L, k, io, seed=9 + k)
     g = x.cuda()
     _, cache = binding.causal_conv1d(g[:, :, :L1].contiguous(), w.cuda(), bias.cuda(), return_state=True)
@@ -74,3 +77,17 @@ def test_conv_decode_steps_equal_one_pass(k, io):
     assert_close(got, ref[:, :, L1:], x.dtype, "decode conv")
     if k > 1:
         np.testing.assert_array_equal(cache.float().cpu().numpy(), ref_st)
+
+
+@pytest.mark.parametrize("io", ["bf16", "f32"])
+def test_conv_step_decode_shape(io):
+    """One decode step at the decode workload's shape (256 x 5120, k = 4) from
+    a random cache."""
+    batch, d, k = 256, 5120, 4
+    x, w, bias, st = _conv_inputs(batch, d, 1, k, io, seed=77)
+    cache = st.cuda().contiguous()
+    out = binding.conv_state_update(cache, x[:, :, 0].contiguous().cuda(), w.cuda(), bias.cuda())
+    torch.cuda.synchronize()
+    ref, ref_st = O.causal_conv1d(x, w, bias, state=st)
+    assert_close(out.float().cpu().numpy(), ref[:, :, 0], x.dtype, "decode conv")
+    np.testing.assert_array_equal(cache.float().cpu().numpy(), ref_st)
