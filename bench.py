@@ -460,6 +460,17 @@ def ncu_case(args):
                                  z=tok["z"][t], y=y[t])
         torch.cuda.synchronize()
         return 0
+    if args.ncu_case == "bwd":
+        spec = HEADLINE
+        inp = I.make_scan_inputs(spec)
+        g = {k: v.cuda() for k, v in inp.items() if k != "reset_pos"}
+        dout = I.make_bwd_inputs(spec)["dout"].cuda()
+        grads = None
+        for _ in range(args.warmup + args.steps):
+            grads = binding.scan_bwd(g["x"], g["dt"], g["A"], g["B"], g["C"], dout, D=g["D"], z=g["z"],
+                                     dt_bias=g["dt_bias"], grads=grads)
+        torch.cuda.synchronize()
+        return 0
     if args.ncu_case == "conv":
         spec, k = HEADLINE, 4
         x = I.normal(spec.seed, 11, (spec.batch, spec.d_inner, spec.L), 1.0, torch.bfloat16).cuda()
@@ -494,7 +505,7 @@ def main(argv=None):
     ap.add_argument("--headline-only", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-soak", action="store_true", help="skip the 1 s untimed soak before timing")
-    ap.add_argument("--ncu-case", choices=["scan", "decode", "conv"], default=None,
+    ap.add_argument("--ncu-case", choices=["scan", "decode", "conv", "bwd"], default=None,
                     help="profiling case: warmup + steps launches of the headline scan (or of the decode "
                          "update, on the first warmup + steps tokens of the decode workload), nothing else")
     args = ap.parse_args(argv)

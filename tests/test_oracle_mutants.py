@@ -41,6 +41,20 @@ MUTANTS = {
                                "out[r * L + t] = (silu ? acc * sigmoid(acc) : acc) + (bias ? bias[d] : 0.0);")],
     "conv_history_newest_first": [("v = state[(b * (k - 1) + (k - 1 + s)) * d_inner + d];\n                else\n                    v = 0.0;\n                acc",
                                    "v = state[(b * (k - 1) + (-1 - s)) * d_inner + d];\n                else\n                    v = 0.0;\n                acc")],
+    "bwd_adjoint_without_decay": [("lam[n] *= as[(t + 1) * N + n];", "lam[n] *= 1.0;")],
+    "bwd_dA_uses_new_state": [("const double ah = as[t * N + n] * hs[t * N + n];  /* a_t h_{t-1} */",
+                               "const double ah = as[t * N + n] * hs[(t + 1) * N + n];")],
+    "bwd_dfinal_ignored": [("lam[n] = dfinal ? dfinal[r * N + n] : 0.0;", "lam[n] = 0.0;")],
+    "bwd_gate_derivative_short": [("dz[r * L + t] = gr[t] * y * s * (1.0 + zr[t] * (1.0 - s));",
+                                   "dz[r * L + t] = gr[t] * y * s;")],
+    "bwd_softplus_derivative_at_step": [("const double dv = delta_softplus ? ddel * sigmoid(v) : ddel;",
+                                         "const double dv = delta_softplus ? ddel * sigmoid(del[t]) : ddel;")],
+    "bwd_dC_uses_old_state": [("dC[(b * N + n) * L + t] += gy * hs[(t + 1) * N + n];",
+                               "dC[(b * N + n) * L + t] += gy * hs[t * N + n];")],
+    "bwd_dB_without_step": [("dB[(b * N + n) * L + t] += lam[n] * del[t] * xr[t];",
+                             "dB[(b * N + n) * L + t] += lam[n] * xr[t];")],
+    "bwd_skip_gradient_missing": [("double dxt = Dd * gy;", "double dxt = 0.0;")],
+    "bwd_dh0_without_decay": [("dh0[r * N + n] = as[n] * lam[n];", "dh0[r * N + n] = lam[n];")],
 }
 
 
