@@ -1017,7 +1017,7 @@ struct BwdParams {
     int vec4;   // dB, dC rows take 16-byte atomic adds (L % 4 == 0, aligned)
 };
 
-#define SS_BWD_STAGES 3
+#define SS_BWD_STAGES 2
 
 template <typename T, int S>
 struct BwdShape {
@@ -1052,7 +1052,7 @@ struct BwdShape {
 __device__ __forceinline__ u64 neg2(u64 a) { return a ^ 0x8000000080000000ull; }
 
 template <typename T, int S>
-__global__ void __launch_bounds__(BwdShape<T, S>::NT, BwdShape<T, S>::NT <= 128 ? 2 : 1)
+__global__ void __launch_bounds__(BwdShape<T, S>::NT, BwdShape<T, S>::NT <= 128 ? 3 : 1)
 scan_bwd_kernel(const BwdParams p)
 {
     using SH = BwdShape<T, S>;
@@ -1314,6 +1314,10 @@ scan_bwd_kernel(const BwdParams p)
     T *dzr = gate && p.dz ? static_cast<T *>(p.dz) + (b * Dn + de) * L : nullptr;
     const u64 ln2_2 = splat(0.6931471805599453f);
 
+    float4 ck_cur = make_float4(0.f, 0.f, 0.f, 0.f);   // stored state of the sub-chunk processed next
+    if (act_s)
+        ck_cur = ck[(p.nsub - 1) * ckstride];
+
     // chunk order j = 0, 1, ... is k = nchunks - 1 - j
 #pragma unroll 1
     for (int s = 0; s < STAGES - 1; ++s)
@@ -1340,13 +1344,16 @@ scan_bwd_kernel(const BwdParams p)
         for (int hh = NH - 1; hh >= 0; --hh) {
             const int64_t s = k * NH + hh;
             if (s < p.nsub) {
+                // the stored state of the next sub-chunk is fetched while this one runs
+                float4 ck_next = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (act_s && s >= 1)
+                    ck_next = ck[(s - 1) * ckstride];
                 // recompute the HC states of this sub-chunk from its stored start
                 u64 H01[HC], H23[HC];
                 u64 S01, S23;   // the state before the sub-chunk
                 {
-                    float4 c4 = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (act_s)
-                        c4 = ck[s * ckstride];
+                    const float4 c4 = ck_cur;
+                    ck_cur = ck_next;
                     S01 = pk(c4.x, c4.y);
                     S23 = pk(c4.z, c4.w);
                     u64 g01 = S01, g23 = S23;
