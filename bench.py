@@ -57,6 +57,17 @@ def scan_alg_bytes(spec: I.ScanSpec, final_state: bool = True) -> int:
     return b
 
 
+def bwd_alg_bytes(spec: I.ScanSpec) -> int:
+    """Bytes the backward pass must move: read x, dt, z, dout and write dx,
+    ddelta, dz (batch, d_inner, L); read B, C (batch, N, L) and write dB, dC in
+    fp32; read A, D, dt_bias and write dA, dD, ddt_bias. The states it
+    recomputes are not counted (they are never stored in full)."""
+    s = io_bytes(spec.io)
+    bdl = spec.batch * spec.d_inner * spec.L
+    bnl = spec.batch * spec.N * spec.L
+    return 7 * bdl * s + bnl * 2 * s + bnl * 2 * 4 + 2 * spec.d_inner * spec.N * 4 + 4 * spec.d_inner * 4
+
+
 def decode_alg_bytes(spec: I.DecodeSpec) -> int:
     """Per step: read and write the fp32 state, read x, delta, z and write y,
     read B, C, A and D."""
@@ -365,6 +376,35 @@ def time_conv_step(spec: I.DecodeSpec, steps: int, k: int = 4):
     return ms, bd * 2 * 2 + 2 * bd * (k - 1) * 2 + spec.d_inner * (k + 1) * 4
 
 
+def time_bwd(spec: I.ScanSpec, steps: int, warmup: int):
+    """Median device time (ms) of the backward pass over ``steps`` launches,
+    each preceded by an L2 flush; outputs and workspace preallocated."""
+    from selective_state_space_138_b300 import binding
+    inp = I.make_scan_inputs(spec)
+    g = {k: inp[k].cuda() for k in ("x", "dt", "z", "B", "C", "A", "D", "dt_bias")}
+    dout = I.make_bwd_inputs(spec)["dout"].cuda()
+    ws = torch.empty(binding.scan_bwd_workspace_bytes(spec.batch, spec.d_inner, spec.L, spec.N),
+                     dtype=torch.uint8, device="cuda")
+    scratch = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    grads = None
+
+    def run():
+        return binding.scan_bwd(g["x"], g["dt"], g["A"], g["B"], g["C"], dout, D=g["D"], z=g["z"],
+                                dt_bias=g["dt_bias"], grads=grads, workspace=ws)
+
+    grads = run()
+    for _ in range(warmup):
+        run()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for a, b in ev:
+        scratch.zero_()
+        a.record()
+        run()
+        b.record()
+    torch.cuda.synchronize()
+    return statistics.median([a.elapsed_time(b) for a, b in ev])
+
+
 def roofline_obj(alg_bytes: float, ms: float, peaks: dict, traffic, elem_steps: float | None = None):
     """HBM roofline of one launch: algorithmic bytes / launch time against the
     measured copy bandwidth. For a scan, also the fraction of the ALU ceiling:
@@ -584,6 +624,17 @@ def main(argv=None):
         t = time_scan(I.TINY, 20, 3, flush=False)
         extras[I.TINY.name] = {"elem_steps_per_s": I.TINY.elem_steps / (statistics.median(t) * 1e-3),
                                "kernel_ms_median": statistics.median(t), "note": "launch-bound; parity case"}
+        bms = time_bwd(HEADLINE, 10, 3)
+        bro = roofline_obj(bwd_alg_bytes(HEADLINE), bms, peaks, None)
+        mufu = peaks["sms"] * 32 / 3 * peaks["sm_max_mhz"] * 1e6
+        bro["alu_ceiling"] = {"elem_steps_per_s": mufu, "achieved": HEADLINE.elem_steps / (bms * 1e-3),
+                              "frac": round(HEADLINE.elem_steps / (bms * 1e-3) / mufu, 4),
+                              "derivation": "three exponentials per element-step (forward walk, recompute, "
+                                            "adjoint): %d SMs x 32/3 element-steps/clk x %.0f MHz"
+                                            % (peaks["sms"], peaks["sm_max_mhz"])}
+        extras["bwd_" + HEADLINE.name] = {
+            "elem_steps_per_s": HEADLINE.elem_steps / (bms * 1e-3), "kernel_ms_median": bms,
+            "roofline": bro, "note": "backward pass (all gradients, states recomputed), L2 flushed before each"}
         cms, cbytes = time_conv(HEADLINE, 10, 3)
         extras["conv1d_silu_k4_" + HEADLINE.name] = {
             "elems_per_s": HEADLINE.batch * HEADLINE.d_inner * HEADLINE.L / (cms * 1e-3), "kernel_ms_median": cms,

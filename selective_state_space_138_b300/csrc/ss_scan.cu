@@ -1067,7 +1067,7 @@ scan_bwd_kernel(const BwdParams p)
     float *DY = reinterpret_cast<float *>(Pd + LC * CH);                    // [LC][CH] gy
     float *Bf = DY + LC * CH;                                               // [LC][NS]
     float *Cf = Bf + LC * NS;                                               // [LC][NS]
-    float *Part = Cf + LC * NS;                                             // [3][S][HC][CH]
+    float *Part = Cf + LC * NS;                                             // [3][S][HC/2][CH] step pairs
     float *DBC = Part + 3 * S * HC * CH;                                    // [2][LC][NS]
     const uint32_t raw_s = static_cast<uint32_t>(__cvta_generic_to_shared(raw));
 
@@ -1370,9 +1370,10 @@ scan_bwd_kernel(const BwdParams p)
                         H23[i] = g23;
                     }
                 }
-                // adjoint recurrence backwards over the sub-chunk
-#pragma unroll
-                for (int i = HC - 1; i >= 0; --i) {
+                // adjoint recurrence backwards over the sub-chunk, two steps per round
+                // step i: lam += C gy; v = (lam dx, gy h) for the channel sums; the
+                // state sums for the epilogue; then lam *= a_i for step i-1
+                auto step = [&](int i, float *v, float &r_, float &pa, float &yy) {
                     const int t = hh * HC + i;
                     float dl, dx;
                     upk(Pd[t * CH + cs], dl, dx);
@@ -1382,54 +1383,64 @@ scan_bwd_kernel(const BwdParams p)
                     const u64 gy2 = splat(gy), dx2 = splat(dx), dd = splat(dl);
                     lam01 = fma2(Cq.x, gy2, lam01);
                     lam23 = fma2(Cq.y, gy2, lam23);
-                    // values whose channel sums are dB_t (lam delta x) and dC_t (gy h)
-                    float v[8];
                     upk(mul2(lam01, dx2), v[0], v[1]);
                     upk(mul2(lam23, dx2), v[2], v[3]);
                     upk(mul2(gy2, H01[i]), v[4], v[5]);
                     upk(mul2(gy2, H23[i]), v[6], v[7]);
-                    // this warp's state sums for the epilogue
                     const u64 a01 = ex2_2(mul2(dd, A01));
                     const u64 a23 = ex2_2(mul2(dd, A23));
                     const u64 p01 = mul2(lam01, mul2(a01, i > 0 ? H01[i > 0 ? i - 1 : 0] : S01));   // lam a_t h_{t-1}
                     const u64 p23 = mul2(lam23, mul2(a23, i > 0 ? H23[i > 0 ? i - 1 : 0] : S23));
                     dA01 = fma2(p01, dd, dA01);
                     dA23 = fma2(p23, dd, dA23);
-                    const float r_ = hsum(fma2(lam23, Bq.y, mul2(lam01, Bq.x)));
-                    const float pa = hsum(fma2(p23, A23, mul2(p01, A01)));
-                    const float yy = hsum(fma2(Cq.y, H23[i], mul2(Cq.x, H01[i])));
-                    Part[((0 * S + q) * HC + i) * CH + cs] = r_;
-                    Part[((1 * S + q) * HC + i) * CH + cs] = pa;
-                    Part[((2 * S + q) * HC + i) * CH + cs] = yy;
-                    // decay into step t-1
+                    r_ = hsum(fma2(lam23, Bq.y, mul2(lam01, Bq.x)));
+                    pa = hsum(fma2(p23, A23, mul2(p01, A01)));
+                    yy = hsum(fma2(Cq.y, H23[i], mul2(Cq.x, H01[i])));
                     lam01 = mul2(lam01, a01);
                     lam23 = mul2(lam23, a23);
-                    // transposing butterfly: value index (lane >> 2) ends summed over the warp
-                    {
-                        const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
-                        float w[4];
+                };
+                const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4, b1 = lane & 2;
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float send = b4 ? v[e] : v[e + 4];
-                            const float keep = b4 ? v[e + 4] : v[e];
-                            w[e] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
-                        }
-                        float u2[2];
+                for (int i = HC - 1; i >= 1; i -= 2) {
+                    float val[16];   // [0, 8): step i, [8, 16): step i-1
+                    float r1, pa1, y1, r0, pa0, y0;
+                    step(i, val, r1, pa1, y1);
+                    step(i - 1, val + 8, r0, pa0, y0);
+                    float2 *pp = reinterpret_cast<float2 *>(Part) + (q * (HC / 2) + (i >> 1)) * CH + cs;
+                    pp[0] = make_float2(r0, r1);
+                    pp[S * (HC / 2) * CH] = make_float2(pa0, pa1);
+                    pp[2 * S * (HC / 2) * CH] = make_float2(y0, y1);
+                    // transposing butterfly: value (lane >> 1) & 15 ends summed over the warp
+                    float w[8];
 #pragma unroll
-                        for (int e = 0; e < 2; ++e) {
-                            const float send = b3 ? w[e] : w[e + 2];
-                            const float keep = b3 ? w[e + 2] : w[e];
-                            u2[e] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
-                        }
-                        const float send = b2 ? u2[0] : u2[1];
-                        const float keep = b2 ? u2[1] : u2[0];
-                        float sum = keep + __shfl_xor_sync(0xffffffffu, send, 4);
-                        sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-                        sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-                        if ((lane & 3) == 0) {
-                            const int kv = lane >> 2;   // 0..3: dB of state 4q+kv, 4..7: dC of 4q+kv-4
-                            DBC[((kv >> 2) * LC + t) * NS + 4 * q + (kv & 3)] = sum;
-                        }
+                    for (int e = 0; e < 8; ++e) {
+                        const float send = b4 ? val[e] : val[e + 8];
+                        const float keep = b4 ? val[e + 8] : val[e];
+                        w[e] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+                    }
+                    float u4[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float send = b3 ? w[e] : w[e + 4];
+                        const float keep = b3 ? w[e + 4] : w[e];
+                        u4[e] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+                    }
+                    float u2[2];
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const float send = b2 ? u4[e] : u4[e + 2];
+                        const float keep = b2 ? u4[e + 2] : u4[e];
+                        u2[e] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+                    }
+                    const float send = b1 ? u2[0] : u2[1];
+                    const float keep = b1 ? u2[1] : u2[0];
+                    float sum = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+                    sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+                    if ((lane & 1) == 0) {
+                        const int kk = (lane >> 1) & 15;   // < 8: step i, else step i-1
+                        const int kv = kk & 7;             // 0..3: dB of state 4q+kv, 4..7: dC of 4q+kv-4
+                        const int t = hh * HC + i - (kk >> 3);
+                        DBC[((kv >> 2) * LC + t) * NS + 4 * q + (kv & 3)] = sum;
                     }
                 }
             }
@@ -1450,14 +1461,12 @@ scan_bwd_kernel(const BwdParams p)
 #pragma unroll
                 for (int i = 0; i < RH; i += 2) {
                     u64 r2 = 0, pa2 = 0, y2 = 0;
+                    const u64 *pp = reinterpret_cast<const u64 *>(Part) + ((re * RH + i) >> 1) * CH + ce;
 #pragma unroll
                     for (int qq = 0; qq < S; ++qq) {
-                        const float *b0 = Part + ((0 * S + qq) * HC + re * RH + i) * CH + ce;
-                        const float *b1 = Part + ((1 * S + qq) * HC + re * RH + i) * CH + ce;
-                        const float *b2p = Part + ((2 * S + qq) * HC + re * RH + i) * CH + ce;
-                        r2 = add2(r2, pk(b0[0], b0[CH]));
-                        pa2 = add2(pa2, pk(b1[0], b1[CH]));
-                        y2 = add2(y2, pk(b2p[0], b2p[CH]));
+                        r2 = add2(r2, pp[(0 * S + qq) * (HC / 2) * CH]);
+                        pa2 = add2(pa2, pp[(1 * S + qq) * (HC / 2) * CH]);
+                        y2 = add2(y2, pp[(2 * S + qq) * (HC / 2) * CH]);
                     }
                     const int tl = off + i;   // step within the chunk
                     float dl0, dx0_, dl1, dx1_;
