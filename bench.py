@@ -88,10 +88,26 @@ def measured_peaks() -> dict:
         return {"hbm_gbs": FALLBACK_HBM_GBS, "source": "fallback", "sms": sms, "sm_max_mhz": 2032.0}
 
 
+# the source part each profiled kernel lives in (besides the shared device helpers)
+KERNEL_PART = {"scan_fwd_": "scan_fwd.cuh", "state_update_": "decode.cuh", "scan_bwd_": "scan_bwd.cuh",
+               "conv1d_": "conv.cuh"}
+
+
+def kernel_source_hash(kernel_key: str) -> str:
+    """sha256 of the shared device helpers followed by the kernel's own part."""
+    part = next(v for k, v in KERNEL_PART.items() if kernel_key.startswith(k))
+    csrc = os.path.dirname(SRC)
+    h = hashlib.sha256()
+    for name in ("device_common.cuh", part):
+        h.update(open(os.path.join(csrc, name), "rb").read())
+    return h.hexdigest()
+
+
 def profiled_traffic(kernel_key: str):
     """Bytes per launch (dram read + write) from the committed ncu summary of
-    ``kernel_key``, when the kernel source has not changed since the capture."""
-    src_hash = hashlib.sha256(open(SRC, "rb").read()).hexdigest()
+    ``kernel_key``, when the kernel's source has not changed since the capture
+    (``source_sha256`` as computed by ``kernel_source_hash``)."""
+    src_hash = kernel_source_hash(kernel_key)
     path = os.path.join(ROOT, "profiles", kernel_key + ".md")
     if not os.path.exists(path):
         return None
@@ -625,7 +641,7 @@ def main(argv=None):
         extras[I.TINY.name] = {"elem_steps_per_s": I.TINY.elem_steps / (statistics.median(t) * 1e-3),
                                "kernel_ms_median": statistics.median(t), "note": "launch-bound; parity case"}
         bms = time_bwd(HEADLINE, 10, 3)
-        bro = roofline_obj(bwd_alg_bytes(HEADLINE), bms, peaks, None)
+        bro = roofline_obj(bwd_alg_bytes(HEADLINE), bms, peaks, profiled_traffic("scan_bwd_" + HEADLINE.name))
         mufu = peaks["sms"] * 32 / 3 * peaks["sm_max_mhz"] * 1e6
         bro["alu_ceiling"] = {"elem_steps_per_s": mufu, "achieved": HEADLINE.elem_steps / (bms * 1e-3),
                               "frac": round(HEADLINE.elem_steps / (bms * 1e-3) / mufu, 4),
@@ -638,7 +654,7 @@ def main(argv=None):
         cms, cbytes = time_conv(HEADLINE, 10, 3)
         extras["conv1d_silu_k4_" + HEADLINE.name] = {
             "elems_per_s": HEADLINE.batch * HEADLINE.d_inner * HEADLINE.L / (cms * 1e-3), "kernel_ms_median": cms,
-            "roofline": roofline_obj(cbytes, cms, peaks, None),
+            "roofline": roofline_obj(cbytes, cms, peaks, profiled_traffic("conv1d_silu_k4_" + HEADLINE.name)),
             "note": "causal depthwise conv (k = 4) + SiLU on the layer's (batch, d_inner, L) input, history out"}
         sms_, sbytes = time_conv_step(I.DECODE, 20)
         extras["conv_state_update_k4_" + I.DECODE.name] = {

@@ -27,11 +27,17 @@ def nvcc() -> str:
     raise RuntimeError("nvcc not found")
 
 
+def sources() -> list[str]:
+    """Every file the library is compiled from (one translation unit and its parts)."""
+    d = os.path.dirname(SRC)
+    return sorted(os.path.join(d, f) for f in os.listdir(d) if f.endswith((".cu", ".cuh")))
+
+
 def needs_build() -> bool:
     if not os.path.exists(LIB):
         return True
     t = os.path.getmtime(LIB)
-    return any(os.path.getmtime(f) > t for f in (SRC, HEADER, __file__))
+    return any(os.path.getmtime(f) > t for f in (*sources(), HEADER, __file__))
 
 
 def build(force: bool = False, verbose: bool = False, extra: list[str] | None = None) -> str:

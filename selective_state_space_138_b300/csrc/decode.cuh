@@ -1,0 +1,229 @@
+// decode.cuh -- the single-token decode state update and its launch logic.
+//
+// Part of the single translation unit ss_scan.cu (included inside its
+// anonymous namespace); not compiled on its own.
+
+#pragma once
+
+// ------------------------------------------------------------------ decode kernel
+
+struct UpdateParams {
+    float *state;
+    const void *x, *delta, *B, *C, *z;
+    const float *A, *D;
+    void *y;
+    int64_t batch, d_inner, N;
+    int vec;     // N % 4 == 0 and 16-byte aligned state and A
+    int vec_bc;  // B and C rows are whole 16-byte words (16-byte aligned, N * sizeof(T) % 16 == 0)
+};
+
+// One thread per (batch row, channel) holding all N = 4 NV states: the state
+// and A of the row move as 16-byte words, B and C of the batch row (shared by
+// all its channels, so served from L1 after the first warp) as 16-byte words
+// where their size allows, and the readout is summed inside the thread.
+template <typename T, int NV>
+__global__ void __launch_bounds__(kBlock)
+state_update_row_kernel(const UpdateParams p)
+{
+    constexpr int N = 4 * NV;
+    const int64_t row = static_cast<int64_t>(blockIdx.x) * kBlock + threadIdx.x;
+    if (row >= p.batch * p.d_inner)
+        return;
+    const int64_t b = row / p.d_inner;
+    const int64_t d = row % p.d_inner;
+    float4 *st = reinterpret_cast<float4 *>(p.state + row * N);
+    const float4 *Ad = reinterpret_cast<const float4 *>(p.A + d * N);
+    const T *Bb = static_cast<const T *>(p.B) + b * N;
+    const T *Cb = static_cast<const T *>(p.C) + b * N;
+
+    float4 h[NV], a[NV];
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+        h[v] = st[v];
+        a[v] = __ldg(Ad + v);
+    }
+    float bv[N], cv[N];
+    if (p.vec_bc) {
+#pragma unroll
+        for (int e = 0; e < N; e += Io<T>::kPerVec) {
+            Io<T>::loadvec(Bb + e, bv + e);
+            Io<T>::loadvec(Cb + e, cv + e);
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < N; ++e) {
+            bv[e] = Io<T>::load1(Bb + e);
+            cv[e] = Io<T>::load1(Cb + e);
+        }
+    }
+    const float xv = Io<T>::load1(static_cast<const T *>(p.x) + row);
+    const float dl = Io<T>::load1(static_cast<const T *>(p.delta) + row);
+    const float dx = dl * xv;
+    const float dl2 = dl * kLog2e;
+    float out = 0.0f;
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+        float *hv = reinterpret_cast<float *>(&h[v]);
+        const float *av = reinterpret_cast<const float *>(&a[v]);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int n = 4 * v + e;
+            hv[e] = fmaf(ex2_approx(dl2 * av[e]), hv[e], dx * bv[n]);
+            out = fmaf(cv[n], hv[e], out);
+        }
+        st[v] = h[v];
+    }
+    out = fmaf(p.D ? __ldg(p.D + d) : 0.0f, xv, out);
+    if (p.z)
+        out *= silu_f(Io<T>::load1(static_cast<const T *>(p.z) + row));
+    Io<T>::store1(static_cast<T *>(p.y) + row, out);
+}
+
+// One thread per (row, group of 4 states); the NQ threads of a row are
+// adjacent lanes of one warp and sum their partial readouts by shuffles.
+template <typename T, int NQ>
+__global__ void __launch_bounds__(kBlock)
+state_update_kernel(const UpdateParams p)
+{
+    const int64_t gid = static_cast<int64_t>(blockIdx.x) * kBlock + threadIdx.x;
+    const int q = static_cast<int>(gid % NQ);
+    int64_t row = gid / NQ;
+    const int64_t rows = p.batch * p.d_inner;
+    const bool active = row < rows;
+    row = active ? row : 0;
+    const int64_t b = row / p.d_inner;
+    const int64_t d = row % p.d_inner;
+    const int64_t N = p.N;
+    const int n0 = 4 * q;
+
+    const float xv = Io<T>::load1(static_cast<const T *>(p.x) + row);
+    const float dl = Io<T>::load1(static_cast<const T *>(p.delta) + row);
+    const float dx = dl * xv;
+    float *st = p.state + row * N;
+    const float *Ad = p.A + d * N;
+    const T *Bb = static_cast<const T *>(p.B) + b * N;
+    const T *Cb = static_cast<const T *>(p.C) + b * N;
+
+    float hv[4] = {0.f, 0.f, 0.f, 0.f}, av[4] = {0.f, 0.f, 0.f, 0.f};
+    float bv[4] = {0.f, 0.f, 0.f, 0.f}, cv[4] = {0.f, 0.f, 0.f, 0.f};
+    const bool mine = active && n0 < N;
+    if (mine) {
+        if (p.vec) {
+            const float4 h4 = *reinterpret_cast<const float4 *>(st + n0);
+            const float4 a4 = __ldg(reinterpret_cast<const float4 *>(Ad + n0));
+            hv[0] = h4.x; hv[1] = h4.y; hv[2] = h4.z; hv[3] = h4.w;
+            av[0] = a4.x; av[1] = a4.y; av[2] = a4.z; av[3] = a4.w;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                bv[k] = Io<T>::load1(Bb + n0 + k);
+                cv[k] = Io<T>::load1(Cb + n0 + k);
+            }
+        } else {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                if (n0 + k < N) {
+                    hv[k] = st[n0 + k];
+                    av[k] = __ldg(Ad + n0 + k);
+                    bv[k] = Io<T>::load1(Bb + n0 + k);
+                    cv[k] = Io<T>::load1(Cb + n0 + k);
+                }
+            }
+        }
+    }
+    float part = 0.0f;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const float a = ex2_approx(dl * av[k] * kLog2e);
+        hv[k] = fmaf(a, hv[k], dx * bv[k]);
+        part = fmaf(cv[k], hv[k], part);
+    }
+#pragma unroll
+    for (int off = NQ / 2; off > 0; off /= 2)
+        part += __shfl_xor_sync(0xffffffffu, part, off, NQ);
+
+    if (mine) {
+        if (p.vec) {
+            *reinterpret_cast<float4 *>(st + n0) = make_float4(hv[0], hv[1], hv[2], hv[3]);
+        } else {
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                if (n0 + k < N)
+                    st[n0 + k] = hv[k];
+        }
+    }
+    if (active && q == 0) {
+        float out = part + (p.D ? __ldg(p.D + d) : 0.0f) * xv;
+        if (p.z)
+            out *= silu_f(Io<T>::load1(static_cast<const T *>(p.z) + row));
+        Io<T>::store1(static_cast<T *>(p.y) + row, out);
+    }
+}
+
+template <typename T, int NQ>
+ss_status launch_update(const UpdateParams &p, cudaStream_t stream)
+{
+    const int64_t threads = p.batch * p.d_inner * NQ;
+    const int64_t blocks = (threads + kBlock - 1) / kBlock;
+    if (blocks > 0x7fffffff)
+        return fail(SS_ERR_DIM, "grid too large");
+    state_update_kernel<T, NQ><<<static_cast<unsigned>(blocks), kBlock, 0, stream>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return fail(SS_ERR_LAUNCH, "state update launch failed: %s", cudaGetErrorString(e));
+    return SS_OK;
+}
+
+template <typename T, int NV>
+ss_status launch_update_rows(const UpdateParams &p, cudaStream_t stream)
+{
+    const int64_t blocks = (p.batch * p.d_inner + kBlock - 1) / kBlock;
+    if (blocks > 0x7fffffff)
+        return fail(SS_ERR_DIM, "grid too large");
+    state_update_row_kernel<T, NV><<<static_cast<unsigned>(blocks), kBlock, 0, stream>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return fail(SS_ERR_LAUNCH, "state update launch failed: %s", cudaGetErrorString(e));
+    return SS_OK;
+}
+
+template <typename T>
+ss_status state_update(float *state, const void *x, const void *delta, const float *A, const void *B,
+                       const void *C, const float *D, const void *z, void *y, int64_t batch,
+                       int64_t d_inner, int64_t N, cudaStream_t stream)
+{
+    g_err[0] = '\0';
+    if (batch <= 0 || d_inner <= 0)
+        return fail(SS_ERR_DIM, "sizes must be positive: batch=%lld d_inner=%lld",
+                    (long long)batch, (long long)d_inner);
+    if (N < 1 || N > SS_MAX_N)
+        return fail(SS_ERR_N, "N=%lld outside [1, %d]", (long long)N, SS_MAX_N);
+    if (batch > (int64_t(1) << 40) / d_inner)
+        return fail(SS_ERR_DIM, "element count overflows");
+    const PtrCheck list[] = {{state, "state", true}, {x, "x", true}, {delta, "delta", true},
+                             {A, "A", true},         {B, "B", true}, {C, "C", true},
+                             {y, "y", true},         {D, "D", false}, {z, "z", false}};
+    int dev = 0;
+    ss_status st = check_ptrs(list, static_cast<int>(sizeof(list) / sizeof(list[0])), &dev);
+    if (st != SS_OK)
+        return st;
+    UpdateParams p;
+    p.state = state; p.x = x; p.delta = delta; p.B = B; p.C = C; p.z = z;
+    p.A = A; p.D = D; p.y = y;
+    p.batch = batch; p.d_inner = d_inner; p.N = N;
+    p.vec = (N % 4 == 0) && aligned16(state) && aligned16(A);
+    p.vec_bc = ((N * static_cast<int64_t>(sizeof(T))) % 16 == 0) && aligned16(B) && aligned16(C);
+    if (p.vec && N <= 16) {
+        switch (N / 4) {
+        case 1: return launch_update_rows<T, 1>(p, stream);
+        case 2: return launch_update_rows<T, 2>(p, stream);
+        case 3: return launch_update_rows<T, 3>(p, stream);
+        default: return launch_update_rows<T, 4>(p, stream);
+        }
+    }
+    const int64_t nq = (N + 3) / 4;
+    if (nq <= 1) return launch_update<T, 1>(p, stream);
+    if (nq <= 2) return launch_update<T, 2>(p, stream);
+    if (nq <= 4) return launch_update<T, 4>(p, stream);
+    if (nq <= 8) return launch_update<T, 8>(p, stream);
+    return launch_update<T, 16>(p, stream);
+}

@@ -1,0 +1,720 @@
+// scan_bwd.cuh -- the backward pass of the scan (states recomputed) and its launch logic.
+//
+// Part of the single translation unit ss_scan.cu (included inside its
+// anonymous namespace); not compiled on its own.
+
+#pragma once
+
+// ------------------------------------------------------------------ backward kernel
+//
+// Gradient of the scan with the states recomputed from the inputs ("Mamba and
+// selective state spaces", section "Why the scan must be fused": the backward
+// pass reloads x, delta, B, C and recomputes the states instead of storing
+// them; the backward of a linear recurrence is a linear recurrence run in
+// reverse). With g(z) = z sigmoid(z), per channel d and state n:
+//   gy_t      = dout_t g(z_t)
+//   lam_t     = a_{t+1} lam_{t+1} + C_t gy_t,   lam_{L-1} = dfinal + C_{L-1} gy_{L-1}
+//   dB_t[n]  += lam_t delta_t x_t,  dC_t[n] += gy_t h_t   (summed over channels)
+//   dA_n     += lam_t delta_t a_t h_{t-1}
+//   dx_t      = D gy_t + delta_t sum_n lam_t B_t
+//   ddelta_t  = sum_n lam_t A_n a_t h_{t-1} + x_t sum_n lam_t B_t
+//   ddt_t     = ddelta_t sigmoid(dt_t + bias) (softplus) or ddelta_t
+//   dz_t      = dout_t y_t g'(z_t),  y_t = sum_n C_t h_t + D x_t
+//   dh0       = a_0 lam_0
+//
+// Layout as in the forward n-split kernel: a CTA owns batch row b and 32
+// channels, warp q holds states 4q..4q+3, lane c channel c.
+//   phase 1  walks the sequence forward (x, dt, B only) and stores the state
+//            at the start of every HC-step sub-chunk in the workspace;
+//   phase 2  walks the chunks in reverse. For each sub-chunk it reloads the
+//            stored state, recomputes the HC states into registers, then runs
+//            the adjoint recurrence backwards over them. Per step, the
+//            channel sums of lam * delta x and gy * h (dB, dC) are formed by a
+//            transposing butterfly over the 32 lanes; the state sums
+//            (lam B, lam A a h, C h) are left per warp in shared memory and
+//            added over the warps by the epilogue, which forms dx, ddt, dz.
+// dB, dC, dA, dD and ddt_bias are accumulated with atomic adds into buffers the
+// host clears first (the order of those fp32 additions is not fixed).
+
+struct BwdParams {
+    const void *x, *dt, *B, *C, *z, *dout;
+    const float *A, *D, *dt_bias, *h0, *dfinal;
+    void *dx, *ddt, *dz;
+    float *dA, *dB, *dC, *dD, *ddt_bias, *dh0;
+    float4 *ckpt;   // [batch][nsub][S][d_inner] states at sub-chunk starts
+    int64_t batch, d_inner, L, N, nsub;
+    int softplus;
+    int vec;    // io rows 16-byte aligned with L a multiple of the piece
+    int vec4;   // dB, dC rows take 16-byte atomic adds (L % 4 == 0, aligned)
+};
+
+#define SS_BWD_STAGES 2
+
+template <typename T, int S>
+struct BwdShape {
+    static constexpr int CH = 32;
+    static constexpr int NT = CH * S;
+    static constexpr int NS = 4 * S;
+    static constexpr int LC = 32;                 // steps per chunk
+    static constexpr int HC = 16;                 // steps per recomputed sub-chunk
+    static constexpr int NH = LC / HC;
+    static constexpr int RL = LC / S;             // prep steps per thread
+    static constexpr int RH = HC / S;             // epilogue steps per thread
+    static constexpr int STAGES = SS_BWD_STAGES;
+    static constexpr int EPP = 16 / (int)sizeof(T);
+    static constexpr int PR = LC / EPP;
+    static constexpr int ROWB = LC * (int)sizeof(T) + 16;
+    static constexpr int RAW_X = CH * ROWB;                     // x, dt, z or dout tile
+    static constexpr int RAW_BC = NS * LC * (int)sizeof(T);    // B or C tile
+    static constexpr int STAGE_BYTES = 4 * RAW_X + 2 * RAW_BC;
+    static constexpr int NPIECE = (4 * CH + 2 * NS) * PR;
+    static constexpr int PPT = (NPIECE + NT - 1) / NT;
+    static constexpr int PD_BYTES = LC * CH * 8;
+    static constexpr int DY_BYTES = LC * CH * 4;
+    static constexpr int BC_BYTES = LC * NS * 4;
+    static constexpr int PART_BYTES = 3 * S * HC * CH * 4;
+    static constexpr int DBC_BYTES = 2 * LC * NS * 4;
+    static constexpr size_t BYTES = (size_t)STAGES * STAGE_BYTES + PD_BYTES + DY_BYTES + 2 * BC_BYTES + PART_BYTES +
+                                    DBC_BYTES;
+    static_assert(RH >= 2 && RH % 2 == 0, "epilogue runs are processed in pairs");
+};
+
+// both halves negated
+__device__ __forceinline__ u64 neg2(u64 a) { return a ^ 0x8000000080000000ull; }
+
+template <typename T, int S>
+__global__ void __launch_bounds__(BwdShape<T, S>::NT, BwdShape<T, S>::NT <= 128 ? 3 : 1)
+scan_bwd_kernel(const BwdParams p)
+{
+    using SH = BwdShape<T, S>;
+    constexpr int NT = SH::NT, CH = SH::CH, NS = SH::NS, LC = SH::LC, HC = SH::HC, NH = SH::NH;
+    constexpr int RL = SH::RL, RH = SH::RH, PR = SH::PR, STAGES = SH::STAGES, EPP = SH::EPP, PPT = SH::PPT;
+    constexpr int RW = RL * (int)sizeof(T) / 4;
+    constexpr int RHW = RH * (int)sizeof(T) / 4 > 0 ? RH * (int)sizeof(T) / 4 : 1;
+
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    unsigned char *raw = smem_raw;                                          // [STAGES][x, dt, z, dout, B, C]
+    u64 *Pd = reinterpret_cast<u64 *>(smem_raw + STAGES * SH::STAGE_BYTES);  // [LC][CH] (delta, delta x)
+    float *DY = reinterpret_cast<float *>(Pd + LC * CH);                    // [LC][CH] gy
+    float *Bf = DY + LC * CH;                                               // [LC][NS]
+    float *Cf = Bf + LC * NS;                                               // [LC][NS]
+    float *Part = Cf + LC * NS;                                             // [3][S][HC/2][CH] step pairs
+    float *DBC = Part + 3 * S * HC * CH;                                    // [2][LC][NS]
+    const uint32_t raw_s = static_cast<uint32_t>(__cvta_generic_to_shared(raw));
+
+    const int tid = threadIdx.x;
+    const int64_t b = blockIdx.y;
+    const int64_t d0 = static_cast<int64_t>(blockIdx.x) * CH;
+    const int64_t L = p.L, N = p.N, Dn = p.d_inner;
+    const bool vec = p.vec != 0;
+    const int64_t nchunks = (L + LC - 1) / LC;
+
+    const int cs = tid % CH;     // scan role: lane = channel, warp = state group
+    const int q = tid / CH;
+    const int lane = tid & 31;
+    const bool act_s = d0 + cs < Dn;
+    const int64_t ds = act_s ? d0 + cs : 0;
+    const int ce = tid % CH;     // prep/epilogue role: channel ce, run re
+    const int re = tid / CH;
+    const bool act_e = d0 + ce < Dn;
+    const int64_t de = act_e ? d0 + ce : 0;
+
+    const float biasv = (p.dt_bias && act_e) ? __ldg(p.dt_bias + de) : 0.0f;
+    const u64 bias2 = splat(biasv);
+    const float Dv = (p.D && act_e) ? __ldg(p.D + de) : 0.0f;
+    const bool gate = p.z != nullptr;
+
+    float A2[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const int n = 4 * q + e;
+        A2[e] = (n < N) ? __ldg(p.A + ds * N + n) * kLog2e : 0.0f;
+    }
+    const u64 A01 = pk(A2[0], A2[1]);
+    const u64 A23 = pk(A2[2], A2[3]);
+
+    // raw pieces this thread copies (x, dt, z, dout rows, then B, C rows)
+    const T *src[PPT];
+    uint32_t soff[PPT];
+    int poff[PPT];
+    bool p2_only[PPT];   // needed by phase 2 only (z, dout, C)
+#pragma unroll
+    for (int u = 0; u < PPT; ++u) {
+        const int pi = tid + u * NT;
+        int r, pc;
+        const T *base;
+        uint32_t off;
+        bool ok = pi < SH::NPIECE;
+        if (pi < 4 * CH * PR) {
+            const int tensor = pi / (CH * PR);
+            r = (pi % (CH * PR)) / PR;
+            pc = pi % PR;
+            const void *gv = tensor == 0 ? p.x : (tensor == 1 ? p.dt : (tensor == 2 ? p.z : p.dout));
+            const T *g = static_cast<const T *>(gv);
+            ok = ok && d0 + r < Dn && g != nullptr;
+            base = ok ? g + (b * Dn + d0 + r) * L : static_cast<const T *>(p.x);
+            off = tensor * SH::RAW_X + r * SH::ROWB;
+            p2_only[u] = tensor >= 2;
+        } else {
+            const int v = pi - 4 * CH * PR;
+            const int m = v / (NS * PR);
+            r = (v % (NS * PR)) / PR;
+            pc = v % PR;
+            ok = ok && r < N;
+            base = static_cast<const T *>(m == 0 ? p.B : p.C) + (b * N + (ok ? r : 0)) * L;
+            off = 4 * SH::RAW_X + m * SH::RAW_BC + r * LC * (int)sizeof(T);
+            p2_only[u] = m == 1;
+        }
+        src[u] = base;
+        soff[u] = off + pc * 16;
+        poff[u] = ok ? pc * EPP : (1 << 30);
+    }
+
+    // copy the raw pieces of chunk k into ring slot `slot`
+    auto stage_in = [&](int64_t k, int slot, bool phase2) {
+        const uint32_t st = raw_s + static_cast<uint32_t>(slot * SH::STAGE_BYTES);
+        const int64_t t1 = k * LC;
+        const int rem = static_cast<int>(L - t1 < (1 << 29) ? L - t1 : (1 << 29));
+#pragma unroll
+        for (int u = 0; u < PPT; ++u) {
+            if (tid + u * NT >= SH::NPIECE)
+                break;
+            if (!phase2 && p2_only[u])
+                continue;
+            const int left = rem - poff[u];
+            const int nb = left >= EPP ? 16 : (left > 0 ? left * (int)sizeof(T) : 0);
+            const T *g = src[u] + (nb > 0 ? t1 + poff[u] : 0);
+            if (vec) {
+                cp_async16(st + soff[u], g, nb);
+            } else {
+                unsigned char *dst = raw + slot * SH::STAGE_BYTES + soff[u];
+                const int ne = nb / (int)sizeof(T);
+#pragma unroll
+                for (int e = 0; e < EPP; ++e) {
+                    if constexpr (sizeof(T) == 4)
+                        reinterpret_cast<float *>(dst)[e] = e < ne ? g[e] : 0.0f;
+                    else
+                        reinterpret_cast<unsigned short *>(dst)[e] =
+                            e < ne ? reinterpret_cast<const unsigned short *>(g)[e] : (unsigned short)0;
+                }
+            }
+        }
+        cp_async_commit();
+    };
+
+    // raw B (and C) of the chunk in `slot` -> fp32 [t][n]
+    auto convert_bc = [&](int slot, bool phase2) {
+        const unsigned char *st = raw + slot * SH::STAGE_BYTES + 4 * SH::RAW_X;
+        const int items = (phase2 ? 2 : 1) * LC * S;
+        for (int w = tid; w < items; w += NT) {
+            const int m = w / (LC * S);
+            const int t = (w % (LC * S)) / S;
+            const int g = w % S;
+            const T *srcm = reinterpret_cast<const T *>(st + m * SH::RAW_BC);
+            float v[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                if constexpr (sizeof(T) == 4)
+                    v[e] = srcm[(4 * g + e) * LC + t];
+                else
+                    v[e] = __uint_as_float(static_cast<uint32_t>(
+                                               reinterpret_cast<const unsigned short *>(srcm)[(4 * g + e) * LC + t])
+                                           << 16);
+            }
+            *reinterpret_cast<float4 *>((m == 0 ? Bf : Cf) + t * NS + 4 * g) = make_float4(v[0], v[1], v[2], v[3]);
+        }
+    };
+
+    // delta, delta*x (and, in phase 2, gy) of this thread's steps of chunk k
+    auto prep = [&](int64_t k, int slot, bool phase2) {
+        const unsigned char *st = raw + slot * SH::STAGE_BYTES;
+        uint32_t xw[RW], dw[RW], zw[RW], gw[RW];
+        read_run_raw<T, RL>(st + ce * SH::ROWB, re * RL, xw);
+        read_run_raw<T, RL>(st + SH::RAW_X + ce * SH::ROWB, re * RL, dw);
+        if (phase2) {
+            read_run_raw<T, RL>(st + 3 * SH::RAW_X + ce * SH::ROWB, re * RL, gw);
+            if (gate)
+                read_run_raw<T, RL>(st + 2 * SH::RAW_X + ce * SH::ROWB, re * RL, zw);
+        }
+        const int64_t left64 = L - (k * LC + re * RL);
+        const int lim = act_e ? static_cast<int>(left64 < RL ? left64 : RL) : 0;
+#pragma unroll
+        for (int i = 0; i < RL; i += 2) {
+            const u64 xx = word_pair<T>(xw, i);
+            const u64 u = add2(word_pair<T>(dw, i), bias2);
+            const u64 s2 = p.softplus ? softplus2(u) : u;
+            float s0, s1;
+            upk(s2, s0, s1);
+            s0 = i < lim ? s0 : 0.0f;
+            s1 = i + 1 < lim ? s1 : 0.0f;
+            float sx0, sx1;
+            upk(mul2(pk(s0, s1), xx), sx0, sx1);
+            Pd[(re * RL + i) * CH + ce] = pk(s0, sx0);
+            Pd[(re * RL + i + 1) * CH + ce] = pk(s1, sx1);
+            if (phase2) {
+                u64 gy = word_pair<T>(gw, i);
+                if (gate)
+                    gy = mul2(gy, silu2(word_pair<T>(zw, i)));
+                float g0, g1;
+                upk(gy, g0, g1);
+                DY[(re * RL + i) * CH + ce] = i < lim ? g0 : 0.0f;
+                DY[(re * RL + i + 1) * CH + ce] = i + 1 < lim ? g1 : 0.0f;
+            }
+        }
+    };
+
+    const float *Bq_s = Bf + 4 * q;
+    const float *Cq_s = Cf + 4 * q;
+    float4 *ck = p.ckpt + (b * p.nsub * S + q) * Dn + ds;   // + s * S * Dn for sub-chunk s
+    const int64_t ckstride = static_cast<int64_t>(S) * Dn;
+
+    // ---- phase 1: forward, storing the state at every sub-chunk start
+    u64 h01 = 0, h23 = 0;
+    if (p.h0 && act_s) {
+        const float *hp = p.h0 + (b * Dn + ds) * N;
+        float hv[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            hv[e] = (4 * q + e < N) ? hp[4 * q + e] : 0.0f;
+        h01 = pk(hv[0], hv[1]);
+        h23 = pk(hv[2], hv[3]);
+    }
+    {
+#pragma unroll
+        for (int s = 0; s < STAGES - 1; ++s)
+            if (s < nchunks)
+                stage_in(s, s, false);
+            else
+                cp_async_commit();
+        cp_async_wait<STAGES - 2>();
+        __syncthreads();
+        prep(0, 0, false);
+        convert_bc(0, false);
+        __syncthreads();
+        for (int64_t k = 0; k < nchunks; ++k) {
+            if (k + STAGES - 1 < nchunks)
+                stage_in(k + STAGES - 1, static_cast<int>((k + STAGES - 1) % STAGES), false);
+            else
+                cp_async_commit();
+#pragma unroll
+            for (int hh = 0; hh < NH; ++hh) {
+                const int64_t s = k * NH + hh;
+                if (act_s && s < p.nsub) {
+                    float a0, a1, a2, a3;
+                    upk(h01, a0, a1);
+                    upk(h23, a2, a3);
+                    ck[s * ckstride] = make_float4(a0, a1, a2, a3);
+                }
+#pragma unroll 4
+                for (int i = 0; i < HC; ++i) {
+                    const int t = hh * HC + i;
+                    float dl, dx;
+                    upk(Pd[t * CH + cs], dl, dx);
+                    const ulonglong2 Bq = *reinterpret_cast<const ulonglong2 *>(Bq_s + t * NS);
+                    const u64 dd = splat(dl), xx = splat(dx);
+                    h01 = fma2(ex2_2(mul2(dd, A01)), h01, mul2(xx, Bq.x));
+                    h23 = fma2(ex2_2(mul2(dd, A23)), h23, mul2(xx, Bq.y));
+                }
+            }
+            cp_async_wait<STAGES - 2>();
+            __syncthreads();
+            if (k + 1 < nchunks) {
+                prep(k + 1, static_cast<int>((k + 1) % STAGES), false);
+                convert_bc(static_cast<int>((k + 1) % STAGES), false);
+            }
+            __syncthreads();
+        }
+        cp_async_wait<0>();
+        __syncthreads();
+    }
+
+    // ---- phase 2: reverse
+    u64 lam01 = 0, lam23 = 0, dA01 = 0, dA23 = 0;
+    if (p.dfinal && act_s) {
+        const float *fp = p.dfinal + (b * Dn + ds) * N;
+        float v[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            v[e] = (4 * q + e < N) ? fp[4 * q + e] : 0.0f;
+        lam01 = pk(v[0], v[1]);
+        lam23 = pk(v[2], v[3]);
+    }
+    float dD_acc = 0.0f, db_acc = 0.0f;
+    T *dxr = static_cast<T *>(p.dx) + (b * Dn + de) * L;
+    T *ddtr = static_cast<T *>(p.ddt) + (b * Dn + de) * L;
+    T *dzr = gate && p.dz ? static_cast<T *>(p.dz) + (b * Dn + de) * L : nullptr;
+    const u64 ln2_2 = splat(0.6931471805599453f);
+
+    float4 ck_cur = make_float4(0.f, 0.f, 0.f, 0.f);   // stored state of the sub-chunk processed next
+    if (act_s)
+        ck_cur = ck[(p.nsub - 1) * ckstride];
+
+    // chunk order j = 0, 1, ... is k = nchunks - 1 - j
+#pragma unroll 1
+    for (int s = 0; s < STAGES - 1; ++s)
+        if (s < nchunks)
+            stage_in(nchunks - 1 - s, s, true);
+        else
+            cp_async_commit();
+    cp_async_wait<STAGES - 2>();
+    __syncthreads();
+    prep(nchunks - 1, 0, true);
+    convert_bc(0, true);
+    __syncthreads();
+
+#pragma unroll 1
+    for (int64_t j = 0; j < nchunks; ++j) {
+        const int64_t k = nchunks - 1 - j;
+        const int slot = static_cast<int>(j % STAGES);
+        if (j + STAGES - 1 < nchunks)
+            stage_in(k - (STAGES - 1), static_cast<int>((j + STAGES - 1) % STAGES), true);
+        else
+            cp_async_commit();
+
+#pragma unroll 1
+        for (int hh = NH - 1; hh >= 0; --hh) {
+            const int64_t s = k * NH + hh;
+            if (s < p.nsub) {
+                // the stored state of the next sub-chunk is fetched while this one runs
+                float4 ck_next = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (act_s && s >= 1)
+                    ck_next = ck[(s - 1) * ckstride];
+                // recompute the HC states of this sub-chunk from its stored start
+                u64 H01[HC], H23[HC];
+                u64 S01, S23;   // the state before the sub-chunk
+                {
+                    const float4 c4 = ck_cur;
+                    ck_cur = ck_next;
+                    S01 = pk(c4.x, c4.y);
+                    S23 = pk(c4.z, c4.w);
+                    u64 g01 = S01, g23 = S23;
+#pragma unroll
+                    for (int i = 0; i < HC; ++i) {
+                        const int t = hh * HC + i;
+                        float dl, dx;
+                        upk(Pd[t * CH + cs], dl, dx);
+                        const ulonglong2 Bq = *reinterpret_cast<const ulonglong2 *>(Bq_s + t * NS);
+                        const u64 dd = splat(dl), xx = splat(dx);
+                        g01 = fma2(ex2_2(mul2(dd, A01)), g01, mul2(xx, Bq.x));
+                        g23 = fma2(ex2_2(mul2(dd, A23)), g23, mul2(xx, Bq.y));
+                        H01[i] = g01;
+                        H23[i] = g23;
+                    }
+                }
+                // adjoint recurrence backwards over the sub-chunk, two steps per round
+                // step i: lam += C gy; v = (lam dx, gy h) for the channel sums; the
+                // state sums for the epilogue; then lam *= a_i for step i-1
+                auto step = [&](int i, float *v, float &r_, float &pa, float &yy) {
+                    const int t = hh * HC + i;
+                    float dl, dx;
+                    upk(Pd[t * CH + cs], dl, dx);
+                    const float gy = DY[t * CH + cs];
+                    const ulonglong2 Bq = *reinterpret_cast<const ulonglong2 *>(Bq_s + t * NS);
+                    const ulonglong2 Cq = *reinterpret_cast<const ulonglong2 *>(Cq_s + t * NS);
+                    const u64 gy2 = splat(gy), dx2 = splat(dx), dd = splat(dl);
+                    lam01 = fma2(Cq.x, gy2, lam01);
+                    lam23 = fma2(Cq.y, gy2, lam23);
+                    upk(mul2(lam01, dx2), v[0], v[1]);
+                    upk(mul2(lam23, dx2), v[2], v[3]);
+                    upk(mul2(gy2, H01[i]), v[4], v[5]);
+                    upk(mul2(gy2, H23[i]), v[6], v[7]);
+                    const u64 a01 = ex2_2(mul2(dd, A01));
+                    const u64 a23 = ex2_2(mul2(dd, A23));
+                    const u64 p01 = mul2(lam01, mul2(a01, i > 0 ? H01[i > 0 ? i - 1 : 0] : S01));   // lam a_t h_{t-1}
+                    const u64 p23 = mul2(lam23, mul2(a23, i > 0 ? H23[i > 0 ? i - 1 : 0] : S23));
+                    dA01 = fma2(p01, dd, dA01);
+                    dA23 = fma2(p23, dd, dA23);
+                    r_ = hsum(fma2(lam23, Bq.y, mul2(lam01, Bq.x)));
+                    pa = hsum(fma2(p23, A23, mul2(p01, A01)));
+                    yy = hsum(fma2(Cq.y, H23[i], mul2(Cq.x, H01[i])));
+                    lam01 = mul2(lam01, a01);
+                    lam23 = mul2(lam23, a23);
+                };
+                const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4, b1 = lane & 2;
+#pragma unroll
+                for (int i = HC - 1; i >= 1; i -= 2) {
+                    float val[16];   // [0, 8): step i, [8, 16): step i-1
+                    float r1, pa1, y1, r0, pa0, y0;
+                    step(i, val, r1, pa1, y1);
+                    step(i - 1, val + 8, r0, pa0, y0);
+                    float2 *pp = reinterpret_cast<float2 *>(Part) + (q * (HC / 2) + (i >> 1)) * CH + cs;
+                    pp[0] = make_float2(r0, r1);
+                    pp[S * (HC / 2) * CH] = make_float2(pa0, pa1);
+                    pp[2 * S * (HC / 2) * CH] = make_float2(y0, y1);
+                    // transposing butterfly: value (lane >> 1) & 15 ends summed over the warp
+                    float w[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const float send = b4 ? val[e] : val[e + 8];
+                        const float keep = b4 ? val[e + 8] : val[e];
+                        w[e] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+                    }
+                    float u4[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float send = b3 ? w[e] : w[e + 4];
+                        const float keep = b3 ? w[e + 4] : w[e];
+                        u4[e] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+                    }
+                    float u2[2];
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const float send = b2 ? u4[e] : u4[e + 2];
+                        const float keep = b2 ? u4[e + 2] : u4[e];
+                        u2[e] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+                    }
+                    const float send = b1 ? u2[0] : u2[1];
+                    const float keep = b1 ? u2[1] : u2[0];
+                    float sum = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+                    sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+                    if ((lane & 1) == 0) {
+                        const int kk = (lane >> 1) & 15;   // < 8: step i, else step i-1
+                        const int kv = kk & 7;             // 0..3: dB of state 4q+kv, 4..7: dC of 4q+kv-4
+                        const int t = hh * HC + i - (kk >> 3);
+                        DBC[((kv >> 2) * LC + t) * NS + 4 * q + (kv & 3)] = sum;
+                    }
+                }
+            }
+            __syncthreads();
+            // ---- epilogue of the sub-chunk: steps hh*HC + re*RH .. + RH - 1
+            if (s < p.nsub) {
+                const unsigned char *st = raw + slot * SH::STAGE_BYTES;
+                const int off = hh * HC + re * RH;
+                uint32_t xw[RHW], dw[RHW], zw[RHW], gw[RHW];
+                read_run_raw<T, RH>(st + ce * SH::ROWB, off, xw);
+                read_run_raw<T, RH>(st + SH::RAW_X + ce * SH::ROWB, off, dw);
+                read_run_raw<T, RH>(st + 3 * SH::RAW_X + ce * SH::ROWB, off, gw);
+                if (gate)
+                    read_run_raw<T, RH>(st + 2 * SH::RAW_X + ce * SH::ROWB, off, zw);
+                float o_dx[RH], o_dt[RH], o_dz[RH];
+                const int64_t tg0 = k * LC + off;
+                const int lim = act_e ? static_cast<int>(L - tg0 < RH ? L - tg0 : RH) : 0;
+#pragma unroll
+                for (int i = 0; i < RH; i += 2) {
+                    u64 r2 = 0, pa2 = 0, y2 = 0;
+                    const u64 *pp = reinterpret_cast<const u64 *>(Part) + ((re * RH + i) >> 1) * CH + ce;
+#pragma unroll
+                    for (int qq = 0; qq < S; ++qq) {
+                        r2 = add2(r2, pp[(0 * S + qq) * (HC / 2) * CH]);
+                        pa2 = add2(pa2, pp[(1 * S + qq) * (HC / 2) * CH]);
+                        y2 = add2(y2, pp[(2 * S + qq) * (HC / 2) * CH]);
+                    }
+                    const int tl = off + i;   // step within the chunk
+                    float dl0, dx0_, dl1, dx1_;
+                    upk(Pd[tl * CH + ce], dl0, dx0_);
+                    upk(Pd[(tl + 1) * CH + ce], dl1, dx1_);
+                    const u64 dl2 = pk(dl0, dl1);
+                    const u64 gy2 = pk(DY[tl * CH + ce], DY[(tl + 1) * CH + ce]);
+                    const u64 xx = word_pair<T>(xw, i);
+                    const u64 D2 = splat(Dv);
+                    // dx = D gy + delta r ; ddelta = ln2 * pa + x r
+                    const u64 gdx = fma2(dl2, r2, mul2(D2, gy2));
+                    u64 gdl = fma2(xx, r2, mul2(ln2_2, pa2));
+                    if (p.softplus) {
+                        const u64 v2 = add2(word_pair<T>(dw, i), bias2);
+                        // sigmoid(v) = 1 / (1 + 2^(-v log2 e))
+                        const u64 sg = rcp_2(add2(splat(1.0f), ex2_2(mul2(v2, splat(-kLog2e)))));
+                        gdl = mul2(gdl, sg);
+                    }
+                    upk(gdx, o_dx[i], o_dx[i + 1]);
+                    upk(gdl, o_dt[i], o_dt[i + 1]);
+                    if (gate) {
+                        const u64 zz = word_pair<T>(zw, i);
+                        const u64 go = word_pair<T>(gw, i);
+                        const u64 yf = fma2(D2, xx, y2);   // pre-gate output
+                        const u64 sz = rcp_2(add2(splat(1.0f), ex2_2(mul2(zz, splat(-kLog2e)))));
+                        // g'(z) = s (1 + z (1 - s))
+                        const u64 one = splat(1.0f);
+                        const u64 gp = mul2(sz, fma2(zz, fma2(neg2(sz), one, one), one));
+                        upk(mul2(mul2(go, yf), gp), o_dz[i], o_dz[i + 1]);
+                    }
+                    float gy0, gy1, x0, x1;
+                    upk(gy2, gy0, gy1);
+                    upk(xx, x0, x1);
+                    if (i < lim) {
+                        dD_acc = fmaf(gy0, x0, dD_acc);
+                        db_acc += o_dt[i];
+                    }
+                    if (i + 1 < lim) {
+                        dD_acc = fmaf(gy1, x1, dD_acc);
+                        db_acc += o_dt[i + 1];
+                    }
+                }
+                if (act_e) {
+                    write_run<T, RH>(dxr, tg0, L, vec, o_dx);
+                    write_run<T, RH>(ddtr, tg0, L, vec, o_dt);
+                    if (dzr)
+                        write_run<T, RH>(dzr, tg0, L, vec, o_dz);
+                }
+            }
+            __syncthreads();   // Part is reused by the next sub-chunk
+        }
+
+        // ---- dB, dC of chunk k: add the CTA's channel sums into global memory
+        {
+            const int64_t t0 = k * LC;
+            constexpr int ITEMS = 2 * NS * (LC / 4);
+            for (int w = tid; w < ITEMS; w += NT) {
+                const int m = w / (NS * (LC / 4));
+                const int n = (w % (NS * (LC / 4))) / (LC / 4);
+                const int t4 = w % (LC / 4);
+                if (n >= N)
+                    continue;
+                const float *sp = DBC + (m * LC + 4 * t4) * NS + n;
+                float *g = (m == 0 ? p.dB : p.dC) + (b * N + n) * L + t0 + 4 * t4;
+                const int64_t left = L - (t0 + 4 * t4);
+                if (p.vec4 && left >= 4) {
+                    atomicAdd(reinterpret_cast<float4 *>(g), make_float4(sp[0], sp[NS], sp[2 * NS], sp[3 * NS]));
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        if (e < left)
+                            atomicAdd(g + e, sp[e * NS]);
+                }
+            }
+        }
+
+        cp_async_wait<STAGES - 2>();
+        __syncthreads();
+        if (j + 1 < nchunks) {
+            const int nslot = static_cast<int>((j + 1) % STAGES);
+            prep(k - 1, nslot, true);
+            convert_bc(nslot, true);
+        }
+        __syncthreads();
+    }
+    cp_async_wait<0>();
+
+    // ---- per-channel and per-(channel, state) sums
+    if (act_s) {
+        float v[4];
+        upk(dA01, v[0], v[1]);
+        upk(dA23, v[2], v[3]);
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            if (4 * q + e < N)
+                atomicAdd(p.dA + ds * N + 4 * q + e, v[e]);
+        if (p.dh0) {
+            float l[4];
+            upk(lam01, l[0], l[1]);
+            upk(lam23, l[2], l[3]);
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                if (4 * q + e < N)
+                    p.dh0[(b * Dn + ds) * N + 4 * q + e] = l[e];
+        }
+    }
+    if (act_e) {
+        if (p.dD)
+            atomicAdd(p.dD + de, dD_acc);
+        if (p.ddt_bias)
+            atomicAdd(p.ddt_bias + de, db_acc);
+    }
+}
+
+// ------------------------------------------------------------------ backward host side
+
+constexpr int64_t kBwdHC = 16;   // steps per stored state (BwdShape::HC)
+
+int64_t bwd_groups(int64_t N) { return N <= 4 ? 1 : (N <= 8 ? 2 : (N <= 16 ? 4 : 8)); }
+
+size_t bwd_workspace_bytes(int64_t batch, int64_t d_inner, int64_t L, int64_t N)
+{
+    if (batch <= 0 || d_inner <= 0 || L <= 0 || N < 1 || N > 32)
+        return 0;
+    const int64_t nsub = (L + kBwdHC - 1) / kBwdHC;
+    return static_cast<size_t>(batch) * nsub * bwd_groups(N) * d_inner * 16;
+}
+
+template <typename T, int S>
+ss_status launch_bwd(const BwdParams &p, cudaStream_t stream)
+{
+    using SH = BwdShape<T, S>;
+    auto kernel = scan_bwd_kernel<T, S>;
+    const size_t smem = SH::BYTES;
+    if (smem > 48u * 1024u) {
+        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem));
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return fail(SS_ERR_LAUNCH, "cudaFuncSetAttribute failed: %s", cudaGetErrorString(e));
+        }
+    }
+    const int64_t gpr = (p.d_inner + SH::CH - 1) / SH::CH;
+    if (gpr > 0x7fffffff || p.batch > 65535)
+        return fail(SS_ERR_DIM, "grid too large: %lld channel blocks x %lld batch rows", (long long)gpr,
+                    (long long)p.batch);
+    kernel<<<dim3(static_cast<unsigned>(gpr), static_cast<unsigned>(p.batch)), SH::NT, smem, stream>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return fail(SS_ERR_LAUNCH, "backward kernel launch failed: %s", cudaGetErrorString(e));
+    return SS_OK;
+}
+
+template <typename T>
+ss_status scan_bwd(const void *x, const void *dt, const float *A, const void *B, const void *C, const float *D,
+                   const void *z, const float *dt_bias, int softplus, const float *h0, const void *dout,
+                   const float *dfinal, void *dx, void *ddt, float *dA, float *dB, float *dC, float *dD, void *dz,
+                   float *ddt_bias, float *dh0, void *workspace, size_t workspace_bytes, int64_t batch,
+                   int64_t d_inner, int64_t L, int64_t N, cudaStream_t stream)
+{
+    g_err[0] = '\0';
+    if (batch <= 0 || d_inner <= 0 || L <= 0)
+        return fail(SS_ERR_DIM, "sizes must be positive: batch=%lld d_inner=%lld L=%lld",
+                    (long long)batch, (long long)d_inner, (long long)L);
+    if (N < 1 || N > 32)
+        return fail(SS_ERR_N, "N=%lld outside [1, 32] (the backward pass)", (long long)N);
+    if (batch > (int64_t(1) << 40) / d_inner || batch * d_inner > (int64_t(1) << 50) / L)
+        return fail(SS_ERR_DIM, "element count overflows");
+    const size_t need = bwd_workspace_bytes(batch, d_inner, L, N);
+    const PtrCheck list[] = {{x, "x", true},         {dt, "delta", true},   {A, "A", true},
+                             {B, "B", true},         {C, "C", true},        {dout, "dout", true},
+                             {dx, "dx", true},       {ddt, "ddelta", true}, {dA, "dA", true},
+                             {dB, "dB", true},       {dC, "dC", true},      {workspace, "workspace", true},
+                             {D, "D", false},        {z, "z", false},       {dt_bias, "dt_bias", false},
+                             {h0, "h0", false},      {dfinal, "dfinal_state", false},
+                             {dD, "dD", false},      {dz, "dz", false},     {ddt_bias, "ddt_bias", false},
+                             {dh0, "dh0", false}};
+    int dev = 0;
+    ss_status st = check_ptrs(list, static_cast<int>(sizeof(list) / sizeof(list[0])), &dev);
+    if (st != SS_OK)
+        return st;
+    if (workspace_bytes < need)
+        return fail(SS_ERR_DIM, "workspace of %zu bytes is smaller than the %zu bytes required", workspace_bytes,
+                    need);
+    if (!aligned16(workspace))
+        return fail(SS_ERR_DIM, "workspace must be 16-byte aligned");
+
+    // accumulated outputs start from zero
+    const struct { void *p; size_t n; } zero[] = {
+        {dA, static_cast<size_t>(d_inner * N) * 4}, {dB, static_cast<size_t>(batch * N * L) * 4},
+        {dC, static_cast<size_t>(batch * N * L) * 4}, {dD, static_cast<size_t>(d_inner) * 4},
+        {ddt_bias, static_cast<size_t>(d_inner) * 4}};
+    for (const auto &zc : zero) {
+        if (!zc.p)
+            continue;
+        cudaError_t e = cudaMemsetAsync(zc.p, 0, zc.n, stream);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return fail(SS_ERR_LAUNCH, "cudaMemsetAsync failed: %s", cudaGetErrorString(e));
+        }
+    }
+
+    BwdParams p;
+    p.x = x; p.dt = dt; p.B = B; p.C = C; p.z = z; p.dout = dout;
+    p.A = A; p.D = D; p.dt_bias = dt_bias; p.h0 = h0; p.dfinal = dfinal;
+    p.dx = dx; p.ddt = ddt; p.dz = z ? dz : nullptr;
+    p.dA = dA; p.dB = dB; p.dC = dC; p.dD = D ? dD : nullptr; p.ddt_bias = ddt_bias; p.dh0 = dh0;
+    p.ckpt = static_cast<float4 *>(workspace);
+    p.batch = batch; p.d_inner = d_inner; p.L = L; p.N = N;
+    p.nsub = (L + kBwdHC - 1) / kBwdHC;
+    p.softplus = softplus ? 1 : 0;
+    p.vec = (L % 16 == 0) && aligned16(x) && aligned16(dt) && aligned16(dout) && aligned16(dx) &&
+            aligned16(ddt) && (!z || aligned16(z)) && (!p.dz || aligned16(p.dz));
+    p.vec4 = (L % 4 == 0) && aligned16(dB) && aligned16(dC);
+    const int64_t S = bwd_groups(N);
+    if (S == 1) return launch_bwd<T, 1>(p, stream);
+    if (S == 2) return launch_bwd<T, 2>(p, stream);
+    if (S == 4) return launch_bwd<T, 4>(p, stream);
+    return launch_bwd<T, 8>(p, stream);
+}

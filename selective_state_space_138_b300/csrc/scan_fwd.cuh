@@ -1,0 +1,804 @@
+// scan_fwd.cuh -- the forward selective scan: the n-split kernel, the time-lane kernel and their launch logic.
+//
+// Part of the single translation unit ss_scan.cu (included inside its
+// anonymous namespace); not compiled on its own.
+
+#pragma once
+
+// ------------------------------------------------------------------ time-lane scan kernel
+//
+// A CTA owns one batch row b and CH consecutive channels d. Each channel is
+// served by W lanes of one warp ("time lanes"); the sequence is walked in
+// chunks of LC = W * K steps, lane j of a channel owning steps
+// [t0 + j*K, t0 + j*K + K) of every chunk.
+//   * B and C of the chunk (shared by every channel of the batch row) are
+//     staged once per CTA into shared memory as fp32, layout [t][n], so that
+//     all CH channels reuse them.
+//   * x, dt, z of a lane's K steps are read with 16-byte loads.
+//   * W == 1: the lane walks its K steps with all N states in registers.
+//   * W > 1: for each state n the lane forms its K pairs
+//     (a_i, b_i) = (exp(delta_i A_n), delta_i x_i B_{i,n}), folds them into one
+//     affine map, the W lanes combine their maps with
+//     (a1, b1) then (a2, b2) = (a1 a2, a2 b1 + b2) in a shuffle scan
+//     ("Mamba, annotated", "The scan, in one equation"), and each lane then
+//     re-walks its K pairs (kept in registers) from its incoming state.
+//   * The state of each (channel, n) is carried between chunks in registers and
+//     written to HBM only once, as final_state.
+// Steps past L are given delta = 0, which is the identity map (a = 1, b = 0).
+
+struct ScanParams {
+    const void *x, *dt, *B, *C, *z;
+    const float *A, *D, *dt_bias;
+    void *y;
+    float *final_state;
+    int64_t batch, d_inner, L, N;
+    int softplus;
+    int vec;          // 16-byte vector loads/stores allowed
+    int nseg;         // segments per channel group (a thread-block cluster when > 1)
+    int64_t seg_len;  // steps per segment, a multiple of the chunk length
+};
+
+// Shared-memory index of (t, n) within a chunk: K-step blocks of NT floats per
+// step, each block followed by 4 floats of padding so that the W lanes of a
+// channel (which read steps K apart) hit distinct banks.
+template <int NT, int K>
+__device__ __forceinline__ int sidx(int t, int n)
+{
+    return (t / K) * (K * NT + 4) + (t % K) * NT + n;
+}
+
+template <typename T, int NT, int W, int K>
+__global__ void __launch_bounds__(kBlock)
+scan_fwd_kernel(const ScanParams p)
+{
+    constexpr int CH = kBlock / W;      // channels per CTA
+    constexpr int LC = W * K;           // steps per chunk
+    constexpr int TILE = W * (K * NT + 4);
+    extern __shared__ __align__(16) float smem[];
+    float *Bs = smem;
+    float *Cs = smem + TILE;
+
+    const int tid = threadIdx.x;
+    const int c = tid / W;              // channel within CTA
+    const int j = tid % W;              // time lane
+    const int64_t b = blockIdx.y;
+    const int64_t d = static_cast<int64_t>(blockIdx.x) * CH + c;
+    const bool active = d < p.d_inner;
+    const int64_t dd = active ? d : 0;
+    const int64_t N = p.N;
+    const int64_t L = p.L;
+    const int64_t row = b * p.d_inner + dd;
+
+    const T *xr = static_cast<const T *>(p.x) + row * L;
+    const T *dtr = static_cast<const T *>(p.dt) + row * L;
+    const T *zr = p.z ? static_cast<const T *>(p.z) + row * L : nullptr;
+    T *yr = static_cast<T *>(p.y) + row * L;
+    const T *Bb = static_cast<const T *>(p.B) + b * N * L;
+    const T *Cb = static_cast<const T *>(p.C) + b * N * L;
+
+    float A2[NT];
+    float h[NT];
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+        A2[n] = (n < N) ? __ldg(p.A + dd * N + n) * kLog2e : 0.0f;
+        h[n] = 0.0f;
+    }
+    const float bias = p.dt_bias ? __ldg(p.dt_bias + dd) : 0.0f;
+    const float Dd = p.D ? __ldg(p.D + dd) : 0.0f;
+    const bool vec = p.vec != 0;
+
+    const int64_t nchunks = (L + LC - 1) / LC;
+    for (int64_t ch = 0; ch < nchunks; ++ch) {
+        const int64_t t0 = ch * LC;
+        __syncthreads();
+        for (int e = tid; e < NT * LC; e += kBlock) {
+            const int n = e / LC;
+            const int tl = e % LC;
+            const int64_t t = t0 + tl;
+            float bv = 0.0f, cv = 0.0f;
+            if (n < N && t < L) {
+                bv = Io<T>::load1(Bb + n * L + t);
+                cv = Io<T>::load1(Cb + n * L + t);
+            }
+            Bs[sidx<NT, K>(tl, n)] = bv;
+            Cs[sidx<NT, K>(tl, n)] = cv;
+        }
+        __syncthreads();
+
+        const int64_t tb = t0 + j * K;  // first step of this lane
+        float dl[K], dx[K], yv[K];
+        {
+            float xv[K], dtv[K];
+            load_items<T, K>(xr, tb, L, vec, xv);
+            load_items<T, K>(dtr, tb, L, vec, dtv);
+#pragma unroll
+            for (int i = 0; i < K; ++i) {
+                const float v = dtv[i] + bias;
+                float s = p.softplus ? softplus_f(v) : v;
+                s = (tb + i < L) ? s : 0.0f;
+                dl[i] = s;
+                dx[i] = s * xv[i];
+                yv[i] = Dd * xv[i];
+            }
+        }
+
+        if constexpr (W == 1) {
+#pragma unroll
+            for (int i = 0; i < K; ++i) {
+                const float *Bi = Bs + sidx<NT, K>(i, 0);
+                const float *Ci = Cs + sidx<NT, K>(i, 0);
+                float acc = yv[i];
+#pragma unroll
+                for (int n = 0; n < NT; ++n) {
+                    const float a = ex2_approx(dl[i] * A2[n]);
+                    h[n] = fmaf(a, h[n], dx[i] * Bi[n]);
+                    acc = fmaf(Ci[n], h[n], acc);
+                }
+                yv[i] = acc;
+            }
+        } else {
+#pragma unroll
+            for (int n = 0; n < NT; ++n) {
+                float a[K], bb[K];
+                float Pa = 1.0f, Pb = 0.0f;
+#pragma unroll
+                for (int i = 0; i < K; ++i) {
+                    a[i] = ex2_approx(dl[i] * A2[n]);
+                    bb[i] = dx[i] * Bs[sidx<NT, K>(j * K + i, n)];
+                    Pb = fmaf(a[i], Pb, bb[i]);
+                    Pa *= a[i];
+                }
+                // inclusive scan of the lanes' maps, earlier lanes first
+#pragma unroll
+                for (int off = 1; off < W; off *= 2) {
+                    const float pa = __shfl_up_sync(0xffffffffu, Pa, off, W);
+                    const float pb = __shfl_up_sync(0xffffffffu, Pb, off, W);
+                    if (j >= off) {
+                        Pb = fmaf(Pa, pb, Pb);
+                        Pa = Pa * pa;
+                    }
+                }
+                float ea = __shfl_up_sync(0xffffffffu, Pa, 1, W);
+                float eb = __shfl_up_sync(0xffffffffu, Pb, 1, W);
+                if (j == 0) {
+                    ea = 1.0f;
+                    eb = 0.0f;
+                }
+                float hh = fmaf(ea, h[n], eb);  // state entering this lane's steps
+                const float hend = fmaf(Pa, h[n], Pb);
+                h[n] = __shfl_sync(0xffffffffu, hend, W - 1, W);
+#pragma unroll
+                for (int i = 0; i < K; ++i) {
+                    hh = fmaf(a[i], hh, bb[i]);
+                    yv[i] = fmaf(Cs[sidx<NT, K>(j * K + i, n)], hh, yv[i]);
+                }
+            }
+        }
+
+        if (zr) {
+            float zv[K];
+            load_items<T, K>(zr, tb, L, vec, zv);
+#pragma unroll
+            for (int i = 0; i < K; ++i)
+                yv[i] *= silu_f(zv[i]);
+        }
+        if (active)
+            store_items<T, K>(yr, tb, L, vec, yv);
+    }
+
+    if (p.final_state && active && j == 0) {
+        float *fs = p.final_state + row * N;
+#pragma unroll
+        for (int n = 0; n < NT; ++n)
+            if (n < N)
+                fs[n] = h[n];
+    }
+}
+
+// ------------------------------------------------------------------ n-split scan kernel
+//
+// A CTA owns batch row b and CH = 32 channels, with S warps (S = ceil(N/4),
+// N padded to 4S with A = B = C = 0, which leaves the padded states at zero):
+// warp q holds states 4q..4q+3 of all 32 channels, lane c holding channel c.
+// Every lane walks the whole sequence one step after another, so each
+// element-step costs one exponential and four fp32 multiply(-add)s, done in
+// pairs with the packed f32x2 instructions; time is not split, so no combine
+// work is added.
+//
+// Shared-memory traffic sets the pace on this part (a 16-byte load by 32
+// lanes takes four shared-memory cycles), so the layout keeps it low: B_t and
+// C_t of a warp's states are the same for all its lanes (a warp-uniform load
+// costs half of a scattered one), the per-step pair (delta, delta*x) is 8
+// bytes, and the raw tiles are read with conflict-free 16-byte loads.
+//
+// The sequence is cut into chunks of LC = 32 steps. Per chunk k:
+//   scan      lane c of warp q advances its 4 states over the chunk (decays of
+//             the next AHEAD steps formed ahead of the state update) and
+//             keeps its partial readouts sum over its states of C_t[n] h_t[n]
+//             in registers, storing them when the chunk is done;
+//   -- barrier --
+//   epilogue  thread (c, r) adds the S partials of its RL = LC / S steps,
+//             adds D x, applies the silu(z) gate and stores y;
+//   prep      the same thread forms delta = softplus(dt + bias) (or dt + bias)
+//             and delta*x for its steps of chunk k+1, and B, C of chunk k+1
+//             are converted to fp32 [t][n];
+//   -- barrier --
+// The raw x, dt, z, B, C tiles of every chunk are copied into a ring of
+// STAGES chunks with cp.async (16-byte pieces, zero fill past the ends) three
+// chunks ahead of their use, so DRAM latency hides behind three iterations.
+// The per-step work (softplus, gate, conversions) is done once per (channel,
+// step), two steps at a time with f32x2 arithmetic.
+
+#ifndef SS_NSPLIT_AHEAD
+#define SS_NSPLIT_AHEAD 4  // steps whose decays are formed ahead of the state update
+#endif
+#define SS_NSPLIT_STAGES 4  // raw chunks resident in shared memory: k .. k+3
+
+template <typename T, int S>
+struct NSplitShape {
+    static constexpr int CH = 32;                 // channels per CTA
+    static constexpr int NT = CH * S;             // threads per CTA
+    static constexpr int NS = 4 * S;              // padded states
+    static constexpr int LC = 32;                 // steps per chunk
+    static constexpr int RL = LC / S;             // steps per epilogue/prep thread
+    static constexpr int STAGES = SS_NSPLIT_STAGES;
+    static constexpr int EPP = 16 / (int)sizeof(T);        // elements per 16-byte piece
+    static constexpr int PR = LC / EPP;                    // pieces per raw row
+    static constexpr int ROWB = LC * (int)sizeof(T) + 16;  // raw x/dt/z row stride, padded
+    static constexpr int RAW_X = CH * ROWB;                // one raw x, dt or z tile
+    static constexpr int RAW_BC = NS * LC * (int)sizeof(T);  // one raw B or C tile
+    static constexpr int STAGE_BYTES = 3 * RAW_X + 2 * RAW_BC;
+    static constexpr int NPIECE = (3 * CH + 2 * NS) * PR;
+    static constexpr int PPT = (NPIECE + NT - 1) / NT;    // raw pieces per thread
+    static constexpr int YROW = LC + 4;           // floats per partial row (conflict-free)
+    static constexpr int YQ = CH * YROW;          // floats per state group
+    static constexpr int PD_BYTES = LC * CH * 8;
+    static constexpr int BC_BYTES = LC * NS * 4;
+    static constexpr int Y_BYTES = S * YQ * 4;
+    static constexpr int X_BYTES = S * CH * 16 + S * CH * 4;   // segment end states and step sums
+    static constexpr size_t BYTES = (size_t)STAGES * STAGE_BYTES + PD_BYTES + 2 * BC_BYTES + Y_BYTES + X_BYTES;
+    static_assert(RL % 2 == 0, "steps are processed in pairs");
+};
+
+template <typename T, int S>
+__global__ void __launch_bounds__(NSplitShape<T, S>::NT, NSplitShape<T, S>::NT <= 128 ? 3 : 1)
+scan_nsplit_kernel(const ScanParams p)
+{
+    using SH = NSplitShape<T, S>;
+    constexpr int NT = SH::NT, CH = SH::CH, NS = SH::NS, LC = SH::LC, RL = SH::RL, PR = SH::PR;
+    constexpr int STAGES = SH::STAGES, EPP = SH::EPP, PPT = SH::PPT;
+    constexpr int D = SS_NSPLIT_AHEAD;
+    constexpr int RW = RL * (int)sizeof(T) / 4;   // 32-bit words per prep/epilogue run
+    static_assert(LC % 4 == 0 && D >= 1 && D <= LC, "chunk shape");
+
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    unsigned char *raw = smem_raw;                                          // [STAGES][x, dt, z, B, C]
+    u64 *Pd = reinterpret_cast<u64 *>(smem_raw + STAGES * SH::STAGE_BYTES);  // [LC][CH] (delta, delta x)
+    float *Bf = reinterpret_cast<float *>(Pd + LC * CH);                    // [LC][NS]
+    float *Cf = Bf + LC * NS;                                               // [LC][NS]
+    float *Yp = Cf + LC * NS;                                               // [S][CH][YROW]
+    float4 *Hx = reinterpret_cast<float4 *>(Yp + S * SH::YQ);               // [S][CH] segment end states
+    float *Sx = reinterpret_cast<float *>(Hx + S * CH);                     // [S][CH] step sums
+    const uint32_t raw_s = static_cast<uint32_t>(__cvta_generic_to_shared(raw));
+
+    const int tid = threadIdx.x;
+    const int nseg = p.nseg;
+    const int seg = static_cast<int>(blockIdx.x % nseg);
+    const int64_t b = blockIdx.y;
+    const int64_t d0 = static_cast<int64_t>(blockIdx.x / nseg) * CH;
+    const int64_t L = p.L, N = p.N, Dn = p.d_inner;
+    const int64_t t_lo = seg * p.seg_len;
+    const int64_t t_hi = (t_lo + p.seg_len < L) ? t_lo + p.seg_len : L;
+    const bool vec = p.vec != 0;
+
+    // scan role: channel cs = lane, state group q = warp
+    const int cs = tid % CH;
+    const int q = tid / CH;
+    const bool act_s = d0 + cs < Dn;
+    const int64_t ds = act_s ? d0 + cs : 0;
+    // epilogue/prep role: channel ce, run re (steps re*RL .. re*RL+RL-1 of a chunk)
+    const int ce = tid % CH;
+    const int re = tid / CH;
+    const bool act_e = d0 + ce < Dn;
+    const int64_t de = act_e ? d0 + ce : 0;
+    T *yr = static_cast<T *>(p.y) + (b * Dn + de) * L;
+
+    const u64 bias2 = splat((p.dt_bias && act_e) ? __ldg(p.dt_bias + de) : 0.0f);
+    const u64 D2 = splat((p.D && act_e) ? __ldg(p.D + de) : 0.0f);
+    const bool gate = p.z != nullptr;
+
+    float A2[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const int n = 4 * q + e;
+        A2[e] = (n < N) ? __ldg(p.A + ds * N + n) * kLog2e : 0.0f;
+    }
+    const u64 A01 = pk(A2[0], A2[1]);
+    const u64 A23 = pk(A2[2], A2[3]);
+    u64 h01 = 0, h23 = 0;   // +0.0f in both halves
+
+    // the raw pieces this thread copies: source row pointer, element offset
+    // within the chunk, shared-memory offset within a stage, whether the piece
+    // is needed by the readout only (z, C); rows past d_inner or N (and a
+    // missing z) copy nothing
+    const T *src[PPT];
+    uint32_t soff[PPT];
+    int poff[PPT];
+    bool ro_only[PPT];
+#pragma unroll
+    for (int u = 0; u < PPT; ++u) {
+        const int pi = tid + u * NT;
+        int r, pc;
+        const T *base;
+        uint32_t off;
+        bool ok = pi < SH::NPIECE;
+        if (pi < 3 * CH * PR) {
+            const int tensor = pi / (CH * PR);
+            r = (pi % (CH * PR)) / PR;
+            pc = pi % PR;
+            const T *g = static_cast<const T *>(tensor == 0 ? p.x : (tensor == 1 ? p.dt : p.z));
+            ok = ok && d0 + r < Dn && g != nullptr;
+            base = ok ? g + (b * Dn + d0 + r) * L : static_cast<const T *>(p.x);
+            off = tensor * SH::RAW_X + r * SH::ROWB;
+            ro_only[u] = tensor == 2;
+        } else {
+            const int v = pi - 3 * CH * PR;
+            const int m = v / (NS * PR);
+            r = (v % (NS * PR)) / PR;
+            pc = v % PR;
+            ok = ok && r < N;
+            base = static_cast<const T *>(m == 0 ? p.B : p.C) + (b * N + (ok ? r : 0)) * L;
+            off = 3 * SH::RAW_X + m * SH::RAW_BC + r * LC * (int)sizeof(T);
+            ro_only[u] = m == 1;
+        }
+        src[u] = base;
+        soff[u] = off + pc * 16;
+        poff[u] = ok ? pc * EPP : (1 << 30);   // a piece that does not exist is always past the end
+    }
+
+    // copy the raw pieces of chunk j of the segment into stage j % STAGES
+    // (steps at or past the segment end and rows that do not exist are zero)
+    auto stage_in = [&](int64_t j, bool readout) {
+        const uint32_t st = raw_s + static_cast<uint32_t>((j % STAGES) * SH::STAGE_BYTES);
+        const int64_t t1 = t_lo + j * LC;
+        const int rem = static_cast<int>(t_hi - t1 < (1 << 29) ? t_hi - t1 : (1 << 29));   // steps left
+#pragma unroll
+        for (int u = 0; u < PPT; ++u) {
+            if (tid + u * NT >= SH::NPIECE)
+                break;
+            if (!readout && ro_only[u])
+                continue;
+            const int left = rem - poff[u];
+            const int nb = left >= EPP ? 16 : (left > 0 ? left * (int)sizeof(T) : 0);
+            const T *g = src[u] + (nb > 0 ? t1 + poff[u] : 0);
+            if (vec) {
+                cp_async16(st + soff[u], g, nb);
+            } else {
+                unsigned char *dst = raw + (j % STAGES) * SH::STAGE_BYTES + soff[u];
+                const int ne = nb / (int)sizeof(T);
+#pragma unroll
+                for (int e = 0; e < EPP; ++e) {
+                    if constexpr (sizeof(T) == 4)
+                        reinterpret_cast<float *>(dst)[e] = e < ne ? g[e] : 0.0f;
+                    else
+                        reinterpret_cast<unsigned short *>(dst)[e] =
+                            e < ne ? reinterpret_cast<const unsigned short *>(g)[e] : (unsigned short)0;
+                }
+            }
+        }
+        cp_async_commit();
+    };
+
+    // raw B (and C) of chunk j -> fp32 [t][n]: each item is (tensor, step t,
+    // states 4g..4g+3), written as one 16-byte word
+    auto convert_bc = [&](int64_t j, bool readout) {
+        const unsigned char *st = raw + (j % STAGES) * SH::STAGE_BYTES + 3 * SH::RAW_X;
+        const int items = (readout ? 2 : 1) * LC * S;
+        for (int w = tid; w < items; w += NT) {
+            const int m = w / (LC * S);
+            const int t = (w % (LC * S)) / S;
+            const int g = w % S;
+            const T *srcm = reinterpret_cast<const T *>(st + m * SH::RAW_BC);
+            float v[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                if constexpr (sizeof(T) == 4)
+                    v[e] = srcm[(4 * g + e) * LC + t];
+                else
+                    v[e] = __uint_as_float(static_cast<uint32_t>(
+                                               reinterpret_cast<const unsigned short *>(srcm)[(4 * g + e) * LC + t])
+                                           << 16);
+            }
+            *reinterpret_cast<float4 *>((m == 0 ? Bf : Cf) + t * NS + 4 * g) = make_float4(v[0], v[1], v[2], v[3]);
+        }
+    };
+
+    // this thread's sum of the steps it prepares (compensated), for the segment carry
+    float ssum = 0.0f, scomp = 0.0f;
+    auto kahan = [&](float v) {
+        const float yv = v - scomp;
+        const float tv = ssum + yv;
+        scomp = (tv - ssum) - yv;
+        ssum = tv;
+    };
+
+    // delta and delta*x of this thread's steps of chunk j
+    auto prep = [&](int64_t j, bool sum_steps) {
+        const unsigned char *st = raw + (j % STAGES) * SH::STAGE_BYTES;
+        uint32_t xw[RW], dw[RW];
+        read_run_raw<T, RL>(st + ce * SH::ROWB, re * RL, xw);
+        read_run_raw<T, RL>(st + SH::RAW_X + ce * SH::ROWB, re * RL, dw);
+        const int64_t left64 = t_hi - (t_lo + j * LC + re * RL);
+        const int lim = act_e ? static_cast<int>(left64 < RL ? left64 : RL) : 0;
+#pragma unroll
+        for (int i = 0; i < RL; i += 2) {
+            const u64 xx = word_pair<T>(xw, i);
+            const u64 u = add2(word_pair<T>(dw, i), bias2);
+            const u64 s2 = p.softplus ? softplus2(u) : u;
+            float s0, s1;
+            upk(s2, s0, s1);
+            s0 = i < lim ? s0 : 0.0f;
+            s1 = i + 1 < lim ? s1 : 0.0f;
+            if (sum_steps) {
+                kahan(s0);
+                kahan(s1);
+            }
+            float sx0, sx1;
+            upk(mul2(pk(s0, s1), xx), sx0, sx1);
+            Pd[(re * RL + i) * CH + ce] = pk(s0, sx0);
+            Pd[(re * RL + i + 1) * CH + ce] = pk(s1, sx1);
+        }
+    };
+
+    float *yq_s = Yp + q * SH::YQ + cs * SH::YROW;   // this lane's partial readouts
+    const float *Bq_s = Bf + 4 * q;                   // this warp's states of B_t, C_t
+    const float *Cq_s = Cf + 4 * q;
+
+    // walk the segment [t_lo, t_hi): with the readout (y stored) or without
+    // it (state and step sum only)
+    auto run = [&](auto ro) {
+        constexpr bool RO = decltype(ro)::value;
+        const int64_t nchunks = (t_hi - t_lo + LC - 1) / LC;
+#pragma unroll
+        for (int s = 0; s < STAGES - 1; ++s)
+            if (s < nchunks)
+                stage_in(s, RO);
+            else
+                cp_async_commit();
+        cp_async_wait<STAGES - 2>();
+        __syncthreads();
+        prep(0, !RO);
+        convert_bc(0, RO);
+        __syncthreads();
+
+        for (int64_t k = 0; k < nchunks; ++k) {
+            const int64_t t0 = t_lo + k * LC;
+            if (k + STAGES - 1 < nchunks)
+                stage_in(k + STAGES - 1, RO);
+            else
+                cp_async_commit();
+
+            // ---- scan: 4 states of channel cs over the chunk; the decays and
+            // writes of step t + D are formed while the state takes step t
+            {
+                u64 ra01[D], ra23[D], rb01[D], rb23[D];
+                float yv[LC];
+                auto form = [&](int t, int slot) {
+                    float dl, dx;
+                    upk(Pd[t * CH + cs], dl, dx);
+                    const ulonglong2 Bq = *reinterpret_cast<const ulonglong2 *>(Bq_s + t * NS);
+                    const u64 dd = splat(dl);
+                    const u64 xx = splat(dx);
+                    ra01[slot] = ex2_2(mul2(dd, A01));
+                    ra23[slot] = ex2_2(mul2(dd, A23));
+                    rb01[slot] = mul2(xx, Bq.x);
+                    rb23[slot] = mul2(xx, Bq.y);
+                };
+#pragma unroll
+                for (int i = 0; i < D; ++i)
+                    form(i, i);
+#pragma unroll
+                for (int t = 0; t < LC; ++t) {
+                    const int slot = t % D;
+                    const u64 a01 = ra01[slot], a23 = ra23[slot], b01 = rb01[slot], b23 = rb23[slot];
+                    if (t + D < LC)
+                        form(t + D, slot);
+                    h01 = fma2(a01, h01, b01);
+                    h23 = fma2(a23, h23, b23);
+                    if constexpr (RO) {
+                        const ulonglong2 Cq = *reinterpret_cast<const ulonglong2 *>(Cq_s + t * NS);
+                        yv[t] = hsum(fma2(Cq.y, h23, mul2(Cq.x, h01)));
+                    }
+                }
+                if constexpr (RO) {
+#pragma unroll
+                    for (int t = 0; t < LC; t += 4)
+                        *reinterpret_cast<float4 *>(yq_s + t) = make_float4(yv[t], yv[t + 1], yv[t + 2], yv[t + 3]);
+                }
+            }
+            cp_async_wait<STAGES - 2>();   // chunk k+1 has landed (this thread's copies)
+            __syncthreads();
+
+            // ---- epilogue of chunk k: sum partials, skip term, gate, store
+            if constexpr (RO) {
+                const unsigned char *st = raw + (k % STAGES) * SH::STAGE_BYTES;
+                uint32_t xw[RW], zw[RW];
+                read_run_raw<T, RL>(st + ce * SH::ROWB, re * RL, xw);
+                if (gate)
+                    read_run_raw<T, RL>(st + 2 * SH::RAW_X + ce * SH::ROWB, re * RL, zw);
+                float out[RL];
+#pragma unroll
+                for (int i = 0; i < RL; i += 2) {
+                    const float *yp = Yp + ce * SH::YROW + re * RL + i;
+                    u64 acc = *reinterpret_cast<const u64 *>(yp);
+#pragma unroll
+                    for (int qq = 1; qq < S; ++qq)
+                        acc = add2(acc, *reinterpret_cast<const u64 *>(yp + qq * SH::YQ));
+                    acc = fma2(D2, word_pair<T>(xw, i), acc);
+                    if (gate)
+                        acc = mul2(acc, silu2(word_pair<T>(zw, i)));
+                    upk(acc, out[i], out[i + 1]);
+                }
+                if (act_e)
+                    write_run<T, RL>(yr, t0 + re * RL, t_hi, vec, out);
+            }
+
+            // ---- prep of chunk k+1
+            if (k + 1 < nchunks) {
+                prep(k + 1, !RO);
+                convert_bc(k + 1, RO);
+            }
+            __syncthreads();
+        }
+        cp_async_wait<0>();
+    };
+
+    if (nseg > 1) {
+        // Segments of one channel group form a thread-block cluster. Each
+        // segment but the last walks its steps from a zero state (no readout)
+        // and publishes its end state and step sum; the state entering
+        // segment s is then the predecessors' maps folded in order,
+        // h <- exp(A * sum of steps) h + end state, read through distributed
+        // shared memory.
+        cg::cluster_group cluster = cg::this_cluster();
+        if (seg < nseg - 1)
+            run(Flag<false>{});
+        float hv[4];
+        upk(h01, hv[0], hv[1]);
+        upk(h23, hv[2], hv[3]);
+        Hx[q * CH + cs] = make_float4(hv[0], hv[1], hv[2], hv[3]);
+        Sx[re * CH + ce] = ssum;
+        cluster.sync();
+        u64 f01 = 0, f23 = 0;
+        for (int sp = 0; sp < seg; ++sp) {
+            const float4 *ph = cluster.map_shared_rank(Hx, sp);
+            const float *psum = cluster.map_shared_rank(Sx, sp);
+            float tot = 0.0f;
+#pragma unroll
+            for (int r = 0; r < S; ++r)
+                tot += psum[r * CH + cs];
+            const float4 he = ph[q * CH + cs];
+            const u64 tt = splat(tot);
+            f01 = fma2(ex2_2(mul2(tt, A01)), f01, pk(he.x, he.y));
+            f23 = fma2(ex2_2(mul2(tt, A23)), f23, pk(he.z, he.w));
+        }
+        cluster.sync();   // peers have finished reading this CTA's end state
+        h01 = f01;
+        h23 = f23;
+    }
+    run(Flag<true>{});
+
+    if (p.final_state && act_s && seg == nseg - 1) {
+        float *fs = p.final_state + (b * Dn + ds) * N;
+        float hv[4];
+        upk(h01, hv[0], hv[1]);
+        upk(h23, hv[2], hv[3]);
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            if (4 * q + e < N)
+                fs[4 * q + e] = hv[e];
+    }
+}
+
+
+template <typename T, int NT, int W, int K>
+ss_status launch_scan(const ScanParams &p, cudaStream_t stream)
+{
+    constexpr int CH = kBlock / W;
+    const size_t smem = 2u * W * (K * NT + 4) * sizeof(float);
+    if (smem > 48u * 1024u) {
+        cudaError_t e = cudaFuncSetAttribute(scan_fwd_kernel<T, NT, W, K>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem));
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return fail(SS_ERR_LAUNCH, "cudaFuncSetAttribute failed: %s", cudaGetErrorString(e));
+        }
+    }
+    const int64_t gx = (p.d_inner + CH - 1) / CH;
+    if (gx > 0x7fffffff || p.batch > 65535)
+        return fail(SS_ERR_DIM, "grid too large: %lld channel blocks x %lld batch rows",
+                    (long long)gx, (long long)p.batch);
+    dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(p.batch));
+    scan_fwd_kernel<T, NT, W, K><<<grid, kBlock, smem, stream>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return fail(SS_ERR_LAUNCH, "scan kernel launch failed: %s", cudaGetErrorString(e));
+    return SS_OK;
+}
+
+// Time lanes per channel: the fewest that give every SM enough warps.
+int pick_lanes(int64_t channels, int64_t L, int sms)
+{
+    const char *env = getenv("SS_SCAN_LANES");
+    if (env) {
+        int w = atoi(env);
+        if (w == 1 || w == 4 || w == 16)
+            return w;
+    }
+    const int64_t want_threads = static_cast<int64_t>(sms) * 512;
+    int w = 1;
+    while (w < 16 && channels * w < want_threads && static_cast<int64_t>(w) * 16 * 4 <= L)
+        w *= 4;
+    return w;
+}
+
+template <typename T, int NT>
+ss_status dispatch_scan_lanes(const ScanParams &p, int lanes, cudaStream_t s)
+{
+    switch (lanes) {
+    case 1: return launch_scan<T, NT, 1, 16>(p, s);
+    case 4: return launch_scan<T, NT, 4, 16>(p, s);
+    default: return launch_scan<T, NT, 16, 16>(p, s);
+    }
+}
+
+// Segments per channel group for the n-split kernel: when the channel groups
+// fill less than half of the CTA slots of the GPU, the sequence is cut into
+// up to 8 segments (one thread-block cluster per group) so that the grid
+// fills one wave, keeping at least 4 chunks per segment.
+int pick_segments(int64_t groups, int64_t L, int64_t lc, int64_t slots)
+{
+    const char *env = getenv("SS_SCAN_SEGMENTS");
+    if (env) {
+        const int v = atoi(env);
+        if (v >= 1 && v <= 8)
+            return v;
+    }
+    if (2 * groups > slots)
+        return 1;
+    int64_t n = slots / groups;
+    n = n < 8 ? n : 8;
+    const int64_t by_len = L / (4 * lc);
+    n = n < by_len ? n : by_len;
+    return n < 1 ? 1 : static_cast<int>(n);
+}
+
+template <typename T, int S>
+ss_status launch_nsplit(const ScanParams &p0, cudaStream_t stream, int sms)
+{
+    using SH = NSplitShape<T, S>;
+    auto kernel = scan_nsplit_kernel<T, S>;
+    const size_t smem = SH::BYTES;
+    if (smem > 48u * 1024u) {
+        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem));
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return fail(SS_ERR_LAUNCH, "cudaFuncSetAttribute failed: %s", cudaGetErrorString(e));
+        }
+    }
+    ScanParams p = p0;
+    const int64_t gpr = (p.d_inner + SH::CH - 1) / SH::CH;   // channel groups per batch row
+    int occ = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, SH::NT, smem) != cudaSuccess || occ < 1) {
+        cudaGetLastError();
+        occ = 1;
+    }
+    int nseg = pick_segments(gpr * p.batch, p.L, SH::LC, static_cast<int64_t>(sms) * occ);
+    int64_t seg_len = (p.L + nseg - 1) / nseg;
+    seg_len = (seg_len + SH::LC - 1) / SH::LC * SH::LC;
+    nseg = static_cast<int>((p.L + seg_len - 1) / seg_len);
+    if (gpr * nseg > 0x7fffffff || p.batch > 65535)
+        return fail(SS_ERR_DIM, "grid too large: %lld channel blocks x %lld batch rows",
+                    (long long)(gpr * nseg), (long long)p.batch);
+
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.gridDim = dim3(static_cast<unsigned>(gpr * nseg), static_cast<unsigned>(p.batch));
+    cfg.blockDim = dim3(SH::NT);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    if (nseg > 1) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = nseg;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int clusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg) != cudaSuccess || clusters < 1) {
+            cudaGetLastError();   // a cluster of this size cannot be placed: do not split
+            nseg = 1;
+            seg_len = p.L;
+            cfg.gridDim.x = static_cast<unsigned>(gpr);
+            cfg.attrs = nullptr;
+            cfg.numAttrs = 0;
+        }
+    }
+    p.nseg = nseg;
+    p.seg_len = seg_len;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, p);
+    if (e == cudaSuccess)
+        e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(SS_ERR_LAUNCH, "scan kernel launch failed: %s", cudaGetErrorString(e));
+    }
+    return SS_OK;
+}
+
+template <typename T>
+ss_status dispatch_nsplit(const ScanParams &p, cudaStream_t s, int sms)
+{
+    if (p.N <= 4) return launch_nsplit<T, 1>(p, s, sms);
+    if (p.N <= 8) return launch_nsplit<T, 2>(p, s, sms);
+    if (p.N <= 16) return launch_nsplit<T, 4>(p, s, sms);
+    return launch_nsplit<T, 8>(p, s, sms);
+}
+
+// The n-split kernel serves N <= 32 (cutting long sequences into segments
+// when the channels alone do not fill the GPU); the time-lane kernel serves
+// N > 32. SS_SCAN_KERNEL=nsplit|lanes overrides the choice.
+bool use_nsplit(int64_t N)
+{
+    if (N > 32)
+        return false;
+    const char *env = getenv("SS_SCAN_KERNEL");
+    if (env && strcmp(env, "lanes") == 0)
+        return false;
+    return true;
+}
+
+template <typename T>
+ss_status scan_fwd(const void *x, const void *dt, const float *A, const void *B, const void *C,
+                   const float *D, const void *z, const float *dt_bias, int softplus, void *y,
+                   float *final_state, int64_t batch, int64_t d_inner, int64_t L, int64_t N,
+                   cudaStream_t stream)
+{
+    g_err[0] = '\0';
+    if (batch <= 0 || d_inner <= 0 || L <= 0)
+        return fail(SS_ERR_DIM, "sizes must be positive: batch=%lld d_inner=%lld L=%lld",
+                    (long long)batch, (long long)d_inner, (long long)L);
+    if (N < 1 || N > SS_MAX_N)
+        return fail(SS_ERR_N, "N=%lld outside [1, %d]", (long long)N, SS_MAX_N);
+    if (batch > (int64_t(1) << 40) / d_inner || batch * d_inner > (int64_t(1) << 50) / L)
+        return fail(SS_ERR_DIM, "element count overflows");
+    const PtrCheck list[] = {{x, "x", true},          {dt, "delta", true},  {A, "A", true},
+                             {B, "B", true},          {C, "C", true},       {y, "y", true},
+                             {D, "D", false},         {z, "z", false},      {dt_bias, "dt_bias", false},
+                             {final_state, "final_state", false}};
+    int dev = 0;
+    ss_status st = check_ptrs(list, static_cast<int>(sizeof(list) / sizeof(list[0])), &dev);
+    if (st != SS_OK)
+        return st;
+
+    ScanParams p;
+    p.x = x; p.dt = dt; p.B = B; p.C = C; p.z = z;
+    p.A = A; p.D = D; p.dt_bias = dt_bias;
+    p.y = y; p.final_state = final_state;
+    p.batch = batch; p.d_inner = d_inner; p.L = L; p.N = N;
+    p.softplus = softplus ? 1 : 0;
+    p.vec = (L % 16 == 0) && aligned16(x) && aligned16(dt) && aligned16(y) && (!z || aligned16(z));
+
+    p.nseg = 1;
+    p.seg_len = L;
+    if (use_nsplit(N))
+        return dispatch_nsplit<T>(p, stream, sm_count(dev));
+    const int lanes = pick_lanes(batch * d_inner, L, sm_count(dev));
+    if (N <= 4)
+        return dispatch_scan_lanes<T, 4>(p, lanes, stream);
+    if (N <= 16)
+        return dispatch_scan_lanes<T, 16>(p, lanes, stream);
+    return dispatch_scan_lanes<T, 64>(p, lanes, stream);
+}
