@@ -35,6 +35,10 @@ HEADLINE = I.MAMBA130M
 METRIC = "selective-scan element-steps/s (B*D*L*N)"
 UNIT = "element-steps/s"
 L2_FLUSH_BYTES = 256 << 20  # > the 126 MB L2
+# A device-side wait enqueued after the flush and before each start event, so
+# that the host has enqueued the timed launch before the event fires: the
+# measured interval then holds the kernel, not the host's launch latency.
+LAUNCH_COVER_CYCLES = 200_000
 FALLBACK_HBM_GBS = 6400.0
 SRC = os.path.join(ROOT, "selective_state_space_138_b300", "csrc", "ss_scan.cu")
 
@@ -240,6 +244,7 @@ def time_scan(spec: I.ScanSpec, steps: int, warmup: int, flush: bool = True, soa
     for i in range(steps):
         if flush:
             scratch.zero_()
+        torch.cuda._sleep(LAUNCH_COVER_CYCLES)
         starts[i].record()
         run()
         ends[i].record()
@@ -332,6 +337,7 @@ def time_decode(spec: I.DecodeSpec, reps: int, warmup: int):
     en = [torch.cuda.Event(enable_timing=True) for _ in range(n_flushed)]
     for t in range(n_flushed):
         scratch.zero_()
+        torch.cuda._sleep(LAUNCH_COVER_CYCLES)
         st[t].record()
         binding.state_update(state, gt["x"][t], gt["delta"][t], A, gt["B"][t], gt["C"][t], D=D, z=gt["z"][t],
                              y=ys[t])
@@ -359,6 +365,7 @@ def time_conv(spec: I.ScanSpec, steps: int, warmup: int, k: int = 4):
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     for a, b in ev:
         scratch.zero_()
+        torch.cuda._sleep(LAUNCH_COVER_CYCLES)
         a.record()
         binding.causal_conv1d(x, w, bias, out=out, state_out=st)
         b.record()
@@ -383,6 +390,7 @@ def time_conv_step(spec: I.DecodeSpec, steps: int, k: int = 4):
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     for a, b in ev:
         scratch.zero_()
+        torch.cuda._sleep(LAUNCH_COVER_CYCLES)
         a.record()
         binding.conv_state_update(st, x, w, bias, out=out)
         b.record()
@@ -414,6 +422,7 @@ def time_bwd(spec: I.ScanSpec, steps: int, warmup: int):
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     for a, b in ev:
         scratch.zero_()
+        torch.cuda._sleep(LAUNCH_COVER_CYCLES)
         a.record()
         run()
         b.record()
