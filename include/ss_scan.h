@@ -23,7 +23,8 @@
  * - Every tensor pointer is DEVICE memory of the current CUDA device,
  *   contiguous and row-major, owned by the caller. The library allocates
  *   nothing and keeps no state between calls, apart from a thread-local
- *   message for the last error (ss_last_error).
+ *   message for the last error (ss_last_error) and the built-in scratch of
+ *   ss_scan_bwd_noalloc_* (see there).
  * - A is the negative real state eigenvalue lambda itself (not its log).
  *   A, D, dt_bias and every state buffer are fp32 whatever the io dtype.
  * - "bf16" arguments are raw bfloat16 bit patterns (ss_bf16).
@@ -236,6 +237,41 @@ ss_status ss_scan_bwd_f32(const float *x, const float *delta, const float *A, co
                           float *dC, float *dD, float *dz, float *ddt_bias, float *dh0, void *workspace,
                           size_t workspace_bytes, int64_t batch, int64_t d_inner, int64_t L, int64_t N,
                           cudaStream_t stream);
+
+/*
+ * ss_scan_bwd_noalloc_bf16 / ss_scan_bwd_noalloc_f32 -- ss_scan_bwd_* without
+ * a caller workspace: the stored states live in a device array built into the
+ * library (SS_BWD_NOALLOC_MAX_BYTES bytes per device), so the call needs no
+ * memory beyond its inputs and outputs. Arguments and results are those of
+ * ss_scan_bwd_* minus workspace / workspace_bytes.
+ *
+ * Limits: a problem whose ss_scan_bwd_workspace_bytes(...) exceeds
+ * SS_BWD_NOALLOC_MAX_BYTES is rejected with SS_ERR_DIM (use ss_scan_bwd_*).
+ * The array is shared by every call in the process on that device: calls whose
+ * work overlaps in time (unordered streams, several host threads) race on it
+ * and must be ordered by the caller. The first call on a device resolves the
+ * array's address (which can load the module) and must not be made during
+ * stream capture; later calls may be captured. Nothing in the array needs
+ * clearing between calls.
+ */
+#define SS_BWD_NOALLOC_MAX_BYTES (64u << 20)
+
+ss_status ss_scan_bwd_noalloc_bf16(const ss_bf16 *x, const ss_bf16 *delta, const float *A,
+                                   const ss_bf16 *B, const ss_bf16 *C, const float *D,
+                                   const ss_bf16 *z, const float *dt_bias, int delta_softplus,
+                                   const float *h0, const ss_bf16 *dout, const float *dfinal_state,
+                                   ss_bf16 *dx, ss_bf16 *ddelta, float *dA, float *dB, float *dC,
+                                   float *dD, ss_bf16 *dz, float *ddt_bias, float *dh0,
+                                   int64_t batch, int64_t d_inner, int64_t L, int64_t N,
+                                   cudaStream_t stream);
+
+ss_status ss_scan_bwd_noalloc_f32(const float *x, const float *delta, const float *A,
+                                  const float *B, const float *C, const float *D, const float *z,
+                                  const float *dt_bias, int delta_softplus, const float *h0,
+                                  const float *dout, const float *dfinal_state, float *dx,
+                                  float *ddelta, float *dA, float *dB, float *dC, float *dD,
+                                  float *dz, float *ddt_bias, float *dh0, int64_t batch,
+                                  int64_t d_inner, int64_t L, int64_t N, cudaStream_t stream);
 
 /* Message describing the last non-OK status returned on this host thread
  * ("" if none). The string is owned by the library. */

@@ -20,12 +20,14 @@ LIB_PATH = os.path.join(_PKG, "libssscan.so")
 EXPORTS = ("ss_scan_fwd_bf16", "ss_scan_fwd_f32", "ss_state_update_bf16", "ss_state_update_f32",
            "ss_causal_conv1d_bf16", "ss_causal_conv1d_f32", "ss_conv_state_update_bf16",
            "ss_conv_state_update_f32", "ss_scan_bwd_bf16", "ss_scan_bwd_f32", "ss_scan_bwd_workspace_bytes",
+           "ss_scan_bwd_noalloc_bf16", "ss_scan_bwd_noalloc_f32",
            "ss_last_error", "ss_abi_version")
 
 STATUS = {0: "SS_OK", -1: "SS_ERR_NULL", -2: "SS_ERR_DIM", -3: "SS_ERR_N", -4: "SS_ERR_DEVICE_PTR",
           -5: "SS_ERR_LAUNCH", -6: "SS_ERR_INTERNAL"}
 MAX_N = 64
 MAX_CONV_K = 8
+BWD_NOALLOC_MAX_BYTES = 64 << 20   # SS_BWD_NOALLOC_MAX_BYTES
 
 _lib = None
 
@@ -62,6 +64,9 @@ def lib() -> ctypes.CDLL:
         getattr(L, name).restype = ci
     for name in ("ss_scan_bwd_bf16", "ss_scan_bwd_f32"):
         getattr(L, name).argtypes = [vp] * 8 + [ci] + [vp] * 13 + [ctypes.c_size_t] + [i64] * 4 + [vp]
+        getattr(L, name).restype = ci
+    for name in ("ss_scan_bwd_noalloc_bf16", "ss_scan_bwd_noalloc_f32"):
+        getattr(L, name).argtypes = [vp] * 8 + [ci] + [vp] * 12 + [i64] * 4 + [vp]
         getattr(L, name).restype = ci
     L.ss_scan_bwd_workspace_bytes.argtypes = [i64] * 4
     L.ss_scan_bwd_workspace_bytes.restype = ctypes.c_size_t
@@ -223,12 +228,15 @@ def scan_bwd_workspace_bytes(batch, d_inner, L, N) -> int:
 
 
 def scan_bwd(x, delta, A, B, C, dout, D=None, z=None, dt_bias=None, delta_softplus=True, h0=None,
-             dfinal_state=None, grads=None, workspace=None, stream=None):
+             dfinal_state=None, grads=None, workspace=None, stream=None, noalloc=False):
     """Gradient of ``scan_fwd`` (see ``ss_scan_bwd_*``): the forward inputs,
     dout (batch, d_inner, L) in the io dtype and optionally dfinal_state
     (batch, d_inner, N) fp32. ``grads`` may hold preallocated outputs under the
     names below; missing ones are allocated. ``workspace`` is a uint8 device
     tensor of at least ``scan_bwd_workspace_bytes`` bytes (allocated when None).
+    With ``noalloc`` the library's built-in scratch is used instead
+    (``ss_scan_bwd_noalloc_*``; problems needing more than
+    BWD_NOALLOC_MAX_BYTES are rejected).
 
     Returns a dict: dx, ddelta, dz (io dtype; dz None without z), dA, dB, dC,
     dD, ddt_bias, dh0 (fp32; dD / ddt_bias None without D / dt_bias, dh0 None
@@ -260,6 +268,14 @@ def scan_bwd(x, delta, A, B, C, dout, D=None, z=None, dt_bias=None, delta_softpl
         if g.get(k) is None:
             g[k] = torch.empty(shp, dtype=dt_, device=dev)
         _need(g[k], k, dt_, shp)
+    if noalloc:
+        fn = getattr(lib(), "ss_scan_bwd_noalloc_" + sfx)
+        _check(fn(_ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(dt_bias),
+                  int(bool(delta_softplus)), _ptr(h0), _ptr(dout), _ptr(dfinal_state), _ptr(g["dx"]),
+                  _ptr(g["ddelta"]), _ptr(g["dA"]), _ptr(g["dB"]), _ptr(g["dC"]), _ptr(g.get("dD")),
+                  _ptr(g.get("dz")), _ptr(g.get("ddt_bias")), _ptr(g.get("dh0")), batch, d_inner, L, N,
+                  _stream(stream)))
+        return {k: g.get(k) for k in ("dx", "ddelta", "dz", "dA", "dB", "dC", "dD", "ddt_bias", "dh0")}
     need = scan_bwd_workspace_bytes(batch, d_inner, L, N)
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)

@@ -718,3 +718,70 @@ ss_status scan_bwd(const void *x, const void *dt, const float *A, const void *B,
     if (S == 4) return launch_bwd<T, 4>(p, stream);
     return launch_bwd<T, 8>(p, stream);
 }
+
+// ------------------------------------------------------------------ built-in scratch (no caller workspace)
+//
+// ss_scan_bwd_noalloc_* keeps the stored states in this file-scope device
+// array instead of a caller workspace, so a call allocates nothing and needs
+// nothing beyond its inputs and outputs. There is one array per device context,
+// shared by every call in the process: two calls whose work overlaps in time
+// (different streams without ordering, or different host threads) race on it,
+// so callers order them. Its address is resolved with cudaGetSymbolAddress on
+// the first call on each device (which can load the module), so that first call
+// must not be made while a stream is being captured; later calls can be.
+// Nothing in it has to start at zero: the forward walk writes every stored
+// state before the reverse walk reads it.
+constexpr size_t kBwdScratchBytes = static_cast<size_t>(SS_BWD_NOALLOC_MAX_BYTES);
+static __device__ __align__(256) unsigned char g_bwd_scratch[kBwdScratchBytes];
+
+void *bwd_scratch(int dev)
+{
+    static std::atomic<void *> cache[64];
+    if (dev >= 0 && dev < 64) {
+        void *p = cache[dev].load(std::memory_order_acquire);
+        if (p)
+            return p;
+    }
+    void *q = nullptr;
+    if (cudaGetSymbolAddress(&q, g_bwd_scratch) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    if (dev >= 0 && dev < 64)
+        cache[dev].store(q, std::memory_order_release);
+    return q;
+}
+
+template <typename T>
+ss_status scan_bwd_noalloc(const void *x, const void *dt, const float *A, const void *B, const void *C,
+                           const float *D, const void *z, const float *dt_bias, int softplus, const float *h0,
+                           const void *dout, const float *dfinal, void *dx, void *ddt, float *dA, float *dB,
+                           float *dC, float *dD, void *dz, float *ddt_bias, float *dh0, int64_t batch,
+                           int64_t d_inner, int64_t L, int64_t N, cudaStream_t stream)
+{
+    g_err[0] = '\0';
+    const PtrCheck req[] = {{x, "x", true},   {dt, "delta", true}, {A, "A", true},    {B, "B", true},
+                            {C, "C", true},   {dout, "dout", true}, {dx, "dx", true}, {ddt, "ddelta", true},
+                            {dA, "dA", true}, {dB, "dB", true},     {dC, "dC", true}};
+    for (const auto &r : req)
+        if (!r.p)
+            return fail(SS_ERR_NULL, "required pointer %s is NULL", r.name);
+    const size_t need = bwd_workspace_bytes(batch, d_inner, L, N);
+    if (need > kBwdScratchBytes)
+        return fail(SS_ERR_DIM, "this problem needs %zu bytes of stored states; the built-in scratch holds %zu "
+                    "(use ss_scan_bwd_* with a workspace)", need, kBwdScratchBytes);
+    if (need == 0)   // sizes or N out of range: the checks of the workspace form report it
+        return scan_bwd<T>(x, dt, A, B, C, D, z, dt_bias, softplus, h0, dout, dfinal, dx, ddt, dA, dB, dC, dD, dz,
+                           ddt_bias, dh0, nullptr, 0, batch, d_inner, L, N, stream);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(SS_ERR_INTERNAL, "cudaGetDevice failed: %s", cudaGetErrorString(e));
+    }
+    void *ws = bwd_scratch(dev);
+    if (!ws)
+        return fail(SS_ERR_INTERNAL, "the address of the built-in scratch could not be resolved");
+    return scan_bwd<T>(x, dt, A, B, C, D, z, dt_bias, softplus, h0, dout, dfinal, dx, ddt, dA, dB, dC, dD, dz,
+                       ddt_bias, dh0, ws, kBwdScratchBytes, batch, d_inner, L, N, stream);
+}

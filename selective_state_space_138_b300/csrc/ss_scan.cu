@@ -135,6 +135,29 @@ ss_status ss_scan_bwd_f32(const float *x, const float *delta, const float *A, co
                            stream);
 }
 
+ss_status ss_scan_bwd_noalloc_bf16(const ss_bf16 *x, const ss_bf16 *delta, const float *A, const ss_bf16 *B,
+                                   const ss_bf16 *C, const float *D, const ss_bf16 *z, const float *dt_bias,
+                                   int delta_softplus, const float *h0, const ss_bf16 *dout,
+                                   const float *dfinal_state, ss_bf16 *dx, ss_bf16 *ddelta, float *dA, float *dB,
+                                   float *dC, float *dD, ss_bf16 *dz, float *ddt_bias, float *dh0, int64_t batch,
+                                   int64_t d_inner, int64_t L, int64_t N, cudaStream_t stream)
+{
+    return scan_bwd_noalloc<__nv_bfloat16>(x, delta, A, B, C, D, z, dt_bias, delta_softplus, h0, dout, dfinal_state,
+                                           dx, ddelta, dA, dB, dC, dD, dz, ddt_bias, dh0, batch, d_inner, L, N,
+                                           stream);
+}
+
+ss_status ss_scan_bwd_noalloc_f32(const float *x, const float *delta, const float *A, const float *B,
+                                  const float *C, const float *D, const float *z, const float *dt_bias,
+                                  int delta_softplus, const float *h0, const float *dout, const float *dfinal_state,
+                                  float *dx, float *ddelta, float *dA, float *dB, float *dC, float *dD, float *dz,
+                                  float *ddt_bias, float *dh0, int64_t batch, int64_t d_inner, int64_t L, int64_t N,
+                                  cudaStream_t stream)
+{
+    return scan_bwd_noalloc<float>(x, delta, A, B, C, D, z, dt_bias, delta_softplus, h0, dout, dfinal_state, dx,
+                                   ddelta, dA, dB, dC, dD, dz, ddt_bias, dh0, batch, d_inner, L, N, stream);
+}
+
 const char *ss_last_error(void) { return g_err; }
 
 int ss_abi_version(void) { return SS_ABI_VERSION; }

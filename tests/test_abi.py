@@ -137,3 +137,21 @@ def test_bwd_workspace_size(lib):
     assert ws(1, 1, 17, 1) == 2 * 16
     assert ws(2, 3, 16, 20) == 2 * 3 * 1 * 8 * 16
     assert ws(1, 1, 1, 33) == 0 and ws(0, 1, 1, 1) == 0
+
+
+@pytest.mark.parametrize("sfx", ["bf16", "f32"])
+def test_bwd_noalloc_host_validation(lib, sfx):
+    one = ctypes.c_void_p(1)
+    fn = getattr(lib, "ss_scan_bwd_noalloc_" + sfx)
+
+    def call(x=one, batch=2, d=4, L=16, N=16):
+        return fn(x, one, one, one, one, None, None, None, 1, None, one, None, one, one, one, one, one,
+                  None, None, None, None, batch, d, L, N, None)
+
+    assert call(x=None) == -1
+    assert call(N=33) == -3
+    assert call(batch=0) == -2
+    # the headline layer's stored states (about 100 MB) exceed the built-in scratch
+    assert call(batch=8, d=1536, L=2048, N=16) == -2
+    assert "built-in scratch" in binding.last_error()
+    assert binding.scan_bwd_workspace_bytes(8, 1536, 2048, 16) > binding.BWD_NOALLOC_MAX_BYTES
