@@ -102,6 +102,42 @@ ss_status ss_scan_fwd_f32(const float *x, const float *delta, const float *A,
                           int64_t d_inner, int64_t L, int64_t N, cudaStream_t stream);
 
 /*
+ * ss_scan_fwd_ex_bf16 / ss_scan_fwd_ex_f32 -- ss_scan_fwd_* with three
+ * extensions, each off when its argument is NULL / 0:
+ *
+ *   h0        : (batch, d_inner, N) fp32 state before the first step walked
+ *               (chunked prefill continues from a cached state, "Decoding with
+ *               a constant-size cache"); NULL = zero.
+ *   seq_start : (batch, L) bytes; non-zero at t means a new sequence starts
+ *               there (documents packed into one row, "What each parameter
+ *               does": the state should forget everything at a document
+ *               break). Nothing carries across the boundary between t-1 and
+ *               t: the state entering step t is zero (forward), or the state
+ *               leaving step t towards t-1 is zero (reverse). h0 reaches only
+ *               the first sequence walked.
+ *   reverse   : non-zero runs the recurrence from t = L-1 down to 0,
+ *               h_t = exp(delta_t A) h_{t+1} + delta_t B_t x_t, y_t read from h_t
+ *               (one direction of a bidirectional layer, "Mamba and selective
+ *               state spaces", section on later uses: Vision Mamba scans
+ *               patches both ways); final_state is then the state after t = 0.
+ *
+ * Other arguments as ss_scan_fwd_*. With any extension on, 1 <= N <= 32
+ * (SS_ERR_N otherwise).
+ */
+ss_status ss_scan_fwd_ex_bf16(const ss_bf16 *x, const ss_bf16 *delta, const float *A,
+                              const ss_bf16 *B, const ss_bf16 *C, const float *D,
+                              const ss_bf16 *z, const float *dt_bias, int delta_softplus,
+                              const float *h0, const uint8_t *seq_start, int reverse, ss_bf16 *y,
+                              float *final_state, int64_t batch, int64_t d_inner, int64_t L,
+                              int64_t N, cudaStream_t stream);
+
+ss_status ss_scan_fwd_ex_f32(const float *x, const float *delta, const float *A, const float *B,
+                             const float *C, const float *D, const float *z, const float *dt_bias,
+                             int delta_softplus, const float *h0, const uint8_t *seq_start,
+                             int reverse, float *y, float *final_state, int64_t batch,
+                             int64_t d_inner, int64_t L, int64_t N, cudaStream_t stream);
+
+/*
  * ss_state_update_bf16 / ss_state_update_f32 -- one decode step on a cached
  * state, "Mamba and selective state spaces", section "Decoding with a
  * constant-size cache": the state update of the definition applied once,

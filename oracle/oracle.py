@@ -7,6 +7,8 @@ does. Nothing here imports the CUDA library or its binding.
 * ``scan`` / ``scan_rows`` run the plain float64 loop of ``ss_oracle.c`` over
   all rows or over a sample of rows, in parallel over rows (the C call releases
   the GIL).
+* ``scan_ex`` is the scan with an initial state, packed-sequence starts and/or
+  the reverse direction.
 * ``scan_bwd`` is the gradient of the scan by the chain rule (float64; the
   states are kept, the reverse recurrence is run literally).
 * ``causal_conv1d`` is the block's causal depthwise convolution (+ SiLU)
@@ -56,6 +58,10 @@ def load(path: str | None = None):
     lib.oracle_softplus.restype = ctypes.c_double
     lib.oracle_scan_rows.argtypes = [dp] * 8 + [ctypes.c_int, dp, dp, dp] + [ctypes.c_int64] * 6
     lib.oracle_scan_rows.restype = ctypes.c_int
+    if hasattr(lib, "oracle_scan_ex_rows"):
+        lib.oracle_scan_ex_rows.argtypes = ([dp] * 8 + [ctypes.c_int, dp, ctypes.c_void_p, ctypes.c_int, dp, dp]
+                                            + [ctypes.c_int64] * 6)
+        lib.oracle_scan_ex_rows.restype = ctypes.c_int
     if hasattr(lib, "oracle_scan_bwd_rows"):
         lib.oracle_scan_bwd_rows.argtypes = [dp] * 8 + [ctypes.c_int] + [dp] * 12 + [ctypes.c_int64] * 6
         lib.oracle_scan_bwd_rows.restype = ctypes.c_int
@@ -122,6 +128,45 @@ def scan(x, dt, A, B, C, D=None, z=None, dt_bias=None, delta_softplus=True, h0=N
             codes = list(ex.map(run, range(nt)))
     if any(c != 0 for c in codes):
         raise RuntimeError("oracle_scan_rows failed: %r" % (codes,))
+    return y, fs
+
+
+def scan_ex(x, dt, A, B, C, D=None, z=None, dt_bias=None, delta_softplus=True, h0=None, seq_start=None,
+            reverse=False, threads: int | None = None, lib=None):
+    """The scan with an initial state, sequence starts (batch, L) bool/uint8
+    and/or the reverse direction (``oracle_scan_ex_rows``), float64.
+    Returns (y, final_state)."""
+    lib = lib or load()
+    x, dt, A, B, C = map(_f64, (x, dt, A, B, C))
+    D, z, dt_bias, h0 = map(_f64, (D, z, dt_bias, h0))
+    batch, d_inner, L = x.shape
+    N = A.shape[1]
+    st = None
+    if seq_start is not None:
+        if hasattr(seq_start, "detach"):
+            seq_start = seq_start.detach().cpu().numpy()
+        st = np.ascontiguousarray(np.asarray(seq_start) != 0, dtype=np.uint8)
+        assert st.shape == (batch, L)
+    y = np.empty((batch, d_inner, L))
+    fs = np.empty((batch, d_inner, N))
+    rows = batch * d_inner
+    nt = max(1, min(threads or default_threads(), rows)) if rows else 1
+    bounds = [(rows * i) // nt for i in range(nt + 1)]
+
+    def run(i):
+        return lib.oracle_scan_ex_rows(_ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
+                                       _ptr(dt_bias), int(bool(delta_softplus)), _ptr(h0),
+                                       None if st is None else st.ctypes.data_as(ctypes.c_void_p),
+                                       int(bool(reverse)), _ptr(y), _ptr(fs), batch, d_inner, L, N,
+                                       bounds[i], bounds[i + 1])
+
+    if nt == 1:
+        codes = [run(0)]
+    else:
+        with ThreadPoolExecutor(nt) as ex:
+            codes = list(ex.map(run, range(nt)))
+    if any(c != 0 for c in codes):
+        raise RuntimeError("oracle_scan_ex_rows failed: %r" % (codes,))
     return y, fs
 
 

@@ -288,3 +288,65 @@ int oracle_scan_bwd_rows(const double *x, const double *dt, const double *A,
     free(hs); free(as); free(del); free(lam);
     return 0;
 }
+
+/*
+ * The scan with the options of the extended entry point, written as its
+ * definition: the same step as oracle_scan_rows, walked over t = 0 .. L-1 or,
+ * when `reverse` is set, over t = L-1 .. 0 (h_t = a_t h_{t+1} + delta_t B_t x_t,
+ * one direction of a bidirectional layer). `seq_start` (batch, L), when given,
+ * marks the first step of each sequence packed into a row ("What each parameter
+ * does": the state should forget everything at a document break): nothing is
+ * carried across the boundary between t-1 and t, so the state is set to zero
+ * before step t when walking forward and after step t when walking backward.
+ * The walk starts from h0 (or zero).
+ */
+int oracle_scan_ex_rows(const double *x, const double *dt, const double *A,
+                        const double *B, const double *C, const double *D,
+                        const double *z, const double *dt_bias, int delta_softplus,
+                        const double *h0, const unsigned char *seq_start, int reverse,
+                        double *y, double *final_state,
+                        int64_t batch, int64_t d_inner, int64_t L, int64_t N,
+                        int64_t row_begin, int64_t row_end)
+{
+    if (!x || !dt || !A || !B || !C || !y)
+        return -1;
+    if (batch < 0 || d_inner < 0 || L < 0 || N <= 0)
+        return -1;
+    if (row_begin < 0 || row_end > batch * d_inner || row_begin > row_end)
+        return -1;
+    double *h = (double *)malloc((size_t)N * sizeof(double));
+    if (!h)
+        return -2;
+    for (int64_t r = row_begin; r < row_end; ++r) {
+        const int64_t b = r / d_inner;
+        const int64_t d = r % d_inner;
+        for (int64_t n = 0; n < N; ++n)
+            h[n] = h0 ? h0[r * N + n] : 0.0;
+        for (int64_t i = 0; i < L; ++i) {
+            const int64_t t = reverse ? L - 1 - i : i;
+            const int starts = seq_start && seq_start[b * L + t];
+            if (starts && !reverse)
+                for (int64_t n = 0; n < N; ++n)
+                    h[n] = 0.0;
+            const double v = dt[r * L + t] + (dt_bias ? dt_bias[d] : 0.0);
+            const double delta = delta_softplus ? oracle_softplus(v) : v;
+            double out = 0.0;
+            for (int64_t n = 0; n < N; ++n) {
+                h[n] = exp(delta * A[d * N + n]) * h[n] + delta * B[(b * N + n) * L + t] * x[r * L + t];
+                out += C[(b * N + n) * L + t] * h[n];
+            }
+            out += (D ? D[d] : 0.0) * x[r * L + t];
+            if (z)
+                out *= z[r * L + t] * sigmoid(z[r * L + t]);
+            y[r * L + t] = out;
+            if (starts && reverse)
+                for (int64_t n = 0; n < N; ++n)
+                    h[n] = 0.0;
+        }
+        if (final_state)
+            for (int64_t n = 0; n < N; ++n)
+                final_state[r * N + n] = h[n];
+    }
+    free(h);
+    return 0;
+}

@@ -17,7 +17,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libssscan.so")
 
 # names declared in include/ss_scan.h
-EXPORTS = ("ss_scan_fwd_bf16", "ss_scan_fwd_f32", "ss_state_update_bf16", "ss_state_update_f32",
+EXPORTS = ("ss_scan_fwd_bf16", "ss_scan_fwd_f32", "ss_scan_fwd_ex_bf16", "ss_scan_fwd_ex_f32", "ss_state_update_bf16", "ss_state_update_f32",
            "ss_causal_conv1d_bf16", "ss_causal_conv1d_f32", "ss_conv_state_update_bf16",
            "ss_conv_state_update_f32", "ss_scan_bwd_bf16", "ss_scan_bwd_f32", "ss_scan_bwd_workspace_bytes",
            "ss_scan_bwd_noalloc_bf16", "ss_scan_bwd_noalloc_f32",
@@ -52,6 +52,9 @@ def lib() -> ctypes.CDLL:
     upd_args = [vp] * 9 + [i64, i64, i64, vp]
     for name in ("ss_scan_fwd_bf16", "ss_scan_fwd_f32"):
         getattr(L, name).argtypes = scan_args
+        getattr(L, name).restype = ci
+    for name in ("ss_scan_fwd_ex_bf16", "ss_scan_fwd_ex_f32"):
+        getattr(L, name).argtypes = [vp] * 8 + [ci, vp, vp, ci, vp, vp, i64, i64, i64, i64, vp]
         getattr(L, name).restype = ci
     for name in ("ss_state_update_bf16", "ss_state_update_f32"):
         getattr(L, name).argtypes = upd_args
@@ -149,6 +152,37 @@ def scan_fwd(x, delta, A, B, C, D=None, z=None, dt_bias=None, delta_softplus=Tru
     _check(fn(_ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(dt_bias),
               int(bool(delta_softplus)), _ptr(y), _ptr(final_state), batch, d_inner, L, N,
               _stream(stream)))
+    return y, final_state
+
+
+def scan_fwd_ex(x, delta, A, B, C, D=None, z=None, dt_bias=None, delta_softplus=True, h0=None, seq_start=None,
+                reverse=False, y=None, final_state=None, return_final_state=True, stream=None):
+    """``scan_fwd`` with an initial state h0 (batch, d_inner, N) fp32, sequence
+    starts seq_start (batch, L) bool/uint8 and/or the reverse direction; see
+    ``ss_scan_fwd_ex_*``. Returns (y, final_state)."""
+    io = x.dtype
+    sfx = _io_suffix(io)
+    batch, d_inner, L = x.shape
+    N = A.shape[1] if A.dim() == 2 else -1
+    for t, n, dt_, shp in ((delta, "delta", io, x.shape), (z, "z", io, x.shape), (B, "B", io, (batch, N, L)),
+                           (C, "C", io, (batch, N, L)), (A, "A", torch.float32, (d_inner, N)),
+                           (D, "D", torch.float32, (d_inner,)), (dt_bias, "dt_bias", torch.float32, (d_inner,)),
+                           (h0, "h0", torch.float32, (batch, d_inner, N))):
+        _need(t, n, dt_, shp)
+    if seq_start is not None:
+        if seq_start.dtype == torch.bool:
+            seq_start = seq_start.to(torch.uint8)
+        _need(seq_start, "seq_start", torch.uint8, (batch, L))
+    if y is None:
+        y = torch.empty_like(x)
+    _need(y, "y", io, x.shape)
+    if final_state is None and return_final_state:
+        final_state = torch.empty((batch, d_inner, N), dtype=torch.float32, device=x.device)
+    _need(final_state, "final_state", torch.float32, (batch, d_inner, N))
+    fn = getattr(lib(), "ss_scan_fwd_ex_" + sfx)
+    _check(fn(_ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(dt_bias),
+              int(bool(delta_softplus)), _ptr(h0), _ptr(seq_start), int(bool(reverse)), _ptr(y),
+              _ptr(final_state), batch, d_inner, L, N, _stream(stream)))
     return y, final_state
 
 

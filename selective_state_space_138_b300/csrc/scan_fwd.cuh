@@ -36,6 +36,8 @@ struct ScanParams {
     int vec;          // 16-byte vector loads/stores allowed
     int nseg;         // segments per channel group (a thread-block cluster when > 1)
     int64_t seg_len;  // steps per segment, a multiple of the chunk length
+    const float *h0;        // (batch, d_inner, N) initial state, or NULL for zero
+    const uint8_t *reset;   // (batch, L) sequence starts, or NULL (n-split kernel only)
 };
 
 // Shared-memory index of (t, n) within a chunk: K-step blocks of NT floats per
@@ -256,11 +258,18 @@ struct NSplitShape {
     static constexpr int BC_BYTES = LC * NS * 4;
     static constexpr int Y_BYTES = S * YQ * 4;
     static constexpr int X_BYTES = S * CH * 16 + S * CH * 4;   // segment end states and step sums
-    static constexpr size_t BYTES = (size_t)STAGES * STAGE_BYTES + PD_BYTES + 2 * BC_BYTES + Y_BYTES + X_BYTES;
+    static constexpr int R_BYTES = LC + 16;                     // sequence starts of a chunk, segment flag
+    static constexpr size_t BYTES = (size_t)STAGES * STAGE_BYTES + PD_BYTES + 2 * BC_BYTES + Y_BYTES + X_BYTES +
+                                    R_BYTES;
     static_assert(RL % 2 == 0, "steps are processed in pairs");
 };
 
-template <typename T, int S>
+// REV: the recurrence runs from t = L-1 down to 0 (h_t = a_t h_{t+1} + delta_t
+// B_t x_t); chunks and the steps inside them are walked in that order, the
+// tiles themselves are the same. RST: p.reset marks sequence starts; the
+// carried state is zeroed before a marked step (forward) or after it
+// (reverse), i.e. at the boundary between t-1 and t either way.
+template <typename T, int S, bool REV, bool RST>
 __global__ void __launch_bounds__(NSplitShape<T, S>::NT, NSplitShape<T, S>::NT <= 128 ? 3 : 1)
 scan_nsplit_kernel(const ScanParams p)
 {
@@ -279,6 +288,8 @@ scan_nsplit_kernel(const ScanParams p)
     float *Yp = Cf + LC * NS;                                               // [S][CH][YROW]
     float4 *Hx = reinterpret_cast<float4 *>(Yp + S * SH::YQ);               // [S][CH] segment end states
     float *Sx = reinterpret_cast<float *>(Hx + S * CH);                     // [S][CH] step sums
+    unsigned char *Rst = reinterpret_cast<unsigned char *>(Sx + S * CH);    // [LC] sequence starts
+    int *Rx = reinterpret_cast<int *>(Rst + LC);                            // any start in the segment
     const uint32_t raw_s = static_cast<uint32_t>(__cvta_generic_to_shared(raw));
 
     const int tid = threadIdx.x;
@@ -290,6 +301,9 @@ scan_nsplit_kernel(const ScanParams p)
     const int64_t t_lo = seg * p.seg_len;
     const int64_t t_hi = (t_lo + p.seg_len < L) ? t_lo + p.seg_len : L;
     const bool vec = p.vec != 0;
+    const int64_t nchunks = (t_hi - t_lo + LC - 1) / LC;
+    // chunk j in walking order sits at chunk phys(j) of the segment
+    auto phys = [&](int64_t j) -> int64_t { return REV ? nchunks - 1 - j : j; };
 
     // scan role: channel cs = lane, state group q = warp
     const int cs = tid % CH;
@@ -360,7 +374,7 @@ scan_nsplit_kernel(const ScanParams p)
     // (steps at or past the segment end and rows that do not exist are zero)
     auto stage_in = [&](int64_t j, bool readout) {
         const uint32_t st = raw_s + static_cast<uint32_t>((j % STAGES) * SH::STAGE_BYTES);
-        const int64_t t1 = t_lo + j * LC;
+        const int64_t t1 = t_lo + phys(j) * LC;
         const int rem = static_cast<int>(t_hi - t1 < (1 << 29) ? t_hi - t1 : (1 << 29));   // steps left
 #pragma unroll
         for (int u = 0; u < PPT; ++u) {
@@ -428,7 +442,11 @@ scan_nsplit_kernel(const ScanParams p)
         uint32_t xw[RW], dw[RW];
         read_run_raw<T, RL>(st + ce * SH::ROWB, re * RL, xw);
         read_run_raw<T, RL>(st + SH::RAW_X + ce * SH::ROWB, re * RL, dw);
-        const int64_t left64 = t_hi - (t_lo + j * LC + re * RL);
+        const int64_t left64 = t_hi - (t_lo + phys(j) * LC + re * RL);
+        if (RST && tid < LC) {
+            const int64_t tt = t_lo + phys(j) * LC + tid;
+            Rst[tid] = (tt < t_hi && p.reset[b * L + tt]) ? 1 : 0;
+        }
         const int lim = act_e ? static_cast<int>(left64 < RL ? left64 : RL) : 0;
 #pragma unroll
         for (int i = 0; i < RL; i += 2) {
@@ -458,7 +476,6 @@ scan_nsplit_kernel(const ScanParams p)
     // it (state and step sum only)
     auto run = [&](auto ro) {
         constexpr bool RO = decltype(ro)::value;
-        const int64_t nchunks = (t_hi - t_lo + LC - 1) / LC;
 #pragma unroll
         for (int s = 0; s < STAGES - 1; ++s)
             if (s < nchunks)
@@ -472,7 +489,7 @@ scan_nsplit_kernel(const ScanParams p)
         __syncthreads();
 
         for (int64_t k = 0; k < nchunks; ++k) {
-            const int64_t t0 = t_lo + k * LC;
+            const int64_t t0 = t_lo + phys(k) * LC;
             if (k + STAGES - 1 < nchunks)
                 stage_in(k + STAGES - 1, RO);
             else
@@ -494,20 +511,31 @@ scan_nsplit_kernel(const ScanParams p)
                     rb01[slot] = mul2(xx, Bq.x);
                     rb23[slot] = mul2(xx, Bq.y);
                 };
+                // walking step u is chunk step t = tu(u)
+                auto tu = [](int u) { return REV ? LC - 1 - u : u; };
 #pragma unroll
                 for (int i = 0; i < D; ++i)
-                    form(i, i);
+                    form(tu(i), i);
 #pragma unroll
-                for (int t = 0; t < LC; ++t) {
-                    const int slot = t % D;
+                for (int u = 0; u < LC; ++u) {
+                    const int t = tu(u);
+                    const int slot = u % D;
                     const u64 a01 = ra01[slot], a23 = ra23[slot], b01 = rb01[slot], b23 = rb23[slot];
-                    if (t + D < LC)
-                        form(t + D, slot);
+                    if (u + D < LC)
+                        form(tu(u + D), slot);
+                    if (RST && !REV && Rst[t]) {   // a sequence starts at t: nothing carries in
+                        h01 = 0;
+                        h23 = 0;
+                    }
                     h01 = fma2(a01, h01, b01);
                     h23 = fma2(a23, h23, b23);
                     if constexpr (RO) {
                         const ulonglong2 Cq = *reinterpret_cast<const ulonglong2 *>(Cq_s + t * NS);
                         yv[t] = hsum(fma2(Cq.y, h23, mul2(Cq.x, h01)));
+                    }
+                    if (RST && REV && Rst[t]) {    // a sequence starts at t: nothing carries to t-1
+                        h01 = 0;
+                        h23 = 0;
                     }
                 }
                 if constexpr (RO) {
@@ -553,24 +581,47 @@ scan_nsplit_kernel(const ScanParams p)
         cp_async_wait<0>();
     };
 
+    // the initial state (zero unless given)
+    u64 g01 = 0, g23 = 0;
+    if (p.h0 && act_s) {
+        const float *hp = p.h0 + (b * Dn + ds) * N;
+        float hv[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            hv[e] = (4 * q + e < N) ? hp[4 * q + e] : 0.0f;
+        g01 = pk(hv[0], hv[1]);
+        g23 = pk(hv[2], hv[3]);
+    }
     if (nseg > 1) {
         // Segments of one channel group form a thread-block cluster. Each
-        // segment but the last walks its steps from a zero state (no readout)
-        // and publishes its end state and step sum; the state entering
-        // segment s is then the predecessors' maps folded in order,
-        // h <- exp(A * sum of steps) h + end state, read through distributed
-        // shared memory.
+        // segment but the one walked last walks its steps from a zero state
+        // (no readout) and publishes its end state, its step sum and whether a
+        // sequence starts inside it; the state entering segment s is then the
+        // initial state and the maps of the segments walked before it, folded
+        // in walking order, h <- exp(A * sum of steps) h + end state (the
+        // decay is 0 across a sequence start), read through distributed shared
+        // memory.
         cg::cluster_group cluster = cg::this_cluster();
-        if (seg < nseg - 1)
+        const int last = REV ? 0 : nseg - 1;
+        if (seg != last)
             run(Flag<false>{});
+        int has_start = 0;
+        if (RST)
+            for (int64_t t = t_lo + tid; t < t_hi; t += NT)
+                has_start |= p.reset[b * L + t] != 0;
+        has_start = __syncthreads_or(has_start);
+        if (tid == 0)
+            *Rx = has_start;
         float hv[4];
         upk(h01, hv[0], hv[1]);
         upk(h23, hv[2], hv[3]);
         Hx[q * CH + cs] = make_float4(hv[0], hv[1], hv[2], hv[3]);
         Sx[re * CH + ce] = ssum;
         cluster.sync();
-        u64 f01 = 0, f23 = 0;
-        for (int sp = 0; sp < seg; ++sp) {
+        u64 f01 = g01, f23 = g23;
+        const int n_before = REV ? nseg - 1 - seg : seg;
+        for (int i = 0; i < n_before; ++i) {
+            const int sp = REV ? nseg - 1 - i : i;
             const float4 *ph = cluster.map_shared_rank(Hx, sp);
             const float *psum = cluster.map_shared_rank(Sx, sp);
             float tot = 0.0f;
@@ -578,17 +629,24 @@ scan_nsplit_kernel(const ScanParams p)
             for (int r = 0; r < S; ++r)
                 tot += psum[r * CH + cs];
             const float4 he = ph[q * CH + cs];
-            const u64 tt = splat(tot);
-            f01 = fma2(ex2_2(mul2(tt, A01)), f01, pk(he.x, he.y));
-            f23 = fma2(ex2_2(mul2(tt, A23)), f23, pk(he.z, he.w));
+            u64 a01 = ex2_2(mul2(splat(tot), A01)), a23 = ex2_2(mul2(splat(tot), A23));
+            if (RST && *cluster.map_shared_rank(Rx, sp)) {
+                a01 = 0;
+                a23 = 0;
+            }
+            f01 = fma2(a01, f01, pk(he.x, he.y));
+            f23 = fma2(a23, f23, pk(he.z, he.w));
         }
         cluster.sync();   // peers have finished reading this CTA's end state
         h01 = f01;
         h23 = f23;
+    } else {
+        h01 = g01;
+        h23 = g23;
     }
     run(Flag<true>{});
 
-    if (p.final_state && act_s && seg == nseg - 1) {
+    if (p.final_state && act_s && seg == (REV ? 0 : nseg - 1)) {
         float *fs = p.final_state + (b * Dn + ds) * N;
         float hv[4];
         upk(h01, hv[0], hv[1]);
@@ -674,11 +732,11 @@ int pick_segments(int64_t groups, int64_t L, int64_t lc, int64_t slots)
     return n < 1 ? 1 : static_cast<int>(n);
 }
 
-template <typename T, int S>
+template <typename T, int S, bool REV, bool RST>
 ss_status launch_nsplit(const ScanParams &p0, cudaStream_t stream, int sms)
 {
     using SH = NSplitShape<T, S>;
-    auto kernel = scan_nsplit_kernel<T, S>;
+    auto kernel = scan_nsplit_kernel<T, S, REV, RST>;
     const size_t smem = SH::BYTES;
     if (smem > 48u * 1024u) {
         cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -738,13 +796,23 @@ ss_status launch_nsplit(const ScanParams &p0, cudaStream_t stream, int sms)
     return SS_OK;
 }
 
-template <typename T>
-ss_status dispatch_nsplit(const ScanParams &p, cudaStream_t s, int sms)
+template <typename T, bool REV, bool RST>
+ss_status dispatch_nsplit_n(const ScanParams &p, cudaStream_t s, int sms)
 {
-    if (p.N <= 4) return launch_nsplit<T, 1>(p, s, sms);
-    if (p.N <= 8) return launch_nsplit<T, 2>(p, s, sms);
-    if (p.N <= 16) return launch_nsplit<T, 4>(p, s, sms);
-    return launch_nsplit<T, 8>(p, s, sms);
+    if (p.N <= 4) return launch_nsplit<T, 1, REV, RST>(p, s, sms);
+    if (p.N <= 8) return launch_nsplit<T, 2, REV, RST>(p, s, sms);
+    if (p.N <= 16) return launch_nsplit<T, 4, REV, RST>(p, s, sms);
+    return launch_nsplit<T, 8, REV, RST>(p, s, sms);
+}
+
+template <typename T>
+ss_status dispatch_nsplit(const ScanParams &p, bool reverse, cudaStream_t s, int sms)
+{
+    const bool rst = p.reset != nullptr;
+    if (!reverse && !rst) return dispatch_nsplit_n<T, false, false>(p, s, sms);
+    if (!reverse) return dispatch_nsplit_n<T, false, true>(p, s, sms);
+    if (!rst) return dispatch_nsplit_n<T, true, false>(p, s, sms);
+    return dispatch_nsplit_n<T, true, true>(p, s, sms);
 }
 
 // The n-split kernel serves N <= 32 (cutting long sequences into segments
@@ -762,9 +830,9 @@ bool use_nsplit(int64_t N)
 
 template <typename T>
 ss_status scan_fwd(const void *x, const void *dt, const float *A, const void *B, const void *C,
-                   const float *D, const void *z, const float *dt_bias, int softplus, void *y,
-                   float *final_state, int64_t batch, int64_t d_inner, int64_t L, int64_t N,
-                   cudaStream_t stream)
+                   const float *D, const void *z, const float *dt_bias, int softplus, const float *h0,
+                   const uint8_t *reset, int reverse, void *y, float *final_state, int64_t batch,
+                   int64_t d_inner, int64_t L, int64_t N, cudaStream_t stream)
 {
     g_err[0] = '\0';
     if (batch <= 0 || d_inner <= 0 || L <= 0)
@@ -777,13 +845,20 @@ ss_status scan_fwd(const void *x, const void *dt, const float *A, const void *B,
     const PtrCheck list[] = {{x, "x", true},          {dt, "delta", true},  {A, "A", true},
                              {B, "B", true},          {C, "C", true},       {y, "y", true},
                              {D, "D", false},         {z, "z", false},      {dt_bias, "dt_bias", false},
-                             {final_state, "final_state", false}};
+                             {final_state, "final_state", false}, {h0, "h0", false},
+                             {reset, "reset", false}};
+    const bool extended = h0 || reset || reverse;
+    if (extended && N > 32)
+        return fail(SS_ERR_N, "N=%lld: an initial state, sequence starts or the reverse direction need N <= 32",
+                    (long long)N);
     int dev = 0;
     ss_status st = check_ptrs(list, static_cast<int>(sizeof(list) / sizeof(list[0])), &dev);
     if (st != SS_OK)
         return st;
 
     ScanParams p;
+    p.h0 = h0;
+    p.reset = reset;
     p.x = x; p.dt = dt; p.B = B; p.C = C; p.z = z;
     p.A = A; p.D = D; p.dt_bias = dt_bias;
     p.y = y; p.final_state = final_state;
@@ -793,8 +868,8 @@ ss_status scan_fwd(const void *x, const void *dt, const float *A, const void *B,
 
     p.nseg = 1;
     p.seg_len = L;
-    if (use_nsplit(N))
-        return dispatch_nsplit<T>(p, stream, sm_count(dev));
+    if (extended || use_nsplit(N))
+        return dispatch_nsplit<T>(p, reverse != 0, stream, sm_count(dev));
     const int lanes = pick_lanes(batch * d_inner, L, sm_count(dev));
     if (N <= 4)
         return dispatch_scan_lanes<T, 4>(p, lanes, stream);

@@ -51,8 +51,8 @@ ss_status ss_scan_fwd_bf16(const ss_bf16 *x, const ss_bf16 *delta, const float *
                            int delta_softplus, ss_bf16 *y, float *final_state, int64_t batch,
                            int64_t d_inner, int64_t L, int64_t N, cudaStream_t stream)
 {
-    return scan_fwd<__nv_bfloat16>(x, delta, A, B, C, D, z, dt_bias, delta_softplus, y, final_state,
-                                   batch, d_inner, L, N, stream);
+    return scan_fwd<__nv_bfloat16>(x, delta, A, B, C, D, z, dt_bias, delta_softplus, nullptr, nullptr, 0, y,
+                                   final_state, batch, d_inner, L, N, stream);
 }
 
 ss_status ss_scan_fwd_f32(const float *x, const float *delta, const float *A, const float *B,
@@ -60,8 +60,27 @@ ss_status ss_scan_fwd_f32(const float *x, const float *delta, const float *A, co
                           int delta_softplus, float *y, float *final_state, int64_t batch,
                           int64_t d_inner, int64_t L, int64_t N, cudaStream_t stream)
 {
-    return scan_fwd<float>(x, delta, A, B, C, D, z, dt_bias, delta_softplus, y, final_state, batch,
-                           d_inner, L, N, stream);
+    return scan_fwd<float>(x, delta, A, B, C, D, z, dt_bias, delta_softplus, nullptr, nullptr, 0, y, final_state,
+                           batch, d_inner, L, N, stream);
+}
+
+ss_status ss_scan_fwd_ex_bf16(const ss_bf16 *x, const ss_bf16 *delta, const float *A, const ss_bf16 *B,
+                              const ss_bf16 *C, const float *D, const ss_bf16 *z, const float *dt_bias,
+                              int delta_softplus, const float *h0, const uint8_t *seq_start, int reverse,
+                              ss_bf16 *y, float *final_state, int64_t batch, int64_t d_inner, int64_t L, int64_t N,
+                              cudaStream_t stream)
+{
+    return scan_fwd<__nv_bfloat16>(x, delta, A, B, C, D, z, dt_bias, delta_softplus, h0, seq_start, reverse, y,
+                                   final_state, batch, d_inner, L, N, stream);
+}
+
+ss_status ss_scan_fwd_ex_f32(const float *x, const float *delta, const float *A, const float *B, const float *C,
+                             const float *D, const float *z, const float *dt_bias, int delta_softplus,
+                             const float *h0, const uint8_t *seq_start, int reverse, float *y, float *final_state,
+                             int64_t batch, int64_t d_inner, int64_t L, int64_t N, cudaStream_t stream)
+{
+    return scan_fwd<float>(x, delta, A, B, C, D, z, dt_bias, delta_softplus, h0, seq_start, reverse, y, final_state,
+                           batch, d_inner, L, N, stream);
 }
 
 ss_status ss_state_update_bf16(float *state, const ss_bf16 *x, const ss_bf16 *delta, const float *A,

@@ -397,8 +397,68 @@ def check_bwd_linear_in_cotangent(lib):
         np.testing.assert_allclose(g12[k], 2.0 * g1[k] - 3.0 * g2[k], rtol=1e-10, atol=1e-12, err_msg=k)
 
 
+def check_reverse_is_forward_on_flipped_inputs(lib):
+    """The reverse walk equals the forward walk of the time-flipped inputs,
+    flipped back (the recurrence h_t = a_t h_{t+1} + delta_t B_t x_t read from
+    the other end); its final state is the forward walk's final state."""
+    rng = np.random.default_rng(51)
+    p = _bwd_problem(rng, L=13)
+    f = lambda a: np.ascontiguousarray(a[..., ::-1])
+    y_r, fs_r = O.scan_ex(p["x"], p["dt"], p["A"], p["B"], p["C"], D=p["D"], z=p["z"], dt_bias=p["dt_bias"],
+                          h0=p["h0"], reverse=True, threads=1, lib=lib)
+    y_f, fs_f = O.scan(f(p["x"]), f(p["dt"]), p["A"], f(p["B"]), f(p["C"]), D=p["D"], z=f(p["z"]),
+                       dt_bias=p["dt_bias"], h0=p["h0"], threads=1, lib=lib)
+    np.testing.assert_allclose(y_r, f(y_f), rtol=1e-14, atol=1e-15)
+    np.testing.assert_allclose(fs_r, fs_f, rtol=1e-14, atol=1e-15)
+    # no options: the extended walk is the plain scan
+    y0, fs0 = O.scan_ex(p["x"], p["dt"], p["A"], p["B"], p["C"], D=p["D"], z=p["z"], dt_bias=p["dt_bias"],
+                        threads=1, lib=lib)
+    y1, fs1 = O.scan(p["x"], p["dt"], p["A"], p["B"], p["C"], D=p["D"], z=p["z"], dt_bias=p["dt_bias"],
+                     threads=1, lib=lib)
+    np.testing.assert_array_equal(y0, y1)
+    np.testing.assert_array_equal(fs0, fs1)
+
+
+def check_sequence_starts_are_separate_sequences(lib):
+    """Packed sequences with their starts marked give, in either direction,
+    what scanning each sequence on its own from a zero state gives (the
+    state forgets everything at a document break); the initial state reaches
+    only the first sequence walked, and the final state is the last walked
+    sequence's."""
+    rng = np.random.default_rng(52)
+    L = 17
+    p = _bwd_problem(rng, bt=2, L=L)
+    starts = np.zeros((2, L), dtype=bool)
+    cuts = {0: [5, 6, 12], 1: [1, 9]}
+    for b, cs in cuts.items():
+        starts[b, cs] = True
+    for reverse in (False, True):
+        y, fs = O.scan_ex(p["x"], p["dt"], p["A"], p["B"], p["C"], D=p["D"], z=p["z"], dt_bias=p["dt_bias"],
+                          h0=p["h0"], seq_start=starts, reverse=reverse, threads=1, lib=lib)
+        for b, cs in cuts.items():
+            bounds = [0] + cs + [L]
+            pieces = list(zip(bounds[:-1], bounds[1:]))
+            first = pieces[-1] if reverse else pieces[0]
+            for lo, hi in pieces:
+                sl = lambda a: np.ascontiguousarray(a[b:b + 1, ..., lo:hi])
+                h0 = p["h0"][b:b + 1] if (lo, hi) == first else None
+                if reverse:
+                    f = lambda a: np.ascontiguousarray(a[..., ::-1])
+                    yy, ff = O.scan(f(sl(p["x"])), f(sl(p["dt"])), p["A"], f(sl(p["B"])), f(sl(p["C"])),
+                                    D=p["D"], z=f(sl(p["z"])), dt_bias=p["dt_bias"], h0=h0, threads=1, lib=lib)
+                    yy = f(yy)
+                else:
+                    yy, ff = O.scan(sl(p["x"]), sl(p["dt"]), p["A"], sl(p["B"]), sl(p["C"]), D=p["D"],
+                                    z=sl(p["z"]), dt_bias=p["dt_bias"], h0=h0, threads=1, lib=lib)
+                np.testing.assert_allclose(y[b:b + 1, :, lo:hi], yy, rtol=1e-13, atol=1e-14)
+                last = pieces[0] if reverse else pieces[-1]
+                if (lo, hi) == last:
+                    np.testing.assert_allclose(fs[b:b + 1], ff, rtol=1e-13, atol=1e-14)
+
+
 ALL_CHECKS = [check_recurrence_example, check_softplus_values, check_gate_theorem,
               check_selective_copy_euler, check_impulse_response, check_mixing_matrix,
               check_lti_convolution, check_zero_and_huge_step, check_causality_linearity_chain,
               check_conv_impulse_and_silu, check_conv_constant_input_and_zero_history, check_conv_history_chain,
-              check_bwd_finite_differences, check_bwd_impulse_closed_form, check_bwd_linear_in_cotangent]
+              check_bwd_finite_differences, check_bwd_impulse_closed_form, check_bwd_linear_in_cotangent,
+              check_reverse_is_forward_on_flipped_inputs, check_sequence_starts_are_separate_sequences]

@@ -41,6 +41,14 @@ MUTANTS = {
                                "out[r * L + t] = (silu ? acc * sigmoid(acc) : acc) + (bias ? bias[d] : 0.0);")],
     "conv_history_newest_first": [("v = state[(b * (k - 1) + (k - 1 + s)) * d_inner + d];\n                else\n                    v = 0.0;\n                acc",
                                    "v = state[(b * (k - 1) + (-1 - s)) * d_inner + d];\n                else\n                    v = 0.0;\n                acc")],
+    "ex_start_zeroed_on_wrong_side": [("if (starts && !reverse)\n                for (int64_t n = 0; n < N; ++n)\n                    h[n] = 0.0;",
+                                       "if (starts && reverse)\n                for (int64_t n = 0; n < N; ++n)\n                    h[n] = 0.0;"),
+                                      ("if (starts && reverse)\n                for (int64_t n = 0; n < N; ++n)\n                    h[n] = 0.0;\n        }",
+                                       "if (starts && !reverse)\n                for (int64_t n = 0; n < N; ++n)\n                    h[n] = 0.0;\n        }")],
+    "ex_reverse_walks_forward": [("const int64_t t = reverse ? L - 1 - i : i;", "const int64_t t = i;")],
+    "ex_starts_ignored": [("const int starts = seq_start && seq_start[b * L + t];", "const int starts = 0;")],
+    "ex_h0_ignored": [("            h[n] = h0 ? h0[r * N + n] : 0.0;\n        for (int64_t i = 0; i < L; ++i) {",
+                       "            h[n] = 0.0;\n        for (int64_t i = 0; i < L; ++i) {")],
     "bwd_adjoint_without_decay": [("lam[n] *= as[(t + 1) * N + n];", "lam[n] *= 1.0;")],
     "bwd_dA_uses_new_state": [("const double ah = as[t * N + n] * hs[t * N + n];  /* a_t h_{t-1} */",
                                "const double ah = as[t * N + n] * hs[(t + 1) * N + n];")],
