@@ -117,9 +117,10 @@ def profiled_traffic(kernel_key: str):
         return None
     vals = {}
     for line in open(path):
-        if ":" in line and line.strip().startswith(("traffic_bytes_per_launch", "source_sha256")):
-            k, v = line.strip().strip("`").split(":", 1)
-            vals[k.strip()] = v.strip().strip("`")
+        item = line.strip().lstrip("-").strip().strip("`")   # "- `key: value`"
+        if ":" in item and item.startswith(("traffic_bytes_per_launch", "source_sha256")):
+            k, v = item.split(":", 1)
+            vals[k.strip()] = v.strip()
     if vals.get("source_sha256") != src_hash:
         return None
     try:

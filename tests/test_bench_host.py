@@ -76,3 +76,18 @@ def test_shards_differ_by_seed_only():
     a, b = bench.shard_spec(I.MAMBA130M, 0), bench.shard_spec(I.MAMBA130M, 1)
     assert (a.batch, a.d_inner, a.L, a.N) == (b.batch, b.d_inner, b.L, b.N)
     assert a.seed != b.seed
+
+
+def test_profiled_traffic_reads_the_committed_summary(tmp_path, monkeypatch):
+    """The bench takes a kernel's DRAM traffic from its committed ncu summary
+    only while the recorded source hash matches the kernel's source."""
+    import bench
+    key = "conv1d_silu_k4_test"
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    h = bench.kernel_source_hash(key)
+    (prof / (key + ".md")).write_text("# x\n\n- `traffic_bytes_per_launch: 12345`\n- `source_sha256: %s`\n" % h)
+    assert bench.profiled_traffic(key) == 12345.0
+    (prof / (key + ".md")).write_text("- `traffic_bytes_per_launch: 12345`\n- `source_sha256: %s`\n" % ("0" * 64))
+    assert bench.profiled_traffic(key) is None
