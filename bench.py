@@ -35,10 +35,11 @@ HEADLINE = I.MAMBA130M
 METRIC = "selective-scan element-steps/s (B*D*L*N)"
 UNIT = "element-steps/s"
 L2_FLUSH_BYTES = 256 << 20  # > the 126 MB L2
-# A device-side wait enqueued after the flush and before each start event, so
-# that the host has enqueued the timed launch before the event fires: the
-# measured interval then holds the kernel, not the host's launch latency.
-LAUNCH_COVER_CYCLES = 200_000
+# A device-side wait enqueued after the flush and before each start event of a
+# short kernel (the conv kernels, the tiny scan), so that the host has enqueued
+# the timed launch before the event fires: the measured interval then holds the
+# kernel, not the host's launch latency. Long kernels need no cover.
+LAUNCH_COVER_CYCLES = 2_000_000   # about 1 ms at the B300 clock
 FALLBACK_HBM_GBS = 6400.0
 SRC = os.path.join(ROOT, "selective_state_space_138_b300", "csrc", "ss_scan.cu")
 
@@ -216,9 +217,12 @@ def shard_spec(spec: I.ScanSpec, rank: int) -> I.ScanSpec:
     return dataclasses.replace(spec, seed=spec.seed + 1000 * rank)
 
 
-def time_scan(spec: I.ScanSpec, steps: int, warmup: int, flush: bool = True, soak_s: float = 0.0):
+def time_scan(spec: I.ScanSpec, steps: int, warmup: int, flush: bool = True, soak_s: float = 0.0,
+              cover: bool = False):
     """Per-launch device times (ms) of the scan kernel over ``steps`` launches,
-    each preceded by an L2 flush; events on the launching stream."""
+    each preceded by an L2 flush; events on the launching stream. ``cover``
+    adds the device-side wait before each start event (for launches shorter
+    than the host's launch latency)."""
     from selective_state_space_138_b300 import binding
     inp = I.make_scan_inputs(spec)
     g = {k: v.cuda() for k, v in inp.items() if k != "reset_pos"}
@@ -245,7 +249,8 @@ def time_scan(spec: I.ScanSpec, steps: int, warmup: int, flush: bool = True, soa
     for i in range(steps):
         if flush:
             scratch.zero_()
-        torch.cuda._sleep(LAUNCH_COVER_CYCLES)
+        if cover:
+            torch.cuda._sleep(LAUNCH_COVER_CYCLES)
         starts[i].record()
         run()
         ends[i].record()
@@ -423,7 +428,6 @@ def time_bwd(spec: I.ScanSpec, steps: int, warmup: int):
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     for a, b in ev:
         scratch.zero_()
-        torch.cuda._sleep(LAUNCH_COVER_CYCLES)
         a.record()
         run()
         b.record()
@@ -647,7 +651,7 @@ def main(argv=None):
                 "elem_steps_per_s": wspec.elem_steps / (ms * 1e-3), "kernel_ms_median": ms,
                 "roofline": roofline_obj(scan_alg_bytes(wspec), ms, peaks, profiled_traffic("scan_fwd_" + wspec.name),
                                          elem_steps=wspec.elem_steps)}
-        t = time_scan(I.TINY, 20, 3, flush=False)
+        t = time_scan(I.TINY, 20, 3, flush=False, cover=True)
         extras[I.TINY.name] = {"elem_steps_per_s": I.TINY.elem_steps / (statistics.median(t) * 1e-3),
                                "kernel_ms_median": statistics.median(t), "note": "launch-bound; parity case"}
         bms = time_bwd(HEADLINE, 10, 3)
