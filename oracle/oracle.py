@@ -7,6 +7,8 @@ does. Nothing here imports the CUDA library or its binding.
 * ``scan`` / ``scan_rows`` run the plain float64 loop of ``ss_oracle.c`` over
   all rows or over a sample of rows, in parallel over rows (the C call releases
   the GIL).
+* ``ssd`` is Mamba-2's scalar-decay scan (one decay per head of P channels,
+  B and C shared by the heads of a group), time-major layouts.
 * ``scan_ex`` is the scan with an initial state, packed-sequence starts and/or
   the reverse direction.
 * ``scan_bwd`` is the gradient of the scan by the chain rule (float64; the
@@ -58,6 +60,9 @@ def load(path: str | None = None):
     lib.oracle_softplus.restype = ctypes.c_double
     lib.oracle_scan_rows.argtypes = [dp] * 8 + [ctypes.c_int, dp, dp, dp] + [ctypes.c_int64] * 6
     lib.oracle_scan_rows.restype = ctypes.c_int
+    if hasattr(lib, "oracle_ssd_rows"):
+        lib.oracle_ssd_rows.argtypes = [dp] * 8 + [ctypes.c_int, dp, dp, dp] + [ctypes.c_int64] * 8
+        lib.oracle_ssd_rows.restype = ctypes.c_int
     if hasattr(lib, "oracle_scan_ex_rows"):
         lib.oracle_scan_ex_rows.argtypes = ([dp] * 8 + [ctypes.c_int, dp, ctypes.c_void_p, ctypes.c_int, dp, dp]
                                             + [ctypes.c_int64] * 6)
@@ -167,6 +172,41 @@ def scan_ex(x, dt, A, B, C, D=None, z=None, dt_bias=None, delta_softplus=True, h
             codes = list(ex.map(run, range(nt)))
     if any(c != 0 for c in codes):
         raise RuntimeError("oracle_scan_ex_rows failed: %r" % (codes,))
+    return y, fs
+
+
+def ssd(x, dt, A, B, C, D=None, z=None, dt_bias=None, delta_softplus=True, h0=None, threads: int | None = None,
+        lib=None):
+    """Mamba-2's scalar-decay scan (``oracle_ssd_rows``) in float64.
+
+    x, z: (batch, L, H, P); dt: (batch, L, H); B, C: (batch, L, G, N);
+    A, D, dt_bias: (H,); h0: (batch, H, P, N) or None.
+    Returns (y (batch, L, H, P), final_state (batch, H, P, N)).
+    """
+    lib = lib or load()
+    x, dt, A, B, C = map(_f64, (x, dt, A, B, C))
+    D, z, dt_bias, h0 = map(_f64, (D, z, dt_bias, h0))
+    batch, L, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    assert dt.shape == (batch, L, H) and B.shape == (batch, L, G, N) and C.shape == B.shape and A.shape == (H,)
+    y = np.empty_like(x)
+    fs = np.empty((batch, H, P, N))
+    rows = batch * H
+    nt = max(1, min(threads or default_threads(), rows)) if rows else 1
+    bounds = [(rows * i) // nt for i in range(nt + 1)]
+
+    def run(i):
+        return lib.oracle_ssd_rows(_ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(dt_bias),
+                                   int(bool(delta_softplus)), _ptr(h0), _ptr(y), _ptr(fs), batch, L, H, P, G, N,
+                                   bounds[i], bounds[i + 1])
+
+    if nt == 1:
+        codes = [run(0)]
+    else:
+        with ThreadPoolExecutor(nt) as ex:
+            codes = list(ex.map(run, range(nt)))
+    if any(c != 0 for c in codes):
+        raise RuntimeError("oracle_ssd_rows failed: %r" % (codes,))
     return y, fs
 
 

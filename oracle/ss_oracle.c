@@ -350,3 +350,69 @@ int oracle_scan_ex_rows(const double *x, const double *dt, const double *A,
     free(h);
     return 0;
 }
+
+/*
+ * Mamba-2's scalar-decay scan (SSD), written as its recurrence ("Mamba and
+ * selective state spaces": each head, a group of P channels, has one scalar
+ * decay; "Mamba in practice": h_t = alpha_t h_{t-1} + Bbar_t x_t with the
+ * decay a scalar). Per batch b, head h (group g = h / (H / G)):
+ *
+ *   delta_t = softplus(dt[b,t,h] + dt_bias[h])   (or dt + dt_bias)
+ *   alpha_t = exp(delta_t * A[h])
+ *   S_t[p][n] = alpha_t * S_{t-1}[p][n] + delta_t * x[b,t,h,p] * B[b,t,g,n]
+ *   y[b,t,h,p] = sum_n C[b,t,g,n] * S_t[p][n] + D[h] * x[b,t,h,p]
+ *   y *= z * sigmoid(z)                          (when z is given)
+ *
+ * from S_{-1} = h0[b,h] (or 0). Layouts (time-major, as a projection writes
+ * them): x, z, y (batch, L, H, P); dt (batch, L, H); B, C (batch, L, G, N);
+ * A, D, dt_bias (H); h0, final_state (batch, H, P, N). Runs heads
+ * (b, h) = r / H, r % H for r in [row_begin, row_end).
+ */
+int oracle_ssd_rows(const double *x, const double *dt, const double *A, const double *B,
+                    const double *C, const double *D, const double *z, const double *dt_bias,
+                    int delta_softplus, const double *h0, double *y, double *final_state,
+                    int64_t batch, int64_t L, int64_t H, int64_t P, int64_t G, int64_t N,
+                    int64_t row_begin, int64_t row_end)
+{
+    if (!x || !dt || !A || !B || !C || !y || G <= 0 || H % G != 0)
+        return -1;
+    if (batch < 0 || L < 0 || H <= 0 || P <= 0 || N <= 0)
+        return -1;
+    if (row_begin < 0 || row_end > batch * H || row_begin > row_end)
+        return -1;
+    double *S = (double *)malloc((size_t)(P * N) * sizeof(double));
+    if (!S)
+        return -2;
+    for (int64_t r = row_begin; r < row_end; ++r) {
+        const int64_t b = r / H;
+        const int64_t h = r % H;
+        const int64_t g = h / (H / G);
+        for (int64_t i = 0; i < P * N; ++i)
+            S[i] = h0 ? h0[r * P * N + i] : 0.0;
+        for (int64_t t = 0; t < L; ++t) {
+            const double v = dt[(b * L + t) * H + h] + (dt_bias ? dt_bias[h] : 0.0);
+            const double delta = delta_softplus ? oracle_softplus(v) : v;
+            const double alpha = exp(delta * A[h]);
+            const double *Bt = B + ((b * L + t) * G + g) * N;
+            const double *Ct = C + ((b * L + t) * G + g) * N;
+            for (int64_t p = 0; p < P; ++p) {
+                const double xv = x[((b * L + t) * H + h) * P + p];
+                double out = 0.0;
+                for (int64_t n = 0; n < N; ++n) {
+                    S[p * N + n] = alpha * S[p * N + n] + delta * xv * Bt[n];
+                    out += Ct[n] * S[p * N + n];
+                }
+                out += (D ? D[h] : 0.0) * xv;
+                const int64_t o = ((b * L + t) * H + h) * P + p;
+                if (z)
+                    out *= z[o] * sigmoid(z[o]);
+                y[o] = out;
+            }
+        }
+        if (final_state)
+            for (int64_t i = 0; i < P * N; ++i)
+                final_state[r * P * N + i] = S[i];
+    }
+    free(S);
+    return 0;
+}

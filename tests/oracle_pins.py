@@ -456,9 +456,69 @@ def check_sequence_starts_are_separate_sequences(lib):
                     np.testing.assert_allclose(fs[b:b + 1], ff, rtol=1e-13, atol=1e-14)
 
 
+def _ssd_problem(rng, bt=2, L=9, H=4, P=3, G=2, N=5):
+    return dict(x=rng.normal(size=(bt, L, H, P)), dt=rng.normal(size=(bt, L, H)) * 0.5,
+                A=-rng.uniform(0.2, 2.0, size=H), B=rng.normal(size=(bt, L, G, N)), C=rng.normal(size=(bt, L, G, N)),
+                D=rng.normal(size=H), z=rng.normal(size=(bt, L, H, P)), dt_bias=rng.normal(size=H) * 0.3,
+                h0=rng.normal(size=(bt, H, P, N)))
+
+
+def check_ssd_is_the_scan_with_one_decay_per_head(lib):
+    """Mamba-2's scan is the selective scan whose decay rate is the same for
+    all states of a head and whose B, C are shared by the heads of a group:
+    channel d = (h, p) of the S6 oracle with A[d, n] = A[h], dt[d] = dt[h]."""
+    rng = np.random.default_rng(61)
+    p = _ssd_problem(rng)
+    bt, L, H, P = p["x"].shape
+    G, N = p["B"].shape[2:]
+    y, fs = O.ssd(p["x"], p["dt"], p["A"], p["B"], p["C"], D=p["D"], z=p["z"], dt_bias=p["dt_bias"], h0=p["h0"],
+                  threads=1, lib=lib)
+    hpg = H // G
+    for g in range(G):
+        hs = list(range(g * hpg, (g + 1) * hpg))
+        chan = lambda a: np.ascontiguousarray(np.transpose(a[:, :, hs, :], (0, 2, 3, 1)).reshape(bt, hpg * P, L))
+        per_d = lambda v: np.repeat(v[hs], P)
+        y6, f6 = O.scan(chan(p["x"]), np.ascontiguousarray(np.repeat(np.transpose(p["dt"][:, :, hs], (0, 2, 1)), P,
+                                                                     axis=1)),
+                        np.repeat(per_d(p["A"])[:, None], N, axis=1), np.ascontiguousarray(np.transpose(
+                            p["B"][:, :, g, :], (0, 2, 1))), np.ascontiguousarray(np.transpose(p["C"][:, :, g, :],
+                                                                                              (0, 2, 1))),
+                        D=per_d(p["D"]), z=chan(p["z"]), dt_bias=per_d(p["dt_bias"]),
+                        h0=p["h0"][:, hs].reshape(bt, hpg * P, N), threads=1, lib=lib)
+        np.testing.assert_allclose(chan(y), y6, rtol=1e-13, atol=1e-13)
+        np.testing.assert_allclose(fs[:, hs].reshape(bt, hpg * P, N), f6, rtol=1e-13, atol=1e-13)
+
+
+def check_ssd_masked_matmul_form(lib):
+    """The structured-matmul form of the pages ("Mamba in practice": Y is a
+    mask M applied over the pairwise scores C_t . B_s): per head,
+    Y = (M o C B^T) diag(delta) X + D X with M[t, s] = exp(A sum_{s<r<=t} delta_r)
+    for s <= t and 0 above the diagonal, plus exp(A sum_{r<=t} delta_r) C_t h0
+    from an initial state; computed with numpy matrix products."""
+    rng = np.random.default_rng(62)
+    p = _ssd_problem(rng, L=11)
+    bt, L, H, P = p["x"].shape
+    G, N = p["B"].shape[2:]
+    y, fs = O.ssd(p["x"], p["dt"], p["A"], p["B"], p["C"], D=p["D"], dt_bias=p["dt_bias"], h0=p["h0"],
+                  threads=1, lib=lib)
+    v = p["dt"] + p["dt_bias"]
+    delta = np.maximum(v, 0) + np.log1p(np.exp(-np.abs(v)))
+    for b in range(bt):
+        for h in range(H):
+            g = h // (H // G)
+            cs = np.cumsum(delta[b, :, h])
+            M = np.exp(p["A"][h] * (cs[:, None] - cs[None, :])) * np.tri(L)
+            Cb, Bb = p["C"][b, :, g, :], p["B"][b, :, g, :]
+            X = p["x"][b, :, h, :]
+            Y = (M * (Cb @ Bb.T)) @ (delta[b, :, h][:, None] * X) + p["D"][h] * X
+            Y += np.exp(p["A"][h] * cs)[:, None] * (Cb @ p["h0"][b, h].T)
+            np.testing.assert_allclose(y[b, :, h, :], Y, rtol=1e-12, atol=1e-12)
+
+
 ALL_CHECKS = [check_recurrence_example, check_softplus_values, check_gate_theorem,
               check_selective_copy_euler, check_impulse_response, check_mixing_matrix,
               check_lti_convolution, check_zero_and_huge_step, check_causality_linearity_chain,
               check_conv_impulse_and_silu, check_conv_constant_input_and_zero_history, check_conv_history_chain,
               check_bwd_finite_differences, check_bwd_impulse_closed_form, check_bwd_linear_in_cotangent,
-              check_reverse_is_forward_on_flipped_inputs, check_sequence_starts_are_separate_sequences]
+              check_reverse_is_forward_on_flipped_inputs, check_sequence_starts_are_separate_sequences,
+              check_ssd_is_the_scan_with_one_decay_per_head, check_ssd_masked_matmul_form]

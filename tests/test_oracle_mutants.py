@@ -49,6 +49,11 @@ MUTANTS = {
     "ex_starts_ignored": [("const int starts = seq_start && seq_start[b * L + t];", "const int starts = 0;")],
     "ex_h0_ignored": [("            h[n] = h0 ? h0[r * N + n] : 0.0;\n        for (int64_t i = 0; i < L; ++i) {",
                        "            h[n] = 0.0;\n        for (int64_t i = 0; i < L; ++i) {")],
+    "ssd_group_index_wrong": [("const int64_t g = h / (H / G);", "const int64_t g = h % G;")],
+    "ssd_read_before_write": [("S[p * N + n] = alpha * S[p * N + n] + delta * xv * Bt[n];\n                    out += Ct[n] * S[p * N + n];",
+                               "out += Ct[n] * S[p * N + n];\n                    S[p * N + n] = alpha * S[p * N + n] + delta * xv * Bt[n];")],
+    "ssd_decay_without_step": [("const double alpha = exp(delta * A[h]);", "const double alpha = exp(A[h]);")],
+    "ssd_state_transposed": [("final_state[r * P * N + i] = S[i];", "final_state[r * P * N + i] = S[(i % N) * P + i / N];")],
     "bwd_adjoint_without_decay": [("lam[n] *= as[(t + 1) * N + n];", "lam[n] *= 1.0;")],
     "bwd_dA_uses_new_state": [("const double ah = as[t * N + n] * hs[t * N + n];  /* a_t h_{t-1} */",
                                "const double ah = as[t * N + n] * hs[(t + 1) * N + n];")],
