@@ -309,6 +309,44 @@ ss_status ss_scan_bwd_noalloc_f32(const float *x, const float *delta, const floa
                                   float *dz, float *ddt_bias, float *dh0, int64_t batch,
                                   int64_t d_inner, int64_t L, int64_t N, cudaStream_t stream);
 
+/*
+ * ss_ssd_fwd_bf16 -- Mamba-2's scalar-decay scan (SSD): one decay per head of
+ * P channels, B and C shared by the heads of a group ("Mamba and selective
+ * state spaces": Mamba-2 gives each head a single scalar decay, which turns
+ * most of the work into matrix products and allows N = 64 to 256; "Mamba in
+ * practice": h_t = alpha_t h_{t-1} + Bbar_t x_t, Y = M o (C B^T) X with a
+ * 1-semiseparable mask M). Per batch b, head h, group g = h / (nheads / ngroups):
+ *
+ *   delta_t = softplus(dt[b,t,h] + dt_bias[h])   (or dt + dt_bias)
+ *   S_t[p][n] = exp(delta_t A[h]) S_{t-1}[p][n] + delta_t x[b,t,h,p] B[b,t,g,n]
+ *   y[b,t,h,p] = (sum_n C[b,t,g,n] S_t[p][n] + D[h] x[b,t,h,p]) * silu(z[b,t,h,p])
+ *
+ * computed chunk by chunk (64 steps) with the products on the tensor cores
+ * (bf16 operands, fp32 accumulation; the decays, masks and the carried state
+ * are fp32).
+ *
+ *   x, z, y     : (batch, L, nheads, headdim) bf16, time-major; z may be NULL.
+ *   dt          : (batch, L, nheads) bf16 raw step.
+ *   A, D, dt_bias : (nheads) fp32 (A the negative decay rate); D, dt_bias may be NULL.
+ *   B, C        : (batch, L, ngroups, N) bf16.
+ *   h0          : (batch, nheads, headdim, N) fp32 initial state, or NULL.
+ *   final_state : (batch, nheads, headdim, N) fp32 output, or NULL.
+ *   workspace   : >= ss_ssd_workspace_bytes(batch, L, ngroups) bytes of device
+ *                 scratch (holds C_c B_c^T of every chunk), caller-owned.
+ *   headdim = 64, N = 64 or 128, nheads a multiple of ngroups; x, B, C, y, z
+ *   and the workspace 16-byte aligned.
+ * Errors: SS_ERR_NULL, SS_ERR_DIM (sizes, alignment, workspace), SS_ERR_N,
+ * SS_ERR_DEVICE_PTR, SS_ERR_LAUNCH, SS_ERR_INTERNAL.
+ */
+size_t ss_ssd_workspace_bytes(int64_t batch, int64_t L, int64_t ngroups);
+
+ss_status ss_ssd_fwd_bf16(const ss_bf16 *x, const ss_bf16 *dt, const float *A, const ss_bf16 *B,
+                          const ss_bf16 *C, const float *D, const ss_bf16 *z, const float *dt_bias,
+                          int delta_softplus, const float *h0, ss_bf16 *y, float *final_state,
+                          void *workspace, size_t workspace_bytes, int64_t batch, int64_t L,
+                          int64_t nheads, int64_t headdim, int64_t ngroups, int64_t N,
+                          cudaStream_t stream);
+
 /* Message describing the last non-OK status returned on this host thread
  * ("" if none). The string is owned by the library. */
 const char *ss_last_error(void);

@@ -20,7 +20,7 @@ LIB_PATH = os.path.join(_PKG, "libssscan.so")
 EXPORTS = ("ss_scan_fwd_bf16", "ss_scan_fwd_f32", "ss_scan_fwd_ex_bf16", "ss_scan_fwd_ex_f32", "ss_state_update_bf16", "ss_state_update_f32",
            "ss_causal_conv1d_bf16", "ss_causal_conv1d_f32", "ss_conv_state_update_bf16",
            "ss_conv_state_update_f32", "ss_scan_bwd_bf16", "ss_scan_bwd_f32", "ss_scan_bwd_workspace_bytes",
-           "ss_scan_bwd_noalloc_bf16", "ss_scan_bwd_noalloc_f32",
+           "ss_scan_bwd_noalloc_bf16", "ss_scan_bwd_noalloc_f32", "ss_ssd_fwd_bf16", "ss_ssd_workspace_bytes",
            "ss_last_error", "ss_abi_version")
 
 STATUS = {0: "SS_OK", -1: "SS_ERR_NULL", -2: "SS_ERR_DIM", -3: "SS_ERR_N", -4: "SS_ERR_DEVICE_PTR",
@@ -71,6 +71,10 @@ def lib() -> ctypes.CDLL:
     for name in ("ss_scan_bwd_noalloc_bf16", "ss_scan_bwd_noalloc_f32"):
         getattr(L, name).argtypes = [vp] * 8 + [ci] + [vp] * 12 + [i64] * 4 + [vp]
         getattr(L, name).restype = ci
+    L.ss_ssd_fwd_bf16.argtypes = [vp] * 8 + [ci, vp, vp, vp, vp, ctypes.c_size_t] + [i64] * 6 + [vp]
+    L.ss_ssd_fwd_bf16.restype = ci
+    L.ss_ssd_workspace_bytes.argtypes = [i64] * 3
+    L.ss_ssd_workspace_bytes.restype = ctypes.c_size_t
     L.ss_scan_bwd_workspace_bytes.argtypes = [i64] * 4
     L.ss_scan_bwd_workspace_bytes.restype = ctypes.c_size_t
     L.ss_last_error.argtypes = []
@@ -320,3 +324,38 @@ def scan_bwd(x, delta, A, B, C, dout, D=None, z=None, dt_bias=None, delta_softpl
               _ptr(g.get("dz")), _ptr(g.get("ddt_bias")), _ptr(g.get("dh0")), _ptr(workspace),
               workspace.numel() * workspace.element_size(), batch, d_inner, L, N, _stream(stream)))
     return {k: g.get(k) for k in ("dx", "ddelta", "dz", "dA", "dB", "dC", "dD", "ddt_bias", "dh0")}
+
+
+def ssd_workspace_bytes(batch, L, ngroups) -> int:
+    return int(lib().ss_ssd_workspace_bytes(batch, L, ngroups))
+
+
+def ssd_fwd(x, dt, A, B, C, D=None, z=None, dt_bias=None, delta_softplus=True, h0=None, y=None, final_state=None,
+            return_final_state=True, workspace=None, stream=None):
+    """Mamba-2's scalar-decay scan; see ``ss_ssd_fwd_bf16``. x, z: (batch, L,
+    H, P) bf16; dt (batch, L, H) bf16; B, C (batch, L, G, N) bf16; A, D,
+    dt_bias (H,) fp32; h0 (batch, H, P, N) fp32. Returns (y, final_state)."""
+    if x.dtype != torch.bfloat16:
+        raise TypeError("x must be bfloat16")
+    batch, L, H, P = x.shape
+    G, N = (B.shape[2], B.shape[3]) if B.dim() == 4 else (-1, -1)
+    for t, n, dt_, shp in ((dt, "dt", torch.bfloat16, (batch, L, H)), (z, "z", torch.bfloat16, x.shape),
+                           (B, "B", torch.bfloat16, (batch, L, G, N)), (C, "C", torch.bfloat16, (batch, L, G, N)),
+                           (A, "A", torch.float32, (H,)), (D, "D", torch.float32, (H,)),
+                           (dt_bias, "dt_bias", torch.float32, (H,)), (h0, "h0", torch.float32, (batch, H, P, N))):
+        _need(t, n, dt_, shp)
+    _need(x, "x", torch.bfloat16, x.shape)
+    if y is None:
+        y = torch.empty_like(x)
+    _need(y, "y", torch.bfloat16, x.shape)
+    if final_state is None and return_final_state:
+        final_state = torch.empty((batch, H, P, N), dtype=torch.float32, device=x.device)
+    _need(final_state, "final_state", torch.float32, (batch, H, P, N))
+    need = ssd_workspace_bytes(batch, L, G)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=x.device)
+    _check(lib().ss_ssd_fwd_bf16(_ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(dt_bias),
+                                 int(bool(delta_softplus)), _ptr(h0), _ptr(y), _ptr(final_state), _ptr(workspace),
+                                 workspace.numel() * workspace.element_size(), batch, L, H, P, G, N,
+                                 _stream(stream)))
+    return y, final_state

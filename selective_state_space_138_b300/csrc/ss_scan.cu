@@ -12,6 +12,7 @@
 //   scan_bwd.cuh       backward pass (states recomputed)
 //   decode.cuh         single-token state update
 //   conv.cuh           causal depthwise conv1d + SiLU and its decode step
+//   ssd.cuh            Mamba-2's scalar-decay scan on the tensor cores
 // followed here by the extern "C" entry points.
 
 #include <cuda_runtime.h>
@@ -39,6 +40,7 @@ namespace {
 #include "scan_bwd.cuh"
 #include "decode.cuh"
 #include "conv.cuh"
+#include "ssd.cuh"
 
 }  // namespace
 
@@ -175,6 +177,21 @@ ss_status ss_scan_bwd_noalloc_f32(const float *x, const float *delta, const floa
 {
     return scan_bwd_noalloc<float>(x, delta, A, B, C, D, z, dt_bias, delta_softplus, h0, dout, dfinal_state, dx,
                                    ddelta, dA, dB, dC, dD, dz, ddt_bias, dh0, batch, d_inner, L, N, stream);
+}
+
+size_t ss_ssd_workspace_bytes(int64_t batch, int64_t L, int64_t ngroups)
+{
+    return ssd_workspace_bytes(batch, L, ngroups);
+}
+
+ss_status ss_ssd_fwd_bf16(const ss_bf16 *x, const ss_bf16 *dt, const float *A, const ss_bf16 *B, const ss_bf16 *C,
+                          const float *D, const ss_bf16 *z, const float *dt_bias, int delta_softplus,
+                          const float *h0, ss_bf16 *y, float *final_state, void *workspace, size_t workspace_bytes,
+                          int64_t batch, int64_t L, int64_t nheads, int64_t headdim, int64_t ngroups, int64_t N,
+                          cudaStream_t stream)
+{
+    return ssd_fwd(x, dt, A, B, C, D, z, dt_bias, delta_softplus, h0, y, final_state, workspace, workspace_bytes,
+                   batch, L, nheads, headdim, ngroups, N, stream);
 }
 
 const char *ss_last_error(void) { return g_err; }

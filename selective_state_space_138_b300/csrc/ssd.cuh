@@ -1,0 +1,486 @@
+// ssd.cuh -- Mamba-2's scalar-decay scan (SSD) on the tensor cores, and its launch logic.
+//
+// Part of the single translation unit ss_scan.cu (included inside its
+// anonymous namespace); not compiled on its own.
+//
+// With one decay per head ("Mamba and selective state spaces": each head, a
+// group of P channels, gets a single scalar decay, which turns most of the work
+// into matrix products; "Mamba in practice": Y = M o (pairwise scores) X with a
+// 1-semiseparable mask M), a chunk of Q steps of one head is
+//
+//   Y_c = diag(e^{cum}) C_c H_{c-1}^T + (CB_c o M_c o delta) X_c + D X_c
+//   H_c = e^{cum[Q-1]} H_{c-1} + (w o X_c)^T B_c,   w_s = e^{cum[Q-1] - cum[s]} delta_s
+//
+// where cum[t] = A_h * (delta_0 + .. + delta_t) within the chunk, CB_c = C_c B_c^T
+// (Q x Q, shared by the heads of a group), M_c[t][s] = e^{cum[t] - cum[s]} for
+// s <= t and 0 above the diagonal, and H (P x N, fp32) is the state carried
+// between chunks. Every product is a bf16 x bf16 -> fp32 tensor-core MMA
+// (mma.sync m16n8k16); the decays, masks and the carried state are fp32, and
+// the state enters C_c H^T as a bf16 high part plus a bf16 residual (two
+// MMAs), straight from the accumulator registers that hold it.
+//
+//   ssd_cb_kernel     CB_c for every (batch, chunk, group) into the workspace.
+//   ssd_chunk_kernel  one CTA per (batch, head), walking its chunks in order.
+
+constexpr int kSsdQ = 64;    // steps per chunk
+constexpr int kSsdP = 64;    // channels per head (headdim)
+
+struct SsdParams {
+    const __nv_bfloat16 *x, *dt, *B, *C, *z;
+    const float *A, *D, *dt_bias, *h0;
+    __nv_bfloat16 *y;
+    float *final_state;
+    float *cb;   // workspace: [batch][nchunks][G][Q][Q] fp32
+    int64_t batch, L, H, G, nchunks;
+    int softplus;
+};
+
+// ---- warp-level MMA helpers (PTX mma.sync / ldmatrix; operands in shared memory)
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];\n"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];\n"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+// D += A (16x16, row) * B (16x8, col), bf16 in, fp32 accumulate
+__device__ __forceinline__ void mma_bf16(float *d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                         uint32_t b1)
+{
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+                 "{%8, %9}, {%0, %1, %2, %3};\n"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// A fragment (16 rows x 16 k) of a row-major bf16 tile: rows r0.., k0.., row stride `ld` elements
+__device__ __forceinline__ void frag_a(const __nv_bfloat16 *base, int ld, int r0, int k0, int lane, uint32_t *a)
+{
+    const int r = r0 + (lane & 7) + ((lane >> 3) & 1) * 8;
+    const int k = k0 + (lane >> 4) * 8;
+    ldsm_x4(smem_u32(base + r * ld + k), a[0], a[1], a[2], a[3]);
+}
+
+// A fragment of the transpose of a row-major tile T (A[m][k] = T[k][m]): m0.., k0..
+__device__ __forceinline__ void frag_a_t(const __nv_bfloat16 *base, int ld, int m0, int k0, int lane, uint32_t *a)
+{
+    const int k = k0 + (lane & 7) + (lane >> 4) * 8;
+    const int m = m0 + ((lane >> 3) & 1) * 8;
+    ldsm_x4_t(smem_u32(base + k * ld + m), a[0], a[1], a[2], a[3]);
+}
+
+// B fragments for two 8-column tiles (n0.. and n0+8..) x 16 k, from a tile stored
+// [n][k] (k contiguous): b[0], b[1] for columns n0..n0+7, b[2], b[3] for n0+8..
+__device__ __forceinline__ void frag_b_nk(const __nv_bfloat16 *base, int ld, int n0, int k0, int lane, uint32_t *b)
+{
+    const int n = n0 + (lane & 7) + (lane >> 4) * 8;
+    const int k = k0 + ((lane >> 3) & 1) * 8;
+    ldsm_x4(smem_u32(base + n * ld + k), b[0], b[1], b[2], b[3]);
+}
+
+// the same from a tile stored [k][n] (n contiguous)
+__device__ __forceinline__ void frag_b_kn(const __nv_bfloat16 *base, int ld, int n0, int k0, int lane, uint32_t *b)
+{
+    const int k = k0 + (lane & 7) + ((lane >> 3) & 1) * 8;
+    const int n = n0 + (lane >> 4) * 8;
+    ldsm_x4_t(smem_u32(base + k * ld + n), b[0], b[1], b[2], b[3]);
+}
+
+// Copy `rows` rows of `row_elems` bf16 (a multiple of 8) from global rows at
+// stride `gstride` elements into shared rows at stride `sld`, zero-filling rows
+// at or past `valid`, with 16-byte cp.async pieces spread over the CTA.
+__device__ __forceinline__ void stage_rows(__nv_bfloat16 *s, int sld, const __nv_bfloat16 *g, int64_t gstride,
+                                           int rows, int row_elems, int valid, int tid, int nthreads)
+{
+    const int ppr = row_elems / 8;
+    for (int i = tid; i < rows * ppr; i += nthreads) {
+        const int r = i / ppr;
+        const int c = (i % ppr) * 8;
+        const bool ok = r < valid;
+        cp_async16(smem_u32(s + r * sld + c), ok ? g + r * gstride + c : g, ok ? 16 : 0);
+    }
+}
+
+// ---- CB_c = C_c B_c^T, one CTA (4 warps) per (chunk, batch, group)
+template <int N>
+__global__ void __launch_bounds__(128)
+ssd_cb_kernel(const SsdParams p)
+{
+    constexpr int Q = kSsdQ, LDN = N + 8;
+    __shared__ __align__(16) __nv_bfloat16 Cs[Q * LDN];
+    __shared__ __align__(16) __nv_bfloat16 Bs[Q * LDN];
+    const int c = blockIdx.x;
+    const int64_t b = blockIdx.y;
+    const int g = blockIdx.z;
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    const int64_t t0 = static_cast<int64_t>(c) * Q;
+    const int valid = static_cast<int>(p.L - t0 < Q ? p.L - t0 : Q);
+    const int64_t rs = p.G * N;   // B, C row stride
+    stage_rows(Cs, LDN, p.C + ((b * p.L + t0) * p.G + g) * N, rs, Q, N, valid, tid, 128);
+    stage_rows(Bs, LDN, p.B + ((b * p.L + t0) * p.G + g) * N, rs, Q, N, valid, tid, 128);
+    cp_async_commit();
+    cp_async_wait<0>();
+    __syncthreads();
+    float acc[8][4];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.0f;
+#pragma unroll
+    for (int kk = 0; kk < N; kk += 16) {
+        uint32_t a[4];
+        frag_a(Cs, LDN, 16 * w, kk, lane, a);
+#pragma unroll
+        for (int j = 0; j < 8; j += 2) {
+            uint32_t bb[4];
+            frag_b_nk(Bs, LDN, 8 * j, kk, lane, bb);   // column s = row of B_c
+            mma_bf16(acc[j], a[0], a[1], a[2], a[3], bb[0], bb[1]);
+            mma_bf16(acc[j + 1], a[0], a[1], a[2], a[3], bb[2], bb[3]);
+        }
+    }
+    float *out = p.cb + (((b * p.nchunks + c) * p.G + g) * Q) * Q;
+    const int gr = lane >> 2, t4 = lane & 3;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const int col = 8 * j + 2 * t4;
+        *reinterpret_cast<float2 *>(out + (16 * w + gr) * Q + col) = make_float2(acc[j][0], acc[j][1]);
+        *reinterpret_cast<float2 *>(out + (16 * w + gr + 8) * Q + col) = make_float2(acc[j][2], acc[j][3]);
+    }
+}
+
+template <int N>
+struct SsdShape {
+    static constexpr int Q = kSsdQ, P = kSsdP;
+    static constexpr int LDP = P + 8, LDN = N + 8, LDQ = Q + 8, LDF = Q + 4;
+    static constexpr int X_OFF = 0;                                  // X_c   [Q][LDP] bf16
+    static constexpr int Z_OFF = X_OFF + Q * LDP * 2;                // z_c   [Q][LDP] bf16
+    static constexpr int B_OFF = Z_OFF + Q * LDP * 2;                // B_c   [Q][LDN] bf16
+    static constexpr int C_OFF = B_OFF + Q * LDN * 2;                // C_c   [Q][LDN] bf16
+    static constexpr int CB_OFF = C_OFF + Q * LDN * 2;               // CB_c  [Q][LDF] fp32
+    static constexpr int S_OFF = CB_OFF + Q * LDF * 4;               // S'_c  [Q][LDQ] bf16
+    static constexpr int XW_OFF = S_OFF + Q * LDQ * 2;               // w o X [Q][LDP] bf16
+    static constexpr int CUM_OFF = XW_OFF + Q * LDP * 2;             // cum[Q], delta[Q] fp32
+    static constexpr size_t BYTES = CUM_OFF + 2 * Q * 4;
+};
+
+// ---- one CTA (4 warps) per (batch, head); the chunks of the row in order.
+// Warp w owns channels p = 16w .. 16w+15: those rows of H and those columns of Y_c.
+template <int N>
+__global__ void __launch_bounds__(128, 2)
+ssd_chunk_kernel(const SsdParams p)
+{
+    using SH = SsdShape<N>;
+    constexpr int Q = SH::Q, P = SH::P, LDP = SH::LDP, LDN = SH::LDN, LDQ = SH::LDQ, LDF = SH::LDF;
+    constexpr int NT = N / 8;   // 8-column tiles of the state
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    __nv_bfloat16 *Xs = reinterpret_cast<__nv_bfloat16 *>(smem_raw + SH::X_OFF);
+    __nv_bfloat16 *Zs = reinterpret_cast<__nv_bfloat16 *>(smem_raw + SH::Z_OFF);
+    __nv_bfloat16 *Bs = reinterpret_cast<__nv_bfloat16 *>(smem_raw + SH::B_OFF);
+    __nv_bfloat16 *Cs = reinterpret_cast<__nv_bfloat16 *>(smem_raw + SH::C_OFF);
+    float *CBs = reinterpret_cast<float *>(smem_raw + SH::CB_OFF);
+    __nv_bfloat16 *Sp = reinterpret_cast<__nv_bfloat16 *>(smem_raw + SH::S_OFF);
+    __nv_bfloat16 *Xw = reinterpret_cast<__nv_bfloat16 *>(smem_raw + SH::XW_OFF);
+    float *cum = reinterpret_cast<float *>(smem_raw + SH::CUM_OFF);
+    float *dl = cum + Q;
+
+    const int64_t b = blockIdx.y;
+    const int h = blockIdx.x;
+    const int g = static_cast<int>(h / (p.H / p.G));
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    const int gr = lane >> 2, t4 = lane & 3;
+    const float Ah = __ldg(p.A + h);
+    const float Dh = p.D ? __ldg(p.D + h) : 0.0f;
+    const float bias = p.dt_bias ? __ldg(p.dt_bias + h) : 0.0f;
+    const bool gate = p.z != nullptr;
+    const int64_t xs = p.H * P;   // x, z, y row stride (one time step)
+
+    // the carried state H, fp32 fragments: rows p = 16w + gr (+8), columns n = 8j + 2t4 (+1)
+    float Hf[NT][4];
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int pr = 16 * w + gr + (e >> 1) * 8;
+            const int n = 8 * j + 2 * t4 + (e & 1);
+            Hf[j][e] = p.h0 ? p.h0[((b * p.H + h) * P + pr) * N + n] : 0.0f;
+        }
+    }
+    bool have_state = p.h0 != nullptr;
+    for (int64_t c = 0; c < p.nchunks; ++c) {
+        const int64_t t0 = c * Q;
+        const int valid = static_cast<int>(p.L - t0 < Q ? p.L - t0 : Q);
+        // ---- stage the chunk
+        stage_rows(Xs, LDP, p.x + ((b * p.L + t0) * p.H + h) * P, xs, Q, P, valid, tid, 128);
+        if (gate)
+            stage_rows(Zs, LDP, p.z + ((b * p.L + t0) * p.H + h) * P, xs, Q, P, valid, tid, 128);
+        stage_rows(Bs, LDN, p.B + ((b * p.L + t0) * p.G + g) * N, p.G * N, Q, N, valid, tid, 128);
+        stage_rows(Cs, LDN, p.C + ((b * p.L + t0) * p.G + g) * N, p.G * N, Q, N, valid, tid, 128);
+        {
+            const float *cbg = p.cb + (((b * p.nchunks + c) * p.G + g) * Q) * Q;
+            for (int i = tid; i < Q * (Q / 4); i += 128) {
+                const int r = i / (Q / 4), q4 = (i % (Q / 4)) * 4;
+                cp_async16(smem_u32(CBs + r * LDF + q4), cbg + r * Q + q4, 16);
+            }
+        }
+        cp_async_commit();
+        // the step sizes of the chunk (zero past L)
+        if (tid < Q) {
+            float d = 0.0f;
+            if (tid < valid) {
+                const float v = __bfloat162float(p.dt[(b * p.L + t0 + tid) * p.H + h]) + bias;
+                d = p.softplus ? softplus_f(v) : v;
+            }
+            dl[tid] = d;
+        }
+        cp_async_wait<0>();
+        __syncthreads();
+        // ---- cum[t] = A_h * (delta_0 + .. + delta_t), one warp
+        if (w == 0) {
+            const float a0 = Ah * dl[2 * lane], a1 = Ah * dl[2 * lane + 1];
+            float s = a0 + a1;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float u = __shfl_up_sync(0xffffffffu, s, o);
+                if (lane >= o)
+                    s += u;
+            }
+            cum[2 * lane] = s - a1;
+            cum[2 * lane + 1] = s;
+        }
+        __syncthreads();
+        // ---- S' = CB o M o delta (bf16) and w o X (bf16)
+        const float cq = cum[Q - 1];
+        for (int i = tid; i < Q * Q / 2; i += 128) {
+            const int t = i / (Q / 2), s2 = (i % (Q / 2)) * 2;
+            float v0 = 0.0f, v1 = 0.0f;
+            if (s2 <= t)
+                v0 = CBs[t * LDF + s2] * ex2_approx((cum[t] - cum[s2]) * kLog2e) * dl[s2];
+            if (s2 + 1 <= t)
+                v1 = CBs[t * LDF + s2 + 1] * ex2_approx((cum[t] - cum[s2 + 1]) * kLog2e) * dl[s2 + 1];
+            *reinterpret_cast<uint32_t *>(Sp + t * LDQ + s2) = pack_bf16x2(v0, v1);
+        }
+        for (int i = tid; i < Q * P / 2; i += 128) {
+            const int s = i / (P / 2), p2 = (i % (P / 2)) * 2;
+            const float ws = ex2_approx((cq - cum[s]) * kLog2e) * dl[s];
+            const uint32_t xw = *reinterpret_cast<const uint32_t *>(Xs + s * LDP + p2);
+            *reinterpret_cast<uint32_t *>(Xw + s * LDP + p2) = pack_bf16x2(bf16lo(xw) * ws, bf16hi(xw) * ws);
+        }
+        __syncthreads();
+
+        // ---- Y columns p = 16w .. 16w+15, all Q rows: e^{cum[t]} C_c H^T + S' X_c.
+        // The warp's own state rows are the B operand of C_c H^T, taken from its
+        // fp32 accumulators as a bf16 high part plus a bf16 residual.
+        float acc[4][2][4];   // [row tile][column tile][fragment]
+#pragma unroll
+        for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+                acc[mt][nt][0] = acc[mt][nt][1] = acc[mt][nt][2] = acc[mt][nt][3] = 0.0f;
+        if (have_state) {
+#pragma unroll
+            for (int kk = 0; kk < N / 16; ++kk) {
+                uint32_t bh[2][2], bl[2][2];   // [column tile][b0, b1]
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        const float v0 = Hf[2 * kk + half][2 * nt], v1 = Hf[2 * kk + half][2 * nt + 1];
+                        const uint32_t hi = pack_bf16x2(v0, v1);
+                        bh[nt][half] = hi;
+                        bl[nt][half] = pack_bf16x2(v0 - bf16lo(hi), v1 - bf16hi(hi));
+                    }
+                }
+#pragma unroll
+                for (int mt = 0; mt < 4; ++mt) {
+                    uint32_t a[4];
+                    frag_a(Cs, LDN, 16 * mt, 16 * kk, lane, a);
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt) {
+                        mma_bf16(acc[mt][nt], a[0], a[1], a[2], a[3], bh[nt][0], bh[nt][1]);
+                        mma_bf16(acc[mt][nt], a[0], a[1], a[2], a[3], bl[nt][0], bl[nt][1]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int mt = 0; mt < 4; ++mt) {
+                const float e0 = ex2_approx(cum[16 * mt + gr] * kLog2e);
+                const float e1 = ex2_approx(cum[16 * mt + gr + 8] * kLog2e);
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    acc[mt][nt][0] *= e0;
+                    acc[mt][nt][1] *= e0;
+                    acc[mt][nt][2] *= e1;
+                    acc[mt][nt][3] *= e1;
+                }
+            }
+        }
+#pragma unroll
+        for (int kk = 0; kk < Q; kk += 16) {
+            uint32_t bb[4];
+            frag_b_kn(Xs, LDP, 16 * w, kk, lane, bb);    // X stored [s][p]: k = s, columns 16w ..
+#pragma unroll
+            for (int mt = 0; mt < 4; ++mt) {
+                uint32_t a[4];
+                frag_a(Sp, LDQ, 16 * mt, kk, lane, a);
+                mma_bf16(acc[mt][0], a[0], a[1], a[2], a[3], bb[0], bb[1]);
+                mma_bf16(acc[mt][1], a[0], a[1], a[2], a[3], bb[2], bb[3]);
+            }
+        }
+        // ---- epilogue: + D x, gate, store
+#pragma unroll
+        for (int mt = 0; mt < 4; ++mt) {
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                const int t = 16 * mt + gr + half * 8;
+                if (t < valid) {
+                    __nv_bfloat16 *yr = p.y + ((b * p.L + t0 + t) * p.H + h) * P;
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt) {
+                        const int col = 16 * w + 8 * nt + 2 * t4;
+                        const uint32_t xw = *reinterpret_cast<const uint32_t *>(Xs + t * LDP + col);
+                        float o0 = fmaf(Dh, bf16lo(xw), acc[mt][nt][2 * half]);
+                        float o1 = fmaf(Dh, bf16hi(xw), acc[mt][nt][2 * half + 1]);
+                        if (gate) {
+                            const uint32_t zw = *reinterpret_cast<const uint32_t *>(Zs + t * LDP + col);
+                            o0 *= silu_f(bf16lo(zw));
+                            o1 *= silu_f(bf16hi(zw));
+                        }
+                        *reinterpret_cast<uint32_t *>(yr + col) = pack_bf16x2(o0, o1);
+                    }
+                }
+            }
+        }
+
+        // ---- H rows p = 16w .. : e^{cum[Q-1]} H + (w o X)^T B_c
+        const float ec = ex2_approx(cq * kLog2e);
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+            Hf[j][0] *= ec;
+            Hf[j][1] *= ec;
+            Hf[j][2] *= ec;
+            Hf[j][3] *= ec;
+        }
+#pragma unroll
+        for (int kk = 0; kk < Q; kk += 16) {
+            uint32_t a[4];
+            frag_a_t(Xw, LDP, 16 * w, kk, lane, a);          // A[p][s] = Xw[s][p]
+#pragma unroll
+            for (int j = 0; j < NT; j += 2) {
+                uint32_t bb[4];
+                frag_b_kn(Bs, LDN, 8 * j, kk, lane, bb);     // B_c stored [s][n]: k = s, column n
+                mma_bf16(Hf[j], a[0], a[1], a[2], a[3], bb[0], bb[1]);
+                mma_bf16(Hf[j + 1], a[0], a[1], a[2], a[3], bb[2], bb[3]);
+            }
+        }
+        have_state = true;
+        __syncthreads();   // every warp is done with Xs, Sp, Xw, ... of this chunk
+    }
+    if (p.final_state) {
+        float *fs = p.final_state + ((b * p.H + h) * P) * N;
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+            const int n = 8 * j + 2 * t4;
+            *reinterpret_cast<float2 *>(fs + (16 * w + gr) * N + n) = make_float2(Hf[j][0], Hf[j][1]);
+            *reinterpret_cast<float2 *>(fs + (16 * w + gr + 8) * N + n) = make_float2(Hf[j][2], Hf[j][3]);
+        }
+    }
+}
+
+// ------------------------------------------------------------------ SSD host side
+
+size_t ssd_workspace_bytes(int64_t batch, int64_t L, int64_t G)
+{
+    if (batch <= 0 || L <= 0 || G <= 0)
+        return 0;
+    const int64_t nchunks = (L + kSsdQ - 1) / kSsdQ;
+    return static_cast<size_t>(batch) * nchunks * G * kSsdQ * kSsdQ * 4;
+}
+
+template <int N>
+ss_status launch_ssd(const SsdParams &p, cudaStream_t stream)
+{
+    using SH = SsdShape<N>;
+    if (p.nchunks > 0x7fffffff || p.batch > 65535 || p.G > 65535 || p.H > 0x7fffffff)
+        return fail(SS_ERR_DIM, "grid too large");
+    ssd_cb_kernel<N><<<dim3(static_cast<unsigned>(p.nchunks), static_cast<unsigned>(p.batch),
+                            static_cast<unsigned>(p.G)), 128, 0, stream>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return fail(SS_ERR_LAUNCH, "SSD CB kernel launch failed: %s", cudaGetErrorString(e));
+    auto kernel = ssd_chunk_kernel<N>;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(SH::BYTES));
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(SS_ERR_LAUNCH, "cudaFuncSetAttribute failed: %s", cudaGetErrorString(e));
+    }
+    kernel<<<dim3(static_cast<unsigned>(p.H), static_cast<unsigned>(p.batch)), 128, SH::BYTES, stream>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return fail(SS_ERR_LAUNCH, "SSD chunk kernel launch failed: %s", cudaGetErrorString(e));
+    return SS_OK;
+}
+
+ss_status ssd_fwd(const void *x, const void *dt, const float *A, const void *B, const void *C, const float *D,
+                  const void *z, const float *dt_bias, int softplus, const float *h0, void *y, float *final_state,
+                  void *workspace, size_t workspace_bytes, int64_t batch, int64_t L, int64_t nheads,
+                  int64_t headdim, int64_t ngroups, int64_t N, cudaStream_t stream)
+{
+    g_err[0] = '\0';
+    if (batch <= 0 || L <= 0 || nheads <= 0 || ngroups <= 0)
+        return fail(SS_ERR_DIM, "sizes must be positive: batch=%lld L=%lld nheads=%lld ngroups=%lld",
+                    (long long)batch, (long long)L, (long long)nheads, (long long)ngroups);
+    if (nheads % ngroups != 0)
+        return fail(SS_ERR_DIM, "nheads=%lld is not a multiple of ngroups=%lld", (long long)nheads,
+                    (long long)ngroups);
+    if (headdim != kSsdP)
+        return fail(SS_ERR_DIM, "headdim=%lld: this kernel takes headdim %d", (long long)headdim, kSsdP);
+    if (N != 64 && N != 128)
+        return fail(SS_ERR_N, "N=%lld: this kernel takes N = 64 or 128", (long long)N);
+    if (batch > (int64_t(1) << 40) / L || batch * L > (int64_t(1) << 50) / (nheads * headdim))
+        return fail(SS_ERR_DIM, "element count overflows");
+    const PtrCheck list[] = {{x, "x", true},       {dt, "dt", true},         {A, "A", true},
+                             {B, "B", true},       {C, "C", true},           {y, "y", true},
+                             {workspace, "workspace", true}, {D, "D", false}, {z, "z", false},
+                             {dt_bias, "dt_bias", false},    {h0, "h0", false},
+                             {final_state, "final_state", false}};
+    int dev = 0;
+    ss_status st = check_ptrs(list, static_cast<int>(sizeof(list) / sizeof(list[0])), &dev);
+    if (st != SS_OK)
+        return st;
+    const size_t need = ssd_workspace_bytes(batch, L, ngroups);
+    if (workspace_bytes < need)
+        return fail(SS_ERR_DIM, "workspace of %zu bytes is smaller than the %zu bytes required", workspace_bytes,
+                    need);
+    const void *ptrs[] = {x, B, C, y, workspace, z};
+    for (const void *q : ptrs)
+        if (q && !aligned16(q))
+            return fail(SS_ERR_DIM, "x, B, C, y, z and the workspace must be 16-byte aligned");
+    if ((ngroups * N * 2) % 16 != 0)
+        return fail(SS_ERR_DIM, "B and C rows must be whole 16-byte pieces");
+    SsdParams p;
+    p.x = static_cast<const __nv_bfloat16 *>(x);
+    p.dt = static_cast<const __nv_bfloat16 *>(dt);
+    p.B = static_cast<const __nv_bfloat16 *>(B);
+    p.C = static_cast<const __nv_bfloat16 *>(C);
+    p.z = static_cast<const __nv_bfloat16 *>(z);
+    p.A = A; p.D = D; p.dt_bias = dt_bias; p.h0 = h0;
+    p.y = static_cast<__nv_bfloat16 *>(y);
+    p.final_state = final_state;
+    p.cb = static_cast<float *>(workspace);
+    p.batch = batch; p.L = L; p.H = nheads; p.G = ngroups;
+    p.nchunks = (L + kSsdQ - 1) / kSsdQ;
+    p.softplus = softplus ? 1 : 0;
+    return N == 64 ? launch_ssd<64>(p, stream) : launch_ssd<128>(p, stream);
+}

@@ -256,3 +256,47 @@ def make_bwd_inputs(spec: ScanSpec) -> dict:
     return dict(dout=normal(s, TAG_DOUT, (Bt, Dn, L), 1.0, spec.torch_dtype),
                 dfinal=normal(s, TAG_DFINAL, (Bt, Dn, N), 1.0, torch.float32),
                 h0=normal(s, TAG_H0, (Bt, Dn, N), 1.0, torch.float32))
+
+
+@dataclass
+class SsdSpec:
+    """Shape and recipe of one scalar-decay (Mamba-2) scan workload."""
+
+    batch: int
+    L: int
+    nheads: int
+    headdim: int = 64
+    ngroups: int = 1
+    N: int = 128
+    seed: int = 0
+    name: str = ""
+
+    @property
+    def elem_steps(self) -> int:
+        return self.batch * self.L * self.nheads * self.headdim * self.N
+
+
+def make_ssd_inputs(spec: SsdSpec) -> dict:
+    """Inputs of a scalar-decay scan, time-major, as CPU tensors: x, z
+    (batch, L, H, P), dt (batch, L, H), B, C (batch, L, G, N) in bf16; A, D,
+    dt_bias (H,) fp32. x, z, B, C ~ N(0, 1), dt ~ N(0, 0.1); dt_bias =
+    softplus^-1(u), u log-uniform in [1e-3, 1e-1] per head; A_h = -(1 + 15 v_h),
+    v_h uniform in [0, 1) (decay rates spread over [1, 16] per head); D = 1."""
+    Bt, L, H, P, G, N, s = spec.batch, spec.L, spec.nheads, spec.headdim, spec.ngroups, spec.N, spec.seed
+    x = normal(s, TAG_X, (Bt, L, H, P), 1.0, torch.bfloat16)
+    z = normal(s, TAG_Z, (Bt, L, H, P), 1.0, torch.bfloat16)
+    B = normal(s, TAG_B, (Bt, L, G, N), 1.0, torch.bfloat16)
+    C = normal(s, TAG_C, (Bt, L, G, N), 1.0, torch.bfloat16)
+    dt = normal(s, TAG_DT, (Bt, L, H), 0.1, torch.bfloat16)
+    rng = np.random.default_rng([s, TAG_U, 0])
+    u = np.exp(rng.uniform(math.log(1e-3), math.log(1e-1), size=H))
+    dt_bias = torch.from_numpy(_inv_softplus(u).astype(np.float32))
+    rng = np.random.default_rng([s, TAG_EPS, 0])
+    A = torch.from_numpy((-(1.0 + 15.0 * rng.random(H))).astype(np.float32))
+    D = torch.ones(H, dtype=torch.float32)
+    return dict(x=x, z=z, B=B, C=C, dt=dt, A=A, D=D, dt_bias=dt_bias)
+
+
+# one Mamba-2 layer of the 2.7B width (d_model 2560, expand 2: 80 heads of 64, N = 128)
+MAMBA2_LAYER = SsdSpec(batch=8, L=2048, nheads=80, headdim=64, ngroups=1, N=128, seed=7,
+                       name="mamba2_layer_b8_l2048_h80_p64_n128")
