@@ -95,7 +95,7 @@ def measured_peaks() -> dict:
 
 # the source part each profiled kernel lives in (besides the shared device helpers)
 KERNEL_PART = {"scan_fwd_": "scan_fwd.cuh", "state_update_": "decode.cuh", "scan_bwd_": "scan_bwd.cuh",
-               "conv1d_": "conv.cuh"}
+               "conv1d_": "conv.cuh", "ssd_chunk_": "ssd.cuh"}
 
 
 def kernel_source_hash(kernel_key: str) -> str:
@@ -435,6 +435,48 @@ def time_bwd(spec: I.ScanSpec, steps: int, warmup: int):
     return statistics.median([a.elapsed_time(b) for a, b in ev])
 
 
+def ssd_alg(spec: I.SsdSpec):
+    """(bytes, flops) the scalar-decay scan must move and compute: read x, z,
+    dt and write y (batch, L, H, P / H); read B, C (batch, L, G, N); A, D,
+    dt_bias; write the final state (batch, H, P, N) fp32. FLOPs: the chunked
+    algorithm's products, 2 Q^2 N per (batch, chunk, group) for C B^T and
+    2 Q^2 P + 4 Q N P per (batch, chunk, head) for the masked product, the
+    state readout and the state update (Q = 64)."""
+    b, L, H, P, G, N = spec.batch, spec.L, spec.nheads, spec.headdim, spec.ngroups, spec.N
+    q = 64
+    chunks = (L + q - 1) // q
+    by = 3 * b * L * H * P * 2 + b * L * H * 2 + 2 * b * L * G * N * 2 + 3 * H * 4 + b * H * P * N * 4
+    fl = b * chunks * (G * 2 * q * q * N + H * (2 * q * q * P + 4 * q * N * P))
+    return by, fl
+
+
+def time_ssd(spec: I.SsdSpec, steps: int, warmup: int):
+    """Median device time (ms) of the scalar-decay scan (both kernels), L2
+    flushed before each launch."""
+    from selective_state_space_138_b300 import binding
+    inp = I.make_ssd_inputs(spec)
+    g = {k: v.cuda() for k, v in inp.items()}
+    y = torch.empty_like(g["x"])
+    fs = torch.empty(spec.batch, spec.nheads, spec.headdim, spec.N, device="cuda")
+    ws = torch.empty(binding.ssd_workspace_bytes(spec.batch, spec.L, spec.ngroups), dtype=torch.uint8, device="cuda")
+    scratch = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+
+    def run():
+        binding.ssd_fwd(g["x"], g["dt"], g["A"], g["B"], g["C"], D=g["D"], z=g["z"], dt_bias=g["dt_bias"], y=y,
+                        final_state=fs, workspace=ws)
+
+    for _ in range(warmup):
+        run()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for a, b in ev:
+        scratch.zero_()
+        a.record()
+        run()
+        b.record()
+    torch.cuda.synchronize()
+    return statistics.median([a.elapsed_time(b) for a, b in ev])
+
+
 def roofline_obj(alg_bytes: float, ms: float, peaks: dict, traffic, elem_steps: float | None = None):
     """HBM roofline of one launch: algorithmic bytes / launch time against the
     measured copy bandwidth. For a scan, also the fraction of the ALU ceiling:
@@ -541,6 +583,17 @@ def ncu_case(args):
                                      dt_bias=g["dt_bias"], grads=grads)
         torch.cuda.synchronize()
         return 0
+    if args.ncu_case == "ssd":
+        spec = I.MAMBA2_LAYER
+        inp = I.make_ssd_inputs(spec)
+        g = {k: v.cuda() for k, v in inp.items()}
+        ws = torch.empty(binding.ssd_workspace_bytes(spec.batch, spec.L, spec.ngroups), dtype=torch.uint8,
+                         device="cuda")
+        for _ in range(args.warmup + args.steps):
+            binding.ssd_fwd(g["x"], g["dt"], g["A"], g["B"], g["C"], D=g["D"], z=g["z"], dt_bias=g["dt_bias"],
+                            workspace=ws)
+        torch.cuda.synchronize()
+        return 0
     if args.ncu_case == "conv":
         spec, k = HEADLINE, 4
         x = I.normal(spec.seed, 11, (spec.batch, spec.d_inner, spec.L), 1.0, torch.bfloat16).cuda()
@@ -575,7 +628,7 @@ def main(argv=None):
     ap.add_argument("--headline-only", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-soak", action="store_true", help="skip the 1 s untimed soak before timing")
-    ap.add_argument("--ncu-case", choices=["scan", "decode", "conv", "bwd"], default=None,
+    ap.add_argument("--ncu-case", choices=["scan", "decode", "conv", "bwd", "ssd"], default=None,
                     help="profiling case: warmup + steps launches of the headline scan (or of the decode "
                          "update, on the first warmup + steps tokens of the decode workload), nothing else")
     args = ap.parse_args(argv)
@@ -665,6 +718,17 @@ def main(argv=None):
         extras["bwd_" + HEADLINE.name] = {
             "elem_steps_per_s": HEADLINE.elem_steps / (bms * 1e-3), "kernel_ms_median": bms,
             "roofline": bro, "note": "backward pass (all gradients, states recomputed), L2 flushed before each"}
+        sspec = I.MAMBA2_LAYER
+        sms2 = time_ssd(sspec, 10, 3)
+        sby, sfl = ssd_alg(sspec)
+        sro = roofline_obj(sby, sms2, peaks, profiled_traffic("ssd_chunk_" + sspec.name))
+        tens = sfl / (sms2 * 1e-3) / 1e12
+        sro["tensor"] = {"achieved_tflops": round(tens, 1), "peak_tflops": peaks["bf16_tflops"],
+                         "frac": round(tens / peaks["bf16_tflops"], 4), "flops": sfl,
+                         "peak_source": "measured (MEASURED_PEAKS.json bf16_tflops, burst)"}
+        extras["ssd_" + sspec.name] = {
+            "elem_steps_per_s": sspec.elem_steps / (sms2 * 1e-3), "kernel_ms_median": sms2, "roofline": sro,
+            "note": "Mamba-2 scalar-decay scan, C B^T and chunk kernels, mma.sync bf16 tensor cores"}
         cms, cbytes = time_conv(HEADLINE, 10, 3)
         extras["conv1d_silu_k4_" + HEADLINE.name] = {
             "elems_per_s": HEADLINE.batch * HEADLINE.d_inner * HEADLINE.L / (cms * 1e-3), "kernel_ms_median": cms,
