@@ -16,11 +16,12 @@
 // s <= t and 0 above the diagonal, and H (P x N, fp32) is the state carried
 // between chunks. Every product is a bf16 x bf16 -> fp32 tensor-core MMA
 // (mma.sync m16n8k16); the decays, masks and the carried state are fp32, and
-// the state enters C_c H^T as a bf16 high part plus a bf16 residual (two
-// MMAs), straight from the accumulator registers that hold it.
+// the state enters C_c H^T rounded to bf16 straight from the accumulator
+// registers that hold it. C B^T is kept in bf16.
 //
-//   ssd_cb_kernel     CB_c for every (batch, chunk, group) into the workspace.
-//   ssd_chunk_kernel  one CTA per (batch, head), walking its chunks in order.
+//   ssd_cb_kernel     CB_c for every (batch, chunk, group) into the workspace (bf16).
+//   ssd_chunk_kernel  one CTA per (batch, head), walking its chunks in order;
+//                     C and CB of chunk c+1 are fetched while chunk c finishes.
 
 constexpr int kSsdQ = 64;    // steps per chunk
 constexpr int kSsdP = 64;    // channels per head (headdim)
@@ -30,7 +31,7 @@ struct SsdParams {
     const float *A, *D, *dt_bias, *h0;
     __nv_bfloat16 *y;
     float *final_state;
-    float *cb;   // workspace: [batch][nchunks][G][Q][Q] fp32
+    __nv_bfloat16 *cb;   // workspace: [batch][nchunks][G][Q][Q] bf16
     int64_t batch, L, H, G, nchunks;
     int softplus;
 };
@@ -102,7 +103,7 @@ __device__ __forceinline__ void frag_b_kn(const __nv_bfloat16 *base, int ld, int
 // Copy `rows` rows of `row_elems` bf16 (a multiple of 8) from global rows at
 // stride `gstride` elements into shared rows at stride `sld`, zero-filling rows
 // at or past `valid`, with 16-byte cp.async pieces spread over the CTA.
-__device__ __forceinline__ void stage_rows(__nv_bfloat16 *s, int sld, const __nv_bfloat16 *g, int64_t gstride,
+__device__ __forceinline__ void stage_rows(__nv_bfloat16 *s, int sld, const __nv_bfloat16 *g, int gstride,
                                            int rows, int row_elems, int valid, int tid, int nthreads)
 {
     const int ppr = row_elems / 8;
@@ -128,7 +129,7 @@ ssd_cb_kernel(const SsdParams p)
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
     const int64_t t0 = static_cast<int64_t>(c) * Q;
     const int valid = static_cast<int>(p.L - t0 < Q ? p.L - t0 : Q);
-    const int64_t rs = p.G * N;   // B, C row stride
+    const int rs = static_cast<int>(p.G * N);   // B, C row stride
     stage_rows(Cs, LDN, p.C + ((b * p.L + t0) * p.G + g) * N, rs, Q, N, valid, tid, 128);
     stage_rows(Bs, LDN, p.B + ((b * p.L + t0) * p.G + g) * N, rs, Q, N, valid, tid, 128);
     cp_async_commit();
@@ -150,50 +151,49 @@ ssd_cb_kernel(const SsdParams p)
             mma_bf16(acc[j + 1], a[0], a[1], a[2], a[3], bb[2], bb[3]);
         }
     }
-    float *out = p.cb + (((b * p.nchunks + c) * p.G + g) * Q) * Q;
+    __nv_bfloat16 *out = p.cb + (((b * p.nchunks + c) * p.G + g) * Q) * Q;
     const int gr = lane >> 2, t4 = lane & 3;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
         const int col = 8 * j + 2 * t4;
-        *reinterpret_cast<float2 *>(out + (16 * w + gr) * Q + col) = make_float2(acc[j][0], acc[j][1]);
-        *reinterpret_cast<float2 *>(out + (16 * w + gr + 8) * Q + col) = make_float2(acc[j][2], acc[j][3]);
+        *reinterpret_cast<uint32_t *>(out + (16 * w + gr) * Q + col) = pack_bf16x2(acc[j][0], acc[j][1]);
+        *reinterpret_cast<uint32_t *>(out + (16 * w + gr + 8) * Q + col) = pack_bf16x2(acc[j][2], acc[j][3]);
     }
 }
 
 template <int N>
 struct SsdShape {
     static constexpr int Q = kSsdQ, P = kSsdP;
-    static constexpr int LDP = P + 8, LDN = N + 8, LDQ = Q + 8, LDF = Q + 4;
+    static constexpr int LDP = P + 8, LDN = N + 8, LDQ = Q + 8;
     static constexpr int X_OFF = 0;                                  // X_c   [Q][LDP] bf16
-    static constexpr int Z_OFF = X_OFF + Q * LDP * 2;                // z_c   [Q][LDP] bf16
-    static constexpr int B_OFF = Z_OFF + Q * LDP * 2;                // B_c   [Q][LDN] bf16
+    static constexpr int B_OFF = X_OFF + Q * LDP * 2;                // B_c   [Q][LDN] bf16
     static constexpr int C_OFF = B_OFF + Q * LDN * 2;                // C_c   [Q][LDN] bf16
-    static constexpr int CB_OFF = C_OFF + Q * LDN * 2;               // CB_c  [Q][LDF] fp32
-    static constexpr int S_OFF = CB_OFF + Q * LDF * 4;               // S'_c  [Q][LDQ] bf16
+    static constexpr int CB_OFF = C_OFF + Q * LDN * 2;               // CB_c  [Q][LDQ] bf16
+    static constexpr int S_OFF = CB_OFF + Q * LDQ * 2;               // S'_c  [Q][LDQ] bf16
     static constexpr int XW_OFF = S_OFF + Q * LDQ * 2;               // w o X [Q][LDP] bf16
-    static constexpr int CUM_OFF = XW_OFF + Q * LDP * 2;             // cum[Q], delta[Q] fp32
-    static constexpr size_t BYTES = CUM_OFF + 2 * Q * 4;
+    static constexpr int CUM_OFF = XW_OFF + Q * LDP * 2;             // cum, delta, e^cum [Q] fp32
+    static constexpr size_t BYTES = CUM_OFF + 3 * Q * 4;
 };
 
 // ---- one CTA (4 warps) per (batch, head); the chunks of the row in order.
 // Warp w owns channels p = 16w .. 16w+15: those rows of H and those columns of Y_c.
 template <int N>
-__global__ void __launch_bounds__(128, 2)
+__global__ void __launch_bounds__(128, 3)
 ssd_chunk_kernel(const SsdParams p)
 {
     using SH = SsdShape<N>;
-    constexpr int Q = SH::Q, P = SH::P, LDP = SH::LDP, LDN = SH::LDN, LDQ = SH::LDQ, LDF = SH::LDF;
+    constexpr int Q = SH::Q, P = SH::P, LDP = SH::LDP, LDN = SH::LDN, LDQ = SH::LDQ;
     constexpr int NT = N / 8;   // 8-column tiles of the state
     extern __shared__ __align__(16) unsigned char smem_raw[];
     __nv_bfloat16 *Xs = reinterpret_cast<__nv_bfloat16 *>(smem_raw + SH::X_OFF);
-    __nv_bfloat16 *Zs = reinterpret_cast<__nv_bfloat16 *>(smem_raw + SH::Z_OFF);
     __nv_bfloat16 *Bs = reinterpret_cast<__nv_bfloat16 *>(smem_raw + SH::B_OFF);
     __nv_bfloat16 *Cs = reinterpret_cast<__nv_bfloat16 *>(smem_raw + SH::C_OFF);
-    float *CBs = reinterpret_cast<float *>(smem_raw + SH::CB_OFF);
+    __nv_bfloat16 *CBs = reinterpret_cast<__nv_bfloat16 *>(smem_raw + SH::CB_OFF);
     __nv_bfloat16 *Sp = reinterpret_cast<__nv_bfloat16 *>(smem_raw + SH::S_OFF);
     __nv_bfloat16 *Xw = reinterpret_cast<__nv_bfloat16 *>(smem_raw + SH::XW_OFF);
     float *cum = reinterpret_cast<float *>(smem_raw + SH::CUM_OFF);
     float *dl = cum + Q;
+    float *ecum = dl + Q;
 
     const int64_t b = blockIdx.y;
     const int h = blockIdx.x;
@@ -204,7 +204,9 @@ ssd_chunk_kernel(const SsdParams p)
     const float Dh = p.D ? __ldg(p.D + h) : 0.0f;
     const float bias = p.dt_bias ? __ldg(p.dt_bias + h) : 0.0f;
     const bool gate = p.z != nullptr;
-    const int64_t xs = p.H * P;   // x, z, y row stride (one time step)
+    const int xs = static_cast<int>(p.H * P);   // x, z, y row stride (one time step)
+    const int bcs = static_cast<int>(p.G * N);  // B, C row stride
+    const int dts = static_cast<int>(p.H);      // dt row stride
 
     // the carried state H, fp32 fragments: rows p = 16w + gr (+8), columns n = 8j + 2t4 (+1)
     float Hf[NT][4];
@@ -218,28 +220,29 @@ ssd_chunk_kernel(const SsdParams p)
         }
     }
     bool have_state = p.h0 != nullptr;
+
+    // C_c and C_c B_c^T of chunk c (issued early: their buffers free up first)
+    auto stage_c = [&](int64_t c) {
+        const int64_t t0 = c * Q;
+        const int valid = static_cast<int>(p.L - t0 < Q ? p.L - t0 : Q);
+        stage_rows(Cs, LDN, p.C + ((b * p.L + t0) * p.G + g) * N, bcs, Q, N, valid, tid, 128);
+        stage_rows(CBs, LDQ, p.cb + (((b * p.nchunks + c) * p.G + g) * Q) * Q, Q, Q, Q, Q, tid, 128);
+        cp_async_commit();
+    };
+    stage_c(0);
+
     for (int64_t c = 0; c < p.nchunks; ++c) {
         const int64_t t0 = c * Q;
         const int valid = static_cast<int>(p.L - t0 < Q ? p.L - t0 : Q);
-        // ---- stage the chunk
-        stage_rows(Xs, LDP, p.x + ((b * p.L + t0) * p.H + h) * P, xs, Q, P, valid, tid, 128);
-        if (gate)
-            stage_rows(Zs, LDP, p.z + ((b * p.L + t0) * p.H + h) * P, xs, Q, P, valid, tid, 128);
-        stage_rows(Bs, LDN, p.B + ((b * p.L + t0) * p.G + g) * N, p.G * N, Q, N, valid, tid, 128);
-        stage_rows(Cs, LDN, p.C + ((b * p.L + t0) * p.G + g) * N, p.G * N, Q, N, valid, tid, 128);
-        {
-            const float *cbg = p.cb + (((b * p.nchunks + c) * p.G + g) * Q) * Q;
-            for (int i = tid; i < Q * (Q / 4); i += 128) {
-                const int r = i / (Q / 4), q4 = (i % (Q / 4)) * 4;
-                cp_async16(smem_u32(CBs + r * LDF + q4), cbg + r * Q + q4, 16);
-            }
-        }
+        const __nv_bfloat16 *xrow = p.x + ((b * p.L + t0) * p.H + h) * P;
+        // ---- stage X_c, B_c; the step sizes (zero past L)
+        stage_rows(Xs, LDP, xrow, xs, Q, P, valid, tid, 128);
+        stage_rows(Bs, LDN, p.B + ((b * p.L + t0) * p.G + g) * N, bcs, Q, N, valid, tid, 128);
         cp_async_commit();
-        // the step sizes of the chunk (zero past L)
         if (tid < Q) {
             float d = 0.0f;
             if (tid < valid) {
-                const float v = __bfloat162float(p.dt[(b * p.L + t0 + tid) * p.H + h]) + bias;
+                const float v = __bfloat162float(p.dt[(b * p.L + t0) * dts + tid * dts + h]) + bias;
                 d = p.softplus ? softplus_f(v) : v;
             }
             dl[tid] = d;
@@ -249,39 +252,43 @@ ssd_chunk_kernel(const SsdParams p)
         // ---- cum[t] = A_h * (delta_0 + .. + delta_t), one warp
         if (w == 0) {
             const float a0 = Ah * dl[2 * lane], a1 = Ah * dl[2 * lane + 1];
-            float s = a0 + a1;
+            float sum = a0 + a1;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
-                const float u = __shfl_up_sync(0xffffffffu, s, o);
+                const float u = __shfl_up_sync(0xffffffffu, sum, o);
                 if (lane >= o)
-                    s += u;
+                    sum += u;
             }
-            cum[2 * lane] = s - a1;
-            cum[2 * lane + 1] = s;
+            cum[2 * lane] = sum - a1;
+            cum[2 * lane + 1] = sum;
+            ecum[2 * lane] = ex2_approx((sum - a1) * kLog2e);
+            ecum[2 * lane + 1] = ex2_approx(sum * kLog2e);
         }
         __syncthreads();
-        // ---- S' = CB o M o delta (bf16) and w o X (bf16)
+        // ---- S' = CB o M o delta and w o X, both bf16
         const float cq = cum[Q - 1];
         for (int i = tid; i < Q * Q / 2; i += 128) {
-            const int t = i / (Q / 2), s2 = (i % (Q / 2)) * 2;
+            const int t = i >> 5, s2 = (i & 31) * 2;   // Q / 2 = 32 pairs per row
+            const uint32_t cb2 = *reinterpret_cast<const uint32_t *>(CBs + t * LDQ + s2);
+            const float ct = cum[t];
             float v0 = 0.0f, v1 = 0.0f;
             if (s2 <= t)
-                v0 = CBs[t * LDF + s2] * ex2_approx((cum[t] - cum[s2]) * kLog2e) * dl[s2];
+                v0 = bf16lo(cb2) * ex2_approx((ct - cum[s2]) * kLog2e) * dl[s2];
             if (s2 + 1 <= t)
-                v1 = CBs[t * LDF + s2 + 1] * ex2_approx((cum[t] - cum[s2 + 1]) * kLog2e) * dl[s2 + 1];
+                v1 = bf16hi(cb2) * ex2_approx((ct - cum[s2 + 1]) * kLog2e) * dl[s2 + 1];
             *reinterpret_cast<uint32_t *>(Sp + t * LDQ + s2) = pack_bf16x2(v0, v1);
         }
         for (int i = tid; i < Q * P / 2; i += 128) {
-            const int s = i / (P / 2), p2 = (i % (P / 2)) * 2;
-            const float ws = ex2_approx((cq - cum[s]) * kLog2e) * dl[s];
-            const uint32_t xw = *reinterpret_cast<const uint32_t *>(Xs + s * LDP + p2);
-            *reinterpret_cast<uint32_t *>(Xw + s * LDP + p2) = pack_bf16x2(bf16lo(xw) * ws, bf16hi(xw) * ws);
+            const int s_ = i >> 5, p2 = (i & 31) * 2;  // P / 2 = 32 pairs per row
+            const float ws = ex2_approx((cq - cum[s_]) * kLog2e) * dl[s_];
+            const uint32_t xw = *reinterpret_cast<const uint32_t *>(Xs + s_ * LDP + p2);
+            *reinterpret_cast<uint32_t *>(Xw + s_ * LDP + p2) = pack_bf16x2(bf16lo(xw) * ws, bf16hi(xw) * ws);
         }
         __syncthreads();
 
         // ---- Y columns p = 16w .. 16w+15, all Q rows: e^{cum[t]} C_c H^T + S' X_c.
-        // The warp's own state rows are the B operand of C_c H^T, taken from its
-        // fp32 accumulators as a bf16 high part plus a bf16 residual.
+        // The warp's own state rows are the B operand of C_c H^T, converted to
+        // bf16 from the fp32 accumulator registers that hold them.
         float acc[4][2][4];   // [row tile][column tile][fragment]
 #pragma unroll
         for (int mt = 0; mt < 4; ++mt)
@@ -291,32 +298,24 @@ ssd_chunk_kernel(const SsdParams p)
         if (have_state) {
 #pragma unroll
             for (int kk = 0; kk < N / 16; ++kk) {
-                uint32_t bh[2][2], bl[2][2];   // [column tile][b0, b1]
+                uint32_t bh[2][2];   // [column tile][b0, b1]
 #pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
+                for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-                    for (int half = 0; half < 2; ++half) {
-                        const float v0 = Hf[2 * kk + half][2 * nt], v1 = Hf[2 * kk + half][2 * nt + 1];
-                        const uint32_t hi = pack_bf16x2(v0, v1);
-                        bh[nt][half] = hi;
-                        bl[nt][half] = pack_bf16x2(v0 - bf16lo(hi), v1 - bf16hi(hi));
-                    }
-                }
+                    for (int half = 0; half < 2; ++half)
+                        bh[nt][half] = pack_bf16x2(Hf[2 * kk + half][2 * nt], Hf[2 * kk + half][2 * nt + 1]);
 #pragma unroll
                 for (int mt = 0; mt < 4; ++mt) {
                     uint32_t a[4];
                     frag_a(Cs, LDN, 16 * mt, 16 * kk, lane, a);
 #pragma unroll
-                    for (int nt = 0; nt < 2; ++nt) {
+                    for (int nt = 0; nt < 2; ++nt)
                         mma_bf16(acc[mt][nt], a[0], a[1], a[2], a[3], bh[nt][0], bh[nt][1]);
-                        mma_bf16(acc[mt][nt], a[0], a[1], a[2], a[3], bl[nt][0], bl[nt][1]);
-                    }
                 }
             }
 #pragma unroll
             for (int mt = 0; mt < 4; ++mt) {
-                const float e0 = ex2_approx(cum[16 * mt + gr] * kLog2e);
-                const float e1 = ex2_approx(cum[16 * mt + gr + 8] * kLog2e);
+                const float e0 = ecum[16 * mt + gr], e1 = ecum[16 * mt + gr + 8];
 #pragma unroll
                 for (int nt = 0; nt < 2; ++nt) {
                     acc[mt][nt][0] *= e0;
@@ -326,6 +325,9 @@ ssd_chunk_kernel(const SsdParams p)
                 }
             }
         }
+        __syncthreads();   // Cs and CBs are free: fetch the next chunk's while this one finishes
+        if (c + 1 < p.nchunks)
+            stage_c(c + 1);
 #pragma unroll
         for (int kk = 0; kk < Q; kk += 16) {
             uint32_t bb[4];
@@ -345,7 +347,9 @@ ssd_chunk_kernel(const SsdParams p)
             for (int half = 0; half < 2; ++half) {
                 const int t = 16 * mt + gr + half * 8;
                 if (t < valid) {
-                    __nv_bfloat16 *yr = p.y + ((b * p.L + t0 + t) * p.H + h) * P;
+                    const int64_t ro = t * static_cast<int64_t>(xs);
+                    __nv_bfloat16 *yr = p.y + ((b * p.L + t0) * p.H + h) * P + ro;
+                    const __nv_bfloat16 *zr = p.z + ((b * p.L + t0) * p.H + h) * P + ro;
 #pragma unroll
                     for (int nt = 0; nt < 2; ++nt) {
                         const int col = 16 * w + 8 * nt + 2 * t4;
@@ -353,7 +357,7 @@ ssd_chunk_kernel(const SsdParams p)
                         float o0 = fmaf(Dh, bf16lo(xw), acc[mt][nt][2 * half]);
                         float o1 = fmaf(Dh, bf16hi(xw), acc[mt][nt][2 * half + 1]);
                         if (gate) {
-                            const uint32_t zw = *reinterpret_cast<const uint32_t *>(Zs + t * LDP + col);
+                            const uint32_t zw = __ldg(reinterpret_cast<const unsigned int *>(zr + col));
                             o0 *= silu_f(bf16lo(zw));
                             o1 *= silu_f(bf16hi(zw));
                         }
@@ -364,7 +368,7 @@ ssd_chunk_kernel(const SsdParams p)
         }
 
         // ---- H rows p = 16w .. : e^{cum[Q-1]} H + (w o X)^T B_c
-        const float ec = ex2_approx(cq * kLog2e);
+        const float ec = ecum[Q - 1];
 #pragma unroll
         for (int j = 0; j < NT; ++j) {
             Hf[j][0] *= ec;
@@ -385,7 +389,7 @@ ssd_chunk_kernel(const SsdParams p)
             }
         }
         have_state = true;
-        __syncthreads();   // every warp is done with Xs, Sp, Xw, ... of this chunk
+        __syncthreads();   // every warp is done with Xs, Bs, Sp, Xw and the step sizes of this chunk
     }
     if (p.final_state) {
         float *fs = p.final_state + ((b * p.H + h) * P) * N;
@@ -405,7 +409,7 @@ size_t ssd_workspace_bytes(int64_t batch, int64_t L, int64_t G)
     if (batch <= 0 || L <= 0 || G <= 0)
         return 0;
     const int64_t nchunks = (L + kSsdQ - 1) / kSsdQ;
-    return static_cast<size_t>(batch) * nchunks * G * kSsdQ * kSsdQ * 4;
+    return static_cast<size_t>(batch) * nchunks * G * kSsdQ * kSsdQ * 2;
 }
 
 template <int N>
@@ -469,6 +473,8 @@ ss_status ssd_fwd(const void *x, const void *dt, const float *A, const void *B, 
             return fail(SS_ERR_DIM, "x, B, C, y, z and the workspace must be 16-byte aligned");
     if ((ngroups * N * 2) % 16 != 0)
         return fail(SS_ERR_DIM, "B and C rows must be whole 16-byte pieces");
+    if (nheads * headdim > 0x7fffffff || ngroups * N > 0x7fffffff)
+        return fail(SS_ERR_DIM, "nheads * headdim and ngroups * N must fit in 31 bits");
     SsdParams p;
     p.x = static_cast<const __nv_bfloat16 *>(x);
     p.dt = static_cast<const __nv_bfloat16 *>(dt);
@@ -478,7 +484,7 @@ ss_status ssd_fwd(const void *x, const void *dt, const float *A, const void *B, 
     p.A = A; p.D = D; p.dt_bias = dt_bias; p.h0 = h0;
     p.y = static_cast<__nv_bfloat16 *>(y);
     p.final_state = final_state;
-    p.cb = static_cast<float *>(workspace);
+    p.cb = static_cast<__nv_bfloat16 *>(workspace);
     p.batch = batch; p.L = L; p.H = nheads; p.G = ngroups;
     p.nchunks = (L + kSsdQ - 1) / kSsdQ;
     p.softplus = softplus ? 1 : 0;
