@@ -21,7 +21,9 @@
 //
 //   ssd_cb_kernel     CB_c for every (batch, chunk, group) into the workspace (bf16).
 //   ssd_chunk_kernel  one CTA per (batch, head), walking its chunks in order;
-//                     C and CB of chunk c+1 are fetched while chunk c finishes.
+//                     C and CB of chunk c+1 are fetched as soon as chunk c has
+//                     used them, X and B of chunk c+1 while chunk c's outputs
+//                     are written.
 
 constexpr int kSsdQ = 64;    // steps per chunk
 constexpr int kSsdP = 64;    // channels per head (headdim)
@@ -230,23 +232,33 @@ ssd_chunk_kernel(const SsdParams p)
         cp_async_commit();
     };
     stage_c(0);
+    {
+        const int v0 = static_cast<int>(p.L < Q ? p.L : Q);
+        stage_rows(Xs, LDP, p.x + (b * p.L * p.H + h) * P, xs, Q, P, v0, tid, 128);
+        stage_rows(Bs, LDN, p.B + (b * p.L * p.G + g) * N, bcs, Q, N, v0, tid, 128);
+        cp_async_commit();
+    }
+    // raw step of this thread's row of the next chunk, fetched a chunk ahead
+    auto load_dt = [&](int64_t c) -> float {
+        const int64_t t = c * Q + tid;
+        return (tid < Q && t < p.L) ? __bfloat162float(p.dt[(b * p.L + t) * dts + h]) : 0.0f;
+    };
+    float dt_next = load_dt(0);
 
     for (int64_t c = 0; c < p.nchunks; ++c) {
         const int64_t t0 = c * Q;
         const int valid = static_cast<int>(p.L - t0 < Q ? p.L - t0 : Q);
-        const __nv_bfloat16 *xrow = p.x + ((b * p.L + t0) * p.H + h) * P;
-        // ---- stage X_c, B_c; the step sizes (zero past L)
-        stage_rows(Xs, LDP, xrow, xs, Q, P, valid, tid, 128);
-        stage_rows(Bs, LDN, p.B + ((b * p.L + t0) * p.G + g) * N, bcs, Q, N, valid, tid, 128);
-        cp_async_commit();
+        // ---- (X_c and B_c were issued at the end of the previous chunk); the step sizes (zero past L)
         if (tid < Q) {
             float d = 0.0f;
             if (tid < valid) {
-                const float v = __bfloat162float(p.dt[(b * p.L + t0) * dts + tid * dts + h]) + bias;
+                const float v = dt_next + bias;
                 d = p.softplus ? softplus_f(v) : v;
             }
             dl[tid] = d;
         }
+        if (c + 1 < p.nchunks)
+            dt_next = load_dt(c + 1);
         cp_async_wait<0>();
         __syncthreads();
         // ---- cum[t] = A_h * (delta_0 + .. + delta_t), one warp
@@ -328,6 +340,20 @@ ssd_chunk_kernel(const SsdParams p)
         __syncthreads();   // Cs and CBs are free: fetch the next chunk's while this one finishes
         if (c + 1 < p.nchunks)
             stage_c(c + 1);
+        // the gate's z of this warp's outputs, fetched before the products that precede their use
+        uint32_t zv[4][2][2];
+#pragma unroll
+        for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                const int t = 16 * mt + gr + half * 8;
+                const __nv_bfloat16 *zr = p.z + ((b * p.L + t0) * p.H + h) * P + t * static_cast<int64_t>(xs);
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+                    zv[mt][half][nt] = (gate && t < valid)
+                                           ? __ldg(reinterpret_cast<const unsigned int *>(zr + 16 * w + 8 * nt + 2 * t4))
+                                           : 0u;
+            }
 #pragma unroll
         for (int kk = 0; kk < Q; kk += 16) {
             uint32_t bb[4];
@@ -340,32 +366,16 @@ ssd_chunk_kernel(const SsdParams p)
                 mma_bf16(acc[mt][1], a[0], a[1], a[2], a[3], bb[2], bb[3]);
             }
         }
-        // ---- epilogue: + D x, gate, store
+        // x of this warp's outputs (for D x), so that the shared tiles can be refilled
+        uint32_t xv[4][2][2];
 #pragma unroll
-        for (int mt = 0; mt < 4; ++mt) {
+        for (int mt = 0; mt < 4; ++mt)
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                const int t = 16 * mt + gr + half * 8;
-                if (t < valid) {
-                    const int64_t ro = t * static_cast<int64_t>(xs);
-                    __nv_bfloat16 *yr = p.y + ((b * p.L + t0) * p.H + h) * P + ro;
-                    const __nv_bfloat16 *zr = p.z + ((b * p.L + t0) * p.H + h) * P + ro;
+            for (int half = 0; half < 2; ++half)
 #pragma unroll
-                    for (int nt = 0; nt < 2; ++nt) {
-                        const int col = 16 * w + 8 * nt + 2 * t4;
-                        const uint32_t xw = *reinterpret_cast<const uint32_t *>(Xs + t * LDP + col);
-                        float o0 = fmaf(Dh, bf16lo(xw), acc[mt][nt][2 * half]);
-                        float o1 = fmaf(Dh, bf16hi(xw), acc[mt][nt][2 * half + 1]);
-                        if (gate) {
-                            const uint32_t zw = __ldg(reinterpret_cast<const unsigned int *>(zr + col));
-                            o0 *= silu_f(bf16lo(zw));
-                            o1 *= silu_f(bf16hi(zw));
-                        }
-                        *reinterpret_cast<uint32_t *>(yr + col) = pack_bf16x2(o0, o1);
-                    }
-                }
-            }
-        }
+                for (int nt = 0; nt < 2; ++nt)
+                    xv[mt][half][nt] = *reinterpret_cast<const uint32_t *>(
+                        Xs + (16 * mt + gr + half * 8) * LDP + 16 * w + 8 * nt + 2 * t4);
 
         // ---- H rows p = 16w .. : e^{cum[Q-1]} H + (w o X)^T B_c
         const float ec = ecum[Q - 1];
@@ -390,6 +400,40 @@ ssd_chunk_kernel(const SsdParams p)
         }
         have_state = true;
         __syncthreads();   // every warp is done with Xs, Bs, Sp, Xw and the step sizes of this chunk
+        // the next chunk's X and B land while this one's outputs are written
+        if (c + 1 < p.nchunks) {
+            const int64_t t1 = (c + 1) * Q;
+            const int v1 = static_cast<int>(p.L - t1 < Q ? p.L - t1 : Q);
+            stage_rows(Xs, LDP, p.x + ((b * p.L + t1) * p.H + h) * P, xs, Q, P, v1, tid, 128);
+            stage_rows(Bs, LDN, p.B + ((b * p.L + t1) * p.G + g) * N, bcs, Q, N, v1, tid, 128);
+            cp_async_commit();
+        }
+        // ---- epilogue: + D x, gate, store
+#pragma unroll
+        for (int mt = 0; mt < 4; ++mt) {
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                const int t = 16 * mt + gr + half * 8;
+                if (t < valid) {
+                    const int64_t ro = t * static_cast<int64_t>(xs);
+                    __nv_bfloat16 *yr = p.y + ((b * p.L + t0) * p.H + h) * P + ro;
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt) {
+                        const int col = 16 * w + 8 * nt + 2 * t4;
+                        const uint32_t xw = xv[mt][half][nt];
+                        float o0 = fmaf(Dh, bf16lo(xw), acc[mt][nt][2 * half]);
+                        float o1 = fmaf(Dh, bf16hi(xw), acc[mt][nt][2 * half + 1]);
+                        if (gate) {
+                            const uint32_t zw = zv[mt][half][nt];
+                            o0 *= silu_f(bf16lo(zw));
+                            o1 *= silu_f(bf16hi(zw));
+                        }
+                        *reinterpret_cast<uint32_t *>(yr + col) = pack_bf16x2(o0, o1);
+                    }
+                }
+            }
+        }
+
     }
     if (p.final_state) {
         float *fs = p.final_state + ((b * p.H + h) * P) * N;
