@@ -430,9 +430,12 @@ def time_conv_step(spec: I.DecodeSpec, steps: int, k: int = 4):
     return ms, bd * 2 * 2 + 2 * bd * (k - 1) * 2 + spec.d_inner * (k + 1) * 4
 
 
-def time_bwd(spec: I.ScanSpec, steps: int, warmup: int):
+def time_bwd(spec: I.ScanSpec, steps: int, warmup: int, from_forward: bool = False):
     """Median device time (ms) of the backward pass over ``steps`` launches,
-    each preceded by an L2 flush; outputs and workspace preallocated."""
+    each preceded by an L2 flush; outputs and workspace preallocated. With
+    ``from_forward`` the workspace is filled once by the training forward and
+    every timed backward skips its own forward walk; the training forward's
+    median time is then returned too."""
     from selective_state_space_138_b300 import binding
     inp = I.make_scan_inputs(spec)
     g = {k: inp[k].cuda() for k in ("x", "dt", "z", "B", "C", "A", "D", "dt_bias")}
@@ -444,8 +447,23 @@ def time_bwd(spec: I.ScanSpec, steps: int, warmup: int):
 
     def run():
         return binding.scan_bwd(g["x"], g["dt"], g["A"], g["B"], g["C"], dout, D=g["D"], z=g["z"],
-                                dt_bias=g["dt_bias"], grads=grads, workspace=ws)
+                                dt_bias=g["dt_bias"], grads=grads, workspace=ws, states_from_forward=from_forward)
 
+    fwd_ms = None
+    if from_forward:
+        y = torch.empty_like(g["x"])
+        fwd = lambda: binding.scan_fwd_train(g["x"], g["dt"], g["A"], g["B"], g["C"], D=g["D"], z=g["z"],
+                                             dt_bias=g["dt_bias"], y=y, workspace=ws)
+        for _ in range(warmup):
+            fwd()
+        fe = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for a, b in fe:
+            scratch.zero_()
+            a.record()
+            fwd()
+            b.record()
+        torch.cuda.synchronize()
+        fwd_ms = statistics.median([a.elapsed_time(b) for a, b in fe])
     grads = run()
     for _ in range(warmup):
         run()
@@ -456,7 +474,8 @@ def time_bwd(spec: I.ScanSpec, steps: int, warmup: int):
         run()
         b.record()
     torch.cuda.synchronize()
-    return statistics.median([a.elapsed_time(b) for a, b in ev])
+    ms = statistics.median([a.elapsed_time(b) for a, b in ev])
+    return (ms, fwd_ms) if from_forward else ms
 
 
 def ssd_alg(spec: I.SsdSpec):
@@ -742,6 +761,12 @@ def main(argv=None):
         extras["bwd_" + HEADLINE.name] = {
             "elem_steps_per_s": HEADLINE.elem_steps / (bms * 1e-3), "kernel_ms_median": bms,
             "roofline": bro, "note": "backward pass (all gradients, states recomputed), L2 flushed before each"}
+        tbms, tfms = time_bwd(HEADLINE, 10, 3, from_forward=True)
+        extras["train_step_" + HEADLINE.name] = {
+            "fwd_train_ms_median": tfms, "bwd_from_forward_ms_median": tbms,
+            "elem_steps_per_s": HEADLINE.elem_steps / ((tfms + tbms) * 1e-3),
+            "note": "training forward (also stores the state at every 16th step) + backward that starts from "
+                    "those states; L2 flushed before each launch"}
         sspec = I.MAMBA2_LAYER
         sms2 = time_ssd(sspec, 10, 3)
         sby, sfl = ssd_alg(sspec)

@@ -250,6 +250,9 @@ ss_status ss_conv_state_update_f32(float *conv_state, const float *x, const floa
  *                 bytes, 16-byte aligned, owned by the caller; it holds the
  *                 state at every 16th step between the forward and reverse
  *                 walks and may be reused after the call's work completes.
+ *   states_from_forward : non-zero when ss_scan_fwd_train_* has already
+ *                 filled the workspace from these inputs (the backward's own
+ *                 forward walk is then skipped).
  *   1 <= N <= 32.
  * dA, dB, dC, dD and ddt_bias are cleared on `stream` and accumulated with
  * fp32 atomic adds, so their last bits may differ between runs.
@@ -263,16 +266,38 @@ ss_status ss_scan_bwd_bf16(const ss_bf16 *x, const ss_bf16 *delta, const float *
                            int delta_softplus, const float *h0, const ss_bf16 *dout,
                            const float *dfinal_state, ss_bf16 *dx, ss_bf16 *ddelta, float *dA, float *dB,
                            float *dC, float *dD, ss_bf16 *dz, float *ddt_bias, float *dh0,
-                           void *workspace, size_t workspace_bytes, int64_t batch, int64_t d_inner,
-                           int64_t L, int64_t N, cudaStream_t stream);
+                           void *workspace, size_t workspace_bytes, int states_from_forward,
+                           int64_t batch, int64_t d_inner, int64_t L, int64_t N, cudaStream_t stream);
 
 ss_status ss_scan_bwd_f32(const float *x, const float *delta, const float *A, const float *B,
                           const float *C, const float *D, const float *z, const float *dt_bias,
                           int delta_softplus, const float *h0, const float *dout,
                           const float *dfinal_state, float *dx, float *ddelta, float *dA, float *dB,
                           float *dC, float *dD, float *dz, float *ddt_bias, float *dh0, void *workspace,
-                          size_t workspace_bytes, int64_t batch, int64_t d_inner, int64_t L, int64_t N,
-                          cudaStream_t stream);
+                          size_t workspace_bytes, int states_from_forward, int64_t batch,
+                          int64_t d_inner, int64_t L, int64_t N, cudaStream_t stream);
+
+/*
+ * ss_scan_fwd_train_bf16 / ss_scan_fwd_train_f32 -- ss_scan_fwd_* for training:
+ * the same outputs (with an optional initial state h0, as ss_scan_fwd_ex_*),
+ * and in `workspace` (at least ss_scan_bwd_workspace_bytes(...) bytes, 16-byte
+ * aligned, caller-owned) the state at every 16th step, which the backward pass
+ * would otherwise recompute with a forward walk of its own. Pass the same
+ * workspace, untouched, and the same inputs to ss_scan_bwd_* with
+ * states_from_forward = 1. 1 <= N <= 32.
+ */
+ss_status ss_scan_fwd_train_bf16(const ss_bf16 *x, const ss_bf16 *delta, const float *A,
+                                 const ss_bf16 *B, const ss_bf16 *C, const float *D,
+                                 const ss_bf16 *z, const float *dt_bias, int delta_softplus,
+                                 const float *h0, ss_bf16 *y, float *final_state, void *workspace,
+                                 size_t workspace_bytes, int64_t batch, int64_t d_inner, int64_t L,
+                                 int64_t N, cudaStream_t stream);
+
+ss_status ss_scan_fwd_train_f32(const float *x, const float *delta, const float *A, const float *B,
+                                const float *C, const float *D, const float *z, const float *dt_bias,
+                                int delta_softplus, const float *h0, float *y, float *final_state,
+                                void *workspace, size_t workspace_bytes, int64_t batch,
+                                int64_t d_inner, int64_t L, int64_t N, cudaStream_t stream);
 
 /*
  * ss_scan_bwd_noalloc_bf16 / ss_scan_bwd_noalloc_f32 -- ss_scan_bwd_* without

@@ -21,6 +21,7 @@ EXPORTS = ("ss_scan_fwd_bf16", "ss_scan_fwd_f32", "ss_scan_fwd_ex_bf16", "ss_sca
            "ss_causal_conv1d_bf16", "ss_causal_conv1d_f32", "ss_conv_state_update_bf16",
            "ss_conv_state_update_f32", "ss_scan_bwd_bf16", "ss_scan_bwd_f32", "ss_scan_bwd_workspace_bytes",
            "ss_scan_bwd_noalloc_bf16", "ss_scan_bwd_noalloc_f32", "ss_ssd_fwd_bf16", "ss_ssd_workspace_bytes",
+           "ss_scan_fwd_train_bf16", "ss_scan_fwd_train_f32",
            "ss_last_error", "ss_abi_version")
 
 STATUS = {0: "SS_OK", -1: "SS_ERR_NULL", -2: "SS_ERR_DIM", -3: "SS_ERR_N", -4: "SS_ERR_DEVICE_PTR",
@@ -66,7 +67,10 @@ def lib() -> ctypes.CDLL:
         getattr(L, name).argtypes = [vp, vp, vp, vp, ci, vp, i64, i64, i64, vp]
         getattr(L, name).restype = ci
     for name in ("ss_scan_bwd_bf16", "ss_scan_bwd_f32"):
-        getattr(L, name).argtypes = [vp] * 8 + [ci] + [vp] * 13 + [ctypes.c_size_t] + [i64] * 4 + [vp]
+        getattr(L, name).argtypes = [vp] * 8 + [ci] + [vp] * 13 + [ctypes.c_size_t, ci] + [i64] * 4 + [vp]
+        getattr(L, name).restype = ci
+    for name in ("ss_scan_fwd_train_bf16", "ss_scan_fwd_train_f32"):
+        getattr(L, name).argtypes = [vp] * 8 + [ci, vp, vp, vp, vp, ctypes.c_size_t] + [i64] * 4 + [vp]
         getattr(L, name).restype = ci
     for name in ("ss_scan_bwd_noalloc_bf16", "ss_scan_bwd_noalloc_f32"):
         getattr(L, name).argtypes = [vp] * 8 + [ci] + [vp] * 12 + [i64] * 4 + [vp]
@@ -265,8 +269,39 @@ def scan_bwd_workspace_bytes(batch, d_inner, L, N) -> int:
     return int(lib().ss_scan_bwd_workspace_bytes(batch, d_inner, L, N))
 
 
+def scan_fwd_train(x, delta, A, B, C, D=None, z=None, dt_bias=None, delta_softplus=True, h0=None, y=None,
+                   final_state=None, workspace=None, stream=None):
+    """``scan_fwd`` that also stores the backward pass's states in
+    ``workspace`` (allocated when None); see ``ss_scan_fwd_train_*``. Returns
+    (y, final_state, workspace); hand the workspace to ``scan_bwd`` with
+    states_from_forward=True."""
+    io = x.dtype
+    sfx = _io_suffix(io)
+    batch, d_inner, L = x.shape
+    N = A.shape[1] if A.dim() == 2 else -1
+    for t, n, dt_, shp in ((delta, "delta", io, x.shape), (z, "z", io, x.shape), (B, "B", io, (batch, N, L)),
+                           (C, "C", io, (batch, N, L)), (A, "A", torch.float32, (d_inner, N)),
+                           (D, "D", torch.float32, (d_inner,)), (dt_bias, "dt_bias", torch.float32, (d_inner,)),
+                           (h0, "h0", torch.float32, (batch, d_inner, N))):
+        _need(t, n, dt_, shp)
+    if y is None:
+        y = torch.empty_like(x)
+    _need(y, "y", io, x.shape)
+    if final_state is None:
+        final_state = torch.empty((batch, d_inner, N), dtype=torch.float32, device=x.device)
+    _need(final_state, "final_state", torch.float32, (batch, d_inner, N))
+    if workspace is None:
+        workspace = torch.empty(max(scan_bwd_workspace_bytes(batch, d_inner, L, N), 16), dtype=torch.uint8,
+                                device=x.device)
+    fn = getattr(lib(), "ss_scan_fwd_train_" + sfx)
+    _check(fn(_ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(dt_bias),
+              int(bool(delta_softplus)), _ptr(h0), _ptr(y), _ptr(final_state), _ptr(workspace),
+              workspace.numel() * workspace.element_size(), batch, d_inner, L, N, _stream(stream)))
+    return y, final_state, workspace
+
+
 def scan_bwd(x, delta, A, B, C, dout, D=None, z=None, dt_bias=None, delta_softplus=True, h0=None,
-             dfinal_state=None, grads=None, workspace=None, stream=None, noalloc=False):
+             dfinal_state=None, grads=None, workspace=None, stream=None, noalloc=False, states_from_forward=False):
     """Gradient of ``scan_fwd`` (see ``ss_scan_bwd_*``): the forward inputs,
     dout (batch, d_inner, L) in the io dtype and optionally dfinal_state
     (batch, d_inner, N) fp32. ``grads`` may hold preallocated outputs under the
@@ -316,13 +351,16 @@ def scan_bwd(x, delta, A, B, C, dout, D=None, z=None, dt_bias=None, delta_softpl
         return {k: g.get(k) for k in ("dx", "ddelta", "dz", "dA", "dB", "dC", "dD", "ddt_bias", "dh0")}
     need = scan_bwd_workspace_bytes(batch, d_inner, L, N)
     if workspace is None:
+        if states_from_forward:
+            raise ValueError("states_from_forward needs the workspace that scan_fwd_train filled")
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
     fn = getattr(lib(), "ss_scan_bwd_" + sfx)
     _check(fn(_ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(dt_bias),
               int(bool(delta_softplus)), _ptr(h0), _ptr(dout), _ptr(dfinal_state), _ptr(g["dx"]),
               _ptr(g["ddelta"]), _ptr(g["dA"]), _ptr(g["dB"]), _ptr(g["dC"]), _ptr(g.get("dD")),
               _ptr(g.get("dz")), _ptr(g.get("ddt_bias")), _ptr(g.get("dh0")), _ptr(workspace),
-              workspace.numel() * workspace.element_size(), batch, d_inner, L, N, _stream(stream)))
+              workspace.numel() * workspace.element_size(), int(bool(states_from_forward)), batch, d_inner, L, N,
+              _stream(stream)))
     return {k: g.get(k) for k in ("dx", "ddelta", "dz", "dA", "dB", "dC", "dD", "ddt_bias", "dh0")}
 
 

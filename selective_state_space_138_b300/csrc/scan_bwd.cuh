@@ -46,6 +46,7 @@ struct BwdParams {
     int softplus;
     int vec;    // io rows 16-byte aligned with L a multiple of the piece
     int vec4;   // dB, dC rows take 16-byte atomic adds (L % 4 == 0, aligned)
+    int states_ready;   // the workspace already holds the stored states (written by the forward pass)
 };
 
 #define SS_BWD_STAGES 2
@@ -268,7 +269,8 @@ scan_bwd_kernel(const BwdParams p)
     float4 *ck = p.ckpt + (b * p.nsub * S + q) * Dn + ds;   // + s * S * Dn for sub-chunk s
     const int64_t ckstride = static_cast<int64_t>(S) * Dn;
 
-    // ---- phase 1: forward, storing the state at every sub-chunk start
+    // ---- phase 1: forward, storing the state at every sub-chunk start (skipped
+    // when the forward pass has stored them)
     u64 h01 = 0, h23 = 0;
     if (p.h0 && act_s) {
         const float *hp = p.h0 + (b * Dn + ds) * N;
@@ -279,7 +281,7 @@ scan_bwd_kernel(const BwdParams p)
         h01 = pk(hv[0], hv[1]);
         h23 = pk(hv[2], hv[3]);
     }
-    {
+    if (!p.states_ready) {
 #pragma unroll
         for (int s = 0; s < STAGES - 1; ++s)
             if (s < nchunks)
@@ -656,7 +658,7 @@ ss_status scan_bwd(const void *x, const void *dt, const float *A, const void *B,
                    const void *z, const float *dt_bias, int softplus, const float *h0, const void *dout,
                    const float *dfinal, void *dx, void *ddt, float *dA, float *dB, float *dC, float *dD, void *dz,
                    float *ddt_bias, float *dh0, void *workspace, size_t workspace_bytes, int64_t batch,
-                   int64_t d_inner, int64_t L, int64_t N, cudaStream_t stream)
+                   int64_t d_inner, int64_t L, int64_t N, cudaStream_t stream, int states_ready = 0)
 {
     g_err[0] = '\0';
     if (batch <= 0 || d_inner <= 0 || L <= 0)
@@ -709,6 +711,7 @@ ss_status scan_bwd(const void *x, const void *dt, const float *A, const void *B,
     p.batch = batch; p.d_inner = d_inner; p.L = L; p.N = N;
     p.nsub = (L + kBwdHC - 1) / kBwdHC;
     p.softplus = softplus ? 1 : 0;
+    p.states_ready = states_ready ? 1 : 0;
     p.vec = (L % 16 == 0) && aligned16(x) && aligned16(dt) && aligned16(dout) && aligned16(dx) &&
             aligned16(ddt) && (!z || aligned16(z)) && (!p.dz || aligned16(p.dz));
     p.vec4 = (L % 4 == 0) && aligned16(dB) && aligned16(dC);

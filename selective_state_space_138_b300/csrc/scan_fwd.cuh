@@ -38,6 +38,8 @@ struct ScanParams {
     int64_t seg_len;  // steps per segment, a multiple of the chunk length
     const float *h0;        // (batch, d_inner, N) initial state, or NULL for zero
     const uint8_t *reset;   // (batch, L) sequence starts, or NULL (n-split kernel only)
+    float4 *ckpt;           // the backward's stored states (its workspace layout), or NULL
+    int64_t nsub;           // 16-step sub-chunks of the sequence (when ckpt is set)
 };
 
 // Shared-memory index of (t, n) within a chunk: K-step blocks of NT floats per
@@ -537,6 +539,18 @@ scan_nsplit_kernel(const ScanParams p)
                         h01 = 0;
                         h23 = 0;
                     }
+                    if constexpr (RO && !REV && !RST) {
+                        // the state entering each 16-step sub-chunk, for the backward pass
+                        if ((u == 15 || u == 31) && p.ckpt && act_s) {
+                            const int64_t sc = (t0 + u + 1) / 16;
+                            if (sc < p.nsub) {
+                                float hv[4];
+                                upk(h01, hv[0], hv[1]);
+                                upk(h23, hv[2], hv[3]);
+                                p.ckpt[((b * p.nsub + sc) * S + q) * Dn + ds] = make_float4(hv[0], hv[1], hv[2], hv[3]);
+                            }
+                        }
+                    }
                 }
                 if constexpr (RO) {
 #pragma unroll
@@ -643,6 +657,12 @@ scan_nsplit_kernel(const ScanParams p)
     } else {
         h01 = g01;
         h23 = g23;
+    }
+    if (!REV && !RST && p.ckpt && act_s && seg == 0) {   // the state entering sub-chunk 0
+        float hv[4];
+        upk(h01, hv[0], hv[1]);
+        upk(h23, hv[2], hv[3]);
+        p.ckpt[((b * p.nsub) * S + q) * Dn + ds] = make_float4(hv[0], hv[1], hv[2], hv[3]);
     }
     run(Flag<true>{});
 
@@ -828,11 +848,14 @@ bool use_nsplit(int64_t N)
     return true;
 }
 
+size_t bwd_workspace_bytes(int64_t batch, int64_t d_inner, int64_t L, int64_t N);
+
 template <typename T>
 ss_status scan_fwd(const void *x, const void *dt, const float *A, const void *B, const void *C,
                    const float *D, const void *z, const float *dt_bias, int softplus, const float *h0,
                    const uint8_t *reset, int reverse, void *y, float *final_state, int64_t batch,
-                   int64_t d_inner, int64_t L, int64_t N, cudaStream_t stream)
+                   int64_t d_inner, int64_t L, int64_t N, cudaStream_t stream, void *ckpt = nullptr,
+                   size_t ckpt_bytes = 0)
 {
     g_err[0] = '\0';
     if (batch <= 0 || d_inner <= 0 || L <= 0)
@@ -846,11 +869,22 @@ ss_status scan_fwd(const void *x, const void *dt, const float *A, const void *B,
                              {B, "B", true},          {C, "C", true},       {y, "y", true},
                              {D, "D", false},         {z, "z", false},      {dt_bias, "dt_bias", false},
                              {final_state, "final_state", false}, {h0, "h0", false},
-                             {reset, "reset", false}};
-    const bool extended = h0 || reset || reverse;
+                             {reset, "reset", false}, {ckpt, "workspace", false}};
+    const bool extended = h0 || reset || reverse || ckpt;
     if (extended && N > 32)
-        return fail(SS_ERR_N, "N=%lld: an initial state, sequence starts or the reverse direction need N <= 32",
-                    (long long)N);
+        return fail(SS_ERR_N, "N=%lld: an initial state, sequence starts, the reverse direction or stored states "
+                    "need N <= 32", (long long)N);
+    if (ckpt) {
+        if (reset || reverse)
+            return fail(SS_ERR_DIM, "stored states for the backward pass are kept for the forward direction "
+                        "without sequence starts only");
+        const size_t need = bwd_workspace_bytes(batch, d_inner, L, N);
+        if (ckpt_bytes < need)
+            return fail(SS_ERR_DIM, "workspace of %zu bytes is smaller than the %zu bytes required", ckpt_bytes,
+                        need);
+        if (!aligned16(ckpt))
+            return fail(SS_ERR_DIM, "workspace must be 16-byte aligned");
+    }
     int dev = 0;
     ss_status st = check_ptrs(list, static_cast<int>(sizeof(list) / sizeof(list[0])), &dev);
     if (st != SS_OK)
@@ -859,6 +893,8 @@ ss_status scan_fwd(const void *x, const void *dt, const float *A, const void *B,
     ScanParams p;
     p.h0 = h0;
     p.reset = reset;
+    p.ckpt = static_cast<float4 *>(ckpt);
+    p.nsub = (L + 15) / 16;
     p.x = x; p.dt = dt; p.B = B; p.C = C; p.z = z;
     p.A = A; p.D = D; p.dt_bias = dt_bias;
     p.y = y; p.final_state = final_state;

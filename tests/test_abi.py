@@ -118,7 +118,7 @@ def test_bwd_host_validation(lib, sfx):
 
     def call(x=one, ws=one, ws_bytes=1 << 40, batch=2, d=4, L=16, N=16, dout=one):
         return fn(x, one, one, one, one, None, None, None, 1, None, dout, None, one, one, one, one, one,
-                  None, None, None, None, ws, ws_bytes, batch, d, L, N, None)
+                  None, None, None, None, ws, ws_bytes, 0, batch, d, L, N, None)
 
     assert call(batch=0) == -2
     assert call(N=33) == -3
@@ -155,3 +155,16 @@ def test_bwd_noalloc_host_validation(lib, sfx):
     assert call(batch=8, d=1536, L=2048, N=16) == -2
     assert "built-in scratch" in binding.last_error()
     assert binding.scan_bwd_workspace_bytes(8, 1536, 2048, 16) > binding.BWD_NOALLOC_MAX_BYTES
+
+
+@pytest.mark.parametrize("sfx", ["bf16", "f32"])
+def test_fwd_train_host_validation(lib, sfx):
+    one = ctypes.c_void_p(1)
+    fn = getattr(lib, "ss_scan_fwd_train_" + sfx)
+
+    def call(ws=one, ws_bytes=1 << 40, N=16):
+        return fn(one, one, one, one, one, None, None, None, 1, None, one, None, ws, ws_bytes, 2, 4, 16, N, None)
+
+    assert call(ws=None) == -1
+    assert "workspace" in binding.last_error()
+    assert call(N=40) == -3

@@ -130,3 +130,31 @@ def test_bwd_repeat_is_stable():
         assert torch.equal(outs[0][k], outs[1][k]), k
     for k in ("dA", "dB", "dC", "dD", "ddt_bias"):
         torch.testing.assert_close(outs[0][k], outs[1][k], rtol=1e-5, atol=1e-5)
+
+
+@pytest.mark.parametrize("shape", [(2, 64, 300, 16), (1, 64, 8192, 16), (2, 33, 47, 8)],
+                         ids=lambda s: "b%d_d%d_l%d_n%d" % s)
+def test_bwd_with_states_stored_by_the_training_forward(shape):
+    """The training forward stores the state at every 16th step (also when it
+    splits a long row into cluster segments); the backward then skips its own
+    forward walk and gives the oracle's gradients."""
+    b, d, L, N = shape
+    spec = I.ScanSpec(b, d, L, N, io="bf16", seed=77 + L)
+    inp = I.make_scan_inputs(spec)
+    bw = I.make_bwd_inputs(spec)
+    g = {k: inp[k].cuda() for k in ("x", "dt", "z", "B", "C", "A", "D", "dt_bias")}
+    y0, f0 = binding.scan_fwd(g["x"], g["dt"], g["A"], g["B"], g["C"], D=g["D"], z=g["z"], dt_bias=g["dt_bias"])
+    y1, f1, ws = binding.scan_fwd_train(g["x"], g["dt"], g["A"], g["B"], g["C"], D=g["D"], z=g["z"],
+                                        dt_bias=g["dt_bias"])
+    got = binding.scan_bwd(g["x"], g["dt"], g["A"], g["B"], g["C"], bw["dout"].cuda(), D=g["D"], z=g["z"],
+                           dt_bias=g["dt_bias"], dfinal_state=bw["dfinal"].cuda(), workspace=ws,
+                           states_from_forward=True)
+    torch.cuda.synchronize()
+    assert torch.equal(y0, y1) and torch.equal(f0, f1)   # the stores do not change the forward's results
+    ref = O.scan_bwd(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], bw["dout"], D=inp["D"], z=inp["z"],
+                     dt_bias=inp["dt_bias"], dfinal=bw["dfinal"])
+    for k, r in ref.items():
+        if r is None or k == "dh0":
+            continue
+        kg = "ddelta" if k == "ddt" else k
+        assert_grad_close(got[kg].float().cpu().numpy(), r, torch.bfloat16, kg)
