@@ -79,6 +79,123 @@ state_update_row_kernel(const UpdateParams p)
     Io<T>::store1(static_cast<T *>(p.y) + row, out);
 }
 
+// N = 16 with 16-byte rows (the decode workload): grid = (channel blocks,
+// groups of kDecRows batch rows); a thread owns channel d of kDecRows batch
+// rows. The fp32 states of all its rows, and B, C of the batch rows, are
+// requested at once with cp.async into shared memory (no registers held while
+// they are in flight, so ~200 KB per SM is outstanding), the per-row scalars
+// are loaded together, A of the channel once for all rows; each row is then
+// updated from its staged state and written straight back. State pieces are
+// XOR-swizzled so that the row reads are free of bank conflicts.
+constexpr int kDecRows = 4;
+
+template <typename T>
+__global__ void __launch_bounds__(kBlock)
+state_update_rows16_kernel(const UpdateParams p)
+{
+    constexpr int NV = 4, R = kDecRows;
+    constexpr int BCP = 2 * 16 * (int)sizeof(T) / 16;   // 16-byte pieces of one batch row's B and C
+    __shared__ __align__(16) float4 sst[R * kBlock * NV];
+    __shared__ __align__(16) T sbc[R * 2 * 16];        // [row][B, C][16]
+    const int r = threadIdx.x;
+    const int64_t d = static_cast<int64_t>(blockIdx.x) * kBlock + r;
+    const bool act = d < p.d_inner;
+    const int64_t dd = act ? d : 0;
+    const int sw = (r >> 1) & 3;
+    float4 a[NV];
+#pragma unroll
+    for (int v = 0; v < NV; ++v)
+        a[v] = __ldg(reinterpret_cast<const float4 *>(p.A + dd * 16) + v);
+    const float Dd = p.D ? __ldg(p.D + dd) : 0.0f;
+    for (int64_t b0 = static_cast<int64_t>(blockIdx.y) * R; b0 < p.batch;
+         b0 += static_cast<int64_t>(gridDim.y) * R) {
+        // the states of this thread's R rows, and B, C of the R batch rows, into shared memory
+#pragma unroll
+        for (int k = 0; k < R; ++k) {
+            const int64_t b = b0 + k;
+            const bool ok = act && b < p.batch;
+            const float4 *st = reinterpret_cast<const float4 *>(p.state + ((ok ? b : 0) * p.d_inner + dd) * 16);
+#pragma unroll
+            for (int v = 0; v < NV; ++v)
+                cp_async16(static_cast<uint32_t>(__cvta_generic_to_shared(&sst[(k * kBlock + r) * NV + (v ^ sw)])),
+                           st + v, ok ? 16 : 0);
+        }
+        if (r < R * BCP) {
+            const int k = r / BCP, piece = r % BCP;   // pieces of B first, then C
+            const int half = piece / (BCP / 2), pp = piece % (BCP / 2);
+            const int64_t b = b0 + k;
+            const bool ok = b < p.batch;
+            const T *src = static_cast<const T *>(half ? p.C : p.B) + (ok ? b : 0) * 16 + pp * (16 / (int)sizeof(T));
+            cp_async16(static_cast<uint32_t>(__cvta_generic_to_shared(sbc + (k * 2 + half) * 16 +
+                                                                       pp * (16 / (int)sizeof(T)))),
+                       src, ok ? 16 : 0);
+        }
+        cp_async_commit();
+        float xv[R], dlv[R], zv[R];
+#pragma unroll
+        for (int k = 0; k < R; ++k) {
+            const int64_t b = b0 + k;
+            const bool ok = act && b < p.batch;
+            const int64_t row = (ok ? b : 0) * p.d_inner + dd;
+            xv[k] = ok ? Io<T>::load1(static_cast<const T *>(p.x) + row) : 0.0f;
+            dlv[k] = ok ? Io<T>::load1(static_cast<const T *>(p.delta) + row) : 0.0f;
+            zv[k] = (ok && p.z) ? Io<T>::load1(static_cast<const T *>(p.z) + row) : 0.0f;
+        }
+        cp_async_wait<0>();
+        __syncthreads();   // B and C were staged by a few threads for all
+#pragma unroll
+        for (int k = 0; k < R; ++k) {
+            const int64_t b = b0 + k;
+            if (!act || b >= p.batch)
+                continue;
+            const int64_t row = b * p.d_inner + d;
+            float bv[16], cv[16];
+            const uint4 *sb = reinterpret_cast<const uint4 *>(sbc + (k * 2) * 16);   // B then C of row k
+#pragma unroll
+            for (int e = 0; e < 16 / Io<T>::kPerVec; ++e) {   // plain shared loads, one address for all threads
+                unpack_piece<T>(sb[e], bv + e * Io<T>::kPerVec);
+                unpack_piece<T>(sb[16 / Io<T>::kPerVec + e], cv + e * Io<T>::kPerVec);
+            }
+            const float dx = dlv[k] * xv[k], dl2 = dlv[k] * kLog2e;
+            float out = 0.0f;
+            float4 *so = reinterpret_cast<float4 *>(p.state + row * 16);
+#pragma unroll
+            for (int v = 0; v < NV; ++v) {
+                float4 h = sst[(k * kBlock + r) * NV + (v ^ sw)];
+                float *hv = reinterpret_cast<float *>(&h);
+                const float *av = reinterpret_cast<const float *>(&a[v]);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int n = 4 * v + e;
+                    hv[e] = fmaf(ex2_approx(dl2 * av[e]), hv[e], dx * bv[n]);
+                    out = fmaf(cv[n], hv[e], out);
+                }
+                so[v] = h;
+            }
+            out = fmaf(Dd, xv[k], out);
+            if (p.z)
+                out *= silu_f(zv[k]);
+            Io<T>::store1(static_cast<T *>(p.y) + row, out);
+        }
+        __syncthreads();   // the staged B, C (and states) are reused by the next group of rows
+    }
+}
+
+template <typename T>
+ss_status launch_update_rows16(const UpdateParams &p, cudaStream_t stream)
+{
+    const int64_t dblocks = (p.d_inner + kBlock - 1) / kBlock;
+    const int64_t groups = (p.batch + kDecRows - 1) / kDecRows;
+    if (dblocks > 0x7fffffff)
+        return fail(SS_ERR_DIM, "grid too large");
+    const dim3 grid(static_cast<unsigned>(dblocks), static_cast<unsigned>(std::min<int64_t>(groups, 65535)));
+    state_update_rows16_kernel<T><<<grid, kBlock, 0, stream>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return fail(SS_ERR_LAUNCH, "state update launch failed: %s", cudaGetErrorString(e));
+    return SS_OK;
+}
+
 // One thread per (row, group of 4 states); the NQ threads of a row are
 // adjacent lanes of one warp and sum their partial readouts by shuffles.
 template <typename T, int NQ>
@@ -212,6 +329,9 @@ ss_status state_update(float *state, const void *x, const void *delta, const flo
     p.batch = batch; p.d_inner = d_inner; p.N = N;
     p.vec = (N % 4 == 0) && aligned16(state) && aligned16(A);
     p.vec_bc = ((N * static_cast<int64_t>(sizeof(T))) % 16 == 0) && aligned16(B) && aligned16(C);
+    const char *env = getenv("SS_DECODE_KERNEL");
+    if (p.vec && p.vec_bc && N == 16 && !(env && strcmp(env, "rows") == 0))
+        return launch_update_rows16<T>(p, stream);
     if (p.vec && N <= 16) {
         switch (N / 4) {
         case 1: return launch_update_rows<T, 1>(p, stream);
