@@ -41,6 +41,7 @@ L2_FLUSH_BYTES = 256 << 20  # > the 126 MB L2
 # kernel, not the host's launch latency. Long kernels need no cover.
 LAUNCH_COVER_CYCLES = 2_000_000   # about 1 ms at the B300 clock
 FALLBACK_HBM_GBS = 6400.0
+FALLBACK_BF16_TFLOPS = 1800.0
 SRC = os.path.join(ROOT, "selective_state_space_138_b300", "csrc", "ss_scan.cu")
 
 
@@ -88,9 +89,11 @@ def measured_peaks() -> dict:
         with open(path) as f:
             d = json.load(f)
         return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured", "sms": sms,
-                "sm_max_mhz": float(d.get("sm_max_mhz", 2032.0))}
+                "sm_max_mhz": float(d.get("sm_max_mhz", 2032.0)),
+                "bf16_tflops": float(d.get("bf16_tflops", FALLBACK_BF16_TFLOPS))}
     except Exception:
-        return {"hbm_gbs": FALLBACK_HBM_GBS, "source": "fallback", "sms": sms, "sm_max_mhz": 2032.0}
+        return {"hbm_gbs": FALLBACK_HBM_GBS, "source": "fallback", "sms": sms, "sm_max_mhz": 2032.0,
+                "bf16_tflops": FALLBACK_BF16_TFLOPS}
 
 
 # the source part each profiled kernel lives in (besides the shared device helpers)

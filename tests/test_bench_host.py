@@ -91,3 +91,13 @@ def test_profiled_traffic_reads_the_committed_summary(tmp_path, monkeypatch):
     assert bench.profiled_traffic(key) == 12345.0
     (prof / (key + ".md")).write_text("- `traffic_bytes_per_launch: 12345`\n- `source_sha256: %s`\n" % ("0" * 64))
     assert bench.profiled_traffic(key) is None
+
+
+def test_measured_peaks_carry_every_denominator_the_bench_reports():
+    """The roofline objects divide by the HBM copy bandwidth and by the bf16
+    tensor peak (SSD); both must come back whether the peaks file is read or
+    the fallback is taken."""
+    pk = bench.measured_peaks()
+    for key in ("hbm_gbs", "bf16_tflops", "sm_max_mhz", "sms", "source"):
+        assert key in pk, key
+    assert pk["hbm_gbs"] > 1000 and pk["bf16_tflops"] > 100
