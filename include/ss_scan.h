@@ -372,6 +372,18 @@ ss_status ss_ssd_fwd_bf16(const ss_bf16 *x, const ss_bf16 *dt, const float *A, c
                           int64_t nheads, int64_t headdim, int64_t ngroups, int64_t N,
                           cudaStream_t stream);
 
+/* Device-side faults recorded by the kernels since the last clear, as a bit
+ * set: SS_FAULT_WAIT_TIMEOUT = a wait for a tensor copy into shared memory
+ * (the forward scan's tiles, "Why the scan must be fused": inputs are staged
+ * once on chip) ran out of its one-second limit; the kernel then stops
+ * waiting, its outputs are not valid, and it lets the copies it issued land
+ * before it exits. Synchronises the device (reads a device word).
+ *   flags  host pointer, receives the bit set
+ *   clear  non-zero: reset the recorded faults to none
+ * Errors: SS_ERR_NULL (flags NULL), SS_ERR_INTERNAL (the read failed). */
+#define SS_FAULT_WAIT_TIMEOUT 1u
+ss_status ss_device_faults(unsigned int *flags, int clear);
+
 /* Message describing the last non-OK status returned on this host thread
  * ("" if none). The string is owned by the library. */
 const char *ss_last_error(void);

@@ -22,7 +22,7 @@ EXPORTS = ("ss_scan_fwd_bf16", "ss_scan_fwd_f32", "ss_scan_fwd_ex_bf16", "ss_sca
            "ss_conv_state_update_f32", "ss_scan_bwd_bf16", "ss_scan_bwd_f32", "ss_scan_bwd_workspace_bytes",
            "ss_scan_bwd_noalloc_bf16", "ss_scan_bwd_noalloc_f32", "ss_ssd_fwd_bf16", "ss_ssd_workspace_bytes",
            "ss_scan_fwd_train_bf16", "ss_scan_fwd_train_f32",
-           "ss_last_error", "ss_abi_version")
+           "ss_device_faults", "ss_last_error", "ss_abi_version")
 
 STATUS = {0: "SS_OK", -1: "SS_ERR_NULL", -2: "SS_ERR_DIM", -3: "SS_ERR_N", -4: "SS_ERR_DEVICE_PTR",
           -5: "SS_ERR_LAUNCH", -6: "SS_ERR_INTERNAL"}
@@ -81,6 +81,8 @@ def lib() -> ctypes.CDLL:
     L.ss_ssd_workspace_bytes.restype = ctypes.c_size_t
     L.ss_scan_bwd_workspace_bytes.argtypes = [i64] * 4
     L.ss_scan_bwd_workspace_bytes.restype = ctypes.c_size_t
+    L.ss_device_faults.argtypes = [ctypes.POINTER(ctypes.c_uint), ci]
+    L.ss_device_faults.restype = ci
     L.ss_last_error.argtypes = []
     L.ss_last_error.restype = ctypes.c_char_p
     L.ss_abi_version.argtypes = []
@@ -91,6 +93,17 @@ def lib() -> ctypes.CDLL:
 
 def last_error() -> str:
     return lib().ss_last_error().decode()
+
+
+FAULT_WAIT_TIMEOUT = 1   # SS_FAULT_WAIT_TIMEOUT
+
+
+def device_faults(clear: bool = True) -> int:
+    """Bit set of device-side faults the kernels recorded (0 = none);
+    synchronises the device."""
+    v = ctypes.c_uint(0)
+    _check(lib().ss_device_faults(ctypes.byref(v), 1 if clear else 0))
+    return v.value
 
 
 def abi_version() -> int:

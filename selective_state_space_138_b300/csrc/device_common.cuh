@@ -287,6 +287,77 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int PENDING>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(PENDING) : "memory"); }
 
+// ------------------------------------------------------------------ mbarriers and tensor copies
+//
+// Tiles are brought into shared memory by the tensor-memory accelerator
+// (cp.async.bulk.tensor) and signal an mbarrier with the bytes they deliver.
+// Every wait on such a barrier is bounded: after kWaitLimitNs it sets
+// kFaultWaitTimeout in g_fault_flags (read by the host through
+// ss_device_faults) and gives up, so that a copy that never lands cannot hang
+// the GPU.
+
+constexpr unsigned int kFaultWaitTimeout = 1u;
+constexpr uint64_t kWaitLimitNs = 1000000000ull;   // one second
+__device__ unsigned int g_fault_flags;
+
+__device__ __forceinline__ uint64_t global_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+// makes initialised barriers visible to the tensor copies (the async proxy)
+__device__ __forceinline__ void mbar_fence_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok)
+                 : "r"(bar), "r"(parity)
+                 : "memory");
+    return ok != 0;
+}
+
+// waits until the phase of the barrier with this parity has completed;
+// false (and the fault flag set) if it did not within kWaitLimitNs
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
+{
+    if (mbar_try_wait(bar, parity))
+        return true;
+    const uint64_t t0 = global_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (global_ns() - t0 > kWaitLimitNs) {
+            atomicOr(&g_fault_flags, kFaultWaitTimeout);
+            return false;
+        }
+    }
+    return true;
+}
+
+// tile (c0, c1, c2) of a 3-d tensor map into shared memory at dst, completing
+// on the barrier bar
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, uint32_t bar, int c0, int c1, int c2)
+{
+    asm volatile("cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                 " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+                 "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+}
+
 // element pair i, i+1 of a raw shared-memory row (i even)
 template <typename T>
 __device__ __forceinline__ u64 raw_pair(const unsigned char *row, int i)

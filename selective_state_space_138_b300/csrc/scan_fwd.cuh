@@ -40,6 +40,10 @@ struct ScanParams {
     const uint8_t *reset;   // (batch, L) sequence starts, or NULL (n-split kernel only)
     float4 *ckpt;           // the backward's stored states (its workspace layout), or NULL
     int64_t nsub;           // 16-step sub-chunks of the sequence (when ckpt is set)
+    int tma;                // n-split kernel: tiles come in through the tensor maps below
+    // 3-d maps over (step, row, batch row): x, dt, z with rows = channels and
+    // B, C with rows = states; boxes as the n-split kernel stages them
+    CUtensorMap tm_x, tm_dt, tm_z, tm_B, tm_C;
 };
 
 // Shared-memory index of (t, n) within a chunk: K-step blocks of NT floats per
@@ -261,8 +265,10 @@ struct NSplitShape {
     static constexpr int Y_BYTES = S * YQ * 4;
     static constexpr int X_BYTES = S * CH * 16 + S * CH * 4;   // segment end states and step sums
     static constexpr int R_BYTES = LC + 16;                     // sequence starts of a chunk, segment flag
-    static constexpr size_t BYTES = (size_t)STAGES * STAGE_BYTES + PD_BYTES + 2 * BC_BYTES + Y_BYTES + X_BYTES +
-                                    R_BYTES;
+    static constexpr size_t BAR_OFF = ((size_t)STAGES * STAGE_BYTES + PD_BYTES + 2 * BC_BYTES + Y_BYTES + X_BYTES +
+                                       R_BYTES + 7) / 8 * 8;
+    static constexpr size_t BYTES = BAR_OFF + 8 * STAGES;   // + the stage barriers
+    static_assert(STAGE_BYTES % 128 == 0 && RAW_X % 128 == 0 && RAW_BC % 128 == 0, "tensor-copy tiles 128-aligned");
     static_assert(RL % 2 == 0, "steps are processed in pairs");
 };
 
@@ -273,7 +279,7 @@ struct NSplitShape {
 // (reverse), i.e. at the boundary between t-1 and t either way.
 template <typename T, int S, bool REV, bool RST>
 __global__ void __launch_bounds__(NSplitShape<T, S>::NT, NSplitShape<T, S>::NT <= 128 ? 3 : 1)
-scan_nsplit_kernel(const ScanParams p)
+scan_nsplit_kernel(const __grid_constant__ ScanParams p)
 {
     using SH = NSplitShape<T, S>;
     constexpr int NT = SH::NT, CH = SH::CH, NS = SH::NS, LC = SH::LC, RL = SH::RL, PR = SH::PR;
@@ -282,7 +288,7 @@ scan_nsplit_kernel(const ScanParams p)
     constexpr int RW = RL * (int)sizeof(T) / 4;   // 32-bit words per prep/epilogue run
     static_assert(LC % 4 == 0 && D >= 1 && D <= LC, "chunk shape");
 
-    extern __shared__ __align__(16) unsigned char smem_raw[];
+    extern __shared__ __align__(128) unsigned char smem_raw[];
     unsigned char *raw = smem_raw;                                          // [STAGES][x, dt, z, B, C]
     u64 *Pd = reinterpret_cast<u64 *>(smem_raw + STAGES * SH::STAGE_BYTES);  // [LC][CH] (delta, delta x)
     float *Bf = reinterpret_cast<float *>(Pd + LC * CH);                    // [LC][NS]
@@ -293,6 +299,10 @@ scan_nsplit_kernel(const ScanParams p)
     unsigned char *Rst = reinterpret_cast<unsigned char *>(Sx + S * CH);    // [LC] sequence starts
     int *Rx = reinterpret_cast<int *>(Rst + LC);                            // any start in the segment
     const uint32_t raw_s = static_cast<uint32_t>(__cvta_generic_to_shared(raw));
+    const uint32_t bars_s = raw_s + static_cast<uint32_t>(SH::BAR_OFF);   // [STAGES] "stage filled" barriers
+    // tensor copies need 128-byte aligned destinations: should the dynamic
+    // shared memory not start on one, the tiles are staged in pieces instead
+    const bool tma = p.tma && (raw_s & 127u) == 0;
 
     const int tid = threadIdx.x;
     const int nseg = p.nseg;
@@ -372,11 +382,59 @@ scan_nsplit_kernel(const ScanParams p)
         poff[u] = ok ? pc * EPP : (1 << 30);   // a piece that does not exist is always past the end
     }
 
-    // copy the raw pieces of chunk j of the segment into stage j % STAGES
-    // (steps at or past the segment end and rows that do not exist are zero)
+    // Chunks are numbered across the walks of this CTA: chunk j of the current
+    // walk is number g0 + j and sits in stage (g0 + j) % STAGES. With tensor
+    // maps, a stage is filled by one thread's tensor copies completing on the
+    // stage's barrier (phase parity (g0 + j) / STAGES); g_issued and g_done
+    // count the numbers issued and waited for, so that copies still in flight
+    // after a wait gave up can be let land before the CTA exits.
+    int64_t g0 = 0, g_issued = 0, g_done = 0;
+    bool aborted = false;
+    static_assert((STAGES & (STAGES - 1)) == 0, "stage of a chunk number by masking");
+    auto stage_of = [](int64_t g) { return static_cast<int>(static_cast<uint32_t>(g) & (STAGES - 1)); };
+    auto parity_of = [](int64_t g) { return (static_cast<uint32_t>(g) / STAGES) & 1u; };
+    if (tma) {
+        if (tid == 0) {
+            for (int s = 0; s < STAGES; ++s)
+                mbar_init(bars_s + 8u * s, 1);
+            mbar_fence_init();
+        }
+        __syncthreads();
+    }
+    auto wait_chunk = [&](int64_t j) {
+        if (tma && !aborted) {
+            const int64_t g = g0 + j;
+            aborted = !mbar_wait(bars_s + 8u * stage_of(g), parity_of(g));
+            if (!aborted)
+                g_done = g + 1;
+        }
+    };
+
+    // bring chunk j of the segment into its stage (with the pieces: steps at
+    // or past the segment end and rows that do not exist are zero; with the
+    // tensor maps: rows past d_inner or N and steps past L are zero, a raw
+    // row holds the 16 bytes that follow the chunk as well)
     auto stage_in = [&](int64_t j, bool readout) {
-        const uint32_t st = raw_s + static_cast<uint32_t>((j % STAGES) * SH::STAGE_BYTES);
+        const int stage = stage_of(g0 + j);
+        const uint32_t st = raw_s + static_cast<uint32_t>(stage * SH::STAGE_BYTES);
         const int64_t t1 = t_lo + phys(j) * LC;
+        if (tma) {
+            if (tid == 0 && !aborted) {
+                const uint32_t bar = bars_s + 8u * stage;
+                const bool zz = readout && gate;
+                mbar_expect_tx(bar, 2 * SH::RAW_X + SH::RAW_BC + (zz ? SH::RAW_X : 0) + (readout ? SH::RAW_BC : 0));
+                const int c0 = static_cast<int>(t1), cd = static_cast<int>(d0), cb = static_cast<int>(b);
+                tma_load_3d(st, &p.tm_x, bar, c0, cd, cb);
+                tma_load_3d(st + SH::RAW_X, &p.tm_dt, bar, c0, cd, cb);
+                if (zz)
+                    tma_load_3d(st + 2 * SH::RAW_X, &p.tm_z, bar, c0, cd, cb);
+                tma_load_3d(st + 3 * SH::RAW_X, &p.tm_B, bar, c0, 0, cb);
+                if (readout)
+                    tma_load_3d(st + 3 * SH::RAW_X + SH::RAW_BC, &p.tm_C, bar, c0, 0, cb);
+                g_issued = g0 + j + 1;
+            }
+            return;
+        }
         const int rem = static_cast<int>(t_hi - t1 < (1 << 29) ? t_hi - t1 : (1 << 29));   // steps left
 #pragma unroll
         for (int u = 0; u < PPT; ++u) {
@@ -390,7 +448,7 @@ scan_nsplit_kernel(const ScanParams p)
             if (vec) {
                 cp_async16(st + soff[u], g, nb);
             } else {
-                unsigned char *dst = raw + (j % STAGES) * SH::STAGE_BYTES + soff[u];
+                unsigned char *dst = raw + stage * SH::STAGE_BYTES + soff[u];
                 const int ne = nb / (int)sizeof(T);
 #pragma unroll
                 for (int e = 0; e < EPP; ++e) {
@@ -408,7 +466,7 @@ scan_nsplit_kernel(const ScanParams p)
     // raw B (and C) of chunk j -> fp32 [t][n]: each item is (tensor, step t,
     // states 4g..4g+3), written as one 16-byte word
     auto convert_bc = [&](int64_t j, bool readout) {
-        const unsigned char *st = raw + (j % STAGES) * SH::STAGE_BYTES + 3 * SH::RAW_X;
+        const unsigned char *st = raw + stage_of(g0 + j) * SH::STAGE_BYTES + 3 * SH::RAW_X;
         const int items = (readout ? 2 : 1) * LC * S;
         for (int w = tid; w < items; w += NT) {
             const int m = w / (LC * S);
@@ -440,7 +498,7 @@ scan_nsplit_kernel(const ScanParams p)
 
     // delta and delta*x of this thread's steps of chunk j
     auto prep = [&](int64_t j, bool sum_steps) {
-        const unsigned char *st = raw + (j % STAGES) * SH::STAGE_BYTES;
+        const unsigned char *st = raw + stage_of(g0 + j) * SH::STAGE_BYTES;
         uint32_t xw[RW], dw[RW];
         read_run_raw<T, RL>(st + ce * SH::ROWB, re * RL, xw);
         read_run_raw<T, RL>(st + SH::RAW_X + ce * SH::ROWB, re * RL, dw);
@@ -485,6 +543,8 @@ scan_nsplit_kernel(const ScanParams p)
             else
                 cp_async_commit();
         cp_async_wait<STAGES - 2>();
+        if (nchunks > 0)
+            wait_chunk(0);
         __syncthreads();
         prep(0, !RO);
         convert_bc(0, RO);
@@ -559,11 +619,13 @@ scan_nsplit_kernel(const ScanParams p)
                 }
             }
             cp_async_wait<STAGES - 2>();   // chunk k+1 has landed (this thread's copies)
+            if (k + 1 < nchunks)
+                wait_chunk(k + 1);          // (the tensor copies of chunk k+1)
             __syncthreads();
 
             // ---- epilogue of chunk k: sum partials, skip term, gate, store
             if constexpr (RO) {
-                const unsigned char *st = raw + (k % STAGES) * SH::STAGE_BYTES;
+                const unsigned char *st = raw + stage_of(g0 + k) * SH::STAGE_BYTES;
                 uint32_t xw[RW], zw[RW];
                 read_run_raw<T, RL>(st + ce * SH::ROWB, re * RL, xw);
                 if (gate)
@@ -593,6 +655,7 @@ scan_nsplit_kernel(const ScanParams p)
             __syncthreads();
         }
         cp_async_wait<0>();
+        g0 += nchunks;
     };
 
     // the initial state (zero unless given)
@@ -676,6 +739,9 @@ scan_nsplit_kernel(const ScanParams p)
             if (4 * q + e < N)
                 fs[4 * q + e] = hv[e];
     }
+    if (tma && tid == 0)   // after a wait gave up: let the copies issued since land (each wait bounded)
+        for (int64_t g = g_done; g < g_issued; ++g)
+            mbar_wait(bars_s + 8u * stage_of(g), parity_of(g));
 }
 
 
@@ -750,6 +816,70 @@ int pick_segments(int64_t groups, int64_t L, int64_t lc, int64_t slots)
     const int64_t by_len = L / (4 * lc);
     n = n < by_len ? n : by_len;
     return n < 1 ? 1 : static_cast<int>(n);
+}
+
+// ------------------------------------------------------------------ tensor maps of the n-split kernel
+
+using EncodeTiledFn = PFN_cuTensorMapEncodeTiled_v12000;
+
+// the driver's tensor-map encoder, looked up once; null when unavailable
+EncodeTiledFn encode_tiled_fn()
+{
+    static const EncodeTiledFn fn = [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess) {
+            cudaGetLastError();
+            f = nullptr;
+        }
+        return reinterpret_cast<EncodeTiledFn>(f);
+    }();
+    return fn;
+}
+
+// map of a (batch, rows, L) tensor of T as three dimensions (L, rows, batch),
+// box (box_t, box_rows, 1); elements outside the tensor read as zero
+template <typename T>
+bool encode_rows_map(CUtensorMap *m, const void *base, int64_t L, int64_t rows, int64_t batch, uint32_t box_t,
+                     uint32_t box_rows)
+{
+    const EncodeTiledFn fn = encode_tiled_fn();
+    if (!fn || !base)
+        return false;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(L), static_cast<cuuint64_t>(rows),
+                                static_cast<cuuint64_t>(batch)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(L) * sizeof(T),
+                                   static_cast<cuuint64_t>(L) * static_cast<cuuint64_t>(rows) * sizeof(T)};
+    const cuuint32_t box[3] = {box_t, box_rows, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUtensorMapDataType dt = sizeof(T) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    return fn(m, dt, 3, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The n-split kernel's tiles as tensor maps: x, dt, z by channel rows with a
+// box of CH channels x one padded raw row (LC steps + 16 bytes), B and C by
+// state rows with a box of NS states x LC steps. Needs 16-byte aligned rows
+// (the caller's vec condition); SS_SCAN_TMA=0 keeps the cp.async staging.
+template <typename T>
+bool encode_scan_maps(ScanParams &p)
+{
+    const char *env = getenv("SS_SCAN_TMA");
+    if (env && strcmp(env, "0") == 0)
+        return false;
+    using SH = NSplitShape<T, 1>;   // CH, LC and the raw row do not depend on the state split
+    const uint32_t ns = p.N <= 4 ? 4u : (p.N <= 8 ? 8u : (p.N <= 16 ? 16u : 32u));
+    const uint32_t row_t = SH::ROWB / sizeof(T);
+    bool ok = encode_rows_map<T>(&p.tm_x, p.x, p.L, p.d_inner, p.batch, row_t, SH::CH) &&
+              encode_rows_map<T>(&p.tm_dt, p.dt, p.L, p.d_inner, p.batch, row_t, SH::CH) &&
+              encode_rows_map<T>(&p.tm_B, p.B, p.L, p.N, p.batch, SH::LC, ns) &&
+              encode_rows_map<T>(&p.tm_C, p.C, p.L, p.N, p.batch, SH::LC, ns);
+    if (ok && p.z)
+        ok = encode_rows_map<T>(&p.tm_z, p.z, p.L, p.d_inner, p.batch, row_t, SH::CH);
+    return ok;
 }
 
 template <typename T, int S, bool REV, bool RST>
@@ -890,7 +1020,7 @@ ss_status scan_fwd(const void *x, const void *dt, const float *A, const void *B,
     if (st != SS_OK)
         return st;
 
-    ScanParams p;
+    ScanParams p{};
     p.h0 = h0;
     p.reset = reset;
     p.ckpt = static_cast<float4 *>(ckpt);
@@ -900,12 +1030,17 @@ ss_status scan_fwd(const void *x, const void *dt, const float *A, const void *B,
     p.y = y; p.final_state = final_state;
     p.batch = batch; p.d_inner = d_inner; p.L = L; p.N = N;
     p.softplus = softplus ? 1 : 0;
-    p.vec = (L % 16 == 0) && aligned16(x) && aligned16(dt) && aligned16(y) && (!z || aligned16(z));
+    p.vec = (L % 16 == 0) && aligned16(x) && aligned16(dt) && aligned16(y) && (!z || aligned16(z)) &&
+            aligned16(B) && aligned16(C);
+    p.tma = 0;
 
     p.nseg = 1;
     p.seg_len = L;
-    if (extended || use_nsplit(N))
+    if (extended || use_nsplit(N)) {
+        if (p.vec && encode_scan_maps<T>(p))
+            p.tma = 1;
         return dispatch_nsplit<T>(p, reverse != 0, stream, sm_count(dev));
+    }
     const int lanes = pick_lanes(batch * d_inner, L, sm_count(dev));
     if (N <= 4)
         return dispatch_scan_lanes<T, 4>(p, lanes, stream);

@@ -6,7 +6,7 @@
 // constant-size cache", "Why the scan must be fused").
 //
 // One translation unit, kept in parts:
-//   device_common.cuh  device math, io conversion, f32x2 pairs, cp.async
+//   device_common.cuh  device math, io conversion, f32x2 pairs, cp.async, mbarriers and tensor copies
 //   host_common.cuh    error strings, pointer validation, device queries
 //   scan_fwd.cuh       forward scan (n-split and time-lane kernels)
 //   scan_bwd.cuh       backward pass (states recomputed)
@@ -15,6 +15,8 @@
 //   ssd.cuh            Mamba-2's scalar-decay scan on the tensor cores
 // followed here by the extern "C" entry points.
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <cooperative_groups.h>
@@ -220,6 +222,26 @@ ss_status ss_ssd_fwd_bf16(const ss_bf16 *x, const ss_bf16 *dt, const float *A, c
 {
     return ssd_fwd(x, dt, A, B, C, D, z, dt_bias, delta_softplus, h0, y, final_state, workspace, workspace_bytes,
                    batch, L, nheads, headdim, ngroups, N, stream);
+}
+
+ss_status ss_device_faults(unsigned int *flags, int clear)
+{
+    g_err[0] = '\0';
+    if (!flags)
+        return fail(SS_ERR_NULL, "flags is NULL");
+    static_assert(SS_FAULT_WAIT_TIMEOUT == kFaultWaitTimeout, "fault bits agree");
+    unsigned int v = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_fault_flags, sizeof(v));
+    if (e == cudaSuccess && clear) {
+        const unsigned int none = 0;
+        e = cudaMemcpyToSymbol(g_fault_flags, &none, sizeof(none));
+    }
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(SS_ERR_INTERNAL, "reading the device fault word failed: %s", cudaGetErrorString(e));
+    }
+    *flags = v;
+    return SS_OK;
 }
 
 const char *ss_last_error(void) { return g_err; }
