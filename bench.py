@@ -546,26 +546,46 @@ def roofline_obj(alg_bytes: float, ms: float, peaks: dict, traffic, elem_steps: 
 
 def oracle_rate(spec: I.ScanSpec, budget_s: float, inp=None):
     """The float64 oracle timed on this host's cores on a bounded sample of the
-    workload's rows (whole rows, every time step). Returns (elem-steps/s,
-    cores, sample description, seconds)."""
+    workload's rows (whole rows, every time step); when the whole workload
+    takes less than the budget, whole passes over it are repeated (at most 20).
+    Returns (elem-steps/s, cores, sample description, seconds)."""
     from oracle import oracle as O
     inp = inp if inp is not None else I.make_scan_inputs(spec)
     cores = O.default_threads()
     rows_total = spec.batch * spec.d_inner
     probe_rows = list(range(0, rows_total, max(1, rows_total // (4 * cores))))[: 4 * cores]
+    O.scan_rows(inp, probe_rows[:cores], threads=cores)   # first call: library load, page faults
     t = time.time()
     O.scan_rows(inp, probe_rows, threads=cores)
     per_row = (time.time() - t) / len(probe_rows)
     n_rows = int(min(rows_total, max(cores, budget_s / max(per_row, 1e-9))))
     stride = max(1, rows_total // n_rows)
     rows = list(range(0, rows_total, stride))[:n_rows]
+    passes = 0
     t = time.time()
-    O.scan_rows(inp, rows, threads=cores)
-    sec = time.time() - t
-    elems = len(rows) * spec.L * spec.N
+    while True:
+        O.scan_rows(inp, rows, threads=cores)
+        passes += 1
+        sec = time.time() - t
+        if len(rows) < rows_total or sec >= budget_s or passes >= 20:
+            break
+    elems = passes * len(rows) * spec.L * spec.N
     desc = "%d of %d (batch, channel) rows, every %d-th, all %d steps x %d states" % (
         len(rows), rows_total, stride, spec.L, spec.N)
+    if passes > 1:
+        desc += ", %d passes" % passes
     return elems / sec, cores, desc, sec
+
+
+def oracle_single_thread_rate(spec: I.ScanSpec, rows: int = 16, inp=None):
+    """The float64 oracle on one host thread over the workload's first rows
+    (elem-steps/s)."""
+    from oracle import oracle as O
+    inp = inp if inp is not None else I.make_scan_inputs(spec)
+    O.scan_rows(inp, [0], threads=1)
+    t = time.time()
+    O.scan_rows(inp, list(range(rows)), threads=1)
+    return rows * spec.L * spec.N / (time.time() - t)
 
 
 def reference_arm(args, rank, world):
@@ -580,7 +600,7 @@ def reference_arm(args, rank, world):
     desc, cores = "", 1
     t0 = time.time()
     for _ in range(args.steps):
-        r, cores, desc, s = oracle_rate(spec, budget_s=3.0, inp=inp)
+        r, cores, desc, s = oracle_rate(spec, budget_s=2.0, inp=inp)
         rates.append(r)
         secs += s
     value = statistics.median(rates)
@@ -804,7 +824,9 @@ def main(argv=None):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         r, cores, desc, sec = oracle_rate(spec, budget_s=12.0)
         line["cpu_baseline"] = {"value": r, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc,
-                                "seconds": round(sec, 2)}
+                                "seconds": round(sec, 2),
+                                "single_thread_value": oracle_single_thread_rate(spec),
+                                "single_thread_sample": "the first 16 (batch, channel) rows, one thread"}
 
     if rank == 0:
         print(json.dumps(line), flush=True)
