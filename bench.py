@@ -539,7 +539,20 @@ def roofline_obj(alg_bytes: float, ms: float, peaks: dict, traffic, elem_steps: 
         rate = elem_steps / (ms * 1e-3)
         out["alu_ceiling"] = {"elem_steps_per_s": ceiling, "achieved": rate, "frac": round(rate / ceiling, 4),
                               "derivation": "%d SMs x 32 element-steps/clk x %.0f MHz" % (peaks["sms"], peaks["sm_max_mhz"])}
+        out["floors_us"] = scan_floors_us(alg_bytes, elem_steps, peaks)
     return out
+
+
+def scan_floors_us(alg_bytes: float, elem_steps: float, peaks: dict) -> dict:
+    """The three lower bounds on a scan launch (microseconds): HBM (algorithmic
+    bytes at the measured copy bandwidth), the exponentials (one MUFU ex2 per
+    element-step, 32 per clock per SM) and fp32 issue (four FMA-pipe
+    operations per element-step, packed two to an f32x2 instruction, 128
+    lanes per clock per SM), at the maximum SM clock."""
+    clk = peaks["sm_max_mhz"] * 1e6
+    return {"hbm": round(alg_bytes / (peaks["hbm_gbs"] * 1e9) * 1e6, 2),
+            "exp": round(elem_steps / (peaks["sms"] * 32 * clk) * 1e6, 2),
+            "fp32_issue": round(elem_steps * 4 / (peaks["sms"] * 128 * 2 * clk) * 1e6, 2)}
 
 
 # ----------------------------------------------------------------- CPU (oracle)

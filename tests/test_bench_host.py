@@ -101,3 +101,16 @@ def test_measured_peaks_carry_every_denominator_the_bench_reports():
     for key in ("hbm_gbs", "bf16_tflops", "sm_max_mhz", "sms", "source"):
         assert key in pk, key
     assert pk["hbm_gbs"] > 1000 and pk["bf16_tflops"] > 100
+
+
+def test_scan_floors_of_the_headline_layer():
+    """HBM floor of the Mamba-130M layer at 6498.7 GB/s is the 31.3 us of the
+    scope table; one exponential per element-step at 32 per clock per SM is
+    the binding floor."""
+    pk = {"hbm_gbs": 6498.7, "sms": 148, "sm_max_mhz": 2032.0, "source": "measured"}
+    sp = bench.HEADLINE
+    E = sp.batch * sp.d_inner * sp.L * sp.N
+    fl = bench.scan_floors_us(bench.scan_alg_bytes(sp), E, pk)
+    assert abs(fl["hbm"] - 31.3) < 0.1
+    assert abs(fl["exp"] - E / (148 * 32 * 2032e6) * 1e6) < 1e-6 * fl["exp"] + 0.01
+    assert fl["exp"] > fl["hbm"] > fl["fp32_issue"]
