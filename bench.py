@@ -575,29 +575,35 @@ def scan_floors_us(alg_bytes: float, elem_steps: float, peaks: dict) -> dict:
 
 def oracle_rate(spec: I.ScanSpec, budget_s: float, inp=None):
     """The float64 oracle timed on this host's cores on a bounded sample of the
-    workload's rows (whole rows, every time step); when the whole workload
-    takes less than the budget, whole passes over it are repeated (at most 20).
-    Returns (elem-steps/s, cores, sample description, seconds)."""
+    workload's rows (whole rows, every time step): the sample grows until one
+    timed pass over it takes about budget_s; when the whole workload takes less
+    than that, whole passes over it are repeated (at most 20). Returns
+    (elem-steps/s, cores, sample description, seconds of the timed passes)."""
     from oracle import oracle as O
     inp = inp if inp is not None else I.make_scan_inputs(spec)
     cores = O.default_threads()
     rows_total = spec.batch * spec.d_inner
-    probe_rows = list(range(0, rows_total, max(1, rows_total // (4 * cores))))[: 4 * cores]
-    O.scan_rows(inp, probe_rows[:cores], threads=cores)   # first call: library load, page faults
-    t = time.time()
-    O.scan_rows(inp, probe_rows, threads=cores)
-    per_row = (time.time() - t) / len(probe_rows)
-    n_rows = int(min(rows_total, max(cores, budget_s / max(per_row, 1e-9))))
-    stride = max(1, rows_total // n_rows)
-    rows = list(range(0, rows_total, stride))[:n_rows]
-    passes = 0
-    t = time.time()
+    O.scan_rows(inp, list(range(min(rows_total, cores))), threads=cores)   # first call: library load, page faults
+
+    def sample(n):
+        stride = max(1, rows_total // n)
+        return list(range(0, rows_total, stride))[:n], stride
+
+    n = min(rows_total, 4 * cores)
     while True:
+        rows, stride = sample(n)
+        t = time.time()
         O.scan_rows(inp, rows, threads=cores)
-        passes += 1
         sec = time.time() - t
-        if len(rows) < rows_total or sec >= budget_s or passes >= 20:
+        if sec >= 0.5 * budget_s or n >= rows_total:
             break
+        n = min(rows_total, max(2 * n, int(n * 0.9 * budget_s / max(sec, 1e-3))))
+    passes = 1
+    while len(rows) == rows_total and sec < budget_s and passes < 20:
+        t = time.time()
+        O.scan_rows(inp, rows, threads=cores)
+        sec += time.time() - t
+        passes += 1
     elems = passes * len(rows) * spec.L * spec.N
     desc = "%d of %d (batch, channel) rows, every %d-th, all %d steps x %d states" % (
         len(rows), rows_total, stride, spec.L, spec.N)
