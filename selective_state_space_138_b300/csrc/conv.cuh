@@ -131,12 +131,37 @@ causal_conv1d_kernel(const ConvParams p)
 }
 
 // Vector path (16-byte aligned rows, L a multiple of the piece): a CTA stages
-// CG channels x LT steps of one batch row, plus the HP pieces before them, into
-// shared memory with asynchronous 16-byte copies (no registers held while the
-// loads are in flight), then each thread turns pieces of that tile into
-// outputs. Inputs before t = 0 come from the carried history (or are zero).
+// CG channels x PT pieces of one batch row, plus the HP pieces before them,
+// into shared memory with asynchronous 16-byte copies (no registers held while
+// the loads are in flight). Then 16 threads share a row, each turning PPL
+// consecutive pieces into outputs: the last K-1 inputs ride along in
+// registers from one piece to the next, so each input is unpacked once, and
+// the channel's taps and bias are read once. Outputs overwrite their own
+// input pieces in shared memory and leave for HBM with consecutive threads on
+// consecutive pieces. Pieces are stored XOR-swizzled within groups of 8
+// (piece j at column (j & ~7) | ((j ^ (j >> 3)) & 7)), so that the 16 threads
+// of a row, reading pieces PPL apart, hit distinct banks. Inputs before t = 0
+// come from the carried history (or are zero).
 constexpr int kConvTileBytes = 2048;   // one row of a tile
 constexpr int kConvRows = 8;           // channels per tile
+
+__device__ __forceinline__ int conv_swz(int j) { return (j & ~7) | ((j ^ (j >> 3)) & 7); }
+
+// 16 bytes of outputs in the io type
+template <typename T>
+__device__ __forceinline__ uint4 conv_pack(const float *o)
+{
+    uint4 w;
+    if constexpr (sizeof(T) == 4) {
+        w = make_uint4(__float_as_uint(o[0]), __float_as_uint(o[1]), __float_as_uint(o[2]), __float_as_uint(o[3]));
+    } else {
+        w.x = pack_bf16x2(o[0], o[1]);
+        w.y = pack_bf16x2(o[2], o[3]);
+        w.z = pack_bf16x2(o[4], o[5]);
+        w.w = pack_bf16x2(o[6], o[7]);
+    }
+    return w;
+}
 
 template <typename T, int K>
 __global__ void __launch_bounds__(kBlock)
@@ -147,66 +172,110 @@ causal_conv1d_tile_kernel(const ConvParams p)
     constexpr int HP = (H + EPP - 1) / EPP;      // halo pieces
     constexpr int PT = kConvTileBytes / 16;      // pieces per tile row
     constexpr int CG = kConvRows;
-    __shared__ __align__(16) uint4 tile[CG][PT + HP];
+    constexpr int LPR = kBlock / CG;             // threads per row
+    constexpr int PPL = PT / LPR;                // consecutive pieces per thread
+    static_assert(PT % LPR == 0 && PPL % 8 == 0 && kBlock % CG == 0, "tile shape");
+    __shared__ __align__(16) uint4 tile[CG][HP + PT];   // [halo pieces][swizzled pieces]
 
     const int64_t npieces = p.L / EPP;
     const int64_t pc0 = static_cast<int64_t>(blockIdx.x) * PT;
     const int64_t d0 = static_cast<int64_t>(blockIdx.y) * CG;
     const T *x = static_cast<const T *>(p.x);
+    const int r = threadIdx.x / LPR;             // compute role: row r, pieces j0 .. j0 + PPL - 1
+    const int j0 = (threadIdx.x % LPR) * PPL;
+    const int64_t d = d0 + r;
+    const bool act = d < p.d_inner;
+    float wd[K];
+#pragma unroll
+    for (int k = 0; k < K; ++k)
+        wd[k] = act ? __ldg(p.w + d * K + k) : 0.0f;
+    const float bv = (act && p.bias) ? __ldg(p.bias + d) : 0.0f;
+
     for (int64_t b = blockIdx.z; b < p.batch; b += gridDim.z) {
-        for (int i = threadIdx.x; i < CG * (PT + HP); i += kBlock) {
-            const int r = i / (PT + HP);
-            const int j = i % (PT + HP);
-            const int64_t d = d0 + r;
-            const int64_t pc = pc0 - HP + j;
-            const bool ok = d < p.d_inner && pc >= 0 && pc < npieces;
-            const T *src = ok ? x + (b * p.d_inner + d) * p.L + pc * EPP : x;
-            cp_async16(static_cast<uint32_t>(__cvta_generic_to_shared(&tile[r][j])), src, ok ? 16 : 0);
+#pragma unroll
+        for (int rr = 0; rr < CG; ++rr) {
+            const int64_t dr = d0 + rr;
+            for (int jj = threadIdx.x; jj < HP + PT; jj += kBlock) {
+                const int64_t pc = jj < HP ? pc0 - HP + jj : pc0 + (jj - HP);
+                const int col = jj < HP ? jj : HP + conv_swz(jj - HP);
+                const bool ok = dr < p.d_inner && pc >= 0 && pc < npieces;
+                const T *src = ok ? x + (b * p.d_inner + dr) * p.L + pc * EPP : x;
+                cp_async16(static_cast<uint32_t>(__cvta_generic_to_shared(&tile[rr][col])), src, ok ? 16 : 0);
+            }
         }
         cp_async_commit();
         cp_async_wait<0>();
         __syncthreads();
-        for (int i = threadIdx.x; i < CG * PT; i += kBlock) {
-            const int r = i / PT;
-            const int j = i % PT;
-            const int64_t d = d0 + r;
-            const int64_t pc = pc0 + j;
-            if (d >= p.d_inner || pc >= npieces)
-                continue;
-            float win[(HP + 1) * EPP];   // steps (pc - HP) * EPP ... pc * EPP + EPP - 1
+        const bool work = act && pc0 + j0 < npieces;
+        // the H inputs before piece j0: hist[i] is input (H - i) steps back
+        float hist[H > 0 ? H : 1];
+        if (work) {
+            float pv[HP * EPP > 0 ? HP * EPP : 1];
 #pragma unroll
-            for (int v = 0; v <= HP; ++v)
-                unpack_piece<T>(tile[r][j + v], win + v * EPP);
-            if (pc < HP && p.state_in) {   // steps before 0 come from the carried history
+            for (int v = 0; v < HP; ++v) {
+                const int jp = j0 - HP + v;   // piece index within the tile, negative in the halo
+                const uint4 w = jp < 0 ? tile[r][HP + jp] : tile[r][HP + conv_swz(jp)];
+                unpack_piece<T>(w, pv + v * EPP);
+            }
 #pragma unroll
-                for (int u = 0; u < HP * EPP; ++u) {
-                    const int64_t t = (pc - HP) * EPP + u;
-                    if (t < 0 && t >= -H)
-                        win[u] = Io<T>::load1(static_cast<const T *>(p.state_in) + (b * H + (H + t)) * p.d_inner + d);
+            for (int i = 0; i < H; ++i)
+                hist[i] = pv[HP * EPP - H + i];
+            if (pc0 + j0 == 0 && p.state_in) {   // steps before 0 come from the carried history
+#pragma unroll
+                for (int i = 0; i < H; ++i)
+                    hist[i] = Io<T>::load1(static_cast<const T *>(p.state_in) + (b * H + i) * p.d_inner + d);
+            }
+        }
+        __syncthreads();   // every thread has its history: pieces may now be overwritten by outputs
+        if (work) {
+#pragma unroll 2
+            for (int m = 0; m < PPL; ++m) {
+                const int j = j0 + m;
+                const int64_t pc = pc0 + j;
+                if (pc >= npieces)
+                    break;
+                float v[EPP];
+                unpack_piece<T>(tile[r][HP + conv_swz(j)], v);
+                float o[EPP];
+#pragma unroll
+                for (int e = 0; e < EPP; ++e) {
+                    float acc = bv;
+#pragma unroll
+                    for (int k = 0; k < K; ++k)
+                        acc = fmaf(wd[k], e - k >= 0 ? v[e - k >= 0 ? e - k : 0] : hist[H + e - k >= 0 ? H + e - k : 0],
+                                   acc);
+                    o[e] = p.silu ? silu_f(acc) : acc;
+                }
+                tile[r][HP + conv_swz(j)] = conv_pack<T>(o);   // in place; to HBM below
+                // the last H inputs become the history of the next piece
+                float nh[H > 0 ? H : 1];
+#pragma unroll
+                for (int i = 0; i < H; ++i) {
+                    const int u = EPP - H + i;   // window index relative to v
+                    nh[i] = u >= 0 ? v[u >= 0 ? u : 0] : hist[H + u >= 0 ? H + u : 0];
+                }
+#pragma unroll
+                for (int i = 0; i < H; ++i)
+                    hist[i] = nh[i];
+                if (H > 0 && p.state_out && pc == npieces - 1) {
+#pragma unroll
+                    for (int i = 0; i < H; ++i)
+                        Io<T>::store1(static_cast<T *>(p.state_out) + (b * H + i) * p.d_inner + d, hist[i]);
                 }
             }
-            float wd[K];
+        }
+        __syncthreads();
+        // outputs to HBM, consecutive threads on consecutive pieces of a row
 #pragma unroll
-            for (int k = 0; k < K; ++k)
-                wd[k] = __ldg(p.w + d * K + k);
-            const float bv = p.bias ? __ldg(p.bias + d) : 0.0f;
-            float o[EPP];
-#pragma unroll
-            for (int e = 0; e < EPP; ++e) {
-                float acc = bv;
-#pragma unroll
-                for (int k = 0; k < K; ++k)
-                    acc = fmaf(wd[k], win[HP * EPP + e - k], acc);
-                o[e] = p.silu ? silu_f(acc) : acc;
-            }
-            const int64_t row = b * p.d_inner + d;
-            Io<T>::storevec(static_cast<T *>(p.out) + row * p.L + pc * EPP, o);
-            if (H > 0 && p.state_out && pc == npieces - 1) {
-                // the last H inputs: window index HP * EPP + EPP - H + jj
-#pragma unroll
-                for (int jj = 0; jj < H; ++jj)
-                    Io<T>::store1(static_cast<T *>(p.state_out) + (b * H + jj) * p.d_inner + d,
-                                  win[HP * EPP + EPP - H + jj]);
+        for (int rr = 0; rr < CG; ++rr) {
+            const int64_t dr = d0 + rr;
+            if (dr >= p.d_inner)
+                break;
+            T *orow = static_cast<T *>(p.out) + (b * p.d_inner + dr) * p.L;
+            for (int jj = threadIdx.x; jj < PT; jj += kBlock) {
+                const int64_t pc = pc0 + jj;
+                if (pc < npieces)
+                    *reinterpret_cast<uint4 *>(orow + pc * EPP) = tile[rr][HP + conv_swz(jj)];
             }
         }
         __syncthreads();   // the tile is reused by the next batch row
