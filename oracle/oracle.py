@@ -70,6 +70,10 @@ def load(path: str | None = None):
     if hasattr(lib, "oracle_scan_bwd_rows"):
         lib.oracle_scan_bwd_rows.argtypes = [dp] * 8 + [ctypes.c_int] + [dp] * 12 + [ctypes.c_int64] * 6
         lib.oracle_scan_bwd_rows.restype = ctypes.c_int
+    if hasattr(lib, "oracle_scan_bwd_ex_rows"):
+        lib.oracle_scan_bwd_ex_rows.argtypes = ([dp] * 8 + [ctypes.c_int, dp, ctypes.c_void_p, ctypes.c_int]
+                                                + [dp] * 11 + [ctypes.c_int64] * 6)
+        lib.oracle_scan_bwd_ex_rows.restype = ctypes.c_int
     if hasattr(lib, "oracle_causal_conv1d_rows"):
         lib.oracle_causal_conv1d_rows.argtypes = [dp, dp, dp, ctypes.c_int, dp, dp, dp] + [ctypes.c_int64] * 6
         lib.oracle_causal_conv1d_rows.restype = ctypes.c_int
@@ -211,8 +215,10 @@ def ssd(x, dt, A, B, C, D=None, z=None, dt_bias=None, delta_softplus=True, h0=No
 
 
 def scan_bwd(x, dt, A, B, C, dout, D=None, z=None, dt_bias=None, delta_softplus=True, h0=None,
-             dfinal=None, threads: int | None = None, lib=None):
-    """Gradient of the selective scan in float64 (``oracle_scan_bwd_rows``).
+             dfinal=None, seq_start=None, reverse=False, threads: int | None = None, lib=None):
+    """Gradient of the selective scan in float64 (``oracle_scan_bwd_rows``;
+    with sequence starts (batch, L) or the reverse direction, the gradient of
+    ``scan_ex``: ``oracle_scan_bwd_ex_rows``).
 
     Same inputs as ``scan`` plus dout (batch, d_inner, L), the gradient of the
     (gated) output, and dfinal (batch, d_inner, N) or None, the gradient of the
@@ -237,8 +243,23 @@ def scan_bwd(x, dt, A, B, C, dout, D=None, z=None, dt_bias=None, delta_softplus=
     acc = [dict(dA=np.zeros((d_inner, N)), dB=np.zeros((batch, N, L)), dC=np.zeros((batch, N, L)),
                 dD=np.zeros(d_inner), ddt_bias=np.zeros(d_inner)) for _ in range(nt)]
 
+    st = None
+    if seq_start is not None:
+        if hasattr(seq_start, "detach"):
+            seq_start = seq_start.detach().cpu().numpy()
+        st = np.ascontiguousarray(np.asarray(seq_start) != 0, dtype=np.uint8)
+        assert st.shape == (batch, L)
+    ex = st is not None or bool(reverse)
+
     def run(i):
         a = acc[i]
+        if ex:
+            return lib.oracle_scan_bwd_ex_rows(
+                _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(dt_bias),
+                int(bool(delta_softplus)), _ptr(h0), None if st is None else st.ctypes.data_as(ctypes.c_void_p),
+                int(bool(reverse)), _ptr(dout), _ptr(dfinal), _ptr(dx), _ptr(ddt), _ptr(dz), _ptr(a["dA"]),
+                _ptr(a["dB"]), _ptr(a["dC"]), _ptr(a["dD"]), _ptr(a["ddt_bias"]), _ptr(dh0),
+                batch, d_inner, L, N, bounds[i], bounds[i + 1])
         return lib.oracle_scan_bwd_rows(_ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
                                         _ptr(dt_bias), int(bool(delta_softplus)), _ptr(h0), _ptr(dout),
                                         _ptr(dfinal), _ptr(dx), _ptr(ddt), _ptr(dz), _ptr(a["dA"]),

@@ -290,6 +290,142 @@ int oracle_scan_bwd_rows(const double *x, const double *dt, const double *A,
 }
 
 /*
+ * Gradient of oracle_scan_ex_rows (the scan with sequence starts and/or the
+ * reverse direction). Walking order i = 0 .. L-1 visits t(i) = i, or L-1-i
+ * when `reverse` is set. The scan it differentiates is, in that order,
+ *   h_in(i)  = (i == 0 ? h0 : out(i-1) * (1 - e(i-1))) * (1 - c(i))
+ *   out(i)   = a_t h_in(i) + delta_t B_t x_t,   y_t = C_t out(i) + D x_t (gated)
+ *   final    = out(L-1) * (1 - e(L-1))
+ * where the cut c(i) ("zero before the step") is seq_start[t(i)] walking
+ * forward and e(i) ("zero after the step") is seq_start[t(i)] walking
+ * backward (the other one is 0). Its adjoint, lam(i) = dLoss / d out(i):
+ *   lam(L-1) = C gy + (1 - e(L-1)) dfinal
+ *   lam(i)   = C_t gy_t + (1 - e(i)) (1 - c(i+1)) a_{t(i+1)} lam(i+1)
+ *   dh0      = (1 - c(0)) a_{t(0)} lam(0)
+ * and every term that the plain backward forms with a_t h_{t-1} uses
+ * a_t h_in(i). The per-step formulas are those of oracle_scan_bwd_rows.
+ */
+int oracle_scan_bwd_ex_rows(const double *x, const double *dt, const double *A,
+                            const double *B, const double *C, const double *D,
+                            const double *z, const double *dt_bias, int delta_softplus,
+                            const double *h0, const unsigned char *seq_start, int reverse,
+                            const double *dout, const double *dfinal,
+                            double *dx, double *ddt, double *dz, double *dA, double *dB,
+                            double *dC, double *dD, double *ddt_bias, double *dh0,
+                            int64_t batch, int64_t d_inner, int64_t L, int64_t N,
+                            int64_t row_begin, int64_t row_end)
+{
+    if (!x || !dt || !A || !B || !C || !dout || !dx || !ddt || !dA || !dB || !dC)
+        return -1;
+    if (batch < 0 || d_inner < 0 || L < 1 || N <= 0)
+        return -1;
+    if (row_begin < 0 || row_end > batch * d_inner || row_begin > row_end)
+        return -1;
+
+    double *hin = (double *)malloc((size_t)L * N * sizeof(double));   /* h_in(i), by walking index */
+    double *out = (double *)malloc((size_t)L * N * sizeof(double));   /* out(i) */
+    double *as = (double *)malloc((size_t)L * N * sizeof(double));    /* a_{t(i)} */
+    double *del = (double *)malloc((size_t)L * sizeof(double));       /* delta_{t(i)} */
+    double *lam = (double *)malloc((size_t)N * sizeof(double));
+    double *h = (double *)malloc((size_t)N * sizeof(double));
+    if (!hin || !out || !as || !del || !lam || !h) {
+        free(hin); free(out); free(as); free(del); free(lam); free(h);
+        return -2;
+    }
+
+    for (int64_t r = row_begin; r < row_end; ++r) {
+        const int64_t b = r / d_inner;
+        const int64_t d = r % d_inner;
+        const double *xr = x + r * L;
+        const double *dtr = dt + r * L;
+        const double *zr = z ? z + r * L : NULL;
+        const double *gr = dout + r * L;
+        const double Dd = D ? D[d] : 0.0;
+#define TW(i) (reverse ? L - 1 - (i) : (i))
+#define CUT_BEFORE(i) (!reverse && seq_start && seq_start[b * L + TW(i)])
+#define CUT_AFTER(i) (reverse && seq_start && seq_start[b * L + TW(i)])
+
+        /* forward in walking order, keeping h_in and out of every step */
+        for (int64_t n = 0; n < N; ++n)
+            h[n] = h0 ? h0[r * N + n] : 0.0;
+        for (int64_t i = 0; i < L; ++i) {
+            const int64_t t = TW(i);
+            if (CUT_BEFORE(i))
+                for (int64_t n = 0; n < N; ++n)
+                    h[n] = 0.0;
+            const double v = dtr[t] + (dt_bias ? dt_bias[d] : 0.0);
+            del[i] = delta_softplus ? oracle_softplus(v) : v;
+            for (int64_t n = 0; n < N; ++n) {
+                const double a = exp(del[i] * A[d * N + n]);
+                as[i * N + n] = a;
+                hin[i * N + n] = h[n];
+                h[n] = a * h[n] + del[i] * B[(b * N + n) * L + t] * xr[t];
+                out[i * N + n] = h[n];
+            }
+            if (CUT_AFTER(i))
+                for (int64_t n = 0; n < N; ++n)
+                    h[n] = 0.0;
+        }
+
+        /* adjoint, walking order reversed */
+        for (int64_t n = 0; n < N; ++n)
+            lam[n] = dfinal ? dfinal[r * N + n] : 0.0;
+        for (int64_t i = L - 1; i >= 0; --i) {
+            const int64_t t = TW(i);
+            if (i < L - 1) {
+                const int cut = CUT_BEFORE(i + 1);
+                for (int64_t n = 0; n < N; ++n)
+                    lam[n] = cut ? 0.0 : lam[n] * as[(i + 1) * N + n];
+            }
+            if (CUT_AFTER(i))
+                for (int64_t n = 0; n < N; ++n)
+                    lam[n] = 0.0;
+            double y = Dd * xr[t];
+            for (int64_t n = 0; n < N; ++n)
+                y += C[(b * N + n) * L + t] * out[i * N + n];
+            double gy = gr[t];
+            if (zr) {
+                const double s = sigmoid(zr[t]);
+                gy = gr[t] * zr[t] * s;
+                if (dz)
+                    dz[r * L + t] = gr[t] * y * s * (1.0 + zr[t] * (1.0 - s));
+            }
+            double dxt = Dd * gy;
+            double ddel = 0.0;
+            for (int64_t n = 0; n < N; ++n) {
+                const double Bn = B[(b * N + n) * L + t];
+                const double Cn = C[(b * N + n) * L + t];
+                lam[n] += Cn * gy;
+                const double ah = as[i * N + n] * hin[i * N + n];   /* a_t h_in(i) */
+                dxt += lam[n] * del[i] * Bn;
+                ddel += lam[n] * (A[d * N + n] * ah + Bn * xr[t]);
+                dA[d * N + n] += lam[n] * del[i] * ah;
+                dB[(b * N + n) * L + t] += lam[n] * del[i] * xr[t];
+                dC[(b * N + n) * L + t] += gy * out[i * N + n];
+            }
+            dx[r * L + t] = dxt;
+            const double v = dtr[t] + (dt_bias ? dt_bias[d] : 0.0);
+            const double dv = delta_softplus ? ddel * sigmoid(v) : ddel;
+            ddt[r * L + t] = dv;
+            if (ddt_bias)
+                ddt_bias[d] += dv;
+            if (dD)
+                dD[d] += gy * xr[t];
+        }
+        if (dh0) {
+            const int cut = CUT_BEFORE(0);
+            for (int64_t n = 0; n < N; ++n)
+                dh0[r * N + n] = cut ? 0.0 : as[n] * lam[n];
+        }
+#undef TW
+#undef CUT_BEFORE
+#undef CUT_AFTER
+    }
+    free(hin); free(out); free(as); free(del); free(lam); free(h);
+    return 0;
+}
+
+/*
  * The scan with the options of the extended entry point, written as its
  * definition: the same step as oracle_scan_rows, walked over t = 0 .. L-1 or,
  * when `reverse` is set, over t = L-1 .. 0 (h_t = a_t h_{t+1} + delta_t B_t x_t,

@@ -353,6 +353,42 @@ def check_bwd_finite_differences(lib):
             np.testing.assert_allclose(g[gk], fd, rtol=1e-6, atol=1e-6, err_msg=name)
 
 
+def check_bwd_variants_finite_differences(lib):
+    """The gradient of the scan with sequence starts and/or the reverse
+    direction equals the derivative of that scan: central differences of
+    <dout, out> + <dfinal, final_state> in every input, with starts at the
+    first step, inside the row and at the last step."""
+    rng = np.random.default_rng(43)
+    eps = 1e-6
+    starts = np.zeros((2, 9), dtype=np.uint8)
+    starts[0, [0, 4]] = 1
+    starts[1, [3, 8]] = 1
+    for reverse, st in ((False, starts), (True, None), (True, starts)):
+        p = _bwd_problem(rng)
+        dout = rng.normal(size=p["x"].shape)
+        dfin = rng.normal(size=p["h0"].shape)
+
+        def loss(**over):
+            q = dict(p, **over)
+            y, fs = O.scan_ex(q["x"], q["dt"], q["A"], q["B"], q["C"], D=q["D"], z=q["z"], dt_bias=q["dt_bias"],
+                              h0=q["h0"], seq_start=st, reverse=reverse, threads=1, lib=lib)
+            return float((y * dout).sum() + (fs * dfin).sum())
+
+        g = O.scan_bwd(p["x"], p["dt"], p["A"], p["B"], p["C"], dout, D=p["D"], z=p["z"], dt_bias=p["dt_bias"],
+                       h0=p["h0"], dfinal=dfin, seq_start=st, reverse=reverse, threads=1, lib=lib)
+        for name, gk in (("x", "dx"), ("dt", "ddt"), ("A", "dA"), ("B", "dB"), ("C", "dC"), ("h0", "dh0"),
+                         ("D", "dD"), ("z", "dz"), ("dt_bias", "ddt_bias")):
+            arr = p[name]
+            fd = np.zeros_like(arr)
+            for i in np.ndindex(arr.shape):
+                hi, lo = arr.copy(), arr.copy()
+                hi[i] += eps
+                lo[i] -= eps
+                fd[i] = (loss(**{name: hi}) - loss(**{name: lo})) / (2 * eps)
+            np.testing.assert_allclose(g[gk], fd, rtol=1e-6, atol=1e-6,
+                                       err_msg="%s reverse=%s starts=%s" % (name, reverse, st is not None))
+
+
 def check_bwd_impulse_closed_form(lib):
     """One state, constant step, an impulse x = (1, 0, ...), B = C = 1, no
     softplus, no gate: y_T = e^{A (delta_1 + ... + delta_T)} delta_0, so
@@ -519,6 +555,7 @@ ALL_CHECKS = [check_recurrence_example, check_softplus_values, check_gate_theore
               check_selective_copy_euler, check_impulse_response, check_mixing_matrix,
               check_lti_convolution, check_zero_and_huge_step, check_causality_linearity_chain,
               check_conv_impulse_and_silu, check_conv_constant_input_and_zero_history, check_conv_history_chain,
-              check_bwd_finite_differences, check_bwd_impulse_closed_form, check_bwd_linear_in_cotangent,
+              check_bwd_finite_differences, check_bwd_variants_finite_differences,
+              check_bwd_impulse_closed_form, check_bwd_linear_in_cotangent,
               check_reverse_is_forward_on_flipped_inputs, check_sequence_starts_are_separate_sequences,
               check_ssd_is_the_scan_with_one_decay_per_head, check_ssd_masked_matmul_form]

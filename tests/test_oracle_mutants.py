@@ -68,6 +68,12 @@ MUTANTS = {
                              "dB[(b * N + n) * L + t] += lam[n] * xr[t];")],
     "bwd_skip_gradient_missing": [("double dxt = Dd * gy;", "double dxt = 0.0;")],
     "bwd_dh0_without_decay": [("dh0[r * N + n] = as[n] * lam[n];", "dh0[r * N + n] = lam[n];")],
+    "bwd_ex_cut_ignored_in_adjoint": [("lam[n] = cut ? 0.0 : lam[n] * as[(i + 1) * N + n];",
+                                       "lam[n] = lam[n] * as[(i + 1) * N + n];")],
+    "bwd_ex_dfinal_through_cut": [("            if (CUT_AFTER(i))\n                for (int64_t n = 0; n < N; ++n)\n                    lam[n] = 0.0;\n            double y",
+                                   "            double y")],
+    "bwd_ex_state_before_cut": [("                hin[i * N + n] = h[n];", "                hin[i * N + n] = i > 0 ? out[(i - 1) * N + n] : h[n];")],
+    "bwd_ex_walks_forward": [("#define TW(i) (reverse ? L - 1 - (i) : (i))", "#define TW(i) (i)")],
 }
 
 
