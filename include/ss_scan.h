@@ -278,6 +278,38 @@ ss_status ss_scan_bwd_f32(const float *x, const float *delta, const float *A, co
                           int64_t d_inner, int64_t L, int64_t N, cudaStream_t stream);
 
 /*
+ * ss_scan_bwd_ex_bf16 / ss_scan_bwd_ex_f32 -- gradient of ss_scan_fwd_ex_*:
+ * the backward pass above for the scan with sequence starts and/or the
+ * reverse direction ("What each parameter does": the state forgets everything
+ * at a document break; one direction of a bidirectional layer).
+ *   seq_start : (batch, L) bytes, non-zero at the first step of each packed
+ *               sequence, or NULL. As in the forward, nothing crosses the
+ *               boundary before a marked step: no state into it and no
+ *               gradient back across it.
+ *   reverse   : non-zero for the reverse-direction scan
+ *               h_t = exp(delta_t A) h_{t+1} + delta_t B_t x_t.
+ * Every other argument as ss_scan_bwd_* (the workspace holds the backward's
+ * own stored states; there is no states_from_forward). dh0 is the gradient of
+ * the state that enters the walk (at t = 0, or t = L-1 when reversed).
+ * Errors: as ss_scan_bwd_*.
+ */
+ss_status ss_scan_bwd_ex_bf16(const ss_bf16 *x, const ss_bf16 *delta, const float *A, const ss_bf16 *B,
+                              const ss_bf16 *C, const float *D, const ss_bf16 *z, const float *dt_bias,
+                              int delta_softplus, const float *h0, const uint8_t *seq_start, int reverse,
+                              const ss_bf16 *dout, const float *dfinal_state, ss_bf16 *dx, ss_bf16 *ddelta,
+                              float *dA, float *dB, float *dC, float *dD, ss_bf16 *dz, float *ddt_bias,
+                              float *dh0, void *workspace, size_t workspace_bytes, int64_t batch,
+                              int64_t d_inner, int64_t L, int64_t N, cudaStream_t stream);
+
+ss_status ss_scan_bwd_ex_f32(const float *x, const float *delta, const float *A, const float *B,
+                             const float *C, const float *D, const float *z, const float *dt_bias,
+                             int delta_softplus, const float *h0, const uint8_t *seq_start, int reverse,
+                             const float *dout, const float *dfinal_state, float *dx, float *ddelta,
+                             float *dA, float *dB, float *dC, float *dD, float *dz, float *ddt_bias,
+                             float *dh0, void *workspace, size_t workspace_bytes, int64_t batch,
+                             int64_t d_inner, int64_t L, int64_t N, cudaStream_t stream);
+
+/*
  * ss_scan_fwd_train_bf16 / ss_scan_fwd_train_f32 -- ss_scan_fwd_* for training:
  * the same outputs (with an optional initial state h0, as ss_scan_fwd_ex_*),
  * and in `workspace` (at least ss_scan_bwd_workspace_bytes(...) bytes, 16-byte

@@ -21,7 +21,7 @@ EXPORTS = ("ss_scan_fwd_bf16", "ss_scan_fwd_f32", "ss_scan_fwd_ex_bf16", "ss_sca
            "ss_causal_conv1d_bf16", "ss_causal_conv1d_f32", "ss_conv_state_update_bf16",
            "ss_conv_state_update_f32", "ss_scan_bwd_bf16", "ss_scan_bwd_f32", "ss_scan_bwd_workspace_bytes",
            "ss_scan_bwd_noalloc_bf16", "ss_scan_bwd_noalloc_f32", "ss_ssd_fwd_bf16", "ss_ssd_workspace_bytes",
-           "ss_scan_fwd_train_bf16", "ss_scan_fwd_train_f32",
+           "ss_scan_fwd_train_bf16", "ss_scan_fwd_train_f32", "ss_scan_bwd_ex_bf16", "ss_scan_bwd_ex_f32",
            "ss_device_faults", "ss_last_error", "ss_abi_version")
 
 STATUS = {0: "SS_OK", -1: "SS_ERR_NULL", -2: "SS_ERR_DIM", -3: "SS_ERR_N", -4: "SS_ERR_DEVICE_PTR",
@@ -68,6 +68,9 @@ def lib() -> ctypes.CDLL:
         getattr(L, name).restype = ci
     for name in ("ss_scan_bwd_bf16", "ss_scan_bwd_f32"):
         getattr(L, name).argtypes = [vp] * 8 + [ci] + [vp] * 13 + [ctypes.c_size_t, ci] + [i64] * 4 + [vp]
+        getattr(L, name).restype = ci
+    for name in ("ss_scan_bwd_ex_bf16", "ss_scan_bwd_ex_f32"):
+        getattr(L, name).argtypes = [vp] * 8 + [ci, vp, vp, ci] + [vp] * 12 + [ctypes.c_size_t] + [i64] * 4 + [vp]
         getattr(L, name).restype = ci
     for name in ("ss_scan_fwd_train_bf16", "ss_scan_fwd_train_f32"):
         getattr(L, name).argtypes = [vp] * 8 + [ci, vp, vp, vp, vp, ctypes.c_size_t] + [i64] * 4 + [vp]
@@ -314,8 +317,11 @@ def scan_fwd_train(x, delta, A, B, C, D=None, z=None, dt_bias=None, delta_softpl
 
 
 def scan_bwd(x, delta, A, B, C, dout, D=None, z=None, dt_bias=None, delta_softplus=True, h0=None,
-             dfinal_state=None, grads=None, workspace=None, stream=None, noalloc=False, states_from_forward=False):
-    """Gradient of ``scan_fwd`` (see ``ss_scan_bwd_*``): the forward inputs,
+             dfinal_state=None, grads=None, workspace=None, stream=None, noalloc=False, states_from_forward=False,
+             seq_start=None, reverse=False):
+    """Gradient of ``scan_fwd`` (see ``ss_scan_bwd_*``), or with ``seq_start``
+    (batch, L) bool/uint8 and/or ``reverse`` of ``scan_fwd_ex`` (see
+    ``ss_scan_bwd_ex_*``; not with ``noalloc`` or ``states_from_forward``): the forward inputs,
     dout (batch, d_inner, L) in the io dtype and optionally dfinal_state
     (batch, d_inner, N) fp32. ``grads`` may hold preallocated outputs under the
     names below; missing ones are allocated. ``workspace`` is a uint8 device
@@ -354,6 +360,14 @@ def scan_bwd(x, delta, A, B, C, dout, D=None, z=None, dt_bias=None, delta_softpl
         if g.get(k) is None:
             g[k] = torch.empty(shp, dtype=dt_, device=dev)
         _need(g[k], k, dt_, shp)
+    ex = seq_start is not None or bool(reverse)
+    if ex and (noalloc or states_from_forward):
+        raise ValueError("sequence starts and the reverse direction take the workspace form without "
+                         "states_from_forward")
+    if seq_start is not None:
+        if seq_start.dtype == torch.bool:
+            seq_start = seq_start.to(torch.uint8)
+        _need(seq_start, "seq_start", torch.uint8, (batch, L))
     if noalloc:
         fn = getattr(lib(), "ss_scan_bwd_noalloc_" + sfx)
         _check(fn(_ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(dt_bias),
@@ -367,6 +381,15 @@ def scan_bwd(x, delta, A, B, C, dout, D=None, z=None, dt_bias=None, delta_softpl
         if states_from_forward:
             raise ValueError("states_from_forward needs the workspace that scan_fwd_train filled")
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    if ex:
+        fn = getattr(lib(), "ss_scan_bwd_ex_" + sfx)
+        _check(fn(_ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(dt_bias),
+                  int(bool(delta_softplus)), _ptr(h0), _ptr(seq_start), int(bool(reverse)), _ptr(dout),
+                  _ptr(dfinal_state), _ptr(g["dx"]), _ptr(g["ddelta"]), _ptr(g["dA"]), _ptr(g["dB"]), _ptr(g["dC"]),
+                  _ptr(g.get("dD")), _ptr(g.get("dz")), _ptr(g.get("ddt_bias")), _ptr(g.get("dh0")),
+                  _ptr(workspace), workspace.numel() * workspace.element_size(), batch, d_inner, L, N,
+                  _stream(stream)))
+        return {k: g.get(k) for k in ("dx", "ddelta", "dz", "dA", "dB", "dC", "dD", "ddt_bias", "dh0")}
     fn = getattr(lib(), "ss_scan_bwd_" + sfx)
     _check(fn(_ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(dt_bias),
               int(bool(delta_softplus)), _ptr(h0), _ptr(dout), _ptr(dfinal_state), _ptr(g["dx"]),

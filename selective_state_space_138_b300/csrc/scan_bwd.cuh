@@ -47,6 +47,7 @@ struct BwdParams {
     int vec;    // io rows 16-byte aligned with L a multiple of the piece
     int vec4;   // dB, dC rows take 16-byte atomic adds (L % 4 == 0, aligned)
     int states_ready;   // the workspace already holds the stored states (written by the forward pass)
+    const uint8_t *reset;   // (batch, L) sequence starts (RST kernels only)
 };
 
 #define SS_BWD_STAGES 2
@@ -75,15 +76,25 @@ struct BwdShape {
     static constexpr int BC_BYTES = LC * NS * 4;
     static constexpr int PART_BYTES = 3 * S * HC * CH * 4;
     static constexpr int DBC_BYTES = 2 * LC * NS * 4;
+    static constexpr int R_BYTES = LC;                          // sequence starts of a chunk
     static constexpr size_t BYTES = (size_t)STAGES * STAGE_BYTES + PD_BYTES + DY_BYTES + 2 * BC_BYTES + PART_BYTES +
-                                    DBC_BYTES;
+                                    DBC_BYTES + R_BYTES;
     static_assert(RH >= 2 && RH % 2 == 0, "epilogue runs are processed in pairs");
 };
 
 // both halves negated
 __device__ __forceinline__ u64 neg2(u64 a) { return a ^ 0x8000000080000000ull; }
 
-template <typename T, int S>
+// REV: the gradient of the reverse-direction scan (h_t = a_t h_{t+1} + delta_t
+// B_t x_t); RST: of the scan with sequence starts (nothing carried across the
+// boundary before a marked step). Both are written in walking coordinates: the
+// forward walk of phase 1 follows the recurrence (chunk phys1(j), chunk step
+// tu(u)), phase 2 walks the other way; the tiles, the stored states (indexed by
+// physical 16-step sub-chunk) and every per-step buffer stay in physical order.
+// A walking step can be cut before it (RST forward: its start flag) or after
+// it (RST reverse: its start flag); a cut zeroes the carried state in the
+// walks and the adjoint passed across it.
+template <typename T, int S, bool REV, bool RST>
 __global__ void __launch_bounds__(BwdShape<T, S>::NT, BwdShape<T, S>::NT <= 128 ? 3 : 1)
 scan_bwd_kernel(const BwdParams p)
 {
@@ -101,6 +112,7 @@ scan_bwd_kernel(const BwdParams p)
     float *Cf = Bf + LC * NS;                                               // [LC][NS]
     float *Part = Cf + LC * NS;                                             // [3][S][HC/2][CH] step pairs
     float *DBC = Part + 3 * S * HC * CH;                                    // [2][LC][NS]
+    unsigned char *Rst = reinterpret_cast<unsigned char *>(DBC + 2 * LC * NS);  // [LC] sequence starts
     const uint32_t raw_s = static_cast<uint32_t>(__cvta_generic_to_shared(raw));
 
     const int tid = threadIdx.x;
@@ -109,6 +121,11 @@ scan_bwd_kernel(const BwdParams p)
     const int64_t L = p.L, N = p.N, Dn = p.d_inner;
     const bool vec = p.vec != 0;
     const int64_t nchunks = (L + LC - 1) / LC;
+    // physical chunk of the j-th chunk of the forward walk (phase 1) and of the
+    // reverse walk (phase 2); physical step in a chunk of walking step u
+    auto phys1 = [&](int64_t j) -> int64_t { return REV ? nchunks - 1 - j : j; };
+    auto phys2 = [&](int64_t j) -> int64_t { return REV ? j : nchunks - 1 - j; };
+    auto tu = [](int u) { return REV ? LC - 1 - u : u; };
 
     const int cs = tid % CH;     // scan role: lane = channel, warp = state group
     const int q = tid / CH;
@@ -239,6 +256,10 @@ scan_bwd_kernel(const BwdParams p)
         }
         const int64_t left64 = L - (k * LC + re * RL);
         const int lim = act_e ? static_cast<int>(left64 < RL ? left64 : RL) : 0;
+        if (RST && tid < LC) {
+            const int64_t tt = k * LC + tid;
+            Rst[tid] = (tt < L && p.reset[b * L + tt]) ? 1 : 0;
+        }
 #pragma unroll
         for (int i = 0; i < RL; i += 2) {
             const u64 xx = word_pair<T>(xw, i);
@@ -285,22 +306,23 @@ scan_bwd_kernel(const BwdParams p)
 #pragma unroll
         for (int s = 0; s < STAGES - 1; ++s)
             if (s < nchunks)
-                stage_in(s, s, false);
+                stage_in(phys1(s), s, false);
             else
                 cp_async_commit();
         cp_async_wait<STAGES - 2>();
         __syncthreads();
-        prep(0, 0, false);
+        prep(phys1(0), 0, false);
         convert_bc(0, false);
         __syncthreads();
-        for (int64_t k = 0; k < nchunks; ++k) {
-            if (k + STAGES - 1 < nchunks)
-                stage_in(k + STAGES - 1, static_cast<int>((k + STAGES - 1) % STAGES), false);
+        for (int64_t j = 0; j < nchunks; ++j) {
+            const int64_t k = phys1(j);
+            if (j + STAGES - 1 < nchunks)
+                stage_in(phys1(j + STAGES - 1), static_cast<int>((j + STAGES - 1) % STAGES), false);
             else
                 cp_async_commit();
 #pragma unroll
-            for (int hh = 0; hh < NH; ++hh) {
-                const int64_t s = k * NH + hh;
+            for (int hw = 0; hw < NH; ++hw) {
+                const int64_t s = k * NH + (REV ? NH - 1 - hw : hw);   // physical sub-chunk
                 if (act_s && s < p.nsub) {
                     float a0, a1, a2, a3;
                     upk(h01, a0, a1);
@@ -309,20 +331,28 @@ scan_bwd_kernel(const BwdParams p)
                 }
 #pragma unroll 4
                 for (int i = 0; i < HC; ++i) {
-                    const int t = hh * HC + i;
+                    const int t = tu(hw * HC + i);
+                    if (RST && !REV && Rst[t]) {   // a sequence starts at t: nothing carries in
+                        h01 = 0;
+                        h23 = 0;
+                    }
                     float dl, dx;
                     upk(Pd[t * CH + cs], dl, dx);
                     const ulonglong2 Bq = *reinterpret_cast<const ulonglong2 *>(Bq_s + t * NS);
                     const u64 dd = splat(dl), xx = splat(dx);
                     h01 = fma2(ex2_2(mul2(dd, A01)), h01, mul2(xx, Bq.x));
                     h23 = fma2(ex2_2(mul2(dd, A23)), h23, mul2(xx, Bq.y));
+                    if (RST && REV && Rst[t]) {    // a sequence starts at t: nothing carries to t-1
+                        h01 = 0;
+                        h23 = 0;
+                    }
                 }
             }
             cp_async_wait<STAGES - 2>();
             __syncthreads();
-            if (k + 1 < nchunks) {
-                prep(k + 1, static_cast<int>((k + 1) % STAGES), false);
-                convert_bc(static_cast<int>((k + 1) % STAGES), false);
+            if (j + 1 < nchunks) {
+                prep(phys1(j + 1), static_cast<int>((j + 1) % STAGES), false);
+                convert_bc(static_cast<int>((j + 1) % STAGES), false);
             }
             __syncthreads();
         }
@@ -348,39 +378,41 @@ scan_bwd_kernel(const BwdParams p)
     const u64 ln2_2 = splat(0.6931471805599453f);
 
     float4 ck_cur = make_float4(0.f, 0.f, 0.f, 0.f);   // stored state of the sub-chunk processed next
-    if (act_s)
-        ck_cur = ck[(p.nsub - 1) * ckstride];
+    if (act_s)   // the last sub-chunk of the forward walk comes first
+        ck_cur = ck[(REV ? 0 : p.nsub - 1) * ckstride];
 
-    // chunk order j = 0, 1, ... is k = nchunks - 1 - j
+    // chunk j of the reverse walk is physical chunk phys2(j)
 #pragma unroll 1
     for (int s = 0; s < STAGES - 1; ++s)
         if (s < nchunks)
-            stage_in(nchunks - 1 - s, s, true);
+            stage_in(phys2(s), s, true);
         else
             cp_async_commit();
     cp_async_wait<STAGES - 2>();
     __syncthreads();
-    prep(nchunks - 1, 0, true);
+    prep(phys2(0), 0, true);
     convert_bc(0, true);
     __syncthreads();
 
 #pragma unroll 1
     for (int64_t j = 0; j < nchunks; ++j) {
-        const int64_t k = nchunks - 1 - j;
+        const int64_t k = phys2(j);
         const int slot = static_cast<int>(j % STAGES);
         if (j + STAGES - 1 < nchunks)
-            stage_in(k - (STAGES - 1), static_cast<int>((j + STAGES - 1) % STAGES), true);
+            stage_in(phys2(j + STAGES - 1), static_cast<int>((j + STAGES - 1) % STAGES), true);
         else
             cp_async_commit();
 
 #pragma unroll 1
-        for (int hh = NH - 1; hh >= 0; --hh) {
-            const int64_t s = k * NH + hh;
+        for (int hh = NH - 1; hh >= 0; --hh) {   // walking sub-chunk hh, physical ph
+            const int ph = REV ? NH - 1 - hh : hh;
+            const int64_t s = k * NH + ph;
             if (s < p.nsub) {
-                // the stored state of the next sub-chunk is fetched while this one runs
+                // the stored state of the sub-chunk walked before this one is fetched while this one runs
+                const int64_t s_next = REV ? s + 1 : s - 1;
                 float4 ck_next = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (act_s && s >= 1)
-                    ck_next = ck[(s - 1) * ckstride];
+                if (act_s && s_next >= 0 && s_next < p.nsub)
+                    ck_next = ck[s_next * ckstride];
                 // recompute the HC states of this sub-chunk from its stored start
                 u64 H01[HC], H23[HC];
                 u64 S01, S23;   // the state before the sub-chunk
@@ -392,22 +424,34 @@ scan_bwd_kernel(const BwdParams p)
                     u64 g01 = S01, g23 = S23;
 #pragma unroll
                     for (int i = 0; i < HC; ++i) {
-                        const int t = hh * HC + i;
+                        const int t = tu(hh * HC + i);
+                        if (RST && !REV && Rst[t]) {
+                            g01 = 0;
+                            g23 = 0;
+                        }
                         float dl, dx;
                         upk(Pd[t * CH + cs], dl, dx);
                         const ulonglong2 Bq = *reinterpret_cast<const ulonglong2 *>(Bq_s + t * NS);
                         const u64 dd = splat(dl), xx = splat(dx);
                         g01 = fma2(ex2_2(mul2(dd, A01)), g01, mul2(xx, Bq.x));
                         g23 = fma2(ex2_2(mul2(dd, A23)), g23, mul2(xx, Bq.y));
-                        H01[i] = g01;
+                        H01[i] = g01;   // the step's output, before a cut after it
                         H23[i] = g23;
+                        if (RST && REV && Rst[t]) {
+                            g01 = 0;
+                            g23 = 0;
+                        }
                     }
                 }
                 // adjoint recurrence backwards over the sub-chunk, two steps per round
                 // step i: lam += C gy; v = (lam dx, gy h) for the channel sums; the
                 // state sums for the epilogue; then lam *= a_i for step i-1
                 auto step = [&](int i, float *v, float &r_, float &pa, float &yy) {
-                    const int t = hh * HC + i;
+                    const int t = tu(hh * HC + i);
+                    if (RST && REV && Rst[t]) {   // cut after this step: nothing flows back from the later ones
+                        lam01 = 0;
+                        lam23 = 0;
+                    }
                     float dl, dx;
                     upk(Pd[t * CH + cs], dl, dx);
                     const float gy = DY[t * CH + cs];
@@ -422,8 +466,12 @@ scan_bwd_kernel(const BwdParams p)
                     upk(mul2(gy2, H23[i]), v[6], v[7]);
                     const u64 a01 = ex2_2(mul2(dd, A01));
                     const u64 a23 = ex2_2(mul2(dd, A23));
-                    const u64 p01 = mul2(lam01, mul2(a01, i > 0 ? H01[i > 0 ? i - 1 : 0] : S01));   // lam a_t h_{t-1}
-                    const u64 p23 = mul2(lam23, mul2(a23, i > 0 ? H23[i > 0 ? i - 1 : 0] : S23));
+                    // the state entering the step (zero across a cut)
+                    const bool cut_in = RST && ((!REV && Rst[t]) || (REV && i > 0 && Rst[tu(hh * HC + (i > 0 ? i - 1 : 0))]));
+                    const u64 hin01 = cut_in ? 0 : (i > 0 ? H01[i > 0 ? i - 1 : 0] : S01);
+                    const u64 hin23 = cut_in ? 0 : (i > 0 ? H23[i > 0 ? i - 1 : 0] : S23);
+                    const u64 p01 = mul2(lam01, mul2(a01, hin01));   // lam a_t h_in
+                    const u64 p23 = mul2(lam23, mul2(a23, hin23));
                     dA01 = fma2(p01, dd, dA01);
                     dA23 = fma2(p23, dd, dA23);
                     r_ = hsum(fma2(lam23, Bq.y, mul2(lam01, Bq.x)));
@@ -431,6 +479,10 @@ scan_bwd_kernel(const BwdParams p)
                     yy = hsum(fma2(Cq.y, H23[i], mul2(Cq.x, H01[i])));
                     lam01 = mul2(lam01, a01);
                     lam23 = mul2(lam23, a23);
+                    if (RST && !REV && Rst[t]) {   // cut before this step: nothing flows to the earlier ones
+                        lam01 = 0;
+                        lam23 = 0;
+                    }
                 };
                 const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4, b1 = lane & 2;
 #pragma unroll
@@ -439,10 +491,11 @@ scan_bwd_kernel(const BwdParams p)
                     float r1, pa1, y1, r0, pa0, y0;
                     step(i, val, r1, pa1, y1);
                     step(i - 1, val + 8, r0, pa0, y0);
-                    float2 *pp = reinterpret_cast<float2 *>(Part) + (q * (HC / 2) + (i >> 1)) * CH + cs;
-                    pp[0] = make_float2(r0, r1);
-                    pp[S * (HC / 2) * CH] = make_float2(pa0, pa1);
-                    pp[2 * S * (HC / 2) * CH] = make_float2(y0, y1);
+                    // the pair of physical steps (2m, 2m+1) of the sub-chunk: walking (i-1, i), or (i, i-1) when reversed
+                    float2 *pp = reinterpret_cast<float2 *>(Part) + (q * (HC / 2) + (REV ? (HC - 1 - i) >> 1 : i >> 1)) * CH + cs;
+                    pp[0] = REV ? make_float2(r1, r0) : make_float2(r0, r1);
+                    pp[S * (HC / 2) * CH] = REV ? make_float2(pa1, pa0) : make_float2(pa0, pa1);
+                    pp[2 * S * (HC / 2) * CH] = REV ? make_float2(y1, y0) : make_float2(y0, y1);
                     // transposing butterfly: value (lane >> 1) & 15 ends summed over the warp
                     float w[8];
 #pragma unroll
@@ -472,7 +525,7 @@ scan_bwd_kernel(const BwdParams p)
                     if ((lane & 1) == 0) {
                         const int kk = (lane >> 1) & 15;   // < 8: step i, else step i-1
                         const int kv = kk & 7;             // 0..3: dB of state 4q+kv, 4..7: dC of 4q+kv-4
-                        const int t = hh * HC + i - (kk >> 3);
+                        const int t = tu(hh * HC + i - (kk >> 3));
                         DBC[((kv >> 2) * LC + t) * NS + 4 * q + (kv & 3)] = sum;
                     }
                 }
@@ -481,7 +534,7 @@ scan_bwd_kernel(const BwdParams p)
             // ---- epilogue of the sub-chunk: steps hh*HC + re*RH .. + RH - 1
             if (s < p.nsub) {
                 const unsigned char *st = raw + slot * SH::STAGE_BYTES;
-                const int off = hh * HC + re * RH;
+                const int off = ph * HC + re * RH;
                 uint32_t xw[RHW], dw[RHW], zw[RHW], gw[RHW];
                 read_run_raw<T, RH>(st + ce * SH::ROWB, off, xw);
                 read_run_raw<T, RH>(st + SH::RAW_X + ce * SH::ROWB, off, dw);
@@ -580,7 +633,7 @@ scan_bwd_kernel(const BwdParams p)
         __syncthreads();
         if (j + 1 < nchunks) {
             const int nslot = static_cast<int>((j + 1) % STAGES);
-            prep(k - 1, nslot, true);
+            prep(phys2(j + 1), nslot, true);
             convert_bc(nslot, true);
         }
         __syncthreads();
@@ -628,11 +681,11 @@ size_t bwd_workspace_bytes(int64_t batch, int64_t d_inner, int64_t L, int64_t N)
     return static_cast<size_t>(batch) * nsub * bwd_groups(N) * d_inner * 16;
 }
 
-template <typename T, int S>
+template <typename T, int S, bool REV, bool RST>
 ss_status launch_bwd(const BwdParams &p, cudaStream_t stream)
 {
     using SH = BwdShape<T, S>;
-    auto kernel = scan_bwd_kernel<T, S>;
+    auto kernel = scan_bwd_kernel<T, S, REV, RST>;
     const size_t smem = SH::BYTES;
     if (smem > 48u * 1024u) {
         cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -653,12 +706,23 @@ ss_status launch_bwd(const BwdParams &p, cudaStream_t stream)
     return SS_OK;
 }
 
+template <typename T, int S>
+ss_status dispatch_bwd(const BwdParams &p, bool reverse, cudaStream_t stream)
+{
+    const bool rst = p.reset != nullptr;
+    if (!reverse && !rst) return launch_bwd<T, S, false, false>(p, stream);
+    if (!reverse) return launch_bwd<T, S, false, true>(p, stream);
+    if (!rst) return launch_bwd<T, S, true, false>(p, stream);
+    return launch_bwd<T, S, true, true>(p, stream);
+}
+
 template <typename T>
 ss_status scan_bwd(const void *x, const void *dt, const float *A, const void *B, const void *C, const float *D,
                    const void *z, const float *dt_bias, int softplus, const float *h0, const void *dout,
                    const float *dfinal, void *dx, void *ddt, float *dA, float *dB, float *dC, float *dD, void *dz,
                    float *ddt_bias, float *dh0, void *workspace, size_t workspace_bytes, int64_t batch,
-                   int64_t d_inner, int64_t L, int64_t N, cudaStream_t stream, int states_ready = 0)
+                   int64_t d_inner, int64_t L, int64_t N, cudaStream_t stream, int states_ready = 0,
+                   const uint8_t *reset = nullptr, int reverse = 0)
 {
     g_err[0] = '\0';
     if (batch <= 0 || d_inner <= 0 || L <= 0)
@@ -676,7 +740,7 @@ ss_status scan_bwd(const void *x, const void *dt, const float *A, const void *B,
                              {D, "D", false},        {z, "z", false},       {dt_bias, "dt_bias", false},
                              {h0, "h0", false},      {dfinal, "dfinal_state", false},
                              {dD, "dD", false},      {dz, "dz", false},     {ddt_bias, "ddt_bias", false},
-                             {dh0, "dh0", false}};
+                             {dh0, "dh0", false},    {reset, "seq_start", false}};
     int dev = 0;
     ss_status st = check_ptrs(list, static_cast<int>(sizeof(list) / sizeof(list[0])), &dev);
     if (st != SS_OK)
@@ -684,6 +748,9 @@ ss_status scan_bwd(const void *x, const void *dt, const float *A, const void *B,
     if (workspace_bytes < need)
         return fail(SS_ERR_DIM, "workspace of %zu bytes is smaller than the %zu bytes required", workspace_bytes,
                     need);
+    if (states_ready && (reset || reverse))
+        return fail(SS_ERR_DIM, "states stored by the training forward are kept for the forward direction "
+                    "without sequence starts only");
     if (!aligned16(workspace))
         return fail(SS_ERR_DIM, "workspace must be 16-byte aligned");
 
@@ -702,7 +769,7 @@ ss_status scan_bwd(const void *x, const void *dt, const float *A, const void *B,
         }
     }
 
-    BwdParams p;
+    BwdParams p{};
     p.x = x; p.dt = dt; p.B = B; p.C = C; p.z = z; p.dout = dout;
     p.A = A; p.D = D; p.dt_bias = dt_bias; p.h0 = h0; p.dfinal = dfinal;
     p.dx = dx; p.ddt = ddt; p.dz = z ? dz : nullptr;
@@ -712,14 +779,16 @@ ss_status scan_bwd(const void *x, const void *dt, const float *A, const void *B,
     p.nsub = (L + kBwdHC - 1) / kBwdHC;
     p.softplus = softplus ? 1 : 0;
     p.states_ready = states_ready ? 1 : 0;
+    p.reset = reset;
     p.vec = (L % 16 == 0) && aligned16(x) && aligned16(dt) && aligned16(dout) && aligned16(dx) &&
             aligned16(ddt) && (!z || aligned16(z)) && (!p.dz || aligned16(p.dz));
     p.vec4 = (L % 4 == 0) && aligned16(dB) && aligned16(dC);
     const int64_t S = bwd_groups(N);
-    if (S == 1) return launch_bwd<T, 1>(p, stream);
-    if (S == 2) return launch_bwd<T, 2>(p, stream);
-    if (S == 4) return launch_bwd<T, 4>(p, stream);
-    return launch_bwd<T, 8>(p, stream);
+    const bool rev = reverse != 0;
+    if (S == 1) return dispatch_bwd<T, 1>(p, rev, stream);
+    if (S == 2) return dispatch_bwd<T, 2>(p, rev, stream);
+    if (S == 4) return dispatch_bwd<T, 4>(p, rev, stream);
+    return dispatch_bwd<T, 8>(p, rev, stream);
 }
 
 // ------------------------------------------------------------------ built-in scratch (no caller workspace)

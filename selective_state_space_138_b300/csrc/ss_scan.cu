@@ -159,6 +159,32 @@ ss_status ss_scan_bwd_f32(const float *x, const float *delta, const float *A, co
                            stream, states_from_forward);
 }
 
+ss_status ss_scan_bwd_ex_bf16(const ss_bf16 *x, const ss_bf16 *delta, const float *A, const ss_bf16 *B,
+                              const ss_bf16 *C, const float *D, const ss_bf16 *z, const float *dt_bias,
+                              int delta_softplus, const float *h0, const uint8_t *seq_start, int reverse,
+                              const ss_bf16 *dout, const float *dfinal_state, ss_bf16 *dx, ss_bf16 *ddelta, float *dA,
+                              float *dB, float *dC, float *dD, ss_bf16 *dz, float *ddt_bias, float *dh0,
+                              void *workspace, size_t workspace_bytes, int64_t batch, int64_t d_inner, int64_t L,
+                              int64_t N, cudaStream_t stream)
+{
+    return scan_bwd<__nv_bfloat16>(x, delta, A, B, C, D, z, dt_bias, delta_softplus, h0, dout, dfinal_state, dx,
+                                   ddelta, dA, dB, dC, dD, dz, ddt_bias, dh0, workspace, workspace_bytes, batch,
+                                   d_inner, L, N, stream, 0, seq_start, reverse);
+}
+
+ss_status ss_scan_bwd_ex_f32(const float *x, const float *delta, const float *A, const float *B, const float *C,
+                             const float *D, const float *z, const float *dt_bias, int delta_softplus,
+                             const float *h0, const uint8_t *seq_start, int reverse, const float *dout,
+                             const float *dfinal_state, float *dx, float *ddelta, float *dA, float *dB, float *dC,
+                             float *dD, float *dz, float *ddt_bias, float *dh0, void *workspace,
+                             size_t workspace_bytes, int64_t batch, int64_t d_inner, int64_t L, int64_t N,
+                             cudaStream_t stream)
+{
+    return scan_bwd<float>(x, delta, A, B, C, D, z, dt_bias, delta_softplus, h0, dout, dfinal_state, dx, ddelta,
+                           dA, dB, dC, dD, dz, ddt_bias, dh0, workspace, workspace_bytes, batch, d_inner, L, N,
+                           stream, 0, seq_start, reverse);
+}
+
 ss_status ss_scan_fwd_train_bf16(const ss_bf16 *x, const ss_bf16 *delta, const float *A, const ss_bf16 *B,
                                  const ss_bf16 *C, const float *D, const ss_bf16 *z, const float *dt_bias,
                                  int delta_softplus, const float *h0, ss_bf16 *y, float *final_state, void *workspace,

@@ -29,6 +29,27 @@ def test_header_and_binding_agree():
     assert declared_functions() == sorted(binding.EXPORTS)
 
 
+def declared_arity():
+    """Number of parameters of every function the header declares."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    out = {}
+    for m in re.finditer(r"\b(ss_[a-z0-9_]+)\s*\(([^)]*)\)\s*;", text):
+        params = m.group(2).strip()
+        out[m.group(1)] = 0 if params in ("", "void") else params.count(",") + 1
+    return out
+
+
+def test_binding_argtypes_match_the_header(lib):
+    """Every function the binding declares argument types for takes as many
+    arguments as the header says (a miscount would pass the wrong values)."""
+    arity = declared_arity()
+    assert set(arity) == set(binding.EXPORTS)
+    for name, n in arity.items():
+        argtypes = getattr(lib, name).argtypes
+        assert argtypes is not None, name
+        assert len(argtypes) == n, (name, len(argtypes), n)
+
+
 def test_every_declared_symbol_is_exported(lib):
     for name in declared_functions():
         assert hasattr(lib, name), name

@@ -34,7 +34,8 @@ def assert_grad_close(got, ref, io_dtype, key):
     return float(err.max())
 
 
-def run_case(spec, use_D=True, use_z=True, use_bias=True, softplus=True, use_h0=False, use_dfinal=True):
+def run_case(spec, use_D=True, use_z=True, use_bias=True, softplus=True, use_h0=False, use_dfinal=True,
+             seq_start=None, reverse=False):
     inp = I.make_scan_inputs(spec)
     if not softplus and not use_bias:
         # without softplus and bias the raw step is the step: keep it positive
@@ -48,11 +49,13 @@ def run_case(spec, use_D=True, use_z=True, use_bias=True, softplus=True, use_h0=
                            D=g["D"] if use_D else None, z=g["z"] if use_z else None,
                            dt_bias=g["dt_bias"] if use_bias else None, delta_softplus=softplus,
                            h0=None if h0 is None else h0.cuda(),
-                           dfinal_state=None if dfin is None else dfin.cuda())
+                           dfinal_state=None if dfin is None else dfin.cuda(),
+                           seq_start=None if seq_start is None else seq_start.cuda(), reverse=reverse)
     torch.cuda.synchronize()
     ref = O.scan_bwd(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], bw["dout"],
                      D=inp["D"] if use_D else None, z=inp["z"] if use_z else None,
-                     dt_bias=inp["dt_bias"] if use_bias else None, delta_softplus=softplus, h0=h0, dfinal=dfin)
+                     dt_bias=inp["dt_bias"] if use_bias else None, delta_softplus=softplus, h0=h0, dfinal=dfin,
+                     seq_start=seq_start, reverse=reverse)
     errs = {}
     for k, r in ref.items():
         kg = "ddelta" if k == "ddt" else k   # the oracle names it after its dt argument
@@ -158,3 +161,58 @@ def test_bwd_with_states_stored_by_the_training_forward(shape):
             continue
         kg = "ddelta" if k == "ddt" else k
         assert_grad_close(got[kg].float().cpu().numpy(), r, torch.bfloat16, kg)
+
+
+def _starts(batch, L, seed, first=True, last=True):
+    """Sequence starts: every row at step 0 (when `first`), a few seeded
+    interior steps, and the last step (when `last`)."""
+    rng = np.random.default_rng(seed)
+    st = np.zeros((batch, L), dtype=np.uint8)
+    for b in range(batch):
+        if first:
+            st[b, 0] = 1
+        if L > 2:
+            st[b, rng.choice(np.arange(1, L - 1), size=min(3, L - 2), replace=False)] = 1
+        if last and L > 1:
+            st[b, L - 1] = 1
+    return torch.from_numpy(st)
+
+
+EX_SHAPES = [  # batch, d_inner, L, N: a partial last chunk, a partial last 16-step block, several chunks
+    (1, 1, 1, 1), (2, 5, 16, 16), (2, 33, 47, 16), (1, 40, 100, 5), (2, 64, 256, 16), (1, 37, 129, 8),
+    (3, 20, 70, 20), (1, 16, 300, 12), (2, 24, 64, 32)]
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("mode", ["reverse", "starts", "reverse_starts"])
+@pytest.mark.parametrize("shape", EX_SHAPES, ids=lambda s: "b%d_d%d_l%d_n%d" % s)
+def test_bwd_variants_match_oracle(shape, mode, io):
+    """Gradient of the scan with the reverse direction and/or sequence starts
+    (``ss_scan_bwd_ex_*``), with an initial state and a final-state gradient."""
+    b, d, L, N = shape
+    spec = I.ScanSpec(b, d, L, N, io=io, seed=2000 + L + N)
+    st = _starts(b, L, seed=L) if "starts" in mode else None
+    run_case(spec, use_h0=True, seq_start=st, reverse=mode.startswith("reverse"))
+
+
+@pytest.mark.parametrize("mode", ["reverse", "starts", "reverse_starts"])
+def test_bwd_variants_long_row(mode):
+    """A 4096-step row with starts at a few hundred steps: the stored states and
+    the cuts across many chunks and sub-chunks."""
+    spec = I.ScanSpec(1, 64, 4096, 16, io="bf16", seed=5)
+    st = None
+    if "starts" in mode:
+        rng = np.random.default_rng(11)
+        st = torch.zeros(1, 4096, dtype=torch.uint8)
+        st[0, rng.choice(4096, size=300, replace=False)] = 1
+    run_case(spec, use_h0=True, seq_start=st, reverse=mode.startswith("reverse"))
+
+
+def test_bwd_variants_reject_stored_forward_states():
+    spec = I.ScanSpec(1, 8, 32, 4, io="f32", seed=1)
+    inp = I.make_scan_inputs(spec)
+    g = {k: inp[k].cuda() for k in ("x", "dt", "B", "C", "A")}
+    ws = torch.zeros(binding.scan_bwd_workspace_bytes(1, 8, 32, 4), dtype=torch.uint8, device="cuda")
+    with pytest.raises(ValueError):
+        binding.scan_bwd(g["x"], g["dt"], g["A"], g["B"], g["C"], g["x"], workspace=ws, states_from_forward=True,
+                         reverse=True)
