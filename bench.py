@@ -449,12 +449,14 @@ def time_conv_step(spec: I.DecodeSpec, steps: int, k: int = 4):
     return ms, bd * 2 * 2 + 2 * bd * (k - 1) * 2 + spec.d_inner * (k + 1) * 4
 
 
-def time_bwd(spec: I.ScanSpec, steps: int, warmup: int, from_forward: bool = False):
+def time_bwd(spec: I.ScanSpec, steps: int, warmup: int, from_forward: bool = False, variant: bool = False):
     """Median device time (ms) of the backward pass over ``steps`` launches,
     each preceded by an L2 flush; outputs and workspace preallocated. With
     ``from_forward`` the workspace is filled once by the training forward and
     every timed backward skips its own forward walk; the training forward's
-    median time is then returned too."""
+    median time is then returned too. With ``variant`` the gradient of the
+    reverse-direction scan with a sequence start every 250 steps is timed
+    instead."""
     from selective_state_space_138_b300 import binding
     inp = I.make_scan_inputs(spec)
     g = {k: inp[k].cuda() for k in ("x", "dt", "z", "B", "C", "A", "D", "dt_bias")}
@@ -463,8 +465,16 @@ def time_bwd(spec: I.ScanSpec, steps: int, warmup: int, from_forward: bool = Fal
                      dtype=torch.uint8, device="cuda")
     scratch = L2Flush()
     grads = None
+    starts = None
+    if variant:
+        starts = torch.zeros(spec.batch, spec.L, dtype=torch.uint8)
+        starts[:, ::250] = 1
+        starts = starts.cuda()
 
     def run():
+        if variant:
+            return binding.scan_bwd(g["x"], g["dt"], g["A"], g["B"], g["C"], dout, D=g["D"], z=g["z"],
+                                    dt_bias=g["dt_bias"], grads=grads, workspace=ws, seq_start=starts, reverse=True)
         return binding.scan_bwd(g["x"], g["dt"], g["A"], g["B"], g["C"], dout, D=g["D"], z=g["z"],
                                 dt_bias=g["dt_bias"], grads=grads, workspace=ws, states_from_forward=from_forward)
 
@@ -819,6 +829,12 @@ def main(argv=None):
         extras["bwd_" + HEADLINE.name] = {
             "elem_steps_per_s": HEADLINE.elem_steps / (bms * 1e-3), "kernel_ms_median": bms,
             "roofline": bro, "note": "backward pass (all gradients, states recomputed), L2 flushed before each"}
+        vbms = time_bwd(HEADLINE, 10, 3, variant=True)
+        extras["bwd_reverse_starts_" + HEADLINE.name] = {
+            "elem_steps_per_s": HEADLINE.elem_steps / (vbms * 1e-3), "kernel_ms_median": vbms,
+            "roofline": roofline_obj(bwd_alg_bytes(HEADLINE) + HEADLINE.batch * HEADLINE.L, vbms, peaks, None),
+            "note": "backward of the reverse-direction scan with a sequence start every 250 steps "
+                    "(ss_scan_bwd_ex_*), L2 flushed before each"}
         tbms, tfms = time_bwd(HEADLINE, 10, 3, from_forward=True)
         extras["train_step_" + HEADLINE.name] = {
             "fwd_train_ms_median": tfms, "bwd_from_forward_ms_median": tbms,
