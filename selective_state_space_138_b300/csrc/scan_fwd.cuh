@@ -240,7 +240,9 @@ scan_fwd_kernel(const ScanParams p)
 #ifndef SS_NSPLIT_AHEAD
 #define SS_NSPLIT_AHEAD 4  // steps whose decays are formed ahead of the state update
 #endif
-#define SS_NSPLIT_STAGES 4  // raw chunks resident in shared memory: k .. k+3
+#ifndef SS_NSPLIT_STAGES
+#define SS_NSPLIT_STAGES 4  // raw chunks resident in shared memory: k .. k+3 (a power of two)
+#endif
 
 template <typename T, int S>
 struct NSplitShape {
@@ -288,7 +290,8 @@ scan_nsplit_kernel(const __grid_constant__ ScanParams p)
     constexpr int RW = RL * (int)sizeof(T) / 4;   // 32-bit words per prep/epilogue run
     static_assert(LC % 4 == 0 && D >= 1 && D <= LC, "chunk shape");
 
-    extern __shared__ __align__(128) unsigned char smem_raw[];
+    extern __shared__ __align__(128) unsigned char smem_tiles[];
+    unsigned char *smem_raw = smem_tiles;
     unsigned char *raw = smem_raw;                                          // [STAGES][x, dt, z, B, C]
     u64 *Pd = reinterpret_cast<u64 *>(smem_raw + STAGES * SH::STAGE_BYTES);  // [LC][CH] (delta, delta x)
     float *Bf = reinterpret_cast<float *>(Pd + LC * CH);                    // [LC][NS]
