@@ -151,6 +151,30 @@ def test_bwd_host_validation(lib, sfx):
     assert "workspace" in binding.last_error()
 
 
+@pytest.mark.parametrize("sfx", ["bf16", "f32"])
+def test_bwd_ex_host_validation(lib, sfx):
+    """The backward of the scan variants checks its arguments like the plain
+    one, before anything reaches a GPU."""
+    one = ctypes.c_void_p(1)
+    fn = getattr(lib, "ss_scan_bwd_ex_" + sfx)
+
+    def call(x=one, ws=one, ws_bytes=1 << 40, batch=2, d=4, L=16, N=16, dout=one, starts=None, reverse=1):
+        return fn(x, one, one, one, one, None, None, None, 1, None, starts, reverse, dout, None, one, one, one,
+                  one, one, None, None, None, None, ws, ws_bytes, batch, d, L, N, None)
+
+    assert call(batch=0) == -2
+    assert call(N=33, starts=one) == -3
+    assert call(x=None) == -1
+    assert call(dout=None, reverse=0, starts=one) == -1
+    assert "dout" in binding.last_error()
+    assert call(ws=None) == -1
+
+
+def test_device_faults_needs_an_output(lib):
+    assert lib.ss_device_faults(None, 0) == -1
+    assert "flags" in binding.last_error()
+
+
 def test_bwd_workspace_size(lib):
     ws = binding.scan_bwd_workspace_bytes
     # one 16-byte state group (4 states) per channel and batch row at every 16th step
