@@ -173,8 +173,8 @@ struct SsdShape {
     static constexpr int CB_OFF = C_OFF + Q * LDN * 2;               // CB_c  [Q][LDQ] bf16
     static constexpr int S_OFF = CB_OFF + Q * LDQ * 2;               // S'_c  [Q][LDQ] bf16
     static constexpr int XW_OFF = S_OFF + Q * LDQ * 2;               // w o X [Q][LDP] bf16
-    static constexpr int CUM_OFF = XW_OFF + Q * LDP * 2;             // cum, delta, e^cum [Q] fp32
-    static constexpr size_t BYTES = CUM_OFF + 3 * Q * 4;
+    static constexpr int CUM_OFF = XW_OFF + Q * LDP * 2;             // cum, delta, e^cum, e4, w [Q] fp32
+    static constexpr size_t BYTES = CUM_OFF + 5 * Q * 4;
 };
 
 // ---- one CTA (4 warps) per (batch, head); the chunks of the row in order.
@@ -196,6 +196,8 @@ ssd_chunk_kernel(const SsdParams p)
     float *cum = reinterpret_cast<float *>(smem_raw + SH::CUM_OFF);
     float *dl = cum + Q;
     float *ecum = dl + Q;
+    float *e4 = ecum + Q;    // e^{cum[t] - cum[t-4]} (t >= 4)
+    float *wsx = e4 + Q;     // w_s = e^{cum[Q-1] - cum[s]} delta_s
 
     const int64_t b = blockIdx.y;
     const int h = blockIdx.x;
@@ -261,9 +263,10 @@ ssd_chunk_kernel(const SsdParams p)
             dt_next = load_dt(c + 1);
         cp_async_wait<0>();
         __syncthreads();
-        // ---- cum[t] = A_h * (delta_0 + .. + delta_t), one warp
+        // ---- cum[t] = A_h * (delta_0 + .. + delta_t) in units of log2 e, one warp; with
+        // it e^{cum}, the 4-step decays e4 and the state-update weights w
         if (w == 0) {
-            const float a0 = Ah * dl[2 * lane], a1 = Ah * dl[2 * lane + 1];
+            const float a0 = Ah * kLog2e * dl[2 * lane], a1 = Ah * kLog2e * dl[2 * lane + 1];
             float sum = a0 + a1;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -271,28 +274,42 @@ ssd_chunk_kernel(const SsdParams p)
                 if (lane >= o)
                     sum += u;
             }
-            cum[2 * lane] = sum - a1;
-            cum[2 * lane + 1] = sum;
-            ecum[2 * lane] = ex2_approx((sum - a1) * kLog2e);
-            ecum[2 * lane + 1] = ex2_approx(sum * kLog2e);
+            const float c0 = sum - a1, c1 = sum;
+            cum[2 * lane] = c0;
+            cum[2 * lane + 1] = c1;
+            ecum[2 * lane] = ex2_approx(c0);
+            ecum[2 * lane + 1] = ex2_approx(c1);
+            const float cq = __shfl_sync(0xffffffffu, c1, 31);
+            wsx[2 * lane] = ex2_approx(cq - c0) * dl[2 * lane];
+            wsx[2 * lane + 1] = ex2_approx(cq - c1) * dl[2 * lane + 1];
+            const float q0 = __shfl_up_sync(0xffffffffu, c0, 2), q1 = __shfl_up_sync(0xffffffffu, c1, 2);
+            e4[2 * lane] = ex2_approx(c0 - q0);   // lanes 0, 1 (t < 4): unused
+            e4[2 * lane + 1] = ex2_approx(c1 - q1);
         }
         __syncthreads();
-        // ---- S' = CB o M o delta and w o X, both bf16
-        const float cq = cum[Q - 1];
-        for (int i = tid; i < Q * Q / 2; i += 128) {
-            const int t = i >> 5, s2 = (i & 31) * 2;   // Q / 2 = 32 pairs per row
-            const uint32_t cb2 = *reinterpret_cast<const uint32_t *>(CBs + t * LDQ + s2);
-            const float ct = cum[t];
-            float v0 = 0.0f, v1 = 0.0f;
-            if (s2 <= t)
-                v0 = bf16lo(cb2) * ex2_approx((ct - cum[s2]) * kLog2e) * dl[s2];
-            if (s2 + 1 <= t)
-                v1 = bf16hi(cb2) * ex2_approx((ct - cum[s2 + 1]) * kLog2e) * dl[s2 + 1];
-            *reinterpret_cast<uint32_t *>(Sp + t * LDQ + s2) = pack_bf16x2(v0, v1);
+        // ---- S' = CB o M o delta and w o X, both bf16. A thread owns columns s2, s2 + 1
+        // and the rows t = t0 + 4k: M[t][s] delta_s starts at the first such row on or
+        // below the diagonal and is carried down with M[t][s] = M[t-4][s] e4[t].
+        {
+            const int s2 = 2 * (tid & 31), t0 = tid >> 5;
+            const int tf0 = s2 + ((t0 - s2) & 3), tf1 = s2 + 1 + ((t0 - s2 - 1) & 3);
+            float m0 = tf0 < Q ? ex2_approx(cum[tf0] - cum[s2]) * dl[s2] : 0.0f;
+            float m1 = tf1 < Q ? ex2_approx(cum[tf1] - cum[s2 + 1]) * dl[s2 + 1] : 0.0f;
+#pragma unroll 4
+            for (int k = 0; k < Q / 4; ++k) {
+                const int t = t0 + 4 * k;
+                const uint32_t cb2 = *reinterpret_cast<const uint32_t *>(CBs + t * LDQ + s2);
+                const float f = e4[t];
+                m0 = t > tf0 ? m0 * f : m0;
+                m1 = t > tf1 ? m1 * f : m1;
+                const float v0 = t >= tf0 ? bf16lo(cb2) * m0 : 0.0f;
+                const float v1 = t >= tf1 ? bf16hi(cb2) * m1 : 0.0f;
+                *reinterpret_cast<uint32_t *>(Sp + t * LDQ + s2) = pack_bf16x2(v0, v1);
+            }
         }
         for (int i = tid; i < Q * P / 2; i += 128) {
             const int s_ = i >> 5, p2 = (i & 31) * 2;  // P / 2 = 32 pairs per row
-            const float ws = ex2_approx((cq - cum[s_]) * kLog2e) * dl[s_];
+            const float ws = wsx[s_];
             const uint32_t xw = *reinterpret_cast<const uint32_t *>(Xs + s_ * LDP + p2);
             *reinterpret_cast<uint32_t *>(Xw + s_ * LDP + p2) = pack_bf16x2(bf16lo(xw) * ws, bf16hi(xw) * ws);
         }
