@@ -307,11 +307,16 @@ ssd_chunk_kernel(const SsdParams p)
                 *reinterpret_cast<uint32_t *>(Sp + t * LDQ + s2) = pack_bf16x2(v0, v1);
             }
         }
-        for (int i = tid; i < Q * P / 2; i += 128) {
-            const int s_ = i >> 5, p2 = (i & 31) * 2;  // P / 2 = 32 pairs per row
+        for (int i = tid; i < Q * P / 8; i += 128) {
+            const int s_ = i >> 3, p8 = (i & 7) * 8;   // P / 8 = 8 16-byte pieces per row
             const float ws = wsx[s_];
-            const uint32_t xw = *reinterpret_cast<const uint32_t *>(Xs + s_ * LDP + p2);
-            *reinterpret_cast<uint32_t *>(Xw + s_ * LDP + p2) = pack_bf16x2(bf16lo(xw) * ws, bf16hi(xw) * ws);
+            const uint4 xw = *reinterpret_cast<const uint4 *>(Xs + s_ * LDP + p8);
+            uint4 o;
+            o.x = pack_bf16x2(bf16lo(xw.x) * ws, bf16hi(xw.x) * ws);
+            o.y = pack_bf16x2(bf16lo(xw.y) * ws, bf16hi(xw.y) * ws);
+            o.z = pack_bf16x2(bf16lo(xw.z) * ws, bf16hi(xw.z) * ws);
+            o.w = pack_bf16x2(bf16lo(xw.w) * ws, bf16hi(xw.w) * ws);
+            *reinterpret_cast<uint4 *>(Xw + s_ * LDP + p8) = o;
         }
         __syncthreads();
 
