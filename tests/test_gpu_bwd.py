@@ -108,6 +108,16 @@ def test_bwd_headline_layer_full():
     run_case(I.MAMBA130M)
 
 
+def test_bwd_variant_headline_layer_full():
+    """The variant the benchmark times: the backward of the reverse-direction
+    scan with a sequence start every 250 steps on the headline layer shape,
+    every gradient element against the oracle."""
+    spec = I.MAMBA130M
+    st = torch.zeros(spec.batch, spec.L, dtype=torch.uint8)
+    st[:, ::250] = 1
+    run_case(spec, seq_start=st, reverse=True)
+
+
 def test_bwd_workspace_too_small_is_rejected():
     spec = I.ScanSpec(1, 8, 64, 16, io="f32", seed=1)
     inp = I.make_scan_inputs(spec)
@@ -135,7 +145,7 @@ def test_bwd_repeat_is_stable():
         torch.testing.assert_close(outs[0][k], outs[1][k], rtol=1e-5, atol=1e-5)
 
 
-@pytest.mark.parametrize("shape", [(2, 64, 300, 16), (1, 64, 8192, 16), (2, 33, 47, 8)],
+@pytest.mark.parametrize("shape", [(2, 64, 300, 16), (1, 64, 8192, 16), (2, 33, 47, 8), (8, 1536, 2048, 16)],
                          ids=lambda s: "b%d_d%d_l%d_n%d" % s)
 def test_bwd_with_states_stored_by_the_training_forward(shape):
     """The training forward stores the state at every 16th step (also when it
