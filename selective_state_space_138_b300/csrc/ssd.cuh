@@ -36,6 +36,11 @@ struct SsdParams {
     __nv_bfloat16 *cb;   // workspace: [batch][nchunks][G][Q][Q] bf16
     int64_t batch, L, H, G, nchunks;
     int softplus;
+    int tma;   // the chunk kernel's X, B, C and C B^T tiles come in through the tensor maps below
+    // 3-d maps: x over (H*P channels, L, batch) with a box of one head's P + 8 channels x Q steps;
+    // B, C over (G*N, L, batch) with a box of N + 8 x Q; C B^T over (Q, Q, batch*nchunks*G) with
+    // a box of Q + 8 x Q. The 8 extra columns fill each shared-memory row's pad (never read).
+    CUtensorMap tm_x, tm_B, tm_C, tm_cb;
 };
 
 // ---- warp-level MMA helpers (PTX mma.sync / ldmatrix; operands in shared memory)
@@ -174,19 +179,23 @@ struct SsdShape {
     static constexpr int S_OFF = CB_OFF + Q * LDQ * 2;               // S'_c  [Q][LDQ] bf16
     static constexpr int XW_OFF = S_OFF + Q * LDQ * 2;               // w o X [Q][LDP] bf16
     static constexpr int CUM_OFF = XW_OFF + Q * LDP * 2;             // cum, delta, e^cum, e4, w [Q] fp32
-    static constexpr size_t BYTES = CUM_OFF + 5 * Q * 4;
+    static constexpr int BAR_OFF = CUM_OFF + 5 * Q * 4;              // "C, CB landed", "X, B landed"
+    static constexpr size_t BYTES = BAR_OFF + 16;
+    static_assert(B_OFF % 128 == 0 && C_OFF % 128 == 0 && CB_OFF % 128 == 0 && BAR_OFF % 8 == 0,
+                  "tensor-copy destinations on 128-byte boundaries");
 };
 
 // ---- one CTA (4 warps) per (batch, head); the chunks of the row in order.
 // Warp w owns channels p = 16w .. 16w+15: those rows of H and those columns of Y_c.
 template <int N>
 __global__ void __launch_bounds__(128, 3)
-ssd_chunk_kernel(const SsdParams p)
+ssd_chunk_kernel(const __grid_constant__ SsdParams p)
 {
     using SH = SsdShape<N>;
     constexpr int Q = SH::Q, P = SH::P, LDP = SH::LDP, LDN = SH::LDN, LDQ = SH::LDQ;
     constexpr int NT = N / 8;   // 8-column tiles of the state
-    extern __shared__ __align__(16) unsigned char smem_raw[];
+    extern __shared__ __align__(128) unsigned char smem_ssd[];
+    unsigned char *smem_raw = smem_ssd;
     __nv_bfloat16 *Xs = reinterpret_cast<__nv_bfloat16 *>(smem_raw + SH::X_OFF);
     __nv_bfloat16 *Bs = reinterpret_cast<__nv_bfloat16 *>(smem_raw + SH::B_OFF);
     __nv_bfloat16 *Cs = reinterpret_cast<__nv_bfloat16 *>(smem_raw + SH::C_OFF);
@@ -225,21 +234,70 @@ ssd_chunk_kernel(const SsdParams p)
     }
     bool have_state = p.h0 != nullptr;
 
+    // Tiles arrive by tensor copies when the maps are given (and shared memory
+    // starts on a 128-byte boundary), else by 16-byte cp.async pieces. Each of
+    // the two barriers completes once per chunk (phase parity c & 1); waits are
+    // bounded, and after one gives up the CTA issues and waits no more and
+    // thread 0 lets the copies it issued land before exiting.
+    const uint32_t smem_s = static_cast<uint32_t>(__cvta_generic_to_shared(smem_raw));
+    const bool tma = p.tma && (smem_s & 127u) == 0;
+    const uint32_t bar_cc = smem_s + SH::BAR_OFF, bar_xb = bar_cc + 8;
+    int64_t cc_issued = 0, cc_done = 0, xb_issued = 0, xb_done = 0;
+    bool aborted = false;
+    if (tma) {
+        if (tid == 0) {
+            mbar_init(bar_cc, 1);
+            mbar_init(bar_xb, 1);
+            mbar_fence_init();
+        }
+        __syncthreads();
+    }
+
     // C_c and C_c B_c^T of chunk c (issued early: their buffers free up first)
     auto stage_c = [&](int64_t c) {
         const int64_t t0 = c * Q;
+        if (tma) {
+            if (tid == 0 && !aborted) {
+                mbar_expect_tx(bar_cc, 2 * Q * LDN + 2 * Q * LDQ);
+                tma_load_3d(smem_s + SH::C_OFF, &p.tm_C, bar_cc, g * N, static_cast<int>(t0), static_cast<int>(b));
+                tma_load_3d(smem_s + SH::CB_OFF, &p.tm_cb, bar_cc, 0, 0,
+                            static_cast<int>((b * p.nchunks + c) * p.G + g));
+                cc_issued = c + 1;
+            }
+            return;
+        }
         const int valid = static_cast<int>(p.L - t0 < Q ? p.L - t0 : Q);
         stage_rows(Cs, LDN, p.C + ((b * p.L + t0) * p.G + g) * N, bcs, Q, N, valid, tid, 128);
         stage_rows(CBs, LDQ, p.cb + (((b * p.nchunks + c) * p.G + g) * Q) * Q, Q, Q, Q, Q, tid, 128);
         cp_async_commit();
     };
-    stage_c(0);
-    {
-        const int v0 = static_cast<int>(p.L < Q ? p.L : Q);
-        stage_rows(Xs, LDP, p.x + (b * p.L * p.H + h) * P, xs, Q, P, v0, tid, 128);
-        stage_rows(Bs, LDN, p.B + (b * p.L * p.G + g) * N, bcs, Q, N, v0, tid, 128);
+    // X_c and B_c
+    auto stage_xb = [&](int64_t c) {
+        const int64_t t0 = c * Q;
+        if (tma) {
+            if (tid == 0 && !aborted) {
+                mbar_expect_tx(bar_xb, 2 * Q * LDP + 2 * Q * LDN);
+                tma_load_3d(smem_s + SH::X_OFF, &p.tm_x, bar_xb, h * P, static_cast<int>(t0), static_cast<int>(b));
+                tma_load_3d(smem_s + SH::B_OFF, &p.tm_B, bar_xb, g * N, static_cast<int>(t0), static_cast<int>(b));
+                xb_issued = c + 1;
+            }
+            return;
+        }
+        const int v = static_cast<int>(p.L - t0 < Q ? p.L - t0 : Q);
+        stage_rows(Xs, LDP, p.x + ((b * p.L + t0) * p.H + h) * P, xs, Q, P, v, tid, 128);
+        stage_rows(Bs, LDN, p.B + ((b * p.L + t0) * p.G + g) * N, bcs, Q, N, v, tid, 128);
         cp_async_commit();
-    }
+    };
+    auto wait_chunk = [&](int64_t c) {
+        if (tma && !aborted) {
+            const uint32_t par = static_cast<uint32_t>(c & 1);
+            aborted = !mbar_wait(bar_cc, par) || !mbar_wait(bar_xb, par);
+            if (!aborted)
+                cc_done = xb_done = c + 1;
+        }
+    };
+    stage_c(0);
+    stage_xb(0);
     // raw step of this thread's row of the next chunk, fetched a chunk ahead
     auto load_dt = [&](int64_t c) -> float {
         const int64_t t = c * Q + tid;
@@ -262,6 +320,7 @@ ssd_chunk_kernel(const SsdParams p)
         if (c + 1 < p.nchunks)
             dt_next = load_dt(c + 1);
         cp_async_wait<0>();
+        wait_chunk(c);
         __syncthreads();
         // ---- cum[t] = A_h * (delta_0 + .. + delta_t) in units of log2 e, one warp; with
         // it e^{cum}, the 4-step decays e4 and the state-update weights w
@@ -423,13 +482,8 @@ ssd_chunk_kernel(const SsdParams p)
         have_state = true;
         __syncthreads();   // every warp is done with Xs, Bs, Sp, Xw and the step sizes of this chunk
         // the next chunk's X and B land while this one's outputs are written
-        if (c + 1 < p.nchunks) {
-            const int64_t t1 = (c + 1) * Q;
-            const int v1 = static_cast<int>(p.L - t1 < Q ? p.L - t1 : Q);
-            stage_rows(Xs, LDP, p.x + ((b * p.L + t1) * p.H + h) * P, xs, Q, P, v1, tid, 128);
-            stage_rows(Bs, LDN, p.B + ((b * p.L + t1) * p.G + g) * N, bcs, Q, N, v1, tid, 128);
-            cp_async_commit();
-        }
+        if (c + 1 < p.nchunks)
+            stage_xb(c + 1);
         // ---- epilogue: + D x, gate, store
 #pragma unroll
         for (int mt = 0; mt < 4; ++mt) {
@@ -466,6 +520,12 @@ ssd_chunk_kernel(const SsdParams p)
             *reinterpret_cast<float2 *>(fs + (16 * w + gr + 8) * N + n) = make_float2(Hf[j][2], Hf[j][3]);
         }
     }
+    if (tma && tid == 0) {   // after a wait gave up: let the copies issued since land (each wait bounded)
+        for (int64_t c = cc_done; c < cc_issued; ++c)
+            mbar_wait(bar_cc, static_cast<uint32_t>(c & 1));
+        for (int64_t c = xb_done; c < xb_issued; ++c)
+            mbar_wait(bar_xb, static_cast<uint32_t>(c & 1));
+    }
 }
 
 // ------------------------------------------------------------------ SSD host side
@@ -476,6 +536,39 @@ size_t ssd_workspace_bytes(int64_t batch, int64_t L, int64_t G)
         return 0;
     const int64_t nchunks = (L + kSsdQ - 1) / kSsdQ;
     return static_cast<size_t>(batch) * nchunks * G * kSsdQ * kSsdQ * 2;
+}
+
+// 3-d bf16 tensor map (d0 contiguous, then d1, d2; strides in bytes) with box
+// (b0, b1, 1); elements outside the tensor read as zero
+bool ssd_encode_3d(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1,
+                   uint64_t s2, uint32_t b0, uint32_t b1)
+{
+    const EncodeTiledFn fn = encode_tiled_fn();
+    if (!fn)
+        return false;
+    const cuuint64_t dims[3] = {d0, d1, d2};
+    const cuuint64_t strides[2] = {s1, s2};
+    const cuuint32_t box[3] = {b0, b1, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The chunk kernel's tile maps (SS_SCAN_TMA=0 keeps the cp.async pieces).
+bool ssd_encode_maps(SsdParams &p, int64_t N)
+{
+    const char *env = getenv("SS_SCAN_TMA");
+    if (env && strcmp(env, "0") == 0)
+        return false;
+    constexpr int Q = kSsdQ, P = kSsdP;
+    const uint64_t HP = static_cast<uint64_t>(p.H) * P, GN = static_cast<uint64_t>(p.G) * N;
+    const uint64_t L = static_cast<uint64_t>(p.L), bt = static_cast<uint64_t>(p.batch);
+    return ssd_encode_3d(&p.tm_x, p.x, HP, L, bt, HP * 2, HP * L * 2, P + 8, Q) &&
+           ssd_encode_3d(&p.tm_B, p.B, GN, L, bt, GN * 2, GN * L * 2, static_cast<uint32_t>(N + 8), Q) &&
+           ssd_encode_3d(&p.tm_C, p.C, GN, L, bt, GN * 2, GN * L * 2, static_cast<uint32_t>(N + 8), Q) &&
+           ssd_encode_3d(&p.tm_cb, p.cb, Q, Q, bt * static_cast<uint64_t>(p.nchunks) * static_cast<uint64_t>(p.G),
+                         Q * 2, Q * Q * 2, Q + 8, Q);
 }
 
 template <int N>
@@ -541,7 +634,7 @@ ss_status ssd_fwd(const void *x, const void *dt, const float *A, const void *B, 
         return fail(SS_ERR_DIM, "B and C rows must be whole 16-byte pieces");
     if (nheads * headdim > 0x7fffffff || ngroups * N > 0x7fffffff)
         return fail(SS_ERR_DIM, "nheads * headdim and ngroups * N must fit in 31 bits");
-    SsdParams p;
+    SsdParams p{};
     p.x = static_cast<const __nv_bfloat16 *>(x);
     p.dt = static_cast<const __nv_bfloat16 *>(dt);
     p.B = static_cast<const __nv_bfloat16 *>(B);
@@ -554,5 +647,6 @@ ss_status ssd_fwd(const void *x, const void *dt, const float *A, const void *B, 
     p.batch = batch; p.L = L; p.H = nheads; p.G = ngroups;
     p.nchunks = (L + kSsdQ - 1) / kSsdQ;
     p.softplus = softplus ? 1 : 0;
+    p.tma = ssd_encode_maps(p, N) ? 1 : 0;
     return N == 64 ? launch_ssd<64>(p, stream) : launch_ssd<128>(p, stream);
 }
