@@ -187,7 +187,12 @@ struct SsdShape {
 
 // ---- one CTA (4 warps) per (batch, head); the chunks of the row in order.
 // Warp w owns channels p = 16w .. 16w+15: those rows of H and those columns of Y_c.
-template <int N>
+constexpr unsigned int kFaultSsdSmemAlign = 2u;   // SS_FAULT_SMEM_ALIGN
+
+// TMA: the tiles arrive by tensor copies (the maps in p are encoded); the
+// cp.async form is a separate instantiation, so neither carries the other's
+// registers.
+template <int N, bool TMA>
 __global__ void __launch_bounds__(128, 3)
 ssd_chunk_kernel(const __grid_constant__ SsdParams p)
 {
@@ -240,9 +245,14 @@ ssd_chunk_kernel(const __grid_constant__ SsdParams p)
     // bounded, and after one gives up the CTA issues and waits no more and
     // thread 0 lets the copies it issued land before exiting.
     const uint32_t smem_s = static_cast<uint32_t>(__cvta_generic_to_shared(smem_raw));
-    const bool tma = p.tma && (smem_s & 127u) == 0;
+    constexpr bool tma = TMA;
+    if (TMA && (smem_s & 127u) != 0) {   // tensor copies need 128-byte aligned destinations
+        if (tid == 0)
+            atomicOr(&g_fault_flags, kFaultSsdSmemAlign);
+        return;
+    }
     const uint32_t bar_cc = smem_s + SH::BAR_OFF, bar_xb = bar_cc + 8;
-    int64_t cc_issued = 0, cc_done = 0, xb_issued = 0, xb_done = 0;
+    int cc_issued = 0, cc_done = 0, xb_issued = 0, xb_done = 0;   // chunk counts (< 2^31)
     bool aborted = false;
     if (tma) {
         if (tid == 0) {
@@ -256,44 +266,44 @@ ssd_chunk_kernel(const __grid_constant__ SsdParams p)
     // C_c and C_c B_c^T of chunk c (issued early: their buffers free up first)
     auto stage_c = [&](int64_t c) {
         const int64_t t0 = c * Q;
-        if (tma) {
+        if constexpr (TMA) {
             if (tid == 0 && !aborted) {
                 mbar_expect_tx(bar_cc, 2 * Q * LDN + 2 * Q * LDQ);
                 tma_load_3d(smem_s + SH::C_OFF, &p.tm_C, bar_cc, g * N, static_cast<int>(t0), static_cast<int>(b));
                 tma_load_3d(smem_s + SH::CB_OFF, &p.tm_cb, bar_cc, 0, 0,
                             static_cast<int>((b * p.nchunks + c) * p.G + g));
-                cc_issued = c + 1;
+                cc_issued = static_cast<int>(c) + 1;
             }
-            return;
+        } else {
+            const int valid = static_cast<int>(p.L - t0 < Q ? p.L - t0 : Q);
+            stage_rows(Cs, LDN, p.C + ((b * p.L + t0) * p.G + g) * N, bcs, Q, N, valid, tid, 128);
+            stage_rows(CBs, LDQ, p.cb + (((b * p.nchunks + c) * p.G + g) * Q) * Q, Q, Q, Q, Q, tid, 128);
+            cp_async_commit();
         }
-        const int valid = static_cast<int>(p.L - t0 < Q ? p.L - t0 : Q);
-        stage_rows(Cs, LDN, p.C + ((b * p.L + t0) * p.G + g) * N, bcs, Q, N, valid, tid, 128);
-        stage_rows(CBs, LDQ, p.cb + (((b * p.nchunks + c) * p.G + g) * Q) * Q, Q, Q, Q, Q, tid, 128);
-        cp_async_commit();
     };
     // X_c and B_c
     auto stage_xb = [&](int64_t c) {
         const int64_t t0 = c * Q;
-        if (tma) {
+        if constexpr (TMA) {
             if (tid == 0 && !aborted) {
                 mbar_expect_tx(bar_xb, 2 * Q * LDP + 2 * Q * LDN);
                 tma_load_3d(smem_s + SH::X_OFF, &p.tm_x, bar_xb, h * P, static_cast<int>(t0), static_cast<int>(b));
                 tma_load_3d(smem_s + SH::B_OFF, &p.tm_B, bar_xb, g * N, static_cast<int>(t0), static_cast<int>(b));
-                xb_issued = c + 1;
+                xb_issued = static_cast<int>(c) + 1;
             }
-            return;
+        } else {
+            const int v = static_cast<int>(p.L - t0 < Q ? p.L - t0 : Q);
+            stage_rows(Xs, LDP, p.x + ((b * p.L + t0) * p.H + h) * P, xs, Q, P, v, tid, 128);
+            stage_rows(Bs, LDN, p.B + ((b * p.L + t0) * p.G + g) * N, bcs, Q, N, v, tid, 128);
+            cp_async_commit();
         }
-        const int v = static_cast<int>(p.L - t0 < Q ? p.L - t0 : Q);
-        stage_rows(Xs, LDP, p.x + ((b * p.L + t0) * p.H + h) * P, xs, Q, P, v, tid, 128);
-        stage_rows(Bs, LDN, p.B + ((b * p.L + t0) * p.G + g) * N, bcs, Q, N, v, tid, 128);
-        cp_async_commit();
     };
     auto wait_chunk = [&](int64_t c) {
         if (tma && !aborted) {
             const uint32_t par = static_cast<uint32_t>(c & 1);
             aborted = !mbar_wait(bar_cc, par) || !mbar_wait(bar_xb, par);
             if (!aborted)
-                cc_done = xb_done = c + 1;
+                cc_done = xb_done = static_cast<int>(c) + 1;
         }
     };
     stage_c(0);
@@ -521,9 +531,9 @@ ssd_chunk_kernel(const __grid_constant__ SsdParams p)
         }
     }
     if (tma && tid == 0) {   // after a wait gave up: let the copies issued since land (each wait bounded)
-        for (int64_t c = cc_done; c < cc_issued; ++c)
+        for (int c = cc_done; c < cc_issued; ++c)
             mbar_wait(bar_cc, static_cast<uint32_t>(c & 1));
-        for (int64_t c = xb_done; c < xb_issued; ++c)
+        for (int c = xb_done; c < xb_issued; ++c)
             mbar_wait(bar_xb, static_cast<uint32_t>(c & 1));
     }
 }
@@ -582,7 +592,7 @@ ss_status launch_ssd(const SsdParams &p, cudaStream_t stream)
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
         return fail(SS_ERR_LAUNCH, "SSD CB kernel launch failed: %s", cudaGetErrorString(e));
-    auto kernel = ssd_chunk_kernel<N>;
+    auto kernel = p.tma ? ssd_chunk_kernel<N, true> : ssd_chunk_kernel<N, false>;
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(SH::BYTES));
     if (e != cudaSuccess) {
         cudaGetLastError();
