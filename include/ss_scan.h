@@ -414,9 +414,10 @@ ss_status ss_ssd_fwd_bf16(const ss_bf16 *x, const ss_bf16 *dt, const float *A, c
  *   clear  non-zero: reset the recorded faults to none
  * Errors: SS_ERR_NULL (flags NULL), SS_ERR_INTERNAL (the read failed). */
 #define SS_FAULT_WAIT_TIMEOUT 1u
-/* SS_FAULT_SMEM_ALIGN: the scalar-decay (SSD) chunk kernel found its shared
- * memory off the 128-byte boundary its tensor copies need and returned without
- * writing its outputs. */
+/* SS_FAULT_SMEM_ALIGN: a kernel that stages its tiles by tensor copies (the
+ * forward scan of rows that are 16-byte aligned, the SSD chunk kernel) found
+ * its shared memory off the 128-byte boundary the copies need and returned
+ * without writing its outputs. */
 #define SS_FAULT_SMEM_ALIGN 2u
 ss_status ss_device_faults(unsigned int *flags, int clear);
 

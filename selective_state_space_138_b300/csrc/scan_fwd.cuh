@@ -279,7 +279,14 @@ struct NSplitShape {
 // tiles themselves are the same. RST: p.reset marks sequence starts; the
 // carried state is zeroed before a marked step (forward) or after it
 // (reverse), i.e. at the boundary between t-1 and t either way.
-template <typename T, int S, bool REV, bool RST>
+// A kernel that stages its tiles by tensor copies found its dynamic shared
+// memory off the 128-byte boundary the copies need (SS_FAULT_SMEM_ALIGN).
+constexpr unsigned int kFaultSmemAlign = 2u;
+
+// TMA: the chunks arrive by tensor copies (the maps in p are encoded); the
+// cp.async form is a separate instantiation, so neither carries the other's
+// registers.
+template <typename T, int S, bool REV, bool RST, bool TMA>
 __global__ void __launch_bounds__(NSplitShape<T, S>::NT, NSplitShape<T, S>::NT <= 128 ? 3 : 1)
 scan_nsplit_kernel(const __grid_constant__ ScanParams p)
 {
@@ -303,9 +310,12 @@ scan_nsplit_kernel(const __grid_constant__ ScanParams p)
     int *Rx = reinterpret_cast<int *>(Rst + LC);                            // any start in the segment
     const uint32_t raw_s = static_cast<uint32_t>(__cvta_generic_to_shared(raw));
     const uint32_t bars_s = raw_s + static_cast<uint32_t>(SH::BAR_OFF);   // [STAGES] "stage filled" barriers
-    // tensor copies need 128-byte aligned destinations: should the dynamic
-    // shared memory not start on one, the tiles are staged in pieces instead
-    const bool tma = p.tma && (raw_s & 127u) == 0;
+    constexpr bool tma = TMA;
+    if (TMA && (raw_s & 127u) != 0) {   // tensor copies need 128-byte aligned destinations
+        if (threadIdx.x == 0)
+            atomicOr(&g_fault_flags, kFaultSmemAlign);
+        return;
+    }
 
     const int tid = threadIdx.x;
     const int nseg = p.nseg;
@@ -889,7 +899,7 @@ template <typename T, int S, bool REV, bool RST>
 ss_status launch_nsplit(const ScanParams &p0, cudaStream_t stream, int sms)
 {
     using SH = NSplitShape<T, S>;
-    auto kernel = scan_nsplit_kernel<T, S, REV, RST>;
+    auto kernel = p0.tma ? scan_nsplit_kernel<T, S, REV, RST, true> : scan_nsplit_kernel<T, S, REV, RST, false>;
     const size_t smem = SH::BYTES;
     if (smem > 48u * 1024u) {
         cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

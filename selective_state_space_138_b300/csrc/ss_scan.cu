@@ -255,7 +255,7 @@ ss_status ss_device_faults(unsigned int *flags, int clear)
     g_err[0] = '\0';
     if (!flags)
         return fail(SS_ERR_NULL, "flags is NULL");
-    static_assert(SS_FAULT_WAIT_TIMEOUT == kFaultWaitTimeout && SS_FAULT_SMEM_ALIGN == kFaultSsdSmemAlign,
+    static_assert(SS_FAULT_WAIT_TIMEOUT == kFaultWaitTimeout && SS_FAULT_SMEM_ALIGN == kFaultSmemAlign,
                   "fault bits agree");
     unsigned int v = 0;
     cudaError_t e = cudaMemcpyFromSymbol(&v, g_fault_flags, sizeof(v));

@@ -187,8 +187,6 @@ struct SsdShape {
 
 // ---- one CTA (4 warps) per (batch, head); the chunks of the row in order.
 // Warp w owns channels p = 16w .. 16w+15: those rows of H and those columns of Y_c.
-constexpr unsigned int kFaultSsdSmemAlign = 2u;   // SS_FAULT_SMEM_ALIGN
-
 // TMA: the tiles arrive by tensor copies (the maps in p are encoded); the
 // cp.async form is a separate instantiation, so neither carries the other's
 // registers.
@@ -248,7 +246,7 @@ ssd_chunk_kernel(const __grid_constant__ SsdParams p)
     constexpr bool tma = TMA;
     if (TMA && (smem_s & 127u) != 0) {   // tensor copies need 128-byte aligned destinations
         if (tid == 0)
-            atomicOr(&g_fault_flags, kFaultSsdSmemAlign);
+            atomicOr(&g_fault_flags, kFaultSmemAlign);
         return;
     }
     const uint32_t bar_cc = smem_s + SH::BAR_OFF, bar_xb = bar_cc + 8;
