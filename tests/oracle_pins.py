@@ -455,6 +455,35 @@ def check_reverse_is_forward_on_flipped_inputs(lib):
     np.testing.assert_array_equal(fs0, fs1)
 
 
+def check_reverse_gradient_is_forward_gradient_on_flipped_inputs(lib):
+    """The gradient of the reverse walk equals the gradient of the forward walk
+    of the time-flipped inputs, flipped back: per-step gradients (dx, ddt, dz,
+    dB, dC) flipped in time, the rest (dA, dD, ddt_bias, dh0) equal. Starts
+    move with the flip: a cut after reverse step t (start at t) is a cut before
+    forward step L - t of the flipped row, so r'[j] = r[L - j] (no start at
+    t = 0, which would zero the reverse walk's final state)."""
+    rng = np.random.default_rng(53)
+    L = 13
+    p = _bwd_problem(rng, L=L)
+    f = lambda a: np.ascontiguousarray(a[..., ::-1])
+    dout = rng.normal(size=p["x"].shape)
+    dfin = rng.normal(size=p["h0"].shape)
+    st = np.zeros((2, L), dtype=np.uint8)
+    st[0, [3, 7]] = 1
+    st[1, [1, 12]] = 1
+    st_f = np.zeros_like(st)
+    st_f[:, 1:] = st[:, :0:-1]   # r'[j] = r[L - j], j >= 1
+    for starts, starts_f in ((None, None), (st, st_f)):
+        g_r = O.scan_bwd(p["x"], p["dt"], p["A"], p["B"], p["C"], dout, D=p["D"], z=p["z"], dt_bias=p["dt_bias"],
+                         h0=p["h0"], dfinal=dfin, seq_start=starts, reverse=True, threads=1, lib=lib)
+        g_f = O.scan_bwd(f(p["x"]), f(p["dt"]), p["A"], f(p["B"]), f(p["C"]), f(dout), D=p["D"], z=f(p["z"]),
+                         dt_bias=p["dt_bias"], h0=p["h0"], dfinal=dfin, seq_start=starts_f, threads=1, lib=lib)
+        for k in ("dx", "ddt", "dz", "dB", "dC"):
+            np.testing.assert_allclose(g_r[k], f(g_f[k]), rtol=1e-12, atol=1e-13, err_msg=k)
+        for k in ("dA", "dD", "ddt_bias", "dh0"):
+            np.testing.assert_allclose(g_r[k], g_f[k], rtol=1e-12, atol=1e-13, err_msg=k)
+
+
 def check_sequence_starts_are_separate_sequences(lib):
     """Packed sequences with their starts marked give, in either direction,
     what scanning each sequence on its own from a zero state gives (the
@@ -557,5 +586,6 @@ ALL_CHECKS = [check_recurrence_example, check_softplus_values, check_gate_theore
               check_conv_impulse_and_silu, check_conv_constant_input_and_zero_history, check_conv_history_chain,
               check_bwd_finite_differences, check_bwd_variants_finite_differences,
               check_bwd_impulse_closed_form, check_bwd_linear_in_cotangent,
-              check_reverse_is_forward_on_flipped_inputs, check_sequence_starts_are_separate_sequences,
+              check_reverse_is_forward_on_flipped_inputs, check_reverse_gradient_is_forward_gradient_on_flipped_inputs,
+              check_sequence_starts_are_separate_sequences,
               check_ssd_is_the_scan_with_one_decay_per_head, check_ssd_masked_matmul_form]
