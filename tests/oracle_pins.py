@@ -484,6 +484,37 @@ def check_reverse_gradient_is_forward_gradient_on_flipped_inputs(lib):
             np.testing.assert_allclose(g_r[k], g_f[k], rtol=1e-12, atol=1e-13, err_msg=k)
 
 
+def check_packed_gradient_is_per_sequence_gradients(lib):
+    """The gradient of a row of packed sequences (starts marked) is each
+    sequence's own gradient: per-step gradients side by side, per-channel sums
+    (dA, dD, ddt_bias) added; the initial state and its gradient belong to the
+    first sequence, the final-state gradient to the last."""
+    rng = np.random.default_rng(54)
+    L = 17
+    p = _bwd_problem(rng, bt=1, L=L)
+    dout = rng.normal(size=p["x"].shape)
+    dfin = rng.normal(size=p["h0"].shape)
+    st = np.zeros((1, L), dtype=np.uint8)
+    st[0, [5, 11]] = 1
+    g = O.scan_bwd(p["x"], p["dt"], p["A"], p["B"], p["C"], dout, D=p["D"], z=p["z"], dt_bias=p["dt_bias"],
+                   h0=p["h0"], dfinal=dfin, seq_start=st, threads=1, lib=lib)
+    segs = [(0, 5), (5, 11), (11, L)]
+    acc = {k: 0.0 for k in ("dA", "dD", "ddt_bias")}
+    for i, (a, b) in enumerate(segs):
+        sl = lambda arr: np.ascontiguousarray(arr[..., a:b])
+        gs = O.scan_bwd(sl(p["x"]), sl(p["dt"]), p["A"], sl(p["B"]), sl(p["C"]), sl(dout), D=p["D"], z=sl(p["z"]),
+                        dt_bias=p["dt_bias"], h0=p["h0"] if i == 0 else None,
+                        dfinal=dfin if i == len(segs) - 1 else None, threads=1, lib=lib)
+        for k in ("dx", "ddt", "dz", "dB", "dC"):
+            np.testing.assert_allclose(g[k][..., a:b], gs[k], rtol=1e-12, atol=1e-13, err_msg="%s %d" % (k, i))
+        for k in acc:
+            acc[k] = acc[k] + gs[k]
+        if i == 0:
+            np.testing.assert_allclose(g["dh0"], gs["dh0"], rtol=1e-12, atol=1e-13)
+    for k, v in acc.items():
+        np.testing.assert_allclose(g[k], v, rtol=1e-12, atol=1e-13, err_msg=k)
+
+
 def check_sequence_starts_are_separate_sequences(lib):
     """Packed sequences with their starts marked give, in either direction,
     what scanning each sequence on its own from a zero state gives (the
@@ -587,5 +618,5 @@ ALL_CHECKS = [check_recurrence_example, check_softplus_values, check_gate_theore
               check_bwd_finite_differences, check_bwd_variants_finite_differences,
               check_bwd_impulse_closed_form, check_bwd_linear_in_cotangent,
               check_reverse_is_forward_on_flipped_inputs, check_reverse_gradient_is_forward_gradient_on_flipped_inputs,
-              check_sequence_starts_are_separate_sequences,
+              check_sequence_starts_are_separate_sequences, check_packed_gradient_is_per_sequence_gradients,
               check_ssd_is_the_scan_with_one_decay_per_head, check_ssd_masked_matmul_form]
