@@ -48,6 +48,10 @@ struct BwdParams {
     int vec4;   // dB, dC rows take 16-byte atomic adds (L % 4 == 0, aligned)
     int states_ready;   // the workspace already holds the stored states (written by the forward pass)
     const uint8_t *reset;   // (batch, L) sequence starts (RST kernels only)
+    int tma;                // the tiles come in through the tensor maps below
+    // 3-d maps over (step, row, batch row) as in the forward scan: x, dt, z,
+    // dout by channel rows, B, C by state rows
+    CUtensorMap tm_x, tm_dt, tm_z, tm_dout, tm_B, tm_C;
 };
 
 #define SS_BWD_STAGES 2
@@ -77,8 +81,11 @@ struct BwdShape {
     static constexpr int PART_BYTES = 3 * S * HC * CH * 4;
     static constexpr int DBC_BYTES = 2 * LC * NS * 4;
     static constexpr int R_BYTES = LC;                          // sequence starts of a chunk
-    static constexpr size_t BYTES = (size_t)STAGES * STAGE_BYTES + PD_BYTES + DY_BYTES + 2 * BC_BYTES + PART_BYTES +
-                                    DBC_BYTES + R_BYTES;
+    static constexpr size_t BAR_OFF = (size_t)STAGES * STAGE_BYTES + PD_BYTES + DY_BYTES + 2 * BC_BYTES +
+                                      PART_BYTES + DBC_BYTES + R_BYTES;   // "slot filled" barriers
+    static constexpr size_t BYTES = BAR_OFF + 8 * STAGES;
+    static_assert(STAGE_BYTES % 128 == 0 && RAW_X % 128 == 0 && RAW_BC % 128 == 0 && BAR_OFF % 8 == 0,
+                  "tensor-copy tiles on 128-byte boundaries");
     static_assert(RH >= 2 && RH % 2 == 0, "epilogue runs are processed in pairs");
 };
 
@@ -94,9 +101,12 @@ __device__ __forceinline__ u64 neg2(u64 a) { return a ^ 0x8000000080000000ull; }
 // A walking step can be cut before it (RST forward: its start flag) or after
 // it (RST reverse: its start flag); a cut zeroes the carried state in the
 // walks and the adjoint passed across it.
-template <typename T, int S, bool REV, bool RST>
+//
+// TMA: the tiles arrive by tensor copies (one thread per chunk, completion on
+// the slot's barrier, bounded waits) in an instantiation of their own.
+template <typename T, int S, bool REV, bool RST, bool TMA>
 __global__ void __launch_bounds__(BwdShape<T, S>::NT, BwdShape<T, S>::NT <= 128 ? 3 : 1)
-scan_bwd_kernel(const BwdParams p)
+scan_bwd_kernel(const __grid_constant__ BwdParams p)
 {
     using SH = BwdShape<T, S>;
     constexpr int NT = SH::NT, CH = SH::CH, NS = SH::NS, LC = SH::LC, HC = SH::HC, NH = SH::NH;
@@ -104,7 +114,8 @@ scan_bwd_kernel(const BwdParams p)
     constexpr int RW = RL * (int)sizeof(T) / 4;
     constexpr int RHW = RH * (int)sizeof(T) / 4 > 0 ? RH * (int)sizeof(T) / 4 : 1;
 
-    extern __shared__ __align__(16) unsigned char smem_raw[];
+    extern __shared__ __align__(128) unsigned char smem_bwd[];
+    unsigned char *smem_raw = smem_bwd;
     unsigned char *raw = smem_raw;                                          // [STAGES][x, dt, z, dout, B, C]
     u64 *Pd = reinterpret_cast<u64 *>(smem_raw + STAGES * SH::STAGE_BYTES);  // [LC][CH] (delta, delta x)
     float *DY = reinterpret_cast<float *>(Pd + LC * CH);                    // [LC][CH] gy
@@ -114,6 +125,12 @@ scan_bwd_kernel(const BwdParams p)
     float *DBC = Part + 3 * S * HC * CH;                                    // [2][LC][NS]
     unsigned char *Rst = reinterpret_cast<unsigned char *>(DBC + 2 * LC * NS);  // [LC] sequence starts
     const uint32_t raw_s = static_cast<uint32_t>(__cvta_generic_to_shared(raw));
+    const uint32_t bars_s = raw_s + static_cast<uint32_t>(SH::BAR_OFF);
+    if (TMA && (raw_s & 127u) != 0) {   // tensor copies need 128-byte aligned destinations
+        if (threadIdx.x == 0)
+            atomicOr(&g_fault_flags, kFaultSmemAlign);
+        return;
+    }
 
     const int tid = threadIdx.x;
     const int64_t b = blockIdx.y;
@@ -189,9 +206,58 @@ scan_bwd_kernel(const BwdParams p)
     }
 
     // copy the raw pieces of chunk k into ring slot `slot`
+    // tensor copies: copies issued into and waits completed on each of the two
+    // slots (the n-th completion of a slot's barrier has parity n & 1)
+    static_assert(STAGES == 2, "two slots");
+    int iss0 = 0, iss1 = 0, wt0 = 0, wt1 = 0;
+    bool aborted = false;
+    if (TMA) {
+        if (tid == 0) {
+            for (int s2 = 0; s2 < STAGES; ++s2)
+                mbar_init(bars_s + 8u * s2, 1);
+            mbar_fence_init();
+        }
+        __syncthreads();
+    }
+    auto wait_slot = [&](int slot) {
+        if constexpr (TMA) {
+            if (!aborted)
+                aborted = !mbar_wait(bars_s + 8u * slot, static_cast<uint32_t>((slot ? wt1 : wt0) & 1));
+            if (!aborted) {
+                if (slot)
+                    ++wt1;
+                else
+                    ++wt0;
+            }
+        }
+    };
+
     auto stage_in = [&](int64_t k, int slot, bool phase2) {
         const uint32_t st = raw_s + static_cast<uint32_t>(slot * SH::STAGE_BYTES);
         const int64_t t1 = k * LC;
+        if constexpr (TMA) {
+            if (tid == 0 && !aborted) {
+                const uint32_t bar = bars_s + 8u * slot;
+                const bool zz = phase2 && gate;
+                mbar_expect_tx(bar, 2 * SH::RAW_X + SH::RAW_BC + (zz ? SH::RAW_X : 0) +
+                                        (phase2 ? SH::RAW_X + SH::RAW_BC : 0));
+                const int c0 = static_cast<int>(t1), cd = static_cast<int>(d0), cb = static_cast<int>(b);
+                tma_load_3d(st, &p.tm_x, bar, c0, cd, cb);
+                tma_load_3d(st + SH::RAW_X, &p.tm_dt, bar, c0, cd, cb);
+                if (zz)
+                    tma_load_3d(st + 2 * SH::RAW_X, &p.tm_z, bar, c0, cd, cb);
+                if (phase2)
+                    tma_load_3d(st + 3 * SH::RAW_X, &p.tm_dout, bar, c0, cd, cb);
+                tma_load_3d(st + 4 * SH::RAW_X, &p.tm_B, bar, c0, 0, cb);
+                if (phase2)
+                    tma_load_3d(st + 4 * SH::RAW_X + SH::RAW_BC, &p.tm_C, bar, c0, 0, cb);
+                if (slot)
+                    ++iss1;
+                else
+                    ++iss0;
+            }
+            return;
+        }
         const int rem = static_cast<int>(L - t1 < (1 << 29) ? L - t1 : (1 << 29));
 #pragma unroll
         for (int u = 0; u < PPT; ++u) {
@@ -310,6 +376,7 @@ scan_bwd_kernel(const BwdParams p)
             else
                 cp_async_commit();
         cp_async_wait<STAGES - 2>();
+        wait_slot(0);
         __syncthreads();
         prep(phys1(0), 0, false);
         convert_bc(0, false);
@@ -349,6 +416,8 @@ scan_bwd_kernel(const BwdParams p)
                 }
             }
             cp_async_wait<STAGES - 2>();
+            if (j + 1 < nchunks)
+                wait_slot(static_cast<int>((j + 1) % STAGES));
             __syncthreads();
             if (j + 1 < nchunks) {
                 prep(phys1(j + 1), static_cast<int>((j + 1) % STAGES), false);
@@ -389,6 +458,7 @@ scan_bwd_kernel(const BwdParams p)
         else
             cp_async_commit();
     cp_async_wait<STAGES - 2>();
+    wait_slot(0);
     __syncthreads();
     prep(phys2(0), 0, true);
     convert_bc(0, true);
@@ -630,6 +700,8 @@ scan_bwd_kernel(const BwdParams p)
         }
 
         cp_async_wait<STAGES - 2>();
+        if (j + 1 < nchunks)
+            wait_slot(static_cast<int>((j + 1) % STAGES));
         __syncthreads();
         if (j + 1 < nchunks) {
             const int nslot = static_cast<int>((j + 1) % STAGES);
@@ -665,6 +737,12 @@ scan_bwd_kernel(const BwdParams p)
         if (p.ddt_bias)
             atomicAdd(p.ddt_bias + de, db_acc);
     }
+    if (TMA && tid == 0) {   // after a wait gave up: let the copies issued since land (each wait bounded)
+        for (int n = wt0; n < iss0; ++n)
+            mbar_wait(bars_s, static_cast<uint32_t>(n & 1));
+        for (int n = wt1; n < iss1; ++n)
+            mbar_wait(bars_s + 8u, static_cast<uint32_t>(n & 1));
+    }
 }
 
 // ------------------------------------------------------------------ backward host side
@@ -685,7 +763,7 @@ template <typename T, int S, bool REV, bool RST>
 ss_status launch_bwd(const BwdParams &p, cudaStream_t stream)
 {
     using SH = BwdShape<T, S>;
-    auto kernel = scan_bwd_kernel<T, S, REV, RST>;
+    auto kernel = p.tma ? scan_bwd_kernel<T, S, REV, RST, true> : scan_bwd_kernel<T, S, REV, RST, false>;
     const size_t smem = SH::BYTES;
     if (smem > 48u * 1024u) {
         cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -704,6 +782,27 @@ ss_status launch_bwd(const BwdParams &p, cudaStream_t stream)
     if (e != cudaSuccess)
         return fail(SS_ERR_LAUNCH, "backward kernel launch failed: %s", cudaGetErrorString(e));
     return SS_OK;
+}
+
+// The backward's tile maps: the forward scan's boxes, plus dout (SS_SCAN_TMA=0
+// keeps the cp.async pieces).
+template <typename T>
+bool encode_bwd_maps(BwdParams &p)
+{
+    const char *env = getenv("SS_SCAN_TMA");
+    if (env && strcmp(env, "0") == 0)
+        return false;
+    using SH = BwdShape<T, 1>;   // CH, LC and the raw row do not depend on the state split
+    const uint32_t ns = static_cast<uint32_t>(4 * bwd_groups(p.N));
+    const uint32_t row_t = SH::ROWB / sizeof(T);
+    bool ok = encode_rows_map<T>(&p.tm_x, p.x, p.L, p.d_inner, p.batch, row_t, SH::CH) &&
+              encode_rows_map<T>(&p.tm_dt, p.dt, p.L, p.d_inner, p.batch, row_t, SH::CH) &&
+              encode_rows_map<T>(&p.tm_dout, p.dout, p.L, p.d_inner, p.batch, row_t, SH::CH) &&
+              encode_rows_map<T>(&p.tm_B, p.B, p.L, p.N, p.batch, SH::LC, ns) &&
+              encode_rows_map<T>(&p.tm_C, p.C, p.L, p.N, p.batch, SH::LC, ns);
+    if (ok && p.z)
+        ok = encode_rows_map<T>(&p.tm_z, p.z, p.L, p.d_inner, p.batch, row_t, SH::CH);
+    return ok;
 }
 
 template <typename T, int S>
@@ -783,6 +882,7 @@ ss_status scan_bwd(const void *x, const void *dt, const float *A, const void *B,
     p.vec = (L % 16 == 0) && aligned16(x) && aligned16(dt) && aligned16(dout) && aligned16(dx) &&
             aligned16(ddt) && (!z || aligned16(z)) && (!p.dz || aligned16(p.dz));
     p.vec4 = (L % 4 == 0) && aligned16(dB) && aligned16(dC);
+    p.tma = (p.vec && aligned16(B) && aligned16(C) && encode_bwd_maps<T>(p)) ? 1 : 0;
     const int64_t S = bwd_groups(N);
     const bool rev = reverse != 0;
     if (S == 1) return dispatch_bwd<T, 1>(p, rev, stream);
