@@ -15,6 +15,10 @@ struct UpdateParams {
     int64_t batch, d_inner, N;
     int vec;     // N % 4 == 0 and 16-byte aligned state and A
     int vec_bc;  // B and C rows are whole 16-byte words (16-byte aligned, N * sizeof(T) % 16 == 0)
+    // N = 16 kernel with tensor copies: the state as (16, d_inner, batch) fp32 with a
+    // box of 128 channels of one batch row and the 64-byte swizzle; B, C as (16, batch)
+    // with a box of kDecRows rows
+    CUtensorMap tm_state, tm_B, tm_C;
 };
 
 // One thread per (batch row, channel) holding all N = 4 NV states: the state
@@ -89,14 +93,36 @@ state_update_row_kernel(const UpdateParams p)
 // XOR-swizzled so that the row reads are free of bank conflicts.
 constexpr int kDecRows = 4;
 
-template <typename T>
+// TMA: the states and B, C arrive by tensor copies instead: one thread issues
+// a box of 128 channels per batch row with the 64-byte swizzle (16-byte piece
+// v of a channel's 64 bytes at v ^ ((channel >> 1) & 3), the layout the pieces
+// use) and the rows' B and C, completing on one barrier (bounded wait).
+template <typename T, bool TMA>
 __global__ void __launch_bounds__(kBlock)
-state_update_rows16_kernel(const UpdateParams p)
+state_update_rows16_kernel(const __grid_constant__ UpdateParams p)
 {
     constexpr int NV = 4, R = kDecRows;
     constexpr int BCP = 2 * 16 * (int)sizeof(T) / 16;   // 16-byte pieces of one batch row's B and C
-    __shared__ __align__(16) float4 sst[R * kBlock * NV];
-    __shared__ __align__(16) T sbc[R * 2 * 16];        // [row][B, C][16]
+    __shared__ __align__(1024) float4 sst[R * kBlock * NV];
+    __shared__ __align__(128) T sbc[R * 2 * 16];       // pieces: [row][B, C][16]; copies: [B, C][row][16]
+    __shared__ __align__(8) uint64_t dec_bar;
+    const uint32_t sst_s = static_cast<uint32_t>(__cvta_generic_to_shared(sst));
+    const uint32_t sbc_s = static_cast<uint32_t>(__cvta_generic_to_shared(sbc));
+    const uint32_t bar_s = static_cast<uint32_t>(__cvta_generic_to_shared(&dec_bar));
+    if (TMA && ((sst_s & 1023u) != 0 || (sbc_s & 127u) != 0)) {   // the swizzle and the copies need these
+        if (threadIdx.x == 0)
+            atomicOr(&g_fault_flags, kFaultSmemAlign);
+        return;
+    }
+    bool aborted = false;
+    int waits = 0;
+    if (TMA) {
+        if (threadIdx.x == 0) {
+            mbar_init(bar_s, 1);
+            mbar_fence_init();
+        }
+        __syncthreads();
+    }
     const int r = threadIdx.x;
     const int64_t d = static_cast<int64_t>(blockIdx.x) * kBlock + r;
     const bool act = d < p.d_inner;
@@ -110,6 +136,17 @@ state_update_rows16_kernel(const UpdateParams p)
     for (int64_t b0 = static_cast<int64_t>(blockIdx.y) * R; b0 < p.batch;
          b0 += static_cast<int64_t>(gridDim.y) * R) {
         // the states of this thread's R rows, and B, C of the R batch rows, into shared memory
+        if constexpr (TMA) {
+            if (r == 0 && !aborted) {
+                mbar_expect_tx(bar_s, R * kBlock * 64 + 2 * R * 16 * (int)sizeof(T));
+                const int c1 = static_cast<int>(blockIdx.x) * kBlock;
+#pragma unroll
+                for (int k = 0; k < R; ++k)
+                    tma_load_3d(sst_s + k * kBlock * 64, &p.tm_state, bar_s, 0, c1, static_cast<int>(b0 + k));
+                tma_load_3d(sbc_s, &p.tm_B, bar_s, 0, static_cast<int>(b0), 0);
+                tma_load_3d(sbc_s + R * 16 * (int)sizeof(T), &p.tm_C, bar_s, 0, static_cast<int>(b0), 0);
+            }
+        } else {
 #pragma unroll
         for (int k = 0; k < R; ++k) {
             const int64_t b = b0 + k;
@@ -131,6 +168,7 @@ state_update_rows16_kernel(const UpdateParams p)
                        src, ok ? 16 : 0);
         }
         cp_async_commit();
+        }
         float xv[R], dlv[R], zv[R];
 #pragma unroll
         for (int k = 0; k < R; ++k) {
@@ -141,7 +179,13 @@ state_update_rows16_kernel(const UpdateParams p)
             dlv[k] = ok ? Io<T>::load1(static_cast<const T *>(p.delta) + row) : 0.0f;
             zv[k] = (ok && p.z) ? Io<T>::load1(static_cast<const T *>(p.z) + row) : 0.0f;
         }
-        cp_async_wait<0>();
+        if constexpr (TMA) {
+            if (!aborted)
+                aborted = !mbar_wait(bar_s, static_cast<uint32_t>(waits & 1));
+            ++waits;
+        } else {
+            cp_async_wait<0>();
+        }
         __syncthreads();   // B and C were staged by a few threads for all
 #pragma unroll
         for (int k = 0; k < R; ++k) {
@@ -150,11 +194,13 @@ state_update_rows16_kernel(const UpdateParams p)
                 continue;
             const int64_t row = b * p.d_inner + d;
             float bv[16], cv[16];
-            const uint4 *sb = reinterpret_cast<const uint4 *>(sbc + (k * 2) * 16);   // B then C of row k
+            // B then C of row k (pieces: [row][B, C], copies: [B, C][row])
+            const uint4 *sb = reinterpret_cast<const uint4 *>(sbc + (TMA ? k : k * 2) * 16);
+            const uint4 *sc = reinterpret_cast<const uint4 *>(sbc + (TMA ? R * 16 + k * 16 : k * 2 * 16 + 16));
 #pragma unroll
             for (int e = 0; e < 16 / Io<T>::kPerVec; ++e) {   // plain shared loads, one address for all threads
                 unpack_piece<T>(sb[e], bv + e * Io<T>::kPerVec);
-                unpack_piece<T>(sb[16 / Io<T>::kPerVec + e], cv + e * Io<T>::kPerVec);
+                unpack_piece<T>(sc[e], cv + e * Io<T>::kPerVec);
             }
             const float dx = dlv[k] * xv[k], dl2 = dlv[k] * kLog2e;
             float out = 0.0f;
@@ -179,17 +225,53 @@ state_update_rows16_kernel(const UpdateParams p)
         }
         __syncthreads();   // the staged B, C (and states) are reused by the next group of rows
     }
+    if (TMA && threadIdx.x == 0 && aborted)   // the copies whose wait gave up: let them land (bounded)
+        mbar_wait(bar_s, static_cast<uint32_t>((waits - 1) & 1));
+}
+
+// 3-d tensor map with box (b0, b1, 1); elements outside the tensor read as zero
+bool encode_dec_map(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t d0, uint64_t d1, uint64_t d2,
+                    uint64_t s1, uint64_t s2, uint32_t b0, uint32_t b1, CUtensorMapSwizzle swz)
+{
+    const EncodeTiledFn fn = encode_tiled_fn();
+    if (!fn)
+        return false;
+    const cuuint64_t dims[3] = {d0, d1, d2};
+    const cuuint64_t strides[2] = {s1, s2};
+    const cuuint32_t box[3] = {b0, b1, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, dt, 3, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The N = 16 kernel's maps (SS_SCAN_TMA=0 keeps the cp.async pieces).
+template <typename T>
+bool encode_dec_maps(UpdateParams &p)
+{
+    const char *env = getenv("SS_SCAN_TMA");
+    if (env && strcmp(env, "0") == 0)
+        return false;
+    const uint64_t D = static_cast<uint64_t>(p.d_inner), Bt = static_cast<uint64_t>(p.batch);
+    const CUtensorMapDataType io = sizeof(T) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    const uint64_t row = 16 * sizeof(T);
+    return encode_dec_map(&p.tm_state, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.state, 16, D, Bt, 64, D * 64, 16, kBlock,
+                          CU_TENSOR_MAP_SWIZZLE_64B) &&
+           encode_dec_map(&p.tm_B, io, p.B, 16, Bt, 1, row, row * Bt, 16, kDecRows, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+           encode_dec_map(&p.tm_C, io, p.C, 16, Bt, 1, row, row * Bt, 16, kDecRows, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 template <typename T>
-ss_status launch_update_rows16(const UpdateParams &p, cudaStream_t stream)
+ss_status launch_update_rows16(UpdateParams p, cudaStream_t stream)
 {
     const int64_t dblocks = (p.d_inner + kBlock - 1) / kBlock;
     const int64_t groups = (p.batch + kDecRows - 1) / kDecRows;
     if (dblocks > 0x7fffffff)
         return fail(SS_ERR_DIM, "grid too large");
     const dim3 grid(static_cast<unsigned>(dblocks), static_cast<unsigned>(std::min<int64_t>(groups, 65535)));
-    state_update_rows16_kernel<T><<<grid, kBlock, 0, stream>>>(p);
+    if (encode_dec_maps<T>(p))
+        state_update_rows16_kernel<T, true><<<grid, kBlock, 0, stream>>>(p);
+    else
+        state_update_rows16_kernel<T, false><<<grid, kBlock, 0, stream>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
         return fail(SS_ERR_LAUNCH, "state update launch failed: %s", cudaGetErrorString(e));
@@ -323,7 +405,7 @@ ss_status state_update(float *state, const void *x, const void *delta, const flo
     ss_status st = check_ptrs(list, static_cast<int>(sizeof(list) / sizeof(list[0])), &dev);
     if (st != SS_OK)
         return st;
-    UpdateParams p;
+    UpdateParams p{};
     p.state = state; p.x = x; p.delta = delta; p.B = B; p.C = C; p.z = z;
     p.A = A; p.D = D; p.y = y;
     p.batch = batch; p.d_inner = d_inner; p.N = N;
