@@ -636,6 +636,16 @@ def oracle_single_thread_rate(spec: I.ScanSpec, rows: int = 16, inp=None):
     return rows * spec.L * spec.N / (time.time() - t)
 
 
+def bench_config(spec: I.ScanSpec, world: int) -> dict:
+    """The ``config`` object of both arms' lines (the same keys and values, so
+    that the two lines describe the same workload)."""
+    return {"workload": spec.name, "batch": spec.batch, "d_inner": spec.d_inner, "L": spec.L, "N": spec.N,
+            "io": spec.io, "per_gpu": True,
+            "l2": "GPU arm: flushed before every step (256 MB written, then 256 MB read, so the write-back of the "
+                  "written lines happens before the step)",
+            "parallelism": "dp%d (independent batch shards)" % world}
+
+
 def reference_arm(args, rank, world):
     """The oracle as the reference arm: rank 0 only, host cores."""
     if rank != 0:
@@ -656,8 +666,7 @@ def reference_arm(args, rank, world):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / max(1, args.steps),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": spec.name, "batch": spec.batch, "d_inner": spec.d_inner, "L": spec.L, "N": spec.N,
-                   "io": spec.io},
+        "config": bench_config(spec, world),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "wall_s": round(time.time() - t0, 2),
@@ -796,9 +805,7 @@ def main(argv=None):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "io_dtype": "bf16", "data": "synthetic",
-        "config": {"workload": HEADLINE.name, "batch": spec.batch, "d_inner": spec.d_inner, "L": spec.L,
-                   "N": spec.N, "io": spec.io, "per_gpu": True, "l2": "flushed before every step: 256 MB written, then 256 MB read (the write-back of the written lines happens before the step)",
-                   "parallelism": "dp%d (independent batch shards)" % world},
+        "config": bench_config(HEADLINE, world),
         "kernel_ms": {"median": statistics.median(times), "min": min(times), "max": max(times)},
         "roofline": roofline_obj(alg, ms_per_step, peaks, traffic, elem_steps=elems),
         "alg_bytes_per_step": alg,

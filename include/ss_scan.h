@@ -421,6 +421,16 @@ ss_status ss_ssd_fwd_bf16(const ss_bf16 *x, const ss_bf16 *dt, const float *A, c
 #define SS_FAULT_SMEM_ALIGN 2u
 ss_status ss_device_faults(unsigned int *flags, int clear);
 
+/* The architecture the library's kernels were compiled for, as the CUDA
+ * runtime reports it for the loaded module on the current device
+ * (cudaFuncGetAttributes(...).binaryVersion of the forward scan kernel:
+ * major * 10 + minor, 103 for sm_103a). A build check with no counterpart in
+ * the pages; it needs a GPU (it loads the module in the current context).
+ *   binary_version  host pointer, receives the value
+ * Errors: SS_ERR_NULL (binary_version NULL), SS_ERR_INTERNAL (the query
+ * failed, e.g. no GPU or no image for this GPU in the library). */
+ss_status ss_kernel_binary_version(int *binary_version);
+
 /* Message describing the last non-OK status returned on this host thread
  * ("" if none). The string is owned by the library. */
 const char *ss_last_error(void);

@@ -22,7 +22,7 @@ EXPORTS = ("ss_scan_fwd_bf16", "ss_scan_fwd_f32", "ss_scan_fwd_ex_bf16", "ss_sca
            "ss_conv_state_update_f32", "ss_scan_bwd_bf16", "ss_scan_bwd_f32", "ss_scan_bwd_workspace_bytes",
            "ss_scan_bwd_noalloc_bf16", "ss_scan_bwd_noalloc_f32", "ss_ssd_fwd_bf16", "ss_ssd_workspace_bytes",
            "ss_scan_fwd_train_bf16", "ss_scan_fwd_train_f32", "ss_scan_bwd_ex_bf16", "ss_scan_bwd_ex_f32",
-           "ss_device_faults", "ss_last_error", "ss_abi_version")
+           "ss_device_faults", "ss_kernel_binary_version", "ss_last_error", "ss_abi_version")
 
 STATUS = {0: "SS_OK", -1: "SS_ERR_NULL", -2: "SS_ERR_DIM", -3: "SS_ERR_N", -4: "SS_ERR_DEVICE_PTR",
           -5: "SS_ERR_LAUNCH", -6: "SS_ERR_INTERNAL"}
@@ -86,6 +86,8 @@ def lib() -> ctypes.CDLL:
     L.ss_scan_bwd_workspace_bytes.restype = ctypes.c_size_t
     L.ss_device_faults.argtypes = [ctypes.POINTER(ctypes.c_uint), ci]
     L.ss_device_faults.restype = ci
+    L.ss_kernel_binary_version.argtypes = [ctypes.POINTER(ctypes.c_int)]
+    L.ss_kernel_binary_version.restype = ci
     L.ss_last_error.argtypes = []
     L.ss_last_error.restype = ctypes.c_char_p
     L.ss_abi_version.argtypes = []
@@ -111,6 +113,15 @@ def device_faults(clear: bool = True) -> int:
 
 def abi_version() -> int:
     return lib().ss_abi_version()
+
+
+def kernel_binary_version() -> int:
+    """The architecture the library's kernels were compiled for, as the CUDA
+    runtime reports it for the module loaded on the current device (103 for
+    sm_103a); needs a GPU."""
+    v = ctypes.c_int(0)
+    _check(lib().ss_kernel_binary_version(ctypes.byref(v)))
+    return v.value
 
 
 def _ptr(t):

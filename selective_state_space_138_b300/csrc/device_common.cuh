@@ -297,6 +297,9 @@ __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_gr
 // the GPU.
 
 constexpr unsigned int kFaultWaitTimeout = 1u;
+// A kernel that stages its tiles by tensor copies found its dynamic shared
+// memory off the 128-byte boundary the copies need (SS_FAULT_SMEM_ALIGN).
+constexpr unsigned int kFaultSmemAlign = 2u;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;   // one second
 __device__ unsigned int g_fault_flags;
 

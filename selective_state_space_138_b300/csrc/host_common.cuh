@@ -7,7 +7,7 @@
 
 // ------------------------------------------------------------------ host side
 
-thread_local char g_err[512] = "";
+using ssi::g_err;   // one message buffer per host thread, shared by every part of the library
 
 ss_status fail(ss_status s, const char *fmt, ...)
 {
@@ -81,4 +81,68 @@ int sm_count(int dev)
     }
     cache[dev].store(sms, std::memory_order_relaxed);
     return sms;
+}
+
+// ------------------------------------------------------------------ tensor maps (cuTensorMapEncodeTiled)
+
+using EncodeTiledFn = PFN_cuTensorMapEncodeTiled_v12000;
+
+// the driver's tensor-map encoder, looked up once; null when unavailable
+EncodeTiledFn encode_tiled_fn()
+{
+    static const EncodeTiledFn fn = [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess) {
+            cudaGetLastError();
+            f = nullptr;
+        }
+        return reinterpret_cast<EncodeTiledFn>(f);
+    }();
+    return fn;
+}
+
+// map of a (batch, rows, L) tensor of T as three dimensions (L, rows, batch),
+// box (box_t, box_rows, 1); elements outside the tensor read as zero
+template <typename T>
+bool encode_rows_map(CUtensorMap *m, const void *base, int64_t L, int64_t rows, int64_t batch, uint32_t box_t,
+                     uint32_t box_rows)
+{
+    const EncodeTiledFn fn = encode_tiled_fn();
+    if (!fn || !base)
+        return false;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(L), static_cast<cuuint64_t>(rows),
+                                static_cast<cuuint64_t>(batch)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(L) * sizeof(T),
+                                   static_cast<cuuint64_t>(L) * static_cast<cuuint64_t>(rows) * sizeof(T)};
+    const cuuint32_t box[3] = {box_t, box_rows, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUtensorMapDataType dt = sizeof(T) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    return fn(m, dt, 3, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// ------------------------------------------------------------------ the backward pass's stored states
+//
+// Shared by the backward pass and the training forward, which fills the same
+// workspace layout.
+
+constexpr int64_t kBwdHC = 16;   // steps per stored state (BwdShape::HC)
+
+int64_t bwd_groups(int64_t N) { return N <= 4 ? 1 : (N <= 8 ? 2 : (N <= 16 ? 4 : 8)); }
+
+// 0 for sizes the backward pass rejects: a size <= 0, N outside [1, 32], or an
+// element count past the limits of scan_bwd (checked before any product is
+// formed, so nothing here can overflow)
+size_t bwd_workspace_bytes(int64_t batch, int64_t d_inner, int64_t L, int64_t N)
+{
+    if (batch <= 0 || d_inner <= 0 || L <= 0 || N < 1 || N > 32)
+        return 0;
+    if (batch > (int64_t(1) << 40) / d_inner || batch * d_inner > (int64_t(1) << 50) / L)
+        return 0;
+    const int64_t nsub = (L + kBwdHC - 1) / kBwdHC;
+    return static_cast<size_t>(batch) * nsub * bwd_groups(N) * d_inner * 16;
 }

@@ -747,18 +747,6 @@ scan_bwd_kernel(const __grid_constant__ BwdParams p)
 
 // ------------------------------------------------------------------ backward host side
 
-constexpr int64_t kBwdHC = 16;   // steps per stored state (BwdShape::HC)
-
-int64_t bwd_groups(int64_t N) { return N <= 4 ? 1 : (N <= 8 ? 2 : (N <= 16 ? 4 : 8)); }
-
-size_t bwd_workspace_bytes(int64_t batch, int64_t d_inner, int64_t L, int64_t N)
-{
-    if (batch <= 0 || d_inner <= 0 || L <= 0 || N < 1 || N > 32)
-        return 0;
-    const int64_t nsub = (L + kBwdHC - 1) / kBwdHC;
-    return static_cast<size_t>(batch) * nsub * bwd_groups(N) * d_inner * 16;
-}
-
 template <typename T, int S, bool REV, bool RST>
 ss_status launch_bwd(const BwdParams &p, cudaStream_t stream)
 {
@@ -895,32 +883,83 @@ ss_status scan_bwd(const void *x, const void *dt, const float *A, const void *B,
 //
 // ss_scan_bwd_noalloc_* keeps the stored states in this file-scope device
 // array instead of a caller workspace, so a call allocates nothing and needs
-// nothing beyond its inputs and outputs. There is one array per device context,
-// shared by every call in the process: two calls whose work overlaps in time
+// nothing beyond its inputs and outputs. Every CUDA context that loads the
+// library's module holds one copy of the array (kBwdScratchBytes of device
+// memory), whether or not it ever calls the entry point. The copy is shared by
+// every call made in that context: two calls whose work overlaps in time
 // (different streams without ordering, or different host threads) race on it,
-// so callers order them. Its address is resolved with cudaGetSymbolAddress on
-// the first call on each device (which can load the module), so that first call
-// must not be made while a stream is being captured; later calls can be.
-// Nothing in it has to start at zero: the forward walk writes every stored
-// state before the reverse walk reads it.
+// so callers order them. Nothing in it has to start at zero: the forward walk
+// writes every stored state before the reverse walk reads it.
+//
+// Host code cannot use the array's name as a device address; the address is
+// resolved with cudaGetSymbolAddress. It belongs to the current context, so it
+// is cached together with that context's unique id: after cudaDeviceReset (or
+// in another context on the same device) the next call resolves it again. The
+// first call in a context resolves it (which can load the module), so that
+// call must not be made while a stream is being captured; later calls can be.
 constexpr size_t kBwdScratchBytes = static_cast<size_t>(SS_BWD_NOALLOC_MAX_BYTES);
 static __device__ __align__(256) unsigned char g_bwd_scratch[kBwdScratchBytes];
 
+using CtxGetCurrentFn = PFN_cuCtxGetCurrent_v4000;
+using CtxGetIdFn = PFN_cuCtxGetId_v12000;
+
+// unique id of the current context (0 if there is none or it cannot be read)
+unsigned long long current_context_id()
+{
+    static const CtxGetCurrentFn get_ctx = [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess) {
+            cudaGetLastError();
+            f = nullptr;
+        }
+        return reinterpret_cast<CtxGetCurrentFn>(f);
+    }();
+    static const CtxGetIdFn get_id = [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess) {
+            cudaGetLastError();
+            f = nullptr;
+        }
+        return reinterpret_cast<CtxGetIdFn>(f);
+    }();
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (!get_ctx || !get_id || get_ctx(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
+}
+
+// device address of g_bwd_scratch in the current context (the runtime's
+// context of device dev, made current by the caller), or NULL
 void *bwd_scratch(int dev)
 {
-    static std::atomic<void *> cache[64];
-    if (dev >= 0 && dev < 64) {
-        void *p = cache[dev].load(std::memory_order_acquire);
-        if (p)
-            return p;
+    struct Entry {
+        unsigned long long ctx_id;
+        void *addr;
+    };
+    static std::mutex mu;
+    static Entry cache[64] = {};
+    const unsigned long long id = current_context_id();
+    if (id != 0 && dev >= 0 && dev < 64) {
+        std::lock_guard<std::mutex> lock(mu);
+        if (cache[dev].ctx_id == id && cache[dev].addr)
+            return cache[dev].addr;
     }
     void *q = nullptr;
     if (cudaGetSymbolAddress(&q, g_bwd_scratch) != cudaSuccess) {
         cudaGetLastError();
         return nullptr;
     }
-    if (dev >= 0 && dev < 64)
-        cache[dev].store(q, std::memory_order_release);
+    // the context id after the call: resolving the address can create the context
+    const unsigned long long id2 = current_context_id();
+    if (id2 != 0 && dev >= 0 && dev < 64) {
+        std::lock_guard<std::mutex> lock(mu);
+        cache[dev] = Entry{id2, q};
+    }
     return q;
 }
 
@@ -938,13 +977,18 @@ ss_status scan_bwd_noalloc(const void *x, const void *dt, const float *A, const 
     for (const auto &r : req)
         if (!r.p)
             return fail(SS_ERR_NULL, "required pointer %s is NULL", r.name);
+    // sizes and N are checked before the stored-state bytes are formed
+    if (batch <= 0 || d_inner <= 0 || L <= 0)
+        return fail(SS_ERR_DIM, "sizes must be positive: batch=%lld d_inner=%lld L=%lld",
+                    (long long)batch, (long long)d_inner, (long long)L);
+    if (N < 1 || N > 32)
+        return fail(SS_ERR_N, "N=%lld outside [1, 32] (the backward pass)", (long long)N);
+    if (batch > (int64_t(1) << 40) / d_inner || batch * d_inner > (int64_t(1) << 50) / L)
+        return fail(SS_ERR_DIM, "element count overflows");
     const size_t need = bwd_workspace_bytes(batch, d_inner, L, N);
     if (need > kBwdScratchBytes)
         return fail(SS_ERR_DIM, "this problem needs %zu bytes of stored states; the built-in scratch holds %zu "
                     "(use ss_scan_bwd_* with a workspace)", need, kBwdScratchBytes);
-    if (need == 0)   // sizes or N out of range: the checks of the workspace form report it
-        return scan_bwd<T>(x, dt, A, B, C, D, z, dt_bias, softplus, h0, dout, dfinal, dx, ddt, dA, dB, dC, dD, dz,
-                           ddt_bias, dh0, nullptr, 0, batch, d_inner, L, N, stream);
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) {

@@ -279,9 +279,6 @@ struct NSplitShape {
 // tiles themselves are the same. RST: p.reset marks sequence starts; the
 // carried state is zeroed before a marked step (forward) or after it
 // (reverse), i.e. at the boundary between t-1 and t either way.
-// A kernel that stages its tiles by tensor copies found its dynamic shared
-// memory off the 128-byte boundary the copies need (SS_FAULT_SMEM_ALIGN).
-constexpr unsigned int kFaultSmemAlign = 2u;
 
 // TMA: the chunks arrive by tensor copies (the maps in p are encoded); the
 // cp.async form is a separate instantiation, so neither carries the other's
@@ -833,46 +830,6 @@ int pick_segments(int64_t groups, int64_t L, int64_t lc, int64_t slots)
 
 // ------------------------------------------------------------------ tensor maps of the n-split kernel
 
-using EncodeTiledFn = PFN_cuTensorMapEncodeTiled_v12000;
-
-// the driver's tensor-map encoder, looked up once; null when unavailable
-EncodeTiledFn encode_tiled_fn()
-{
-    static const EncodeTiledFn fn = [] {
-        void *f = nullptr;
-        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
-                cudaSuccess ||
-            q != cudaDriverEntryPointSuccess) {
-            cudaGetLastError();
-            f = nullptr;
-        }
-        return reinterpret_cast<EncodeTiledFn>(f);
-    }();
-    return fn;
-}
-
-// map of a (batch, rows, L) tensor of T as three dimensions (L, rows, batch),
-// box (box_t, box_rows, 1); elements outside the tensor read as zero
-template <typename T>
-bool encode_rows_map(CUtensorMap *m, const void *base, int64_t L, int64_t rows, int64_t batch, uint32_t box_t,
-                     uint32_t box_rows)
-{
-    const EncodeTiledFn fn = encode_tiled_fn();
-    if (!fn || !base)
-        return false;
-    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(L), static_cast<cuuint64_t>(rows),
-                                static_cast<cuuint64_t>(batch)};
-    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(L) * sizeof(T),
-                                   static_cast<cuuint64_t>(L) * static_cast<cuuint64_t>(rows) * sizeof(T)};
-    const cuuint32_t box[3] = {box_t, box_rows, 1};
-    const cuuint32_t estr[3] = {1, 1, 1};
-    const CUtensorMapDataType dt = sizeof(T) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
-    return fn(m, dt, 3, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 // The n-split kernel's tiles as tensor maps: x, dt, z by channel rows with a
 // box of CH channels x one padded raw row (LC steps + 16 bytes), B and C by
 // state rows with a box of NS states x LC steps. Needs 16-byte aligned rows
@@ -990,8 +947,6 @@ bool use_nsplit(int64_t N)
         return false;
     return true;
 }
-
-size_t bwd_workspace_bytes(int64_t batch, int64_t d_inner, int64_t L, int64_t N);
 
 template <typename T>
 ss_status scan_fwd(const void *x, const void *dt, const float *A, const void *B, const void *C,

@@ -5,15 +5,21 @@
 // discretization the code actually uses", "The Mamba block", "Decoding with a
 // constant-size cache", "Why the scan must be fused").
 //
-// One translation unit, kept in parts:
+// One source, kept in parts:
 //   device_common.cuh  device math, io conversion, f32x2 pairs, cp.async, mbarriers and tensor copies
-//   host_common.cuh    error strings, pointer validation, device queries
+//   host_common.cuh    error strings, pointer validation, device queries, tensor maps, stored-state layout
 //   scan_fwd.cuh       forward scan (n-split and time-lane kernels)
 //   scan_bwd.cuh       backward pass (states recomputed)
 //   decode.cuh         single-token state update
 //   conv.cuh           causal depthwise conv1d + SiLU and its decode step
 //   ssd.cuh            Mamba-2's scalar-decay scan on the tensor cores
 // followed here by the extern "C" entry points.
+//
+// The library is compiled as several objects from this one file, one per
+// value of SS_PART (1 forward scan, 2 backward pass, 3 decode update and conv,
+// 4 SSD, 0 the entry points every part shares), so that the parts build in
+// parallel; with SS_PART undefined everything is compiled at once. Each
+// object has its own device fault word; ss_device_faults reads them all.
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -29,26 +35,85 @@
 
 #include <algorithm>
 #include <atomic>
+#include <mutex>
 
 #include "ss_scan.h"
 
+#ifndef SS_PART
+#define SS_PART_IS(k) 1
+#else
+#define SS_PART_IS(k) (SS_PART == (k))
+#endif
+
 namespace cg = cooperative_groups;
+
+namespace ssi {
+// the message of the last non-OK status on this host thread (defined once, in part 0)
+extern thread_local char g_err[512];
+// each part's device fault word: read (and cleared when `clear`) into *flags
+cudaError_t fault_word_fwd(unsigned int *flags, int clear);
+cudaError_t fault_word_bwd(unsigned int *flags, int clear);
+cudaError_t fault_word_dec(unsigned int *flags, int clear);
+cudaError_t fault_word_ssd(unsigned int *flags, int clear);
+}  // namespace ssi
 
 namespace {
 
 #include "device_common.cuh"
 #include "host_common.cuh"
+#if SS_PART_IS(1)
 #include "scan_fwd.cuh"
+#endif
+#if SS_PART_IS(2)
 #include "scan_bwd.cuh"
+#endif
+#if SS_PART_IS(3)
 #include "decode.cuh"
 #include "conv.cuh"
+#endif
+#if SS_PART_IS(4)
 #include "ssd.cuh"
+#endif
+
+// this object's device fault word, read (and cleared) from the host
+[[maybe_unused]] cudaError_t read_fault_word(unsigned int *flags, int clear)
+{
+    unsigned int v = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_fault_flags, sizeof(v));
+    if (e == cudaSuccess && clear) {
+        const unsigned int none = 0;
+        e = cudaMemcpyToSymbol(g_fault_flags, &none, sizeof(none));
+    }
+    *flags = v;
+    return e;
+}
 
 }  // namespace
+
+namespace ssi {
+#if SS_PART_IS(0)
+thread_local char g_err[512] = "";
+#endif
+#if SS_PART_IS(1)
+cudaError_t fault_word_fwd(unsigned int *flags, int clear) { return read_fault_word(flags, clear); }
+#endif
+#if SS_PART_IS(2)
+cudaError_t fault_word_bwd(unsigned int *flags, int clear) { return read_fault_word(flags, clear); }
+#endif
+#if SS_PART_IS(3)
+cudaError_t fault_word_dec(unsigned int *flags, int clear) { return read_fault_word(flags, clear); }
+#endif
+#if SS_PART_IS(4)
+cudaError_t fault_word_ssd(unsigned int *flags, int clear) { return read_fault_word(flags, clear); }
+#endif
+}  // namespace ssi
 
 // ------------------------------------------------------------------ C ABI
 
 extern "C" {
+
+// ---- forward scan
+#if SS_PART_IS(1)
 
 ss_status ss_scan_fwd_bf16(const ss_bf16 *x, const ss_bf16 *delta, const float *A, const ss_bf16 *B,
                            const ss_bf16 *C, const float *D, const ss_bf16 *z, const float *dt_bias,
@@ -87,47 +152,52 @@ ss_status ss_scan_fwd_ex_f32(const float *x, const float *delta, const float *A,
                            batch, d_inner, L, N, stream);
 }
 
-ss_status ss_state_update_bf16(float *state, const ss_bf16 *x, const ss_bf16 *delta, const float *A,
-                               const ss_bf16 *B, const ss_bf16 *C, const float *D, const ss_bf16 *z,
-                               ss_bf16 *y, int64_t batch, int64_t d_inner, int64_t N,
-                               cudaStream_t stream)
+ss_status ss_scan_fwd_train_bf16(const ss_bf16 *x, const ss_bf16 *delta, const float *A, const ss_bf16 *B,
+                                 const ss_bf16 *C, const float *D, const ss_bf16 *z, const float *dt_bias,
+                                 int delta_softplus, const float *h0, ss_bf16 *y, float *final_state, void *workspace,
+                                 size_t workspace_bytes, int64_t batch, int64_t d_inner, int64_t L, int64_t N,
+                                 cudaStream_t stream)
 {
-    return state_update<__nv_bfloat16>(state, x, delta, A, B, C, D, z, y, batch, d_inner, N, stream);
+    if (!workspace) {
+        g_err[0] = '\0';
+        return fail(SS_ERR_NULL, "required pointer workspace is NULL");
+    }
+    return scan_fwd<__nv_bfloat16>(x, delta, A, B, C, D, z, dt_bias, delta_softplus, h0, nullptr, 0, y, final_state,
+                                   batch, d_inner, L, N, stream, workspace, workspace_bytes);
 }
 
-ss_status ss_state_update_f32(float *state, const float *x, const float *delta, const float *A,
-                              const float *B, const float *C, const float *D, const float *z, float *y,
-                              int64_t batch, int64_t d_inner, int64_t N, cudaStream_t stream)
+ss_status ss_scan_fwd_train_f32(const float *x, const float *delta, const float *A, const float *B, const float *C,
+                                const float *D, const float *z, const float *dt_bias, int delta_softplus,
+                                const float *h0, float *y, float *final_state, void *workspace, size_t workspace_bytes,
+                                int64_t batch, int64_t d_inner, int64_t L, int64_t N, cudaStream_t stream)
 {
-    return state_update<float>(state, x, delta, A, B, C, D, z, y, batch, d_inner, N, stream);
+    if (!workspace) {
+        g_err[0] = '\0';
+        return fail(SS_ERR_NULL, "required pointer workspace is NULL");
+    }
+    return scan_fwd<float>(x, delta, A, B, C, D, z, dt_bias, delta_softplus, h0, nullptr, 0, y, final_state, batch,
+                           d_inner, L, N, stream, workspace, workspace_bytes);
 }
 
-ss_status ss_causal_conv1d_bf16(const ss_bf16 *x, const float *w, const float *bias, const ss_bf16 *state_in,
-                                int silu, ss_bf16 *out, ss_bf16 *state_out, int64_t batch, int64_t d_inner,
-                                int64_t L, int64_t k, cudaStream_t stream)
+ss_status ss_kernel_binary_version(int *binary_version)
 {
-    return causal_conv1d<__nv_bfloat16>(x, w, bias, state_in, silu, out, state_out, batch, d_inner, L, k, stream);
+    g_err[0] = '\0';
+    if (!binary_version)
+        return fail(SS_ERR_NULL, "binary_version is NULL");
+    cudaFuncAttributes a{};
+    const cudaError_t e = cudaFuncGetAttributes(&a, scan_nsplit_kernel<__nv_bfloat16, 4, false, false, true>);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(SS_ERR_INTERNAL, "cudaFuncGetAttributes failed: %s", cudaGetErrorString(e));
+    }
+    *binary_version = a.binaryVersion;
+    return SS_OK;
 }
 
-ss_status ss_causal_conv1d_f32(const float *x, const float *w, const float *bias, const float *state_in, int silu,
-                               float *out, float *state_out, int64_t batch, int64_t d_inner, int64_t L, int64_t k,
-                               cudaStream_t stream)
-{
-    return causal_conv1d<float>(x, w, bias, state_in, silu, out, state_out, batch, d_inner, L, k, stream);
-}
+#endif
 
-ss_status ss_conv_state_update_bf16(ss_bf16 *conv_state, const ss_bf16 *x, const float *w, const float *bias,
-                                    int silu, ss_bf16 *out, int64_t batch, int64_t d_inner, int64_t k,
-                                    cudaStream_t stream)
-{
-    return conv_state_update<__nv_bfloat16>(conv_state, x, w, bias, silu, out, batch, d_inner, k, stream);
-}
-
-ss_status ss_conv_state_update_f32(float *conv_state, const float *x, const float *w, const float *bias, int silu,
-                                   float *out, int64_t batch, int64_t d_inner, int64_t k, cudaStream_t stream)
-{
-    return conv_state_update<float>(conv_state, x, w, bias, silu, out, batch, d_inner, k, stream);
-}
+// ---- backward pass
+#if SS_PART_IS(2)
 
 size_t ss_scan_bwd_workspace_bytes(int64_t batch, int64_t d_inner, int64_t L, int64_t N)
 {
@@ -185,33 +255,6 @@ ss_status ss_scan_bwd_ex_f32(const float *x, const float *delta, const float *A,
                            stream, 0, seq_start, reverse);
 }
 
-ss_status ss_scan_fwd_train_bf16(const ss_bf16 *x, const ss_bf16 *delta, const float *A, const ss_bf16 *B,
-                                 const ss_bf16 *C, const float *D, const ss_bf16 *z, const float *dt_bias,
-                                 int delta_softplus, const float *h0, ss_bf16 *y, float *final_state, void *workspace,
-                                 size_t workspace_bytes, int64_t batch, int64_t d_inner, int64_t L, int64_t N,
-                                 cudaStream_t stream)
-{
-    if (!workspace) {
-        g_err[0] = '\0';
-        return fail(SS_ERR_NULL, "required pointer workspace is NULL");
-    }
-    return scan_fwd<__nv_bfloat16>(x, delta, A, B, C, D, z, dt_bias, delta_softplus, h0, nullptr, 0, y, final_state,
-                                   batch, d_inner, L, N, stream, workspace, workspace_bytes);
-}
-
-ss_status ss_scan_fwd_train_f32(const float *x, const float *delta, const float *A, const float *B, const float *C,
-                                const float *D, const float *z, const float *dt_bias, int delta_softplus,
-                                const float *h0, float *y, float *final_state, void *workspace, size_t workspace_bytes,
-                                int64_t batch, int64_t d_inner, int64_t L, int64_t N, cudaStream_t stream)
-{
-    if (!workspace) {
-        g_err[0] = '\0';
-        return fail(SS_ERR_NULL, "required pointer workspace is NULL");
-    }
-    return scan_fwd<float>(x, delta, A, B, C, D, z, dt_bias, delta_softplus, h0, nullptr, 0, y, final_state, batch,
-                           d_inner, L, N, stream, workspace, workspace_bytes);
-}
-
 ss_status ss_scan_bwd_noalloc_bf16(const ss_bf16 *x, const ss_bf16 *delta, const float *A, const ss_bf16 *B,
                                    const ss_bf16 *C, const float *D, const ss_bf16 *z, const float *dt_bias,
                                    int delta_softplus, const float *h0, const ss_bf16 *dout,
@@ -235,6 +278,58 @@ ss_status ss_scan_bwd_noalloc_f32(const float *x, const float *delta, const floa
                                    ddelta, dA, dB, dC, dD, dz, ddt_bias, dh0, batch, d_inner, L, N, stream);
 }
 
+#endif
+
+// ---- decode update and conv
+#if SS_PART_IS(3)
+
+ss_status ss_state_update_bf16(float *state, const ss_bf16 *x, const ss_bf16 *delta, const float *A,
+                               const ss_bf16 *B, const ss_bf16 *C, const float *D, const ss_bf16 *z,
+                               ss_bf16 *y, int64_t batch, int64_t d_inner, int64_t N,
+                               cudaStream_t stream)
+{
+    return state_update<__nv_bfloat16>(state, x, delta, A, B, C, D, z, y, batch, d_inner, N, stream);
+}
+
+ss_status ss_state_update_f32(float *state, const float *x, const float *delta, const float *A,
+                              const float *B, const float *C, const float *D, const float *z, float *y,
+                              int64_t batch, int64_t d_inner, int64_t N, cudaStream_t stream)
+{
+    return state_update<float>(state, x, delta, A, B, C, D, z, y, batch, d_inner, N, stream);
+}
+
+ss_status ss_causal_conv1d_bf16(const ss_bf16 *x, const float *w, const float *bias, const ss_bf16 *state_in,
+                                int silu, ss_bf16 *out, ss_bf16 *state_out, int64_t batch, int64_t d_inner,
+                                int64_t L, int64_t k, cudaStream_t stream)
+{
+    return causal_conv1d<__nv_bfloat16>(x, w, bias, state_in, silu, out, state_out, batch, d_inner, L, k, stream);
+}
+
+ss_status ss_causal_conv1d_f32(const float *x, const float *w, const float *bias, const float *state_in, int silu,
+                               float *out, float *state_out, int64_t batch, int64_t d_inner, int64_t L, int64_t k,
+                               cudaStream_t stream)
+{
+    return causal_conv1d<float>(x, w, bias, state_in, silu, out, state_out, batch, d_inner, L, k, stream);
+}
+
+ss_status ss_conv_state_update_bf16(ss_bf16 *conv_state, const ss_bf16 *x, const float *w, const float *bias,
+                                    int silu, ss_bf16 *out, int64_t batch, int64_t d_inner, int64_t k,
+                                    cudaStream_t stream)
+{
+    return conv_state_update<__nv_bfloat16>(conv_state, x, w, bias, silu, out, batch, d_inner, k, stream);
+}
+
+ss_status ss_conv_state_update_f32(float *conv_state, const float *x, const float *w, const float *bias, int silu,
+                                   float *out, int64_t batch, int64_t d_inner, int64_t k, cudaStream_t stream)
+{
+    return conv_state_update<float>(conv_state, x, w, bias, silu, out, batch, d_inner, k, stream);
+}
+
+#endif
+
+// ---- SSD
+#if SS_PART_IS(4)
+
 size_t ss_ssd_workspace_bytes(int64_t batch, int64_t L, int64_t ngroups)
 {
     return ssd_workspace_bytes(batch, L, ngroups);
@@ -250,6 +345,11 @@ ss_status ss_ssd_fwd_bf16(const ss_bf16 *x, const ss_bf16 *dt, const float *A, c
                    batch, L, nheads, headdim, ngroups, N, stream);
 }
 
+#endif
+
+// ---- shared by every part
+#if SS_PART_IS(0)
+
 ss_status ss_device_faults(unsigned int *flags, int clear)
 {
     g_err[0] = '\0';
@@ -257,15 +357,17 @@ ss_status ss_device_faults(unsigned int *flags, int clear)
         return fail(SS_ERR_NULL, "flags is NULL");
     static_assert(SS_FAULT_WAIT_TIMEOUT == kFaultWaitTimeout && SS_FAULT_SMEM_ALIGN == kFaultSmemAlign,
                   "fault bits agree");
+    cudaError_t (*const parts[])(unsigned int *, int) = {ssi::fault_word_fwd, ssi::fault_word_bwd,
+                                                          ssi::fault_word_dec, ssi::fault_word_ssd};
     unsigned int v = 0;
-    cudaError_t e = cudaMemcpyFromSymbol(&v, g_fault_flags, sizeof(v));
-    if (e == cudaSuccess && clear) {
-        const unsigned int none = 0;
-        e = cudaMemcpyToSymbol(g_fault_flags, &none, sizeof(none));
-    }
-    if (e != cudaSuccess) {
-        cudaGetLastError();
-        return fail(SS_ERR_INTERNAL, "reading the device fault word failed: %s", cudaGetErrorString(e));
+    for (auto read : parts) {
+        unsigned int w = 0;
+        const cudaError_t e = read(&w, clear);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return fail(SS_ERR_INTERNAL, "reading the device fault word failed: %s", cudaGetErrorString(e));
+        }
+        v |= w;
     }
     *flags = v;
     return SS_OK;
@@ -274,5 +376,7 @@ ss_status ss_device_faults(unsigned int *flags, int clear)
 const char *ss_last_error(void) { return g_err; }
 
 int ss_abi_version(void) { return SS_ABI_VERSION; }
+
+#endif
 
 }  // extern "C"

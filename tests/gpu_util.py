@@ -44,3 +44,22 @@ def assert_close(got, ref, dtype, what=""):
         "%s: max normalised error %.3f at %s (gpu %r, oracle %r)"
         % (what, err.max(), worst, got[worst], ref[worst]))
     return float(err.max()) if err.size else 0.0
+
+
+def compare_scan_all_rows(inp: dict, y, fs, dtype, block: int = 256, what: str = ""):
+    """Every (batch, channel) row of a GPU scan -- y (batch, d_inner, L) and
+    the final state (batch, d_inner, N), device tensors -- against the oracle,
+    block by block of channels so that host memory stays bounded. Returns the
+    largest normalised error of y and of the final state (1.0 = tolerance)."""
+    batch, d_inner, L = tuple(inp["x"].shape)
+    worst_y = worst_f = 0.0
+    for b in range(batch):
+        for d0 in range(0, d_inner, block):
+            d1 = min(d_inner, d0 + block)
+            rows = [b * d_inner + d for d in range(d0, d1)]
+            yr, fr = O.scan_rows(inp, rows)
+            got_y = y[b, d0:d1].float().cpu().numpy()
+            got_f = fs[b, d0:d1].cpu().numpy()
+            worst_y = max(worst_y, assert_close(got_y, yr, dtype, "%s y b%d d%d..%d" % (what, b, d0, d1)))
+            worst_f = max(worst_f, assert_close(got_f, fr, dtype, "%s final_state b%d d%d..%d" % (what, b, d0, d1)))
+    return worst_y, worst_f

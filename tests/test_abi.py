@@ -68,8 +68,15 @@ def test_library_has_no_torch_dependency(lib):
     assert "torch" not in out and "c10" not in out
 
 
-def test_library_built_for_sm103a():
-    assert build.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
+@pytest.mark.gpu
+def test_library_kernels_are_sm103a_binaries(lib):
+    """The CUDA runtime loads the library's kernels as sm_103 binaries (the
+    module's own record, read through an exported query), not a JIT of PTX."""
+    assert binding.kernel_binary_version() == 103
+
+
+def test_binary_version_query_needs_an_output(lib):
+    assert lib.ss_kernel_binary_version(None) == -1
 
 
 NULL = None
@@ -200,6 +207,12 @@ def test_bwd_noalloc_host_validation(lib, sfx):
     assert call(batch=8, d=1536, L=2048, N=16) == -2
     assert "built-in scratch" in binding.last_error()
     assert binding.scan_bwd_workspace_bytes(8, 1536, 2048, 16) > binding.BWD_NOALLOC_MAX_BYTES
+    # sizes whose element count overflows are rejected before any size product is formed
+    big = 1 << 40
+    assert call(batch=big, d=big, L=big, N=16) == -2
+    assert "overflows" in binding.last_error()
+    assert binding.scan_bwd_workspace_bytes(big, big, big, 16) == 0
+    assert binding.scan_bwd_workspace_bytes(1 << 20, 1 << 20, 1 << 20, 32) == 0
 
 
 @pytest.mark.parametrize("sfx", ["bf16", "f32"])

@@ -1,8 +1,7 @@
 """CUDA path (through the C ABI) against the float64 oracle, element by element.
 
-Small problems are compared in full; the full-size workloads in the launch
-configuration the benchmark uses are compared on sampled rows, which the
-oracle computes one by one. Tolerance: |gpu - oracle| <= atol + rtol |oracle|
+Small problems and the full-size workloads (in the launch configuration the
+benchmark uses) are compared in full, every row and every step. Tolerance: |gpu - oracle| <= atol + rtol |oracle|
 with (rtol, atol) = (2e-2, 1e-3) for bf16 io and (1e-4, 1e-5) for fp32 io,
 for y and for the final state.
 """
@@ -15,7 +14,7 @@ import torch
 from oracle import oracle as O
 from selective_state_space_138_b300 import binding
 from selective_state_space_138_b300 import inputs as I
-from tests.gpu_util import TOL, assert_close, dev, gpu_scan, oracle_scan
+from tests.gpu_util import TOL, assert_close, compare_scan_all_rows, dev, gpu_scan, oracle_scan
 
 pytestmark = pytest.mark.gpu
 
@@ -152,28 +151,22 @@ def test_host_pointer_is_rejected_before_launch():
 
 # ----------------------------------------------------------------- full sizes
 
-def _sample_rows(rows, k, seed):
-    rng = np.random.default_rng(seed)
-    pick = set(rng.choice(rows, size=min(k, rows), replace=False).tolist())
-    pick.update({0, 1, rows - 1})
-    return sorted(pick)
-
-
 @pytest.mark.parametrize("name", [I.MAMBA130M.name, I.MAMBA1P4B.name, I.LONGSEQ.name])
-def test_full_size_workloads_on_sampled_rows(name):
+def test_full_size_workloads_every_row(name):
+    """The three large workloads at full size, in the launch configuration the
+    benchmark times, compared with the oracle on every (batch, channel) row:
+    every step of y and every final state."""
     spec = I.SCAN_WORKLOADS[name]
     inp = I.make_scan_inputs(spec)
     g = dev(inp)
+    binding.device_faults(clear=True)
     y, fs = binding.scan_fwd(g["x"], g["dt"], g["A"], g["B"], g["C"], D=g["D"], z=g["z"],
                              dt_bias=g["dt_bias"])
     torch.cuda.synchronize()
-    rows = _sample_rows(spec.batch * spec.d_inner, 24 if spec.L > 10000 else 64, spec.seed)
-    yr, fr = O.scan_rows(inp, rows)
-    Lq = spec.L
-    y_rows = y.view(-1, Lq)[rows].float().cpu().numpy()
-    f_rows = fs.view(-1, spec.N)[rows].cpu().numpy()
-    assert_close(y_rows, yr, torch.bfloat16, "y")
-    assert_close(f_rows, fr, torch.bfloat16, "final_state")
+    assert binding.device_faults() == 0
+    del g
+    wy, wf = compare_scan_all_rows(inp, y, fs, torch.bfloat16, what=name)
+    print("%s: max normalised error y %.3f, final state %.3f (1.0 = tolerance)" % (name, wy, wf))
 
 
 # ----------------------------------------------------------------- decode
@@ -239,16 +232,24 @@ def test_prefill_scan_then_decode_continues_the_state():
     assert_close(st.cpu().numpy().reshape(-1, 16), fr, torch.bfloat16, "decode state")
 
 
-def test_full_size_decode_on_sampled_rows():
+def test_full_size_decode_every_row_and_step():
+    """The decode workload (batch 256, d_inner 5120, N 16, 1024 tokens) against
+    the oracle's scan over the same tokens, on every (batch, channel) row:
+    y of every step and the state after the last one."""
     spec = I.DECODE
     tok = I.make_decode_tokens(spec)
     par = I.make_decode_params(spec)
+    binding.device_faults(clear=True)
     ys, st = _gpu_decode(tok, par)
-    rows = _sample_rows(spec.batch * spec.d_inner, 96, spec.seed)
-    yr, fr = O.decode_chain(tok, par, rows)
-    got = ys.view(spec.steps, -1)[:, rows].float().cpu().numpy().T
-    assert_close(got, yr, torch.bfloat16, "decode y (every step)")
-    assert_close(st.view(-1, spec.N)[rows].cpu().numpy(), fr, torch.bfloat16, "decode state")
+    assert binding.device_faults() == 0
+    worst_y = worst_s = 0.0
+    for b in range(spec.batch):
+        rows = list(range(b * spec.d_inner, (b + 1) * spec.d_inner))
+        yr, fr = O.decode_chain(tok, par, rows)
+        got = ys[:, b, :].float().cpu().numpy().T
+        worst_y = max(worst_y, assert_close(got, yr, torch.bfloat16, "decode y (every step) b%d" % b))
+        worst_s = max(worst_s, assert_close(st[b].cpu().numpy(), fr, torch.bfloat16, "decode state b%d" % b))
+    print("%s: max normalised error y %.3f, state %.3f (1.0 = tolerance)" % (spec.name, worst_y, worst_s))
 
 
 # ----------------------------------------------------------------- device math probes
