@@ -205,23 +205,24 @@ scan_fwd_kernel(const ScanParams p)
 
 // ------------------------------------------------------------------ n-split scan kernel
 //
-// A CTA owns batch row b and CH = 32 channels, with S warps (S = ceil(N/4),
-// N padded to 4S with A = B = C = 0, which leaves the padded states at zero):
-// warp q holds states 4q..4q+3 of all 32 channels, lane c holding channel c.
-// Every lane walks the whole sequence one step after another, so each
-// element-step costs one exponential and four fp32 multiply(-add)s, done in
-// pairs with the packed f32x2 instructions; time is not split, so no combine
-// work is added.
+// A CTA owns batch row b and CH = 32 channels, with S warps, lane c of every
+// warp serving channel c. Warp q holds NPL consecutive states (8q.. for NPL =
+// 8, 4q.. for NPL = 4) of all 32 channels; N is padded to S*NPL states with
+// A = B = C = 0, which leaves the padded states at zero. Every lane walks the
+// whole sequence one step after another, so each element-step costs one
+// exponential and four fp32 multiply(-add)s, done in pairs with the packed
+// f32x2 instructions; time is not split, so no combine work is added.
 //
-// Shared-memory traffic sets the pace on this part (a 16-byte load by 32
-// lanes takes four shared-memory cycles), so the layout keeps it low: B_t and
-// C_t of a warp's states are the same for all its lanes (a warp-uniform load
-// costs half of a scattered one), the per-step pair (delta, delta*x) is 8
-// bytes, and the raw tiles are read with conflict-free 16-byte loads.
+// Shared-memory delivery and issue slots set the pace on this part, so the
+// layout keeps both low: B_t and C_t of a warp's states are the same for all
+// its lanes (a warp-uniform load), a lane reads the (delta, delta*x) of two
+// steps in one 16-byte load, and NPL = 8 states per lane share each of those
+// loads and the lane's per-step bookkeeping (N > 8; NPL = 4 for N <= 8 keeps
+// more warps per SM).
 //
 // The sequence is cut into chunks of LC = 32 steps. Per chunk k:
-//   scan      lane c of warp q advances its 4 states over the chunk (decays of
-//             the next AHEAD steps formed ahead of the state update) and
+//   scan      lane c of warp q advances its NPL states over the chunk (decays
+//             of the next AHEAD steps formed ahead of the state update) and
 //             keeps its partial readouts sum over its states of C_t[n] h_t[n]
 //             in registers, storing them when the chunk is done;
 //   -- barrier --
@@ -231,11 +232,11 @@ scan_fwd_kernel(const ScanParams p)
 //             and delta*x for its steps of chunk k+1, and B, C of chunk k+1
 //             are converted to fp32 [t][n];
 //   -- barrier --
-// The raw x, dt, z, B, C tiles of every chunk are copied into a ring of
-// STAGES chunks with cp.async (16-byte pieces, zero fill past the ends) three
-// chunks ahead of their use, so DRAM latency hides behind three iterations.
-// The per-step work (softplus, gate, conversions) is done once per (channel,
-// step), two steps at a time with f32x2 arithmetic.
+// The raw x, dt, z, B, C tiles of every chunk are brought into a ring of
+// STAGES chunks (tensor copies, or cp.async pieces for rows that are not
+// 16-byte aligned) three chunks ahead of their use, so DRAM latency hides
+// behind three iterations. The per-step work (softplus, gate, conversions)
+// is done once per (channel, step), two steps at a time with f32x2 arithmetic.
 
 #ifndef SS_NSPLIT_AHEAD
 #define SS_NSPLIT_AHEAD 4  // steps whose decays are formed ahead of the state update
@@ -244,11 +245,17 @@ scan_fwd_kernel(const ScanParams p)
 #define SS_NSPLIT_STAGES 4  // raw chunks resident in shared memory: k .. k+3 (a power of two)
 #endif
 
-template <typename T, int S>
+// row stride (floats) of the fp32 B, C tiles [t][n]: 16-byte rows, and the
+// conversion's 16-byte stores (lanes over 4-state groups, then step pairs)
+// spread over all banks
+constexpr int nsplit_bc_stride(int ns) { return ns <= 4 ? 8 : (ns == 8 ? 12 : ns + 8); }
+
+template <typename T, int S, int NPL>
 struct NSplitShape {
     static constexpr int CH = 32;                 // channels per CTA
     static constexpr int NT = CH * S;             // threads per CTA
-    static constexpr int NS = 4 * S;              // padded states
+    static constexpr int NS = NPL * S;            // padded states
+    static constexpr int NSP = nsplit_bc_stride(NS);
     static constexpr int LC = 32;                 // steps per chunk
     static constexpr int RL = LC / S;             // steps per epilogue/prep thread
     static constexpr int STAGES = SS_NSPLIT_STAGES;
@@ -262,16 +269,17 @@ struct NSplitShape {
     static constexpr int PPT = (NPIECE + NT - 1) / NT;    // raw pieces per thread
     static constexpr int YROW = LC + 4;           // floats per partial row (conflict-free)
     static constexpr int YQ = CH * YROW;          // floats per state group
-    static constexpr int PD_BYTES = LC * CH * 8;
-    static constexpr int BC_BYTES = LC * NS * 4;
+    static constexpr int PD_BYTES = (LC / 2) * CH * 16;   // (delta, delta x) of step pairs, [t/2][c]
+    static constexpr int BC_BYTES = LC * NSP * 4;
     static constexpr int Y_BYTES = S * YQ * 4;
-    static constexpr int X_BYTES = S * CH * 16 + S * CH * 4;   // segment end states and step sums
-    static constexpr int R_BYTES = LC + 16;                     // sequence starts of a chunk, segment flag
+    static constexpr int X_BYTES = S * CH * NPL * 4 + S * CH * 4;   // segment end states and step sums
+    static constexpr int R_BYTES = LC + 16;                          // sequence starts of a chunk, segment flag
     static constexpr size_t BAR_OFF = ((size_t)STAGES * STAGE_BYTES + PD_BYTES + 2 * BC_BYTES + Y_BYTES + X_BYTES +
                                        R_BYTES + 7) / 8 * 8;
     static constexpr size_t BYTES = BAR_OFF + 8 * STAGES;   // + the stage barriers
     static_assert(STAGE_BYTES % 128 == 0 && RAW_X % 128 == 0 && RAW_BC % 128 == 0, "tensor-copy tiles 128-aligned");
-    static_assert(RL % 2 == 0, "steps are processed in pairs");
+    static_assert(RL % 4 == 0, "epilogue runs are read 4 steps at a time");
+    static_assert(NPL == 4 || NPL == 8, "states per lane");
 };
 
 // REV: the recurrence runs from t = L-1 down to 0 (h_t = a_t h_{t+1} + delta_t
@@ -283,28 +291,31 @@ struct NSplitShape {
 // TMA: the chunks arrive by tensor copies (the maps in p are encoded); the
 // cp.async form is a separate instantiation, so neither carries the other's
 // registers.
-template <typename T, int S, bool REV, bool RST, bool TMA>
-__global__ void __launch_bounds__(NSplitShape<T, S>::NT, NSplitShape<T, S>::NT <= 128 ? 3 : 1)
+template <typename T, int S, int NPL, bool REV, bool RST, bool TMA>
+__global__ void __launch_bounds__(NSplitShape<T, S, NPL>::NT,
+                                  NPL == 8 ? (S <= 2 ? 4 : 2) : (S <= 2 ? 4 : (S == 4 ? 3 : 1)))
 scan_nsplit_kernel(const __grid_constant__ ScanParams p)
 {
-    using SH = NSplitShape<T, S>;
-    constexpr int NT = SH::NT, CH = SH::CH, NS = SH::NS, LC = SH::LC, RL = SH::RL, PR = SH::PR;
+    using SH = NSplitShape<T, S, NPL>;
+    constexpr int NT = SH::NT, CH = SH::CH, NS = SH::NS, NSP = SH::NSP, LC = SH::LC, RL = SH::RL, PR = SH::PR;
     constexpr int STAGES = SH::STAGES, EPP = SH::EPP, PPT = SH::PPT;
     constexpr int D = SS_NSPLIT_AHEAD;
+    constexpr int P = NPL / 2;                    // state pairs per lane
+    constexpr int G4 = NPL / 4;                   // 4-state groups per lane
     constexpr int RW = RL * (int)sizeof(T) / 4;   // 32-bit words per prep/epilogue run
     static_assert(LC % 4 == 0 && D >= 1 && D <= LC, "chunk shape");
 
     extern __shared__ __align__(128) unsigned char smem_tiles[];
     unsigned char *smem_raw = smem_tiles;
-    unsigned char *raw = smem_raw;                                          // [STAGES][x, dt, z, B, C]
-    u64 *Pd = reinterpret_cast<u64 *>(smem_raw + STAGES * SH::STAGE_BYTES);  // [LC][CH] (delta, delta x)
-    float *Bf = reinterpret_cast<float *>(Pd + LC * CH);                    // [LC][NS]
-    float *Cf = Bf + LC * NS;                                               // [LC][NS]
-    float *Yp = Cf + LC * NS;                                               // [S][CH][YROW]
-    float4 *Hx = reinterpret_cast<float4 *>(Yp + S * SH::YQ);               // [S][CH] segment end states
-    float *Sx = reinterpret_cast<float *>(Hx + S * CH);                     // [S][CH] step sums
-    unsigned char *Rst = reinterpret_cast<unsigned char *>(Sx + S * CH);    // [LC] sequence starts
-    int *Rx = reinterpret_cast<int *>(Rst + LC);                            // any start in the segment
+    unsigned char *raw = smem_raw;                                             // [STAGES][x, dt, z, B, C]
+    float4 *Pd = reinterpret_cast<float4 *>(smem_raw + STAGES * SH::STAGE_BYTES);  // [LC/2][CH] step pairs
+    float *Bf = reinterpret_cast<float *>(Pd + (LC / 2) * CH);                 // [LC][NSP]
+    float *Cf = Bf + LC * NSP;                                                 // [LC][NSP]
+    float *Yp = Cf + LC * NSP;                                                 // [S][CH][YROW]
+    float4 *Hx = reinterpret_cast<float4 *>(Yp + S * SH::YQ);                  // [S][CH][G4] segment end states
+    float *Sx = reinterpret_cast<float *>(Hx + S * CH * G4);                   // [S][CH] step sums
+    unsigned char *Rst = reinterpret_cast<unsigned char *>(Sx + S * CH);       // [LC] sequence starts
+    int *Rx = reinterpret_cast<int *>(Rst + LC);                               // any start in the segment
     const uint32_t raw_s = static_cast<uint32_t>(__cvta_generic_to_shared(raw));
     const uint32_t bars_s = raw_s + static_cast<uint32_t>(SH::BAR_OFF);   // [STAGES] "stage filled" barriers
     constexpr bool tma = TMA;
@@ -327,7 +338,7 @@ scan_nsplit_kernel(const __grid_constant__ ScanParams p)
     // chunk j in walking order sits at chunk phys(j) of the segment
     auto phys = [&](int64_t j) -> int64_t { return REV ? nchunks - 1 - j : j; };
 
-    // scan role: channel cs = lane, state group q = warp
+    // scan role: channel cs = lane, states NPL*q .. NPL*q + NPL-1
     const int cs = tid % CH;
     const int q = tid / CH;
     const bool act_s = d0 + cs < Dn;
@@ -343,15 +354,17 @@ scan_nsplit_kernel(const __grid_constant__ ScanParams p)
     const u64 D2 = splat((p.D && act_e) ? __ldg(p.D + de) : 0.0f);
     const bool gate = p.z != nullptr;
 
-    float A2[4];
+    u64 A2p[P];   // (A_n, A_n+1) log2(e) of the lane's states
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        const int n = 4 * q + e;
-        A2[e] = (n < N) ? __ldg(p.A + ds * N + n) * kLog2e : 0.0f;
+    for (int i = 0; i < P; ++i) {
+        const int n = NPL * q + 2 * i;
+        A2p[i] = pk((n < N) ? __ldg(p.A + ds * N + n) * kLog2e : 0.0f,
+                    (n + 1 < N) ? __ldg(p.A + ds * N + n + 1) * kLog2e : 0.0f);
     }
-    const u64 A01 = pk(A2[0], A2[1]);
-    const u64 A23 = pk(A2[2], A2[3]);
-    u64 h01 = 0, h23 = 0;   // +0.0f in both halves
+    u64 h[P];
+#pragma unroll
+    for (int i = 0; i < P; ++i)
+        h[i] = 0;   // +0.0f in both halves
 
     // the raw pieces this thread copies: source row pointer, element offset
     // within the chunk, shared-memory offset within a stage, whether the piece
@@ -473,27 +486,37 @@ scan_nsplit_kernel(const __grid_constant__ ScanParams p)
         cp_async_commit();
     };
 
-    // raw B (and C) of chunk j -> fp32 [t][n]: each item is (tensor, step t,
-    // states 4g..4g+3), written as one 16-byte word
+    // raw B (and C) of chunk j -> fp32 [t][n]: each item is (tensor, step
+    // pair, 4-state group): four 2-step reads of the raw rows, written as two
+    // 16-byte words (lanes run over the groups first, then the step pairs, so
+    // that the stores of a quarter-warp cover every bank once)
     auto convert_bc = [&](int64_t j, bool readout) {
         const unsigned char *st = raw + stage_of(g0 + j) * SH::STAGE_BYTES + 3 * SH::RAW_X;
-        const int items = (readout ? 2 : 1) * LC * S;
+        constexpr int GN = NS / 4;
+        constexpr int TPN = LC / 2;
+        const int items = (readout ? 2 : 1) * TPN * GN;
         for (int w = tid; w < items; w += NT) {
-            const int m = w / (LC * S);
-            const int t = (w % (LC * S)) / S;
-            const int g = w % S;
-            const T *srcm = reinterpret_cast<const T *>(st + m * SH::RAW_BC);
-            float v[4];
+            const int g = w % GN;
+            const int tp = (w / GN) % TPN;
+            const int m = w / (GN * TPN);
+            const unsigned char *srcm = st + m * SH::RAW_BC;
+            float lo[4], hi[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                if constexpr (sizeof(T) == 4)
-                    v[e] = srcm[(4 * g + e) * LC + t];
-                else
-                    v[e] = __uint_as_float(static_cast<uint32_t>(
-                                               reinterpret_cast<const unsigned short *>(srcm)[(4 * g + e) * LC + t])
-                                           << 16);
+                const int n = 4 * g + e;
+                if constexpr (sizeof(T) == 4) {
+                    const float2 v = *reinterpret_cast<const float2 *>(srcm + (n * LC + 2 * tp) * 4);
+                    lo[e] = v.x;
+                    hi[e] = v.y;
+                } else {
+                    const uint32_t v = *reinterpret_cast<const uint32_t *>(srcm + (n * LC + 2 * tp) * 2);
+                    lo[e] = bf16lo(v);
+                    hi[e] = bf16hi(v);
+                }
             }
-            *reinterpret_cast<float4 *>((m == 0 ? Bf : Cf) + t * NS + 4 * g) = make_float4(v[0], v[1], v[2], v[3]);
+            float *dst = (m == 0 ? Bf : Cf) + (2 * tp) * NSP + 4 * g;
+            *reinterpret_cast<float4 *>(dst) = make_float4(lo[0], lo[1], lo[2], lo[3]);
+            *reinterpret_cast<float4 *>(dst + NSP) = make_float4(hi[0], hi[1], hi[2], hi[3]);
         }
     };
 
@@ -506,7 +529,7 @@ scan_nsplit_kernel(const __grid_constant__ ScanParams p)
         ssum = tv;
     };
 
-    // delta and delta*x of this thread's steps of chunk j
+    // delta and delta*x of this thread's steps of chunk j, stored by step pair
     auto prep = [&](int64_t j, bool sum_steps) {
         const unsigned char *st = raw + stage_of(g0 + j) * SH::STAGE_BYTES;
         uint32_t xw[RW], dw[RW];
@@ -533,14 +556,24 @@ scan_nsplit_kernel(const __grid_constant__ ScanParams p)
             }
             float sx0, sx1;
             upk(mul2(pk(s0, s1), xx), sx0, sx1);
-            Pd[(re * RL + i) * CH + ce] = pk(s0, sx0);
-            Pd[(re * RL + i + 1) * CH + ce] = pk(s1, sx1);
+            Pd[((re * RL + i) >> 1) * CH + ce] = make_float4(s0, sx0, s1, sx1);
         }
     };
 
     float *yq_s = Yp + q * SH::YQ + cs * SH::YROW;   // this lane's partial readouts
-    const float *Bq_s = Bf + 4 * q;                   // this warp's states of B_t, C_t
-    const float *Cq_s = Cf + 4 * q;
+    const float *Bq_s = Bf + NPL * q;                 // this warp's states of B_t, C_t
+    const float *Cq_s = Cf + NPL * q;
+
+    // the lane's states as NPL/4 words of 4
+    auto store_groups = [&](float4 *dst, int64_t stride) {
+#pragma unroll
+        for (int gq = 0; gq < G4; ++gq) {
+            float hv[4];
+            upk(h[2 * gq], hv[0], hv[1]);
+            upk(h[2 * gq + 1], hv[2], hv[3]);
+            dst[gq * stride] = make_float4(hv[0], hv[1], hv[2], hv[3]);
+        }
+    };
 
     // walk the segment [t_lo, t_hi): with the readout (y stored) or without
     // it (state and step sum only)
@@ -567,58 +600,76 @@ scan_nsplit_kernel(const __grid_constant__ ScanParams p)
             else
                 cp_async_commit();
 
-            // ---- scan: 4 states of channel cs over the chunk; the decays and
-            // writes of step t + D are formed while the state takes step t
+            // ---- scan: the lane's NPL states of channel cs over the chunk;
+            // the decays and writes of step t + D are formed while the state
+            // takes step t
             {
-                u64 ra01[D], ra23[D], rb01[D], rb23[D];
+                u64 ra[D][P], rb[D][P];
                 float yv[LC];
-                auto form = [&](int t, int slot) {
-                    float dl, dx;
-                    upk(Pd[t * CH + cs], dl, dx);
-                    const ulonglong2 Bq = *reinterpret_cast<const ulonglong2 *>(Bq_s + t * NS);
-                    const u64 dd = splat(dl);
-                    const u64 xx = splat(dx);
-                    ra01[slot] = ex2_2(mul2(dd, A01));
-                    ra23[slot] = ex2_2(mul2(dd, A23));
-                    rb01[slot] = mul2(xx, Bq.x);
-                    rb23[slot] = mul2(xx, Bq.y);
-                };
+                float4 pdv = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
                 // walking step u is chunk step t = tu(u)
                 auto tu = [](int u) { return REV ? LC - 1 - u : u; };
+                auto form = [&](int u, int slot) {
+                    const int t = tu(u);
+                    if ((u & 1) == 0)   // the first step of a pair in walking order loads the pair
+                        pdv = Pd[(t >> 1) * CH + cs];
+                    const u64 dd = splat((t & 1) ? pdv.z : pdv.x);
+                    const u64 xx = splat((t & 1) ? pdv.w : pdv.y);
+                    const float *bt = Bq_s + t * NSP;
+#pragma unroll
+                    for (int i = 0; i < P; i += 2) {
+                        const ulonglong2 Bq = *reinterpret_cast<const ulonglong2 *>(bt + 2 * i);
+                        ra[slot][i] = ex2_2(mul2(dd, A2p[i]));
+                        ra[slot][i + 1] = ex2_2(mul2(dd, A2p[i + 1]));
+                        rb[slot][i] = mul2(xx, Bq.x);
+                        rb[slot][i + 1] = mul2(xx, Bq.y);
+                    }
+                };
 #pragma unroll
                 for (int i = 0; i < D; ++i)
-                    form(tu(i), i);
+                    form(i, i);
 #pragma unroll
                 for (int u = 0; u < LC; ++u) {
                     const int t = tu(u);
                     const int slot = u % D;
-                    const u64 a01 = ra01[slot], a23 = ra23[slot], b01 = rb01[slot], b23 = rb23[slot];
-                    if (u + D < LC)
-                        form(tu(u + D), slot);
-                    if (RST && !REV && Rst[t]) {   // a sequence starts at t: nothing carries in
-                        h01 = 0;
-                        h23 = 0;
+                    u64 a[P], bb[P];
+#pragma unroll
+                    for (int i = 0; i < P; ++i) {
+                        a[i] = ra[slot][i];
+                        bb[i] = rb[slot][i];
                     }
-                    h01 = fma2(a01, h01, b01);
-                    h23 = fma2(a23, h23, b23);
+                    if (u + D < LC)
+                        form(u + D, slot);
+                    if (RST && !REV && Rst[t]) {   // a sequence starts at t: nothing carries in
+#pragma unroll
+                        for (int i = 0; i < P; ++i)
+                            h[i] = 0;
+                    }
+#pragma unroll
+                    for (int i = 0; i < P; ++i)
+                        h[i] = fma2(a[i], h[i], bb[i]);
                     if constexpr (RO) {
-                        const ulonglong2 Cq = *reinterpret_cast<const ulonglong2 *>(Cq_s + t * NS);
-                        yv[t] = hsum(fma2(Cq.y, h23, mul2(Cq.x, h01)));
+                        const float *ct = Cq_s + t * NSP;
+                        u64 acc = 0;
+#pragma unroll
+                        for (int i = 0; i < P; i += 2) {
+                            const ulonglong2 Cq = *reinterpret_cast<const ulonglong2 *>(ct + 2 * i);
+                            acc = (i == 0) ? mul2(Cq.x, h[i]) : fma2(Cq.x, h[i], acc);
+                            acc = fma2(Cq.y, h[i + 1], acc);
+                        }
+                        yv[t] = hsum(acc);
                     }
                     if (RST && REV && Rst[t]) {    // a sequence starts at t: nothing carries to t-1
-                        h01 = 0;
-                        h23 = 0;
+#pragma unroll
+                        for (int i = 0; i < P; ++i)
+                            h[i] = 0;
                     }
                     if constexpr (RO && !REV && !RST) {
                         // the state entering each 16-step sub-chunk, for the backward pass
                         if ((u == 15 || u == 31) && p.ckpt && act_s) {
                             const int64_t sc = (t0 + u + 1) / 16;
-                            if (sc < p.nsub) {
-                                float hv[4];
-                                upk(h01, hv[0], hv[1]);
-                                upk(h23, hv[2], hv[3]);
-                                p.ckpt[((b * p.nsub + sc) * S + q) * Dn + ds] = make_float4(hv[0], hv[1], hv[2], hv[3]);
-                            }
+                            if (sc < p.nsub)
+                                store_groups(p.ckpt + ((b * p.nsub + sc) * (NS / 4) + G4 * q) * Dn + ds, Dn);
                         }
                     }
                 }
@@ -642,16 +693,23 @@ scan_nsplit_kernel(const __grid_constant__ ScanParams p)
                     read_run_raw<T, RL>(st + 2 * SH::RAW_X + ce * SH::ROWB, re * RL, zw);
                 float out[RL];
 #pragma unroll
-                for (int i = 0; i < RL; i += 2) {
+                for (int i = 0; i < RL; i += 4) {
                     const float *yp = Yp + ce * SH::YROW + re * RL + i;
-                    u64 acc = *reinterpret_cast<const u64 *>(yp);
+                    ulonglong2 acc = *reinterpret_cast<const ulonglong2 *>(yp);
 #pragma unroll
-                    for (int qq = 1; qq < S; ++qq)
-                        acc = add2(acc, *reinterpret_cast<const u64 *>(yp + qq * SH::YQ));
-                    acc = fma2(D2, word_pair<T>(xw, i), acc);
-                    if (gate)
-                        acc = mul2(acc, silu2(word_pair<T>(zw, i)));
-                    upk(acc, out[i], out[i + 1]);
+                    for (int qq = 1; qq < S; ++qq) {
+                        const ulonglong2 v = *reinterpret_cast<const ulonglong2 *>(yp + qq * SH::YQ);
+                        acc.x = add2(acc.x, v.x);
+                        acc.y = add2(acc.y, v.y);
+                    }
+                    acc.x = fma2(D2, word_pair<T>(xw, i), acc.x);
+                    acc.y = fma2(D2, word_pair<T>(xw, i + 2), acc.y);
+                    if (gate) {
+                        acc.x = mul2(acc.x, silu2(word_pair<T>(zw, i)));
+                        acc.y = mul2(acc.y, silu2(word_pair<T>(zw, i + 2)));
+                    }
+                    upk(acc.x, out[i], out[i + 1]);
+                    upk(acc.y, out[i + 2], out[i + 3]);
                 }
                 if (act_e)
                     write_run<T, RL>(yr, t0 + re * RL, t_hi, vec, out);
@@ -669,15 +727,17 @@ scan_nsplit_kernel(const __grid_constant__ ScanParams p)
     };
 
     // the initial state (zero unless given)
-    u64 g01 = 0, g23 = 0;
+    u64 g0h[P];
+#pragma unroll
+    for (int i = 0; i < P; ++i)
+        g0h[i] = 0;
     if (p.h0 && act_s) {
         const float *hp = p.h0 + (b * Dn + ds) * N;
-        float hv[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-            hv[e] = (4 * q + e < N) ? hp[4 * q + e] : 0.0f;
-        g01 = pk(hv[0], hv[1]);
-        g23 = pk(hv[2], hv[3]);
+        for (int i = 0; i < P; ++i) {
+            const int n = NPL * q + 2 * i;
+            g0h[i] = pk(n < N ? hp[n] : 0.0f, n + 1 < N ? hp[n + 1] : 0.0f);
+        }
     }
     if (nseg > 1) {
         // Segments of one channel group form a thread-block cluster. Each
@@ -699,13 +759,13 @@ scan_nsplit_kernel(const __grid_constant__ ScanParams p)
         has_start = __syncthreads_or(has_start);
         if (tid == 0)
             *Rx = has_start;
-        float hv[4];
-        upk(h01, hv[0], hv[1]);
-        upk(h23, hv[2], hv[3]);
-        Hx[q * CH + cs] = make_float4(hv[0], hv[1], hv[2], hv[3]);
+        store_groups(Hx + (q * CH + cs) * G4, 1);
         Sx[re * CH + ce] = ssum;
         cluster.sync();
-        u64 f01 = g01, f23 = g23;
+        u64 f[P];
+#pragma unroll
+        for (int i = 0; i < P; ++i)
+            f[i] = g0h[i];
         const int n_before = REV ? nseg - 1 - seg : seg;
         for (int i = 0; i < n_before; ++i) {
             const int sp = REV ? nseg - 1 - i : i;
@@ -715,39 +775,44 @@ scan_nsplit_kernel(const __grid_constant__ ScanParams p)
 #pragma unroll
             for (int r = 0; r < S; ++r)
                 tot += psum[r * CH + cs];
-            const float4 he = ph[q * CH + cs];
-            u64 a01 = ex2_2(mul2(splat(tot), A01)), a23 = ex2_2(mul2(splat(tot), A23));
-            if (RST && *cluster.map_shared_rank(Rx, sp)) {
-                a01 = 0;
-                a23 = 0;
+            const bool cut = RST && *cluster.map_shared_rank(Rx, sp);
+#pragma unroll
+            for (int gq = 0; gq < G4; ++gq) {
+                const float4 he = ph[(q * CH + cs) * G4 + gq];
+                u64 a01 = ex2_2(mul2(splat(tot), A2p[2 * gq])), a23 = ex2_2(mul2(splat(tot), A2p[2 * gq + 1]));
+                if (cut) {
+                    a01 = 0;
+                    a23 = 0;
+                }
+                f[2 * gq] = fma2(a01, f[2 * gq], pk(he.x, he.y));
+                f[2 * gq + 1] = fma2(a23, f[2 * gq + 1], pk(he.z, he.w));
             }
-            f01 = fma2(a01, f01, pk(he.x, he.y));
-            f23 = fma2(a23, f23, pk(he.z, he.w));
         }
         cluster.sync();   // peers have finished reading this CTA's end state
-        h01 = f01;
-        h23 = f23;
+#pragma unroll
+        for (int i = 0; i < P; ++i)
+            h[i] = f[i];
     } else {
-        h01 = g01;
-        h23 = g23;
+#pragma unroll
+        for (int i = 0; i < P; ++i)
+            h[i] = g0h[i];
     }
-    if (!REV && !RST && p.ckpt && act_s && seg == 0) {   // the state entering sub-chunk 0
-        float hv[4];
-        upk(h01, hv[0], hv[1]);
-        upk(h23, hv[2], hv[3]);
-        p.ckpt[((b * p.nsub) * S + q) * Dn + ds] = make_float4(hv[0], hv[1], hv[2], hv[3]);
-    }
+    if (!REV && !RST && p.ckpt && act_s && seg == 0)   // the state entering sub-chunk 0
+        store_groups(p.ckpt + ((b * p.nsub) * (NS / 4) + G4 * q) * Dn + ds, Dn);
     run(Flag<true>{});
 
     if (p.final_state && act_s && seg == (REV ? 0 : nseg - 1)) {
         float *fs = p.final_state + (b * Dn + ds) * N;
-        float hv[4];
-        upk(h01, hv[0], hv[1]);
-        upk(h23, hv[2], hv[3]);
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-            if (4 * q + e < N)
-                fs[4 * q + e] = hv[e];
+        for (int i = 0; i < P; ++i) {
+            const int n = NPL * q + 2 * i;
+            float h0v, h1v;
+            upk(h[i], h0v, h1v);
+            if (n < N)
+                fs[n] = h0v;
+            if (n + 1 < N)
+                fs[n + 1] = h1v;
+        }
     }
     if (tma && tid == 0)   // after a wait gave up: let the copies issued since land (each wait bounded)
         for (int64_t g = g_done; g < g_issued; ++g)
@@ -840,7 +905,7 @@ bool encode_scan_maps(ScanParams &p)
     const char *env = getenv("SS_SCAN_TMA");
     if (env && strcmp(env, "0") == 0)
         return false;
-    using SH = NSplitShape<T, 1>;   // CH, LC and the raw row do not depend on the state split
+    using SH = NSplitShape<T, 1, 4>;   // CH, LC and the raw row do not depend on the state split
     const uint32_t ns = p.N <= 4 ? 4u : (p.N <= 8 ? 8u : (p.N <= 16 ? 16u : 32u));
     const uint32_t row_t = SH::ROWB / sizeof(T);
     bool ok = encode_rows_map<T>(&p.tm_x, p.x, p.L, p.d_inner, p.batch, row_t, SH::CH) &&
@@ -852,11 +917,12 @@ bool encode_scan_maps(ScanParams &p)
     return ok;
 }
 
-template <typename T, int S, bool REV, bool RST>
+template <typename T, int S, int NPL, bool REV, bool RST>
 ss_status launch_nsplit(const ScanParams &p0, cudaStream_t stream, int sms)
 {
-    using SH = NSplitShape<T, S>;
-    auto kernel = p0.tma ? scan_nsplit_kernel<T, S, REV, RST, true> : scan_nsplit_kernel<T, S, REV, RST, false>;
+    using SH = NSplitShape<T, S, NPL>;
+    auto kernel = p0.tma ? scan_nsplit_kernel<T, S, NPL, REV, RST, true>
+                         : scan_nsplit_kernel<T, S, NPL, REV, RST, false>;
     const size_t smem = SH::BYTES;
     if (smem > 48u * 1024u) {
         cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -916,13 +982,19 @@ ss_status launch_nsplit(const ScanParams &p0, cudaStream_t stream, int sms)
     return SS_OK;
 }
 
+// (warps, states per lane) by N: 4 states per lane, so that a 32-channel
+// group runs on ceil(N/4) warps (more warps per SM measured faster than 8
+// states per lane on 2 warps); SS_SCAN_NPL=8 selects 8 states per lane for
+// 8 < N <= 32.
 template <typename T, bool REV, bool RST>
 ss_status dispatch_nsplit_n(const ScanParams &p, cudaStream_t s, int sms)
 {
-    if (p.N <= 4) return launch_nsplit<T, 1, REV, RST>(p, s, sms);
-    if (p.N <= 8) return launch_nsplit<T, 2, REV, RST>(p, s, sms);
-    if (p.N <= 16) return launch_nsplit<T, 4, REV, RST>(p, s, sms);
-    return launch_nsplit<T, 8, REV, RST>(p, s, sms);
+    if (p.N <= 4) return launch_nsplit<T, 1, 4, REV, RST>(p, s, sms);
+    if (p.N <= 8) return launch_nsplit<T, 2, 4, REV, RST>(p, s, sms);
+    const char *env = getenv("SS_SCAN_NPL");
+    const bool npl8 = env && strcmp(env, "8") == 0;
+    if (p.N <= 16) return npl8 ? launch_nsplit<T, 2, 8, REV, RST>(p, s, sms) : launch_nsplit<T, 4, 4, REV, RST>(p, s, sms);
+    return npl8 ? launch_nsplit<T, 4, 8, REV, RST>(p, s, sms) : launch_nsplit<T, 8, 4, REV, RST>(p, s, sms);
 }
 
 template <typename T>

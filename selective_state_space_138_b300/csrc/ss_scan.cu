@@ -185,7 +185,7 @@ ss_status ss_kernel_binary_version(int *binary_version)
     if (!binary_version)
         return fail(SS_ERR_NULL, "binary_version is NULL");
     cudaFuncAttributes a{};
-    const cudaError_t e = cudaFuncGetAttributes(&a, scan_nsplit_kernel<__nv_bfloat16, 4, false, false, true>);
+    const cudaError_t e = cudaFuncGetAttributes(&a, scan_nsplit_kernel<__nv_bfloat16, 4, 4, false, false, true>);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return fail(SS_ERR_INTERNAL, "cudaFuncGetAttributes failed: %s", cudaGetErrorString(e));
