@@ -41,6 +41,8 @@ struct SsdParams {
     // B, C over (G*N, L, batch) with a box of N + 8 x Q; C B^T over (Q, Q, batch*nchunks*G) with
     // a box of Q + 8 x Q. The 8 extra columns fill each shared-memory row's pad (never read).
     CUtensorMap tm_x, tm_B, tm_C, tm_cb;
+    // B, C over (G*N, L, batch) with a box of 64 states x 128 steps, 128-byte swizzled (the C B^T product)
+    CUtensorMap tm_Bsw, tm_Csw;
 };
 
 // ---- warp-level MMA helpers (PTX mma.sync / ldmatrix; operands in shared memory)
@@ -166,6 +168,185 @@ ssd_cb_kernel(const SsdParams p)
         *reinterpret_cast<uint32_t *>(out + (16 * w + gr) * Q + col) = pack_bf16x2(acc[j][0], acc[j][1]);
         *reinterpret_cast<uint32_t *>(out + (16 * w + gr + 8) * Q + col) = pack_bf16x2(acc[j][2], acc[j][3]);
     }
+}
+
+// ---- 5th-generation tensor cores (tcgen05): the accumulator lives in tensor
+// memory (TMEM, 128 lanes x 512 32-bit columns per SM), operands are read from
+// shared memory through 64-bit matrix descriptors, one thread issues the MMA
+// and its completion arrives on an mbarrier.
+
+// K-major bf16 operand tile stored as TMA writes it with the 128-byte swizzle:
+// rows of 64 elements (128 bytes), 8-row groups of 1024 bytes. Fields: start
+// address >> 4 (bits 0-13), leading offset (unused for this layout, 1),
+// stride between 8-row groups >> 4 (bits 32-45), descriptor version 1 (bit
+// 46), swizzle mode 2 = 128-byte (bits 61-63). The tile must start on a
+// 1024-byte boundary; the K slice k (16 elements) of a row starts 32 k bytes
+// in, which the swizzle maps through the address bits.
+__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t smem_addr)
+{
+    return static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>(1) << 16) |
+           (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
+           (static_cast<uint64_t>(2) << 61);
+}
+
+// instruction descriptor of kind::f16 with bf16 A and B, fp32 D, both
+// operands K-major: D format (bits 4-5) = 1, A format (7-9) = 1, B format
+// (10-12) = 1, N >> 3 (17-22), M >> 4 (24-28)
+__host__ __device__ constexpr uint32_t umma_idesc_bf16(int M, int N)
+{
+    return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+           (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// D (tmem) (+)= A (smem desc) * B (smem desc)^T, issued by one thread
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          bool accumulate)
+{
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "setp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+                 ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1 : 0)
+                 : "memory");
+}
+
+// arrive on the mbarrier once every MMA issued so far by this thread has completed
+__device__ __forceinline__ void umma_commit(uint32_t bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+// tensor-memory allocation by one whole warp: the base address is written to shared memory at dst
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// 16 consecutive 32-bit columns of this thread's lane (warp w reads lanes 32w .. 32w+31)
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t *v)
+{
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, "
+                 "%13, %14, %15}, [%16];"
+                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+                   "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]),
+                   "=r"(v[15])
+                 : "r"(taddr)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// ---- CB_c = C_c B_c^T on the tcgen05 tensor cores: one CTA (4 warps) per
+// (pair of chunks, batch, group). The 128 steps of two chunks are the M rows
+// (C) and the N columns (B) of one 128 x 128 product over K = N states,
+// accumulated in tensor memory; the two diagonal 64 x 64 blocks are the
+// chunks' C B^T, read back lane by lane and stored in bf16.
+template <int N>
+struct SsdCbShape {
+    static constexpr int ATOMS = N / 64;                 // 64-element (128-byte) K slices
+    static constexpr int TILE = 128 * 128;               // one [128 rows][64] bf16 slice, bytes
+    static constexpr int A_OFF = 0;                      // C rows, ATOMS slices
+    static constexpr int B_OFF = ATOMS * TILE;           // B rows, ATOMS slices
+    static constexpr int BAR_OFF = 2 * ATOMS * TILE;     // tile barrier, MMA barrier
+    static constexpr int TMEM_OFF = BAR_OFF + 16;        // the allocated tensor-memory address
+    static constexpr size_t BYTES = TMEM_OFF + 16 + 1024;   // + room to align the base to 1024 bytes
+};
+
+template <int N>
+__global__ void __launch_bounds__(128, 1)
+ssd_cb_tc_kernel(const __grid_constant__ SsdParams p)
+{
+    using SH = SsdCbShape<N>;
+    constexpr int Q = kSsdQ;
+    extern __shared__ __align__(1024) unsigned char smem_cb[];
+    const uint32_t raw_s = static_cast<uint32_t>(__cvta_generic_to_shared(smem_cb));
+    const uint32_t base_s = (raw_s + 1023u) & ~1023u;   // 128-byte swizzled tiles on 1024-byte boundaries
+    unsigned char *base = smem_cb + (base_s - raw_s);
+    const uint32_t bar_tile = base_s + SH::BAR_OFF, bar_mma = bar_tile + 8;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(base + SH::TMEM_OFF);
+
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    const int64_t b = blockIdx.y;
+    const int g = blockIdx.z;
+    const int64_t c0 = 2 * static_cast<int64_t>(blockIdx.x);   // first chunk of the pair
+    if (w == 0)
+        tmem_alloc(base_s + SH::TMEM_OFF, 128);
+    if (tid == 0) {
+        mbar_init(bar_tile, 1);
+        mbar_init(bar_mma, 1);
+        mbar_fence_init();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    bool ok = true;
+    if (tid == 0) {
+        mbar_expect_tx(bar_tile, 2 * SH::ATOMS * SH::TILE);
+        const int t0 = static_cast<int>(c0 * Q);
+#pragma unroll
+        for (int a = 0; a < SH::ATOMS; ++a) {
+            tma_load_3d(base_s + SH::A_OFF + a * SH::TILE, &p.tm_Csw, bar_tile, g * N + 64 * a, t0,
+                        static_cast<int>(b));
+            tma_load_3d(base_s + SH::B_OFF + a * SH::TILE, &p.tm_Bsw, bar_tile, g * N + 64 * a, t0,
+                        static_cast<int>(b));
+        }
+        ok = mbar_wait(bar_tile, 0);
+        if (!ok)   // the wait gave up: let the copies land before the CTA leaves (bounded)
+            mbar_wait(bar_tile, 0);
+        if (ok) {
+            constexpr uint32_t idesc = umma_idesc_bf16(128, 128);
+#pragma unroll
+            for (int kk = 0; kk < N / 16; ++kk) {
+                const uint32_t koff = static_cast<uint32_t>((kk / 4) * SH::TILE + (kk % 4) * 32);
+                umma_bf16(tmem, umma_desc_sw128(base_s + SH::A_OFF + koff), umma_desc_sw128(base_s + SH::B_OFF + koff),
+                          idesc, kk > 0);
+            }
+            umma_commit(bar_mma);
+        }
+    }
+    ok = __syncthreads_and(ok ? 1 : 0) != 0;
+    if (ok && mbar_wait(bar_mma, 0)) {
+        tc_fence_after();
+        // lane t of warp w holds row r = 32w + t: the step of chunk c0 + r / 64, whose
+        // diagonal block is columns 64 (r / 64) ..
+        const int r = 32 * w + lane;
+        const int64_t c = c0 + r / 64;
+        uint32_t v[64];
+        const uint32_t ta = tmem + (static_cast<uint32_t>(32 * w) << 16) + static_cast<uint32_t>((r / 64) * 64);
+        tmem_ld16(ta, v);
+        tmem_ld16(ta + 16, v + 16);
+        tmem_ld16(ta + 32, v + 32);
+        tmem_ld16(ta + 48, v + 48);
+        tmem_ld_wait();
+        if (c < p.nchunks) {
+            __nv_bfloat16 *out = p.cb + (((b * p.nchunks + c) * p.G + g) * Q + (r % 64)) * Q;
+#pragma unroll
+            for (int j = 0; j < 64; j += 8) {
+                uint4 o;
+                o.x = pack_bf16x2(__uint_as_float(v[j]), __uint_as_float(v[j + 1]));
+                o.y = pack_bf16x2(__uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]));
+                o.z = pack_bf16x2(__uint_as_float(v[j + 4]), __uint_as_float(v[j + 5]));
+                o.w = pack_bf16x2(__uint_as_float(v[j + 6]), __uint_as_float(v[j + 7]));
+                *reinterpret_cast<uint4 *>(out + j) = o;
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (w == 0)
+        tmem_dealloc(tmem, 128);
 }
 
 template <int N>
@@ -549,7 +730,8 @@ size_t ssd_workspace_bytes(int64_t batch, int64_t L, int64_t G)
 // 3-d bf16 tensor map (d0 contiguous, then d1, d2; strides in bytes) with box
 // (b0, b1, 1); elements outside the tensor read as zero
 bool ssd_encode_3d(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1,
-                   uint64_t s2, uint32_t b0, uint32_t b1)
+                   uint64_t s2, uint32_t b0, uint32_t b1,
+                   CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_NONE)
 {
     const EncodeTiledFn fn = encode_tiled_fn();
     if (!fn)
@@ -559,7 +741,7 @@ bool ssd_encode_3d(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, u
     const cuuint32_t box[3] = {b0, b1, 1};
     const cuuint32_t estr[3] = {1, 1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -576,7 +758,9 @@ bool ssd_encode_maps(SsdParams &p, int64_t N)
            ssd_encode_3d(&p.tm_B, p.B, GN, L, bt, GN * 2, GN * L * 2, static_cast<uint32_t>(N + 8), Q) &&
            ssd_encode_3d(&p.tm_C, p.C, GN, L, bt, GN * 2, GN * L * 2, static_cast<uint32_t>(N + 8), Q) &&
            ssd_encode_3d(&p.tm_cb, p.cb, Q, Q, bt * static_cast<uint64_t>(p.nchunks) * static_cast<uint64_t>(p.G),
-                         Q * 2, Q * Q * 2, Q + 8, Q);
+                         Q * 2, Q * Q * 2, Q + 8, Q) &&
+           ssd_encode_3d(&p.tm_Bsw, p.B, GN, L, bt, GN * 2, GN * L * 2, 64, 2 * Q, CU_TENSOR_MAP_SWIZZLE_128B) &&
+           ssd_encode_3d(&p.tm_Csw, p.C, GN, L, bt, GN * 2, GN * L * 2, 64, 2 * Q, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 template <int N>
@@ -585,9 +769,22 @@ ss_status launch_ssd(const SsdParams &p, cudaStream_t stream)
     using SH = SsdShape<N>;
     if (p.nchunks > 0x7fffffff || p.batch > 65535 || p.G > 65535 || p.H > 0x7fffffff)
         return fail(SS_ERR_DIM, "grid too large");
-    ssd_cb_kernel<N><<<dim3(static_cast<unsigned>(p.nchunks), static_cast<unsigned>(p.batch),
-                            static_cast<unsigned>(p.G)), 128, 0, stream>>>(p);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = cudaSuccess;
+    if (p.tma) {   // C B^T on the tcgen05 tensor cores (tiles by 128-byte swizzled tensor copies)
+        using CS = SsdCbShape<N>;
+        e = cudaFuncSetAttribute(ssd_cb_tc_kernel<N>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(CS::BYTES));
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return fail(SS_ERR_LAUNCH, "cudaFuncSetAttribute failed: %s", cudaGetErrorString(e));
+        }
+        ssd_cb_tc_kernel<N><<<dim3(static_cast<unsigned>((p.nchunks + 1) / 2), static_cast<unsigned>(p.batch),
+                                   static_cast<unsigned>(p.G)), 128, CS::BYTES, stream>>>(p);
+    } else {
+        ssd_cb_kernel<N><<<dim3(static_cast<unsigned>(p.nchunks), static_cast<unsigned>(p.batch),
+                                static_cast<unsigned>(p.G)), 128, 0, stream>>>(p);
+    }
+    e = cudaGetLastError();
     if (e != cudaSuccess)
         return fail(SS_ERR_LAUNCH, "SSD CB kernel launch failed: %s", cudaGetErrorString(e));
     auto kernel = p.tma ? ssd_chunk_kernel<N, true> : ssd_chunk_kernel<N, false>;
