@@ -43,6 +43,9 @@ struct SsdParams {
     CUtensorMap tm_x, tm_B, tm_C, tm_cb;
     // B, C over (G*N, L, batch) with a box of 64 states x 128 steps, 128-byte swizzled (the C B^T product)
     CUtensorMap tm_Bsw, tm_Csw;
+    // the tensor-core chunk walk's tiles, 128-byte swizzled: x over (H*P, L, batch) with a box of
+    // 64 channels x Q steps; B, C with 64 states x Q steps; C B^T with Q x Q
+    CUtensorMap tm_xq, tm_Bq, tm_Cq, tm_cbq;
 };
 
 // ---- warp-level MMA helpers (PTX mma.sync / ldmatrix; operands in shared memory)
@@ -347,6 +350,412 @@ ssd_cb_tc_kernel(const __grid_constant__ SsdParams p)
     __syncthreads();
     if (w == 0)
         tmem_dealloc(tmem, 128);
+}
+
+// 16 consecutive 32-bit columns of this thread's lane written to tensor memory
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t *v)
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, "
+                 "%13, %14, %15, %16};" ::"r"(taddr),
+                 "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+                 "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+                 : "memory");
+}
+
+// M = 64 accumulators sit in lanes 0-15 of each warp's quarter: threads 0-15 read 16
+// columns of lanes 0-15 at taddr, threads 16-31 the same lanes at taddr + `half` columns
+template <int HALF>
+__device__ __forceinline__ void tmem_ld16_split(uint32_t taddr, uint32_t *v)
+{
+    asm volatile("tcgen05.ld.sync.aligned.16x32bx2.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, "
+                 "%13, %14, %15}, [%16], %17;"
+                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+                   "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]),
+                   "=r"(v[15])
+                 : "r"(taddr), "n"(HALF)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// shared-memory writes of this thread become visible to the tensor cores (async proxy)
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// MN-major operand descriptor (128-byte swizzle): atoms of 64 MN elements x 8 K
+// rows (8 rows of 128 bytes), `lbo` bytes between MN atoms, 1024 bytes between
+// 8-row K groups; a K step of 16 rows advances the start by 2048 bytes
+__device__ __forceinline__ uint64_t umma_desc_mn_sw128(uint32_t smem_addr, uint32_t lbo)
+{
+    return static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>(lbo >> 4) << 16) |
+           (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
+           (static_cast<uint64_t>(2) << 61);
+}
+
+// kind::f16 instruction descriptor with the operand majorness: a_mn / b_mn = 1 for MN-major
+__host__ __device__ constexpr uint32_t umma_idesc_bf16_mj(int M, int N, int a_mn, int b_mn)
+{
+    return umma_idesc_bf16(M, N) | (static_cast<uint32_t>(a_mn) << 15) | (static_cast<uint32_t>(b_mn) << 16);
+}
+
+// byte offset of element (r, c), c < 64, in a tile of 128-byte rows stored with
+// the 128-byte swizzle (16-byte piece c/8 of row r sits at piece (c/8) ^ (r % 8))
+__device__ __forceinline__ int sw128_off(int r, int c) { return r * 128 + (((c >> 3) ^ (r & 7)) << 4) + (c & 7) * 2; }
+
+// ---- the chunk walk on the tcgen05 tensor cores: one CTA (4 warps) per
+// (batch, head), the chunks of Q = 64 steps in order. Per chunk, with T the
+// tensor memory of the CTA:
+//   Y[t][p]   = sum_n (e^{cum[t]} C[t][n]) H[p][n] + sum_s (S' + D I)[t][s] X[s][p]   (T cols 64..127;
+//               M = 64 rows t; the decay of the carried state is folded into the C rows, the skip
+//               term D x into the diagonal of S', so both products accumulate in one place)
+//   y[t][p]   = Y[t][p] silu(z[t][p])
+//   H^T[n][p] <- e^{cum[Q-1]} H^T[n][p] + sum_s B[s][n] (w o X)[s][p]   (T cols 0..63; M = N rows n)
+// H^T stays in tensor memory from chunk to chunk (fp32). Operands: C, B, X and
+// C B^T arrive by 128-byte swizzled tensor copies; the threads scale the C rows
+// in place, form S' = C B^T o M o delta (+ D on the diagonal) in place over
+// C B^T, and write w o X and the bf16 copy of H (the B operand of the first
+// product) in the same swizzled layout. Every operand of a product is rounded
+// once to bf16. With N = 128 the state product has M = 128 (row n in lane n);
+// with N = 64, M = 64 (row n in lane 32 (n / 16) + n % 16), as for Y.
+template <int N>
+struct SsdTcShape {
+    static constexpr int Q = kSsdQ, P = kSsdP;
+    static constexpr int NS = N / 64;                       // 64-state slices of C and B
+    static constexpr int XT = Q * 128;                      // X tile [Q][64] bf16
+    static constexpr int CT = Q * 128;                      // one 64-state slice of C or B [Q][64]
+    static constexpr int X_OFF = 0;                         // X
+    static constexpr int C_OFF = X_OFF + XT;                // C slices (scaled in place)
+    static constexpr int B_OFF = C_OFF + NS * CT;           // B slices
+    static constexpr int S_OFF = B_OFF + NS * CT;           // C B^T, then S' in place [Q][Q]
+    static constexpr int XW_OFF = S_OFF + Q * 128;          // w o X [Q][64]
+    static constexpr int H_OFF = XW_OFF + XT;               // bf16 H, stored [N][64]
+    static constexpr int F_OFF = H_OFF + N * 128;           // fp32 per-step values: cum, e^cum, w, delta
+    static constexpr int BAR_OFF = F_OFF + 4 * Q * 4;       // barriers: the chunk's tiles, MMA
+    static constexpr int TMEM_OFF = BAR_OFF + 16;
+    static constexpr size_t BYTES = TMEM_OFF + 16 + 1024;  // + room to align the base to 1024 bytes
+    static constexpr uint32_t TCOLS = 128;
+    static_assert(X_OFF % 1024 == 0 && C_OFF % 1024 == 0 && B_OFF % 1024 == 0 && S_OFF % 1024 == 0 &&
+                      XW_OFF % 1024 == 0 && H_OFF % 1024 == 0,
+                  "swizzled tiles on 1024-byte boundaries");
+};
+
+template <int N>
+__global__ void __launch_bounds__(128, 3)
+ssd_chunk_tc_kernel(const __grid_constant__ SsdParams p)
+{
+    using SH = SsdTcShape<N>;
+    constexpr int Q = SH::Q, P = SH::P;
+    extern __shared__ __align__(1024) unsigned char smem_tc[];
+    const uint32_t raw_s = static_cast<uint32_t>(__cvta_generic_to_shared(smem_tc));
+    const uint32_t base_s = (raw_s + 1023u) & ~1023u;
+    unsigned char *base = smem_tc + (base_s - raw_s);
+    float *cum = reinterpret_cast<float *>(base + SH::F_OFF);
+    float *ecum = cum + Q;
+    float *wsx = ecum + Q;   // w_s = e^{cum[Q-1] - cum[s]} delta_s
+    float *dl = wsx + Q;     // delta_s
+    const uint32_t bar_cb = base_s + SH::BAR_OFF;      // X, C, B, C B^T of a chunk
+    const uint32_t bar_mma = bar_cb + 8;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(base + SH::TMEM_OFF);
+
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    const int64_t b = blockIdx.y;
+    const int h = blockIdx.x;
+    const int g = static_cast<int>(h / (p.H / p.G));
+    const float Ah = __ldg(p.A + h);
+    const float Dh = p.D ? __ldg(p.D + h) : 0.0f;
+    const float bias = p.dt_bias ? __ldg(p.dt_bias + h) : 0.0f;
+    const bool gate = p.z != nullptr;
+    const int64_t xs = p.H * P;   // x, z, y row stride (one time step)
+
+    if (w == 0)
+        tmem_alloc(base_s + SH::TMEM_OFF, SH::TCOLS);
+    if (tid == 0) {
+        mbar_init(bar_cb, 1);
+        mbar_init(bar_mma, 1);
+        mbar_fence_init();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t t_h = tmem, t_y = tmem + 64;   // column bases
+    const uint32_t lane_base = static_cast<uint32_t>(32 * w) << 16;
+
+    // the state row this thread holds in tensor memory (H^T[n][.]), or -1
+    const int hrow = (N == 128) ? tid : ((lane < 16) ? 16 * w + lane : -1);
+
+    // initial state: H^T[n][p] = h0[p][n] (zero without h0)
+    {
+        uint32_t v[64];
+#pragma unroll
+        for (int pp = 0; pp < 64; ++pp)
+            v[pp] = __float_as_uint((p.h0 && hrow >= 0) ? p.h0[((b * p.H + h) * P + pp) * N + hrow] : 0.0f);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            tmem_st16(t_h + lane_base + 16 * j, v + 16 * j);
+        tmem_st_wait();
+    }
+
+    // tensor copies of a chunk's tiles (X, C, B, C B^T) on one barrier; every wait is
+    // bounded, and after one gives up the CTA issues no more and leaves after the
+    // copies it issued have landed
+    int cb_issued = 0, cb_done = 0;
+    bool aborted = false;
+    auto issue_cb = [&](int64_t c) {
+        if (tid == 0 && !aborted) {
+            mbar_expect_tx(bar_cb, SH::XT + 2 * SH::NS * SH::CT + Q * 128);
+            tma_load_3d(base_s + SH::X_OFF, &p.tm_xq, bar_cb, h * P, static_cast<int>(c * Q), static_cast<int>(b));
+#pragma unroll
+            for (int j = 0; j < SH::NS; ++j) {
+                tma_load_3d(base_s + SH::C_OFF + j * SH::CT, &p.tm_Cq, bar_cb, g * N + 64 * j, static_cast<int>(c * Q),
+                            static_cast<int>(b));
+                tma_load_3d(base_s + SH::B_OFF + j * SH::CT, &p.tm_Bq, bar_cb, g * N + 64 * j, static_cast<int>(c * Q),
+                            static_cast<int>(b));
+            }
+            tma_load_3d(base_s + SH::S_OFF, &p.tm_cbq, bar_cb, 0, 0, static_cast<int>((b * p.nchunks + c) * p.G + g));
+            ++cb_issued;
+        }
+    };
+    auto wait_cb = [&]() {
+        if (!aborted) {
+            aborted = !mbar_wait(bar_cb, static_cast<uint32_t>(cb_done & 1));
+            if (!aborted)
+                ++cb_done;
+        }
+    };
+
+    issue_cb(0);
+    float dt_next = (tid < Q && tid < p.L) ? __bfloat162float(p.dt[(b * p.L + tid) * p.H + h]) : 0.0f;
+    int mma_phase = 0;
+
+    for (int64_t c = 0; c < p.nchunks; ++c) {
+        const int64_t t0 = c * Q;
+        const int valid = static_cast<int>(p.L - t0 < Q ? p.L - t0 : Q);
+        const uint32_t xs_s = base_s + SH::X_OFF;
+        const unsigned char *xt = base + SH::X_OFF;
+        // the gate inputs of this thread's epilogue piece (row 16w + lane % 16, 32 channels),
+        // fetched now so that their latency hides behind the chunk's other work
+        uint4 zpre[4];
+        {
+            const int t = 16 * w + (lane & 15), half = lane >> 4;
+            const int64_t ro = (b * p.L + t0 + t) * xs + static_cast<int64_t>(h) * P + 32 * half;
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                zpre[k] = (gate && t < valid) ? __ldg(reinterpret_cast<const uint4 *>(p.z + ro + 8 * k))
+                                              : make_uint4(0, 0, 0, 0);
+        }
+        // ---- step sizes (zero past L), a_s and the next chunk's raw steps
+        if (tid < Q) {
+            float d = 0.0f;
+            if (tid < valid) {
+                const float v = dt_next + bias;
+                d = p.softplus ? softplus_f(v) : v;
+            }
+            dl[tid] = d;
+        }
+        if (c + 1 < p.nchunks) {
+            const int64_t tn = (c + 1) * Q + tid;
+            dt_next = (tid < Q && tn < p.L) ? __bfloat162float(p.dt[(b * p.L + tn) * p.H + h]) : 0.0f;
+        }
+        __syncthreads();
+        // ---- cum[t] = A delta_0 + .. + A delta_t (log2 e units), e^cum, w (one warp)
+        if (w == 0) {
+            const float a0 = Ah * kLog2e * dl[2 * lane], a1 = Ah * kLog2e * dl[2 * lane + 1];
+            float sum = a0 + a1;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float u = __shfl_up_sync(0xffffffffu, sum, o);
+                if (lane >= o)
+                    sum += u;
+            }
+            const float c0v = sum - a1, c1v = sum;
+            cum[2 * lane] = c0v;
+            cum[2 * lane + 1] = c1v;
+            ecum[2 * lane] = ex2_approx(c0v);
+            ecum[2 * lane + 1] = ex2_approx(c1v);
+            const float cq = __shfl_sync(0xffffffffu, c1v, 31);
+            wsx[2 * lane] = ex2_approx(cq - c0v) * dl[2 * lane];
+            wsx[2 * lane + 1] = ex2_approx(cq - c1v) * dl[2 * lane + 1];
+        }
+        // ---- H: the bf16 copy (B operand of D1) and e^{cum[Q-1]} H back into tensor memory
+        //      (cum is read after the barrier below; the copy does not need it)
+        uint32_t hv[64];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            tmem_ld16(t_h + lane_base + 16 * j, hv + 16 * j);
+        tmem_ld_wait();
+        if (hrow >= 0) {
+            unsigned char *hr = base + SH::H_OFF;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                uint4 o;
+                o.x = pack_bf16x2(__uint_as_float(hv[8 * j]), __uint_as_float(hv[8 * j + 1]));
+                o.y = pack_bf16x2(__uint_as_float(hv[8 * j + 2]), __uint_as_float(hv[8 * j + 3]));
+                o.z = pack_bf16x2(__uint_as_float(hv[8 * j + 4]), __uint_as_float(hv[8 * j + 5]));
+                o.w = pack_bf16x2(__uint_as_float(hv[8 * j + 6]), __uint_as_float(hv[8 * j + 7]));
+                *reinterpret_cast<uint4 *>(hr + sw128_off(hrow, 8 * j)) = o;
+            }
+        }
+        __syncthreads();   // cum, e^cum, w, a, delta are in shared memory
+        {
+            const float ec = ex2_approx(cum[Q - 1]);
+#pragma unroll
+            for (int j = 0; j < 64; ++j)
+                hv[j] = __float_as_uint(__uint_as_float(hv[j]) * ec);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                tmem_st16(t_h + lane_base + 16 * j, hv + 16 * j);
+        }
+        wait_cb();
+        // ---- S' = C B^T o M o delta in place and w o X; thread (row r, half j) does 32
+        //      elements of row r: M[t][s] delta_s = e^{cum[t] - cum[s]} delta_s (<= 1) for s <= t
+        {
+            const int r = tid & (Q - 1), j = tid >> 6;
+            unsigned char *srow = base + SH::S_OFF;
+            const float ct = cum[r];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int s0 = 32 * j + 8 * k;
+                const uint4 cbw = *reinterpret_cast<const uint4 *>(srow + sw128_off(r, s0));
+                const uint32_t wv[4] = {cbw.x, cbw.y, cbw.z, cbw.w};
+                const float4 cu0 = *reinterpret_cast<const float4 *>(cum + s0);
+                const float4 cu1 = *reinterpret_cast<const float4 *>(cum + s0 + 4);
+                const float4 dd0 = *reinterpret_cast<const float4 *>(dl + s0);
+                const float4 dd1 = *reinterpret_cast<const float4 *>(dl + s0 + 4);
+                const float cu[8] = {cu0.x, cu0.y, cu0.z, cu0.w, cu1.x, cu1.y, cu1.z, cu1.w};
+                const float dd[8] = {dd0.x, dd0.y, dd0.z, dd0.w, dd1.x, dd1.y, dd1.z, dd1.w};
+                uint32_t ow[4];
+#pragma unroll
+                for (int e = 0; e < 8; e += 2) {
+                    float v0 = (s0 + e <= r) ? bf16lo(wv[e >> 1]) * ex2_approx(ct - cu[e]) * dd[e] : 0.0f;
+                    float v1 = (s0 + e + 1 <= r) ? bf16hi(wv[e >> 1]) * ex2_approx(ct - cu[e + 1]) * dd[e + 1] : 0.0f;
+                    v0 += (s0 + e == r) ? Dh : 0.0f;   // the skip term D x through the diagonal
+                    v1 += (s0 + e + 1 == r) ? Dh : 0.0f;
+                    ow[e >> 1] = pack_bf16x2(v0, v1);
+                }
+                *reinterpret_cast<uint4 *>(srow + sw128_off(r, s0)) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+            }
+            // the C rows scaled by e^{cum[t]} (the decay of the carried state to step t)
+            const float er = ecum[r];
+            unsigned char *crow = base + SH::C_OFF;
+#pragma unroll
+            for (int k2 = 0; k2 < 4 * SH::NS; ++k2) {
+                const int n0 = 32 * j + 8 * (k2 % 4) + 64 * (k2 / 4);   // this thread's half of each slice
+                unsigned char *cp = crow + (n0 / 64) * SH::CT + sw128_off(r, n0 % 64);
+                const uint4 cv = *reinterpret_cast<const uint4 *>(cp);
+                uint4 o;
+                o.x = pack_bf16x2(bf16lo(cv.x) * er, bf16hi(cv.x) * er);
+                o.y = pack_bf16x2(bf16lo(cv.y) * er, bf16hi(cv.y) * er);
+                o.z = pack_bf16x2(bf16lo(cv.z) * er, bf16hi(cv.z) * er);
+                o.w = pack_bf16x2(bf16lo(cv.w) * er, bf16hi(cv.w) * er);
+                *reinterpret_cast<uint4 *>(cp) = o;
+            }
+            const float ws = wsx[r];
+            unsigned char *xw = base + SH::XW_OFF;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int p0 = 32 * j + 8 * k;
+                const uint4 xv = *reinterpret_cast<const uint4 *>(xt + sw128_off(r, p0));
+                uint4 o;
+                o.x = pack_bf16x2(bf16lo(xv.x) * ws, bf16hi(xv.x) * ws);
+                o.y = pack_bf16x2(bf16lo(xv.y) * ws, bf16hi(xv.y) * ws);
+                o.z = pack_bf16x2(bf16lo(xv.z) * ws, bf16hi(xv.z) * ws);
+                o.w = pack_bf16x2(bf16lo(xv.w) * ws, bf16hi(xv.w) * ws);
+                *reinterpret_cast<uint4 *>(xw + sw128_off(r, p0)) = o;
+            }
+        }
+        tmem_st_wait();
+        fence_proxy_async();
+        tc_fence_before();
+        const int go = __syncthreads_and(aborted ? 0 : 1);
+        tc_fence_after();
+        if (!go)
+            break;
+        if (tid == 0) {
+            constexpr uint32_t id_y = umma_idesc_bf16_mj(64, 64, 0, 1);
+            constexpr uint32_t id_h = umma_idesc_bf16_mj(N, 64, 1, 1);
+            // Y = (e^cum C) H^T: A = scaled C (K-major, 64-state slices), B = H stored [n][p] (MN-major)
+#pragma unroll
+            for (int kk = 0; kk < N / 16; ++kk)
+                umma_bf16(t_y, umma_desc_sw128(base_s + SH::C_OFF + (kk / 4) * SH::CT + (kk % 4) * 32),
+                          umma_desc_mn_sw128(base_s + SH::H_OFF + kk * 2048, 8192), id_y, kk > 0);
+            // Y += (S' + D I) X: A = S' (K-major), B = X stored [s][p] (MN-major)
+#pragma unroll
+            for (int kk = 0; kk < Q / 16; ++kk)
+                umma_bf16(t_y, umma_desc_sw128(base_s + SH::S_OFF + kk * 32),
+                          umma_desc_mn_sw128(xs_s + kk * 2048, 8192), id_y, true);
+            // H^T += B^T (w o X): A = B stored [s][n] (MN-major, 64-state atoms CT bytes apart),
+            // B = w o X stored [s][p] (MN-major)
+#pragma unroll
+            for (int kk = 0; kk < Q / 16; ++kk)
+                umma_bf16(t_h, umma_desc_mn_sw128(base_s + SH::B_OFF + kk * 2048, SH::CT),
+                          umma_desc_mn_sw128(base_s + SH::XW_OFF + kk * 2048, 8192), id_h, true);
+            umma_commit(bar_mma);
+        }
+        const bool mma_ok = __syncthreads_and(mbar_wait(bar_mma, static_cast<uint32_t>(mma_phase & 1)) ? 1 : 0) != 0;
+        ++mma_phase;
+        tc_fence_after();
+        // X, C, B and C B^T are free: the next chunk's land while this one finishes
+        if (c + 1 < p.nchunks && mma_ok)
+            issue_cb(c + 1);
+        // ---- epilogue: y[t][p] = Y[t][p] silu(z); warp w holds rows t = 16w .. 16w+15,
+        //      lane l row 16w + (l % 16), columns 32 (l / 16) ..
+        {
+            uint32_t yv[32];
+            tmem_ld16_split<32>(t_y + lane_base, yv);
+            tmem_ld16_split<32>(t_y + lane_base + 16, yv + 16);
+            tmem_ld_wait();
+            const int t = 16 * w + (lane & 15), half = lane >> 4;
+            if (t < valid && mma_ok) {
+                const int64_t ro = (b * p.L + t0 + t) * xs + static_cast<int64_t>(h) * P + 32 * half;
+                __nv_bfloat16 *yr = p.y + ro;
+#pragma unroll
+                for (int k4 = 0; k4 < 4; ++k4) {
+                    const uint32_t zw4[4] = {zpre[k4].x, zpre[k4].y, zpre[k4].z, zpre[k4].w};
+                    uint32_t ow[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int pp = 8 * k4 + 2 * e;
+                        float o0 = __uint_as_float(yv[pp]), o1 = __uint_as_float(yv[pp + 1]);
+                        if (gate) {
+                            o0 *= silu_f(bf16lo(zw4[e]));
+                            o1 *= silu_f(bf16hi(zw4[e]));
+                        }
+                        ow[e] = pack_bf16x2(o0, o1);
+                    }
+                    *reinterpret_cast<uint4 *>(yr + 8 * k4) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+                }
+            }
+        }
+        if (!mma_ok) {
+            aborted = true;
+            break;
+        }
+        tc_fence_before();
+        __syncthreads();   // every thread is done with this chunk's S', w o X, bf16 H and Y
+        tc_fence_after();
+    }
+
+    // the final state: final_state[p][n] = H^T[n][p]
+    if (p.final_state && !aborted) {
+        uint32_t hv[64];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            tmem_ld16(t_h + lane_base + 16 * j, hv + 16 * j);
+        tmem_ld_wait();
+        if (hrow >= 0) {
+            float *fs = p.final_state + ((b * p.H + h) * P) * N + hrow;
+#pragma unroll
+            for (int pp = 0; pp < 64; ++pp)
+                fs[static_cast<int64_t>(pp) * N] = __uint_as_float(hv[pp]);
+        }
+    }
+    if (tid == 0)   // copies issued and not yet waited for (after an abort) land before the CTA leaves
+        for (int i = cb_done; i < cb_issued; ++i)
+            mbar_wait(bar_cb, static_cast<uint32_t>(i & 1));
+    tc_fence_before();
+    __syncthreads();
+    if (w == 0)
+        tmem_dealloc(tmem, SH::TCOLS);
 }
 
 template <int N>
@@ -760,7 +1169,12 @@ bool ssd_encode_maps(SsdParams &p, int64_t N)
            ssd_encode_3d(&p.tm_cb, p.cb, Q, Q, bt * static_cast<uint64_t>(p.nchunks) * static_cast<uint64_t>(p.G),
                          Q * 2, Q * Q * 2, Q + 8, Q) &&
            ssd_encode_3d(&p.tm_Bsw, p.B, GN, L, bt, GN * 2, GN * L * 2, 64, 2 * Q, CU_TENSOR_MAP_SWIZZLE_128B) &&
-           ssd_encode_3d(&p.tm_Csw, p.C, GN, L, bt, GN * 2, GN * L * 2, 64, 2 * Q, CU_TENSOR_MAP_SWIZZLE_128B);
+           ssd_encode_3d(&p.tm_Csw, p.C, GN, L, bt, GN * 2, GN * L * 2, 64, 2 * Q, CU_TENSOR_MAP_SWIZZLE_128B) &&
+           ssd_encode_3d(&p.tm_xq, p.x, HP, L, bt, HP * 2, HP * L * 2, 64, Q, CU_TENSOR_MAP_SWIZZLE_128B) &&
+           ssd_encode_3d(&p.tm_Bq, p.B, GN, L, bt, GN * 2, GN * L * 2, 64, Q, CU_TENSOR_MAP_SWIZZLE_128B) &&
+           ssd_encode_3d(&p.tm_Cq, p.C, GN, L, bt, GN * 2, GN * L * 2, 64, Q, CU_TENSOR_MAP_SWIZZLE_128B) &&
+           ssd_encode_3d(&p.tm_cbq, p.cb, Q, Q, bt * static_cast<uint64_t>(p.nchunks) * static_cast<uint64_t>(p.G),
+                         Q * 2, Q * Q * 2, 64, Q, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 template <int N>
@@ -787,13 +1201,26 @@ ss_status launch_ssd(const SsdParams &p, cudaStream_t stream)
     e = cudaGetLastError();
     if (e != cudaSuccess)
         return fail(SS_ERR_LAUNCH, "SSD CB kernel launch failed: %s", cudaGetErrorString(e));
-    auto kernel = p.tma ? ssd_chunk_kernel<N, true> : ssd_chunk_kernel<N, false>;
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(SH::BYTES));
-    if (e != cudaSuccess) {
-        cudaGetLastError();
-        return fail(SS_ERR_LAUNCH, "cudaFuncSetAttribute failed: %s", cudaGetErrorString(e));
+    const char *env = getenv("SS_SSD_MMA_SYNC");
+    if (p.tma && !(env && strcmp(env, "1") == 0)) {   // the chunk walk on the tcgen05 tensor cores
+        using TS = SsdTcShape<N>;
+        e = cudaFuncSetAttribute(ssd_chunk_tc_kernel<N>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(TS::BYTES));
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return fail(SS_ERR_LAUNCH, "cudaFuncSetAttribute failed: %s", cudaGetErrorString(e));
+        }
+        ssd_chunk_tc_kernel<N><<<dim3(static_cast<unsigned>(p.H), static_cast<unsigned>(p.batch)), 128, TS::BYTES,
+                                 stream>>>(p);
+    } else {   // mma.sync (rows that cannot be copied by tensor maps, or SS_SSD_MMA_SYNC=1)
+        auto kernel = p.tma ? ssd_chunk_kernel<N, true> : ssd_chunk_kernel<N, false>;
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(SH::BYTES));
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return fail(SS_ERR_LAUNCH, "cudaFuncSetAttribute failed: %s", cudaGetErrorString(e));
+        }
+        kernel<<<dim3(static_cast<unsigned>(p.H), static_cast<unsigned>(p.batch)), 128, SH::BYTES, stream>>>(p);
     }
-    kernel<<<dim3(static_cast<unsigned>(p.H), static_cast<unsigned>(p.batch)), 128, SH::BYTES, stream>>>(p);
     e = cudaGetLastError();
     if (e != cudaSuccess)
         return fail(SS_ERR_LAUNCH, "SSD chunk kernel launch failed: %s", cudaGetErrorString(e));
