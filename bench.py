@@ -728,7 +728,7 @@ def ncu_case(args):
             binding.causal_conv1d(x, w, bias, out=out, state_out=st)
         torch.cuda.synchronize()
         return 0
-    spec = HEADLINE
+    spec = {"scan_1p4b": I.MAMBA1P4B, "scan_longseq": I.LONGSEQ}.get(args.ncu_case, HEADLINE)
     inp = I.make_scan_inputs(spec)
     g = {k: v.cuda() for k, v in inp.items() if k != "reset_pos"}
     y = torch.empty_like(g["x"])
@@ -751,9 +751,11 @@ def main(argv=None):
     ap.add_argument("--headline-only", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-soak", action="store_true", help="skip the 1 s untimed soak before timing")
-    ap.add_argument("--ncu-case", choices=["scan", "decode", "conv", "bwd", "ssd"], default=None,
-                    help="profiling case: warmup + steps launches of the headline scan (or of the decode "
-                         "update, on the first warmup + steps tokens of the decode workload), nothing else")
+    ap.add_argument("--ncu-case", choices=["scan", "scan_1p4b", "scan_longseq", "decode", "conv", "bwd", "ssd"],
+                    default=None,
+                    help="profiling case: warmup + steps launches of one kernel on its workload (the headline "
+                         "scan, the 1.4B-layer or long-sequence scan, the decode update on the first warmup + "
+                         "steps tokens, conv, backward, SSD), nothing else")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -861,7 +863,8 @@ def main(argv=None):
                          "peak_source": "measured (MEASURED_PEAKS.json bf16_tflops, burst)"}
         extras["ssd_" + sspec.name] = {
             "elem_steps_per_s": sspec.elem_steps / (sms2 * 1e-3), "kernel_ms_median": sms2, "roofline": sro,
-            "note": "Mamba-2 scalar-decay scan, C B^T and chunk kernels, mma.sync bf16 tensor cores"}
+            "note": "Mamba-2 scalar-decay scan: C B^T and the chunk walk on the tcgen05 tensor cores (TMEM "
+                    "accumulators, 128-byte swizzled tensor-copy operands)"}
         cms, cbytes = time_conv(HEADLINE, 10, 3)
         extras["conv1d_silu_k4_" + HEADLINE.name] = {
             "elems_per_s": HEADLINE.batch * HEADLINE.d_inner * HEADLINE.L / (cms * 1e-3), "kernel_ms_median": cms,

@@ -333,19 +333,27 @@ ss_status ss_scan_fwd_train_f32(const float *x, const float *delta, const float 
 
 /*
  * ss_scan_bwd_noalloc_bf16 / ss_scan_bwd_noalloc_f32 -- ss_scan_bwd_* without
- * a caller workspace: the stored states live in a device array built into the
- * library (SS_BWD_NOALLOC_MAX_BYTES bytes per device), so the call needs no
- * memory beyond its inputs and outputs. Arguments and results are those of
- * ss_scan_bwd_* minus workspace / workspace_bytes.
+ * a caller workspace, for callers that cannot call cudaMalloc (code that runs
+ * under a framework which owns all device memory through its own pool, or a
+ * library that may not allocate on its caller's behalf). The stored states live
+ * in a device array built into the library (SS_BWD_NOALLOC_MAX_BYTES bytes),
+ * so the call needs no memory beyond its inputs and outputs and allocates
+ * nothing. The pages have no counterpart: this is a packaging of the backward
+ * pass. Arguments and results are those of ss_scan_bwd_* minus workspace /
+ * workspace_bytes.
  *
  * Limits: a problem whose ss_scan_bwd_workspace_bytes(...) exceeds
- * SS_BWD_NOALLOC_MAX_BYTES is rejected with SS_ERR_DIM (use ss_scan_bwd_*).
- * The array is shared by every call in the process on that device: calls whose
- * work overlaps in time (unordered streams, several host threads) race on it
- * and must be ordered by the caller. The first call on a device resolves the
- * array's address (which can load the module) and must not be made during
- * stream capture; later calls may be captured. Nothing in the array needs
- * clearing between calls.
+ * SS_BWD_NOALLOC_MAX_BYTES is rejected with SS_ERR_DIM (use ss_scan_bwd_*);
+ * sizes are validated before any size product is formed. Every CUDA context
+ * that loads the library holds one copy of the array (SS_BWD_NOALLOC_MAX_BYTES
+ * of device memory, until the context is destroyed), whether or not it calls
+ * this entry point. The copy is shared by every call in that context: calls
+ * whose work overlaps on the GPU (unordered streams, several host threads)
+ * race on it and must be ordered by the caller. Nothing in the array needs
+ * clearing between calls. The first call in a context resolves the array's
+ * address (which can load the module) and should come before any stream
+ * capture; the address is cached with the context's unique id, so a call after
+ * cudaDeviceReset (or in another context) resolves it again.
  */
 #define SS_BWD_NOALLOC_MAX_BYTES (64u << 20)
 

@@ -896,7 +896,7 @@ ss_status scan_bwd(const void *x, const void *dt, const float *A, const void *B,
 // is cached together with that context's unique id: after cudaDeviceReset (or
 // in another context on the same device) the next call resolves it again. The
 // first call in a context resolves it (which can load the module), so that
-// call must not be made while a stream is being captured; later calls can be.
+// call should come before any stream capture.
 constexpr size_t kBwdScratchBytes = static_cast<size_t>(SS_BWD_NOALLOC_MAX_BYTES);
 static __device__ __align__(256) unsigned char g_bwd_scratch[kBwdScratchBytes];
 
