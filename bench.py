@@ -98,7 +98,7 @@ def measured_peaks() -> dict:
 
 # the source part each profiled kernel lives in (besides the shared device helpers)
 KERNEL_PART = {"scan_fwd_": "scan_fwd.cuh", "state_update_": "decode.cuh", "scan_bwd_": "scan_bwd.cuh",
-               "conv1d_": "conv.cuh", "ssd_chunk_": "ssd.cuh"}
+               "conv1d_": "conv.cuh", "conv_state_update_": "conv.cuh", "ssd_chunk_": "ssd.cuh"}
 
 
 def kernel_source_hash(kernel_key: str) -> str:
@@ -427,27 +427,37 @@ def time_conv(spec: I.ScanSpec, steps: int, warmup: int, k: int = 4):
 
 def time_conv_step(spec: I.DecodeSpec, steps: int, k: int = 4):
     """One decode step of the convolution on the decode workload's shape, L2
-    flushed before each launch. Returns (median ms, algorithmic bytes)."""
+    flushed before each launch. Returns (median ms, algorithmic bytes, median
+    ms of a plain device copy that moves the same bytes under the same
+    protocol: the floor a launch of this size meets)."""
     from selective_state_space_138_b300 import binding
     x = I.normal(spec.seed, 11, (spec.batch, spec.d_inner), 1.0, torch.bfloat16).cuda()
     w = I.normal(spec.seed, 12, (spec.d_inner, k), 0.5, torch.float32).cuda()
     bias = I.normal(spec.seed, 13, (spec.d_inner,), 0.2, torch.float32).cuda()
     st = I.normal(spec.seed, 14, (spec.batch, k - 1, spec.d_inner), 1.0, torch.bfloat16).cuda()
     out = torch.empty_like(x)
-    scratch = L2Flush()
-    for _ in range(3):
-        binding.conv_state_update(st, x, w, bias, out=out)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
-    for a, b in ev:
-        scratch()
-        torch.cuda._sleep(LAUNCH_COVER_CYCLES)
-        a.record()
-        binding.conv_state_update(st, x, w, bias, out=out)
-        b.record()
-    torch.cuda.synchronize()
-    ms = statistics.median([a.elapsed_time(b) for a, b in ev])
     bd = spec.batch * spec.d_inner
-    return ms, bd * 2 * 2 + 2 * bd * (k - 1) * 2 + spec.d_inner * (k + 1) * 4
+    nbytes = bd * 2 * 2 + 2 * bd * (k - 1) * 2 + spec.d_inner * (k + 1) * 4
+    src = torch.zeros(nbytes // 4, dtype=torch.float32, device="cuda")
+    dst = torch.empty_like(src)
+    scratch = L2Flush()
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for a, b in ev:
+            scratch()
+            torch.cuda._sleep(LAUNCH_COVER_CYCLES)
+            a.record()
+            fn()
+            b.record()
+        torch.cuda.synchronize()
+        return statistics.median([a.elapsed_time(b) for a, b in ev])
+
+    ms = timed(lambda: binding.conv_state_update(st, x, w, bias, out=out))
+    copy_ms = timed(lambda: dst.copy_(src))
+    return ms, nbytes, copy_ms
 
 
 def time_bwd(spec: I.ScanSpec, steps: int, warmup: int, from_forward: bool = False, variant: bool = False):
@@ -728,6 +738,17 @@ def ncu_case(args):
             binding.causal_conv1d(x, w, bias, out=out, state_out=st)
         torch.cuda.synchronize()
         return 0
+    if args.ncu_case == "conv_step":
+        spec, k = I.DECODE, 4
+        x = I.normal(spec.seed, 11, (spec.batch, spec.d_inner), 1.0, torch.bfloat16).cuda()
+        w = I.normal(spec.seed, 12, (spec.d_inner, k), 0.5, torch.float32).cuda()
+        bias = I.normal(spec.seed, 13, (spec.d_inner,), 0.2, torch.float32).cuda()
+        st = I.normal(spec.seed, 14, (spec.batch, k - 1, spec.d_inner), 1.0, torch.bfloat16).cuda()
+        out = torch.empty_like(x)
+        for _ in range(args.warmup + args.steps):
+            binding.conv_state_update(st, x, w, bias, out=out)
+        torch.cuda.synchronize()
+        return 0
     spec = {"scan_1p4b": I.MAMBA1P4B, "scan_longseq": I.LONGSEQ}.get(args.ncu_case, HEADLINE)
     inp = I.make_scan_inputs(spec)
     g = {k: v.cuda() for k, v in inp.items() if k != "reset_pos"}
@@ -751,7 +772,7 @@ def main(argv=None):
     ap.add_argument("--headline-only", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-soak", action="store_true", help="skip the 1 s untimed soak before timing")
-    ap.add_argument("--ncu-case", choices=["scan", "scan_1p4b", "scan_longseq", "decode", "conv", "bwd", "ssd"],
+    ap.add_argument("--ncu-case", choices=["scan", "scan_1p4b", "scan_longseq", "decode", "conv", "conv_step", "bwd", "ssd"],
                     default=None,
                     help="profiling case: warmup + steps launches of one kernel on its workload (the headline "
                          "scan, the 1.4B-layer or long-sequence scan, the decode update on the first warmup + "
@@ -870,10 +891,13 @@ def main(argv=None):
             "elems_per_s": HEADLINE.batch * HEADLINE.d_inner * HEADLINE.L / (cms * 1e-3), "kernel_ms_median": cms,
             "roofline": roofline_obj(cbytes, cms, peaks, profiled_traffic("conv1d_silu_k4_" + HEADLINE.name)),
             "note": "causal depthwise conv (k = 4) + SiLU on the layer's (batch, d_inner, L) input, history out"}
-        sms_, sbytes = time_conv_step(I.DECODE, 20)
+        sms_, sbytes, scopy = time_conv_step(I.DECODE, 20)
         extras["conv_state_update_k4_" + I.DECODE.name] = {
-            "ms_per_token": sms_, "roofline": roofline_obj(sbytes, sms_, peaks, None),
-            "note": "one decode step of the convolution (cache of 3 inputs per channel), L2 flushed before each"}
+            "ms_per_token": sms_,
+            "roofline": roofline_obj(sbytes, sms_, peaks, profiled_traffic("conv_state_update_k4_" + I.DECODE.name)),
+            "copy_floor": {"ms": scopy, "frac": sbytes / (scopy * 1e-3) / 1e9 / peaks["hbm_gbs"]},
+            "note": "one decode step of the convolution (cache of 3 inputs per channel), L2 flushed before each; "
+                    "copy_floor: a device copy of the same bytes (half read, half written) under the same protocol"}
         gms, fms = time_decode(I.DECODE, reps=3, warmup=3)
         dbytes = decode_alg_bytes(I.DECODE)
         extras[I.DECODE.name] = {

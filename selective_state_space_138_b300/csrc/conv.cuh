@@ -15,12 +15,15 @@
 // word.
 
 struct ConvParams {
+    CUtensorMap tm_x, tm_out;   // (L, d_inner, batch) boxes of 128 bytes x kConvRows channels, 128-byte swizzle
     const void *x, *state_in;
     const float *w, *bias;
     void *out, *state_out;
     int64_t batch, d_inner, L;
     int silu;
     int vec;  // 16-byte aligned rows of whole pieces
+    int tma;  // tm_x and tm_out are encoded: the tile kernel runs
+    int ntt, ngr, ntiles;   // tile kernel: tiles of steps per row, channel groups, tiles (below 2^31)
 };
 
 // Input t of row (b, d): x for t >= 0, the carried history for -(K-1) <= t < 0
@@ -130,22 +133,91 @@ causal_conv1d_kernel(const ConvParams p)
     }
 }
 
-// Vector path (16-byte aligned rows, L a multiple of the piece): a CTA stages
-// CG channels x PT pieces of one batch row, plus the HP pieces before them,
-// into shared memory with asynchronous 16-byte copies (no registers held while
-// the loads are in flight). Then 16 threads share a row, each turning PPL
-// consecutive pieces into outputs: the last K-1 inputs ride along in
-// registers from one piece to the next, so each input is unpacked once, and
-// the channel's taps and bias are read once. Outputs overwrite their own
-// input pieces in shared memory and leave for HBM with consecutive threads on
-// consecutive pieces. Pieces are stored XOR-swizzled within groups of 8
-// (piece j at column (j & ~7) | ((j ^ (j >> 3)) & 7)), so that the 16 threads
-// of a row, reading pieces PPL apart, hit distinct banks. Inputs before t = 0
-// come from the carried history (or are zero).
-constexpr int kConvTileBytes = 2048;   // one row of a tile
-constexpr int kConvRows = 8;           // channels per tile
+// Aligned rows (16-byte aligned x and out, rows a whole number of 16-byte
+// pieces): tensor copies and persistent CTAs. A tile is kConvRows channels x
+// kConvSegs segments of 128 bytes of one batch row. Each segment arrives as
+// one box of 8 channel rows x 128 bytes with the 128-byte swizzle (16-byte
+// chunk c of channel row ch at ch * 128 + ((c ^ ch) * 16)), and one more box,
+// the segment just before the tile, gives the first segment its k-1 inputs of
+// history (inputs before t = 0 come from the carried history or are zero).
+// A CTA walks its tiles through a ring of kConvStages stages with two roles:
+// four compute warps, in which thread (s, ch) = (tid / 8, tid % 8) turns
+// segment s of channel ch into outputs piece by piece (the last k-1 inputs
+// ride along in registers; the 8 channels of a quarter-warp sit on different
+// chunks, so its 16-byte shared-memory accesses are free of bank conflicts),
+// writing them over their inputs; and one copy warp, which sends each
+// computed tile out with tensor stores and refills its stage with the tensor
+// loads of the tile kConvStages further on.
+constexpr int kConvRows = 8;     // channels per tile (rows of a box)
+constexpr int kConvSegs = 16;    // 128-byte segments per tile row
+constexpr int kConvStages = 3;   // tiles in the ring
+constexpr int kConvThreads = kBlock + 32;   // four compute warps and the copy warp
 
-__device__ __forceinline__ int conv_swz(int j) { return (j & ~7) | ((j ^ (j >> 3)) & 7); }
+template <typename T>
+struct ConvTileShape {
+    static constexpr int EPP = 16 / (int)sizeof(T);     // elements per 16-byte piece
+    static constexpr int SEGE = 128 / (int)sizeof(T);   // elements per segment
+    static constexpr int TT = kConvSegs * SEGE;         // steps per tile
+    static constexpr int BOX = kConvRows * 128;         // bytes of one box
+    static constexpr int STAGE = (kConvSegs + 1) * BOX; // the halo box, then the tile's boxes
+    static constexpr int BYTES = 1024 + kConvStages * STAGE + 2 * kConvStages * 8;   // with the alignment slack
+    static_assert(kConvRows * kConvSegs == kBlock, "one thread per (segment, channel)");
+};
+
+__device__ __forceinline__ void conv_fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// box (c0, c1, c2) of a 3-d tensor map from shared memory at src to global memory
+__device__ __forceinline__ void conv_tma_store_3d(const void *tmap, uint32_t src, int c0, int c1, int c2)
+{
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(tmap)),
+                 "r"(src), "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+}
+
+__device__ __forceinline__ void conv_mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// barrier 1 over the four compute warps (barrier 0 is __syncthreads)
+__device__ __forceinline__ void conv_compute_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kBlock) : "memory"); }
+
+__device__ __forceinline__ void conv_bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// every bulk group but the newest PENDING has finished reading shared memory
+template <int PENDING>
+__device__ __forceinline__ void conv_bulk_wait_read()
+{
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(PENDING) : "memory");
+}
+
+// every bulk group has completed
+__device__ __forceinline__ void conv_bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// One piece of outputs from the window win[i] = input (i - H) steps from the
+// piece's first element (H = K - 1 history values, then the piece's EPP
+// inputs), in packed f32x2 arithmetic on output pairs (e, e + EPP/2):
+// a = bias + sum_k w_k (x_{e-k}, x_{e+EPP/2-k}). Without SILU the output is a.
+// With SILU the taps and bias come scaled by -log2(e), so a = -log2(e) z, and
+// z sigmoid(z) = z / (1 + 2^a) = a / ((1 + 2^a) (-log2(e))).
+template <int K, int EPP, bool SILU>
+__device__ __forceinline__ void conv_piece_pairs(const float *win, const u64 *w2, u64 bias2, float *o)
+{
+    constexpr int H = K - 1, HALF = EPP / 2;
+#pragma unroll
+    for (int e = 0; e < HALF; ++e) {
+        u64 acc = bias2;
+#pragma unroll
+        for (int k = 0; k < K; ++k)
+            acc = fma2(w2[k], pk(win[H + e - k], win[H + e + HALF - k]), acc);
+        if constexpr (SILU) {
+            const u64 c = splat(-kLog2e);
+            acc = mul2(acc, rcp_2(fma2(ex2_2(acc), c, c)));
+        }
+        upk(acc, o[e], o[e + HALF]);
+    }
+}
 
 // 16 bytes of outputs in the io type
 template <typename T>
@@ -163,122 +235,211 @@ __device__ __forceinline__ uint4 conv_pack(const float *o)
     return w;
 }
 
-template <typename T, int K>
-__global__ void __launch_bounds__(kBlock)
-causal_conv1d_tile_kernel(const ConvParams p)
+// piece m of a thread's segment (channel row `row` of a stage, 128-byte
+// swizzle, chunk m at (m ^ ch) * 16): outputs replace the inputs, and hist
+// (the H inputs before the piece) moves on to the H inputs before the next
+template <typename T, int K, bool SILU>
+__device__ __forceinline__ void conv_tile_piece(unsigned char *row, int m, int ch, float *hist, const u64 *w2,
+                                                u64 bias2)
 {
-    constexpr int EPP = 16 / (int)sizeof(T);
-    constexpr int H = K - 1;
-    constexpr int HP = (H + EPP - 1) / EPP;      // halo pieces
-    constexpr int PT = kConvTileBytes / 16;      // pieces per tile row
-    constexpr int CG = kConvRows;
-    constexpr int LPR = kBlock / CG;             // threads per row
-    constexpr int PPL = PT / LPR;                // consecutive pieces per thread
-    static_assert(PT % LPR == 0 && PPL % 8 == 0 && kBlock % CG == 0, "tile shape");
-    __shared__ __align__(16) uint4 tile[CG][HP + PT];   // [halo pieces][swizzled pieces]
-
-    const int64_t npieces = p.L / EPP;
-    const int64_t pc0 = static_cast<int64_t>(blockIdx.x) * PT;
-    const int64_t d0 = static_cast<int64_t>(blockIdx.y) * CG;
-    const T *x = static_cast<const T *>(p.x);
-    const int r = threadIdx.x / LPR;             // compute role: row r, pieces j0 .. j0 + PPL - 1
-    const int j0 = (threadIdx.x % LPR) * PPL;
-    const int64_t d = d0 + r;
-    const bool act = d < p.d_inner;
-    float wd[K];
+    constexpr int H = K - 1, EPP = 16 / (int)sizeof(T);
+    uint4 *piece = reinterpret_cast<uint4 *>(row + ((m ^ ch) << 4));
+    float win[H + EPP];   // the window: H history values, then the piece
 #pragma unroll
-    for (int k = 0; k < K; ++k)
-        wd[k] = act ? __ldg(p.w + d * K + k) : 0.0f;
-    const float bv = (act && p.bias) ? __ldg(p.bias + d) : 0.0f;
-
-    for (int64_t b = blockIdx.z; b < p.batch; b += gridDim.z) {
+    for (int j = 0; j < H; ++j)
+        win[j] = hist[j];
+    unpack_piece<T>(*piece, win + H);
+    float o[EPP];
+    conv_piece_pairs<K, EPP, SILU>(win, w2, bias2, o);
+    *piece = conv_pack<T>(o);
 #pragma unroll
-        for (int rr = 0; rr < CG; ++rr) {
-            const int64_t dr = d0 + rr;
-            for (int jj = threadIdx.x; jj < HP + PT; jj += kBlock) {
-                const int64_t pc = jj < HP ? pc0 - HP + jj : pc0 + (jj - HP);
-                const int col = jj < HP ? jj : HP + conv_swz(jj - HP);
-                const bool ok = dr < p.d_inner && pc >= 0 && pc < npieces;
-                const T *src = ok ? x + (b * p.d_inner + dr) * p.L + pc * EPP : x;
-                cp_async16(static_cast<uint32_t>(__cvta_generic_to_shared(&tile[rr][col])), src, ok ? 16 : 0);
+    for (int j = 0; j < H; ++j)
+        hist[j] = win[EPP + j];
+}
+
+// (tile of steps, channel group, batch row) of a tile number; a CTA's tiles
+// are its first plus multiples of the grid size, reached by adding the
+// step's own digits with carries
+struct ConvTileIdx {
+    int tt, g, b;
+};
+
+__device__ __forceinline__ ConvTileIdx conv_tile_digits(int tile, int ntt, int ngr)
+{
+    const int r = tile / ntt;
+    return {tile - r * ntt, r % ngr, r / ngr};
+}
+
+__device__ __forceinline__ void conv_tile_advance(ConvTileIdx &t, const ConvTileIdx &step, int ntt, int ngr)
+{
+    t.tt += step.tt;
+    if (t.tt >= ntt) {
+        t.tt -= ntt;
+        ++t.g;
+    }
+    t.g += step.g;
+    if (t.g >= ngr) {
+        t.g -= ngr;
+        ++t.b;
+    }
+    t.b += step.b;
+}
+
+template <typename T, int K, bool SILU>
+__global__ void __launch_bounds__(kConvThreads, 4)
+causal_conv1d_tile_kernel(const __grid_constant__ ConvParams p)
+{
+    using SH = ConvTileShape<T>;
+    constexpr int H = K - 1, EPP = SH::EPP, SEGE = SH::SEGE, TT = SH::TT, BOX = SH::BOX, NS = kConvStages;
+    constexpr int HP = (H + EPP - 1) / EPP;   // pieces of the previous segment that hold the history
+    constexpr int PPS = 8;                    // pieces per segment
+    static_assert(HP <= PPS, "history within one segment");
+    extern __shared__ unsigned char conv_smem[];
+    const uint32_t raw_s = static_cast<uint32_t>(__cvta_generic_to_shared(conv_smem));
+    const uint32_t base_s = (raw_s + 1023u) & ~1023u;   // boxes with the 128-byte swizzle sit on 1024 bytes
+    unsigned char *base = conv_smem + (base_s - raw_s);
+    const uint32_t full_s = base_s + NS * SH::STAGE;   // [NS] "stage filled" (the tensor loads landed)
+    const uint32_t done_s = full_s + 8u * NS;          // [NS] "stage computed" (every compute thread arrived)
+
+    const int tid = threadIdx.x, lane = tid & 31;
+    const int L = static_cast<int>(p.L), ntt = p.ntt, ngr = p.ngr;
+    const int mine = static_cast<int>(blockIdx.x) < p.ntiles
+                         ? (p.ntiles - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1
+                         : 0;
+    const ConvTileIdx step = conv_tile_digits(static_cast<int>(gridDim.x), ntt, ngr);
+    const ConvTileIdx first = conv_tile_digits(static_cast<int>(blockIdx.x), ntt, ngr);
+
+    if (tid == 0) {
+#pragma unroll
+        for (int j = 0; j < NS; ++j) {
+            mbar_init(full_s + 8u * j, 1);
+            mbar_init(done_s + 8u * j, kBlock);
+        }
+        mbar_fence_init();
+    }
+    __syncthreads();
+
+    if (tid >= kBlock) {
+        // the copy warp: lane j loads box j of a tile and stores segment j;
+        // boxes wholly outside the row are not fetched (the halo before t = 0,
+        // segments past L)
+        ConvTileIdx ld = first, sv = first;
+        auto issue_load = [&](int n) {
+            const int st = n % NS;
+            const uint32_t bar = full_s + 8u * st;
+            const int t0 = ld.tt * TT;
+            const int lo = ld.tt == 0 ? 1 : 0;
+            const int live = (L - t0 + SEGE - 1) / SEGE;   // segments of the tile that hold inputs
+            const int hi = live < kConvSegs ? live : kConvSegs;
+            if (lane == 0)
+                mbar_expect_tx(bar, static_cast<uint32_t>((hi + 1 - lo) * BOX));
+            __syncwarp();
+            if (lane >= lo && lane <= hi)
+                tma_load_3d(base_s + st * SH::STAGE + lane * BOX, &p.tm_x, bar, t0 + (lane - 1) * SEGE,
+                            ld.g * kConvRows, ld.b);
+            conv_tile_advance(ld, step, ntt, ngr);
+        };
+        for (int n = 0; n < NS && n < mine; ++n)
+            issue_load(n);
+        for (int i = 0; i < mine; ++i, conv_tile_advance(sv, step, ntt, ngr)) {
+            const int st = i % NS;
+            mbar_wait(done_s + 8u * st, static_cast<uint32_t>((i / NS) & 1));
+            const int t0 = sv.tt * TT;
+            if (lane < kConvSegs && t0 + lane * SEGE < L)
+                conv_tma_store_3d(&p.tm_out, base_s + st * SH::STAGE + (lane + 1) * BOX, t0 + lane * SEGE,
+                                  sv.g * kConvRows, sv.b);
+            conv_bulk_commit();
+            if (i + NS < mine) {
+                conv_bulk_wait_read<0>();   // the stores have left the stage: refill it
+                __syncwarp();
+                issue_load(i + NS);
             }
         }
-        cp_async_commit();
-        cp_async_wait<0>();
-        __syncthreads();
-        const bool work = act && pc0 + j0 < npieces;
-        // the H inputs before piece j0: hist[i] is input (H - i) steps back
+        conv_bulk_wait_all();
+        return;
+    }
+
+    // the compute warps
+    const int ch = tid & (kConvRows - 1), s = tid / kConvRows;
+    const float tscale = SILU ? -kLog2e : 1.0f;
+    ConvTileIdx cur = first;
+    // the taps of a tile's channel, each in both halves of a pair (scaled for
+    // SILU), loaded one tile ahead
+    auto load_taps = [&](const ConvTileIdx &t, u64 *w2, u64 &bias2) {
+        const int64_t d = static_cast<int64_t>(t.g) * kConvRows + ch;
+        const bool act = d < p.d_inner;
+#pragma unroll
+        for (int k = 0; k < K; ++k)
+            w2[k] = splat(act ? __ldg(p.w + d * K + k) * tscale : 0.0f);
+        bias2 = splat((act && p.bias) ? __ldg(p.bias + d) * tscale : 0.0f);
+    };
+    u64 w2n[K], bias2n;
+    load_taps(cur, w2n, bias2n);
+    for (int i = 0; i < mine; ++i) {
+        u64 w2[K], bias2 = bias2n;
+#pragma unroll
+        for (int k = 0; k < K; ++k)
+            w2[k] = w2n[k];
+        ConvTileIdx nxt = cur;
+        conv_tile_advance(nxt, step, ntt, ngr);
+        if (i + 1 < mine)
+            load_taps(nxt, w2n, bias2n);
+        const int64_t d = static_cast<int64_t>(cur.g) * kConvRows + ch;
+        const bool act = d < p.d_inner;
+        const int st = i % NS;
+        unsigned char *stage = base + st * SH::STAGE;
+        const int ts = cur.tt * TT + s * SEGE;   // first step of this thread's segment
+        const bool live = ts < L;
+        mbar_wait(full_s + 8u * st, static_cast<uint32_t>((i / NS) & 1));
+
+        // hist[j] = input H - j steps before the segment
         float hist[H > 0 ? H : 1];
-        if (work) {
-            float pv[HP * EPP > 0 ? HP * EPP : 1];
+        if (live && H > 0) {
+            if (ts == 0) {
 #pragma unroll
-            for (int v = 0; v < HP; ++v) {
-                const int jp = j0 - HP + v;   // piece index within the tile, negative in the halo
-                const uint4 w = jp < 0 ? tile[r][HP + jp] : tile[r][HP + conv_swz(jp)];
-                unpack_piece<T>(w, pv + v * EPP);
-            }
+                for (int j = 0; j < H; ++j)
+                    hist[j] = (act && p.state_in)
+                                  ? Io<T>::load1(static_cast<const T *>(p.state_in) +
+                                                 (static_cast<int64_t>(cur.b) * H + j) * p.d_inner + d)
+                                  : 0.0f;
+            } else {
+                float pv[HP * EPP > 0 ? HP * EPP : 1];
+                const unsigned char *prev = stage + s * BOX + ch * 128;   // the segment before (the halo for s = 0)
 #pragma unroll
-            for (int i = 0; i < H; ++i)
-                hist[i] = pv[HP * EPP - H + i];
-            if (pc0 + j0 == 0 && p.state_in) {   // steps before 0 come from the carried history
+                for (int v = 0; v < HP; ++v) {
+                    const int c = PPS - HP + v;
+                    unpack_piece<T>(*reinterpret_cast<const uint4 *>(prev + ((c ^ ch) << 4)), pv + v * EPP);
+                }
 #pragma unroll
-                for (int i = 0; i < H; ++i)
-                    hist[i] = Io<T>::load1(static_cast<const T *>(p.state_in) + (b * H + i) * p.d_inner + d);
+                for (int j = 0; j < H; ++j)
+                    hist[j] = pv[HP * EPP - H + j];
             }
         }
-        __syncthreads();   // every thread has its history: pieces may now be overwritten by outputs
-        if (work) {
-#pragma unroll 2
-            for (int m = 0; m < PPL; ++m) {
-                const int j = j0 + m;
-                const int64_t pc = pc0 + j;
-                if (pc >= npieces)
+        conv_compute_sync();   // every history is read: outputs may now replace their inputs
+
+        unsigned char *row = stage + (s + 1) * BOX + ch * 128;
+        if (ts + SEGE <= L) {   // a whole segment: no bound checks, so its pieces overlap
+#pragma unroll
+            for (int m = 0; m < PPS; ++m)
+                conv_tile_piece<T, K, SILU>(row, m, ch, hist, w2, bias2);
+        } else if (live) {
+#pragma unroll
+            for (int m = 0; m < PPS; ++m) {
+                if (ts + m * EPP >= L)
                     break;
-                float v[EPP];
-                unpack_piece<T>(tile[r][HP + conv_swz(j)], v);
-                float o[EPP];
-#pragma unroll
-                for (int e = 0; e < EPP; ++e) {
-                    float acc = bv;
-#pragma unroll
-                    for (int k = 0; k < K; ++k)
-                        acc = fmaf(wd[k], e - k >= 0 ? v[e - k >= 0 ? e - k : 0] : hist[H + e - k >= 0 ? H + e - k : 0],
-                                   acc);
-                    o[e] = p.silu ? silu_f(acc) : acc;
-                }
-                tile[r][HP + conv_swz(j)] = conv_pack<T>(o);   // in place; to HBM below
-                // the last H inputs become the history of the next piece
-                float nh[H > 0 ? H : 1];
-#pragma unroll
-                for (int i = 0; i < H; ++i) {
-                    const int u = EPP - H + i;   // window index relative to v
-                    nh[i] = u >= 0 ? v[u >= 0 ? u : 0] : hist[H + u >= 0 ? H + u : 0];
-                }
-#pragma unroll
-                for (int i = 0; i < H; ++i)
-                    hist[i] = nh[i];
-                if (H > 0 && p.state_out && pc == npieces - 1) {
-#pragma unroll
-                    for (int i = 0; i < H; ++i)
-                        Io<T>::store1(static_cast<T *>(p.state_out) + (b * H + i) * p.d_inner + d, hist[i]);
-                }
+                conv_tile_piece<T, K, SILU>(row, m, ch, hist, w2, bias2);
             }
         }
-        __syncthreads();
-        // outputs to HBM, consecutive threads on consecutive pieces of a row
+        // the segment holding the row's last input leaves the last H inputs as the next call's history
+        if (H > 0 && p.state_out && act && live && ts + SEGE >= L) {
 #pragma unroll
-        for (int rr = 0; rr < CG; ++rr) {
-            const int64_t dr = d0 + rr;
-            if (dr >= p.d_inner)
-                break;
-            T *orow = static_cast<T *>(p.out) + (b * p.d_inner + dr) * p.L;
-            for (int jj = threadIdx.x; jj < PT; jj += kBlock) {
-                const int64_t pc = pc0 + jj;
-                if (pc < npieces)
-                    *reinterpret_cast<uint4 *>(orow + pc * EPP) = tile[rr][HP + conv_swz(jj)];
-            }
+            for (int j = 0; j < H; ++j)
+                Io<T>::store1(static_cast<T *>(p.state_out) + (static_cast<int64_t>(cur.b) * H + j) * p.d_inner + d,
+                              hist[j]);
         }
-        __syncthreads();   // the tile is reused by the next batch row
+        conv_fence_async_smem();   // the outputs, written by threads, are read by the tensor stores
+        conv_mbar_arrive(done_s + 8u * st);
+        cur = nxt;
     }
 }
 
@@ -410,27 +571,69 @@ conv_state_update_kernel(const ConvStepParams p)
     }
 }
 
-template <typename T, int K>
-ss_status launch_conv(const ConvParams &p, cudaStream_t stream)
+// map of a (batch, d_inner, L) tensor of T as (L, d_inner, batch), box
+// (128 bytes, kConvRows, 1) with the 128-byte swizzle; reads outside the
+// tensor give zero, writes outside it are dropped
+template <typename T>
+bool conv_encode(CUtensorMap *m, const void *base, int64_t L, int64_t d_inner, int64_t batch)
 {
+    const EncodeTiledFn fn = encode_tiled_fn();
+    if (!fn)
+        return false;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(L), static_cast<cuuint64_t>(d_inner),
+                                static_cast<cuuint64_t>(batch)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(L) * sizeof(T),
+                                   static_cast<cuuint64_t>(L) * static_cast<cuuint64_t>(d_inner) * sizeof(T)};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / sizeof(T)), kConvRows, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUtensorMapDataType dt = sizeof(T) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    return fn(m, dt, 3, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// resident CTAs of the tile kernel per SM, after raising its shared-memory limit; 0 on failure
+template <typename T, int K, bool SILU>
+int conv_tile_setup()
+{
+    static const int per_sm = [] {
+        auto kernel = causal_conv1d_tile_kernel<T, K, SILU>;
+        const int smem = ConvTileShape<T>::BYTES;
+        int n = 0;
+        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, kConvThreads, smem) != cudaSuccess) {
+            cudaGetLastError();
+            return 0;
+        }
+        return n;
+    }();
+    return per_sm;
+}
+
+template <typename T, int K, bool SILU>
+ss_status launch_conv_tile(const ConvParams &p, int dev, cudaStream_t stream)
+{
+    using SH = ConvTileShape<T>;
+    const int per_sm = conv_tile_setup<T, K, SILU>();
+    if (per_sm <= 0)
+        return fail(SS_ERR_LAUNCH, "conv tile kernel cannot be made resident (%d bytes of shared memory)", SH::BYTES);
+    const int64_t grid = std::min<int64_t>(p.ntiles, static_cast<int64_t>(sm_count(dev)) * per_sm);
+    causal_conv1d_tile_kernel<T, K, SILU><<<static_cast<unsigned>(grid), kConvThreads, SH::BYTES, stream>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return fail(SS_ERR_LAUNCH, "conv launch failed: %s", cudaGetErrorString(e));
+    return SS_OK;
+}
+
+template <typename T, int K>
+ss_status launch_conv(const ConvParams &p, int dev, cudaStream_t stream)
+{
+    if (p.tma)
+        return p.silu ? launch_conv_tile<T, K, true>(p, dev, stream) : launch_conv_tile<T, K, false>(p, dev, stream);
     constexpr int EPP = 16 / (int)sizeof(T);
     const int64_t pblocks = ((p.L + EPP - 1) / EPP + kBlock - 1) / kBlock;
     if (pblocks > 0x7fffffff)
         return fail(SS_ERR_DIM, "grid too large");
-    if (p.vec) {
-        constexpr int PT = kConvTileBytes / 16;
-        const int64_t tblocks = (p.L / EPP + PT - 1) / PT;
-        if (tblocks > 0x7fffffff || (p.d_inner + kConvRows - 1) / kConvRows > 65535)
-            return fail(SS_ERR_DIM, "grid too large");
-        const dim3 g(static_cast<unsigned>(tblocks),
-                     static_cast<unsigned>((p.d_inner + kConvRows - 1) / kConvRows),
-                     static_cast<unsigned>(std::min<int64_t>(p.batch, 65535)));
-        causal_conv1d_tile_kernel<T, K><<<g, kBlock, 0, stream>>>(p);
-        cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess)
-            return fail(SS_ERR_LAUNCH, "conv launch failed: %s", cudaGetErrorString(e));
-        return SS_OK;
-    }
     constexpr int R = 2;
     const dim3 grid(static_cast<unsigned>(pblocks),
                     static_cast<unsigned>(std::min<int64_t>((p.d_inner + R - 1) / R, 65535)),
@@ -465,15 +668,28 @@ ss_status causal_conv1d(const void *x, const float *w, const float *bias, const 
     p.out = out; p.state_out = k > 1 ? state_out : nullptr;
     p.batch = batch; p.d_inner = d_inner; p.L = L; p.silu = silu ? 1 : 0;
     p.vec = ((L * static_cast<int64_t>(sizeof(T))) % 16 == 0) && aligned16(x) && aligned16(out);
+    // tensor coordinates and tile numbers are 32-bit: the tile kernel takes
+    // rows below 2^31 steps (a tile's last step included) and fewer than 2^31 tiles
+    {
+        const int64_t ntt = (L + ConvTileShape<T>::TT - 1) / ConvTileShape<T>::TT;
+        const int64_t ngr = (d_inner + kConvRows - 1) / kConvRows;
+        const bool fits = L < (int64_t(1) << 31) - ConvTileShape<T>::TT && ngr < (int64_t(1) << 27) &&
+                          ntt * ngr < (int64_t(1) << 31) / batch;
+        p.ntt = fits ? static_cast<int>(ntt) : 0;
+        p.ngr = fits ? static_cast<int>(ngr) : 0;
+        p.ntiles = fits ? static_cast<int>(ntt * ngr * batch) : 0;
+        p.tma = p.vec && fits && conv_encode<T>(&p.tm_x, x, L, d_inner, batch) &&
+                conv_encode<T>(&p.tm_out, out, L, d_inner, batch);
+    }
     switch (k) {
-    case 1: return launch_conv<T, 1>(p, stream);
-    case 2: return launch_conv<T, 2>(p, stream);
-    case 3: return launch_conv<T, 3>(p, stream);
-    case 4: return launch_conv<T, 4>(p, stream);
-    case 5: return launch_conv<T, 5>(p, stream);
-    case 6: return launch_conv<T, 6>(p, stream);
-    case 7: return launch_conv<T, 7>(p, stream);
-    default: return launch_conv<T, 8>(p, stream);
+    case 1: return launch_conv<T, 1>(p, dev, stream);
+    case 2: return launch_conv<T, 2>(p, dev, stream);
+    case 3: return launch_conv<T, 3>(p, dev, stream);
+    case 4: return launch_conv<T, 4>(p, dev, stream);
+    case 5: return launch_conv<T, 5>(p, dev, stream);
+    case 6: return launch_conv<T, 6>(p, dev, stream);
+    case 7: return launch_conv<T, 7>(p, dev, stream);
+    default: return launch_conv<T, 8>(p, dev, stream);
     }
 }
 

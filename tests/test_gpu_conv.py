@@ -25,7 +25,10 @@ CASES = [(1, 1, 1, 4), (2, 3, 3, 4), (2, 5, 7, 4), (1, 16, 8, 4), (3, 33, 9, 4),
          (1, 40, 257, 1), (2, 40, 64, 2), (2, 40, 65, 3), (2, 24, 131, 5), (1, 24, 96, 6), (1, 24, 77, 7),
          (2, 24, 200, 8), (8, 1536, 2048, 4),
          # several shared-memory tiles per row, history longer than a piece, L shorter than the history
-         (2, 17, 2056, 6), (1, 12, 3072, 8), (2, 9, 4, 8), (3, 11, 1032, 4)]
+         (2, 17, 2056, 6), (1, 12, 3072, 8), (2, 9, 4, 8), (3, 11, 1032, 4),
+         # tensor-copy tiles: channels past the last group of 8, a row ending inside a segment,
+         # a row of one piece, a last tile of one segment, many tiles per CTA
+         (2, 13, 136, 4), (1, 5, 8, 4), (2, 20, 1088, 8), (4, 24, 3000, 3), (2, 7, 16, 2), (16, 64, 4096, 4)]
 
 
 @pytest.mark.parametrize("io", ["bf16", "f32"])
