@@ -97,16 +97,17 @@ def measured_peaks() -> dict:
 
 
 # the source part each profiled kernel lives in (besides the shared device helpers)
-KERNEL_PART = {"scan_fwd_": "scan_fwd.cuh", "state_update_": "decode.cuh", "scan_bwd_": "scan_bwd.cuh",
-               "conv1d_": "conv.cuh", "conv_state_update_": "conv.cuh", "ssd_chunk_": "ssd.cuh"}
+KERNEL_PART = {"scan_fwd_": ("scan_fwd.cuh",), "state_update_": ("decode.cuh",),
+               "scan_bwd_": ("scan_bwd.cuh",), "conv1d_": ("conv.cuh",), "conv_state_update_": ("conv.cuh",),
+               "ssd_chunk_": ("ssd.cuh",)}
 
 
 def kernel_source_hash(kernel_key: str) -> str:
-    """sha256 of the shared device helpers followed by the kernel's own part."""
-    part = next(v for k, v in KERNEL_PART.items() if kernel_key.startswith(k))
+    """sha256 of the shared device helpers followed by the kernel's own files."""
+    parts = next(v for k, v in KERNEL_PART.items() if kernel_key.startswith(k))
     csrc = os.path.dirname(SRC)
     h = hashlib.sha256()
-    for name in ("device_common.cuh", part):
+    for name in ("device_common.cuh", *parts):
         h.update(open(os.path.join(csrc, name), "rb").read())
     return h.hexdigest()
 

@@ -592,22 +592,28 @@ bool conv_encode(CUtensorMap *m, const void *base, int64_t L, int64_t d_inner, i
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// resident CTAs of the tile kernel per SM, after raising its shared-memory limit; 0 on failure
+// resident CTAs of the tile kernel per SM, after raising its shared-memory
+// limit on the current device (every call: the limit is a per-device
+// attribute); 0 on failure
 template <typename T, int K, bool SILU>
 int conv_tile_setup()
 {
-    static const int per_sm = [] {
-        auto kernel = causal_conv1d_tile_kernel<T, K, SILU>;
-        const int smem = ConvTileShape<T>::BYTES;
-        int n = 0;
-        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
-            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, kConvThreads, smem) != cudaSuccess) {
+    static std::atomic<int> per_sm{-1};
+    auto kernel = causal_conv1d_tile_kernel<T, K, SILU>;
+    const int smem = ConvTileShape<T>::BYTES;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    int n = per_sm.load(std::memory_order_relaxed);
+    if (n < 0) {
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, kConvThreads, smem) != cudaSuccess) {
             cudaGetLastError();
             return 0;
         }
-        return n;
-    }();
-    return per_sm;
+        per_sm.store(n, std::memory_order_relaxed);
+    }
+    return n;
 }
 
 template <typename T, int K, bool SILU>
