@@ -863,6 +863,12 @@ def main(argv=None):
         extras["bwd_" + HEADLINE.name] = {
             "elem_steps_per_s": HEADLINE.elem_steps / (bms * 1e-3), "kernel_ms_median": bms,
             "roofline": bro, "note": "backward pass (all gradients, states recomputed), L2 flushed before each"}
+        lbms = time_bwd(I.LONGSEQ, 3, 1)
+        extras["bwd_" + I.LONGSEQ.name] = {
+            "elem_steps_per_s": I.LONGSEQ.elem_steps / (lbms * 1e-3), "kernel_ms_median": lbms,
+            "roofline": roofline_obj(bwd_alg_bytes(I.LONGSEQ), lbms, peaks, None),
+            "note": "backward pass on the long sequence (batch 1, d_inner 2048, L 131072): 64 channel groups "
+                    "walk the whole row each way, L2 flushed before each"}
         vbms = time_bwd(HEADLINE, 10, 3, variant=True)
         extras["bwd_reverse_starts_" + HEADLINE.name] = {
             "elem_steps_per_s": HEADLINE.elem_steps / (vbms * 1e-3), "kernel_ms_median": vbms,

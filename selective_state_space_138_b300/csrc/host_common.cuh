@@ -83,6 +83,31 @@ int sm_count(int dev)
     return sms;
 }
 
+// ------------------------------------------------------------------ sequence segments
+
+// Segments per channel group of a scan walk (the forward n-split kernel and
+// the backward pass): when the channel groups fill less than half of the CTA
+// slots of the GPU, the sequence is cut into up to 8 segments (one
+// thread-block cluster per group) so that the grid fills one wave, keeping at
+// least 4 chunks per segment. The environment variable env_name, when set to
+// 1..8, overrides the choice.
+int pick_segments(int64_t groups, int64_t L, int64_t lc, int64_t slots, const char *env_name)
+{
+    const char *env = getenv(env_name);
+    if (env) {
+        const int v = atoi(env);
+        if (v >= 1 && v <= 8)
+            return v;
+    }
+    if (2 * groups > slots)
+        return 1;
+    int64_t n = slots / groups;
+    n = n < 8 ? n : 8;
+    const int64_t by_len = L / (4 * lc);
+    n = n < by_len ? n : by_len;
+    return n < 1 ? 1 : static_cast<int>(n);
+}
+
 // ------------------------------------------------------------------ tensor maps (cuTensorMapEncodeTiled)
 
 using EncodeTiledFn = PFN_cuTensorMapEncodeTiled_v12000;

@@ -35,6 +35,18 @@
 //            added over the warps by the epilogue, which forms dx, ddt, dz.
 // dB, dC, dA, dD and ddt_bias are accumulated with atomic adds into buffers the
 // host clears first (the order of those fp32 additions is not fixed).
+//
+// Long rows with few channel groups (forward direction, no sequence starts)
+// are cut into segments that form a thread-block cluster, as in the forward
+// scan. Phase 1: every segment but the last walks its steps from a zero state
+// without storing and publishes its end state and step sum; each segment folds
+// the maps of the segments before it, h <- exp(A sum delta) h + h_end, through
+// distributed shared memory, and walks again storing its states. Phase 2:
+// every segment but the first walks the adjoint alone over its steps from
+// zero, in reverse (lam += C gy, lam *= a), and publishes what flows out of
+// its first step and its step sum; each segment folds the segments after it
+// from the right, X <- X_zero + exp(A sum delta) X (the last from dfinal), and
+// runs its reverse walk from that adjoint.
 
 struct BwdParams {
     const void *x, *dt, *B, *C, *z, *dout;
@@ -47,6 +59,9 @@ struct BwdParams {
     int vec;    // io rows 16-byte aligned with L a multiple of the piece
     int vec4;   // dB, dC rows take 16-byte atomic adds (L % 4 == 0, aligned)
     int states_ready;   // the workspace already holds the stored states (written by the forward pass)
+    int nseg;           // segments per channel group (a thread-block cluster when > 1; forward direction,
+                        // no sequence starts)
+    int64_t seg_len;    // steps per segment, a multiple of the chunk length
     const uint8_t *reset;   // (batch, L) sequence starts (RST kernels only)
     int tma;                // the tiles come in through the tensor maps below
     // 3-d maps over (step, row, batch row) as in the forward scan: x, dt, z,
@@ -81,8 +96,10 @@ struct BwdShape {
     static constexpr int PART_BYTES = 3 * S * HC * CH * 4;
     static constexpr int DBC_BYTES = 2 * LC * NS * 4;
     static constexpr int R_BYTES = LC;                          // sequence starts of a chunk
+    static constexpr int HX_BYTES = S * CH * 16;                // a segment's end state or adjoint outflow
+    static constexpr int SX_BYTES = S * CH * 4;                 // a segment's step sums (per prep thread)
     static constexpr size_t BAR_OFF = (size_t)STAGES * STAGE_BYTES + PD_BYTES + DY_BYTES + 2 * BC_BYTES +
-                                      PART_BYTES + DBC_BYTES + R_BYTES;   // "slot filled" barriers
+                                      PART_BYTES + DBC_BYTES + R_BYTES + HX_BYTES + SX_BYTES;   // "slot filled" barriers
     static constexpr size_t BYTES = BAR_OFF + 8 * STAGES;
     static_assert(STAGE_BYTES % 128 == 0 && RAW_X % 128 == 0 && RAW_BC % 128 == 0 && BAR_OFF % 8 == 0,
                   "tensor-copy tiles on 128-byte boundaries");
@@ -124,6 +141,8 @@ scan_bwd_kernel(const __grid_constant__ BwdParams p)
     float *Part = Cf + LC * NS;                                             // [3][S][HC/2][CH] step pairs
     float *DBC = Part + 3 * S * HC * CH;                                    // [2][LC][NS]
     unsigned char *Rst = reinterpret_cast<unsigned char *>(DBC + 2 * LC * NS);  // [LC] sequence starts
+    float4 *Hx = reinterpret_cast<float4 *>(Rst + SH::R_BYTES);             // [S][CH] published per lane
+    float *Sx = reinterpret_cast<float *>(Hx + S * CH);                      // [S][CH] step sums per prep thread
     const uint32_t raw_s = static_cast<uint32_t>(__cvta_generic_to_shared(raw));
     const uint32_t bars_s = raw_s + static_cast<uint32_t>(SH::BAR_OFF);
     if (TMA && (raw_s & 127u) != 0) {   // tensor copies need 128-byte aligned destinations
@@ -134,14 +153,20 @@ scan_bwd_kernel(const __grid_constant__ BwdParams p)
 
     const int tid = threadIdx.x;
     const int64_t b = blockIdx.y;
-    const int64_t d0 = static_cast<int64_t>(blockIdx.x) * CH;
+    const int nseg = p.nseg;
+    const int seg = static_cast<int>(blockIdx.x % static_cast<unsigned>(nseg));
+    const int64_t d0 = static_cast<int64_t>(blockIdx.x / static_cast<unsigned>(nseg)) * CH;
     const int64_t L = p.L, N = p.N, Dn = p.d_inner;
     const bool vec = p.vec != 0;
-    const int64_t nchunks = (L + LC - 1) / LC;
+    // this segment's chunks [c_lo, c_hi) (the whole row when nseg = 1)
+    const int64_t seg_chunks = p.seg_len / LC;
+    const int64_t c_lo = seg * seg_chunks;
+    const int64_t c_hi = ((L + LC - 1) / LC < c_lo + seg_chunks) ? (L + LC - 1) / LC : c_lo + seg_chunks;
+    const int64_t nchunks = c_hi - c_lo;
     // physical chunk of the j-th chunk of the forward walk (phase 1) and of the
     // reverse walk (phase 2); physical step in a chunk of walking step u
-    auto phys1 = [&](int64_t j) -> int64_t { return REV ? nchunks - 1 - j : j; };
-    auto phys2 = [&](int64_t j) -> int64_t { return REV ? j : nchunks - 1 - j; };
+    auto phys1 = [&](int64_t j) -> int64_t { return REV ? c_hi - 1 - j : c_lo + j; };
+    auto phys2 = [&](int64_t j) -> int64_t { return REV ? c_lo + j : c_hi - 1 - j; };
     auto tu = [](int u) { return REV ? LC - 1 - u : u; };
 
     const int cs = tid % CH;     // scan role: lane = channel, warp = state group
@@ -309,6 +334,17 @@ scan_bwd_kernel(const __grid_constant__ BwdParams p)
         }
     };
 
+    // this thread's compensated sum of the steps it prepares while `summing`
+    // (the segment folds)
+    float ssum = 0.0f, scomp = 0.0f;
+    bool summing = false;
+    auto kahan = [&](float v) {
+        const float yv = v - scomp;
+        const float tv = ssum + yv;
+        scomp = (tv - ssum) - yv;
+        ssum = tv;
+    };
+
     // delta, delta*x (and, in phase 2, gy) of this thread's steps of chunk k
     auto prep = [&](int64_t k, int slot, bool phase2) {
         const unsigned char *st = raw + slot * SH::STAGE_BYTES;
@@ -335,6 +371,10 @@ scan_bwd_kernel(const __grid_constant__ BwdParams p)
             upk(s2, s0, s1);
             s0 = i < lim ? s0 : 0.0f;
             s1 = i + 1 < lim ? s1 : 0.0f;
+            if (summing) {
+                kahan(s0);
+                kahan(s1);
+            }
             float sx0, sx1;
             upk(mul2(pk(s0, s1), xx), sx0, sx1);
             Pd[(re * RL + i) * CH + ce] = pk(s0, sx0);
@@ -368,7 +408,9 @@ scan_bwd_kernel(const __grid_constant__ BwdParams p)
         h01 = pk(hv[0], hv[1]);
         h23 = pk(hv[2], hv[3]);
     }
-    if (!p.states_ready) {
+    // phase 1 over this segment's chunks from the state in (h01, h23); with
+    // `store`, the state at every sub-chunk start goes to the workspace
+    auto walk1 = [&](bool store) {
 #pragma unroll
         for (int s = 0; s < STAGES - 1; ++s)
             if (s < nchunks)
@@ -390,7 +432,7 @@ scan_bwd_kernel(const __grid_constant__ BwdParams p)
 #pragma unroll
             for (int hw = 0; hw < NH; ++hw) {
                 const int64_t s = k * NH + (REV ? NH - 1 - hw : hw);   // physical sub-chunk
-                if (act_s && s < p.nsub) {
+                if (store && act_s && s < p.nsub) {
                     float a0, a1, a2, a3;
                     upk(h01, a0, a1);
                     upk(h23, a2, a3);
@@ -427,6 +469,57 @@ scan_bwd_kernel(const __grid_constant__ BwdParams p)
         }
         cp_async_wait<0>();
         __syncthreads();
+    };
+
+    // the lane's four values as one word for the peers of its cluster, and back
+    auto publish = [&](u64 v01, u64 v23) {
+        float a0, a1, a2, a3;
+        upk(v01, a0, a1);
+        upk(v23, a2, a3);
+        Hx[q * CH + cs] = make_float4(a0, a1, a2, a3);
+        Sx[re * CH + ce] = ssum;
+    };
+    // (segment i's value for this lane, exp(A * segment i's step sum)), read through distributed shared memory
+    auto peer = [&](cg::cluster_group &cl, int i, u64 &v01, u64 &v23, u64 &a01, u64 &a23) {
+        const float4 *ph = cl.map_shared_rank(Hx, i);
+        const float *ps = cl.map_shared_rank(Sx, i);
+        float tot = 0.0f;
+#pragma unroll
+        for (int r = 0; r < S; ++r)
+            tot += ps[r * CH + cs];
+        const float4 v = ph[q * CH + cs];
+        v01 = pk(v.x, v.y);
+        v23 = pk(v.z, v.w);
+        a01 = ex2_2(mul2(splat(tot), A01));
+        a23 = ex2_2(mul2(splat(tot), A23));
+    };
+
+    if (!p.states_ready) {
+        if (nseg > 1) {
+            cg::cluster_group cluster = cg::this_cluster();
+            const u64 g01 = h01, g23 = h23;   // the state entering segment 0
+            if (seg != nseg - 1) {            // the end state of this segment from a zero start
+                h01 = 0;
+                h23 = 0;
+                ssum = scomp = 0.0f;
+                summing = true;
+                walk1(false);
+                summing = false;
+            }
+            publish(h01, h23);
+            cluster.sync();
+            u64 f01 = g01, f23 = g23;
+            for (int i = 0; i < seg; ++i) {   // h <- exp(A sum delta) h + h_end over the segments before
+                u64 e01, e23, a01, a23;
+                peer(cluster, i, e01, e23, a01, a23);
+                f01 = fma2(a01, f01, e01);
+                f23 = fma2(a23, f23, e23);
+            }
+            cluster.sync();   // the peers have read this CTA's values
+            h01 = f01;
+            h23 = f23;
+        }
+        walk1(true);
     }
 
     // ---- phase 2: reverse
@@ -446,9 +539,84 @@ scan_bwd_kernel(const __grid_constant__ BwdParams p)
     T *dzr = gate && p.dz ? static_cast<T *>(p.dz) + (b * Dn + de) * L : nullptr;
     const u64 ln2_2 = splat(0.6931471805599453f);
 
+    if (nseg > 1) {
+        // the adjoint of this segment alone (zero inflow), walked in reverse over
+        // its chunks: lam += C gy, lam *= a; what flows out of its first step
+        auto walk2pre = [&]() {
+#pragma unroll 1
+            for (int s2 = 0; s2 < STAGES - 1; ++s2)
+                if (s2 < nchunks)
+                    stage_in(phys2(s2), s2, true);
+                else
+                    cp_async_commit();
+            cp_async_wait<STAGES - 2>();
+            wait_slot(0);
+            __syncthreads();
+            prep(phys2(0), 0, true);
+            convert_bc(0, true);
+            __syncthreads();
+#pragma unroll 1
+            for (int64_t j = 0; j < nchunks; ++j) {
+                if (j + STAGES - 1 < nchunks)
+                    stage_in(phys2(j + STAGES - 1), static_cast<int>((j + STAGES - 1) % STAGES), true);
+                else
+                    cp_async_commit();
+#pragma unroll 4
+                for (int u = 0; u < LC; ++u) {
+                    const int t = LC - 1 - u;
+                    float dl, dx;
+                    upk(Pd[t * CH + cs], dl, dx);
+                    const u64 gy2 = splat(DY[t * CH + cs]);
+                    const ulonglong2 Cq = *reinterpret_cast<const ulonglong2 *>(Cq_s + t * NS);
+                    const u64 dd = splat(dl);
+                    lam01 = fma2(Cq.x, gy2, lam01);
+                    lam23 = fma2(Cq.y, gy2, lam23);
+                    lam01 = mul2(lam01, ex2_2(mul2(dd, A01)));
+                    lam23 = mul2(lam23, ex2_2(mul2(dd, A23)));
+                }
+                cp_async_wait<STAGES - 2>();
+                if (j + 1 < nchunks)
+                    wait_slot(static_cast<int>((j + 1) % STAGES));
+                __syncthreads();
+                if (j + 1 < nchunks) {
+                    const int nslot = static_cast<int>((j + 1) % STAGES);
+                    prep(phys2(j + 1), nslot, true);
+                    convert_bc(nslot, true);
+                }
+                __syncthreads();
+            }
+            cp_async_wait<0>();
+            __syncthreads();
+        };
+        cg::cluster_group cluster = cg::this_cluster();
+        const u64 l01 = lam01, l23 = lam23;   // dfinal, the inflow of the last segment
+        if (seg != 0) {
+            lam01 = 0;
+            lam23 = 0;
+            ssum = scomp = 0.0f;
+            summing = true;
+            walk2pre();
+            summing = false;
+        }
+        publish(lam01, lam23);
+        cluster.sync();
+        u64 f01 = l01, f23 = l23;
+        for (int i = nseg - 1; i > seg; --i) {   // X <- X_zero + exp(A sum delta) X over the segments after
+            u64 x01, x23, a01, a23;
+            peer(cluster, i, x01, x23, a01, a23);
+            f01 = fma2(a01, f01, x01);
+            f23 = fma2(a23, f23, x23);
+        }
+        cluster.sync();   // the peers have read this CTA's values
+        lam01 = f01;
+        lam23 = f23;
+    }
+
     float4 ck_cur = make_float4(0.f, 0.f, 0.f, 0.f);   // stored state of the sub-chunk processed next
-    if (act_s)   // the last sub-chunk of the forward walk comes first
-        ck_cur = ck[(REV ? 0 : p.nsub - 1) * ckstride];
+    if (act_s) {   // the last sub-chunk of the forward walk comes first
+        const int64_t s_end = p.nsub < c_hi * NH ? p.nsub : c_hi * NH;   // past this segment's last sub-chunk
+        ck_cur = ck[(REV ? c_lo * NH : s_end - 1) * ckstride];
+    }
 
     // chunk j of the reverse walk is physical chunk phys2(j)
 #pragma unroll 1
@@ -721,7 +889,7 @@ scan_bwd_kernel(const __grid_constant__ BwdParams p)
         for (int e = 0; e < 4; ++e)
             if (4 * q + e < N)
                 atomicAdd(p.dA + ds * N + 4 * q + e, v[e]);
-        if (p.dh0) {
+        if (p.dh0 && seg == 0) {
             float l[4];
             upk(lam01, l[0], l[1]);
             upk(lam23, l[2], l[3]);
@@ -748,10 +916,10 @@ scan_bwd_kernel(const __grid_constant__ BwdParams p)
 // ------------------------------------------------------------------ backward host side
 
 template <typename T, int S, bool REV, bool RST>
-ss_status launch_bwd(const BwdParams &p, cudaStream_t stream)
+ss_status launch_bwd(const BwdParams &p0, cudaStream_t stream, int sms)
 {
     using SH = BwdShape<T, S>;
-    auto kernel = p.tma ? scan_bwd_kernel<T, S, REV, RST, true> : scan_bwd_kernel<T, S, REV, RST, false>;
+    auto kernel = p0.tma ? scan_bwd_kernel<T, S, REV, RST, true> : scan_bwd_kernel<T, S, REV, RST, false>;
     const size_t smem = SH::BYTES;
     if (smem > 48u * 1024u) {
         cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -761,14 +929,57 @@ ss_status launch_bwd(const BwdParams &p, cudaStream_t stream)
             return fail(SS_ERR_LAUNCH, "cudaFuncSetAttribute failed: %s", cudaGetErrorString(e));
         }
     }
+    BwdParams p = p0;
     const int64_t gpr = (p.d_inner + SH::CH - 1) / SH::CH;
-    if (gpr > 0x7fffffff || p.batch > 65535)
-        return fail(SS_ERR_DIM, "grid too large: %lld channel blocks x %lld batch rows", (long long)gpr,
+    const int64_t nchunks = (p.L + SH::LC - 1) / SH::LC;
+    // segments (thread-block clusters) for long rows with few channel groups:
+    // forward direction without sequence starts only
+    int nseg = 1;
+    if (!REV && !RST) {
+        int occ = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, SH::NT, smem) != cudaSuccess || occ < 1) {
+            cudaGetLastError();
+            occ = 1;
+        }
+        nseg = pick_segments(gpr * p.batch, p.L, SH::LC, static_cast<int64_t>(sms) * occ, "SS_BWD_SEGMENTS");
+    }
+    int64_t seg_chunks = (nchunks + nseg - 1) / nseg;
+    nseg = static_cast<int>((nchunks + seg_chunks - 1) / seg_chunks);
+    if (gpr * nseg > 0x7fffffff || p.batch > 65535)
+        return fail(SS_ERR_DIM, "grid too large: %lld channel blocks x %lld batch rows", (long long)(gpr * nseg),
                     (long long)p.batch);
-    kernel<<<dim3(static_cast<unsigned>(gpr), static_cast<unsigned>(p.batch)), SH::NT, smem, stream>>>(p);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess)
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.gridDim = dim3(static_cast<unsigned>(gpr * nseg), static_cast<unsigned>(p.batch));
+    cfg.blockDim = dim3(SH::NT);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    if (nseg > 1) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = nseg;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int clusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg) != cudaSuccess || clusters < 1) {
+            cudaGetLastError();   // a cluster of this size cannot be placed: do not split
+            nseg = 1;
+            seg_chunks = nchunks;
+            cfg.gridDim.x = static_cast<unsigned>(gpr);
+            cfg.attrs = nullptr;
+            cfg.numAttrs = 0;
+        }
+    }
+    p.nseg = nseg;
+    p.seg_len = seg_chunks * SH::LC;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, p);
+    if (e == cudaSuccess)
+        e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        cudaGetLastError();
         return fail(SS_ERR_LAUNCH, "backward kernel launch failed: %s", cudaGetErrorString(e));
+    }
     return SS_OK;
 }
 
@@ -794,13 +1005,13 @@ bool encode_bwd_maps(BwdParams &p)
 }
 
 template <typename T, int S>
-ss_status dispatch_bwd(const BwdParams &p, bool reverse, cudaStream_t stream)
+ss_status dispatch_bwd(const BwdParams &p, bool reverse, cudaStream_t stream, int sms)
 {
     const bool rst = p.reset != nullptr;
-    if (!reverse && !rst) return launch_bwd<T, S, false, false>(p, stream);
-    if (!reverse) return launch_bwd<T, S, false, true>(p, stream);
-    if (!rst) return launch_bwd<T, S, true, false>(p, stream);
-    return launch_bwd<T, S, true, true>(p, stream);
+    if (!reverse && !rst) return launch_bwd<T, S, false, false>(p, stream, sms);
+    if (!reverse) return launch_bwd<T, S, false, true>(p, stream, sms);
+    if (!rst) return launch_bwd<T, S, true, false>(p, stream, sms);
+    return launch_bwd<T, S, true, true>(p, stream, sms);
 }
 
 template <typename T>
@@ -873,10 +1084,11 @@ ss_status scan_bwd(const void *x, const void *dt, const float *A, const void *B,
     p.tma = (p.vec && aligned16(B) && aligned16(C) && encode_bwd_maps<T>(p)) ? 1 : 0;
     const int64_t S = bwd_groups(N);
     const bool rev = reverse != 0;
-    if (S == 1) return dispatch_bwd<T, 1>(p, rev, stream);
-    if (S == 2) return dispatch_bwd<T, 2>(p, rev, stream);
-    if (S == 4) return dispatch_bwd<T, 4>(p, rev, stream);
-    return dispatch_bwd<T, 8>(p, rev, stream);
+    const int sms = sm_count(dev);
+    if (S == 1) return dispatch_bwd<T, 1>(p, rev, stream, sms);
+    if (S == 2) return dispatch_bwd<T, 2>(p, rev, stream, sms);
+    if (S == 4) return dispatch_bwd<T, 4>(p, rev, stream, sms);
+    return dispatch_bwd<T, 8>(p, rev, stream, sms);
 }
 
 // ------------------------------------------------------------------ built-in scratch (no caller workspace)

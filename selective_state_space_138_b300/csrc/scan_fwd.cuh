@@ -872,27 +872,6 @@ ss_status dispatch_scan_lanes(const ScanParams &p, int lanes, cudaStream_t s)
     }
 }
 
-// Segments per channel group for the n-split kernel: when the channel groups
-// fill less than half of the CTA slots of the GPU, the sequence is cut into
-// up to 8 segments (one thread-block cluster per group) so that the grid
-// fills one wave, keeping at least 4 chunks per segment.
-int pick_segments(int64_t groups, int64_t L, int64_t lc, int64_t slots)
-{
-    const char *env = getenv("SS_SCAN_SEGMENTS");
-    if (env) {
-        const int v = atoi(env);
-        if (v >= 1 && v <= 8)
-            return v;
-    }
-    if (2 * groups > slots)
-        return 1;
-    int64_t n = slots / groups;
-    n = n < 8 ? n : 8;
-    const int64_t by_len = L / (4 * lc);
-    n = n < by_len ? n : by_len;
-    return n < 1 ? 1 : static_cast<int>(n);
-}
-
 // ------------------------------------------------------------------ tensor maps of the n-split kernel
 
 // The n-split kernel's tiles as tensor maps: x, dt, z by channel rows with a
@@ -939,7 +918,7 @@ ss_status launch_nsplit(const ScanParams &p0, cudaStream_t stream, int sms)
         cudaGetLastError();
         occ = 1;
     }
-    int nseg = pick_segments(gpr * p.batch, p.L, SH::LC, static_cast<int64_t>(sms) * occ);
+    int nseg = pick_segments(gpr * p.batch, p.L, SH::LC, static_cast<int64_t>(sms) * occ, "SS_SCAN_SEGMENTS");
     int64_t seg_len = (p.L + nseg - 1) / nseg;
     seg_len = (seg_len + SH::LC - 1) / SH::LC * SH::LC;
     nseg = static_cast<int>((p.L + seg_len - 1) / seg_len);

@@ -108,6 +108,32 @@ def test_bwd_headline_layer_full():
     run_case(I.MAMBA130M)
 
 
+SEG_SHAPES = [("bf16", (1, 64, 8192, 16)), ("bf16", (2, 40, 5000, 16)), ("bf16", (1, 33, 3000, 8)),
+              ("bf16", (1, 32, 1024, 4)), ("f32", (2, 40, 5000, 16)), ("f32", (1, 33, 3000, 8)),
+              ("f32", (1, 32, 1024, 4))]
+
+
+@pytest.mark.parametrize("io,shape", SEG_SHAPES, ids=lambda v: v if isinstance(v, str) else "b%d_d%d_l%d_n%d" % v)
+def test_bwd_segments_match_oracle(shape, io):
+    """Rows long enough, with channel groups few enough, to be cut into
+    cluster segments (up to 8): the folds of the states and of the adjoint
+    across segments, a last segment that ends inside a chunk, an initial state
+    and a final-state gradient."""
+    b, d, L, N = shape
+    spec = I.ScanSpec(b, d, L, N, io=io, seed=2000 + L + N)
+    run_case(spec, use_h0=True)
+    assert binding.device_faults() == 0
+
+
+def test_bwd_long_sequence_full():
+    """The long-sequence workload (batch 1, d_inner 2048, L 131072, N 16,
+    bf16): one channel group per 32 channels walks 4096 chunks each way; every
+    gradient element against the oracle."""
+    errs = run_case(I.LONGSEQ)
+    assert binding.device_faults() == 0
+    print("long sequence backward: max normalised errors", errs)
+
+
 def test_bwd_variant_headline_layer_full():
     """The variant the benchmark times: the backward of the reverse-direction
     scan with a sequence start every 250 steps on the headline layer shape,
