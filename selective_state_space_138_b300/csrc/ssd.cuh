@@ -532,17 +532,7 @@ ssd_chunk_tc_kernel(const __grid_constant__ SsdParams p)
         const int valid = static_cast<int>(p.L - t0 < Q ? p.L - t0 : Q);
         const uint32_t xs_s = base_s + SH::X_OFF;
         const unsigned char *xt = base + SH::X_OFF;
-        // the gate inputs of this thread's epilogue piece (row 16w + lane % 16, 32 channels),
-        // fetched now so that their latency hides behind the chunk's other work
         uint4 zpre[4];
-        {
-            const int t = 16 * w + (lane & 15), half = lane >> 4;
-            const int64_t ro = (b * p.L + t0 + t) * xs + static_cast<int64_t>(h) * P + 32 * half;
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-                zpre[k] = (gate && t < valid) ? __ldg(reinterpret_cast<const uint4 *>(p.z + ro + 8 * k))
-                                              : make_uint4(0, 0, 0, 0);
-        }
         // ---- step sizes (zero past L), a_s and the next chunk's raw steps
         if (tid < Q) {
             float d = 0.0f;
@@ -690,6 +680,14 @@ ssd_chunk_tc_kernel(const __grid_constant__ SsdParams p)
                 umma_bf16(t_h, umma_desc_mn_sw128(base_s + SH::B_OFF + kk * 2048, SH::CT),
                           umma_desc_mn_sw128(base_s + SH::XW_OFF + kk * 2048, 8192), id_h, true);
             umma_commit(bar_mma);
+        }
+        {   // the gate inputs of this thread's epilogue piece, fetched while the products run
+            const int t = 16 * w + (lane & 15), half = lane >> 4;
+            const int64_t ro = (b * p.L + t0 + t) * xs + static_cast<int64_t>(h) * P + 32 * half;
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                zpre[k] = (gate && t < valid) ? __ldg(reinterpret_cast<const uint4 *>(p.z + ro + 8 * k))
+                                              : make_uint4(0, 0, 0, 0);
         }
         const bool mma_ok = __syncthreads_and(mbar_wait(bar_mma, static_cast<uint32_t>(mma_phase & 1)) ? 1 : 0) != 0;
         ++mma_phase;
