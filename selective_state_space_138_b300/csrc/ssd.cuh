@@ -46,6 +46,7 @@ struct SsdParams {
     // the tensor-core chunk walk's tiles, 128-byte swizzled: x over (H*P, L, batch) with a box of
     // 64 channels x Q steps; B, C with 64 states x Q steps; C B^T with Q x Q
     CUtensorMap tm_xq, tm_Bq, tm_Cq, tm_cbq;
+    CUtensorMap tm_yq;   // y by (channel of the row, step, batch row), box 64 x 64, 128-byte swizzle (stores)
 };
 
 // ---- warp-level MMA helpers (PTX mma.sync / ldmatrix; operands in shared memory)
@@ -381,6 +382,18 @@ __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.
 // shared-memory writes of this thread become visible to the tensor cores (async proxy)
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
+// box (c0, c1, c2) of a 3-d tensor map from shared memory at src to global memory
+__device__ __forceinline__ void ssd_tma_store_3d(const void *tmap, uint32_t src, int c0, int c1, int c2)
+{
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(tmap)),
+                 "r"(src), "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+}
+__device__ __forceinline__ void ssd_bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void ssd_bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void ssd_bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // MN-major operand descriptor (128-byte swizzle): atoms of 64 MN elements x 8 K
 // rows (8 rows of 128 bytes), `lbo` bytes between MN atoms, 1024 bytes between
 // 8-row K groups; a K step of 16 rows advances the start by 2048 bytes
@@ -533,6 +546,8 @@ ssd_chunk_tc_kernel(const __grid_constant__ SsdParams p)
         const uint32_t xs_s = base_s + SH::X_OFF;
         const unsigned char *xt = base + SH::X_OFF;
         uint4 zpre[4];
+        if (tid == 0)
+            ssd_bulk_wait_read_all();   // the previous chunk's y has left the w o X buffer
         // ---- step sizes (zero past L), a_s and the next chunk's raw steps
         if (tid < Q) {
             float d = 0.0f;
@@ -703,26 +718,24 @@ ssd_chunk_tc_kernel(const __grid_constant__ SsdParams p)
             tmem_ld16_split<32>(t_y + lane_base + 16, yv + 16);
             tmem_ld_wait();
             const int t = 16 * w + (lane & 15), half = lane >> 4;
-            if (t < valid && mma_ok) {
-                const int64_t ro = (b * p.L + t0 + t) * xs + static_cast<int64_t>(h) * P + 32 * half;
-                __nv_bfloat16 *yr = p.y + ro;
+            unsigned char *yt = base + SH::XW_OFF;   // y of the chunk, [t][p] 128-byte swizzled, for one tensor store
 #pragma unroll
-                for (int k4 = 0; k4 < 4; ++k4) {
-                    const uint32_t zw4[4] = {zpre[k4].x, zpre[k4].y, zpre[k4].z, zpre[k4].w};
-                    uint32_t ow[4];
+            for (int k4 = 0; k4 < 4; ++k4) {
+                const uint32_t zw4[4] = {zpre[k4].x, zpre[k4].y, zpre[k4].z, zpre[k4].w};
+                uint32_t ow[4];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int pp = 8 * k4 + 2 * e;
-                        float o0 = __uint_as_float(yv[pp]), o1 = __uint_as_float(yv[pp + 1]);
-                        if (gate) {
-                            o0 *= silu_f(bf16lo(zw4[e]));
-                            o1 *= silu_f(bf16hi(zw4[e]));
-                        }
-                        ow[e] = pack_bf16x2(o0, o1);
+                for (int e = 0; e < 4; ++e) {
+                    const int pp = 8 * k4 + 2 * e;
+                    float o0 = __uint_as_float(yv[pp]), o1 = __uint_as_float(yv[pp + 1]);
+                    if (gate) {
+                        o0 *= silu_f(bf16lo(zw4[e]));
+                        o1 *= silu_f(bf16hi(zw4[e]));
                     }
-                    *reinterpret_cast<uint4 *>(yr + 8 * k4) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+                    ow[e] = pack_bf16x2(o0, o1);
                 }
+                *reinterpret_cast<uint4 *>(yt + sw128_off(t, 32 * half + 8 * k4)) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
             }
+            fence_proxy_async();
         }
         if (!mma_ok) {
             aborted = true;
@@ -731,7 +744,13 @@ ssd_chunk_tc_kernel(const __grid_constant__ SsdParams p)
         tc_fence_before();
         __syncthreads();   // every thread is done with this chunk's S', w o X, bf16 H and Y
         tc_fence_after();
+        if (tid == 0) {   // y of the chunk (steps past L are dropped by the map)
+            ssd_tma_store_3d(&p.tm_yq, base_s + SH::XW_OFF, h * P, static_cast<int>(t0), static_cast<int>(b));
+            ssd_bulk_commit();
+        }
     }
+    if (tid == 0)
+        ssd_bulk_wait_all();
 
     // the final state: final_state[p][n] = H^T[n][p]
     if (p.final_state && !aborted) {
@@ -1172,7 +1191,8 @@ bool ssd_encode_maps(SsdParams &p, int64_t N)
            ssd_encode_3d(&p.tm_Bq, p.B, GN, L, bt, GN * 2, GN * L * 2, 64, Q, CU_TENSOR_MAP_SWIZZLE_128B) &&
            ssd_encode_3d(&p.tm_Cq, p.C, GN, L, bt, GN * 2, GN * L * 2, 64, Q, CU_TENSOR_MAP_SWIZZLE_128B) &&
            ssd_encode_3d(&p.tm_cbq, p.cb, Q, Q, bt * static_cast<uint64_t>(p.nchunks) * static_cast<uint64_t>(p.G),
-                         Q * 2, Q * Q * 2, 64, Q, CU_TENSOR_MAP_SWIZZLE_128B);
+                         Q * 2, Q * Q * 2, 64, Q, CU_TENSOR_MAP_SWIZZLE_128B) &&
+           ssd_encode_3d(&p.tm_yq, p.y, HP, L, bt, HP * 2, HP * L * 2, 64, Q, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 template <int N>
