@@ -413,19 +413,22 @@ ss_status ss_ssd_fwd_bf16(const ss_bf16 *x, const ss_bf16 *dt, const float *A, c
                           cudaStream_t stream);
 
 /* Device-side faults recorded by the kernels since the last clear, as a bit
- * set: SS_FAULT_WAIT_TIMEOUT = a wait for a tensor copy into shared memory
- * (the forward scan's tiles, "Why the scan must be fused": inputs are staged
- * once on chip) ran out of its one-second limit; the kernel then stops
- * waiting, its outputs are not valid, and it lets the copies it issued land
- * before it exits. Synchronises the device (reads a device word).
+ * set: SS_FAULT_WAIT_TIMEOUT = a bounded wait in a kernel (for a tensor copy
+ * into shared memory -- the tiles of "Why the scan must be fused": inputs are
+ * staged once on chip -- or for the hand-over of a buffer between the warps
+ * of a CTA) ran out of its one-second limit; the thread then stops waiting,
+ * the call's outputs are not valid, and the copies already issued are let
+ * land before the kernel exits. Synchronises the device (reads a device word).
  *   flags  host pointer, receives the bit set
  *   clear  non-zero: reset the recorded faults to none
  * Errors: SS_ERR_NULL (flags NULL), SS_ERR_INTERNAL (the read failed). */
 #define SS_FAULT_WAIT_TIMEOUT 1u
-/* SS_FAULT_SMEM_ALIGN: a kernel that stages its tiles by tensor copies (the
- * forward scan of rows that are 16-byte aligned, the SSD chunk kernel) found
- * its shared memory off the 128-byte boundary the copies need and returned
- * without writing its outputs. */
+/* SS_FAULT_SMEM_ALIGN: a kernel that stages its tiles by tensor copies into
+ * dynamic shared memory without aligning the base itself (the forward scan,
+ * the backward pass, the decode update and the SSD chunk kernel that runs
+ * without the tensor cores' operand layouts) found that
+ * memory off the boundary the copies need and returned without writing its
+ * outputs. */
 #define SS_FAULT_SMEM_ALIGN 2u
 ss_status ss_device_faults(unsigned int *flags, int clear);
 
