@@ -432,6 +432,15 @@ ss_status ss_ssd_fwd_bf16(const ss_bf16 *x, const ss_bf16 *dt, const float *A, c
 #define SS_FAULT_SMEM_ALIGN 2u
 ss_status ss_device_faults(unsigned int *flags, int clear);
 
+/* Exercises the fault word: one GPU thread waits on a barrier that nothing
+ * completes, with the same one-second bound every kernel's waits have; the
+ * wait gives up, records SS_FAULT_WAIT_TIMEOUT and the kernel returns, so the
+ * context stays usable. No counterpart in the pages: a check of the bounded
+ * waits themselves, for tests. Asynchronous on `stream` (about one second of
+ * GPU time); read the result with ss_device_faults after synchronising.
+ * Errors: SS_ERR_LAUNCH. */
+ss_status ss_fault_probe(cudaStream_t stream);
+
 /* The architecture the library's kernels were compiled for, as the CUDA
  * runtime reports it for the loaded module on the current device
  * (cudaFuncGetAttributes(...).binaryVersion of the forward scan kernel:

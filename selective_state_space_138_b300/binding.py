@@ -22,7 +22,7 @@ EXPORTS = ("ss_scan_fwd_bf16", "ss_scan_fwd_f32", "ss_scan_fwd_ex_bf16", "ss_sca
            "ss_conv_state_update_f32", "ss_scan_bwd_bf16", "ss_scan_bwd_f32", "ss_scan_bwd_workspace_bytes",
            "ss_scan_bwd_noalloc_bf16", "ss_scan_bwd_noalloc_f32", "ss_ssd_fwd_bf16", "ss_ssd_workspace_bytes",
            "ss_scan_fwd_train_bf16", "ss_scan_fwd_train_f32", "ss_scan_bwd_ex_bf16", "ss_scan_bwd_ex_f32",
-           "ss_device_faults", "ss_kernel_binary_version", "ss_last_error", "ss_abi_version")
+           "ss_device_faults", "ss_fault_probe", "ss_kernel_binary_version", "ss_last_error", "ss_abi_version")
 
 STATUS = {0: "SS_OK", -1: "SS_ERR_NULL", -2: "SS_ERR_DIM", -3: "SS_ERR_N", -4: "SS_ERR_DEVICE_PTR",
           -5: "SS_ERR_LAUNCH", -6: "SS_ERR_INTERNAL"}
@@ -86,6 +86,8 @@ def lib() -> ctypes.CDLL:
     L.ss_scan_bwd_workspace_bytes.restype = ctypes.c_size_t
     L.ss_device_faults.argtypes = [ctypes.POINTER(ctypes.c_uint), ci]
     L.ss_device_faults.restype = ci
+    L.ss_fault_probe.argtypes = [vp]
+    L.ss_fault_probe.restype = ci
     L.ss_kernel_binary_version.argtypes = [ctypes.POINTER(ctypes.c_int)]
     L.ss_kernel_binary_version.restype = ci
     L.ss_last_error.argtypes = []
@@ -109,6 +111,13 @@ def device_faults(clear: bool = True) -> int:
     v = ctypes.c_uint(0)
     _check(lib().ss_device_faults(ctypes.byref(v), 1 if clear else 0))
     return v.value
+
+
+def fault_probe(stream=None) -> None:
+    """Launch the probe whose one GPU thread waits on a barrier nothing
+    completes: its bounded wait gives up after about a second and records
+    FAULT_WAIT_TIMEOUT (read it with ``device_faults``); see ``ss_fault_probe``."""
+    _check(lib().ss_fault_probe(_stream(stream)))
 
 
 def abi_version() -> int:

@@ -194,6 +194,16 @@ ss_status ss_kernel_binary_version(int *binary_version)
     return SS_OK;
 }
 
+ss_status ss_fault_probe(cudaStream_t stream)
+{
+    g_err[0] = '\0';
+    fault_probe_kernel<<<1, 32, 0, stream>>>();
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return fail(SS_ERR_LAUNCH, "fault probe launch failed: %s", cudaGetErrorString(e));
+    return SS_OK;
+}
+
 #endif
 
 // ---- backward pass
