@@ -398,8 +398,10 @@ ss_status ss_scan_bwd_noalloc_f32(const float *x, const float *delta, const floa
  *   final_state : (batch, nheads, headdim, N) fp32 output, or NULL.
  *   workspace   : >= ss_ssd_workspace_bytes(batch, L, ngroups) bytes of device
  *                 scratch (holds C_c B_c^T of every chunk), caller-owned.
- *   headdim = 64, N = 64 or 128, nheads a multiple of ngroups; x, B, C, y, z
- *   and the workspace 16-byte aligned.
+ *   headdim = 64, N = 64, 128 or 256, nheads a multiple of ngroups; x, B, C,
+ *   y, z and the workspace 16-byte aligned. N = 256 runs as two passes over the
+ *   128-state halves (the first stores its partial y, rounded to bf16, in y;
+ *   the second adds it and applies the gate), on the tensor-core kernels only.
  * Errors: SS_ERR_NULL, SS_ERR_DIM (sizes, alignment, workspace), SS_ERR_N,
  * SS_ERR_DEVICE_PTR, SS_ERR_LAUNCH, SS_ERR_INTERNAL.
  */

@@ -37,6 +37,13 @@ struct SsdParams {
     int64_t batch, L, H, G, nchunks;
     int softplus;
     int tma;   // the chunk kernel's X, B, C and C B^T tiles come in through the tensor maps below
+    // the state dimension as stored (the B, C row length per group, the h0 and final-state
+    // stride) and the first state this call handles: N = 256 runs as two passes over the
+    // 128-state halves (n_off 0 and 128) of the tensor-core kernels
+    int Nt, n_off;
+    // 0: the whole state (D skip, gate, y stored); 1: first half (D skip, no gate, the partial y
+    // stored in y); 2: second half (no D, the stored partial added, gate, y stored)
+    int mode;
     // 3-d maps: x over (H*P channels, L, batch) with a box of one head's P + 8 channels x Q steps;
     // B, C over (G*N, L, batch) with a box of N + 8 x Q; C B^T over (Q, Q, batch*nchunks*G) with
     // a box of Q + 8 x Q. The 8 extra columns fill each shared-memory row's pad (never read).
@@ -301,9 +308,9 @@ ssd_cb_tc_kernel(const __grid_constant__ SsdParams p)
         const int t0 = static_cast<int>(c0 * Q);
 #pragma unroll
         for (int a = 0; a < SH::ATOMS; ++a) {
-            tma_load_3d(base_s + SH::A_OFF + a * SH::TILE, &p.tm_Csw, bar_tile, g * N + 64 * a, t0,
+            tma_load_3d(base_s + SH::A_OFF + a * SH::TILE, &p.tm_Csw, bar_tile, g * p.Nt + p.n_off + 64 * a, t0,
                         static_cast<int>(b));
-            tma_load_3d(base_s + SH::B_OFF + a * SH::TILE, &p.tm_Bsw, bar_tile, g * N + 64 * a, t0,
+            tma_load_3d(base_s + SH::B_OFF + a * SH::TILE, &p.tm_Bsw, bar_tile, g * p.Nt + p.n_off + 64 * a, t0,
                         static_cast<int>(b));
         }
         ok = mbar_wait(bar_tile, 0);
@@ -474,9 +481,11 @@ ssd_chunk_tc_kernel(const __grid_constant__ SsdParams p)
     const int h = blockIdx.x;
     const int g = static_cast<int>(h / (p.H / p.G));
     const float Ah = __ldg(p.A + h);
-    const float Dh = p.D ? __ldg(p.D + h) : 0.0f;
+    const float Dh = (p.D && p.mode != 2) ? __ldg(p.D + h) : 0.0f;   // D x once, in the first half's pass
     const float bias = p.dt_bias ? __ldg(p.dt_bias + h) : 0.0f;
-    const bool gate = p.z != nullptr;
+    const bool gate = p.z != nullptr && p.mode != 1;   // the gate once, on the whole state's y
+    const bool add_partial = p.mode == 2;
+    const int Nt = p.Nt, n_off = p.n_off;
     const int64_t xs = p.H * P;   // x, z, y row stride (one time step)
 
     if (w == 0)
@@ -501,7 +510,7 @@ ssd_chunk_tc_kernel(const __grid_constant__ SsdParams p)
         uint32_t v[64];
 #pragma unroll
         for (int pp = 0; pp < 64; ++pp)
-            v[pp] = __float_as_uint((p.h0 && hrow >= 0) ? p.h0[((b * p.H + h) * P + pp) * N + hrow] : 0.0f);
+            v[pp] = __float_as_uint((p.h0 && hrow >= 0) ? p.h0[((b * p.H + h) * P + pp) * Nt + n_off + hrow] : 0.0f);
 #pragma unroll
         for (int j = 0; j < 4; ++j)
             tmem_st16(t_h + lane_base + 16 * j, v + 16 * j);
@@ -519,9 +528,9 @@ ssd_chunk_tc_kernel(const __grid_constant__ SsdParams p)
             tma_load_3d(base_s + SH::X_OFF, &p.tm_xq, bar_cb, h * P, static_cast<int>(c * Q), static_cast<int>(b));
 #pragma unroll
             for (int j = 0; j < SH::NS; ++j) {
-                tma_load_3d(base_s + SH::C_OFF + j * SH::CT, &p.tm_Cq, bar_cb, g * N + 64 * j, static_cast<int>(c * Q),
+                tma_load_3d(base_s + SH::C_OFF + j * SH::CT, &p.tm_Cq, bar_cb, g * Nt + n_off + 64 * j, static_cast<int>(c * Q),
                             static_cast<int>(b));
-                tma_load_3d(base_s + SH::B_OFF + j * SH::CT, &p.tm_Bq, bar_cb, g * N + 64 * j, static_cast<int>(c * Q),
+                tma_load_3d(base_s + SH::B_OFF + j * SH::CT, &p.tm_Bq, bar_cb, g * Nt + n_off + 64 * j, static_cast<int>(c * Q),
                             static_cast<int>(b));
             }
             tma_load_3d(base_s + SH::S_OFF, &p.tm_cbq, bar_cb, 0, 0, static_cast<int>((b * p.nchunks + c) * p.G + g));
@@ -545,7 +554,7 @@ ssd_chunk_tc_kernel(const __grid_constant__ SsdParams p)
         const int valid = static_cast<int>(p.L - t0 < Q ? p.L - t0 : Q);
         const uint32_t xs_s = base_s + SH::X_OFF;
         const unsigned char *xt = base + SH::X_OFF;
-        uint4 zpre[4];
+        uint4 zpre[4], ypre[4];
         if (tid == 0)
             ssd_bulk_wait_read_all();   // the previous chunk's y has left the w o X buffer
         // ---- step sizes (zero past L), a_s and the next chunk's raw steps
@@ -703,6 +712,10 @@ ssd_chunk_tc_kernel(const __grid_constant__ SsdParams p)
             for (int k = 0; k < 4; ++k)
                 zpre[k] = (gate && t < valid) ? __ldg(reinterpret_cast<const uint4 *>(p.z + ro + 8 * k))
                                               : make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)   // the first half's partial y (second-half pass)
+                ypre[k] = (add_partial && t < valid) ? *reinterpret_cast<const uint4 *>(p.y + ro + 8 * k)
+                                                     : make_uint4(0, 0, 0, 0);
         }
         const bool mma_ok = __syncthreads_and(mbar_wait(bar_mma, static_cast<uint32_t>(mma_phase & 1)) ? 1 : 0) != 0;
         ++mma_phase;
@@ -722,11 +735,16 @@ ssd_chunk_tc_kernel(const __grid_constant__ SsdParams p)
 #pragma unroll
             for (int k4 = 0; k4 < 4; ++k4) {
                 const uint32_t zw4[4] = {zpre[k4].x, zpre[k4].y, zpre[k4].z, zpre[k4].w};
+                const uint32_t yw4[4] = {ypre[k4].x, ypre[k4].y, ypre[k4].z, ypre[k4].w};
                 uint32_t ow[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int pp = 8 * k4 + 2 * e;
                     float o0 = __uint_as_float(yv[pp]), o1 = __uint_as_float(yv[pp + 1]);
+                    if (add_partial) {
+                        o0 += bf16lo(yw4[e]);
+                        o1 += bf16hi(yw4[e]);
+                    }
                     if (gate) {
                         o0 *= silu_f(bf16lo(zw4[e]));
                         o1 *= silu_f(bf16hi(zw4[e]));
@@ -760,10 +778,10 @@ ssd_chunk_tc_kernel(const __grid_constant__ SsdParams p)
             tmem_ld16(t_h + lane_base + 16 * j, hv + 16 * j);
         tmem_ld_wait();
         if (hrow >= 0) {
-            float *fs = p.final_state + ((b * p.H + h) * P) * N + hrow;
+            float *fs = p.final_state + ((b * p.H + h) * P) * Nt + n_off + hrow;
 #pragma unroll
             for (int pp = 0; pp < 64; ++pp)
-                fs[static_cast<int64_t>(pp) * N] = __uint_as_float(hv[pp]);
+                fs[static_cast<int64_t>(pp) * Nt] = __uint_as_float(hv[pp]);
         }
     }
     if (tid == 0)   // copies issued and not yet waited for (after an abort) land before the CTA leaves
@@ -1171,7 +1189,28 @@ bool ssd_encode_3d(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, u
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// The chunk kernel's tile maps (SS_SCAN_TMA=0 keeps the cp.async pieces).
+// The tensor-core kernels' tile maps (128-byte swizzled boxes of 64 states or
+// channels): B, C over (G*N, L, batch) with 64 states x 128 steps (C B^T) and
+// 64 states x Q steps (the chunk walk); x and y over (H*P, L, batch) with 64
+// channels x Q steps; C B^T over (Q, Q, batch*nchunks*G).
+bool ssd_encode_tc_maps(SsdParams &p, int64_t N)
+{
+    constexpr int Q = kSsdQ, P = kSsdP;
+    const uint64_t HP = static_cast<uint64_t>(p.H) * P, GN = static_cast<uint64_t>(p.G) * N;
+    const uint64_t L = static_cast<uint64_t>(p.L), bt = static_cast<uint64_t>(p.batch);
+    return ssd_encode_3d(&p.tm_Bsw, p.B, GN, L, bt, GN * 2, GN * L * 2, 64, 2 * Q, CU_TENSOR_MAP_SWIZZLE_128B) &&
+           ssd_encode_3d(&p.tm_Csw, p.C, GN, L, bt, GN * 2, GN * L * 2, 64, 2 * Q, CU_TENSOR_MAP_SWIZZLE_128B) &&
+           ssd_encode_3d(&p.tm_xq, p.x, HP, L, bt, HP * 2, HP * L * 2, 64, Q, CU_TENSOR_MAP_SWIZZLE_128B) &&
+           ssd_encode_3d(&p.tm_Bq, p.B, GN, L, bt, GN * 2, GN * L * 2, 64, Q, CU_TENSOR_MAP_SWIZZLE_128B) &&
+           ssd_encode_3d(&p.tm_Cq, p.C, GN, L, bt, GN * 2, GN * L * 2, 64, Q, CU_TENSOR_MAP_SWIZZLE_128B) &&
+           ssd_encode_3d(&p.tm_cbq, p.cb, Q, Q, bt * static_cast<uint64_t>(p.nchunks) * static_cast<uint64_t>(p.G),
+                         Q * 2, Q * Q * 2, 64, Q, CU_TENSOR_MAP_SWIZZLE_128B) &&
+           ssd_encode_3d(&p.tm_yq, p.y, HP, L, bt, HP * 2, HP * L * 2, 64, Q, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// All the chunk kernels' tile maps (SS_SCAN_TMA=0 keeps the cp.async pieces):
+// the mma.sync kernels' padded boxes (a whole state row + 8) and the
+// tensor-core kernels' swizzled ones.
 bool ssd_encode_maps(SsdParams &p, int64_t N)
 {
     const char *env = getenv("SS_SCAN_TMA");
@@ -1185,14 +1224,41 @@ bool ssd_encode_maps(SsdParams &p, int64_t N)
            ssd_encode_3d(&p.tm_C, p.C, GN, L, bt, GN * 2, GN * L * 2, static_cast<uint32_t>(N + 8), Q) &&
            ssd_encode_3d(&p.tm_cb, p.cb, Q, Q, bt * static_cast<uint64_t>(p.nchunks) * static_cast<uint64_t>(p.G),
                          Q * 2, Q * Q * 2, Q + 8, Q) &&
-           ssd_encode_3d(&p.tm_Bsw, p.B, GN, L, bt, GN * 2, GN * L * 2, 64, 2 * Q, CU_TENSOR_MAP_SWIZZLE_128B) &&
-           ssd_encode_3d(&p.tm_Csw, p.C, GN, L, bt, GN * 2, GN * L * 2, 64, 2 * Q, CU_TENSOR_MAP_SWIZZLE_128B) &&
-           ssd_encode_3d(&p.tm_xq, p.x, HP, L, bt, HP * 2, HP * L * 2, 64, Q, CU_TENSOR_MAP_SWIZZLE_128B) &&
-           ssd_encode_3d(&p.tm_Bq, p.B, GN, L, bt, GN * 2, GN * L * 2, 64, Q, CU_TENSOR_MAP_SWIZZLE_128B) &&
-           ssd_encode_3d(&p.tm_Cq, p.C, GN, L, bt, GN * 2, GN * L * 2, 64, Q, CU_TENSOR_MAP_SWIZZLE_128B) &&
-           ssd_encode_3d(&p.tm_cbq, p.cb, Q, Q, bt * static_cast<uint64_t>(p.nchunks) * static_cast<uint64_t>(p.G),
-                         Q * 2, Q * Q * 2, 64, Q, CU_TENSOR_MAP_SWIZZLE_128B) &&
-           ssd_encode_3d(&p.tm_yq, p.y, HP, L, bt, HP * 2, HP * L * 2, 64, Q, CU_TENSOR_MAP_SWIZZLE_128B);
+           ssd_encode_tc_maps(p, N);
+}
+
+// N = 256 on the tensor-core kernels: two passes over the 128-state halves.
+// The output is linear in the state (y = C h + D x, before the gate), so the
+// first pass stores its partial y without the gate (rounded to bf16 once) and
+// the second adds it, then gates; B, C, h0 and the final state are addressed
+// with their full 256-state stride and the half's offset.
+ss_status launch_ssd_halves(SsdParams p, cudaStream_t stream)
+{
+    using CS = SsdCbShape<128>;
+    using TS = SsdTcShape<128>;
+    if (p.nchunks > 0x7fffffff || p.batch > 65535 || p.G > 65535 || p.H > 0x7fffffff)
+        return fail(SS_ERR_DIM, "grid too large");
+    cudaError_t e = cudaFuncSetAttribute(ssd_cb_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(CS::BYTES));
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(ssd_chunk_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(TS::BYTES));
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(SS_ERR_LAUNCH, "cudaFuncSetAttribute failed: %s", cudaGetErrorString(e));
+    }
+    for (int half = 0; half < 2; ++half) {
+        p.n_off = 128 * half;
+        p.mode = 1 + half;
+        ssd_cb_tc_kernel<128><<<dim3(static_cast<unsigned>((p.nchunks + 1) / 2), static_cast<unsigned>(p.batch),
+                                     static_cast<unsigned>(p.G)), 128, CS::BYTES, stream>>>(p);
+        ssd_chunk_tc_kernel<128><<<dim3(static_cast<unsigned>(p.H), static_cast<unsigned>(p.batch)), 128, TS::BYTES,
+                                   stream>>>(p);
+        e = cudaGetLastError();
+        if (e != cudaSuccess)
+            return fail(SS_ERR_LAUNCH, "SSD kernel launch failed: %s", cudaGetErrorString(e));
+    }
+    return SS_OK;
 }
 
 template <int N>
@@ -1259,8 +1325,8 @@ ss_status ssd_fwd(const void *x, const void *dt, const float *A, const void *B, 
                     (long long)ngroups);
     if (headdim != kSsdP)
         return fail(SS_ERR_DIM, "headdim=%lld: this kernel takes headdim %d", (long long)headdim, kSsdP);
-    if (N != 64 && N != 128)
-        return fail(SS_ERR_N, "N=%lld: this kernel takes N = 64 or 128", (long long)N);
+    if (N != 64 && N != 128 && N != 256)
+        return fail(SS_ERR_N, "N=%lld: this kernel takes N = 64, 128 or 256", (long long)N);
     if (batch > (int64_t(1) << 40) / L || batch * L > (int64_t(1) << 50) / (nheads * headdim))
         return fail(SS_ERR_DIM, "element count overflows");
     const PtrCheck list[] = {{x, "x", true},       {dt, "dt", true},         {A, "A", true},
@@ -1297,6 +1363,16 @@ ss_status ssd_fwd(const void *x, const void *dt, const float *A, const void *B, 
     p.batch = batch; p.L = L; p.H = nheads; p.G = ngroups;
     p.nchunks = (L + kSsdQ - 1) / kSsdQ;
     p.softplus = softplus ? 1 : 0;
+    p.Nt = static_cast<int>(N);
+    p.n_off = 0;
+    p.mode = 0;
+    if (N == 256) {   // the tensor-core kernels only, in two passes over the state halves
+        const char *env = getenv("SS_SCAN_TMA");
+        if ((env && strcmp(env, "0") == 0) || !ssd_encode_tc_maps(p, N))
+            return fail(SS_ERR_N, "N=256 runs on the tensor-core kernels only, whose tensor maps could not be made");
+        p.tma = 1;
+        return launch_ssd_halves(p, stream);
+    }
     p.tma = ssd_encode_maps(p, N) ? 1 : 0;
     return N == 64 ? launch_ssd<64>(p, stream) : launch_ssd<128>(p, stream);
 }

@@ -66,7 +66,9 @@ def run(spec, use_z=True, use_D=True, use_bias=True, softplus=True, use_h0=False
 
 
 SHAPES = [(1, 1, 1, 1, 64), (1, 64, 2, 1, 64), (2, 100, 4, 2, 128), (1, 257, 3, 1, 128), (2, 130, 8, 4, 64),
-          (1, 1000, 2, 1, 128)]
+          (1, 1000, 2, 1, 128),
+          # N = 256: two passes over the state halves
+          (1, 1, 1, 1, 256), (2, 130, 4, 2, 256), (1, 700, 3, 1, 256)]
 
 
 @pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "b%d_l%d_h%d_g%d_n%d" % s)
@@ -75,13 +77,14 @@ def test_ssd_matches_oracle(shape):
     run(I.SsdSpec(b, L, H, 64, G, N, seed=L + H))
 
 
+@pytest.mark.parametrize("N", [128, 256])
 @pytest.mark.parametrize("opts", [dict(use_z=False, use_D=False, use_bias=False), dict(use_h0=True),
                                   dict(softplus=False), dict(use_h0=True, use_z=False)],
                          ids=["bare", "h0", "no_softplus", "h0_no_gate"])
-def test_ssd_options(opts):
-    spec = I.SsdSpec(2, 200, 4, 64, 2, 128, seed=3)
+def test_ssd_options(opts, N):
+    spec = I.SsdSpec(2, 200, 4, 64, 2, N, seed=3)
     if not opts.get("softplus", True):
-        spec = I.SsdSpec(2, 200, 4, 64, 2, 128, seed=4)
+        spec = I.SsdSpec(2, 200, 4, 64, 2, N, seed=4)
     run(spec, **opts)
 
 
