@@ -863,7 +863,7 @@ def main(argv=None):
         extras["bwd_" + HEADLINE.name] = {
             "elem_steps_per_s": HEADLINE.elem_steps / (bms * 1e-3), "kernel_ms_median": bms,
             "roofline": bro, "note": "backward pass (all gradients, states recomputed), L2 flushed before each"}
-        lbms = time_bwd(I.LONGSEQ, 3, 1)
+        lbms = time_bwd(I.LONGSEQ, 3, 3)
         extras["bwd_" + I.LONGSEQ.name] = {
             "elem_steps_per_s": I.LONGSEQ.elem_steps / (lbms * 1e-3), "kernel_ms_median": lbms,
             "roofline": roofline_obj(bwd_alg_bytes(I.LONGSEQ), lbms, peaks, None),
