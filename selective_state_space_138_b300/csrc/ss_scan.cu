@@ -63,6 +63,7 @@ namespace {
 #include "host_common.cuh"
 #if SS_PART_IS(1)
 #include "scan_fwd.cuh"
+#include "fault_probe.cuh"
 #endif
 #if SS_PART_IS(2)
 #include "scan_bwd.cuh"
