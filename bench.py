@@ -544,7 +544,7 @@ def time_ssd(spec: I.SsdSpec, steps: int, warmup: int):
     g = {k: v.cuda() for k, v in inp.items()}
     y = torch.empty_like(g["x"])
     fs = torch.empty(spec.batch, spec.nheads, spec.headdim, spec.N, device="cuda")
-    ws = torch.empty(binding.ssd_workspace_bytes(spec.batch, spec.L, spec.ngroups), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(binding.ssd_workspace_bytes(spec.batch, spec.L, spec.nheads, spec.ngroups, spec.N), dtype=torch.uint8, device="cuda")
     scratch = L2Flush()
 
     def run():
@@ -721,7 +721,7 @@ def ncu_case(args):
         spec = I.MAMBA2_LAYER
         inp = I.make_ssd_inputs(spec)
         g = {k: v.cuda() for k, v in inp.items()}
-        ws = torch.empty(binding.ssd_workspace_bytes(spec.batch, spec.L, spec.ngroups), dtype=torch.uint8,
+        ws = torch.empty(binding.ssd_workspace_bytes(spec.batch, spec.L, spec.nheads, spec.ngroups, spec.N), dtype=torch.uint8,
                          device="cuda")
         for _ in range(args.warmup + args.steps):
             binding.ssd_fwd(g["x"], g["dt"], g["A"], g["B"], g["C"], D=g["D"], z=g["z"], dt_bias=g["dt_bias"],

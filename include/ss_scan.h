@@ -59,7 +59,7 @@ typedef enum ss_status {
 } ss_status;
 
 #define SS_MAX_N 64
-#define SS_ABI_VERSION 1
+#define SS_ABI_VERSION 2
 
 /*
  * ss_scan_fwd_bf16 / ss_scan_fwd_f32 -- selective scan over a whole sequence.
@@ -396,8 +396,13 @@ ss_status ss_scan_bwd_noalloc_f32(const float *x, const float *delta, const floa
  *   B, C        : (batch, L, ngroups, N) bf16.
  *   h0          : (batch, nheads, headdim, N) fp32 initial state, or NULL.
  *   final_state : (batch, nheads, headdim, N) fp32 output, or NULL.
- *   workspace   : >= ss_ssd_workspace_bytes(batch, L, ngroups) bytes of device
- *                 scratch (holds C_c B_c^T of every chunk), caller-owned.
+ *   workspace   : >= ss_ssd_workspace_bytes(batch, L, nheads, ngroups, N) bytes
+ *                 of device scratch, caller-owned: C_c B_c^T of every chunk, the
+ *                 counters of the chunk walk's work items, and the states handed
+ *                 from one chunk segment of a (batch, head) row to the next (the
+ *                 walk may cut each row into 2 or 4 segments, run in order, so that
+ *                 rows x segments spread evenly over the resident CTAs). Calls that
+ *                 share a workspace must not overlap on the GPU.
  *   headdim = 64, N = 64, 128 or 256, nheads a multiple of ngroups; x, B, C,
  *   y, z and the workspace 16-byte aligned. N = 256 runs as two passes over the
  *   128-state halves (the first stores its partial y, rounded to bf16, in y;
@@ -405,7 +410,7 @@ ss_status ss_scan_bwd_noalloc_f32(const float *x, const float *delta, const floa
  * Errors: SS_ERR_NULL, SS_ERR_DIM (sizes, alignment, workspace), SS_ERR_N,
  * SS_ERR_DEVICE_PTR, SS_ERR_LAUNCH, SS_ERR_INTERNAL.
  */
-size_t ss_ssd_workspace_bytes(int64_t batch, int64_t L, int64_t ngroups);
+size_t ss_ssd_workspace_bytes(int64_t batch, int64_t L, int64_t nheads, int64_t ngroups, int64_t N);
 
 ss_status ss_ssd_fwd_bf16(const ss_bf16 *x, const ss_bf16 *dt, const float *A, const ss_bf16 *B,
                           const ss_bf16 *C, const float *D, const ss_bf16 *z, const float *dt_bias,

@@ -80,7 +80,7 @@ def lib() -> ctypes.CDLL:
         getattr(L, name).restype = ci
     L.ss_ssd_fwd_bf16.argtypes = [vp] * 8 + [ci, vp, vp, vp, vp, ctypes.c_size_t] + [i64] * 6 + [vp]
     L.ss_ssd_fwd_bf16.restype = ci
-    L.ss_ssd_workspace_bytes.argtypes = [i64] * 3
+    L.ss_ssd_workspace_bytes.argtypes = [i64] * 5
     L.ss_ssd_workspace_bytes.restype = ctypes.c_size_t
     L.ss_scan_bwd_workspace_bytes.argtypes = [i64] * 4
     L.ss_scan_bwd_workspace_bytes.restype = ctypes.c_size_t
@@ -420,8 +420,8 @@ def scan_bwd(x, delta, A, B, C, dout, D=None, z=None, dt_bias=None, delta_softpl
     return {k: g.get(k) for k in ("dx", "ddelta", "dz", "dA", "dB", "dC", "dD", "ddt_bias", "dh0")}
 
 
-def ssd_workspace_bytes(batch, L, ngroups) -> int:
-    return int(lib().ss_ssd_workspace_bytes(batch, L, ngroups))
+def ssd_workspace_bytes(batch, L, nheads, ngroups, N) -> int:
+    return int(lib().ss_ssd_workspace_bytes(batch, L, nheads, ngroups, N))
 
 
 def ssd_fwd(x, dt, A, B, C, D=None, z=None, dt_bias=None, delta_softplus=True, h0=None, y=None, final_state=None,
@@ -445,7 +445,7 @@ def ssd_fwd(x, dt, A, B, C, D=None, z=None, dt_bias=None, delta_softplus=True, h
     if final_state is None and return_final_state:
         final_state = torch.empty((batch, H, P, N), dtype=torch.float32, device=x.device)
     _need(final_state, "final_state", torch.float32, (batch, H, P, N))
-    need = ssd_workspace_bytes(batch, L, G)
+    need = ssd_workspace_bytes(batch, L, H, G, N)
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=x.device)
     _check(lib().ss_ssd_fwd_bf16(_ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(dt_bias),

@@ -341,9 +341,9 @@ ss_status ss_conv_state_update_f32(float *conv_state, const float *x, const floa
 // ---- SSD
 #if SS_PART_IS(4)
 
-size_t ss_ssd_workspace_bytes(int64_t batch, int64_t L, int64_t ngroups)
+size_t ss_ssd_workspace_bytes(int64_t batch, int64_t L, int64_t nheads, int64_t ngroups, int64_t N)
 {
-    return ssd_workspace_bytes(batch, L, ngroups);
+    return ssd_workspace_bytes(batch, L, nheads, ngroups, N);
 }
 
 ss_status ss_ssd_fwd_bf16(const ss_bf16 *x, const ss_bf16 *dt, const float *A, const ss_bf16 *B, const ss_bf16 *C,

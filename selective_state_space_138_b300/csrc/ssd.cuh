@@ -34,6 +34,12 @@ struct SsdParams {
     __nv_bfloat16 *y;
     float *final_state;
     __nv_bfloat16 *cb;   // workspace: [batch][nchunks][G][Q][Q] bf16
+    // workspace of the tensor-core chunk walk: work[0] counts the work items claimed,
+    // work[1 + row] the chunk segments of row (b, h) done; hbuf holds the state one
+    // segment hands to the next, laid out as final_state
+    unsigned int *work;
+    float *hbuf;
+    int nseg, cps;   // chunk segments per row and chunks per segment
     int64_t batch, L, H, G, nchunks;
     int softplus;
     int tma;   // the chunk kernel's X, B, C and C B^T tiles come in through the tensor maps below
@@ -55,6 +61,29 @@ struct SsdParams {
     CUtensorMap tm_xq, tm_Bq, tm_Cq, tm_cbq;
     CUtensorMap tm_yq;   // y by (channel of the row, step, batch row), box 64 x 64, 128-byte swizzle (stores)
 };
+
+// the segment count of a row as published by the CTA that walked the segment before:
+// waits (bounded, thread 0) until it reaches v; false (and the fault flag set) if not
+__device__ __forceinline__ bool ssd_flag_wait(const unsigned int *f, unsigned int v)
+{
+    const uint64_t t0 = global_ns();
+    for (;;) {
+        unsigned int x;
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(x) : "l"(f) : "memory");
+        if (x >= v)
+            return true;
+        if (global_ns() - t0 > kWaitLimitNs) {
+            atomicOr(&g_fault_flags, kFaultWaitTimeout);
+            return false;
+        }
+        __nanosleep(256);
+    }
+}
+
+__device__ __forceinline__ void ssd_flag_release(unsigned int *f, unsigned int v)
+{
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(f), "r"(v) : "memory");
+}
 
 // ---- warp-level MMA helpers (PTX mma.sync / ldmatrix; operands in shared memory)
 
@@ -290,6 +319,9 @@ ssd_cb_tc_kernel(const __grid_constant__ SsdParams p)
     const int64_t b = blockIdx.y;
     const int g = blockIdx.z;
     const int64_t c0 = 2 * static_cast<int64_t>(blockIdx.x);   // first chunk of the pair
+    if (p.work && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0)   // the chunk walk's counters, fresh
+        for (int64_t i = tid; i <= p.batch * p.H; i += 128)
+            p.work[i] = 0u;
     if (w == 0)
         tmem_alloc(base_s + SH::TMEM_OFF, 128);
     if (tid == 0) {
@@ -421,9 +453,12 @@ __host__ __device__ constexpr uint32_t umma_idesc_bf16_mj(int M, int N, int a_mn
 // the 128-byte swizzle (16-byte piece c/8 of row r sits at piece (c/8) ^ (r % 8))
 __device__ __forceinline__ int sw128_off(int r, int c) { return r * 128 + (((c >> 3) ^ (r & 7)) << 4) + (c & 7) * 2; }
 
-// ---- the chunk walk on the tcgen05 tensor cores: one CTA (4 warps) per
-// (batch, head), the chunks of Q = 64 steps in order. Per chunk, with T the
-// tensor memory of the CTA:
+// ---- the chunk walk on the tcgen05 tensor cores: CTAs of 8 warps, at most as
+// many as fit on the GPU at once, each claiming work items in order: a (batch,
+// head) row's chunks of Q = 64 steps, or one of the 2 or 4 segments of them
+// (walked one after another: a segment starts from the state the segment before
+// hands over), so that rows x segments spread evenly over the CTAs. Per chunk,
+// with T the tensor memory of the CTA:
 //   Y[t][p]   = sum_n (e^{cum[t]} C[t][n]) H[p][n] + sum_s (S' + D I)[t][s] X[s][p]   (T cols 64..127;
 //               M = 64 rows t; the decay of the carried state is folded into the C rows, the skip
 //               term D x into the diagonal of S', so both products accumulate in one place)
@@ -436,6 +471,10 @@ __device__ __forceinline__ int sw128_off(int r, int c) { return r * 128 + (((c >
 // product) in the same swizzled layout. Every operand of a product is rounded
 // once to bf16. With N = 128 the state product has M = 128 (row n in lane n);
 // with N = 64, M = 64 (row n in lane 32 (n / 16) + n % 16), as for Y.
+// Warp 0 forms the next chunk's step sizes while the products run, and the
+// state copy for the next chunk follows the epilogue.
+constexpr int kSsdTcThreads = 256;   // 8 warps: two per lane quarter of tensor memory
+
 template <int N>
 struct SsdTcShape {
     static constexpr int Q = kSsdQ, P = kSsdP;
@@ -459,7 +498,7 @@ struct SsdTcShape {
 };
 
 template <int N>
-__global__ void __launch_bounds__(128, 3)
+__global__ void __launch_bounds__(kSsdTcThreads, 3)
 ssd_chunk_tc_kernel(const __grid_constant__ SsdParams p)
 {
     using SH = SsdTcShape<N>;
@@ -476,13 +515,12 @@ ssd_chunk_tc_kernel(const __grid_constant__ SsdParams p)
     const uint32_t bar_mma = bar_cb + 8;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(base + SH::TMEM_OFF);
 
-    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-    const int64_t b = blockIdx.y;
-    const int h = blockIdx.x;
-    const int g = static_cast<int>(h / (p.H / p.G));
-    const float Ah = __ldg(p.A + h);
-    const float Dh = (p.D && p.mode != 2) ? __ldg(p.D + h) : 0.0f;   // D x once, in the first half's pass
-    const float bias = p.dt_bias ? __ldg(p.dt_bias + h) : 0.0f;
+    // warp w reads and writes lane quarter q = w % 4 of tensor memory; warps w and w + 4
+    // share a quarter and split its columns (hf = w / 4)
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5, q = w & 3, hf = w >> 2;
+    int64_t b = 0;   // the work item's row (b, h), group g and per-head values
+    int h = 0, g = 0;
+    float Ah = 0.0f, Dh = 0.0f, bias = 0.0f;
     const bool gate = p.z != nullptr && p.mode != 1;   // the gate once, on the whole state's y
     const bool add_partial = p.mode == 2;
     const int Nt = p.Nt, n_off = p.n_off;
@@ -500,22 +538,10 @@ ssd_chunk_tc_kernel(const __grid_constant__ SsdParams p)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const uint32_t t_h = tmem, t_y = tmem + 64;   // column bases
-    const uint32_t lane_base = static_cast<uint32_t>(32 * w) << 16;
+    const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
 
     // the state row this thread holds in tensor memory (H^T[n][.]), or -1
-    const int hrow = (N == 128) ? tid : ((lane < 16) ? 16 * w + lane : -1);
-
-    // initial state: H^T[n][p] = h0[p][n] (zero without h0)
-    {
-        uint32_t v[64];
-#pragma unroll
-        for (int pp = 0; pp < 64; ++pp)
-            v[pp] = __float_as_uint((p.h0 && hrow >= 0) ? p.h0[((b * p.H + h) * P + pp) * Nt + n_off + hrow] : 0.0f);
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            tmem_st16(t_h + lane_base + 16 * j, v + 16 * j);
-        tmem_st_wait();
-    }
+    const int hrow = (N == 128) ? 32 * q + lane : ((lane < 16) ? 16 * q + lane : -1);
 
     // tensor copies of a chunk's tiles (X, C, B, C B^T) on one barrier; every wait is
     // bounded, and after one gives up the CTA issues no more and leaves after the
@@ -545,245 +571,312 @@ ssd_chunk_tc_kernel(const __grid_constant__ SsdParams p)
         }
     };
 
-    issue_cb(0);
-    float dt_next = (tid < Q && tid < p.L) ? __bfloat162float(p.dt[(b * p.L + tid) * p.H + h]) : 0.0f;
-    int mma_phase = 0;
-
-    for (int64_t c = 0; c < p.nchunks; ++c) {
-        const int64_t t0 = c * Q;
-        const int valid = static_cast<int>(p.L - t0 < Q ? p.L - t0 : Q);
-        const uint32_t xs_s = base_s + SH::X_OFF;
-        const unsigned char *xt = base + SH::X_OFF;
-        uint4 zpre[4], ypre[4];
-        if (tid == 0)
-            ssd_bulk_wait_read_all();   // the previous chunk's y has left the w o X buffer
-        // ---- step sizes (zero past L), a_s and the next chunk's raw steps
-        if (tid < Q) {
-            float d = 0.0f;
-            if (tid < valid) {
-                const float v = dt_next + bias;
-                d = p.softplus ? softplus_f(v) : v;
-            }
-            dl[tid] = d;
-        }
-        if (c + 1 < p.nchunks) {
-            const int64_t tn = (c + 1) * Q + tid;
-            dt_next = (tid < Q && tn < p.L) ? __bfloat162float(p.dt[(b * p.L + tn) * p.H + h]) : 0.0f;
-        }
-        __syncthreads();
-        // ---- cum[t] = A delta_0 + .. + A delta_t (log2 e units), e^cum, w (one warp)
-        if (w == 0) {
-            const float a0 = Ah * kLog2e * dl[2 * lane], a1 = Ah * kLog2e * dl[2 * lane + 1];
-            float sum = a0 + a1;
+    // the raw step sizes of steps 2 lane and 2 lane + 1 of chunk c (warp 0; zero past L)
+    float dta = 0.0f, dtb = 0.0f;
+    auto load_dt = [&](int64_t c) {
+        const int64_t ta = c * Q + 2 * lane;
+        dta = (c < p.nchunks && ta < p.L) ? __bfloat162float(p.dt[(b * p.L + ta) * p.H + h]) : 0.0f;
+        dtb = (c < p.nchunks && ta + 1 < p.L) ? __bfloat162float(p.dt[(b * p.L + ta + 1) * p.H + h]) : 0.0f;
+    };
+    // warp 0: the step sizes of chunk c from (dta, dtb) and, in shared memory, delta, cum[t] =
+    // A delta_0 + .. + A delta_t (log2 e units), e^cum and w_s = e^{cum[Q-1] - cum[s]} delta_s
+    auto step_sizes = [&](int64_t c) {
+        const int64_t ta = c * Q + 2 * lane;
+        float d0 = 0.0f, d1 = 0.0f;
+        if (ta < p.L)
+            d0 = p.softplus ? softplus_f(dta + bias) : dta + bias;
+        if (ta + 1 < p.L)
+            d1 = p.softplus ? softplus_f(dtb + bias) : dtb + bias;
+        const float a0 = Ah * kLog2e * d0, a1 = Ah * kLog2e * d1;
+        float sum = a0 + a1;
 #pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const float u = __shfl_up_sync(0xffffffffu, sum, o);
-                if (lane >= o)
-                    sum += u;
-            }
-            const float c0v = sum - a1, c1v = sum;
-            cum[2 * lane] = c0v;
-            cum[2 * lane + 1] = c1v;
-            ecum[2 * lane] = ex2_approx(c0v);
-            ecum[2 * lane + 1] = ex2_approx(c1v);
-            const float cq = __shfl_sync(0xffffffffu, c1v, 31);
-            wsx[2 * lane] = ex2_approx(cq - c0v) * dl[2 * lane];
-            wsx[2 * lane + 1] = ex2_approx(cq - c1v) * dl[2 * lane + 1];
+        for (int o = 1; o < 32; o <<= 1) {
+            const float u = __shfl_up_sync(0xffffffffu, sum, o);
+            if (lane >= o)
+                sum += u;
         }
-        // ---- H: the bf16 copy (B operand of D1) and e^{cum[Q-1]} H back into tensor memory
-        //      (cum is read after the barrier below; the copy does not need it)
-        uint32_t hv[64];
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            tmem_ld16(t_h + lane_base + 16 * j, hv + 16 * j);
-        tmem_ld_wait();
+        const float c0v = sum - a1, c1v = sum;
+        const float cq = __shfl_sync(0xffffffffu, c1v, 31);
+        *reinterpret_cast<float2 *>(dl + 2 * lane) = make_float2(d0, d1);
+        *reinterpret_cast<float2 *>(cum + 2 * lane) = make_float2(c0v, c1v);
+        *reinterpret_cast<float2 *>(ecum + 2 * lane) = make_float2(ex2_approx(c0v), ex2_approx(c1v));
+        *reinterpret_cast<float2 *>(wsx + 2 * lane) =
+            make_float2(ex2_approx(cq - c0v) * d0, ex2_approx(cq - c1v) * d1);
+    };
+    // the state entering a chunk (this thread's half row of H^T, columns 32 hf .., in hv):
+    // its bf16 copy, the B operand of Y = (e^cum C) H^T, and e^{cum[Q-1]} H back into
+    // tensor memory
+    auto put_h = [&](uint32_t (&hv)[32], float ec) {
         if (hrow >= 0) {
             unsigned char *hr = base + SH::H_OFF;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
+            for (int j = 0; j < 4; ++j) {
                 uint4 o;
                 o.x = pack_bf16x2(__uint_as_float(hv[8 * j]), __uint_as_float(hv[8 * j + 1]));
                 o.y = pack_bf16x2(__uint_as_float(hv[8 * j + 2]), __uint_as_float(hv[8 * j + 3]));
                 o.z = pack_bf16x2(__uint_as_float(hv[8 * j + 4]), __uint_as_float(hv[8 * j + 5]));
                 o.w = pack_bf16x2(__uint_as_float(hv[8 * j + 6]), __uint_as_float(hv[8 * j + 7]));
-                *reinterpret_cast<uint4 *>(hr + sw128_off(hrow, 8 * j)) = o;
+                *reinterpret_cast<uint4 *>(hr + sw128_off(hrow, 32 * hf + 8 * j)) = o;
             }
         }
-        __syncthreads();   // cum, e^cum, w, a, delta are in shared memory
-        {
-            const float ec = ex2_approx(cum[Q - 1]);
 #pragma unroll
-            for (int j = 0; j < 64; ++j)
-                hv[j] = __float_as_uint(__uint_as_float(hv[j]) * ec);
+        for (int j = 0; j < 32; ++j)
+            hv[j] = __float_as_uint(__uint_as_float(hv[j]) * ec);
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-                tmem_st16(t_h + lane_base + 16 * j, hv + 16 * j);
-        }
-        wait_cb();
-        // ---- S' = C B^T o M o delta in place and w o X; thread (row r, half j) does 32
-        //      elements of row r: M[t][s] delta_s = e^{cum[t] - cum[s]} delta_s (<= 1) for s <= t
-        {
-            const int r = tid & (Q - 1), j = tid >> 6;
-            unsigned char *srow = base + SH::S_OFF;
-            const float ct = cum[r];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int s0 = 32 * j + 8 * k;
-                const uint4 cbw = *reinterpret_cast<const uint4 *>(srow + sw128_off(r, s0));
-                const uint32_t wv[4] = {cbw.x, cbw.y, cbw.z, cbw.w};
-                const float4 cu0 = *reinterpret_cast<const float4 *>(cum + s0);
-                const float4 cu1 = *reinterpret_cast<const float4 *>(cum + s0 + 4);
-                const float4 dd0 = *reinterpret_cast<const float4 *>(dl + s0);
-                const float4 dd1 = *reinterpret_cast<const float4 *>(dl + s0 + 4);
-                const float cu[8] = {cu0.x, cu0.y, cu0.z, cu0.w, cu1.x, cu1.y, cu1.z, cu1.w};
-                const float dd[8] = {dd0.x, dd0.y, dd0.z, dd0.w, dd1.x, dd1.y, dd1.z, dd1.w};
-                uint32_t ow[4];
-#pragma unroll
-                for (int e = 0; e < 8; e += 2) {
-                    float v0 = (s0 + e <= r) ? bf16lo(wv[e >> 1]) * ex2_approx(ct - cu[e]) * dd[e] : 0.0f;
-                    float v1 = (s0 + e + 1 <= r) ? bf16hi(wv[e >> 1]) * ex2_approx(ct - cu[e + 1]) * dd[e + 1] : 0.0f;
-                    v0 += (s0 + e == r) ? Dh : 0.0f;   // the skip term D x through the diagonal
-                    v1 += (s0 + e + 1 == r) ? Dh : 0.0f;
-                    ow[e >> 1] = pack_bf16x2(v0, v1);
-                }
-                *reinterpret_cast<uint4 *>(srow + sw128_off(r, s0)) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
-            }
-            // the C rows scaled by e^{cum[t]} (the decay of the carried state to step t)
-            const float er = ecum[r];
-            unsigned char *crow = base + SH::C_OFF;
-#pragma unroll
-            for (int k2 = 0; k2 < 4 * SH::NS; ++k2) {
-                const int n0 = 32 * j + 8 * (k2 % 4) + 64 * (k2 / 4);   // this thread's half of each slice
-                unsigned char *cp = crow + (n0 / 64) * SH::CT + sw128_off(r, n0 % 64);
-                const uint4 cv = *reinterpret_cast<const uint4 *>(cp);
-                uint4 o;
-                o.x = pack_bf16x2(bf16lo(cv.x) * er, bf16hi(cv.x) * er);
-                o.y = pack_bf16x2(bf16lo(cv.y) * er, bf16hi(cv.y) * er);
-                o.z = pack_bf16x2(bf16lo(cv.z) * er, bf16hi(cv.z) * er);
-                o.w = pack_bf16x2(bf16lo(cv.w) * er, bf16hi(cv.w) * er);
-                *reinterpret_cast<uint4 *>(cp) = o;
-            }
-            const float ws = wsx[r];
-            unsigned char *xw = base + SH::XW_OFF;
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int p0 = 32 * j + 8 * k;
-                const uint4 xv = *reinterpret_cast<const uint4 *>(xt + sw128_off(r, p0));
-                uint4 o;
-                o.x = pack_bf16x2(bf16lo(xv.x) * ws, bf16hi(xv.x) * ws);
-                o.y = pack_bf16x2(bf16lo(xv.y) * ws, bf16hi(xv.y) * ws);
-                o.z = pack_bf16x2(bf16lo(xv.z) * ws, bf16hi(xv.z) * ws);
-                o.w = pack_bf16x2(bf16lo(xv.w) * ws, bf16hi(xv.w) * ws);
-                *reinterpret_cast<uint4 *>(xw + sw128_off(r, p0)) = o;
-            }
-        }
-        tmem_st_wait();
-        fence_proxy_async();
-        tc_fence_before();
-        const int go = __syncthreads_and(aborted ? 0 : 1);
-        tc_fence_after();
-        if (!go)
+        for (int j = 0; j < 2; ++j)
+            tmem_st16(t_h + lane_base + 32 * hf + 16 * j, hv + 16 * j);
+    };
+
+    // Work items: row (b, h) = item % rows, chunk segment item / rows (cps chunks). Items
+    // are claimed in order from a counter, so a row's segment is claimed only after the
+    // one before it, by a CTA that is already running: it starts from the state that
+    // segment hands over (the row's flag counts the segments done) and never waits on a
+    // CTA that has not started.
+    const int64_t rows = p.batch * p.H;
+    const int64_t total = rows * p.nseg;
+    int64_t *item_slot = reinterpret_cast<int64_t *>(base + SH::TMEM_OFF + 8);
+    int mma_phase = 0;
+    for (;;) {
+        if (tid == 0)
+            *item_slot = static_cast<int64_t>(atomicAdd(p.work, 1u));
+        __syncthreads();
+        const int64_t item = *item_slot;
+        if (item >= total)
             break;
-        if (tid == 0) {
-            constexpr uint32_t id_y = umma_idesc_bf16_mj(64, 64, 0, 1);
-            constexpr uint32_t id_h = umma_idesc_bf16_mj(N, 64, 1, 1);
-            // Y = (e^cum C) H^T: A = scaled C (K-major, 64-state slices), B = H stored [n][p] (MN-major)
-#pragma unroll
-            for (int kk = 0; kk < N / 16; ++kk)
-                umma_bf16(t_y, umma_desc_sw128(base_s + SH::C_OFF + (kk / 4) * SH::CT + (kk % 4) * 32),
-                          umma_desc_mn_sw128(base_s + SH::H_OFF + kk * 2048, 8192), id_y, kk > 0);
-            // Y += (S' + D I) X: A = S' (K-major), B = X stored [s][p] (MN-major)
-#pragma unroll
-            for (int kk = 0; kk < Q / 16; ++kk)
-                umma_bf16(t_y, umma_desc_sw128(base_s + SH::S_OFF + kk * 32),
-                          umma_desc_mn_sw128(xs_s + kk * 2048, 8192), id_y, true);
-            // H^T += B^T (w o X): A = B stored [s][n] (MN-major, 64-state atoms CT bytes apart),
-            // B = w o X stored [s][p] (MN-major)
-#pragma unroll
-            for (int kk = 0; kk < Q / 16; ++kk)
-                umma_bf16(t_h, umma_desc_mn_sw128(base_s + SH::B_OFF + kk * 2048, SH::CT),
-                          umma_desc_mn_sw128(base_s + SH::XW_OFF + kk * 2048, 8192), id_h, true);
-            umma_commit(bar_mma);
+        const int seg = static_cast<int>(item / rows);
+        const int64_t row = item % rows;
+        b = row / p.H;
+        h = static_cast<int>(row % p.H);
+        g = static_cast<int>(h / (p.H / p.G));
+        Ah = __ldg(p.A + h);
+        Dh = (p.D && p.mode != 2) ? __ldg(p.D + h) : 0.0f;   // D x once, in the first half's pass
+        bias = p.dt_bias ? __ldg(p.dt_bias + h) : 0.0f;
+        const int64_t c_begin = static_cast<int64_t>(seg) * p.cps;
+        const int64_t c_end = c_begin + p.cps < p.nchunks ? c_begin + p.cps : p.nchunks;
+        const bool last = c_end >= p.nchunks;
+        float *hand = p.hbuf + row * P * Nt + n_off;   // the state handed between the row's segments, [p][n]
+        if (seg > 0 && tid == 0)
+            aborted = !ssd_flag_wait(p.work + 1 + row, static_cast<unsigned int>(seg));
+        aborted = __syncthreads_or(aborted ? 1 : 0) != 0;
+        if (aborted)
+            break;
+        issue_cb(c_begin);
+        if (w == 0) {
+            load_dt(c_begin);
+            step_sizes(c_begin);
+            load_dt(c_begin + 1);
         }
-        {   // the gate inputs of this thread's epilogue piece, fetched while the products run
-            const int t = 16 * w + (lane & 15), half = lane >> 4;
-            const int64_t ro = (b * p.L + t0 + t) * xs + static_cast<int64_t>(h) * P + 32 * half;
+        __syncthreads();   // the segment's first step sizes
+        {   // the state entering the segment: h0 (zero without it) or the one handed over
+            uint32_t hv[32];
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-                zpre[k] = (gate && t < valid) ? __ldg(reinterpret_cast<const uint4 *>(p.z + ro + 8 * k))
-                                              : make_uint4(0, 0, 0, 0);
-#pragma unroll
-            for (int k = 0; k < 4; ++k)   // the first half's partial y (second-half pass)
-                ypre[k] = (add_partial && t < valid) ? *reinterpret_cast<const uint4 *>(p.y + ro + 8 * k)
-                                                     : make_uint4(0, 0, 0, 0);
-        }
-        const bool mma_ok = __syncthreads_and(mbar_wait(bar_mma, static_cast<uint32_t>(mma_phase & 1)) ? 1 : 0) != 0;
-        ++mma_phase;
-        tc_fence_after();
-        // X, C, B and C B^T are free: the next chunk's land while this one finishes
-        if (c + 1 < p.nchunks && mma_ok)
-            issue_cb(c + 1);
-        // ---- epilogue: y[t][p] = Y[t][p] silu(z); warp w holds rows t = 16w .. 16w+15,
-        //      lane l row 16w + (l % 16), columns 32 (l / 16) ..
-        {
-            uint32_t yv[32];
-            tmem_ld16_split<32>(t_y + lane_base, yv);
-            tmem_ld16_split<32>(t_y + lane_base + 16, yv + 16);
-            tmem_ld_wait();
-            const int t = 16 * w + (lane & 15), half = lane >> 4;
-            unsigned char *yt = base + SH::XW_OFF;   // y of the chunk, [t][p] 128-byte swizzled, for one tensor store
-#pragma unroll
-            for (int k4 = 0; k4 < 4; ++k4) {
-                const uint32_t zw4[4] = {zpre[k4].x, zpre[k4].y, zpre[k4].z, zpre[k4].w};
-                const uint32_t yw4[4] = {ypre[k4].x, ypre[k4].y, ypre[k4].z, ypre[k4].w};
-                uint32_t ow[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int pp = 8 * k4 + 2 * e;
-                    float o0 = __uint_as_float(yv[pp]), o1 = __uint_as_float(yv[pp + 1]);
-                    if (add_partial) {
-                        o0 += bf16lo(yw4[e]);
-                        o1 += bf16hi(yw4[e]);
-                    }
-                    if (gate) {
-                        o0 *= silu_f(bf16lo(zw4[e]));
-                        o1 *= silu_f(bf16hi(zw4[e]));
-                    }
-                    ow[e] = pack_bf16x2(o0, o1);
-                }
-                *reinterpret_cast<uint4 *>(yt + sw128_off(t, 32 * half + 8 * k4)) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+            for (int pp = 0; pp < 32; ++pp) {
+                const int64_t o = static_cast<int64_t>(32 * hf + pp) * Nt + hrow;
+                float v = 0.0f;
+                if (hrow >= 0)
+                    v = seg > 0 ? __ldcg(hand + o) : (p.h0 ? p.h0[row * P * Nt + n_off + o] : 0.0f);
+                hv[pp] = __float_as_uint(v);
             }
+            put_h(hv, ex2_approx(cum[Q - 1]));
+        }
+
+        for (int64_t c = c_begin; c < c_end; ++c) {
+            const int64_t t0 = c * Q;
+            const int valid = static_cast<int>(p.L - t0 < Q ? p.L - t0 : Q);
+            const uint32_t xs_s = base_s + SH::X_OFF;
+            const unsigned char *xt = base + SH::X_OFF;
+            uint4 zpre[2], ypre[2];
+            wait_cb();
+            // ---- S' = C B^T o M o delta in place and w o X; thread (row r, quarter j) does 16
+            //      elements of row r: M[t][s] delta_s = e^{cum[t] - cum[s]} delta_s (<= 1) for s <= t
+            {
+                const int r = tid & (Q - 1), j = tid >> 6;
+                unsigned char *srow = base + SH::S_OFF;
+                const float ct = cum[r];
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    const int s0 = 16 * j + 8 * k;
+                    const uint4 cbw = *reinterpret_cast<const uint4 *>(srow + sw128_off(r, s0));
+                    const uint32_t wv[4] = {cbw.x, cbw.y, cbw.z, cbw.w};
+                    const float4 cu0 = *reinterpret_cast<const float4 *>(cum + s0);
+                    const float4 cu1 = *reinterpret_cast<const float4 *>(cum + s0 + 4);
+                    const float4 dd0 = *reinterpret_cast<const float4 *>(dl + s0);
+                    const float4 dd1 = *reinterpret_cast<const float4 *>(dl + s0 + 4);
+                    const float cu[8] = {cu0.x, cu0.y, cu0.z, cu0.w, cu1.x, cu1.y, cu1.z, cu1.w};
+                    const float dd[8] = {dd0.x, dd0.y, dd0.z, dd0.w, dd1.x, dd1.y, dd1.z, dd1.w};
+                    uint32_t ow[4];
+#pragma unroll
+                    for (int e = 0; e < 8; e += 2) {
+                        float v0 = (s0 + e <= r) ? bf16lo(wv[e >> 1]) * ex2_approx(ct - cu[e]) * dd[e] : 0.0f;
+                        float v1 = (s0 + e + 1 <= r) ? bf16hi(wv[e >> 1]) * ex2_approx(ct - cu[e + 1]) * dd[e + 1] : 0.0f;
+                        v0 += (s0 + e == r) ? Dh : 0.0f;   // the skip term D x through the diagonal
+                        v1 += (s0 + e + 1 == r) ? Dh : 0.0f;
+                        ow[e >> 1] = pack_bf16x2(v0, v1);
+                    }
+                    *reinterpret_cast<uint4 *>(srow + sw128_off(r, s0)) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+                }
+                // the C rows scaled by e^{cum[t]} (the decay of the carried state to step t)
+                const float er = ecum[r];
+                unsigned char *crow = base + SH::C_OFF;
+#pragma unroll
+                for (int k2 = 0; k2 < N / 32; ++k2) {
+                    const int n0 = 8 * j + 32 * k2;   // pieces j, j + 4, .. of the row
+                    unsigned char *cp = crow + (n0 / 64) * SH::CT + sw128_off(r, n0 % 64);
+                    const uint4 cv = *reinterpret_cast<const uint4 *>(cp);
+                    uint4 o;
+                    o.x = pack_bf16x2(bf16lo(cv.x) * er, bf16hi(cv.x) * er);
+                    o.y = pack_bf16x2(bf16lo(cv.y) * er, bf16hi(cv.y) * er);
+                    o.z = pack_bf16x2(bf16lo(cv.z) * er, bf16hi(cv.z) * er);
+                    o.w = pack_bf16x2(bf16lo(cv.w) * er, bf16hi(cv.w) * er);
+                    *reinterpret_cast<uint4 *>(cp) = o;
+                }
+                const float ws = wsx[r];
+                unsigned char *xw = base + SH::XW_OFF;
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    const int p0 = 8 * j + 32 * k;
+                    const uint4 xv = *reinterpret_cast<const uint4 *>(xt + sw128_off(r, p0));
+                    uint4 o;
+                    o.x = pack_bf16x2(bf16lo(xv.x) * ws, bf16hi(xv.x) * ws);
+                    o.y = pack_bf16x2(bf16lo(xv.y) * ws, bf16hi(xv.y) * ws);
+                    o.z = pack_bf16x2(bf16lo(xv.z) * ws, bf16hi(xv.z) * ws);
+                    o.w = pack_bf16x2(bf16lo(xv.w) * ws, bf16hi(xv.w) * ws);
+                    *reinterpret_cast<uint4 *>(xw + sw128_off(r, p0)) = o;
+                }
+            }
+            tmem_st_wait();
             fence_proxy_async();
+            tc_fence_before();
+            const int go = __syncthreads_and(aborted ? 0 : 1);
+            tc_fence_after();
+            if (!go) {
+                aborted = true;
+                break;
+            }
+            if (tid == 0) {
+                constexpr uint32_t id_y = umma_idesc_bf16_mj(64, 64, 0, 1);
+                constexpr uint32_t id_h = umma_idesc_bf16_mj(N, 64, 1, 1);
+                // Y = (e^cum C) H^T: A = scaled C (K-major, 64-state slices), B = H stored [n][p] (MN-major)
+#pragma unroll
+                for (int kk = 0; kk < N / 16; ++kk)
+                    umma_bf16(t_y, umma_desc_sw128(base_s + SH::C_OFF + (kk / 4) * SH::CT + (kk % 4) * 32),
+                              umma_desc_mn_sw128(base_s + SH::H_OFF + kk * 2048, 8192), id_y, kk > 0);
+                // Y += (S' + D I) X: A = S' (K-major), B = X stored [s][p] (MN-major)
+#pragma unroll
+                for (int kk = 0; kk < Q / 16; ++kk)
+                    umma_bf16(t_y, umma_desc_sw128(base_s + SH::S_OFF + kk * 32),
+                              umma_desc_mn_sw128(xs_s + kk * 2048, 8192), id_y, true);
+                // H^T += B^T (w o X): A = B stored [s][n] (MN-major, 64-state atoms CT bytes apart),
+                // B = w o X stored [s][p] (MN-major)
+#pragma unroll
+                for (int kk = 0; kk < Q / 16; ++kk)
+                    umma_bf16(t_h, umma_desc_mn_sw128(base_s + SH::B_OFF + kk * 2048, SH::CT),
+                              umma_desc_mn_sw128(base_s + SH::XW_OFF + kk * 2048, 8192), id_h, true);
+                umma_commit(bar_mma);
+            }
+            {   // the gate inputs of this thread's epilogue piece, fetched while the products run
+                const int t = 16 * q + (lane & 15), half = lane >> 4;
+                const int64_t ro = (b * p.L + t0 + t) * xs + static_cast<int64_t>(h) * P + 32 * half + 16 * hf;
+#pragma unroll
+                for (int k = 0; k < 2; ++k)
+                    zpre[k] = (gate && t < valid) ? __ldg(reinterpret_cast<const uint4 *>(p.z + ro + 8 * k))
+                                                  : make_uint4(0, 0, 0, 0);
+#pragma unroll
+                for (int k = 0; k < 2; ++k)   // the first half's partial y (second-half pass)
+                    ypre[k] = (add_partial && t < valid) ? *reinterpret_cast<const uint4 *>(p.y + ro + 8 * k)
+                                                         : make_uint4(0, 0, 0, 0);
+            }
+            if (w == 0 && c + 1 < c_end) {   // the next chunk's step sizes, also while the products run
+                step_sizes(c + 1);
+                load_dt(c + 2);
+            }
+            const bool mma_ok = __syncthreads_and(mbar_wait(bar_mma, static_cast<uint32_t>(mma_phase & 1)) ? 1 : 0) != 0;
+            ++mma_phase;
+            tc_fence_after();
+            // X, C, B and C B^T are free: the next chunk's land while this one finishes
+            if (c + 1 < c_end && mma_ok)
+                issue_cb(c + 1);
+            // ---- epilogue: y[t][p] = Y[t][p] silu(z); warp w holds rows t = 16q .. 16q+15,
+            //      lane l row 16q + (l % 16), columns 32 (l / 16) + 16 hf .. (16 of them)
+            {
+                uint32_t yv[16];
+                tmem_ld16_split<32>(t_y + lane_base + 16 * hf, yv);
+                tmem_ld_wait();
+                const int t = 16 * q + (lane & 15), half = lane >> 4;
+                unsigned char *yt = base + SH::XW_OFF;   // y of the chunk, [t][p] 128-byte swizzled, for one tensor store
+#pragma unroll
+                for (int k4 = 0; k4 < 2; ++k4) {
+                    const uint32_t zw4[4] = {zpre[k4].x, zpre[k4].y, zpre[k4].z, zpre[k4].w};
+                    const uint32_t yw4[4] = {ypre[k4].x, ypre[k4].y, ypre[k4].z, ypre[k4].w};
+                    uint32_t ow[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int pp = 8 * k4 + 2 * e;
+                        float o0 = __uint_as_float(yv[pp]), o1 = __uint_as_float(yv[pp + 1]);
+                        if (add_partial) {
+                            o0 += bf16lo(yw4[e]);
+                            o1 += bf16hi(yw4[e]);
+                        }
+                        if (gate) {
+                            o0 *= silu_f(bf16lo(zw4[e]));
+                            o1 *= silu_f(bf16hi(zw4[e]));
+                        }
+                        ow[e] = pack_bf16x2(o0, o1);
+                    }
+                    *reinterpret_cast<uint4 *>(yt + sw128_off(t, 32 * half + 16 * hf + 8 * k4)) =
+                        make_uint4(ow[0], ow[1], ow[2], ow[3]);
+                }
+                fence_proxy_async();
+            }
+            if (!mma_ok) {
+                aborted = true;
+                break;
+            }
+            tc_fence_before();
+            __syncthreads();   // every thread is done with this chunk's S', w o X, bf16 H and Y
+            tc_fence_after();
+            if (tid == 0) {   // y of the chunk (steps past L are dropped by the map)
+                ssd_tma_store_3d(&p.tm_yq, base_s + SH::XW_OFF, h * P, static_cast<int>(t0), static_cast<int>(b));
+                ssd_bulk_commit();
+            }
+            if (c + 1 < c_end) {   // the state entering the next chunk, meanwhile
+                uint32_t hv[32];
+#pragma unroll
+                for (int j = 0; j < 2; ++j)
+                    tmem_ld16(t_h + lane_base + 32 * hf + 16 * j, hv + 16 * j);
+                tmem_ld_wait();
+                put_h(hv, ex2_approx(cum[Q - 1]));
+            }
+            if (tid == 0)
+                ssd_bulk_wait_read_all();
+            __syncthreads();   // y has left the w o X buffer before the next chunk writes it
         }
-        if (!mma_ok) {
-            aborted = true;
+        if (aborted)
             break;
+        // the state at the end of the segment: handed to the row's next segment, or the final state
+        if (!last || p.final_state) {
+            uint32_t hv[32];
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+                tmem_ld16(t_h + lane_base + 32 * hf + 16 * j, hv + 16 * j);
+            tmem_ld_wait();
+            if (hrow >= 0) {
+                float *dst = last ? p.final_state + row * P * Nt + n_off : hand;
+#pragma unroll
+                for (int pp = 0; pp < 32; ++pp)
+                    dst[static_cast<int64_t>(32 * hf + pp) * Nt + hrow] = __uint_as_float(hv[pp]);
+            }
+            if (!last)
+                __threadfence();
         }
         tc_fence_before();
-        __syncthreads();   // every thread is done with this chunk's S', w o X, bf16 H and Y
+        __syncthreads();   // the end state is out of tensor memory before the next item's enters
         tc_fence_after();
-        if (tid == 0) {   // y of the chunk (steps past L are dropped by the map)
-            ssd_tma_store_3d(&p.tm_yq, base_s + SH::XW_OFF, h * P, static_cast<int>(t0), static_cast<int>(b));
-            ssd_bulk_commit();
-        }
+        if (!last && tid == 0)
+            ssd_flag_release(p.work + 1 + row, static_cast<unsigned int>(seg + 1));
     }
     if (tid == 0)
         ssd_bulk_wait_all();
-
-    // the final state: final_state[p][n] = H^T[n][p]
-    if (p.final_state && !aborted) {
-        uint32_t hv[64];
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            tmem_ld16(t_h + lane_base + 16 * j, hv + 16 * j);
-        tmem_ld_wait();
-        if (hrow >= 0) {
-            float *fs = p.final_state + ((b * p.H + h) * P) * Nt + n_off + hrow;
-#pragma unroll
-            for (int pp = 0; pp < 64; ++pp)
-                fs[static_cast<int64_t>(pp) * Nt] = __uint_as_float(hv[pp]);
-        }
-    }
     if (tid == 0)   // copies issued and not yet waited for (after an abort) land before the CTA leaves
         for (int i = cb_done; i < cb_issued; ++i)
             mbar_wait(bar_cb, static_cast<uint32_t>(i & 1));
@@ -1163,12 +1256,111 @@ ssd_chunk_kernel(const __grid_constant__ SsdParams p)
 
 // ------------------------------------------------------------------ SSD host side
 
-size_t ssd_workspace_bytes(int64_t batch, int64_t L, int64_t G)
+// The workspace: C B^T of every chunk ([batch][nchunks][G][Q][Q] bf16), then the
+// chunk walk's counters (1 + batch * nheads words), then the states handed between
+// the chunk segments of a row (batch * nheads * P * N fp32); each part starts on a
+// 256-byte boundary. Sizes are checked by the caller (ssd_fwd) or give 0 here.
+struct SsdWorkspace {
+    size_t cb, work, hbuf, total;
+};
+
+SsdWorkspace ssd_workspace_layout(int64_t batch, int64_t L, int64_t H, int64_t G, int64_t N)
 {
-    if (batch <= 0 || L <= 0 || G <= 0)
-        return 0;
+    SsdWorkspace w{0, 0, 0, 0};
+    if (batch <= 0 || L <= 0 || H <= 0 || G <= 0 || N <= 0 || G > H || N > 256 || L > (int64_t(1) << 40) ||
+        batch > (int64_t(1) << 40) / L || batch > (int64_t(1) << 40) / H)
+        return w;
     const int64_t nchunks = (L + kSsdQ - 1) / kSsdQ;
-    return static_cast<size_t>(batch) * nchunks * G * kSsdQ * kSsdQ * 2;
+    if (batch * nchunks > (int64_t(1) << 40) / G)
+        return w;
+    auto up = [](size_t v) { return (v + 255) & ~static_cast<size_t>(255); };
+    w.work = up(static_cast<size_t>(batch) * nchunks * G * kSsdQ * kSsdQ * 2);
+    w.hbuf = w.work + up((1 + static_cast<size_t>(batch) * H) * 4);
+    w.total = w.hbuf + static_cast<size_t>(batch) * H * kSsdP * N * 4;
+    return w;
+}
+
+size_t ssd_workspace_bytes(int64_t batch, int64_t L, int64_t H, int64_t G, int64_t N)
+{
+    return ssd_workspace_layout(batch, L, H, G, N).total;
+}
+
+// Chunk segments per row for the tensor-core chunk walk: with rows (b, h) walked by
+// `slots` resident CTAs that claim work items in order, a CTA walks at most
+// ceil(rows * s / slots) items of nchunks / s chunks; s = 2 or 4 when that is shorter
+// than s = 1 (SS_SSD_SEGMENTS overrides). A row's segments still run one after another.
+int ssd_pick_segments(int64_t rows, int64_t nchunks, int64_t slots)
+{
+    int s_best = 1;
+    if (const char *env = getenv("SS_SSD_SEGMENTS")) {
+        const int v = atoi(env);
+        if (v >= 1 && v <= 8)
+            s_best = v;
+    } else if (slots > 0) {
+        int64_t num = (rows + slots - 1) / slots, den = 1;   // the cost ceil(rows s / slots) / s
+        for (int s = 2; s <= 4; s *= 2) {
+            const int64_t k = (rows * s + slots - 1) / slots;
+            if (nchunks >= s && (nchunks + s - 1) / s <= 4096 && k * den < num * s) {
+                num = k;
+                den = s;
+                s_best = s;
+            }
+        }
+    }
+    return static_cast<int>(std::min<int64_t>(s_best, nchunks));
+}
+
+// The grid and segments of ssd_chunk_tc_kernel<N>: one CTA per resident slot at most
+template <int N>
+ss_status ssd_tc_grid(SsdParams &p, unsigned *grid)
+{
+    using TS = SsdTcShape<N>;
+    static std::atomic<int> per_sm{0};
+    static std::atomic<int> sms{0};
+    if (per_sm.load() == 0) {
+        // CTAs per SM from the kernel's registers and shared memory, the SM's limits and
+        // the 512 tensor-memory columns (the runtime's occupancy query answers 1 for this
+        // kernel). The work items are claimed dynamically, so the result is a grid size,
+        // not a residency the kernel relies on.
+        int dev = 0, n_sm = 0, regs_sm = 0, smem_sm = 0, smem_rsv = 0, thr_sm = 0;
+        cudaFuncAttributes fa{};
+        cudaError_t e = cudaFuncSetAttribute(ssd_chunk_tc_kernel<N>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                             static_cast<int>(cudaSharedmemCarveoutMaxShared));
+        if (e == cudaSuccess)
+            e = cudaGetDevice(&dev);
+        if (e == cudaSuccess)
+            e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+        if (e == cudaSuccess)
+            e = cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev);
+        if (e == cudaSuccess)
+            e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+        if (e == cudaSuccess)
+            e = cudaDeviceGetAttribute(&smem_rsv, cudaDevAttrReservedSharedMemoryPerBlock, dev);
+        if (e == cudaSuccess)
+            e = cudaDeviceGetAttribute(&thr_sm, cudaDevAttrMaxThreadsPerMultiProcessor, dev);
+        if (e == cudaSuccess)
+            e = cudaFuncGetAttributes(&fa, ssd_chunk_tc_kernel<N>);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return fail(SS_ERR_LAUNCH, "device or kernel attribute query failed: %s", cudaGetErrorString(e));
+        }
+        const int warp_regs = (fa.numRegs * 32 + 255) / 256 * 256;   // registers go to warps 256 at a time
+        int occ = std::min(thr_sm / kSsdTcThreads, 512 / static_cast<int>(TS::TCOLS));
+        occ = std::min(occ, regs_sm / (warp_regs * (kSsdTcThreads / 32)));
+        occ = std::min(occ, smem_sm / (static_cast<int>(TS::BYTES + fa.sharedSizeBytes) + smem_rsv));
+        sms.store(n_sm > 0 ? n_sm : 1);
+        per_sm.store(occ > 0 ? occ : 1);
+    }
+    const int64_t rows = p.batch * p.H;
+    const int64_t slots = static_cast<int64_t>(per_sm.load()) * sms.load();
+    p.nseg = ssd_pick_segments(rows, p.nchunks, slots);
+    p.cps = static_cast<int>((p.nchunks + p.nseg - 1) / p.nseg);
+    p.nseg = static_cast<int>((p.nchunks + p.cps - 1) / p.cps);   // no empty segment
+    const int64_t items = rows * p.nseg;
+    if (items > 0x7fffffff)
+        return fail(SS_ERR_DIM, "too many work items for the chunk walk");
+    *grid = static_cast<unsigned>(std::min(items, slots));
+    return SS_OK;
 }
 
 // 3-d bf16 tensor map (d0 contiguous, then d1, d2; strides in bytes) with box
@@ -1247,13 +1439,16 @@ ss_status launch_ssd_halves(SsdParams p, cudaStream_t stream)
         cudaGetLastError();
         return fail(SS_ERR_LAUNCH, "cudaFuncSetAttribute failed: %s", cudaGetErrorString(e));
     }
+    unsigned grid = 0;
+    const ss_status st = ssd_tc_grid<128>(p, &grid);
+    if (st != SS_OK)
+        return st;
     for (int half = 0; half < 2; ++half) {
         p.n_off = 128 * half;
         p.mode = 1 + half;
         ssd_cb_tc_kernel<128><<<dim3(static_cast<unsigned>((p.nchunks + 1) / 2), static_cast<unsigned>(p.batch),
                                      static_cast<unsigned>(p.G)), 128, CS::BYTES, stream>>>(p);
-        ssd_chunk_tc_kernel<128><<<dim3(static_cast<unsigned>(p.H), static_cast<unsigned>(p.batch)), 128, TS::BYTES,
-                                   stream>>>(p);
+        ssd_chunk_tc_kernel<128><<<grid, kSsdTcThreads, TS::BYTES, stream>>>(p);
         e = cudaGetLastError();
         if (e != cudaSuccess)
             return fail(SS_ERR_LAUNCH, "SSD kernel launch failed: %s", cudaGetErrorString(e));
@@ -1262,7 +1457,7 @@ ss_status launch_ssd_halves(SsdParams p, cudaStream_t stream)
 }
 
 template <int N>
-ss_status launch_ssd(const SsdParams &p, cudaStream_t stream)
+ss_status launch_ssd(SsdParams p, cudaStream_t stream)
 {
     using SH = SsdShape<N>;
     if (p.nchunks > 0x7fffffff || p.batch > 65535 || p.G > 65535 || p.H > 0x7fffffff)
@@ -1294,8 +1489,11 @@ ss_status launch_ssd(const SsdParams &p, cudaStream_t stream)
             cudaGetLastError();
             return fail(SS_ERR_LAUNCH, "cudaFuncSetAttribute failed: %s", cudaGetErrorString(e));
         }
-        ssd_chunk_tc_kernel<N><<<dim3(static_cast<unsigned>(p.H), static_cast<unsigned>(p.batch)), 128, TS::BYTES,
-                                 stream>>>(p);
+        unsigned grid = 0;
+        const ss_status st = ssd_tc_grid<N>(p, &grid);
+        if (st != SS_OK)
+            return st;
+        ssd_chunk_tc_kernel<N><<<grid, kSsdTcThreads, TS::BYTES, stream>>>(p);
     } else {   // mma.sync (rows that cannot be copied by tensor maps, or SS_SSD_MMA_SYNC=1)
         auto kernel = p.tma ? ssd_chunk_kernel<N, true> : ssd_chunk_kernel<N, false>;
         e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(SH::BYTES));
@@ -1338,7 +1536,10 @@ ss_status ssd_fwd(const void *x, const void *dt, const float *A, const void *B, 
     ss_status st = check_ptrs(list, static_cast<int>(sizeof(list) / sizeof(list[0])), &dev);
     if (st != SS_OK)
         return st;
-    const size_t need = ssd_workspace_bytes(batch, L, ngroups);
+    const SsdWorkspace ws = ssd_workspace_layout(batch, L, nheads, ngroups, N);
+    const size_t need = ws.total;
+    if (need == 0)
+        return fail(SS_ERR_DIM, "sizes too large for the workspace");
     if (workspace_bytes < need)
         return fail(SS_ERR_DIM, "workspace of %zu bytes is smaller than the %zu bytes required", workspace_bytes,
                     need);
@@ -1360,6 +1561,10 @@ ss_status ssd_fwd(const void *x, const void *dt, const float *A, const void *B, 
     p.y = static_cast<__nv_bfloat16 *>(y);
     p.final_state = final_state;
     p.cb = static_cast<__nv_bfloat16 *>(workspace);
+    p.work = reinterpret_cast<unsigned int *>(static_cast<unsigned char *>(workspace) + ws.work);
+    p.hbuf = reinterpret_cast<float *>(static_cast<unsigned char *>(workspace) + ws.hbuf);
+    p.nseg = 1;
+    p.cps = 1;
     p.batch = batch; p.L = L; p.H = nheads; p.G = ngroups;
     p.nchunks = (L + kSsdQ - 1) / kSsdQ;
     p.softplus = softplus ? 1 : 0;

@@ -59,7 +59,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version_and_empty_error(lib):
-    assert binding.abi_version() == 1
+    assert binding.abi_version() == 2
     assert isinstance(binding.last_error(), str)
 
 

@@ -88,6 +88,16 @@ def test_ssd_options(opts, N):
     run(spec, **opts)
 
 
+@pytest.mark.parametrize("N", [64, 128, 256])
+@pytest.mark.parametrize("segments", [2, 3, 4, 8])
+def test_ssd_chunk_segments(segments, N, monkeypatch):
+    """Rows cut into chunk segments walked one after another, possibly by
+    different CTAs, each starting from the state the one before handed over
+    (forced through SS_SSD_SEGMENTS; 8 exceeds the 6 chunks of some rows)."""
+    monkeypatch.setenv("SS_SSD_SEGMENTS", str(segments))
+    run(I.SsdSpec(2, 1000 if N != 256 else 333, 5, 64, 1, N, seed=20 + segments), use_h0=True)
+
+
 def test_ssd_continues_from_its_final_state():
     """Two halves, the second started from the first's final state, equal
     one pass (chunked prefill)."""
