@@ -471,9 +471,10 @@ __device__ __forceinline__ int sw128_off(int r, int c) { return r * 128 + (((c >
 // product) in the same swizzled layout. Every operand of a product is rounded
 // once to bf16. With N = 128 the state product has M = 128 (row n in lane n);
 // with N = 64, M = 64 (row n in lane 32 (n / 16) + n % 16), as for Y.
-// Warp 0 forms the next chunk's step sizes while the products run, and the
+// One warp forms the next chunk's step sizes while the products run, and the
 // state copy for the next chunk follows the epilogue.
 constexpr int kSsdTcThreads = 256;   // 8 warps: two per lane quarter of tensor memory
+constexpr int kSsdStepWarp = 4;      // forms the step sizes (not warp 0, whose thread 0 issues the products)
 
 template <int N>
 struct SsdTcShape {
@@ -571,14 +572,14 @@ ssd_chunk_tc_kernel(const __grid_constant__ SsdParams p)
         }
     };
 
-    // the raw step sizes of steps 2 lane and 2 lane + 1 of chunk c (warp 0; zero past L)
+    // the raw step sizes of steps 2 lane and 2 lane + 1 of chunk c (the step warp; zero past L)
     float dta = 0.0f, dtb = 0.0f;
     auto load_dt = [&](int64_t c) {
         const int64_t ta = c * Q + 2 * lane;
         dta = (c < p.nchunks && ta < p.L) ? __bfloat162float(p.dt[(b * p.L + ta) * p.H + h]) : 0.0f;
         dtb = (c < p.nchunks && ta + 1 < p.L) ? __bfloat162float(p.dt[(b * p.L + ta + 1) * p.H + h]) : 0.0f;
     };
-    // warp 0: the step sizes of chunk c from (dta, dtb) and, in shared memory, delta, cum[t] =
+    // the step warp: the step sizes of chunk c from (dta, dtb) and, in shared memory, delta, cum[t] =
     // A delta_0 + .. + A delta_t (log2 e units), e^cum and w_s = e^{cum[Q-1] - cum[s]} delta_s
     auto step_sizes = [&](int64_t c) {
         const int64_t ta = c * Q + 2 * lane;
@@ -661,7 +662,7 @@ ssd_chunk_tc_kernel(const __grid_constant__ SsdParams p)
         if (aborted)
             break;
         issue_cb(c_begin);
-        if (w == 0) {
+        if (w == kSsdStepWarp) {
             load_dt(c_begin);
             step_sizes(c_begin);
             load_dt(c_begin + 1);
@@ -786,7 +787,7 @@ ssd_chunk_tc_kernel(const __grid_constant__ SsdParams p)
                     ypre[k] = (add_partial && t < valid) ? *reinterpret_cast<const uint4 *>(p.y + ro + 8 * k)
                                                          : make_uint4(0, 0, 0, 0);
             }
-            if (w == 0 && c + 1 < c_end) {   // the next chunk's step sizes, also while the products run
+            if (w == kSsdStepWarp && c + 1 < c_end) {   // the next chunk's step sizes, also while the products run
                 step_sizes(c + 1);
                 load_dt(c + 2);
             }
