@@ -319,9 +319,12 @@ ssd_cb_tc_kernel(const __grid_constant__ SsdParams p)
     const int64_t b = blockIdx.y;
     const int g = blockIdx.z;
     const int64_t c0 = 2 * static_cast<int64_t>(blockIdx.x);   // first chunk of the pair
-    if (p.work && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0)   // the chunk walk's counters, fresh
-        for (int64_t i = tid; i <= p.batch * p.H; i += 128)
+    if (p.work) {   // the chunk walk's counters, fresh for this call (every block a share)
+        const int64_t blk = (static_cast<int64_t>(blockIdx.z) * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
+        const int64_t nblk = static_cast<int64_t>(gridDim.x) * gridDim.y * gridDim.z;
+        for (int64_t i = blk * 128 + tid; i <= p.batch * p.H; i += nblk * 128)
             p.work[i] = 0u;
+    }
     if (w == 0)
         tmem_alloc(base_s + SH::TMEM_OFF, 128);
     if (tid == 0) {
