@@ -74,6 +74,7 @@ namespace {
 #endif
 #if SS_PART_IS(4)
 #include "ssd.cuh"
+#include "ssd_host.cuh"
 #endif
 
 // this object's device fault word, read (and cleared) from the host
