@@ -14,6 +14,7 @@ shard (independent sequences, no collective on the data path: weak scaling).
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import math
@@ -706,15 +707,27 @@ def ncu_case(args):
                                  z=tok["z"][t], y=y[t])
         torch.cuda.synchronize()
         return 0
-    if args.ncu_case == "bwd":
-        spec = HEADLINE
+    if args.ncu_case in ("bwd", "bwd_rev", "bwd_longseq_l16384"):
+        # bwd_longseq_l16384: the long-sequence rows cut to L = 16384 (an eighth), small
+        # enough for a full capture; the long sequence's traffic is 8 times its own
+        spec = {"bwd": HEADLINE, "bwd_rev": HEADLINE,
+                "bwd_longseq_l16384": dataclasses.replace(I.LONGSEQ, L=I.LONGSEQ.L // 8)}[args.ncu_case]
         inp = I.make_scan_inputs(spec)
         g = {k: v.cuda() for k, v in inp.items() if k != "reset_pos"}
         dout = I.make_bwd_inputs(spec)["dout"].cuda()
+        starts = None
+        if args.ncu_case == "bwd_rev":   # as the bench's variant line: reversed, a start every 250 steps
+            starts = torch.zeros(spec.batch, spec.L, dtype=torch.uint8)
+            starts[:, ::250] = 1
+            starts = starts.cuda()
         grads = None
         for _ in range(args.warmup + args.steps):
-            grads = binding.scan_bwd(g["x"], g["dt"], g["A"], g["B"], g["C"], dout, D=g["D"], z=g["z"],
-                                     dt_bias=g["dt_bias"], grads=grads)
+            if starts is not None:
+                grads = binding.scan_bwd(g["x"], g["dt"], g["A"], g["B"], g["C"], dout, D=g["D"], z=g["z"],
+                                         dt_bias=g["dt_bias"], grads=grads, seq_start=starts, reverse=True)
+            else:
+                grads = binding.scan_bwd(g["x"], g["dt"], g["A"], g["B"], g["C"], dout, D=g["D"], z=g["z"],
+                                         dt_bias=g["dt_bias"], grads=grads)
         torch.cuda.synchronize()
         return 0
     if args.ncu_case == "ssd":
@@ -773,7 +786,8 @@ def main(argv=None):
     ap.add_argument("--headline-only", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-soak", action="store_true", help="skip the 1 s untimed soak before timing")
-    ap.add_argument("--ncu-case", choices=["scan", "scan_1p4b", "scan_longseq", "decode", "conv", "conv_step", "bwd", "ssd"],
+    ap.add_argument("--ncu-case", choices=["scan", "scan_1p4b", "scan_longseq", "decode", "conv", "conv_step", "bwd",
+                                           "bwd_rev", "bwd_longseq_l16384", "ssd"],
                     default=None,
                     help="profiling case: warmup + steps launches of one kernel on its workload (the headline "
                          "scan, the 1.4B-layer or long-sequence scan, the decode update on the first warmup + "
@@ -866,13 +880,14 @@ def main(argv=None):
         lbms = time_bwd(I.LONGSEQ, 3, 3)
         extras["bwd_" + I.LONGSEQ.name] = {
             "elem_steps_per_s": I.LONGSEQ.elem_steps / (lbms * 1e-3), "kernel_ms_median": lbms,
-            "roofline": roofline_obj(bwd_alg_bytes(I.LONGSEQ), lbms, peaks, None),
+            "roofline": roofline_obj(bwd_alg_bytes(I.LONGSEQ), lbms, peaks, profiled_traffic("scan_bwd_" + I.LONGSEQ.name)),
             "note": "backward pass on the long sequence (batch 1, d_inner 2048, L 131072): 64 channel groups "
                     "walk the whole row each way, L2 flushed before each"}
         vbms = time_bwd(HEADLINE, 10, 3, variant=True)
         extras["bwd_reverse_starts_" + HEADLINE.name] = {
             "elem_steps_per_s": HEADLINE.elem_steps / (vbms * 1e-3), "kernel_ms_median": vbms,
-            "roofline": roofline_obj(bwd_alg_bytes(HEADLINE) + HEADLINE.batch * HEADLINE.L, vbms, peaks, None),
+            "roofline": roofline_obj(bwd_alg_bytes(HEADLINE) + HEADLINE.batch * HEADLINE.L, vbms, peaks,
+                                     profiled_traffic("scan_bwd_reverse_starts_" + HEADLINE.name)),
             "note": "backward of the reverse-direction scan with a sequence start every 250 steps "
                     "(ss_scan_bwd_ex_*), L2 flushed before each"}
         tbms, tfms = time_bwd(HEADLINE, 10, 3, from_forward=True)
