@@ -452,6 +452,14 @@ __host__ __device__ constexpr uint32_t umma_idesc_bf16_mj(int M, int N, int a_mn
     return umma_idesc_bf16(M, N) | (static_cast<uint32_t>(a_mn) << 15) | (static_cast<uint32_t>(b_mn) << 16);
 }
 
+// a bf16 pair times f (both lanes of f2), rounded back to a bf16 pair
+__device__ __forceinline__ uint32_t scale_bf16x2(uint32_t w, u64 f2)
+{
+    float a, b;
+    upk(mul2(pk(bf16lo(w), bf16hi(w)), f2), a, b);
+    return pack_bf16x2(a, b);
+}
+
 // byte offset of element (r, c), c < 64, in a tile of 128-byte rows stored with
 // the 128-byte swizzle (16-byte piece c/8 of row r sits at piece (c/8) ^ (r % 8))
 __device__ __forceinline__ int sw128_off(int r, int c) { return r * 128 + (((c >> 3) ^ (r & 7)) << 4) + (c & 7) * 2; }
@@ -700,6 +708,10 @@ ssd_chunk_tc_kernel(const __grid_constant__ SsdParams p)
 #pragma unroll
                 for (int k = 0; k < 2; ++k) {
                     const int s0 = 16 * j + 8 * k;
+                    if ((w & 1) == 0 && s0 >= 32) {   // rows 0-31 of this warp, steps past all of them
+                        *reinterpret_cast<uint4 *>(srow + sw128_off(r, s0)) = make_uint4(0, 0, 0, 0);
+                        continue;
+                    }
                     const uint4 cbw = *reinterpret_cast<const uint4 *>(srow + sw128_off(r, s0));
                     const uint32_t wv[4] = {cbw.x, cbw.y, cbw.z, cbw.w};
                     const float4 cu0 = *reinterpret_cast<const float4 *>(cum + s0);
@@ -720,32 +732,24 @@ ssd_chunk_tc_kernel(const __grid_constant__ SsdParams p)
                     *reinterpret_cast<uint4 *>(srow + sw128_off(r, s0)) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
                 }
                 // the C rows scaled by e^{cum[t]} (the decay of the carried state to step t)
-                const float er = ecum[r];
+                const u64 er = splat(ecum[r]);
                 unsigned char *crow = base + SH::C_OFF;
 #pragma unroll
                 for (int k2 = 0; k2 < N / 32; ++k2) {
                     const int n0 = 8 * j + 32 * k2;   // pieces j, j + 4, .. of the row
                     unsigned char *cp = crow + (n0 / 64) * SH::CT + sw128_off(r, n0 % 64);
                     const uint4 cv = *reinterpret_cast<const uint4 *>(cp);
-                    uint4 o;
-                    o.x = pack_bf16x2(bf16lo(cv.x) * er, bf16hi(cv.x) * er);
-                    o.y = pack_bf16x2(bf16lo(cv.y) * er, bf16hi(cv.y) * er);
-                    o.z = pack_bf16x2(bf16lo(cv.z) * er, bf16hi(cv.z) * er);
-                    o.w = pack_bf16x2(bf16lo(cv.w) * er, bf16hi(cv.w) * er);
-                    *reinterpret_cast<uint4 *>(cp) = o;
+                    *reinterpret_cast<uint4 *>(cp) = make_uint4(scale_bf16x2(cv.x, er), scale_bf16x2(cv.y, er),
+                                                                scale_bf16x2(cv.z, er), scale_bf16x2(cv.w, er));
                 }
-                const float ws = wsx[r];
+                const u64 ws = splat(wsx[r]);
                 unsigned char *xw = base + SH::XW_OFF;
 #pragma unroll
                 for (int k = 0; k < 2; ++k) {
                     const int p0 = 8 * j + 32 * k;
                     const uint4 xv = *reinterpret_cast<const uint4 *>(xt + sw128_off(r, p0));
-                    uint4 o;
-                    o.x = pack_bf16x2(bf16lo(xv.x) * ws, bf16hi(xv.x) * ws);
-                    o.y = pack_bf16x2(bf16lo(xv.y) * ws, bf16hi(xv.y) * ws);
-                    o.z = pack_bf16x2(bf16lo(xv.z) * ws, bf16hi(xv.z) * ws);
-                    o.w = pack_bf16x2(bf16lo(xv.w) * ws, bf16hi(xv.w) * ws);
-                    *reinterpret_cast<uint4 *>(xw + sw128_off(r, p0)) = o;
+                    *reinterpret_cast<uint4 *>(xw + sw128_off(r, p0)) = make_uint4(
+                        scale_bf16x2(xv.x, ws), scale_bf16x2(xv.y, ws), scale_bf16x2(xv.z, ws), scale_bf16x2(xv.w, ws));
                 }
             }
             tmem_st_wait();
