@@ -191,6 +191,24 @@ def test_bwd_workspace_size(lib):
     assert ws(1, 1, 1, 33) == 0 and ws(0, 1, 1, 1) == 0
 
 
+def test_ssd_workspace_size(lib):
+    ws = binding.ssd_workspace_bytes
+    up = lambda v: (v + 255) // 256 * 256
+
+    def expect(batch, L, H, G, N):
+        chunks = (L + 63) // 64
+        # C B^T of every chunk (bf16 64 x 64 per batch row, chunk and group), the chunk
+        # walk's counters (one claim counter, one flag per row), the states handed
+        # between a row's chunk segments (fp32 headdim 64 x N per row)
+        return up(batch * chunks * G * 64 * 64 * 2) + up((1 + batch * H) * 4) + batch * H * 64 * N * 4
+
+    assert ws(8, 2048, 80, 1, 128) == expect(8, 2048, 80, 1, 128)
+    assert ws(1, 1, 1, 1, 64) == expect(1, 1, 1, 1, 64)
+    assert ws(2, 130, 8, 4, 256) == expect(2, 130, 8, 4, 256)
+    assert ws(0, 1, 1, 1, 64) == 0 and ws(1, 1, 1, 2, 64) == 0 and ws(1, 1, 1, 1, 512) == 0
+    assert ws(1 << 40, 1 << 40, 1, 1, 64) == 0
+
+
 @pytest.mark.parametrize("sfx", ["bf16", "f32"])
 def test_bwd_noalloc_host_validation(lib, sfx):
     one = ctypes.c_void_p(1)
