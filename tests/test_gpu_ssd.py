@@ -98,6 +98,22 @@ def test_ssd_chunk_segments(segments, N, monkeypatch):
     run(I.SsdSpec(2, 1000 if N != 256 else 333, 5, 64, 1, N, seed=20 + segments), use_h0=True)
 
 
+@pytest.mark.parametrize("segments", [1, 2, 4])
+def test_ssd_without_final_state(segments, monkeypatch):
+    """No final state asked for: y is the same, bit for bit, as with it (the
+    segments still hand their states over through the workspace)."""
+    monkeypatch.setenv("SS_SSD_SEGMENTS", str(segments))
+    spec = I.SsdSpec(2, 700, 3, 64, 1, 128, seed=31)
+    inp = I.make_ssd_inputs(spec)
+    g = {k: v.cuda() for k, v in inp.items()}
+    y1, fs = binding.ssd_fwd(g["x"], g["dt"], g["A"], g["B"], g["C"], D=g["D"], z=g["z"], dt_bias=g["dt_bias"])
+    y2, none = binding.ssd_fwd(g["x"], g["dt"], g["A"], g["B"], g["C"], D=g["D"], z=g["z"], dt_bias=g["dt_bias"],
+                               return_final_state=False)
+    torch.cuda.synchronize()
+    assert none is None and fs is not None
+    assert torch.equal(y1, y2)
+
+
 def test_ssd_continues_from_its_final_state():
     """Two halves, the second started from the first's final state, equal
     one pass (chunked prefill)."""
