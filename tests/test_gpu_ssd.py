@@ -98,6 +98,13 @@ def test_ssd_chunk_segments(segments, N, monkeypatch):
     run(I.SsdSpec(2, 1000 if N != 256 else 333, 5, 64, 1, N, seed=20 + segments), use_h0=True)
 
 
+def test_ssd_more_rows_than_ctas():
+    """640 (batch, head) rows with an initial state: more rows than CTAs fit at once,
+    so CTAs walk several work items, each row cut into segments by the default
+    choice (every item starts from h0 or from the state handed over)."""
+    run(I.SsdSpec(8, 130, 80, 64, 1, 128, seed=41), use_h0=True)
+
+
 @pytest.mark.parametrize("segments", [1, 2, 4])
 def test_ssd_without_final_state(segments, monkeypatch):
     """No final state asked for: y is the same, bit for bit, as with it (the
