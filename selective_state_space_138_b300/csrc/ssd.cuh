@@ -714,20 +714,27 @@ ssd_chunk_tc_kernel(const __grid_constant__ SsdParams p)
                     }
                     const uint4 cbw = *reinterpret_cast<const uint4 *>(srow + sw128_off(r, s0));
                     const uint32_t wv[4] = {cbw.x, cbw.y, cbw.z, cbw.w};
-                    const float4 cu0 = *reinterpret_cast<const float4 *>(cum + s0);
-                    const float4 cu1 = *reinterpret_cast<const float4 *>(cum + s0 + 4);
-                    const float4 dd0 = *reinterpret_cast<const float4 *>(dl + s0);
-                    const float4 dd1 = *reinterpret_cast<const float4 *>(dl + s0 + 4);
-                    const float cu[8] = {cu0.x, cu0.y, cu0.z, cu0.w, cu1.x, cu1.y, cu1.z, cu1.w};
-                    const float dd[8] = {dd0.x, dd0.y, dd0.z, dd0.w, dd1.x, dd1.y, dd1.z, dd1.w};
+                    const ulonglong2 cu0 = *reinterpret_cast<const ulonglong2 *>(cum + s0);   // step pairs
+                    const ulonglong2 cu1 = *reinterpret_cast<const ulonglong2 *>(cum + s0 + 4);
+                    const ulonglong2 dd0 = *reinterpret_cast<const ulonglong2 *>(dl + s0);
+                    const ulonglong2 dd1 = *reinterpret_cast<const ulonglong2 *>(dl + s0 + 4);
+                    const u64 cu[4] = {cu0.x, cu0.y, cu1.x, cu1.y};
+                    const u64 dd[4] = {dd0.x, dd0.y, dd1.x, dd1.y};
+                    const u64 ct2 = splat(ct), m1 = splat(-1.0f);
                     uint32_t ow[4];
 #pragma unroll
-                    for (int e = 0; e < 8; e += 2) {
-                        float v0 = (s0 + e <= r) ? bf16lo(wv[e >> 1]) * ex2_approx(ct - cu[e]) * dd[e] : 0.0f;
-                        float v1 = (s0 + e + 1 <= r) ? bf16hi(wv[e >> 1]) * ex2_approx(ct - cu[e + 1]) * dd[e + 1] : 0.0f;
+                    for (int e2 = 0; e2 < 4; ++e2) {
+                        const int e = 2 * e2;
+                        // C B^T e^{cum[t] - cum[s]} delta_s for the pair of steps s, s + 1
+                        const u64 g = mul2(mul2(ex2_2(fma2(cu[e2], m1, ct2)), dd[e2]),
+                                           pk(bf16lo(wv[e2]), bf16hi(wv[e2])));
+                        float v0, v1;
+                        upk(g, v0, v1);
+                        v0 = (s0 + e <= r) ? v0 : 0.0f;
+                        v1 = (s0 + e + 1 <= r) ? v1 : 0.0f;
                         v0 += (s0 + e == r) ? Dh : 0.0f;   // the skip term D x through the diagonal
                         v1 += (s0 + e + 1 == r) ? Dh : 0.0f;
-                        ow[e >> 1] = pack_bf16x2(v0, v1);
+                        ow[e2] = pack_bf16x2(v0, v1);
                     }
                     *reinterpret_cast<uint4 *>(srow + sw128_off(r, s0)) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
                 }
