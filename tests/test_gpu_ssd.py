@@ -125,6 +125,29 @@ def test_ssd_without_final_state(segments, monkeypatch):
     assert torch.equal(y1, y2)
 
 
+def test_ssd_concurrent_calls_with_own_workspaces():
+    """Two calls on two streams at once, each with its own workspace (its own work
+    counters and handed-over states): each equals the same call made alone."""
+    spec = I.SsdSpec(8, 130, 80, 64, 1, 128, seed=51)
+    inp = I.make_ssd_inputs(spec)
+    g = {k: v.cuda() for k, v in inp.items()}
+    args = (g["x"], g["dt"], g["A"], g["B"], g["C"])
+    kw = dict(D=g["D"], z=g["z"], dt_bias=g["dt_bias"])
+    y0, f0 = binding.ssd_fwd(*args, **kw)
+    torch.cuda.synchronize()
+    need = binding.ssd_workspace_bytes(spec.batch, spec.L, spec.nheads, spec.ngroups, spec.N)
+    ws = [torch.empty(need, dtype=torch.uint8, device="cuda") for _ in range(2)]
+    streams = [torch.cuda.Stream() for _ in range(2)]
+    outs = []
+    for s, w in zip(streams, ws):
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            outs.append(binding.ssd_fwd(*args, **kw, workspace=w, stream=s))
+    torch.cuda.synchronize()
+    for y, f in outs:
+        assert torch.equal(y, y0) and torch.equal(f, f0)
+
+
 def test_ssd_continues_from_its_final_state():
     """Two halves, the second started from the first's final state, equal
     one pass (chunked prefill)."""
