@@ -250,7 +250,7 @@ scan_fwd_kernel(const ScanParams p)
 // spread over all banks
 constexpr int nsplit_bc_stride(int ns) { return ns <= 4 ? 8 : (ns == 8 ? 12 : ns + 8); }
 
-template <typename T, int S, int NPL>
+template <typename T, int S, int NPL, int ST = SS_NSPLIT_STAGES>
 struct NSplitShape {
     static constexpr int CH = 32;                 // channels per CTA
     static constexpr int NT = CH * S;             // threads per CTA
@@ -258,7 +258,7 @@ struct NSplitShape {
     static constexpr int NSP = nsplit_bc_stride(NS);
     static constexpr int LC = 32;                 // steps per chunk
     static constexpr int RL = LC / S;             // steps per epilogue/prep thread
-    static constexpr int STAGES = SS_NSPLIT_STAGES;
+    static constexpr int STAGES = ST;
     static constexpr int EPP = 16 / (int)sizeof(T);        // elements per 16-byte piece
     static constexpr int PR = LC / EPP;                    // pieces per raw row
     static constexpr int ROWB = LC * (int)sizeof(T) + 16;  // raw x/dt/z row stride, padded
@@ -291,12 +291,16 @@ struct NSplitShape {
 // TMA: the chunks arrive by tensor copies (the maps in p are encoded); the
 // cp.async form is a separate instantiation, so neither carries the other's
 // registers.
-template <typename T, int S, int NPL, bool REV, bool RST, bool TMA>
-__global__ void __launch_bounds__(NSplitShape<T, S, NPL>::NT,
-                                  NPL == 8 ? (S <= 2 ? 4 : 2) : (S <= 2 ? 4 : (S == 4 ? 3 : 1)))
+// ST: the stages of the ring; 2 stages with 4 states per lane on 4 warps fit four CTAs
+// on an SM (the wide form, for grids that three per SM would leave as a partial
+// second wave).
+template <typename T, int S, int NPL, bool REV, bool RST, bool TMA, int ST = SS_NSPLIT_STAGES>
+__global__ void __launch_bounds__(NSplitShape<T, S, NPL, ST>::NT,
+                                  NPL == 8 ? (S <= 2 ? 4 : 2)
+                                           : (S <= 2 ? 4 : (S == 4 ? (ST == 2 ? 4 : 3) : 1)))
 scan_nsplit_kernel(const __grid_constant__ ScanParams p)
 {
-    using SH = NSplitShape<T, S, NPL>;
+    using SH = NSplitShape<T, S, NPL, ST>;
     constexpr int NT = SH::NT, CH = SH::CH, NS = SH::NS, NSP = SH::NSP, LC = SH::LC, RL = SH::RL, PR = SH::PR;
     constexpr int STAGES = SH::STAGES, EPP = SH::EPP, PPT = SH::PPT;
     constexpr int D = SS_NSPLIT_AHEAD;
@@ -896,12 +900,17 @@ bool encode_scan_maps(ScanParams &p)
     return ok;
 }
 
-template <typename T, int S, int NPL, bool REV, bool RST>
+template <typename T, int S, int NPL, bool REV, bool RST, int ST = SS_NSPLIT_STAGES>
 ss_status launch_nsplit(const ScanParams &p0, cudaStream_t stream, int sms)
 {
-    using SH = NSplitShape<T, S, NPL>;
-    auto kernel = p0.tma ? scan_nsplit_kernel<T, S, NPL, REV, RST, true>
-                         : scan_nsplit_kernel<T, S, NPL, REV, RST, false>;
+    using SH = NSplitShape<T, S, NPL, ST>;
+    // the wide form (ST != the default) stages by cp.async pieces: its tensor-copy
+    // instantiation does not fit four CTAs' registers without spilling
+    auto kernel = scan_nsplit_kernel<T, S, NPL, REV, RST, false, ST>;
+    if constexpr (ST == SS_NSPLIT_STAGES) {
+        if (p0.tma)
+            kernel = scan_nsplit_kernel<T, S, NPL, REV, RST, true, ST>;
+    }
     const size_t smem = SH::BYTES;
     if (smem > 48u * 1024u) {
         cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -965,6 +974,33 @@ ss_status launch_nsplit(const ScanParams &p0, cudaStream_t stream, int sms)
 // group runs on ceil(N/4) warps (more warps per SM measured faster than 8
 // states per lane on 2 warps); SS_SCAN_NPL=8 selects 8 states per lane for
 // 8 < N <= 32.
+// The wide form (2 stages, 4 CTAs per SM) for 8 < N <= 16 in the plain direction when
+// the channel groups of all batch rows outnumber the CTAs that fit three per SM but not
+// four (a grid that would otherwise run a partial second wave); SS_SCAN_WIDE=0 / 1
+// turns it off / on whatever the grid.
+template <typename T>
+bool use_wide_nsplit(const ScanParams &p, int sms)
+{
+    const char *env = getenv("SS_SCAN_WIDE");
+    if (env && strcmp(env, "0") == 0)
+        return false;
+    if (env && strcmp(env, "1") == 0)
+        return true;
+    auto k3 = scan_nsplit_kernel<T, 4, 4, false, false, true>;
+    auto k4 = scan_nsplit_kernel<T, 4, 4, false, false, false, 2>;
+    const int b3 = static_cast<int>(NSplitShape<T, 4, 4>::BYTES), b4 = static_cast<int>(NSplitShape<T, 4, 4, 2>::BYTES);
+    int occ3 = 0, occ4 = 0;   // (the dynamic shared memory each asks for is allowed first)
+    if (cudaFuncSetAttribute(k3, cudaFuncAttributeMaxDynamicSharedMemorySize, b3) != cudaSuccess ||
+        cudaFuncSetAttribute(k4, cudaFuncAttributeMaxDynamicSharedMemorySize, b4) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ3, k3, 128, b3) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ4, k4, 128, b4) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    const int64_t rows = (p.d_inner + 31) / 32 * p.batch;
+    return occ4 > occ3 && rows > static_cast<int64_t>(occ3) * sms && rows <= static_cast<int64_t>(occ4) * sms;
+}
+
 template <typename T, bool REV, bool RST>
 ss_status dispatch_nsplit_n(const ScanParams &p, cudaStream_t s, int sms)
 {
@@ -972,6 +1008,10 @@ ss_status dispatch_nsplit_n(const ScanParams &p, cudaStream_t s, int sms)
     if (p.N <= 8) return launch_nsplit<T, 2, 4, REV, RST>(p, s, sms);
     const char *env = getenv("SS_SCAN_NPL");
     const bool npl8 = env && strcmp(env, "8") == 0;
+    if constexpr (!REV && !RST) {
+        if (p.N <= 16 && !npl8 && use_wide_nsplit<T>(p, sms))
+            return launch_nsplit<T, 4, 4, false, false, 2>(p, s, sms);
+    }
     if (p.N <= 16) return npl8 ? launch_nsplit<T, 2, 8, REV, RST>(p, s, sms) : launch_nsplit<T, 4, 4, REV, RST>(p, s, sms);
     return npl8 ? launch_nsplit<T, 4, 8, REV, RST>(p, s, sms) : launch_nsplit<T, 8, 4, REV, RST>(p, s, sms);
 }

@@ -19,16 +19,18 @@ from tests.gpu_util import TOL, assert_close, compare_scan_all_rows, dev, gpu_sc
 pytestmark = pytest.mark.gpu
 
 # kernel variants: the n-split kernel (whole sequence, or cut into 3 or 8
-# segments joined through a thread-block cluster), and the time-lane kernel
-# with 1, 4, 16 lanes
-LANES = ["nsplit", "seg3", "seg8", "1", "4", "16"]
+# segments joined through a thread-block cluster; "wide": its 2-stage form at
+# four CTAs per SM, which 8 < N <= 16 takes), and the time-lane kernel with 1, 4,
+# 16 lanes
+LANES = ["nsplit", "seg3", "seg8", "wide", "1", "4", "16"]
 
 
 @pytest.fixture
 def lanes(request, monkeypatch):
-    if request.param == "nsplit":
+    if request.param in ("nsplit", "wide"):
         monkeypatch.setenv("SS_SCAN_KERNEL", "nsplit")
         monkeypatch.setenv("SS_SCAN_SEGMENTS", "1")
+        monkeypatch.setenv("SS_SCAN_WIDE", "1" if request.param == "wide" else "0")
         return 0
     if request.param.startswith("seg"):
         monkeypatch.setenv("SS_SCAN_KERNEL", "nsplit")
@@ -73,7 +75,7 @@ OPTIONAL = [dict(use_D=False), dict(use_z=False), dict(use_bias=False), dict(sof
             dict(use_D=False, use_z=False, use_bias=False, softplus=False), dict(final_state=False)]
 
 
-@pytest.mark.parametrize("lanes", ["nsplit", "seg3", "1", "16"], indirect=True)
+@pytest.mark.parametrize("lanes", ["nsplit", "seg3", "wide", "1", "16"], indirect=True)
 @pytest.mark.parametrize("opt", OPTIONAL, ids=lambda o: "_".join("%s=%s" % kv for kv in o.items()))
 @pytest.mark.parametrize("io", ["bf16", "f32"])
 def test_optional_pointers_and_flag(opt, io, lanes):
