@@ -38,7 +38,7 @@ def sources() -> list[str]:
 
 # the files each part is compiled from besides ss_scan.cu, the shared headers and the C header
 COMMON = ("ss_scan.cu", "device_common.cuh", "host_common.cuh")
-PART_FILES = {0: (), 1: ("scan_fwd.cuh", "fault_probe.cuh"), 2: ("scan_bwd.cuh",), 3: ("decode.cuh", "conv.cuh"), 4: ("ssd.cuh", "ssd_host.cuh")}
+PART_FILES = {0: (), 1: ("scan_fwd.cuh", "scan_fwd_host.cuh", "fault_probe.cuh"), 2: ("scan_bwd.cuh",), 3: ("decode.cuh", "conv.cuh"), 4: ("ssd.cuh", "ssd_host.cuh")}
 OBJDIR = os.path.join(PKG, "_build")
 
 

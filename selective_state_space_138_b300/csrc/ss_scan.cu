@@ -63,6 +63,7 @@ namespace {
 #include "host_common.cuh"
 #if SS_PART_IS(1)
 #include "scan_fwd.cuh"
+#include "scan_fwd_host.cuh"
 #include "fault_probe.cuh"
 #endif
 #if SS_PART_IS(2)
